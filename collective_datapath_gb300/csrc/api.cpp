@@ -1,0 +1,471 @@
+// api.cpp -- the C ABI (include/coll.h): argument checks, workspace binding
+// and kernel launches.  No device allocation anywhere in this file.
+#include <cuda_runtime.h>
+
+#include <cstring>
+#include <new>
+#include <vector>
+
+#include "../../include/coll.h"
+#include "derive.h"
+#include "launch.h"
+
+using namespace coll;
+
+struct coll_spec {
+  Plan plan;
+  char* ws = nullptr;
+  size_t ws_bytes = 0;
+  bool bound = false;
+  RunParams base{};
+};
+
+namespace {
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+cudaStream_t as_stream(coll_stream_t s) { return reinterpret_cast<cudaStream_t>(s); }
+
+coll_status_t cuda_status(cudaError_t e) {
+  return e == cudaSuccess ? COLL_OK : COLL_ERR_CUDA;
+}
+
+// SM count and co-resident fused CTAs of the current device; defaults when
+// no device is visible (the deriver is pure host code).
+void device_shape(int enc, int* sms, int* cap) {
+  int count = 0;
+  *sms = 0;
+  *cap = 0;
+  if (cudaGetDeviceCount(&count) != cudaSuccess || count == 0) {
+    cudaGetLastError();  // clear the sticky "no device" error
+    return;
+  }
+  *sms = device_sms();
+  *cap = fused_capacity(enc);
+}
+
+void fill_base(coll_spec* s) {
+  const Plan& p = s->plan;
+  RunParams& P = s->base;
+  P = RunParams{};
+  P.ws = s->ws;
+  P.nranks = p.n;
+  P.enc = p.enc;
+  P.reset_mode = p.reset_mode;
+  P.ctas_per_rank = p.ctas_per_rank;
+  P.timeout_ns = p.timeout_ns;
+  P.P = p.P;
+  P.AG = p.AG;
+  P.sitems = reinterpret_cast<const StageItem*>(s->ws + p.off_sitems);
+  P.items1 = reinterpret_cast<const Item*>(s->ws + p.off_items1);
+  P.items2 = p.items2.empty() ? nullptr : reinterpret_cast<const Item*>(s->ws + p.off_items2);
+  P.counters = reinterpret_cast<uint32_t*>(s->ws + p.off_counters);
+  for (int r = 0; r <= kMaxRanks; ++r) {
+    P.sbeg[r] = p.sbeg[r];
+    P.beg1[r] = p.beg1[r];
+    P.beg2[r] = p.beg2[r];
+  }
+  P.nseg = (int)p.pseg[0].size();
+  for (int k = 0; k < P.nseg && k < kMaxRanks; ++k) {
+    P.seg_line0[k] = p.pseg[0][k].line0;
+    P.seg_elems[k] = p.pseg[0][k].elems;
+    P.seg_in0[k] = p.pseg[0][k].in_elem;
+  }
+  P.stage_rank = -1;
+  P.advance_epoch = 0;
+}
+
+coll_status_t check_outs(const coll_spec* s, void* const* outs) {
+  if (outs == nullptr) return COLL_ERR_INVALID;
+  for (int r = 0; r < s->plan.n; ++r) {
+    if (s->plan.out_elems[r] > 0 && outs[r] == nullptr) return COLL_ERR_INVALID;
+    if (!aligned16(outs[r])) return COLL_ERR_ALIGN;
+  }
+  return COLL_OK;
+}
+
+coll_status_t check_ins(const coll_spec* s, const void* const* ins) {
+  for (int r = 0; r < s->plan.n; ++r) {
+    if (s->plan.in_elems[r] > 0 && ins[r] == nullptr) return COLL_ERR_INVALID;
+    if (!aligned16(ins[r])) return COLL_ERR_ALIGN;
+  }
+  return COLL_OK;
+}
+
+// Consume phase(s) of a run whose inputs are staged; the last launch
+// advances the epoch.
+coll_status_t launch_consumers(coll_spec* s, RunParams P, cudaStream_t st) {
+  const Plan& p = s->plan;
+  const bool rearm_kernel = p.enc == ENC_LL8 && p.reset_mode == COLL_RESET_KERNEL;
+  const bool two = !p.items2.empty();
+  if (p.items1.empty() && !two) {
+    P.advance_epoch = !rearm_kernel;
+    if (cudaError_t e = launch_advance(P, st)) return cuda_status(e);
+  } else {
+    P.advance_epoch = !two && !rearm_kernel;
+    if (cudaError_t e = launch_consume(P, 1, p.consume_grid, st)) return cuda_status(e);
+    if (two) {
+      P.advance_epoch = !rearm_kernel;
+      if (cudaError_t e = launch_consume(P, 2, p.consume_grid, st)) return cuda_status(e);
+    }
+  }
+  if (rearm_kernel) {
+    P.advance_epoch = 1;
+    if (cudaError_t e = launch_rearm(P, device_sms() * 4, st)) return cuda_status(e);
+  }
+  return COLL_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+void coll_options_default(coll_options_t* opt) {
+  if (opt == nullptr) return;
+  std::memset(opt, 0, sizeof(*opt));
+  opt->encoding = COLL_LL8;
+  opt->algorithm = COLL_ALGO_AUTO;
+  opt->reset_mode = COLL_RESET_FUSED;
+  opt->path = COLL_PATH_AUTO;
+}
+
+coll_status_t coll_spec_create(coll_layout_t in_layout, coll_layout_t out_layout,
+                               coll_op_t op, coll_dtype_t dtype, int nranks, size_t count,
+                               const coll_options_t* opt, coll_spec_t** spec) {
+  if (spec == nullptr) return COLL_ERR_INVALID;
+  *spec = nullptr;
+  coll_options_t o;
+  coll_options_default(&o);
+  if (opt != nullptr) o = *opt;
+  DeriveInput d{};
+  d.in_layout = in_layout;
+  d.out_layout = out_layout;
+  d.op = op;
+  d.dtype = dtype;
+  d.nranks = nranks;
+  d.count = count;
+  d.encoding = o.encoding;
+  d.algorithm = o.algorithm;
+  d.reset_mode = o.reset_mode;
+  d.path = o.path;
+  d.ctas = o.ctas;
+  d.tile_lines = o.tile_lines;
+  d.timeout_ns = o.timeout_ns;
+  d.tokens = o.tokens;
+  d.hidden = o.hidden;
+  d.topk = o.topk;
+  d.experts = o.experts;
+  device_shape(o.encoding, &d.sms, &d.fused_capacity);
+  coll_spec* s = new (std::nothrow) coll_spec();
+  if (s == nullptr) return COLL_ERR_INVALID;
+  int st = derive(d, s->plan);
+  if (st != COLL_OK) {
+    delete s;
+    return (coll_status_t)st;
+  }
+  *spec = s;
+  return COLL_OK;
+}
+
+coll_status_t coll_workspace_bytes(const coll_spec_t* s, size_t* bytes) {
+  if (s == nullptr || bytes == nullptr) return COLL_ERR_INVALID;
+  *bytes = (size_t)s->plan.ws_bytes;
+  return COLL_OK;
+}
+
+coll_status_t coll_buffer_elems(const coll_spec_t* s, int rank, size_t* in_elems,
+                                size_t* out_elems) {
+  if (s == nullptr || rank < 0 || rank >= s->plan.n) return COLL_ERR_INVALID;
+  if (in_elems) *in_elems = (size_t)s->plan.in_elems[rank];
+  if (out_elems) *out_elems = (size_t)s->plan.out_elems[rank];
+  return COLL_OK;
+}
+
+coll_status_t coll_bind(coll_spec_t* s, void* dev_workspace, size_t bytes,
+                        coll_stream_t stream) {
+  if (s == nullptr || dev_workspace == nullptr) return COLL_ERR_INVALID;
+  if ((reinterpret_cast<uintptr_t>(dev_workspace) & 255u) != 0) return COLL_ERR_ALIGN;
+  if (bytes < s->plan.ws_bytes) return COLL_ERR_NOMEM;
+  cudaStream_t st = as_stream(stream);
+  const Plan& p = s->plan;
+  s->ws = static_cast<char*>(dev_workspace);
+  s->ws_bytes = bytes;
+  if (cudaError_t e = cudaMemsetAsync(s->ws, 0, p.ws_bytes, st)) return cuda_status(e);
+  WsHeader h{};
+  h.epoch = 1;
+  // Pageable sources: the runtime copies them before returning.
+  if (cudaError_t e = cudaMemcpyAsync(s->ws, &h, sizeof h, cudaMemcpyHostToDevice, st))
+    return cuda_status(e);
+  if (!p.sitems.empty())
+    if (cudaError_t e = cudaMemcpyAsync(s->ws + p.off_sitems, p.sitems.data(),
+                                        p.sitems.size() * sizeof(StageItem),
+                                        cudaMemcpyHostToDevice, st))
+      return cuda_status(e);
+  if (!p.items1.empty())
+    if (cudaError_t e = cudaMemcpyAsync(s->ws + p.off_items1, p.items1.data(),
+                                        p.items1.size() * sizeof(Item),
+                                        cudaMemcpyHostToDevice, st))
+      return cuda_status(e);
+  if (!p.items2.empty())
+    if (cudaError_t e = cudaMemcpyAsync(s->ws + p.off_items2, p.items2.data(),
+                                        p.items2.size() * sizeof(Item),
+                                        cudaMemcpyHostToDevice, st))
+      return cuda_status(e);
+  if (cudaError_t e = cudaStreamSynchronize(st)) return cuda_status(e);
+  fill_base(s);
+  s->bound = true;
+  return COLL_OK;
+}
+
+coll_status_t coll_set_routing(coll_spec_t* s, int rank, const int32_t* dev_topk,
+                               coll_stream_t stream) {
+  (void)stream;
+  if (s == nullptr || dev_topk == nullptr || rank < 0 || rank >= s->plan.n)
+    return COLL_ERR_INVALID;
+  return COLL_ERR_UNSUPPORTED;
+}
+
+coll_status_t coll_stage(coll_spec_t* s, int rank, const void* dev_in,
+                         coll_stream_t stream) {
+  if (s == nullptr || rank < 0 || rank >= s->plan.n) return COLL_ERR_INVALID;
+  if (!s->bound) return COLL_ERR_STATE;
+  if (s->plan.in_elems[rank] > 0 && dev_in == nullptr) return COLL_ERR_INVALID;
+  if (!aligned16(dev_in)) return COLL_ERR_ALIGN;
+  RunParams P = s->base;
+  P.in[rank] = static_cast<const uint16_t*>(dev_in);
+  P.stage_rank = rank;
+  const int items = P.sbeg[rank + 1] - P.sbeg[rank];
+  const int grid = std::min(items, device_sms() * 8);
+  return cuda_status(launch_stage(P, grid, as_stream(stream)));
+}
+
+coll_status_t coll_run(coll_spec_t* s, const void* const* dev_ins, void* const* dev_outs,
+                       coll_stream_t stream) {
+  if (s == nullptr) return COLL_ERR_INVALID;
+  if (!s->bound) return COLL_ERR_STATE;
+  if (coll_status_t e = check_outs(s, dev_outs)) return e;
+  if (dev_ins != nullptr)
+    if (coll_status_t e = check_ins(s, dev_ins)) return e;
+  const Plan& p = s->plan;
+  cudaStream_t st = as_stream(stream);
+  RunParams P = s->base;
+  for (int r = 0; r < p.n; ++r) {
+    P.out[r] = static_cast<uint16_t*>(dev_outs[r]);
+    if (dev_ins) P.in[r] = static_cast<const uint16_t*>(dev_ins[r]);
+  }
+  const bool empty = p.items1.empty() && p.items2.empty();
+  if (dev_ins != nullptr && p.path == COLL_PATH_FUSED && !empty &&
+      !(p.enc == ENC_LL8 && p.reset_mode == COLL_RESET_KERNEL)) {
+    P.advance_epoch = 1;
+    return cuda_status(launch_fused(P, p.n * p.ctas_per_rank, st));
+  }
+  if (dev_ins != nullptr && !p.sitems.empty()) {
+    P.stage_rank = -1;
+    const int grid = std::min((int)p.sitems.size(), device_sms() * 8);
+    if (cudaError_t e = launch_stage(P, grid, st)) return cuda_status(e);
+  }
+  return launch_consumers(s, P, st);
+}
+
+coll_status_t coll_run_host(coll_spec_t* s, const void* const* host_ins,
+                            void* const* dev_ins, void* const* dev_outs,
+                            void* const* host_outs, coll_stream_t stream) {
+  if (s == nullptr || host_ins == nullptr || dev_ins == nullptr || dev_outs == nullptr ||
+      host_outs == nullptr)
+    return COLL_ERR_INVALID;
+  if (!s->bound) return COLL_ERR_STATE;
+  const Plan& p = s->plan;
+  cudaStream_t st = as_stream(stream);
+  for (int r = 0; r < p.n; ++r) {
+    const size_t b = 2 * (size_t)p.in_elems[r];
+    if (b && cudaMemcpyAsync(dev_ins[r], host_ins[r], b, cudaMemcpyHostToDevice, st))
+      return COLL_ERR_CUDA;
+  }
+  if (coll_status_t e = coll_run(s, reinterpret_cast<const void* const*>(dev_ins), dev_outs,
+                                 stream))
+    return e;
+  for (int r = 0; r < p.n; ++r) {
+    const size_t b = 2 * (size_t)p.out_elems[r];
+    if (b && cudaMemcpyAsync(host_outs[r], dev_outs[r], b, cudaMemcpyDeviceToHost, st))
+      return COLL_ERR_CUDA;
+  }
+  return COLL_OK;
+}
+
+coll_status_t coll_get_counts(const coll_spec_t* s, int32_t* dev_counts,
+                              coll_stream_t stream) {
+  (void)stream;
+  if (s == nullptr || dev_counts == nullptr) return COLL_ERR_INVALID;
+  return COLL_ERR_UNSUPPORTED;
+}
+
+coll_status_t coll_query_status(coll_spec_t* s, coll_stream_t stream, int* code, int* rank,
+                                int64_t* line) {
+  if (s == nullptr) return COLL_ERR_INVALID;
+  if (!s->bound) return COLL_ERR_STATE;
+  cudaStream_t st = as_stream(stream);
+  if (cudaStreamSynchronize(st) != cudaSuccess) return COLL_ERR_CUDA;
+  WsHeader h;
+  if (cudaMemcpy(&h, s->ws, sizeof h, cudaMemcpyDeviceToHost) != cudaSuccess)
+    return COLL_ERR_CUDA;
+  if (code) *code = (int)h.status_code;
+  if (rank) *rank = (int)h.status_rank;
+  if (line) *line = h.status_line;
+  if (h.status_code != 0 || h.abort != 0) {
+    // Clear status_code .. abort (bytes 8..31) and leave the epoch alone.
+    // An aborted run may have skipped items, so the reader counters of the
+    // counted re-arm are reset as well.
+    char zeros[24] = {0};
+    if (cudaMemcpy(s->ws + 8, zeros, sizeof zeros, cudaMemcpyHostToDevice) != cudaSuccess)
+      return COLL_ERR_CUDA;
+    const size_t cbytes = 4 * (size_t)(s->plan.ncounters ? s->plan.ncounters : 1);
+    if (cudaMemset(s->ws + s->plan.off_counters, 0, cbytes) != cudaSuccess)
+      return COLL_ERR_CUDA;
+  }
+  return COLL_OK;
+}
+
+coll_status_t coll_get_epoch(coll_spec_t* s, coll_stream_t stream, uint64_t* epoch) {
+  if (s == nullptr || epoch == nullptr) return COLL_ERR_INVALID;
+  if (!s->bound) return COLL_ERR_STATE;
+  if (cudaStreamSynchronize(as_stream(stream)) != cudaSuccess) return COLL_ERR_CUDA;
+  if (cudaMemcpy(epoch, s->ws, 8, cudaMemcpyDeviceToHost) != cudaSuccess) return COLL_ERR_CUDA;
+  return COLL_OK;
+}
+
+coll_status_t coll_get_rejections(coll_spec_t* s, coll_stream_t stream,
+                                  uint64_t* rejections) {
+  if (s == nullptr || rejections == nullptr) return COLL_ERR_INVALID;
+  if (!s->bound) return COLL_ERR_STATE;
+  if (cudaStreamSynchronize(as_stream(stream)) != cudaSuccess) return COLL_ERR_CUDA;
+  if (cudaMemcpy(rejections, s->ws + offsetof(WsHeader, rejections), 8,
+                 cudaMemcpyDeviceToHost) != cudaSuccess)
+    return COLL_ERR_CUDA;
+  return COLL_OK;
+}
+
+coll_status_t coll_staging_layout(const coll_spec_t* s, int region, int slot, int rank,
+                                  int seg, uint64_t* byte_offset, uint64_t* lines,
+                                  int* line_bytes_out) {
+  if (s == nullptr || rank < 0 || rank >= s->plan.n || slot < 0 || slot > 1)
+    return COLL_ERR_INVALID;
+  const Plan& p = s->plan;
+  const std::vector<Seg>* segs;
+  const Region* R;
+  if (region == 0) {
+    segs = &p.pseg[rank];
+    R = &p.P;
+  } else if (region == 1) {
+    segs = &p.agseg[rank];
+    R = &p.AG;
+  } else {
+    return COLL_ERR_INVALID;
+  }
+  if (seg < 0 || seg >= (int)segs->size()) return COLL_ERR_INVALID;
+  const int lb = line_bytes(p.enc);
+  if (byte_offset)
+    *byte_offset = R->base + (uint64_t)slot * R->slot_bytes + (uint64_t)rank * R->rank_bytes +
+                   (*segs)[seg].line0 * (uint64_t)lb;
+  if (lines) *lines = (*segs)[seg].lines;
+  if (line_bytes_out) *line_bytes_out = lb;
+  return COLL_OK;
+}
+
+coll_status_t coll_stage_withheld(coll_spec_t* s, int rank, const void* dev_in,
+                                  const int64_t* dev_lines, const int32_t* dev_kind,
+                                  const uint16_t* dev_poison, int64_t n,
+                                  coll_stream_t stream) {
+  if (n < 0 || (n > 0 && (dev_lines == nullptr || dev_kind == nullptr || dev_poison == nullptr)))
+    return COLL_ERR_INVALID;
+  if (coll_status_t e = coll_stage(s, rank, dev_in, stream)) return e;
+  RunParams P = s->base;
+  P.stage_rank = rank;
+  P.wh_lines = dev_lines;
+  P.wh_kind = dev_kind;
+  P.wh_poison = dev_poison;
+  P.wh_n = n;
+  return cuda_status(launch_withhold(P, as_stream(stream)));
+}
+
+coll_status_t coll_run_late(coll_spec_t* s, const void* const* dev_ins, void* const* dev_outs,
+                            const int64_t* const* dev_order, const int64_t* n_late,
+                            coll_stream_t stream) {
+  if (s == nullptr || dev_ins == nullptr || dev_order == nullptr || n_late == nullptr)
+    return COLL_ERR_INVALID;
+  if (!s->bound) return COLL_ERR_STATE;
+  const Plan& p = s->plan;
+  if (p.kind == CK_ALLGATHER || p.enc == ENC_LL8 && p.reset_mode == COLL_RESET_KERNEL)
+    return COLL_ERR_UNSUPPORTED;  // late producers need identical rank images
+  if (coll_status_t e = check_outs(s, dev_outs)) return e;
+  if (coll_status_t e = check_ins(s, dev_ins)) return e;
+  RunParams P = s->base;
+  for (int r = 0; r < p.n; ++r) {
+    P.out[r] = static_cast<uint16_t*>(dev_outs[r]);
+    P.in[r] = static_cast<const uint16_t*>(dev_ins[r]);
+    P.late_order[r] = dev_order[r];
+    P.late_n[r] = n_late[r];
+    if (n_late[r] < 0 || (n_late[r] > 0 && dev_order[r] == nullptr)) return COLL_ERR_INVALID;
+  }
+  P.sitems = nullptr;  // inputs were staged (with lines withheld)
+  P.late_ctas = p.n;
+  P.advance_epoch = 1;
+  return cuda_status(launch_fused(P, p.n * p.ctas_per_rank + p.n, as_stream(stream)));
+}
+
+coll_status_t coll_debug_items(const coll_spec_t* s, int which, int64_t* buf, size_t cap,
+                               size_t* n) {
+  if (s == nullptr || n == nullptr || which < 0 || which > 2) return COLL_ERR_INVALID;
+  const Plan& p = s->plan;
+  if (which == 0) {
+    *n = p.sitems.size();
+    for (size_t i = 0; i < p.sitems.size() && i < cap && buf; ++i) {
+      const StageItem& it = p.sitems[i];
+      int64_t* o = buf + 10 * i;
+      o[0] = it.rank; o[1] = o[2] = o[3] = o[4] = 0;
+      o[5] = it.nlines; o[6] = it.nelems; o[7] = (int64_t)it.dst_line;
+      o[8] = (int64_t)it.in_elem; o[9] = 0;
+    }
+    return COLL_OK;
+  }
+  const std::vector<Item>& v = which == 1 ? p.items1 : p.items2;
+  *n = v.size();
+  for (size_t i = 0; i < v.size() && i < cap && buf; ++i) {
+    const Item& it = v[i];
+    int64_t* o = buf + 10 * i;
+    o[0] = it.kind; o[1] = it.flags; o[2] = it.dst; o[3] = it.src; o[4] = it.readers;
+    o[5] = it.nlines; o[6] = it.nelems; o[7] = (int64_t)it.src_line;
+    o[8] = (int64_t)it.out_off; o[9] = it.counter;
+  }
+  return COLL_OK;
+}
+
+coll_status_t coll_debug_plan(const coll_spec_t* s, int* algorithm, int* path,
+                              int* ctas_per_rank, int* encoding) {
+  if (s == nullptr) return COLL_ERR_INVALID;
+  if (algorithm) *algorithm = s->plan.algorithm;
+  if (path) *path = s->plan.path;
+  if (ctas_per_rank) *ctas_per_rank = s->plan.ctas_per_rank;
+  if (encoding) *encoding = s->plan.enc;
+  return COLL_OK;
+}
+
+coll_status_t coll_destroy(coll_spec_t* s) {
+  delete s;
+  return COLL_OK;
+}
+
+const char* coll_status_string(coll_status_t st) {
+  switch (st) {
+    case COLL_OK: return "ok";
+    case COLL_ERR_INVALID: return "invalid argument";
+    case COLL_ERR_UNSUPPORTED: return "unsupported collective, type or option";
+    case COLL_ERR_ALIGN: return "pointer or count not 16-byte aligned";
+    case COLL_ERR_NOMEM: return "workspace smaller than coll_workspace_bytes";
+    case COLL_ERR_CUDA: return "CUDA runtime error";
+    case COLL_ERR_TIMEOUT: return "a device wait exceeded its time bound";
+    case COLL_ERR_STATE: return "call out of sequence";
+  }
+  return "unknown status";
+}
+
+}  // extern "C"

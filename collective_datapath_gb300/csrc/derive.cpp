@@ -1,0 +1,361 @@
+// derive.cpp -- layout-to-schedule deriver (see derive.h).
+#include "derive.h"
+
+#include <algorithm>
+#include <map>
+#include <utility>
+
+#include "../../include/coll.h"
+
+namespace coll {
+
+int line_bytes(int enc) { return enc == ENC_LL8 ? kLL8LineBytes : kLL128LineBytes; }
+int line_elems(int enc) { return enc == ENC_LL8 ? kLL8Elems : kLL128Elems; }
+
+uint64_t lines_for(int enc, uint64_t elems) {
+  const uint64_t e = (uint64_t)line_elems(enc);
+  return (elems + e - 1) / e;
+}
+
+// Partition rule: M = roundup(ceil(count / n), 8); partition r covers
+// [r*M, min(count, (r+1)*M)).  Equal partitions whenever 8n divides count.
+uint64_t shard_elems(uint64_t count, int n) {
+  const uint64_t per = (count + (uint64_t)n - 1) / (uint64_t)n;
+  return (per + 7) / 8 * 8;
+}
+uint64_t shard_begin(uint64_t count, int n, int r) {
+  return std::min<uint64_t>(count, (uint64_t)r * shard_elems(count, n));
+}
+uint64_t shard_len(uint64_t count, int n, int r) {
+  const uint64_t b = shard_begin(count, n, r);
+  return std::min<uint64_t>(count, b + shard_elems(count, n)) - b;
+}
+
+static uint64_t round_up(uint64_t x, uint64_t a) { return (x + a - 1) / a * a; }
+
+// Segments in image order; each starts on a 4-line boundary (one LL8 group
+// of a 16-byte chunk, one LL128 warp row).
+static uint64_t build_image(int enc, const std::vector<std::pair<uint64_t, uint64_t>>& parts,
+                            std::vector<Seg>& segs) {
+  uint64_t line = 0;
+  segs.clear();
+  for (auto& pr : parts) {
+    Seg s;
+    s.line0 = line;
+    s.elems = pr.first;
+    s.in_elem = pr.second;
+    s.lines = lines_for(enc, s.elems);
+    segs.push_back(s);
+    line += round_up(s.lines, 4);
+  }
+  return line;
+}
+
+namespace {
+
+struct Tiler {
+  uint64_t tile;  // lines per tile, a multiple of 4
+  int enc;
+  template <class F>
+  void over(const Seg& s, F&& f) const {
+    for (uint64_t t0 = 0; t0 < s.lines; t0 += tile) {
+      const uint64_t nl = std::min<uint64_t>(tile, s.lines - t0);
+      const uint64_t e0 = t0 * (uint64_t)line_elems(enc);
+      const uint64_t ne = std::min<uint64_t>(s.elems - e0, nl * (uint64_t)line_elems(enc));
+      f(t0, nl, ne);
+    }
+  }
+};
+
+struct Counters {
+  std::map<std::pair<int, uint64_t>, uint32_t> keys;
+  uint32_t get(int space, uint64_t key) {
+    auto it = keys.find({space, key});
+    if (it != keys.end()) return it->second;
+    const uint32_t id = (uint32_t)keys.size();
+    keys[{space, key}] = id;
+    return id;
+  }
+};
+
+Item make_item(uint8_t kind, uint8_t dst, uint8_t src, uint64_t src_line, uint64_t nl,
+               uint64_t ne, uint64_t out_off) {
+  Item it{};
+  it.kind = kind;
+  it.dst = dst;
+  it.src = src;
+  it.src_line = src_line;
+  it.nlines = (uint32_t)nl;
+  it.nelems = (uint32_t)ne;
+  it.out_off = out_off;
+  return it;
+}
+
+void set_reset(Item& it, int readers, uint32_t counter) {
+  if (readers <= 1) {
+    it.flags |= IF_RESET_SOLE;
+  } else {
+    it.flags |= IF_RESET_COUNTED;
+    it.readers = (uint16_t)readers;
+    it.counter = counter;
+  }
+}
+
+// Group items by destination rank and fill the begin offsets.
+void group_by_dst(std::vector<Item>& items, int n, int* beg) {
+  std::stable_sort(items.begin(), items.end(),
+                   [](const Item& a, const Item& b) { return a.dst < b.dst; });
+  int k = 0;
+  for (int r = 0; r <= n; ++r) {
+    while (k < (int)items.size() && items[k].dst < r) ++k;
+    beg[r] = k;
+  }
+  for (int r = n + 1; r <= kMaxRanks; ++r) beg[r] = (int)items.size();
+}
+
+}  // namespace
+
+int derive(const DeriveInput& in, Plan& p) {
+  p = Plan{};
+  const int n = in.nranks;
+  if (n < 1 || n > kMaxRanks) return COLL_ERR_UNSUPPORTED;
+  if (in.dtype != COLL_BF16) return COLL_ERR_UNSUPPORTED;
+  if (in.encoding != COLL_LL8 && in.encoding != COLL_LL128) return COLL_ERR_UNSUPPORTED;
+  if (in.reset_mode < 0 || in.reset_mode > 2 || in.path < 0 || in.path > 2 ||
+      in.algorithm < 0 || in.algorithm > 2 || in.ctas < 0 || in.tile_lines < 0)
+    return COLL_ERR_INVALID;
+
+  const int L = in.in_layout, O = in.out_layout;
+  if (L == COLL_SCATTERED && O == COLL_SCATTERED && in.op == COLL_REDUCE)
+    p.kind = CK_ALLREDUCE;
+  else if (L == COLL_SCATTERED && O == COLL_PACKED && in.op == COLL_REDUCE)
+    p.kind = CK_REDUCE_SCATTER;
+  else if (L == COLL_PACKED && O == COLL_SCATTERED && in.op == COLL_COPY)
+    p.kind = CK_ALLGATHER;
+  else if (L == COLL_SCATTERED && O == COLL_TRANSPOSED && in.op == COLL_COPY)
+    p.kind = CK_ALLTOALL;
+  else
+    return COLL_ERR_UNSUPPORTED;
+
+  if (in.count % 8 != 0) return COLL_ERR_ALIGN;
+  p.enc = in.encoding;
+  p.n = n;
+  p.count = in.count;
+  p.shard = shard_elems(in.count, n);
+  p.reset_mode = p.enc == ENC_LL8 ? in.reset_mode : COLL_RESET_NONE;
+  p.timeout_ns = in.timeout_ns ? in.timeout_ns : 200000000ull;
+  if (p.kind == CK_ALLTOALL && p.shard * (uint64_t)n != in.count)
+    return COLL_ERR_ALIGN;  // the exchange needs equal partitions
+
+  const uint64_t count = in.count, M = p.shard;
+  uint64_t in_bytes_per_rank = 0;
+  for (int r = 0; r < n; ++r) {
+    switch (p.kind) {
+      case CK_ALLREDUCE: p.in_elems[r] = count; p.out_elems[r] = count; break;
+      case CK_REDUCE_SCATTER: p.in_elems[r] = count; p.out_elems[r] = shard_len(count, n, r); break;
+      case CK_ALLGATHER: p.in_elems[r] = shard_len(count, n, r); p.out_elems[r] = count; break;
+      case CK_ALLTOALL: p.in_elems[r] = count; p.out_elems[r] = count; break;
+      default: break;
+    }
+    in_bytes_per_rank = std::max<uint64_t>(in_bytes_per_rank, 2 * p.in_elems[r]);
+  }
+
+  // Algorithm and path.
+  p.algorithm = 0;
+  if (p.kind == CK_ALLREDUCE) {
+    p.algorithm = in.algorithm;
+    if (p.algorithm == COLL_ALGO_AUTO)
+      p.algorithm = (n <= 2 || in_bytes_per_rank <= 64 * 1024) ? COLL_ONESHOT : COLL_TWOSHOT;
+  }
+  p.path = in.path;
+  if (p.path == COLL_PATH_AUTO)
+    p.path = in_bytes_per_rank <= 64 * 1024 ? COLL_PATH_FUSED : COLL_PATH_STREAMED;
+
+  // Rank images of region P.
+  for (int r = 0; r < n; ++r) {
+    std::vector<std::pair<uint64_t, uint64_t>> parts;
+    if (L == COLL_SCATTERED) {
+      for (int k = 0; k < n; ++k) parts.push_back({shard_len(count, n, k), shard_begin(count, n, k)});
+    } else {
+      parts.push_back({p.in_elems[r], 0});
+    }
+    p.p_rank_lines = std::max<uint64_t>(p.p_rank_lines, build_image(p.enc, parts, p.pseg[r]));
+  }
+  const bool twoshot = p.kind == CK_ALLREDUCE && p.algorithm == COLL_TWOSHOT;
+  if (twoshot) {
+    for (int r = 0; r < n; ++r) {
+      std::vector<std::pair<uint64_t, uint64_t>> parts{{shard_len(count, n, r), 0}};
+      p.ag_rank_lines = std::max<uint64_t>(p.ag_rank_lines, build_image(p.enc, parts, p.agseg[r]));
+    }
+  }
+
+  // CTAs per rank on the fused path: every worker CTA plus one late producer
+  // per rank must be co-resident (cooperative launch).
+  const int sms = in.sms > 0 ? in.sms : 152;
+  int cap = in.fused_capacity > 0 ? std::min(in.fused_capacity, sms) : sms;
+  int B = std::max(1, cap / n - 1);
+  if (in.ctas > 0) B = std::max(1, std::min(B, in.ctas / n));
+
+  // Tile sizes (lines, multiples of 4).
+  auto fused = p.path == COLL_PATH_FUSED;
+  const uint64_t max_tile = p.enc == ENC_LL8 ? 2048 : 512;
+  auto pick_tile = [&](uint64_t lines_per_rank) -> uint64_t {
+    if (in.tile_lines > 0) return round_up((uint64_t)in.tile_lines, 4);
+    if (!fused) return max_tile;
+    // about B items per rank per phase
+    uint64_t t = round_up((lines_per_rank + B - 1) / (uint64_t)B, 4);
+    return std::max<uint64_t>(4, std::min<uint64_t>(t, max_tile));
+  };
+  uint64_t rank_lines = 0;
+  for (auto& s : p.pseg[0]) rank_lines += s.lines;
+  const Tiler stage_tiler{pick_tile(rank_lines), p.enc};
+  const uint64_t epl = (uint64_t)line_elems(p.enc);
+
+  // Stage items.
+  for (int r = 0; r < n; ++r)
+    for (auto& s : p.pseg[r])
+      stage_tiler.over(s, [&](uint64_t t0, uint64_t nl, uint64_t ne) {
+        StageItem it{};
+        it.rank = (uint16_t)r;
+        it.nlines = (uint32_t)nl;
+        it.nelems = (uint32_t)ne;
+        it.dst_line = s.line0 + t0;
+        it.in_elem = s.in_elem + t0 * epl;
+        p.sitems.push_back(it);
+      });
+  {
+    int k = 0;
+    for (int r = 0; r <= kMaxRanks; ++r) {
+      while (k < (int)p.sitems.size() && p.sitems[k].rank < r) ++k;
+      p.sbeg[r] = r <= n ? k : (int)p.sitems.size();
+    }
+  }
+
+  // Consume items.
+  Counters ctr;
+  switch (p.kind) {
+    case CK_ALLREDUCE:
+      if (!twoshot) {
+        // oneshot: every rank folds every partition of every rank
+        uint64_t lines = 0;
+        for (auto& s : p.pseg[0]) lines += s.lines;
+        const Tiler t{pick_tile(lines), p.enc};
+        for (int d = 0; d < n; ++d)
+          for (int k = 0; k < n; ++k) {
+            const Seg& s = p.pseg[0][k];
+            t.over(s, [&](uint64_t t0, uint64_t nl, uint64_t ne) {
+              Item it = make_item(IK_REDUCE, d, 0, s.line0 + t0, nl, ne,
+                                  shard_begin(count, n, k) + t0 * epl);
+              set_reset(it, n, ctr.get(1, s.line0 + t0));
+              p.items1.push_back(it);
+            });
+          }
+      } else {
+        // twoshot phase 1: owner r folds partition r of every rank and
+        // publishes it into its reduced-partition image
+        const Tiler t1{pick_tile(lines_for(p.enc, M) * 1), p.enc};
+        for (int r = 0; r < n; ++r) {
+          const Seg& s = p.pseg[0][r];
+          t1.over(s, [&](uint64_t t0, uint64_t nl, uint64_t ne) {
+            Item it = make_item(IK_REDUCE, r, 0, s.line0 + t0, nl, ne, t0);
+            it.flags |= IF_PUBLISH;
+            set_reset(it, 1, 0);
+            p.items1.push_back(it);
+          });
+        }
+        // phase 2: every rank copies every owner's reduced partition
+        const Tiler t2{pick_tile(lines_for(p.enc, M) * n), p.enc};
+        for (int d = 0; d < n; ++d)
+          for (int r = 0; r < n; ++r) {
+            const Seg& s = p.agseg[r][0];
+            t2.over(s, [&](uint64_t t0, uint64_t nl, uint64_t ne) {
+              Item it = make_item(IK_COPY, d, r, s.line0 + t0, nl, ne,
+                                  shard_begin(count, n, r) + t0 * epl);
+              set_reset(it, n, ctr.get(2, ((uint64_t)r << 40) | (s.line0 + t0)));
+              p.items2.push_back(it);
+            });
+          }
+      }
+      break;
+    case CK_REDUCE_SCATTER: {
+      const Tiler t{pick_tile(lines_for(p.enc, M)), p.enc};
+      for (int r = 0; r < n; ++r) {
+        const Seg& s = p.pseg[0][r];
+        t.over(s, [&](uint64_t t0, uint64_t nl, uint64_t ne) {
+          Item it = make_item(IK_REDUCE, r, 0, s.line0 + t0, nl, ne, t0 * epl);
+          set_reset(it, 1, 0);
+          p.items1.push_back(it);
+        });
+      }
+      break;
+    }
+    case CK_ALLGATHER: {
+      const Tiler t{pick_tile(lines_for(p.enc, M) * n), p.enc};
+      for (int d = 0; d < n; ++d)
+        for (int q = 0; q < n; ++q) {
+          const Seg& s = p.pseg[q][0];
+          t.over(s, [&](uint64_t t0, uint64_t nl, uint64_t ne) {
+            Item it = make_item(IK_COPY, d, q, s.line0 + t0, nl, ne,
+                                shard_begin(count, n, q) + t0 * epl);
+            set_reset(it, n, ctr.get(3, ((uint64_t)q << 40) | (s.line0 + t0)));
+            p.items1.push_back(it);
+          });
+        }
+      break;
+    }
+    case CK_ALLTOALL: {
+      const Tiler t{pick_tile(lines_for(p.enc, M) * n), p.enc};
+      for (int d = 0; d < n; ++d)
+        for (int q = 0; q < n; ++q) {
+          const Seg& s = p.pseg[q][d];
+          t.over(s, [&](uint64_t t0, uint64_t nl, uint64_t ne) {
+            Item it = make_item(IK_COPY, d, q, s.line0 + t0, nl, ne, (uint64_t)q * M + t0 * epl);
+            set_reset(it, 1, 0);
+            p.items1.push_back(it);
+          });
+        }
+      break;
+    }
+    default:
+      return COLL_ERR_UNSUPPORTED;
+  }
+  p.ncounters = (uint32_t)ctr.keys.size();
+  group_by_dst(p.items1, n, p.beg1);
+  group_by_dst(p.items2, n, p.beg2);
+
+  // Fused grid: never more CTAs per rank than the largest per-rank list.
+  int most = 1;
+  for (int r = 0; r < n; ++r) {
+    most = std::max(most, p.sbeg[r + 1] - p.sbeg[r]);
+    most = std::max(most, p.beg1[r + 1] - p.beg1[r]);
+    most = std::max(most, p.beg2[r + 1] - p.beg2[r]);
+  }
+  p.ctas_per_rank = std::max(1, std::min(B, most));
+  const int consume_cap = in.ctas > 0 ? in.ctas : sms * 8;
+  p.consume_grid = std::max(1, std::min<int>(consume_cap, (int)std::max(p.items1.size(), p.items2.size())));
+
+  // Workspace layout.
+  uint64_t off = sizeof(WsHeader);
+  off = round_up(off, 256);
+  p.off_sitems = off;
+  off = round_up(off + p.sitems.size() * sizeof(StageItem), 256);
+  p.off_items1 = off;
+  off = round_up(off + p.items1.size() * sizeof(Item), 256);
+  p.off_items2 = off;
+  off = round_up(off + p.items2.size() * sizeof(Item), 256);
+  p.off_counters = off;
+  off = round_up(off + (uint64_t)std::max<uint32_t>(p.ncounters, 1) * 4, 4096);
+  const uint64_t lb = (uint64_t)line_bytes(p.enc);
+  p.P.rank_bytes = round_up(p.p_rank_lines * lb, 4096);
+  p.P.slot_bytes = p.P.rank_bytes * (uint64_t)n;
+  p.P.base = off;
+  off += 2 * p.P.slot_bytes;
+  p.AG.rank_bytes = round_up(p.ag_rank_lines * lb, 4096);
+  p.AG.slot_bytes = p.AG.rank_bytes * (uint64_t)n;
+  p.AG.base = off;
+  off += 2 * p.AG.slot_bytes;
+  p.ws_bytes = off;
+  return COLL_OK;
+}
+
+}  // namespace coll

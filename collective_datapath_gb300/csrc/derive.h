@@ -1,0 +1,79 @@
+// derive.h -- layout-to-schedule deriver (host only, no CUDA calls).
+//
+// From (input layout, output layout, op, nranks, count) it derives what the
+// pages' orchestration layer derives from a collective's naming (Purlin §3.2
+// "Deriving the dependencies from layouts", Listing 2): which rank images
+// are staged (one segment per partition of a scattered input, one for a
+// packed input), who consumes which segment (a packed output reduces over
+// all ranks, a scattered or transposed output copies into rank-ordered
+// slots), and for a twoshot all-reduce the composition reduce-scatter ->
+// publish -> all-gather (Purlin §3.1 "Composing transformations").  The
+// result is a set of per-CTA work lists (tiles of lines) plus the workspace
+// layout.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <vector>
+
+#include "plan.h"
+
+namespace coll {
+
+enum CollKind { CK_ALLREDUCE, CK_REDUCE_SCATTER, CK_ALLGATHER, CK_ALLTOALL, CK_MOE };
+
+struct Seg {
+  uint64_t line0;    // first line in the rank image
+  uint64_t lines;    // lines holding payload
+  uint64_t elems;    // payload elements
+  uint64_t in_elem;  // first element in the rank's input buffer
+};
+
+struct DeriveInput {
+  int in_layout, out_layout, op, dtype;
+  int nranks;
+  uint64_t count;
+  int encoding, algorithm, reset_mode, path, ctas, tile_lines;
+  uint64_t timeout_ns;
+  int tokens, hidden, topk, experts;
+  int sms;             // device SM count (a default when no device is present)
+  int fused_capacity;  // co-resident CTAs of the fused kernel
+};
+
+struct Plan {
+  CollKind kind;
+  int algorithm;  // COLL_ONESHOT / COLL_TWOSHOT for all-reduce, else 0
+  int enc;
+  int n;
+  uint64_t count;
+  uint64_t shard;  // M: elements per partition
+  int path;        // COLL_PATH_FUSED / COLL_PATH_STREAMED (when inputs are given)
+  int reset_mode;
+  uint64_t timeout_ns;
+  int ctas_per_rank;  // fused path
+  int consume_grid;   // streamed consume grid
+  uint64_t in_elems[kMaxRanks], out_elems[kMaxRanks];
+  std::vector<Seg> pseg[kMaxRanks];   // rank images written by stage
+  std::vector<Seg> agseg[kMaxRanks];  // reduced partitions (twoshot)
+  uint64_t p_rank_lines, ag_rank_lines;
+  std::vector<StageItem> sitems;
+  std::vector<Item> items1, items2;
+  int sbeg[kMaxRanks + 1], beg1[kMaxRanks + 1], beg2[kMaxRanks + 1];
+  uint32_t ncounters;
+  // workspace layout (byte offsets from the workspace base)
+  uint64_t off_sitems, off_items1, off_items2, off_counters;
+  Region P, AG;
+  uint64_t ws_bytes;
+};
+
+// Returns a coll_status_t value (0 = ok).
+int derive(const DeriveInput& in, Plan& plan);
+
+int line_bytes(int enc);
+int line_elems(int enc);
+uint64_t lines_for(int enc, uint64_t elems);
+uint64_t shard_elems(uint64_t count, int n);
+uint64_t shard_begin(uint64_t count, int n, int r);
+uint64_t shard_len(uint64_t count, int n, int r);
+
+}  // namespace coll

@@ -1,0 +1,185 @@
+// dev_common.cuh -- device helpers of the datapath kernels: memory accesses
+// with explicit PTX memory-model semantics, bounded waits, bf16 conversion,
+// error latching.  sm_103a only.
+#pragma once
+
+#include <cstdint>
+
+#include "plan.h"
+
+namespace coll {
+
+// coll_status_t values used on the device (see coll.h).
+constexpr uint32_t kStatusTimeout = 6;
+
+// ---- global memory accesses ------------------------------------------------
+// Readiness lines are written and polled with .relaxed.gpu accesses: they are
+// morally strong at GPU scope (no data race in the PTX memory model) and
+// bypass the non-coherent L1.  A vector access is a set of element accesses;
+// each 8-byte element is single-copy atomic, which is what makes an LL8 line
+// (4 bytes of data + its 4-byte flag in one element) self-validating.
+
+__device__ __forceinline__ void ld_relaxed_v2u64(const void* p, uint64_t& a,
+                                                 uint64_t& b) {
+  asm volatile("ld.relaxed.gpu.global.v2.b64 {%0, %1}, [%2];"
+               : "=l"(a), "=l"(b)
+               : "l"(p)
+               : "memory");
+}
+
+__device__ __forceinline__ void st_relaxed_v2u64(void* p, uint64_t a, uint64_t b) {
+  asm volatile("st.relaxed.gpu.global.v2.b64 [%0], {%1, %2};" ::"l"(p), "l"(a),
+               "l"(b)
+               : "memory");
+}
+
+__device__ __forceinline__ uint64_t ld_relaxed_u64(const void* p) {
+  uint64_t v;
+  asm volatile("ld.relaxed.gpu.global.b64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ void st_relaxed_u64(void* p, uint64_t v) {
+  asm volatile("st.relaxed.gpu.global.b64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+
+__device__ __forceinline__ uint32_t ld_relaxed_u32(const void* p) {
+  uint32_t v;
+  asm volatile("ld.relaxed.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ void st_relaxed_u32(void* p, uint32_t v) {
+  asm volatile("st.relaxed.gpu.global.b32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+// Acquire/release fences at GPU scope: a relaxed load followed by this fence
+// is an acquire pattern; this fence followed by a relaxed store is a release
+// pattern (PTX memory consistency model).
+__device__ __forceinline__ void fence_acq_rel_gpu() {
+  asm volatile("fence.acq_rel.gpu;" ::: "memory");
+}
+
+// Read-only input data: non-coherent path, no L1 allocation (streamed once).
+__device__ __forceinline__ uint4 ld_stream_v4(const void* p) {
+  uint4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
+}
+
+// Plain 16-byte accesses for data no other CTA of the same launch touches.
+__device__ __forceinline__ uint4 ld_v4(const void* p) {
+  uint4 v;
+  asm volatile("ld.global.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p)
+               : "memory");
+  return v;
+}
+
+__device__ __forceinline__ void st_v4(void* p, uint4 v) {
+  asm volatile("st.global.v4.u32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(v.x),
+               "r"(v.y), "r"(v.z), "r"(v.w)
+               : "memory");
+}
+
+__device__ __forceinline__ void st_v2u32(void* p, uint32_t a, uint32_t b) {
+  asm volatile("st.global.v2.u32 [%0], {%1, %2};" ::"l"(p), "r"(a), "r"(b)
+               : "memory");
+}
+
+__device__ __forceinline__ uint64_t globaltimer_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// ---- bf16 <-> fp32 -----------------------------------------------------------
+// Widening is exact: a bf16 pattern is the high half of a binary32 pattern.
+__device__ __forceinline__ float bf16_lo_to_f32(uint32_t w) {
+  return __uint_as_float(w << 16);
+}
+__device__ __forceinline__ float bf16_hi_to_f32(uint32_t w) {
+  return __uint_as_float(w & 0xFFFF0000u);
+}
+
+// binary32 -> bf16 with IEEE roundTiesToEven on the 16 dropped bits, written
+// as the usual integer formulation: add 0x7FFF plus the lowest kept bit, then
+// truncate (a carry into the exponent yields the next magnitude or Inf).
+// Subnormals are kept; any NaN becomes the quiet NaN 0x7FC0.
+__device__ __forceinline__ uint32_t f32_to_bf16_rne(float f) {
+  uint32_t u = __float_as_uint(f);
+  if ((u & 0x7FFFFFFFu) > 0x7F800000u) return 0x7FC0u;
+  return (u + 0x7FFFu + ((u >> 16) & 1u)) >> 16;
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  return f32_to_bf16_rne(lo) | (f32_to_bf16_rne(hi) << 16);
+}
+
+// ---- status -----------------------------------------------------------------
+
+__device__ __forceinline__ WsHeader* header(char* ws) {
+  return reinterpret_cast<WsHeader*>(ws);
+}
+
+// Latch the first device error (later ones are dropped) and raise `abort`
+// so that every other wait of the run gives up promptly.
+__device__ __noinline__ void latch_error(char* ws, uint32_t code, uint32_t rank,
+                                         int64_t line) {
+  WsHeader* h = header(ws);
+  if (atomicCAS(&h->status_code, 0u, code) == 0u) {
+    h->status_rank = rank;
+    h->status_line = line;
+  }
+  __threadfence();
+  st_relaxed_u32(&h->abort, 1u);
+}
+
+__device__ __forceinline__ bool aborted(char* ws) {
+  return ld_relaxed_u32(&header(ws)->abort) != 0u;
+}
+
+// Bounded wait bookkeeping: the first failed check starts the clock; the
+// wait gives up when the bound passes or another wait of the run failed.
+struct Waiter {
+  uint64_t t0 = 0;
+  __device__ __forceinline__ bool expired(char* ws, uint64_t timeout_ns) {
+    uint64_t now = globaltimer_ns();
+    if (t0 == 0) {
+      t0 = now;
+      return false;
+    }
+    return (now - t0) > timeout_ns || aborted(ws);
+  }
+};
+
+__device__ __forceinline__ void count_rejection(char* ws) {
+  atomicAdd(reinterpret_cast<unsigned long long*>(&header(ws)->rejections), 1ull);
+}
+
+// Last CTA of the run's final launch advances the epoch (the next run uses
+// the other staging slot).  Every CTA calls this once, after its work.
+__device__ __forceinline__ void finish_run(const RunParams& P, uint64_t epoch) {
+  if (!P.advance_epoch) return;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    WsHeader* h = header(P.ws);
+    __threadfence();
+    uint32_t total = gridDim.x * gridDim.y * gridDim.z;
+    if (atomicAdd(&h->done_ctas, 1u) == total - 1) {
+      h->done_ctas = 0;
+      h->started = 0;
+      st_relaxed_u64(&h->epoch, epoch + 1);
+      __threadfence();
+    }
+  }
+}
+
+__device__ __forceinline__ uint64_t read_epoch(const RunParams& P) {
+  return ld_relaxed_u64(&header(P.ws)->epoch);
+}
+
+}  // namespace coll

@@ -1,0 +1,295 @@
+// kernels.cu -- the datapath kernels and their host-side launchers.
+//
+//  k_stage     stream-ordered staging of rank inputs into LL lines
+//  k_consume   stream-ordered validate + unpack + (fold) + write, per phase
+//  k_fused     one cooperative launch: each CTA serves one emulated rank,
+//              stages its tiles, then polls and consumes; optional late
+//              producer CTAs publish withheld lines while consumers poll
+//  k_withhold  fault injection: overwrite listed lines with stale content
+//  k_rearm     LL8 re-arm of a whole slot by a separate kernel
+//  k_advance   an empty run: only the epoch advances
+#include <cuda_runtime.h>
+
+#include "launch.h"
+#include "ll128.cuh"
+#include "ll8.cuh"
+
+namespace coll {
+
+constexpr int kThreads = 256;
+
+template <int ENC, bool kConc>
+__device__ __forceinline__ void stage_item(const RunParams& P, const StageItem& it,
+                                           uint64_t e) {
+  if (ENC == ENC_LL8)
+    ll8_stage_tile(P, it, e);
+  else
+    ll128_stage_tile<kConc>(P, it, e);
+}
+
+template <int ENC, bool kConc>
+__device__ __forceinline__ void consume_item(const RunParams& P, const Region& R,
+                                             const Item& it, uint64_t e) {
+  if (ENC == ENC_LL8)
+    ll8_consume_item(P, R, it, e);
+  else
+    ll128_consume_item<kConc>(P, R, it, e);
+}
+
+template <int ENC>
+__global__ void __launch_bounds__(kThreads) k_stage(RunParams P) {
+  const uint64_t e = read_epoch(P);
+  const int lo = P.stage_rank < 0 ? 0 : P.stage_rank;
+  const int hi = P.stage_rank < 0 ? P.nranks : P.stage_rank + 1;
+  for (int i = P.sbeg[lo] + blockIdx.x; i < P.sbeg[hi]; i += gridDim.x)
+    stage_item<ENC, false>(P, P.sitems[i], e);
+}
+
+template <int ENC>
+__global__ void __launch_bounds__(kThreads) k_consume(RunParams P, int phase) {
+  const uint64_t e = read_epoch(P);
+  const Item* items = phase == 1 ? P.items1 : P.items2;
+  const int n_items = phase == 1 ? P.beg1[P.nranks] : P.beg2[P.nranks];
+  const Region& R = phase == 1 ? P.P : P.AG;
+  for (int i = blockIdx.x; i < n_items; i += gridDim.x) {
+    if (aborted(P.ws)) break;
+    consume_item<ENC, false>(P, R, items[i], e);
+  }
+  finish_run(P, e);
+}
+
+// Late producer: publish rank p's withheld lines in the given order, after
+// every consumer CTA has started polling.  One warp publishes, in order.
+template <int ENC>
+__device__ void late_producer(const RunParams& P, uint64_t e, int p, int workers) {
+  WsHeader* h = header(P.ws);
+  __shared__ int go;
+  if (threadIdx.x == 0) {
+    Waiter w;
+    go = 1;
+    while (ld_relaxed_u32(&h->started) < (uint32_t)workers) {
+      if (w.expired(P.ws, P.timeout_ns)) {
+        latch_error(P.ws, kStatusTimeout, p, -1);
+        go = 0;
+        break;
+      }
+      __nanosleep(200);
+    }
+  }
+  __syncthreads();
+  if (!go || threadIdx.x >= 32) return;
+  __nanosleep(2000);  // consumers are polling the stale lines by now
+  const int lane = threadIdx.x;
+  const int64_t n = P.late_n[p];
+  const int64_t* order = P.late_order[p];
+  const uint16_t* in = P.in[p];
+  auto locate = [&](int64_t line, uint64_t& elem0, int64_t& elems) {
+    // segment containing `line` (segments are in image order)
+    int k = 0;
+    while (k + 1 < P.nseg && (uint64_t)line >= P.seg_line0[k + 1]) ++k;
+    const int epl = ENC == ENC_LL8 ? kLL8Elems : kLL128Elems;
+    const uint64_t off = ((uint64_t)line - P.seg_line0[k]) * epl;
+    elem0 = P.seg_in0[k] + off;
+    elems = (int64_t)P.seg_elems[k] - (int64_t)off;  // elements left in segment
+  };
+  if (ENC == ENC_LL8) {
+    uint64_t* img = image_lines(P, P.P, e, p);
+    for (int64_t j = 0; j < n; j += 32) {
+      if (j + lane < n) {
+        const int64_t line = order[j + lane];
+        uint64_t elem0;
+        int64_t left;
+        locate(line, elem0, left);
+        const uint32_t data = *reinterpret_cast<const uint32_t*>(in + elem0);
+        st_relaxed_u64(img + line, (uint64_t)data | ((uint64_t)(uint32_t)e << 32));
+      }
+      __syncwarp();
+      __nanosleep(500);
+    }
+  } else {
+    char* img = image_bytes(P, P.P, e, p);
+    const int i = lane >> 3, k = lane & 7;
+    for (int64_t j = 0; j < n; j += 4) {
+      const bool valid = j + i < n;
+      char* dst = nullptr;
+      if (valid) {
+        const int64_t line = order[j + i];
+        uint64_t elem0;
+        int64_t left;
+        locate(line, elem0, left);
+        dst = img + (uint64_t)line * kLL128LineBytes + 16 * k;
+        // this lane's 8 (k < 7) or 4 (k = 7) elements; zero past the segment
+        uint16_t v[8];
+        for (int q = 0; q < 8; ++q) {
+          const int64_t idx = 8 * k + q;
+          v[q] = (q < (k == 7 ? 4 : 8) && idx < left) ? in[elem0 + idx] : 0;
+        }
+        const uint64_t lo = (uint64_t)v[0] | ((uint64_t)v[1] << 16) |
+                            ((uint64_t)v[2] << 32) | ((uint64_t)v[3] << 48);
+        const uint64_t hi = (uint64_t)v[4] | ((uint64_t)v[5] << 16) |
+                            ((uint64_t)v[6] << 32) | ((uint64_t)v[7] << 48);
+        if (k == 7)
+          st_relaxed_u64(dst, lo);
+        else
+          st_relaxed_v2u64(dst, lo, hi);
+      }
+      __syncwarp();
+      if (valid && k == 7) {
+        fence_acq_rel_gpu();
+        st_relaxed_u64(dst + 8, e);
+      }
+      __syncwarp();
+      __nanosleep(500);
+    }
+  }
+}
+
+template <int ENC>
+__global__ void __launch_bounds__(kThreads) k_fused(RunParams P) {
+  const uint64_t e = read_epoch(P);
+  const int B = P.ctas_per_rank;
+  const int workers = P.nranks * B;
+  if ((int)blockIdx.x >= workers) {
+    late_producer<ENC>(P, e, ((int)blockIdx.x - workers) % P.nranks, workers);
+    finish_run(P, e);
+    return;
+  }
+  const int d = blockIdx.x / B, b = blockIdx.x % B;
+  if (P.sitems != nullptr)
+    for (int i = P.sbeg[d] + b; i < P.sbeg[d + 1]; i += B)
+      stage_item<ENC, true>(P, P.sitems[i], e);
+  if (threadIdx.x == 0) atomicAdd(&header(P.ws)->started, 1u);
+  for (int i = P.beg1[d] + b; i < P.beg1[d + 1]; i += B) {
+    if (aborted(P.ws)) break;
+    consume_item<ENC, true>(P, P.P, P.items1[i], e);
+  }
+  if (P.items2 != nullptr)
+    for (int i = P.beg2[d] + b; i < P.beg2[d + 1]; i += B) {
+      if (aborted(P.ws)) break;
+      consume_item<ENC, true>(P, P.AG, P.items2[i], e);
+    }
+  finish_run(P, e);
+}
+
+// Overwrite the listed lines of rank `stage_rank`'s image with stale
+// content: readiness value e-1 / e-2 / 0 (by kind) and a poison payload.
+template <int ENC>
+__global__ void k_withhold(RunParams P) {
+  const uint64_t e = read_epoch(P);
+  const int p = P.stage_rank;
+  for (int64_t j = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; j < P.wh_n;
+       j += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t line = P.wh_lines[j];
+    const int kind = P.wh_kind[j];
+    const uint64_t stale = kind == 0 ? e - 1 : (kind == 1 ? e - 2 : 0);
+    const uint64_t pz = P.wh_poison[j];
+    const uint64_t pw = pz | (pz << 16) | (pz << 32) | (pz << 48);
+    if (ENC == ENC_LL8) {
+      uint64_t* img = image_lines(P, P.P, e, p);
+      st_relaxed_u64(img + line, (pw & 0xFFFFFFFFull) | ((uint64_t)(uint32_t)stale << 32));
+    } else {
+      char* l = image_bytes(P, P.P, e, p) + (uint64_t)line * kLL128LineBytes;
+      for (int q = 0; q < 15; ++q) st_relaxed_u64(l + 8 * q, pw);
+      st_relaxed_u64(l + 120, stale);
+    }
+  }
+}
+
+// Re-arm every LL8 line of the current slot (both regions), then end the run.
+__global__ void __launch_bounds__(kThreads) k_rearm(RunParams P) {
+  const uint64_t e = read_epoch(P);
+  for (int region = 0; region < 2; ++region) {
+    const Region& R = region == 0 ? P.P : P.AG;
+    if (R.rank_bytes == 0) continue;
+    const uint64_t words = (uint64_t)P.nranks * R.rank_bytes / 16;
+    uint4* base = reinterpret_cast<uint4*>(P.ws + R.base + (e & 1) * R.slot_bytes);
+    for (uint64_t i = blockIdx.x * (uint64_t)blockDim.x + threadIdx.x; i < words;
+         i += (uint64_t)gridDim.x * blockDim.x)
+      st_relaxed_v2u64(base + i, 0ull, 0ull);
+  }
+  finish_run(P, e);
+}
+
+__global__ void k_advance(RunParams P) { finish_run(P, read_epoch(P)); }
+
+// ---- launchers ---------------------------------------------------------------
+
+static int g_num_sms = 0;
+
+int device_sms() {
+  if (g_num_sms == 0) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&g_num_sms, cudaDevAttrMultiProcessorCount, dev);
+    if (g_num_sms <= 0) g_num_sms = 1;
+  }
+  return g_num_sms;
+}
+
+int fused_capacity(int enc) {
+  int per_sm = 0;
+  cudaError_t err = enc == ENC_LL8
+                        ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+                              &per_sm, k_fused<ENC_LL8>, kThreads, 0)
+                        : cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+                              &per_sm, k_fused<ENC_LL128>, kThreads, 0);
+  if (err != cudaSuccess || per_sm <= 0) return 0;
+  return per_sm * device_sms();
+}
+
+int block_threads() { return kThreads; }
+
+cudaError_t launch_stage(const RunParams& P, int grid, cudaStream_t s) {
+  if (grid <= 0) return cudaSuccess;
+  if (P.enc == ENC_LL8)
+    k_stage<ENC_LL8><<<grid, kThreads, 0, s>>>(P);
+  else
+    k_stage<ENC_LL128><<<grid, kThreads, 0, s>>>(P);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_consume(const RunParams& P, int phase, int grid, cudaStream_t s) {
+  if (grid <= 0) grid = 1;
+  if (P.enc == ENC_LL8)
+    k_consume<ENC_LL8><<<grid, kThreads, 0, s>>>(P, phase);
+  else
+    k_consume<ENC_LL128><<<grid, kThreads, 0, s>>>(P, phase);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_fused(const RunParams& P, int grid, cudaStream_t s) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (P.enc == ENC_LL8) return cudaLaunchKernelEx(&cfg, k_fused<ENC_LL8>, P);
+  return cudaLaunchKernelEx(&cfg, k_fused<ENC_LL128>, P);
+}
+
+cudaError_t launch_withhold(const RunParams& P, cudaStream_t s) {
+  if (P.wh_n <= 0) return cudaSuccess;
+  const int grid = (int)((P.wh_n + kThreads - 1) / kThreads);
+  if (P.enc == ENC_LL8)
+    k_withhold<ENC_LL8><<<grid, kThreads, 0, s>>>(P);
+  else
+    k_withhold<ENC_LL128><<<grid, kThreads, 0, s>>>(P);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_rearm(const RunParams& P, int grid, cudaStream_t s) {
+  k_rearm<<<grid, kThreads, 0, s>>>(P);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_advance(const RunParams& P, cudaStream_t s) {
+  k_advance<<<1, 32, 0, s>>>(P);
+  return cudaGetLastError();
+}
+
+}  // namespace coll

@@ -1,0 +1,22 @@
+// launch.h -- host-side launchers of the datapath kernels (kernels.cu).
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include "plan.h"
+
+namespace coll {
+
+int device_sms();
+int block_threads();
+// Co-resident CTAs of the fused kernel on this device (0 if unknown).
+int fused_capacity(int enc);
+
+cudaError_t launch_stage(const RunParams& P, int grid, cudaStream_t s);
+cudaError_t launch_consume(const RunParams& P, int phase, int grid, cudaStream_t s);
+cudaError_t launch_fused(const RunParams& P, int grid, cudaStream_t s);
+cudaError_t launch_withhold(const RunParams& P, cudaStream_t s);
+cudaError_t launch_rearm(const RunParams& P, int grid, cudaStream_t s);
+cudaError_t launch_advance(const RunParams& P, cudaStream_t s);
+
+}  // namespace coll

@@ -1,0 +1,264 @@
+// ll128.cuh -- LL128 datapath: 128-byte lines holding 120 bytes of data (60
+// bf16) and the epoch as an 8-byte sequence number in bytes 120..127
+// (flash-comm §3.1 "Sequence-number readiness": accept a unit only when its
+// number is the current call's; no re-arm is needed).
+//
+// A warp moves one "row" of four lines (512 bytes of lines, 480 bytes of
+// payload) per step: lane L holds bytes [16L, 16L+16) of the row, i.e. chunk
+// k = L & 7 of line i = L >> 3; chunk 7 of a line holds its last 8 data bytes
+// and the sequence number.  Payload is 16-byte aligned per row (480 = 30 x 16)
+// but not per line (120 is 8 mod 16), so rows are re-aligned between the line
+// view and the payload view with warp shuffles of 8-byte granules.
+//
+// Two publication protocols:
+//  * stream-ordered (stage and consume are separate kernels on one stream):
+//    the kernel boundary orders every staged byte before every consumer
+//    load, so a line is written with one 16-byte store per lane and read the
+//    same way; the consumer still checks every line's number and rejects a
+//    line that was not staged for this epoch.
+//  * concurrent (producer and consumer CTAs of one cooperative launch):
+//    data stores, __syncwarp, fence.acq_rel.gpu, then the number (a release
+//    pattern); the consumer reads the number, fence.acq_rel.gpu, __syncwarp,
+//    then the data (an acquire pattern).  A 128-byte line is not single-copy
+//    atomic, so this ordering -- not the line size -- is what makes it safe.
+#pragma once
+
+#include "dev_common.cuh"
+
+namespace coll {
+
+constexpr int kRowElems = kLL128RowLines * kLL128Elems;  // 240
+constexpr int kRowBytes = kLL128RowLines * kLL128LineBytes;  // 512
+
+__device__ __forceinline__ char* image_bytes(const RunParams& P, const Region& R,
+                                             uint64_t epoch, int rank) {
+  return P.ws + R.base + (epoch & 1) * R.slot_bytes + (uint64_t)rank * R.rank_bytes;
+}
+
+__device__ __forceinline__ uint4 shfl4(uint4 v, int src) {
+  uint4 r;
+  r.x = __shfl_sync(0xFFFFFFFFu, v.x, src);
+  r.y = __shfl_sync(0xFFFFFFFFu, v.y, src);
+  r.z = __shfl_sync(0xFFFFFFFFu, v.z, src);
+  r.w = __shfl_sync(0xFFFFFFFFu, v.w, src);
+  return r;
+}
+
+// Payload chunks (lane q < 30 holds payload bytes [16q, 16q+16) of the row)
+// -> line chunks (lane L holds its 16 bytes of the row's lines).  For lane
+// chunk k = 7 only .x/.y are data; .z/.w are left for the sequence number.
+__device__ __forceinline__ uint4 payload_to_lines(uint4 pay, int lane) {
+  const int i = lane >> 3, k = lane & 7;
+  const int G = 15 * i + 2 * k;             // first 8-byte payload granule
+  const int A = G >> 1;
+  const int B = (k == 7) ? A : ((G + 1) >> 1);
+  uint4 a = shfl4(pay, A);
+  uint4 b = shfl4(pay, B);
+  uint4 r;
+  if ((G & 1) == 0) {
+    r = a;
+  } else {
+    r.x = a.z; r.y = a.w; r.z = b.x; r.w = b.y;
+  }
+  return r;
+}
+
+// Line chunks -> payload chunks (inverse of payload_to_lines).
+__device__ __forceinline__ uint4 lines_to_payload(uint4 ln, int lane) {
+  const int q = lane < 30 ? lane : 29;
+  const int G0 = 2 * q, G1 = 2 * q + 1;
+  const int i0 = G0 / 15, g0 = G0 % 15, i1 = G1 / 15, g1 = G1 % 15;
+  const int A = 8 * i0 + (g0 >> 1), B = 8 * i1 + (g1 >> 1);
+  uint4 a = shfl4(ln, A);
+  uint4 b = shfl4(ln, B);
+  uint4 r;
+  r.x = (g0 & 1) ? a.z : a.x;
+  r.y = (g0 & 1) ? a.w : a.y;
+  r.z = (g1 & 1) ? b.z : b.x;
+  r.w = (g1 & 1) ? b.w : b.y;
+  return r;
+}
+
+// Write one row of lines.  `ln` = this lane's line chunk (data), the lane
+// with k = 7 adds the sequence number.  Lanes of lines >= nl write nothing.
+template <bool kConc>
+__device__ __forceinline__ void ll128_store_row(char* row, uint4 ln, int lane, int nl,
+                                                uint64_t seq) {
+  const int i = lane >> 3, k = lane & 7;
+  const bool valid = i < nl;
+  char* p = row + 16 * lane;
+  if (!kConc) {
+    if (valid) {
+      if (k == 7) {
+        ln.z = (uint32_t)seq;
+        ln.w = (uint32_t)(seq >> 32);
+      }
+      st_v4(p, ln);
+    }
+    return;
+  }
+  if (valid) {
+    if (k == 7)
+      st_relaxed_u64(p, (uint64_t)ln.x | ((uint64_t)ln.y << 32));
+    else
+      st_relaxed_v2u64(p, (uint64_t)ln.x | ((uint64_t)ln.y << 32),
+                       (uint64_t)ln.z | ((uint64_t)ln.w << 32));
+  }
+  __syncwarp();
+  if (valid && k == 7) {
+    fence_acq_rel_gpu();
+    st_relaxed_u64(p + 8, seq);
+  }
+}
+
+// Bounded wait for the sequence number at `p` (a lane with k = 7).
+__device__ __noinline__ bool ll128_wait_seq(const RunParams& P, const char* p,
+                                            uint64_t seq, uint32_t rank, int64_t line) {
+  count_rejection(P.ws);
+  Waiter w;
+  for (;;) {
+    if (w.expired(P.ws, P.timeout_ns)) {
+      latch_error(P.ws, kStatusTimeout, rank, line);
+      return false;
+    }
+    __nanosleep(64);
+    if (ld_relaxed_u64(p) == seq) return true;
+  }
+}
+
+// Read one row of lines of one image, validated.  Returns false on timeout.
+// Stream-ordered: load, check, and only on a mismatch wait and reload.
+// Concurrent: number first, acquire fence, then the data.
+template <bool kConc>
+__device__ __forceinline__ bool ll128_load_row(const RunParams& P, const char* row,
+                                               uint4& ln, int lane, int nl,
+                                               uint64_t seq, uint32_t rank,
+                                               int64_t row_line) {
+  const int i = lane >> 3, k = lane & 7;
+  const bool valid = i < nl;
+  const char* p = row + 16 * lane;
+  bool ok = true;
+  if (!kConc) {
+    ln = valid ? ld_v4(p) : make_uint4(0, 0, 0, 0);
+    bool ready = !(valid && k == 7) ||
+                 (((uint64_t)ln.w << 32) | ln.z) == seq;
+    if (__all_sync(0xFFFFFFFFu, ready)) return true;
+    if (!ready) {
+      ok = ll128_wait_seq(P, p + 8, seq, rank, row_line + i);
+      fence_acq_rel_gpu();
+    }
+    __syncwarp();
+    if (__all_sync(0xFFFFFFFFu, ok)) {
+      if (valid) ln = ld_v4(p);
+      return true;
+    }
+    return false;
+  }
+  if (valid && k == 7) {
+    if (ld_relaxed_u64(p + 8) != seq) ok = ll128_wait_seq(P, p + 8, seq, rank, row_line + i);
+    fence_acq_rel_gpu();
+  }
+  __syncwarp();
+  if (!__all_sync(0xFFFFFFFFu, ok)) return false;
+  if (valid) {
+    uint64_t a, b;
+    ld_relaxed_v2u64(p, a, b);
+    ln = make_uint4((uint32_t)a, (uint32_t)(a >> 32), (uint32_t)b, (uint32_t)(b >> 32));
+  } else {
+    ln = make_uint4(0, 0, 0, 0);
+  }
+  return true;
+}
+
+// Stage one tile: rows of 240 input elements -> rows of four lines.
+template <bool kConc>
+__device__ __forceinline__ void ll128_stage_tile(const RunParams& P, const StageItem& it,
+                                                 uint64_t epoch) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
+  const uint16_t* in = P.in[it.rank] + it.in_elem;
+  char* img = image_bytes(P, P.P, epoch, it.rank) + it.dst_line * kLL128LineBytes;
+  const uint32_t nrows = (it.nlines + kLL128RowLines - 1) / kLL128RowLines;
+  for (uint32_t r = warp; r < nrows; r += nwarps) {
+    const int64_t left = (int64_t)it.nelems - (int64_t)r * kRowElems;
+    uint4 pay = make_uint4(0, 0, 0, 0);
+    if (lane < 30 && 8 * lane < left) pay = ld_stream_v4(in + (size_t)r * kRowElems + 8 * lane);
+    uint4 ln = payload_to_lines(pay, lane);
+    const int nl = min((int)kLL128RowLines, (int)(it.nlines - r * kLL128RowLines));
+    ll128_store_row<kConc>(img + (size_t)r * kRowBytes, ln, lane, nl, epoch);
+  }
+}
+
+// Fold the 8 (k < 7) or 4 (k = 7) bf16 of this lane's chunk over n images.
+__device__ __forceinline__ uint4 ll128_fold(const uint4* s, int n) {
+  float a[8];
+  a[0] = bf16_lo_to_f32(s[0].x); a[1] = bf16_hi_to_f32(s[0].x);
+  a[2] = bf16_lo_to_f32(s[0].y); a[3] = bf16_hi_to_f32(s[0].y);
+  a[4] = bf16_lo_to_f32(s[0].z); a[5] = bf16_hi_to_f32(s[0].z);
+  a[6] = bf16_lo_to_f32(s[0].w); a[7] = bf16_hi_to_f32(s[0].w);
+#pragma unroll
+  for (int p = 1; p < kMaxRanks; ++p) {
+    if (p < n) {
+      a[0] = __fadd_rn(a[0], bf16_lo_to_f32(s[p].x));
+      a[1] = __fadd_rn(a[1], bf16_hi_to_f32(s[p].x));
+      a[2] = __fadd_rn(a[2], bf16_lo_to_f32(s[p].y));
+      a[3] = __fadd_rn(a[3], bf16_hi_to_f32(s[p].y));
+      a[4] = __fadd_rn(a[4], bf16_lo_to_f32(s[p].z));
+      a[5] = __fadd_rn(a[5], bf16_hi_to_f32(s[p].z));
+      a[6] = __fadd_rn(a[6], bf16_lo_to_f32(s[p].w));
+      a[7] = __fadd_rn(a[7], bf16_hi_to_f32(s[p].w));
+    }
+  }
+  return make_uint4(pack_bf16x2(a[0], a[1]), pack_bf16x2(a[2], a[3]),
+                    pack_bf16x2(a[4], a[5]), pack_bf16x2(a[6], a[7]));
+}
+
+// Write the row's payload (line view `ln`) to a plain output buffer.
+__device__ __forceinline__ void ll128_write_payload(uint16_t* out_row, uint4 ln, int lane,
+                                                    int64_t left) {
+  uint4 pay = lines_to_payload(ln, lane);
+  if (lane < 30 && 8 * lane < left) st_v4(out_row + 8 * lane, pay);
+}
+
+// Process one consume item (see ll8_consume_item); `R` = source region.
+template <bool kConc>
+__device__ __forceinline__ void ll128_consume_item(const RunParams& P, const Region& R,
+                                                   const Item& it, uint64_t epoch) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
+  const int n = P.nranks;
+  const bool reduce = it.kind == IK_REDUCE;
+  const bool publish = (it.flags & IF_PUBLISH) != 0;
+  const uint32_t nrows = (it.nlines + kLL128RowLines - 1) / kLL128RowLines;
+  for (uint32_t r = warp; r < nrows; r += nwarps) {
+    const int nl = min((int)kLL128RowLines, (int)(it.nlines - r * kLL128RowLines));
+    const uint64_t row_line = it.src_line + (uint64_t)r * kLL128RowLines;
+    const int64_t left = (int64_t)it.nelems - (int64_t)r * kRowElems;
+    uint4 res;
+    bool ok = true;
+    if (reduce) {
+      uint4 s[kMaxRanks];
+#pragma unroll
+      for (int p = 0; p < kMaxRanks; ++p)
+        if (p < n)
+          ok = ok && ll128_load_row<kConc>(P, image_bytes(P, R, epoch, p) +
+                                                  row_line * kLL128LineBytes,
+                                           s[p], lane, nl, epoch, p, (int64_t)row_line);
+      if (!ok) return;
+      res = ll128_fold(s, n);
+    } else {
+      ok = ll128_load_row<kConc>(P, image_bytes(P, R, epoch, it.src) +
+                                        row_line * kLL128LineBytes,
+                                 res, lane, nl, epoch, it.src, (int64_t)row_line);
+      if (!ok) return;
+    }
+    if (publish) {
+      char* dst = image_bytes(P, P.AG, epoch, it.dst) +
+                  (it.out_off + (uint64_t)r * kLL128RowLines) * kLL128LineBytes;
+      ll128_store_row<kConc>(dst, res, lane, nl, epoch);
+    } else {
+      ll128_write_payload(P.out[it.dst] + it.out_off + (uint64_t)r * kRowElems, res,
+                          lane, left);
+    }
+  }
+}
+
+}  // namespace coll

@@ -1,0 +1,191 @@
+// ll8.cuh -- LL8 datapath: 8-byte lines of 4 data bytes (two bf16) and a
+// 4-byte flag equal to the epoch's low 32 bits.  A thread handles groups of
+// four lines (one 16-byte input chunk, 32 bytes of lines, two 16-byte stores).
+//
+// The line is the notification: Purlin §3.2 "Specializing for latency"
+// packs payload and flag in one packet written by a single store; flash-comm
+// §4.3 carries two copies of the sequence number beside 8 payload bytes in a
+// 16-byte unit, which is exactly two LL8 lines.  Because data and flag share
+// one single-copy-atomic 8-byte element, a consumer that sees the right flag
+// also sees the right data, with no fence on either side.
+#pragma once
+
+#include "dev_common.cuh"
+
+namespace coll {
+
+struct LL8Group {
+  uint64_t l0, l1, l2, l3;
+};
+
+__device__ __forceinline__ void ll8_load(const uint64_t* p, LL8Group& g) {
+  ld_relaxed_v2u64(p, g.l0, g.l1);
+  ld_relaxed_v2u64(p + 2, g.l2, g.l3);
+}
+
+__device__ __forceinline__ bool ll8_ready(const LL8Group& g, uint32_t flag) {
+  return (uint32_t)(g.l0 >> 32) == flag && (uint32_t)(g.l1 >> 32) == flag &&
+         (uint32_t)(g.l2 >> 32) == flag && (uint32_t)(g.l3 >> 32) == flag;
+}
+
+__device__ __forceinline__ void ll8_store(uint64_t* p, uint4 v, uint32_t flag) {
+  const uint64_t f = (uint64_t)flag << 32;
+  st_relaxed_v2u64(p, (uint64_t)v.x | f, (uint64_t)v.y | f);
+  st_relaxed_v2u64(p + 2, (uint64_t)v.z | f, (uint64_t)v.w | f);
+}
+
+__device__ __forceinline__ void ll8_rearm(uint64_t* p) {
+  st_relaxed_v2u64(p, 0ull, 0ull);
+  st_relaxed_v2u64(p + 2, 0ull, 0ull);
+}
+
+// Poll a group until every line carries `flag` (bounded); the caller then
+// reloads it.  Returns false on timeout or abort (the error is latched).
+__device__ __noinline__ bool ll8_wait(const RunParams& P, const uint64_t* p, uint32_t flag,
+                                      uint32_t rank, int64_t line) {
+  count_rejection(P.ws);
+  Waiter w;
+  for (;;) {
+    if (w.expired(P.ws, P.timeout_ns)) {
+      latch_error(P.ws, kStatusTimeout, rank, line);
+      return false;
+    }
+    __nanosleep(64);
+    LL8Group g;
+    ll8_load(p, g);
+    if (ll8_ready(g, flag)) return true;
+  }
+}
+
+__device__ __forceinline__ uint64_t* image_lines(const RunParams& P, const Region& R,
+                                                 uint64_t epoch, int rank) {
+  return reinterpret_cast<uint64_t*>(P.ws + R.base + (epoch & 1) * R.slot_bytes +
+                                     (uint64_t)rank * R.rank_bytes);
+}
+
+// Encode one staging tile (nlines is a multiple of 4 for LL8).
+__device__ __forceinline__ void ll8_stage_tile(const RunParams& P, const StageItem& it,
+                                               uint64_t epoch) {
+  const uint16_t* in = P.in[it.rank] + it.in_elem;
+  uint64_t* img = image_lines(P, P.P, epoch, it.rank) + it.dst_line;
+  const uint32_t flag = (uint32_t)epoch;
+  const uint32_t ngroups = it.nlines / kLL8GroupLines;
+  for (uint32_t g = threadIdx.x; g < ngroups; g += blockDim.x) {
+    uint4 v = ld_stream_v4(in + 8 * (size_t)g);
+    ll8_store(img + 4 * (size_t)g, v, flag);
+  }
+}
+
+// Fold one group of every rank in rank order (fp32, one rounding).
+__device__ __forceinline__ uint4 ll8_fold(const LL8Group* s, int n) {
+  float a[8];
+  {
+    const uint32_t w0 = (uint32_t)s[0].l0, w1 = (uint32_t)s[0].l1,
+                   w2 = (uint32_t)s[0].l2, w3 = (uint32_t)s[0].l3;
+    a[0] = bf16_lo_to_f32(w0); a[1] = bf16_hi_to_f32(w0);
+    a[2] = bf16_lo_to_f32(w1); a[3] = bf16_hi_to_f32(w1);
+    a[4] = bf16_lo_to_f32(w2); a[5] = bf16_hi_to_f32(w2);
+    a[6] = bf16_lo_to_f32(w3); a[7] = bf16_hi_to_f32(w3);
+  }
+#pragma unroll
+  for (int p = 1; p < kMaxRanks; ++p) {
+    if (p < n) {
+      const uint32_t w0 = (uint32_t)s[p].l0, w1 = (uint32_t)s[p].l1,
+                     w2 = (uint32_t)s[p].l2, w3 = (uint32_t)s[p].l3;
+      a[0] = __fadd_rn(a[0], bf16_lo_to_f32(w0));
+      a[1] = __fadd_rn(a[1], bf16_hi_to_f32(w0));
+      a[2] = __fadd_rn(a[2], bf16_lo_to_f32(w1));
+      a[3] = __fadd_rn(a[3], bf16_hi_to_f32(w1));
+      a[4] = __fadd_rn(a[4], bf16_lo_to_f32(w2));
+      a[5] = __fadd_rn(a[5], bf16_hi_to_f32(w2));
+      a[6] = __fadd_rn(a[6], bf16_lo_to_f32(w3));
+      a[7] = __fadd_rn(a[7], bf16_hi_to_f32(w3));
+    }
+  }
+  uint4 r;
+  r.x = pack_bf16x2(a[0], a[1]);
+  r.y = pack_bf16x2(a[2], a[3]);
+  r.z = pack_bf16x2(a[4], a[5]);
+  r.w = pack_bf16x2(a[6], a[7]);
+  return r;
+}
+
+// Process one consume item: validate + unpack (+ fold) + write (+ re-arm).
+// `R` is the source region (P for phase 1, AG for twoshot phase 2).
+__device__ __forceinline__ void ll8_consume_item(const RunParams& P, const Region& R,
+                                                 const Item& it, uint64_t epoch) {
+  const uint32_t flag = (uint32_t)epoch;
+  const int n = P.nranks;
+  const uint32_t ngroups = it.nlines / kLL8GroupLines;
+  const bool reduce = it.kind == IK_REDUCE;
+  const bool publish = (it.flags & IF_PUBLISH) != 0;
+  const bool sole = (it.flags & IF_RESET_SOLE) != 0 && P.reset_mode == 0;
+  bool ok = true;
+  for (uint32_t g = threadIdx.x; g < ngroups; g += blockDim.x) {
+    const uint64_t line = it.src_line + 4 * (uint64_t)g;
+    uint4 res;
+    if (reduce) {
+      LL8Group s[kMaxRanks];
+#pragma unroll
+      for (int p = 0; p < kMaxRanks; ++p)
+        if (p < n) ll8_load(image_lines(P, R, epoch, p) + line, s[p]);
+#pragma unroll
+      for (int p = 0; p < kMaxRanks; ++p)
+        if (p < n && !ll8_ready(s[p], flag)) {
+          const uint64_t* src = image_lines(P, R, epoch, p) + line;
+          ok = ok && ll8_wait(P, src, flag, p, (int64_t)line);
+          ll8_load(src, s[p]);
+        }
+      res = ll8_fold(s, n);
+      if (sole) {
+#pragma unroll
+        for (int p = 0; p < kMaxRanks; ++p)
+          if (p < n) ll8_rearm(image_lines(P, R, epoch, p) + line);
+      }
+    } else {
+      LL8Group s;
+      uint64_t* src = image_lines(P, R, epoch, it.src) + line;
+      ll8_load(src, s);
+      if (!ll8_ready(s, flag)) {
+        ok = ok && ll8_wait(P, src, flag, it.src, (int64_t)line);
+        ll8_load(src, s);
+      }
+      res = make_uint4((uint32_t)s.l0, (uint32_t)s.l1, (uint32_t)s.l2, (uint32_t)s.l3);
+      if (sole) ll8_rearm(src);
+    }
+    if (!ok) break;
+    if (publish) {
+      ll8_store(image_lines(P, P.AG, epoch, it.dst) + it.out_off + 4 * (uint64_t)g, res,
+                flag);
+    } else {
+      st_v4(P.out[it.dst] + it.out_off + 8 * (uint64_t)g, res);
+    }
+  }
+  if ((it.flags & IF_RESET_COUNTED) && P.reset_mode == 0) {
+    // The last of `readers` items over these lines re-arms them.
+    __shared__ uint32_t last;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      __threadfence();
+      uint32_t old = atomicAdd(&P.counters[it.counter], 1u);
+      last = (old == (uint32_t)it.readers - 1u);
+      if (last) {
+        P.counters[it.counter] = 0u;
+        __threadfence();
+      }
+    }
+    __syncthreads();
+    if (last) {
+      for (uint32_t g = threadIdx.x; g < ngroups; g += blockDim.x) {
+        const uint64_t line = it.src_line + 4 * (uint64_t)g;
+        if (reduce) {
+          for (int p = 0; p < n; ++p) ll8_rearm(image_lines(P, R, epoch, p) + line);
+        } else {
+          ll8_rearm(image_lines(P, R, epoch, it.src) + line);
+        }
+      }
+    }
+  }
+}
+
+}  // namespace coll

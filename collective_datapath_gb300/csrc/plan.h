@@ -1,0 +1,127 @@
+// plan.h -- schedule and workspace structures shared by the host deriver
+// (derive.cpp, api.cpp) and the CUDA kernels.  Plain C++ structs, no CUDA
+// types, so both compilers see the same layout.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+
+namespace coll {
+
+constexpr int kMaxRanks = 8;
+
+// Readiness encodings (values match COLL_LL8 / COLL_LL128 of coll.h).
+enum Encoding : int { ENC_LL8 = 0, ENC_LL128 = 1 };
+
+// Bytes per line and bf16 payload elements per line of each encoding.
+constexpr int kLL8LineBytes = 8, kLL8Elems = 2;
+constexpr int kLL128LineBytes = 128, kLL128Elems = 60;
+// Lines of one 16-byte LL8 input chunk / one 512-byte LL128 warp row.
+constexpr int kLL8GroupLines = 4;
+constexpr int kLL128RowLines = 4;
+
+// Work item kinds: fold the same tile of every rank's image in rank order
+// ("Atom::reduce" of Purlin Listing 3) or copy one rank's tile ("Atom::copy").
+enum ItemKind : uint8_t { IK_REDUCE = 0, IK_COPY = 1 };
+
+enum ItemFlags : uint8_t {
+  IF_PUBLISH = 1,        // write the result as lines into the reduced-partition
+                         // region of rank `dst` (twoshot reduce-scatter owner)
+  IF_RESET_SOLE = 2,     // sole reader: re-arm the lines it read right away
+  IF_RESET_COUNTED = 4,  // one of `readers` readers: the last one re-arms
+};
+
+// One consume work item: a tile of lines served for one destination rank.
+// Lines are counted within a rank image of the source region.  40 bytes.
+struct Item {
+  uint8_t kind;      // ItemKind
+  uint8_t flags;     // ItemFlags
+  uint8_t dst;       // rank whose output (or published partition) this writes
+  uint8_t src;       // IK_COPY: the source rank image; IK_REDUCE: unused
+  uint16_t readers;  // IF_RESET_COUNTED: readers sharing `counter`
+  uint16_t pad0;
+  uint32_t nlines;   // lines in the tile (a multiple of the group/row size
+                     // except at the end of a segment)
+  uint32_t nelems;   // payload elements in the tile
+  uint64_t src_line; // first line of the tile in the source image
+  uint64_t out_off;  // IF_PUBLISH: first line in dst's image of the reduced
+                     // region; otherwise first output element in out[dst]
+  uint32_t counter;  // reader counter index (IF_RESET_COUNTED)
+  uint32_t pad1;
+};
+static_assert(sizeof(Item) == 40, "Item layout");
+
+// One staging work item: encode a tile of rank `rank`'s input.  32 bytes.
+struct StageItem {
+  uint16_t rank;
+  uint16_t pad0;
+  uint32_t nlines;
+  uint32_t nelems;
+  uint32_t pad1;
+  uint64_t dst_line;  // first line in the rank image
+  uint64_t in_elem;   // first input element
+};
+static_assert(sizeof(StageItem) == 32, "StageItem layout");
+
+// Device-resident control block at the start of the workspace.
+struct WsHeader {
+  uint64_t epoch;          // current epoch; slot = epoch & 1
+  uint32_t status_code;    // 0 or a coll_status_t latched by a kernel
+  uint32_t status_rank;
+  int64_t status_line;
+  uint32_t abort;          // nonzero after an error: waits give up at once
+  uint32_t done_ctas;      // last-CTA counter of the run's final kernel
+  uint32_t started;        // fused late runs: consumer CTAs that started
+  uint32_t pad0;
+  uint64_t rejections;     // stale lines observed (diagnostic)
+  uint64_t pad1[26];
+};
+static_assert(sizeof(WsHeader) == 256, "WsHeader layout");
+
+// A staging region: two slots, each holding one image per rank.
+struct Region {
+  uint64_t base;        // byte offset of slot 0 from the workspace base
+  uint64_t slot_bytes;  // bytes between slot 0 and slot 1
+  uint64_t rank_bytes;  // bytes between consecutive rank images
+};
+
+// Everything a kernel launch needs; passed by value (captured by graphs).
+struct RunParams {
+  char* ws;                       // workspace base
+  const uint16_t* in[kMaxRanks];  // rank inputs (stage / late producers)
+  uint16_t* out[kMaxRanks];       // rank outputs
+  int nranks;
+  int enc;
+  int reset_mode;                 // COLL_RESET_*
+  int ctas_per_rank;              // fused path: CTAs bound to each rank
+  uint64_t timeout_ns;
+  Region P;                       // rank images written by stage
+  Region AG;                      // reduced partitions (twoshot)
+  const StageItem* sitems;        // grouped by rank: [sbeg[r], sbeg[r+1])
+  const Item* items1;             // phase 1, grouped by dst rank
+  const Item* items2;             // phase 2 (twoshot), grouped by dst rank
+  uint32_t* counters;
+  int sbeg[kMaxRanks + 1];
+  int beg1[kMaxRanks + 1];
+  int beg2[kMaxRanks + 1];
+  // Segments of a rank image in region P (identical for every rank when the
+  // input layout is scattered): used by late producers to find the input
+  // elements of an image line.
+  int nseg;
+  uint64_t seg_line0[kMaxRanks];
+  uint64_t seg_elems[kMaxRanks];
+  uint64_t seg_in0[kMaxRanks];
+  int stage_rank;                 // streamed stage of one rank, -1 = all
+  int advance_epoch;              // this launch ends the run
+  // late producers (fault-injection runs)
+  const int64_t* late_order[kMaxRanks];
+  int64_t late_n[kMaxRanks];
+  int late_ctas;                  // extra CTAs at the end of the grid
+  // withheld staging (fault-injection runs)
+  const int64_t* wh_lines;
+  const int32_t* wh_kind;
+  const uint16_t* wh_poison;
+  int64_t wh_n;
+};
+
+}  // namespace coll

@@ -1,0 +1,281 @@
+/*
+ * coll.h -- C ABI of the single-GPU collective datapath for GB300 (sm_103a).
+ *
+ * What it computes.  N emulated ranks live in one GPU's HBM.  Each rank's
+ * bf16 buffer is staged as self-synchronizing lines that carry their own
+ * readiness evidence (a flag or sequence word equal to the current epoch);
+ * consumers poll the lines they need, reject stale ones, unpack them, and
+ * either copy them into the output layout or fold the N contributions in
+ * fixed rank order (fp32 accumulate, one rounding to bf16).  A collective is
+ * named by (input layout, output layout, copy-or-reduce), as in
+ *   "Purlin: Separating Orchestration from the Datapath of Collectives",
+ *   §3.1 Listing 1 (collective declarations) and Figure 4;
+ * staging and consumption follow its Stage-Notify-Consume protocol (§3.2,
+ * Listing 2), with the notification carried inside the data as in its
+ * latency path (§3.2 "Specializing for latency") and in
+ *   "flash-comm: Self-Synchronizing Collective Communication for LLM
+ *   Decoding", §3.1 (self-synchronizing transfers, sequence-number
+ *   readiness), §3.3 (rank-order reduction), §4.2 (device-side call counter
+ *   selects the buffer slot).
+ *
+ * Supported (in, out, op) triples and the meaning of `count` (always the
+ * element count of the scattered buffer of the collective, the per-rank size
+ * convention of Purlin §5 "Microbenchmarks"):
+ *   (SCATTERED,   SCATTERED,   REDUCE)  all-reduce      in = out = count
+ *   (SCATTERED,   PACKED,      REDUCE)  reduce-scatter  in = count, out = len(r)
+ *   (PACKED,      SCATTERED,   COPY)    all-gather      in = len(p), out = count
+ *   (SCATTERED,   TRANSPOSED,  COPY)    all-to-all      in = out = count
+ *   (SCATTERED_V, TRANSPOSED_V,COPY)    MoE dispatch    (rows routed by top-k)
+ * Partition r of a scattered buffer covers [r*M, min(count, (r+1)*M)) with
+ * M = roundup(ceil(count / nranks), 8) elements (equal partitions when
+ * 8*nranks divides count).  Every other triple returns COLL_ERR_UNSUPPORTED.
+ *
+ * Ownership.  The caller owns every device buffer: inputs, outputs and the
+ * workspace (obtain its size from coll_workspace_bytes, allocate it however
+ * it likes, hand it over with coll_bind).  The library allocates no device
+ * memory and frees nothing of the caller's.  A spec holds host state only;
+ * it is not thread-safe and must be used from one stream at a time.
+ *
+ * Asynchrony.  coll_bind, coll_stage, coll_run and coll_set_routing only
+ * enqueue work on the given stream and may be captured in a CUDA graph: the
+ * epoch that selects the staging slot and the readiness value lives in the
+ * workspace, on the device, and advances on the device.
+ *
+ * Errors.  Host-side argument errors return a status immediately and enqueue
+ * nothing.  Device-side errors (a wait that exceeded its time bound) are
+ * latched in the workspace; coll_query_status reports and clears them.
+ * Kernels never trap and never wait without a bound.
+ *
+ * Streams are passed as `coll_stream_t` (a cudaStream_t; NULL = the legacy
+ * default stream).
+ */
+#ifndef COLL_H
+#define COLL_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define COLL_VERSION 1
+#define COLL_MAX_RANKS 8
+
+typedef void *coll_stream_t;
+
+/* Layouts of Purlin §3.1: packed = one contiguous contribution; scattered =
+ * rank-indexed contiguous partitions; transposed = partition r of every
+ * source, in source-rank order.  _V variants take sizes at runtime. */
+typedef enum {
+    COLL_PACKED = 0,
+    COLL_SCATTERED = 1,
+    COLL_TRANSPOSED = 2,
+    COLL_PACKED_V = 3,
+    COLL_SCATTERED_V = 4,
+    COLL_TRANSPOSED_V = 5
+} coll_layout_t;
+
+/* Consume operation of Purlin Listing 1: copy into distinct output regions,
+ * or reduce corresponding elements. */
+typedef enum { COLL_COPY = 0, COLL_REDUCE = 1 } coll_op_t;
+
+typedef enum { COLL_BF16 = 0 } coll_dtype_t;
+
+typedef enum {
+    COLL_OK = 0,
+    COLL_ERR_INVALID = 1,     /* bad argument (null pointer, rank range...) */
+    COLL_ERR_UNSUPPORTED = 2, /* triple, dtype, rank count or option */
+    COLL_ERR_ALIGN = 3,       /* pointer or count not 16-byte aligned */
+    COLL_ERR_NOMEM = 4,       /* bound workspace smaller than required */
+    COLL_ERR_CUDA = 5,        /* a CUDA runtime call failed */
+    COLL_ERR_TIMEOUT = 6,     /* a device wait exceeded its bound */
+    COLL_ERR_STATE = 7        /* call out of sequence (e.g. run before bind) */
+} coll_status_t;
+
+/* Readiness encodings.
+ * COLL_LL8: 8-byte line = 4 bytes of data (two bf16) + 4-byte flag = the
+ *   epoch's low 32 bits; two lines per 16-byte store.  Purlin §3.2 packet,
+ *   flash-comm §4.3 sequence-numbered packet.
+ * COLL_LL128: 128-byte line = 120 bytes of data (60 bf16) + 8-byte sequence
+ *   number = the epoch (bytes 120..127).  flash-comm §3.1 sequence-number
+ *   readiness, at 128-byte granularity. */
+enum { COLL_LL8 = 0, COLL_LL128 = 1 };
+
+/* All-reduce algorithm: oneshot (every rank folds all N inputs), twoshot
+ * (reduce-scatter to an owner per partition, which publishes its reduced
+ * partition, then all-gather).  Purlin §3.1 compose<reduceScatter,
+ * allGather>; SiFAR §3.1; flash-comm §4.3 (one-hop / sharded two-hop). */
+enum { COLL_ALGO_AUTO = 0, COLL_ONESHOT = 1, COLL_TWOSHOT = 2 };
+
+/* Flag re-arm (LL8 only; LL128 lines need none): after every reader of a
+ * line consumed it, its flag word is set back to 0 -- by the last reader
+ * (FUSED), by a separate kernel at the end of the run (KERNEL), or never
+ * (NONE).  flash-comm §3.1 / Table 2 (checking and re-arming). */
+enum { COLL_RESET_FUSED = 0, COLL_RESET_KERNEL = 1, COLL_RESET_NONE = 2 };
+
+/* Launch path: FUSED = stage and consume inside one cooperative kernel
+ * (all CTAs co-resident; a CTA serves one emulated rank); STREAMED =
+ * separate stage and consume kernels ordered by the stream.  AUTO picks
+ * FUSED up to 64 KiB per rank. */
+enum { COLL_PATH_AUTO = 0, COLL_PATH_FUSED = 1, COLL_PATH_STREAMED = 2 };
+
+typedef struct {
+    int encoding;        /* COLL_LL8 | COLL_LL128 (default LL8) */
+    int algorithm;       /* COLL_ALGO_AUTO | COLL_ONESHOT | COLL_TWOSHOT */
+    int reset_mode;      /* COLL_RESET_* (default FUSED) */
+    int path;            /* COLL_PATH_* (default AUTO) */
+    int ctas;            /* CTAs of the consume grid, 0 = auto */
+    int tile_lines;      /* lines per work item, 0 = auto */
+    uint64_t timeout_ns; /* bound on every device wait, 0 = 200 ms */
+    /* MoE dispatch (SCATTERED_V -> TRANSPOSED_V) only: */
+    int tokens;          /* rows per source rank */
+    int hidden;          /* bf16 elements per row */
+    int topk;            /* experts per token */
+    int experts;         /* total experts, a multiple of nranks */
+} coll_options_t;
+
+typedef struct coll_spec coll_spec_t;
+
+/* Fill *opt with the defaults above. */
+void coll_options_default(coll_options_t *opt);
+
+/* Validate a collective and derive its schedule (host only, no CUDA call).
+ * Purlin §3.1 Listing 1: the triple names the collective; §3.2 Listing 2:
+ * the layouts decide who notifies whom and whether consumers copy or reduce.
+ * nranks in [1, 8]; count % 8 == 0 (16-byte length alignment, flash-comm
+ * §4.1 admission); count may be 0 (an empty call still advances the epoch,
+ * flash-comm §4.2).  For MoE dispatch `count` is ignored and tokens, hidden
+ * (a multiple of 8), topk and experts come from *opt.
+ * Returns COLL_OK and a new spec in *spec, or an error and *spec = NULL. */
+coll_status_t coll_spec_create(coll_layout_t in_layout, coll_layout_t out_layout,
+                               coll_op_t op, coll_dtype_t dtype, int nranks,
+                               size_t count, const coll_options_t *opt,
+                               coll_spec_t **spec);
+
+/* Bytes of device workspace the spec needs (header, work lists, reader
+ * counters, two staging slots per rank, and for twoshot the two slots of the
+ * reduced-partition region).  Purlin §4.1: two staging buffers alternate. */
+coll_status_t coll_workspace_bytes(const coll_spec_t *spec, size_t *bytes);
+
+/* Element counts of rank `rank`'s input and output buffers. */
+coll_status_t coll_buffer_elems(const coll_spec_t *spec, int rank,
+                                size_t *in_elems, size_t *out_elems);
+
+/* Hand the caller-allocated workspace (device memory, 256-byte aligned) to
+ * the spec and initialise it on `stream`: every readiness word = 0, epoch =
+ * 1, status clear, work lists uploaded.  Purlin §4 "Initialization": buffers
+ * are given once and reused for every call.  COLL_ERR_NOMEM if bytes is
+ * smaller than coll_workspace_bytes. */
+coll_status_t coll_bind(coll_spec_t *spec, void *dev_workspace, size_t bytes,
+                        coll_stream_t stream);
+
+/* MoE dispatch only: give source rank `rank`'s routing, dev_topk[tokens*topk]
+ * (int32 expert ids, distinct per token).  Counting, the prefix sums and the
+ * row placement run on the device at the next coll_stage / coll_run. */
+coll_status_t coll_set_routing(coll_spec_t *spec, int rank,
+                               const int32_t *dev_topk, coll_stream_t stream);
+
+/* Stage rank `rank`'s input for the current epoch e: encode it as lines with
+ * readiness value e into staging slot e & 1 of that rank.  The store of a
+ * line is its notification (no separate notify step): Purlin §3.2 latency
+ * path, flash-comm §3.1.  All ranks must be staged before coll_run(ins=NULL)
+ * of the same epoch, in stream order. */
+coll_status_t coll_stage(coll_spec_t *spec, int rank, const void *dev_in,
+                         coll_stream_t stream);
+
+/* Run the collective for the current epoch, then advance the epoch.
+ * dev_ins == NULL: every rank was staged by coll_stage; the consume kernels
+ * validate and consume.  dev_ins != NULL (nranks input pointers): staging is
+ * done here too -- inside the same cooperative kernel on the FUSED path.
+ * dev_outs: nranks output pointers (16-byte aligned).  Consumers reduce in
+ * rank order 0..N-1 whatever order lines become ready in (flash-comm §3.3). */
+coll_status_t coll_run(coll_spec_t *spec, const void *const *dev_ins,
+                       void *const *dev_outs, coll_stream_t stream);
+
+/* End to end from host memory: copy each rank's input from (pinned) host
+ * memory into dev_ins[r], run the collective, copy each output back into
+ * host_outs[r].  One cudaMemcpyAsync per buffer, all on `stream`. */
+coll_status_t coll_run_host(coll_spec_t *spec, const void *const *host_ins,
+                            void *const *dev_ins, void *const *dev_outs,
+                            void *const *host_outs, coll_stream_t stream);
+
+/* MoE dispatch only: copy counts[dest][local expert][source] (int32,
+ * nranks * experts) and, after it, rows per destination (nranks int32) of
+ * the last run into dev_counts. */
+coll_status_t coll_get_counts(const coll_spec_t *spec, int32_t *dev_counts,
+                              coll_stream_t stream);
+
+/* Synchronize `stream`, report the latched device error (COLL_OK if none)
+ * with the rank and line it concerns, and clear it. */
+coll_status_t coll_query_status(coll_spec_t *spec, coll_stream_t stream,
+                                int *code, int *rank, int64_t *line);
+
+/* Synchronize `stream` and read the device epoch. */
+coll_status_t coll_get_epoch(coll_spec_t *spec, coll_stream_t stream,
+                             uint64_t *epoch);
+
+/* Staging geometry, for inspection: region 0 = the rank images written by
+ * coll_stage, region 1 = the reduced partitions published by twoshot owners.
+ * Returns the byte offset (from the workspace base) of segment `seg` of rank
+ * `rank` in slot `slot`, its line count and the line size in bytes. */
+coll_status_t coll_staging_layout(const coll_spec_t *spec, int region, int slot,
+                                  int rank, int seg, uint64_t *byte_offset,
+                                  uint64_t *lines, int *line_bytes);
+
+/* Fault-injection support for the stale-line tests (host-made failures, no
+ * GPU fault).  coll_stage_withheld stages rank `rank` like coll_stage but
+ * leaves the listed lines stale: their readiness word holds the previous
+ * epoch (kind 0), the slot's previous occupant e-2 (kind 1) or zero
+ * (kind 2), and their payload a poison pattern.  Line indices are global
+ * line numbers of the rank image (segments in order, as given by
+ * coll_staging_layout).  All arrays are device arrays of n entries. */
+coll_status_t coll_stage_withheld(coll_spec_t *spec, int rank, const void *dev_in,
+                                  const int64_t *dev_lines, const int32_t *dev_kind,
+                                  const uint16_t *dev_poison, int64_t n,
+                                  coll_stream_t stream);
+
+/* Run (inputs already staged, some lines withheld) with late producers in
+ * the same cooperative launch: for each rank r, dev_order[r] lists its
+ * withheld lines in the order a producer CTA of rank r publishes them after
+ * the consumers have started polling; n_late[r] (host array) is the count.
+ * dev_ins gives the producers the data to publish. */
+coll_status_t coll_run_late(coll_spec_t *spec, const void *const *dev_ins,
+                            void *const *dev_outs,
+                            const int64_t *const *dev_order,
+                            const int64_t *n_late, coll_stream_t stream);
+
+/* Number of stale lines the consumers of the last runs observed and rejected
+ * (a diagnostic counter, reset by coll_bind). */
+coll_status_t coll_get_rejections(coll_spec_t *spec, coll_stream_t stream,
+                                  uint64_t *rejections);
+
+/* Inspection of the derived schedule (host only, no CUDA call).  which = 0:
+ * staging items, 1: first consume phase, 2: second consume phase (twoshot
+ * all-gather).  Each item is written as 10 int64 values:
+ *   consume: kind (0 fold, 1 copy), flags (1 publish, 2 sole-reader re-arm,
+ *            4 counted re-arm), dst rank, src rank, readers, lines, elements,
+ *            first source line, output offset (element, or line when
+ *            publishing), counter index;
+ *   staging: rank, 0, 0, 0, 0, lines, elements, first image line, first
+ *            input element, 0.
+ * *n receives the number of items; at most cap items are written. */
+coll_status_t coll_debug_items(const coll_spec_t *spec, int which, int64_t *buf,
+                               size_t cap, size_t *n);
+
+/* Summary of the derived plan: all-reduce algorithm (COLL_ONESHOT /
+ * COLL_TWOSHOT, 0 for other collectives), launch path used when inputs are
+ * given to coll_run (COLL_PATH_FUSED / COLL_PATH_STREAMED), CTAs per rank of
+ * the fused path, and the encoding. */
+coll_status_t coll_debug_plan(const coll_spec_t *spec, int *algorithm, int *path,
+                              int *ctas_per_rank, int *encoding);
+
+/* Release the spec's host state (never the caller's device memory). */
+coll_status_t coll_destroy(coll_spec_t *spec);
+
+const char *coll_status_string(coll_status_t status);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* COLL_H */

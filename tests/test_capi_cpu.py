@@ -1,0 +1,182 @@
+"""CPU checks of the C ABI: the library loads, exports what include/coll.h
+declares, validates arguments, and derives work lists that -- interpreted
+line by line on the CPU with the oracle's encoders and fold -- produce exactly
+the oracle's collective results.  No GPU, no kernel launch."""
+from __future__ import annotations
+
+import os
+import re
+
+import numpy as np
+import pytest
+
+import oracle
+import synth
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def cd():
+    import importlib.util
+
+    spec = importlib.util.spec_from_file_location(
+        "_coll_build", os.path.join(ROOT, "collective_datapath_gb300", "_build.py"))
+    b = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(b)
+    b.build()
+    import collective_datapath_gb300 as m
+
+    return m
+
+
+def declared_functions() -> list[str]:
+    text = open(os.path.join(ROOT, "include", "coll.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(coll_[a-z_]+)\s*\(", text)))
+
+
+def test_library_exports_every_declared_symbol(cd):
+    import ctypes
+
+    lib = ctypes.CDLL(cd.library_path())
+    names = declared_functions()
+    assert len(names) >= 19
+    for name in names:
+        assert hasattr(lib, name), f"{name} declared in coll.h but not exported"
+    assert sorted(cd.EXPORTS) == names
+
+
+def test_argument_validation(cd):
+    with pytest.raises(cd.CollError) as e:
+        cd.coll_spec_create(cd.COLL_PACKED, cd.COLL_PACKED, cd.COLL_REDUCE, 8, 64)
+    assert e.value.status == cd.COLL_ERR_UNSUPPORTED
+    with pytest.raises(cd.CollError) as e:
+        cd.coll_spec_create(*cd.ALLREDUCE, 8, 12)          # not 16-byte aligned
+    assert e.value.status == cd.COLL_ERR_ALIGN
+    for bad_n in (0, 9):
+        with pytest.raises(cd.CollError) as e:
+            cd.coll_spec_create(*cd.ALLREDUCE, bad_n, 64)
+        assert e.value.status == cd.COLL_ERR_UNSUPPORTED
+    with pytest.raises(cd.CollError) as e:
+        cd.coll_spec_create(*cd.ALLTOALL, 8, 24)           # unequal partitions
+    assert e.value.status == cd.COLL_ERR_ALIGN
+    with pytest.raises(cd.CollError) as e:
+        cd.coll_spec_create(*cd.ALLREDUCE, 8, 64, encoding=7)
+    assert e.value.status == cd.COLL_ERR_UNSUPPORTED
+    s = cd.coll_spec_create(*cd.ALLREDUCE, 8, 64)
+    with pytest.raises(cd.CollError) as e:                 # not bound yet
+        cd.coll_stage(s, 0, 0x1000, stream=0)
+    assert e.value.status == cd.COLL_ERR_STATE
+    assert cd.coll_workspace_bytes(s) > 0
+    cd.coll_destroy(s)
+
+
+# ---- CPU interpretation of the derived schedule --------------------------------
+
+def _encode(enc, x, epoch):
+    return oracle.ll8_encode(x, epoch) if enc == 0 else \
+        oracle.ll128_encode(x, epoch).reshape(-1, 128)
+
+
+def _decode(enc, lines, elems, epoch):
+    out, rej = (oracle.ll8_decode(lines, elems, epoch) if enc == 0 else
+                oracle.ll128_decode(np.ascontiguousarray(lines).ravel(), elems, epoch))
+    assert rej == 0
+    return out
+
+
+def interpret(cd, spec, enc, n, ins, epoch=5):
+    """Run the derived items on the CPU: stage, phase 1, phase 2."""
+    st = cd.coll_debug_items(spec, 0)
+    p1 = cd.coll_debug_items(spec, 1)
+    p2 = cd.coll_debug_items(spec, 2)
+    width = 1 if enc == 0 else 128
+    dt = np.uint64 if enc == 0 else np.uint8
+    img_lines = int(max([r[7] + r[5] for r in st] + [4]))
+    ag_lines = int(max([r[8] + r[5] for r in p1 if r[1] & 1] + [4]))
+    P = [np.zeros((img_lines, width) if enc else img_lines, dtype=dt) for _ in range(n)]
+    AG = [np.zeros((ag_lines, width) if enc else ag_lines, dtype=dt) for _ in range(n)]
+    for rank, _, _, _, _, nl, ne, dst_line, in_elem, _ in st:
+        assert dst_line % 4 == 0
+        P[rank][dst_line:dst_line + nl] = _encode(enc, ins[rank][in_elem:in_elem + ne], epoch)
+    outs = [np.full(cd.coll_buffer_elems(spec, r)[1], 0xDEAD, dtype=np.uint16)
+            for r in range(n)]
+    written = [np.zeros(o.size, dtype=np.int32) for o in outs]
+
+    def run(items, images):
+        for kind, flags, dst, src, readers, nl, ne, sl, off, ctr in items:
+            assert sl % 4 == 0
+            if kind == 0:
+                xs = [_decode(enc, images[q][sl:sl + nl], ne, epoch) for q in range(n)]
+                res = oracle.allreduce(xs)[0]
+            else:
+                res = _decode(enc, images[src][sl:sl + nl], ne, epoch)
+            if flags & 1:
+                AG[dst][off:off + nl] = _encode(enc, res, epoch)
+            else:
+                outs[dst][off:off + ne] = res
+                written[dst][off:off + ne] += 1
+
+    run(p1, P)
+    run(p2, AG)
+    for w in written:
+        assert np.all(w == 1), "every output element written exactly once"
+    return outs
+
+
+CASES = [
+    # (triple name, n, count, enc, algorithm, path)
+    ("ALLREDUCE", 2, 512, 0, 1, 1),
+    ("ALLREDUCE", 8, 8 * 4096, 0, 1, 1),
+    ("ALLREDUCE", 8, 8 * 4096, 0, 2, 1),
+    ("ALLREDUCE", 8, 8 * 4096, 1, 2, 2),
+    ("ALLREDUCE", 8, 16 * 7168, 1, 1, 1),
+    ("ALLREDUCE", 3, 1000, 1, 2, 2),        # ragged partitions
+    ("ALLREDUCE", 8, 24, 0, 2, 1),          # empty partitions
+    ("ALLREDUCE", 1, 64, 0, 1, 1),
+    ("REDUCE_SCATTER", 8, 8 * 3000, 1, 0, 2),
+    ("REDUCE_SCATTER", 5, 5 * 8 * 7 + 16, 0, 0, 1),
+    ("ALLGATHER", 8, 8 * 2048, 0, 0, 2),
+    ("ALLGATHER", 4, 4 * 104 + 8, 1, 0, 1),
+    ("ALLTOALL", 8, 8 * 960, 1, 0, 2),
+    ("ALLTOALL", 4, 4 * 64, 0, 0, 1),
+]
+
+
+@pytest.mark.parametrize("name,n,count,enc,algo,path", CASES)
+def test_derived_schedule_computes_the_oracle_result(cd, name, n, count, enc, algo, path):
+    triple = getattr(cd, name)
+    spec = cd.coll_spec_create(*triple, n, count, encoding=enc, algorithm=algo, path=path)
+    try:
+        ins = [synth.normal_bf16(3, cd.coll_buffer_elems(spec, r)[0], n, count, r)
+               for r in range(n)]
+        got = interpret(cd, spec, enc, n, ins)
+        if name == "ALLREDUCE":
+            want = oracle.allreduce(ins)
+        elif name == "REDUCE_SCATTER":
+            want = oracle.reduce_scatter(ins)
+        elif name == "ALLGATHER":
+            want = oracle.all_gather(ins, count)
+        else:
+            want = oracle.all_to_all(ins)
+        for r in range(n):
+            assert np.array_equal(got[r], want[r]), f"rank {r}"
+    finally:
+        cd.coll_destroy(spec)
+
+
+def test_reset_counters_match_reader_counts(cd):
+    """Counted re-arm: every counter is shared by exactly `readers` items."""
+    for triple, algo in ((cd.ALLREDUCE, 1), (cd.ALLREDUCE, 2), (cd.ALLGATHER, 0)):
+        spec = cd.coll_spec_create(*triple, 8, 8 * 1024, algorithm=algo, path=1)
+        for which in (1, 2):
+            items = cd.coll_debug_items(spec, which)
+            counted = items[(items[:, 1] & 4) != 0]
+            if counted.size == 0:
+                continue
+            ids, uses = np.unique(counted[:, 9], return_counts=True)
+            for cid, u in zip(ids, uses):
+                readers = counted[counted[:, 9] == cid][:, 4]
+                assert np.all(readers == u)
+        cd.coll_destroy(spec)

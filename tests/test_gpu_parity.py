@@ -1,0 +1,221 @@
+"""GPU parity: every collective, both encodings, both launch paths, against
+the CPU oracle, bit for bit (tolerance 0 ulp: the fold order is fixed and the
+accumulation is fp32 with one rounding)."""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+
+import oracle
+import synth
+from tests.gpu_util import buffers, empty_dev, from_dev, make, read_lines, to_dev
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def cd():
+    import torch
+
+    if not torch.cuda.is_available():
+        pytest.skip("no GPU")
+    import collective_datapath_gb300 as m
+
+    return m
+
+
+def expected(cd, triple, ins, count):
+    if triple == cd.ALLREDUCE:
+        return oracle.allreduce(ins)
+    if triple == cd.REDUCE_SCATTER:
+        return oracle.reduce_scatter(ins)
+    if triple == cd.ALLGATHER:
+        return oracle.all_gather(ins, count)
+    return oracle.all_to_all(ins)
+
+
+def check(coll, outs, want, n):
+    import collective_datapath_gb300 as cd
+
+    code, rank, line = coll.status()
+    assert code == cd.COLL_OK, f"device status {code} rank {rank} line {line}"
+    for r in range(n):
+        got = from_dev(outs[r])[:want[r].size]
+        if not np.array_equal(got, want[r]):
+            bad = np.flatnonzero(got != want[r])
+            raise AssertionError(f"rank {r}: {bad.size} mismatches, first at {bad[0]}: "
+                                 f"got {got[bad[0]]:#06x} want {want[r][bad[0]]:#06x}")
+
+
+def test_config1_oneshot_two_ranks_1kib(cd):
+    """2 ranks x 512 bf16 uniform[-1,1] seed 0, LL8, oneshot, one epoch."""
+    n, count = 2, 512
+    coll = make(cd, cd.ALLREDUCE, n, count, encoding=cd.COLL_LL8,
+                algorithm=cd.COLL_ONESHOT, path=cd.COLL_PATH_FUSED)
+    xs = [synth.uniform_bf16(0, count, -1.0, 1.0, 1, p) for p in range(n)]
+    ins = [to_dev(x) for x in xs]
+    outs = [empty_dev(count) for _ in range(n)]
+    coll.run(ins, outs)
+    check(coll, outs, oracle.allreduce(xs), n)
+    assert coll.epoch() == 2
+
+
+@pytest.mark.parametrize("algo", [1, 2])
+@pytest.mark.parametrize("path", [1, 2])
+@pytest.mark.parametrize("T", [1, 2, 4, 8, 16, 32, 64, 128])
+def test_config2_decode_allreduce(cd, T, path, algo):
+    """8 ranks x [T x 4096] normal(0,1), LL8, oneshot and twoshot; all 8
+    output copies identical and equal to the oracle."""
+    n, count = 8, T * 4096
+    coll = make(cd, cd.ALLREDUCE, n, count, encoding=cd.COLL_LL8, algorithm=algo,
+                path=path)
+    xs, ins, outs = buffers(coll, n, seed=2, tag=T)
+    coll.run(ins, outs)
+    want = oracle.allreduce(xs)
+    check(coll, outs, want, n)
+    first = from_dev(outs[0])
+    for r in range(1, n):
+        assert np.array_equal(from_dev(outs[r]), first)
+
+
+CASES = [
+    ("ALLREDUCE", 8, 8 * 1000, 1, 1), ("ALLREDUCE", 8, 8 * 1000, 1, 2),
+    ("ALLREDUCE", 3, 1000, 0, 1), ("ALLREDUCE", 3, 1000, 1, 2),
+    ("ALLREDUCE", 8, 24, 0, 1), ("ALLREDUCE", 1, 4096, 0, 2), ("ALLREDUCE", 1, 4096, 1, 1),
+    ("REDUCE_SCATTER", 8, 8 * 3000, 0, 1), ("REDUCE_SCATTER", 8, 8 * 3000, 1, 2),
+    ("REDUCE_SCATTER", 5, 5 * 56 + 16, 1, 1),
+    ("ALLGATHER", 8, 8 * 2048, 0, 2), ("ALLGATHER", 8, 8 * 2048, 1, 1),
+    ("ALLGATHER", 4, 4 * 104 + 8, 1, 2),
+    ("ALLTOALL", 8, 8 * 960, 1, 2), ("ALLTOALL", 8, 8 * 960, 0, 1), ("ALLTOALL", 4, 256, 1, 1),
+]
+
+
+@pytest.mark.parametrize("name,n,count,enc,path", CASES)
+def test_layout_collectives(cd, name, n, count, enc, path):
+    triple = getattr(cd, name)
+    for algo in ((1, 2) if name == "ALLREDUCE" else (0,)):
+        coll = make(cd, triple, n, count, encoding=enc, path=path, algorithm=algo)
+        xs, ins, outs = buffers(coll, n, seed=4, dist="bits" if name != "REDUCE_SCATTER" and
+                                name != "ALLREDUCE" else "normal", tag=count)
+        coll.run(ins, outs)
+        check(coll, outs, expected(cd, triple, xs, count), n)
+
+
+@pytest.mark.parametrize("enc", [0, 1])
+def test_staged_lines_match_the_oracle_encoding(cd, enc):
+    """coll_stage writes exactly the oracle's LL8 / LL128 lines (epoch 1,
+    slot 1), one segment per partition of the scattered input."""
+    n, count = 4, 4 * 1000
+    coll = make(cd, cd.ALLREDUCE, n, count, encoding=enc, path=cd.COLL_PATH_STREAMED)
+    xs, ins, outs = buffers(coll, n, seed=5, dist="bits")
+    for r in range(n):
+        coll.stage(r, ins[r])
+    import torch
+
+    torch.cuda.synchronize()
+    for r in range(n):
+        for k in range(n):
+            raw, lines, lb = read_lines(coll, 0, 1, r, k)
+            b, ln = oracle.shard_begin(count, n, k), oracle.shard_len(count, n, k)
+            seg = xs[r][b:b + ln]
+            want = (oracle.ll8_encode(seg, 1).view(np.uint8) if enc == 0
+                    else oracle.ll128_encode(seg, 1))
+            assert np.array_equal(raw, want), f"rank {r} segment {k}"
+    coll.run(None, outs)
+    check(coll, outs, oracle.allreduce(xs), n)
+
+
+@pytest.mark.parametrize("algo", [1, 2])
+@pytest.mark.parametrize("reset", [0, 1])
+@pytest.mark.parametrize("path", [1, 2])
+def test_flags_rearmed_after_run(cd, algo, reset, path):
+    """LL8: after a run every flag word of the slot it used is 0."""
+    n, count = 8, 8 * 512
+    coll = make(cd, cd.ALLREDUCE, n, count, encoding=0, algorithm=algo,
+                reset_mode=reset, path=path)
+    xs, ins, outs = buffers(coll, n, seed=6)
+    coll.run(ins, outs)
+    check(coll, outs, oracle.allreduce(xs), n)
+    regions = (0, 1) if algo == 2 else (0,)
+    for region in regions:
+        for r in range(n):
+            for k in range(n if region == 0 else 1):
+                raw, lines, lb = read_lines(coll, region, 1, r, k)
+                flags = raw.view(np.uint32)[1::2]
+                assert np.all(flags == 0), f"region {region} rank {r} seg {k}"
+
+
+@pytest.mark.parametrize("enc", [0, 1])
+@pytest.mark.parametrize("path", [1, 2])
+def test_consecutive_epochs_alternate_slots(cd, enc, path):
+    n, count = 8, 8 * 2000
+    coll = make(cd, cd.ALLREDUCE, n, count, encoding=enc, path=path)
+    _, ins, outs = buffers(coll, n, seed=7)
+    for e in range(1, 9):
+        xs = [synth.normal_bf16(70 + e, count, r) for r in range(n)]
+        for r in range(n):
+            ins[r].copy_(to_dev(xs[r]))
+        coll.run(ins, outs)
+        check(coll, outs, oracle.allreduce(xs), n)
+        assert coll.epoch() == e + 1
+
+
+def test_empty_collective_advances_the_epoch(cd):
+    coll = make(cd, cd.ALLREDUCE, 8, 0)
+    outs = [empty_dev(0) for _ in range(8)]
+    coll.run(None, outs)
+    coll.run([empty_dev(0) for _ in range(8)], outs)
+    code, _, _ = coll.status()
+    assert code == cd.COLL_OK and coll.epoch() == 3
+
+
+@pytest.mark.parametrize("enc", [0, 1])
+def test_unpublished_line_times_out_with_status(cd, enc):
+    """A line that never gets its readiness value: the consumer gives up
+    after the bound, latches COLL_ERR_TIMEOUT with the rank, and the context
+    stays usable."""
+    import torch
+
+    n, count = 4, 4 * 480
+    coll = make(cd, cd.ALLREDUCE, n, count, encoding=enc, path=cd.COLL_PATH_STREAMED,
+                algorithm=cd.COLL_ONESHOT, timeout_ns=2_000_000)
+    xs, ins, outs = buffers(coll, n, seed=8)
+    lines = torch.tensor([3], dtype=torch.int64, device="cuda")
+    kind = torch.tensor([0], dtype=torch.int32, device="cuda")
+    poison = torch.tensor([0x4880], dtype=torch.int16, device="cuda")
+    for r in range(n):
+        if r == 2:
+            cd.coll_stage_withheld(coll.spec, r, ins[r], lines, kind, poison)
+        else:
+            coll.stage(r, ins[r])
+    coll.run(None, outs)
+    code, rank, line = coll.status()
+    assert code == cd.COLL_ERR_TIMEOUT and rank == 2 and line >= 0
+    # the next epoch works
+    coll.run(ins, outs)
+    check(coll, outs, oracle.allreduce(xs), n)
+
+
+@pytest.mark.parametrize("enc", [0, 1])
+def test_graph_replay_advances_epoch_on_device(cd, enc):
+    """coll_run captured once in a CUDA graph: each replay uses the next
+    epoch and slot (the epoch lives on the device)."""
+    import torch
+
+    n, count = 8, 8 * 512
+    coll = make(cd, cd.ALLREDUCE, n, count, encoding=enc, path=cd.COLL_PATH_FUSED)
+    _, ins, outs = buffers(coll, n, seed=9)
+    s = torch.cuda.Stream()
+    g = torch.cuda.CUDAGraph()
+    torch.cuda.synchronize()
+    with torch.cuda.graph(g, stream=s):
+        coll.run(ins, outs, stream=s)
+    for rep in range(4):
+        xs = [synth.normal_bf16(90 + rep, count, r) for r in range(n)]
+        for r in range(n):
+            ins[r].copy_(to_dev(xs[r]))
+        torch.cuda.synchronize()
+        g.replay()
+        torch.cuda.synchronize()
+        check(coll, outs, oracle.allreduce(xs), n)
+    assert coll.epoch() == 5
