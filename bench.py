@@ -1,0 +1,490 @@
+#!/usr/bin/env python
+"""Benchmark of the single-GPU collective datapath.
+
+Default workload (one step = one all-reduce through the whole datapath:
+stage as LL128 lines, validate + fold the partitions at their owners,
+publish, validate + unpack at every rank):
+    8 emulated ranks, 256 MiB of bf16 per rank (uniform[-4, 4], seeded),
+    LL128 sequence-number lines, twoshot, stream-ordered kernels.
+The inputs (2 GiB) and staging (4.8 GiB) exceed the 126 MiB L2, so no L2
+flush is needed between steps.
+
+value = algorithmic bytes of one all-reduce / device time per step (GB/s),
+summed over replicas for --gpus N (one independent replica per GPU: the
+single-GPU emulation does not shard across GPUs).
+
+The same JSON line carries the roofline of the dominant kernel (per-launch
+CUDA events around each kernel of every timed step), the end-to-end number
+through coll_run_host (pinned host buffers, copies in the timed region), the
+small-message latency sweep (8 ranks x [T x 4096] bf16, LL8, oneshot and
+twoshot; warm = 128 ops per CUDA graph, cold = L2 flushed before every op),
+reduce-scatter and all-gather at 256 MiB, and the CPU oracle timed on a
+bounded sample.  ``--impl reference`` times the CPU oracle instead.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = ("all-reduce µs/op (1 KB–1 MB) and HBM GB/s vs 8 TB/s peak, "
+          "N=8 emulated ranks")
+N_RANKS = 8
+EPS_LL128 = 128.0 / 120.0
+EPS_LL8 = 2.0
+L2_BYTES = 126.5 * 2**20
+
+
+# ---- algorithmic bytes (per op, whole job of one GPU) ------------------------------
+
+def bytes_allreduce_twoshot(n: int, s: float, eps: float) -> float:
+    """stage NS read + NS*eps write; owners read NS*eps, publish S*eps; every
+    rank reads N*S*eps lines and writes S."""
+    return 2 * n * s + (3 * n + 1) * s * eps
+
+
+def kernel_bytes_allreduce_twoshot(n: int, s: float, eps: float) -> list[float]:
+    return [n * s + n * s * eps,          # stage
+            n * s * eps + s * eps,        # reduce-scatter + publish
+            n * s * eps + n * s]          # all-gather copy
+
+
+def bytes_allreduce_oneshot(n: int, s: float, eps: float) -> float:
+    return 2 * n * s + n * s * eps + n * n * s * eps
+
+
+def bytes_reduce_scatter(n: int, s: float, eps: float) -> float:
+    return (n + 1) * s + 2 * n * s * eps
+
+
+def bytes_all_gather(n: int, s: float, eps: float) -> float:
+    """s = gathered output per rank; every rank contributes s / n."""
+    return (n + 1) * s * (1 + eps)
+
+
+# ---- helpers -----------------------------------------------------------------------
+
+def load_peaks() -> dict:
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return {"hbm_gbs": float(d.get("hbm_gbs", 6800.0)), "source": "measured"}
+    return {"hbm_gbs": 6800.0, "source": "fallback"}
+
+
+class Clocks:
+    """nvidia-smi sampler around the timed region (200 ms period)."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        time.sleep(0.3)
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+
+        def num(v):
+            try:
+                return float(v)
+            except ValueError:
+                return None
+
+        sm = [num(r[1]) for r in rows if num(r[1]) is not None]
+        mx = [num(r[2]) for r in rows if num(r[2]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4)
+                          if r[5 + i].lower().startswith("active")})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def barrier_max(value: float, world: int) -> float:
+    """Max of a per-rank number over ranks (identity for one rank)."""
+    if world <= 1:
+        return value
+    import torch
+    import torch.distributed as dist
+
+    t = torch.tensor([value], dtype=torch.float64,
+                     device="cuda" if dist.get_backend() == "nccl" else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int) -> None:
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.barrier()
+
+
+# ---- CPU baseline (the oracle, as it stands) ----------------------------------------
+
+def cpu_oracle_allreduce(per_rank_mib: int, seed: int = 4) -> dict:
+    import oracle
+    import synth
+
+    count = per_rank_mib * 2**20 // 2
+    xs = [synth.uniform_bf16(seed, count, -4.0, 4.0, 99, r) for r in range(N_RANKS)]
+    t0 = time.perf_counter()
+    oracle.allreduce(xs)
+    dt = time.perf_counter() - t0
+    s = count * 2.0
+    gbs = bytes_allreduce_twoshot(N_RANKS, s, EPS_LL128) / dt / 1e9
+    return {"value": round(gbs, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "seconds": round(dt, 3),
+            "sample": f"all-reduce of {N_RANKS} ranks x {per_rank_mib} MiB bf16 by the "
+                      f"plain C oracle (single thread), one run; GB/s counted with the "
+                      f"same algorithmic bytes as the GPU line"}
+
+
+def run_reference(args) -> int:
+    world, rank, _ = dist_setup()
+    if rank != 0:
+        return 0
+    per_rank_mib = 8
+    times = []
+    for i in range(args.warmup + args.steps):
+        r = cpu_oracle_allreduce(per_rank_mib, seed=100 + i)
+        if i >= args.warmup:
+            times.append(r["seconds"])
+    sec = sum(times) / len(times)
+    s = per_rank_mib * 2**20
+    value = bytes_allreduce_twoshot(N_RANKS, s, EPS_LL128) / sec / 1e9
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(sec * 1e3, 3), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": f"all-reduce, {N_RANKS} emulated ranks, {per_rank_mib} MiB "
+                               f"bf16 per rank per step (a bounded sample of the 256 MiB "
+                               f"workload), CPU oracle",
+                   "parallelism": "replicas"},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1,
+                         "kind": "oracle",
+                         "sample": f"{N_RANKS} ranks x {per_rank_mib} MiB per step"},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line))
+    return 0
+
+
+# ---- GPU measurements ---------------------------------------------------------------
+
+def make_inputs(count: int, seed: int):
+    import torch
+
+    xs = []
+    for r in range(N_RANKS):
+        g = torch.Generator(device="cuda")
+        g.manual_seed(seed * 1000 + r)
+        u = torch.rand(count, generator=g, device="cuda", dtype=torch.float32)
+        xs.append((u * 8.0 - 4.0).to(torch.bfloat16).view(torch.int16))
+    return xs
+
+
+def timed(step, k: int, w: int, stream, world: int) -> float:
+    """ms for k steps after w warm-up steps (CUDA events on `stream`)."""
+    import torch
+
+    for i in range(w):
+        step(i)
+    torch.cuda.synchronize()
+    barrier(world)
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(k):
+        step(i)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    return e0.elapsed_time(e1)
+
+
+def latency_sweep(cd, stream) -> dict:
+    """8 ranks x [T x 4096] bf16, LL8 (config of the decode-time sweep)."""
+    import torch
+
+    out = {}
+    flush = torch.empty(int(2 * L2_BYTES), dtype=torch.uint8, device="cuda")
+    for T in (1, 2, 4, 8, 16, 32, 64, 128):
+        count = T * 4096
+        row = {}
+        for algo, name in ((cd.COLL_ONESHOT, "oneshot"), (cd.COLL_TWOSHOT, "twoshot")):
+            coll = cd.Collective(cd.ALLREDUCE, N_RANKS, count, encoding=cd.COLL_LL8,
+                                 algorithm=algo)
+            ins = make_inputs(count, 7 + T)
+            outs = [torch.empty(count, dtype=torch.int16, device="cuda")
+                    for _ in range(N_RANKS)]
+            with torch.cuda.stream(stream):
+                for _ in range(3):
+                    coll.run(ins, outs, stream)
+                # warm: 128 ops per graph, 1 warm-up replay, 8 timed replays
+                g = torch.cuda.CUDAGraph()
+                stream.synchronize()
+                with torch.cuda.graph(g, stream=stream):
+                    for _ in range(128):
+                        coll.run(ins, outs, stream)
+                g.replay()
+                e0 = torch.cuda.Event(enable_timing=True)
+                e1 = torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                for _ in range(8):
+                    g.replay()
+                e1.record(stream)
+                stream.synchronize()
+                warm = e0.elapsed_time(e1) * 1e3 / 1024
+                # cold: L2 flushed (2x L2 written) before each op
+                evs = []
+                for _ in range(32):
+                    flush.fill_(1)
+                    a = torch.cuda.Event(enable_timing=True)
+                    b = torch.cuda.Event(enable_timing=True)
+                    a.record(stream)
+                    coll.run(ins, outs, stream)
+                    b.record(stream)
+                    evs.append((a, b))
+                stream.synchronize()
+                cold = statistics.median(a.elapsed_time(b) * 1e3 for a, b in evs)
+            st = coll.status(stream)
+            row[name] = {"warm_us": round(warm, 3), "cold_us": round(cold, 3),
+                         "path": "fused" if coll.plan()["path"] == cd.COLL_PATH_FUSED
+                         else "streamed", "status": st[0]}
+            coll.close()
+            del coll, ins, outs, g
+        out[f"T={T}"] = {"bytes_per_rank": count * 2, **row}
+    del flush
+    torch.cuda.empty_cache()
+    return out
+
+
+def bandwidth_row(cd, triple, count_in_out, kind, stream, steps=5) -> dict:
+    import torch
+
+    n = N_RANKS
+    count = count_in_out
+    coll = cd.Collective(triple, n, count, encoding=cd.COLL_LL128,
+                         path=cd.COLL_PATH_STREAMED)
+    ins = make_inputs(max(coll.elems(r)[0] for r in range(n)), 11)
+    ins = [x[:coll.elems(r)[0]] for r, x in enumerate(ins)]
+    outs = [torch.empty(max(coll.elems(r)[1], 8), dtype=torch.int16, device="cuda")
+            for r in range(n)]
+    with torch.cuda.stream(stream):
+        for _ in range(2):
+            coll.run(ins, outs, stream)
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(steps):
+            coll.run(ins, outs, stream)
+        e1.record(stream)
+        stream.synchronize()
+    ms = e0.elapsed_time(e1) / steps
+    s = count * 2.0
+    b = bytes_reduce_scatter(n, s, EPS_LL128) if kind == "rs" else bytes_all_gather(n, s, EPS_LL128)
+    st = coll.status(stream)[0]
+    coll.close()
+    del coll, ins, outs
+    torch.cuda.empty_cache()
+    return {"ms": round(ms, 4), "GB/s": round(b / ms / 1e6, 1), "algorithmic_bytes": b,
+            "status": st}
+
+
+def main() -> int:
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--mib", type=int, default=256, help="per-rank MiB of the main workload")
+    ap.add_argument("--quick", action="store_true", help="skip sweep, extra rows and CPU leg")
+    args = ap.parse_args()
+    if args.impl == "reference":
+        return run_reference(args)
+
+    import torch
+
+    world, rank, local = dist_setup()
+    if world > 1:
+        import torch.distributed as dist
+
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    else:
+        torch.cuda.set_device(0)
+    args.warmup = max(args.warmup, 3)
+    if not os.path.exists(os.path.join(ROOT, "collective_datapath_gb300", "libcoll.so")):
+        import __graft_entry__
+
+        __graft_entry__.build()
+    import collective_datapath_gb300 as cd
+
+    peaks = load_peaks()
+    stream = torch.cuda.Stream()
+    count = args.mib * 2**20 // 2
+    s_bytes = count * 2.0
+    coll = cd.Collective(cd.ALLREDUCE, N_RANKS, count, encoding=cd.COLL_LL128,
+                         algorithm=cd.COLL_TWOSHOT, path=cd.COLL_PATH_STREAMED)
+    ins = make_inputs(count, 4)
+    outs = [torch.empty(count, dtype=torch.int16, device="cuda") for _ in range(N_RANKS)]
+    K, W = args.steps, args.warmup
+    nk = 3
+    events = [[torch.cuda.Event(enable_timing=True) for _ in range(nk + 1)]
+              for _ in range(W + K)]
+    launches = [0]
+
+    def step(i):
+        cd.coll_set_profile_events(coll.spec, events[i % len(events)])
+        coll.run(ins, outs, stream)
+        launches[0] += cd.coll_last_launches(coll.spec)
+
+    clocks = Clocks(local)
+    with torch.cuda.stream(stream):
+        for i in range(W):
+            step(i)
+        torch.cuda.synchronize()
+        launches[0] = 0
+        clocks.start()
+        ms_total = timed(lambda i: step(W + i), K, 0, stream, world)
+        clk = clocks.stop()
+    cd.coll_set_profile_events(coll.spec, [])
+    code = coll.status(stream)[0]
+    if code != cd.COLL_OK:
+        raise RuntimeError(f"device status {code} during the timed steps")
+    ms_step = barrier_max(ms_total / K, world)
+    algo_bytes = bytes_allreduce_twoshot(N_RANKS, s_bytes, EPS_LL128)
+    value = world * algo_bytes / (ms_step * 1e-3) / 1e9
+
+    # per-kernel durations over the timed steps
+    names = ["stage (LL128 encode)", "reduce-scatter fold + publish", "all-gather unpack"]
+    kb = kernel_bytes_allreduce_twoshot(N_RANKS, s_bytes, EPS_LL128)
+    dur = [statistics.mean(events[W + i][k].elapsed_time(events[W + i][k + 1])
+                           for i in range(K)) for k in range(nk)]
+    kernels = [{"name": names[k], "ms": round(dur[k], 4), "bytes": kb[k],
+                "GB/s": round(kb[k] / dur[k] / 1e6, 1)} for k in range(nk)]
+    dom = max(range(nk), key=lambda k: dur[k])
+    achieved = kb[dom] / dur[dom] / 1e6
+    traffic = None
+    prof = os.path.join(ROOT, "profiles", "traffic.json")
+    if os.path.exists(prof):
+        with open(prof) as f:
+            t = json.load(f)
+        key = f"allreduce_twoshot_ll128_{args.mib}mib"
+        traffic = t.get(key, {}).get(["stage", "rs", "ag"][dom])
+
+    line = {
+        "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world,
+        "steps": K, "warmup": W, "ms_per_step": round(ms_step, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": f"all-reduce, {N_RANKS} emulated ranks, {args.mib} MiB bf16 "
+                               f"per rank, LL128 lines, twoshot (bandwidth regime)",
+                   "n_ranks": N_RANKS, "per_rank_mib": args.mib, "encoding": "LL128",
+                   "algorithm": "twoshot", "parallelism": f"replicas{world}",
+                   "l2": "inputs (2 GiB) and staging larger than L2; no flush"},
+        "roofline": {"bound": "hbm", "kernel": names[dom], "achieved": round(achieved, 1),
+                     "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                     "frac": round(achieved / peaks["hbm_gbs"], 4), "traffic": traffic,
+                     "peak_source": peaks["source"]},
+        "kernels": kernels,
+        "gpu_launches": launches[0],
+        "clocks": clk,
+    }
+
+    if not args.quick and rank == 0:
+        # end to end from pinned host memory through coll_run_host
+        host_in = [x.cpu().pin_memory() for x in ins]
+        host_out = [torch.empty(count, dtype=torch.int16).pin_memory() for _ in range(N_RANKS)]
+        with torch.cuda.stream(stream):
+            cd.coll_run_host(coll.spec, host_in, ins, outs, host_out, stream)
+            stream.synchronize()
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            ke = 3
+            e0.record(stream)
+            for _ in range(ke):
+                cd.coll_run_host(coll.spec, host_in, ins, outs, host_out, stream)
+            e1.record(stream)
+            stream.synchronize()
+        e2e_ms = e0.elapsed_time(e1) / ke
+        line["e2e"] = {"value": round(algo_bytes / (e2e_ms * 1e-3) / 1e9, 1), "unit": "GB/s",
+                       "h2d_bytes_per_step": int(N_RANKS * s_bytes),
+                       "d2h_bytes_per_step": int(N_RANKS * s_bytes),
+                       "ms_per_step": round(e2e_ms, 3)}
+        del host_in, host_out
+    coll.close()
+    del coll, ins, outs
+    torch.cuda.empty_cache()
+
+    if not args.quick and rank == 0:
+        line["rows"] = {
+            "reduce_scatter_256MiB": bandwidth_row(cd, cd.REDUCE_SCATTER, count, "rs", stream),
+            "all_gather_256MiB": bandwidth_row(cd, cd.ALLGATHER, count, "ag", stream),
+        }
+        line["latency_us_per_op"] = latency_sweep(cd, stream)
+        if world == 1:
+            line["cpu_baseline"] = cpu_oracle_allreduce(64)
+    if rank == 0:
+        print(json.dumps(line))
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

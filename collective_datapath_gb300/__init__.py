@@ -40,7 +40,8 @@ EXPORTS = [
     "coll_buffer_elems", "coll_bind", "coll_set_routing", "coll_stage", "coll_run",
     "coll_run_host", "coll_get_counts", "coll_query_status", "coll_get_epoch",
     "coll_staging_layout", "coll_stage_withheld", "coll_run_late",
-    "coll_get_rejections", "coll_debug_items", "coll_debug_plan", "coll_destroy",
+    "coll_get_rejections", "coll_debug_items", "coll_debug_plan",
+    "coll_set_profile_events", "coll_last_launches", "coll_destroy",
     "coll_status_string",
 ]
 
@@ -90,6 +91,8 @@ _sig("coll_get_rejections", _st, _vp, _vp, _P(ctypes.c_uint64))
 _sig("coll_debug_items", _st, _vp, ctypes.c_int, _P(ctypes.c_int64), _sz, _P(_sz))
 _sig("coll_debug_plan", _st, _vp, _P(ctypes.c_int), _P(ctypes.c_int),
      _P(ctypes.c_int), _P(ctypes.c_int))
+_sig("coll_set_profile_events", _st, _vp, _P(_vp), ctypes.c_int)
+_sig("coll_last_launches", _st, _vp, _P(ctypes.c_int))
 _sig("coll_destroy", _st, _vp)
 _sig("coll_status_string", ctypes.c_char_p, ctypes.c_int)
 
@@ -270,6 +273,20 @@ def coll_debug_plan(spec: int) -> dict:
                                 ctypes.byref(e)), "coll_debug_plan")
     return {"algorithm": a.value, "path": p.value, "ctas_per_rank": c.value,
             "encoding": e.value}
+
+
+def coll_set_profile_events(spec: int, events: Sequence) -> None:
+    """events: torch.cuda.Event objects (or raw cudaEvent_t handles)."""
+    handles = [e if isinstance(e, int) else e.cuda_event for e in events]
+    arr = (_vp * max(len(handles), 1))(*handles)
+    _check(_lib.coll_set_profile_events(spec, arr, len(handles)),
+           "coll_set_profile_events")
+
+
+def coll_last_launches(spec: int) -> int:
+    n = ctypes.c_int()
+    _check(_lib.coll_last_launches(spec, ctypes.byref(n)), "coll_last_launches")
+    return n.value
 
 
 def coll_destroy(spec: int) -> None:

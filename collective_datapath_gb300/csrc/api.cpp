@@ -18,6 +18,8 @@ struct coll_spec {
   size_t ws_bytes = 0;
   bool bound = false;
   RunParams base{};
+  std::vector<cudaEvent_t> events;  // optional per-launch timing events
+  int launches = 0;                 // launches of the current / last run
 };
 
 namespace {
@@ -92,6 +94,19 @@ coll_status_t check_ins(const coll_spec* s, const void* const* ins) {
   return COLL_OK;
 }
 
+// Optional timing: event k is recorded after the k-th launch of a run.
+void run_begin(coll_spec* s, cudaStream_t st) {
+  s->launches = 0;
+  if (!s->events.empty()) cudaEventRecord(s->events[0], st);
+}
+
+cudaError_t launched(coll_spec* s, cudaError_t e, cudaStream_t st) {
+  if (e != cudaSuccess) return e;
+  s->launches += 1;
+  if (s->launches < (int)s->events.size()) return cudaEventRecord(s->events[s->launches], st);
+  return cudaSuccess;
+}
+
 // Consume phase(s) of a run whose inputs are staged; the last launch
 // advances the epoch.
 coll_status_t launch_consumers(coll_spec* s, RunParams P, cudaStream_t st) {
@@ -100,18 +115,21 @@ coll_status_t launch_consumers(coll_spec* s, RunParams P, cudaStream_t st) {
   const bool two = !p.items2.empty();
   if (p.items1.empty() && !two) {
     P.advance_epoch = !rearm_kernel;
-    if (cudaError_t e = launch_advance(P, st)) return cuda_status(e);
+    if (cudaError_t e = launched(s, launch_advance(P, st), st)) return cuda_status(e);
   } else {
     P.advance_epoch = !two && !rearm_kernel;
-    if (cudaError_t e = launch_consume(P, 1, p.consume_grid, st)) return cuda_status(e);
+    if (cudaError_t e = launched(s, launch_consume(P, 1, p.consume_grid, st), st))
+      return cuda_status(e);
     if (two) {
       P.advance_epoch = !rearm_kernel;
-      if (cudaError_t e = launch_consume(P, 2, p.consume_grid, st)) return cuda_status(e);
+      if (cudaError_t e = launched(s, launch_consume(P, 2, p.consume_grid, st), st))
+        return cuda_status(e);
     }
   }
   if (rearm_kernel) {
     P.advance_epoch = 1;
-    if (cudaError_t e = launch_rearm(P, device_sms() * 4, st)) return cuda_status(e);
+    if (cudaError_t e = launched(s, launch_rearm(P, device_sms() * 4, st), st))
+      return cuda_status(e);
   }
   return COLL_OK;
 }
@@ -254,15 +272,16 @@ coll_status_t coll_run(coll_spec_t* s, const void* const* dev_ins, void* const* 
     if (dev_ins) P.in[r] = static_cast<const uint16_t*>(dev_ins[r]);
   }
   const bool empty = p.items1.empty() && p.items2.empty();
+  run_begin(s, st);
   if (dev_ins != nullptr && p.path == COLL_PATH_FUSED && !empty &&
       !(p.enc == ENC_LL8 && p.reset_mode == COLL_RESET_KERNEL)) {
     P.advance_epoch = 1;
-    return cuda_status(launch_fused(P, p.n * p.ctas_per_rank, st));
+    return cuda_status(launched(s, launch_fused(P, p.n * p.ctas_per_rank, st), st));
   }
   if (dev_ins != nullptr && !p.sitems.empty()) {
     P.stage_rank = -1;
     const int grid = std::min((int)p.sitems.size(), device_sms() * 8);
-    if (cudaError_t e = launch_stage(P, grid, st)) return cuda_status(e);
+    if (cudaError_t e = launched(s, launch_stage(P, grid, st), st)) return cuda_status(e);
   }
   return launch_consumers(s, P, st);
 }
@@ -446,6 +465,19 @@ coll_status_t coll_debug_plan(const coll_spec_t* s, int* algorithm, int* path,
   if (path) *path = s->plan.path;
   if (ctas_per_rank) *ctas_per_rank = s->plan.ctas_per_rank;
   if (encoding) *encoding = s->plan.enc;
+  return COLL_OK;
+}
+
+coll_status_t coll_set_profile_events(coll_spec_t* s, void* const* events, int n) {
+  if (s == nullptr || n < 0 || (n > 0 && events == nullptr)) return COLL_ERR_INVALID;
+  s->events.clear();
+  for (int i = 0; i < n; ++i) s->events.push_back(static_cast<cudaEvent_t>(events[i]));
+  return COLL_OK;
+}
+
+coll_status_t coll_last_launches(const coll_spec_t* s, int* launches) {
+  if (s == nullptr || launches == nullptr) return COLL_ERR_INVALID;
+  *launches = s->launches;
   return COLL_OK;
 }
 

@@ -270,6 +270,16 @@ coll_status_t coll_debug_items(const coll_spec_t *spec, int which, int64_t *buf,
 coll_status_t coll_debug_plan(const coll_spec_t *spec, int *algorithm, int *path,
                               int *ctas_per_rank, int *encoding);
 
+/* Per-launch timing: when set, every following coll_run records events[0]
+ * on its stream before its first launch and events[k] after its k-th launch
+ * (k = 1 .. n-1; launches beyond n-1 record nothing).  `events` are
+ * cudaEvent_t handles owned by the caller; n = 0 turns recording off.  The
+ * array is copied, so the caller may reuse its own storage. */
+coll_status_t coll_set_profile_events(coll_spec_t *spec, void *const *events, int n);
+
+/* Number of kernel launches the last coll_run issued. */
+coll_status_t coll_last_launches(const coll_spec_t *spec, int *launches);
+
 /* Release the spec's host state (never the caller's device memory). */
 coll_status_t coll_destroy(coll_spec_t *spec);
 
