@@ -351,6 +351,8 @@ def main() -> int:
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--mib", type=int, default=256, help="per-rank MiB of the main workload")
     ap.add_argument("--quick", action="store_true", help="skip sweep, extra rows and CPU leg")
+    ap.add_argument("--sweep-only", action="store_true",
+                    help="only the small-message latency sweep (profiling runs)")
     args = ap.parse_args()
     if args.impl == "reference":
         return run_reference(args)
@@ -374,6 +376,9 @@ def main() -> int:
 
     peaks = load_peaks()
     stream = torch.cuda.Stream()
+    if args.sweep_only:
+        print(json.dumps({"latency_us_per_op": latency_sweep(cd, stream)}))
+        return 0
     count = args.mib * 2**20 // 2
     s_bytes = count * 2.0
     coll = cd.Collective(cd.ALLREDUCE, N_RANKS, count, encoding=cd.COLL_LL128,
@@ -384,6 +389,10 @@ def main() -> int:
     nk = 3
     events = [[torch.cuda.Event(enable_timing=True) for _ in range(nk + 1)]
               for _ in range(W + K)]
+    for evs in events:          # torch creates the CUDA event on first record
+        for e in evs:
+            e.record(stream)
+    stream.synchronize()
     launches = [0]
 
     def step(i):

@@ -31,7 +31,7 @@ COLL_OK, COLL_ERR_INVALID, COLL_ERR_UNSUPPORTED, COLL_ERR_ALIGN = 0, 1, 2, 3
 COLL_ERR_NOMEM, COLL_ERR_CUDA, COLL_ERR_TIMEOUT, COLL_ERR_STATE = 4, 5, 6, 7
 COLL_LL8, COLL_LL128 = 0, 1
 COLL_ALGO_AUTO, COLL_ONESHOT, COLL_TWOSHOT = 0, 1, 2
-COLL_RESET_FUSED, COLL_RESET_KERNEL, COLL_RESET_NONE = 0, 1, 2
+COLL_RESET_FUSED, COLL_RESET_KERNEL, COLL_RESET_NONE, COLL_RESET_DEFERRED = 0, 1, 2, 3
 COLL_PATH_AUTO, COLL_PATH_FUSED, COLL_PATH_STREAMED = 0, 1, 2
 
 # Every symbol include/coll.h declares (checked by the tests).
@@ -278,6 +278,8 @@ def coll_debug_plan(spec: int) -> dict:
 def coll_set_profile_events(spec: int, events: Sequence) -> None:
     """events: torch.cuda.Event objects (or raw cudaEvent_t handles)."""
     handles = [e if isinstance(e, int) else e.cuda_event for e in events]
+    if any(not h for h in handles):
+        raise ValueError("an event has no CUDA handle yet (record it once first)")
     arr = (_vp * max(len(handles), 1))(*handles)
     _check(_lib.coll_set_profile_events(spec, arr, len(handles)),
            "coll_set_profile_events")

@@ -73,6 +73,13 @@ void fill_base(coll_spec* s) {
     P.seg_elems[k] = p.pseg[0][k].elems;
     P.seg_in0[k] = p.pseg[0][k].in_elem;
   }
+  auto equal_lists = [&](const int* beg) {
+    for (int r = 1; r < p.n; ++r)
+      if (beg[r + 1] - beg[r] != beg[1] - beg[0]) return 0;
+    return 1;
+  };
+  P.interleave1 = equal_lists(p.beg1);
+  P.interleave2 = equal_lists(p.beg2);
   P.stage_rank = -1;
   P.advance_epoch = 0;
 }
@@ -118,8 +125,14 @@ coll_status_t launch_consumers(coll_spec* s, RunParams P, cudaStream_t st) {
     if (cudaError_t e = launched(s, launch_advance(P, st), st)) return cuda_status(e);
   } else {
     P.advance_epoch = !two && !rearm_kernel;
-    if (cudaError_t e = launched(s, launch_consume(P, 1, p.consume_grid, st), st))
+    bool all_fold = p.enc == ENC_LL128 && !p.items1.empty();
+    for (const Item& it : p.items1) all_fold = all_fold && it.kind == IK_REDUCE;
+    if (all_fold) {
+      const int grid = std::min<int>((int)p.items1.size(), device_sms() * 2);
+      if (cudaError_t e = launched(s, launch_fold(P, grid, st), st)) return cuda_status(e);
+    } else if (cudaError_t e = launched(s, launch_consume(P, 1, p.consume_grid, st), st)) {
       return cuda_status(e);
+    }
     if (two) {
       P.advance_epoch = !rearm_kernel;
       if (cudaError_t e = launched(s, launch_consume(P, 2, p.consume_grid, st), st))
@@ -143,7 +156,7 @@ void coll_options_default(coll_options_t* opt) {
   std::memset(opt, 0, sizeof(*opt));
   opt->encoding = COLL_LL8;
   opt->algorithm = COLL_ALGO_AUTO;
-  opt->reset_mode = COLL_RESET_FUSED;
+  opt->reset_mode = COLL_RESET_DEFERRED;
   opt->path = COLL_PATH_AUTO;
 }
 
@@ -331,10 +344,10 @@ coll_status_t coll_query_status(coll_spec_t* s, coll_stream_t stream, int* code,
   if (rank) *rank = (int)h.status_rank;
   if (line) *line = h.status_line;
   if (h.status_code != 0 || h.abort != 0) {
-    // Clear status_code .. abort (bytes 8..31) and leave the epoch alone.
+    // Clear status_code .. abort (bytes 8..27) and leave the epoch alone.
     // An aborted run may have skipped items, so the reader counters of the
     // counted re-arm are reset as well.
-    char zeros[24] = {0};
+    char zeros[20] = {0};
     if (cudaMemcpy(s->ws + 8, zeros, sizeof zeros, cudaMemcpyHostToDevice) != cudaSuccess)
       return COLL_ERR_CUDA;
     const size_t cbytes = 4 * (size_t)(s->plan.ncounters ? s->plan.ncounters : 1);

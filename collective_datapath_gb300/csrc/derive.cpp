@@ -121,7 +121,7 @@ int derive(const DeriveInput& in, Plan& p) {
   if (n < 1 || n > kMaxRanks) return COLL_ERR_UNSUPPORTED;
   if (in.dtype != COLL_BF16) return COLL_ERR_UNSUPPORTED;
   if (in.encoding != COLL_LL8 && in.encoding != COLL_LL128) return COLL_ERR_UNSUPPORTED;
-  if (in.reset_mode < 0 || in.reset_mode > 2 || in.path < 0 || in.path > 2 ||
+  if (in.reset_mode < 0 || in.reset_mode > 3 || in.path < 0 || in.path > 2 ||
       in.algorithm < 0 || in.algorithm > 2 || in.ctas < 0 || in.tile_lines < 0)
     return COLL_ERR_INVALID;
 
@@ -198,17 +198,34 @@ int derive(const DeriveInput& in, Plan& p) {
 
   // Tile sizes (lines, multiples of 4).
   auto fused = p.path == COLL_PATH_FUSED;
-  const uint64_t max_tile = p.enc == ENC_LL8 ? 2048 : 512;
-  auto pick_tile = [&](uint64_t lines_per_rank) -> uint64_t {
+  // Streamed tiles: a 256-thread CTA moves 4 LL8 groups per thread or 4
+  // LL128 rows per warp per step.
+  const uint64_t max_tile = p.enc == ENC_LL8 ? 4096 : 1024;
+  // Fused tiles: the smallest tile (multiple of 4 lines) that gives every
+  // CTA of a rank at most one item of the phase.
+  auto pick_tile = [&](const std::vector<uint64_t>& seg_lines) -> uint64_t {
     if (in.tile_lines > 0) return round_up((uint64_t)in.tile_lines, 4);
     if (!fused) return max_tile;
-    // about B items per rank per phase
-    uint64_t t = round_up((lines_per_rank + B - 1) / (uint64_t)B, 4);
-    return std::max<uint64_t>(4, std::min<uint64_t>(t, max_tile));
+    uint64_t lo = 4, hi = max_tile;
+    auto items_for = [&](uint64_t t) {
+      uint64_t c = 0;
+      for (uint64_t l : seg_lines) c += (l + t - 1) / t;
+      return c;
+    };
+    if (items_for(hi) > (uint64_t)B) return hi;
+    while (lo < hi) {
+      const uint64_t mid = round_up((lo + hi) / 2, 4);
+      if (mid >= hi) break;
+      if (items_for(mid) <= (uint64_t)B) hi = mid; else lo = mid + 4;
+    }
+    return hi;
   };
-  uint64_t rank_lines = 0;
-  for (auto& s : p.pseg[0]) rank_lines += s.lines;
-  const Tiler stage_tiler{pick_tile(rank_lines), p.enc};
+  auto seg_lines = [&](const std::vector<Seg>& segs) {
+    std::vector<uint64_t> v;
+    for (auto& s : segs) v.push_back(s.lines);
+    return v;
+  };
+  const Tiler stage_tiler{pick_tile(seg_lines(p.pseg[0])), p.enc};
   const uint64_t epl = (uint64_t)line_elems(p.enc);
 
   // Stage items.
@@ -237,9 +254,7 @@ int derive(const DeriveInput& in, Plan& p) {
     case CK_ALLREDUCE:
       if (!twoshot) {
         // oneshot: every rank folds every partition of every rank
-        uint64_t lines = 0;
-        for (auto& s : p.pseg[0]) lines += s.lines;
-        const Tiler t{pick_tile(lines), p.enc};
+        const Tiler t{pick_tile(seg_lines(p.pseg[0])), p.enc};
         for (int d = 0; d < n; ++d)
           for (int k = 0; k < n; ++k) {
             const Seg& s = p.pseg[0][k];
@@ -253,7 +268,7 @@ int derive(const DeriveInput& in, Plan& p) {
       } else {
         // twoshot phase 1: owner r folds partition r of every rank and
         // publishes it into its reduced-partition image
-        const Tiler t1{pick_tile(lines_for(p.enc, M) * 1), p.enc};
+        const Tiler t1{pick_tile({lines_for(p.enc, M)}), p.enc};
         for (int r = 0; r < n; ++r) {
           const Seg& s = p.pseg[0][r];
           t1.over(s, [&](uint64_t t0, uint64_t nl, uint64_t ne) {
@@ -264,7 +279,7 @@ int derive(const DeriveInput& in, Plan& p) {
           });
         }
         // phase 2: every rank copies every owner's reduced partition
-        const Tiler t2{pick_tile(lines_for(p.enc, M) * n), p.enc};
+        const Tiler t2{pick_tile(std::vector<uint64_t>(n, lines_for(p.enc, M))), p.enc};
         for (int d = 0; d < n; ++d)
           for (int r = 0; r < n; ++r) {
             const Seg& s = p.agseg[r][0];
@@ -278,7 +293,7 @@ int derive(const DeriveInput& in, Plan& p) {
       }
       break;
     case CK_REDUCE_SCATTER: {
-      const Tiler t{pick_tile(lines_for(p.enc, M)), p.enc};
+      const Tiler t{pick_tile({lines_for(p.enc, M)}), p.enc};
       for (int r = 0; r < n; ++r) {
         const Seg& s = p.pseg[0][r];
         t.over(s, [&](uint64_t t0, uint64_t nl, uint64_t ne) {
@@ -290,7 +305,7 @@ int derive(const DeriveInput& in, Plan& p) {
       break;
     }
     case CK_ALLGATHER: {
-      const Tiler t{pick_tile(lines_for(p.enc, M) * n), p.enc};
+      const Tiler t{pick_tile(std::vector<uint64_t>(n, lines_for(p.enc, M))), p.enc};
       for (int d = 0; d < n; ++d)
         for (int q = 0; q < n; ++q) {
           const Seg& s = p.pseg[q][0];
@@ -304,7 +319,7 @@ int derive(const DeriveInput& in, Plan& p) {
       break;
     }
     case CK_ALLTOALL: {
-      const Tiler t{pick_tile(lines_for(p.enc, M) * n), p.enc};
+      const Tiler t{pick_tile(std::vector<uint64_t>(n, lines_for(p.enc, M))), p.enc};
       for (int d = 0; d < n; ++d)
         for (int q = 0; q < n; ++q) {
           const Seg& s = p.pseg[q][d];

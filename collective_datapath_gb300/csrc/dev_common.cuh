@@ -11,6 +11,8 @@ namespace coll {
 
 // coll_status_t values used on the device (see coll.h).
 constexpr uint32_t kStatusTimeout = 6;
+// COLL_RESET_* values used on the device (see coll.h).
+constexpr int kResetLastReader = 0, kResetKernel = 1, kResetNone = 2, kResetDeferred = 3;
 
 // ---- global memory accesses ------------------------------------------------
 // Readiness lines are written and polled with .relaxed.gpu accesses: they are
@@ -160,26 +162,43 @@ __device__ __forceinline__ void count_rejection(char* ws) {
   atomicAdd(reinterpret_cast<unsigned long long*>(&header(ws)->rejections), 1ull);
 }
 
-// Last CTA of the run's final launch advances the epoch (the next run uses
-// the other staging slot).  Every CTA calls this once, after its work.
-__device__ __forceinline__ void finish_run(const RunParams& P, uint64_t epoch) {
-  if (!P.advance_epoch) return;
-  __syncthreads();
+// Epoch protocol of a launch.  Thread 0 reads the device epoch once and
+// shares it with the CTA; in the launch that ends a run every CTA then adds
+// one to `arrived` (fire-and-forget).  The last CTA of the grid advances the
+// epoch once every CTA has read it (arrived == grid), so the next run uses
+// the other staging slot; no CTA waits at the end of its own work.
+__device__ __forceinline__ uint64_t begin_run(const RunParams& P) {
+  __shared__ uint64_t s_epoch;
   if (threadIdx.x == 0) {
     WsHeader* h = header(P.ws);
-    __threadfence();
-    uint32_t total = gridDim.x * gridDim.y * gridDim.z;
-    if (atomicAdd(&h->done_ctas, 1u) == total - 1) {
-      h->done_ctas = 0;
-      h->started = 0;
-      st_relaxed_u64(&h->epoch, epoch + 1);
-      __threadfence();
+    s_epoch = ld_relaxed_u64(&h->epoch);
+    if (P.advance_epoch) {
+      asm volatile("red.relaxed.gpu.global.add.u32 [%0], 1;" ::"l"(&h->arrived) : "memory");
     }
   }
+  __syncthreads();
+  return s_epoch;
 }
 
-__device__ __forceinline__ uint64_t read_epoch(const RunParams& P) {
-  return ld_relaxed_u64(&header(P.ws)->epoch);
+__device__ __forceinline__ void finish_run(const RunParams& P, uint64_t epoch) {
+  if (!P.advance_epoch || threadIdx.x != 0) return;
+  const uint32_t total = gridDim.x * gridDim.y * gridDim.z;
+  if (blockIdx.x != gridDim.x - 1) return;
+  WsHeader* h = header(P.ws);
+  // Every CTA has started (and read the epoch) long before the last CTA
+  // finishes; the 10 s bound only guards against a broken launch.  This wait
+  // ignores `abort`: the epoch must not move before every CTA has read it.
+  const uint64_t t0 = globaltimer_ns();
+  while (ld_relaxed_u32(&h->arrived) < total) {
+    if (globaltimer_ns() - t0 > 10000000000ull) {
+      latch_error(P.ws, kStatusTimeout, 0xFFFFFFFFu, -2);
+      break;
+    }
+    __nanosleep(100);
+  }
+  st_relaxed_u32(&h->arrived, 0u);
+  st_relaxed_u32(&h->started[(epoch + 1) & 1], 0u);  // the next run's counter
+  st_relaxed_u64(&h->epoch, epoch + 1);
 }
 
 }  // namespace coll

@@ -38,22 +38,139 @@ __device__ __forceinline__ void consume_item(const RunParams& P, const Region& R
 
 template <int ENC>
 __global__ void __launch_bounds__(kThreads) k_stage(RunParams P) {
-  const uint64_t e = read_epoch(P);
+  const uint64_t e = begin_run(P);
   const int lo = P.stage_rank < 0 ? 0 : P.stage_rank;
   const int hi = P.stage_rank < 0 ? P.nranks : P.stage_rank + 1;
   for (int i = P.sbeg[lo] + blockIdx.x; i < P.sbeg[hi]; i += gridDim.x)
     stage_item<ENC, false>(P, P.sitems[i], e);
 }
 
+// Stream-ordered consume.  When every rank has the same item list shape the
+// launch walks the items rank-interleaved (item j of rank 0, of rank 1, ...)
+// so the ranks that read the same source tile run together and share L2.
 template <int ENC>
-__global__ void __launch_bounds__(kThreads) k_consume(RunParams P, int phase) {
-  const uint64_t e = read_epoch(P);
+__global__ void __launch_bounds__(kThreads, 2) k_consume(RunParams P, int phase) {
+  const uint64_t e = begin_run(P);
   const Item* items = phase == 1 ? P.items1 : P.items2;
-  const int n_items = phase == 1 ? P.beg1[P.nranks] : P.beg2[P.nranks];
+  const int* beg = phase == 1 ? P.beg1 : P.beg2;
+  const int n_items = beg[P.nranks];
+  const bool inter = phase == 1 ? P.interleave1 : P.interleave2;
   const Region& R = phase == 1 ? P.P : P.AG;
-  for (int i = blockIdx.x; i < n_items; i += gridDim.x) {
+  for (int v = blockIdx.x; v < n_items; v += gridDim.x) {
     if (aborted(P.ws)) break;
+    const int i = inter ? beg[v % P.nranks] + v / P.nranks : v;
     consume_item<ENC, false>(P, R, items[i], e);
+  }
+  finish_run(P, e);
+}
+
+// ---- LL128 fold with a cp.async shared-memory pipeline ------------------------
+// The unified pipeline of Purlin §3.3 (Algorithm 2) applied to the fold: each
+// warp keeps kFoldStages rows of all n rank images in flight in shared memory
+// (prime; steady state: wait for the oldest row, read it into registers,
+// refetch the slot, validate, fold, write; drain).  A lane only ever copies
+// and reads its own 16-byte chunks, so the per-thread cp.async groups need no
+// warp synchronisation.  Stream-ordered launches only.
+constexpr int kFoldStages = 3;
+
+__device__ __forceinline__ void cp_async16(uint32_t saddr, const void* g, bool valid) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(saddr), "l"(g),
+               "r"(valid ? 16 : 0)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+  asm volatile("cp.async.commit_group;" ::: "memory");
+}
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+__device__ __forceinline__ uint4 lds_v4(uint32_t saddr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "r"(saddr)
+               : "memory");
+  return v;
+}
+
+size_t fold_smem_bytes(int nranks) {
+  return (size_t)(kThreads / 32) * kFoldStages * nranks * kRowBytes;
+}
+
+__global__ void __launch_bounds__(kThreads, 2) k_fold_ll128(RunParams P) {
+  extern __shared__ __align__(128) char smem[];
+  const uint64_t e = begin_run(P);
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
+  const int n = P.nranks;
+  const int li = lane >> 3;
+  const uint32_t wbase = (uint32_t)__cvta_generic_to_shared(smem) +
+                         (uint32_t)(warp * kFoldStages * n * kRowBytes + 16 * lane);
+  const int n_items = P.beg1[P.nranks];
+  for (int v = blockIdx.x; v < n_items; v += gridDim.x) {
+    if (aborted(P.ws)) break;
+    const int i = P.interleave1 ? P.beg1[v % P.nranks] + v / P.nranks : v;
+    const Item it = P.items1[i];
+    const bool publish = (it.flags & IF_PUBLISH) != 0;
+    const uint32_t nrows = (it.nlines + kLL128RowLines - 1) / kLL128RowLines;
+    const int nj = (uint32_t)warp < nrows ? (int)((nrows - warp + nwarps - 1) / nwarps) : 0;
+    auto issue = [&](int j) {
+      if (j < nj) {
+        const uint32_t r = warp + j * nwarps;
+        const int nl = min((int)kLL128RowLines, (int)(it.nlines - r * kLL128RowLines));
+        const uint64_t off =
+            (it.src_line + (uint64_t)r * kLL128RowLines) * kLL128LineBytes + 16 * lane;
+        const uint32_t slot = wbase + (uint32_t)((j % kFoldStages) * n * kRowBytes);
+        for (int p = 0; p < n; ++p)
+          cp_async16(slot + p * kRowBytes, image_bytes(P, P.P, e, p) + off, li < nl);
+      }
+      cp_async_commit();
+    };
+#pragma unroll
+    for (int j = 0; j < kFoldStages; ++j) issue(j);
+    for (int j = 0; j < nj; ++j) {
+      cp_async_wait<kFoldStages - 1>();
+      const uint32_t slot = wbase + (uint32_t)((j % kFoldStages) * n * kRowBytes);
+      uint4 s[kMaxRanks];
+#pragma unroll
+      for (int p = 0; p < kMaxRanks; ++p)
+        if (p < n) s[p] = lds_v4(slot + p * kRowBytes);
+      issue(j + kFoldStages);
+      const uint32_t r = warp + j * nwarps;
+      const int nl = min((int)kLL128RowLines, (int)(it.nlines - r * kLL128RowLines));
+      const bool valid = li < nl;
+      const uint64_t row_line = it.src_line + (uint64_t)r * kLL128RowLines;
+      bool ready = true;
+#pragma unroll
+      for (int p = 0; p < kMaxRanks; ++p)
+        if (p < n) ready = ready && ll128_chunk_ready(s[p], lane, valid, e);
+      if (!__all_sync(0xFFFFFFFFu, ready)) {
+        bool ok = true;
+#pragma unroll
+        for (int p = 0; p < kMaxRanks; ++p) {
+          if (p < n && ok) {
+            const bool rp = ll128_chunk_ready(s[p], lane, valid, e);
+            if (!__all_sync(0xFFFFFFFFu, rp)) {
+              const char* row = image_bytes(P, P.P, e, p) + row_line * kLL128LineBytes;
+              ok = ll128_wait_chunk(P, row, lane, rp, e, p, (int64_t)row_line);
+              if (ok && valid) s[p] = ld_v4(row + 16 * lane);
+            }
+          }
+        }
+        if (!ok) break;
+      }
+      const uint4 res = ll128_fold(s, n);
+      if (publish) {
+        char* dst = image_bytes(P, P.AG, e, it.dst) +
+                    (it.out_off + (uint64_t)r * kLL128RowLines) * kLL128LineBytes;
+        ll128_store_row<false>(dst, res, lane, nl, e);
+      } else {
+        const int64_t left = (int64_t)it.nelems - (int64_t)r * kRowElems;
+        ll128_write_payload(P.out[it.dst] + it.out_off + (uint64_t)r * kRowElems, res, lane,
+                            left);
+      }
+    }
+    cp_async_wait<0>();
   }
   finish_run(P, e);
 }
@@ -67,7 +184,7 @@ __device__ void late_producer(const RunParams& P, uint64_t e, int p, int workers
   if (threadIdx.x == 0) {
     Waiter w;
     go = 1;
-    while (ld_relaxed_u32(&h->started) < (uint32_t)workers) {
+    while (ld_relaxed_u32(&h->started[e & 1]) < (uint32_t)workers) {
       if (w.expired(P.ws, P.timeout_ns)) {
         latch_error(P.ws, kStatusTimeout, p, -1);
         go = 0;
@@ -146,7 +263,7 @@ __device__ void late_producer(const RunParams& P, uint64_t e, int p, int workers
 
 template <int ENC>
 __global__ void __launch_bounds__(kThreads) k_fused(RunParams P) {
-  const uint64_t e = read_epoch(P);
+  const uint64_t e = begin_run(P);
   const int B = P.ctas_per_rank;
   const int workers = P.nranks * B;
   if ((int)blockIdx.x >= workers) {
@@ -158,7 +275,7 @@ __global__ void __launch_bounds__(kThreads) k_fused(RunParams P) {
   if (P.sitems != nullptr)
     for (int i = P.sbeg[d] + b; i < P.sbeg[d + 1]; i += B)
       stage_item<ENC, true>(P, P.sitems[i], e);
-  if (threadIdx.x == 0) atomicAdd(&header(P.ws)->started, 1u);
+  if (threadIdx.x == 0) atomicAdd(&header(P.ws)->started[e & 1], 1u);
   for (int i = P.beg1[d] + b; i < P.beg1[d + 1]; i += B) {
     if (aborted(P.ws)) break;
     consume_item<ENC, true>(P, P.P, P.items1[i], e);
@@ -175,7 +292,7 @@ __global__ void __launch_bounds__(kThreads) k_fused(RunParams P) {
 // content: readiness value e-1 / e-2 / 0 (by kind) and a poison payload.
 template <int ENC>
 __global__ void k_withhold(RunParams P) {
-  const uint64_t e = read_epoch(P);
+  const uint64_t e = begin_run(P);
   const int p = P.stage_rank;
   for (int64_t j = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; j < P.wh_n;
        j += (int64_t)gridDim.x * blockDim.x) {
@@ -197,7 +314,7 @@ __global__ void k_withhold(RunParams P) {
 
 // Re-arm every LL8 line of the current slot (both regions), then end the run.
 __global__ void __launch_bounds__(kThreads) k_rearm(RunParams P) {
-  const uint64_t e = read_epoch(P);
+  const uint64_t e = begin_run(P);
   for (int region = 0; region < 2; ++region) {
     const Region& R = region == 0 ? P.P : P.AG;
     if (R.rank_bytes == 0) continue;
@@ -210,7 +327,7 @@ __global__ void __launch_bounds__(kThreads) k_rearm(RunParams P) {
   finish_run(P, e);
 }
 
-__global__ void k_advance(RunParams P) { finish_run(P, read_epoch(P)); }
+__global__ void k_advance(RunParams P) { finish_run(P, begin_run(P)); }
 
 // ---- launchers ---------------------------------------------------------------
 
@@ -270,6 +387,20 @@ cudaError_t launch_fused(const RunParams& P, int grid, cudaStream_t s) {
   cfg.numAttrs = 1;
   if (P.enc == ENC_LL8) return cudaLaunchKernelEx(&cfg, k_fused<ENC_LL8>, P);
   return cudaLaunchKernelEx(&cfg, k_fused<ENC_LL128>, P);
+}
+
+cudaError_t launch_fold(const RunParams& P, int grid, cudaStream_t s) {
+  static size_t configured = 0;
+  const size_t bytes = fold_smem_bytes(P.nranks);
+  if (bytes > configured) {
+    cudaError_t e = cudaFuncSetAttribute(k_fold_ll128,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)fold_smem_bytes(kMaxRanks));
+    if (e != cudaSuccess) return e;
+    configured = fold_smem_bytes(kMaxRanks);
+  }
+  k_fold_ll128<<<grid, kThreads, bytes, s>>>(P);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_withhold(const RunParams& P, cudaStream_t s) {

@@ -15,6 +15,8 @@ int fused_capacity(int enc);
 cudaError_t launch_stage(const RunParams& P, int grid, cudaStream_t s);
 cudaError_t launch_consume(const RunParams& P, int phase, int grid, cudaStream_t s);
 cudaError_t launch_fused(const RunParams& P, int grid, cudaStream_t s);
+// LL128 phase-1 folds through the shared-memory pipeline (all items IK_REDUCE).
+cudaError_t launch_fold(const RunParams& P, int grid, cudaStream_t s);
 cudaError_t launch_withhold(const RunParams& P, cudaStream_t s);
 cudaError_t launch_rearm(const RunParams& P, int grid, cudaStream_t s);
 cudaError_t launch_advance(const RunParams& P, cudaStream_t s);

@@ -126,51 +126,11 @@ __device__ __noinline__ bool ll128_wait_seq(const RunParams& P, const char* p,
   }
 }
 
-// Read one row of lines of one image, validated.  Returns false on timeout.
-// Stream-ordered: load, check, and only on a mismatch wait and reload.
-// Concurrent: number first, acquire fence, then the data.
-template <bool kConc>
-__device__ __forceinline__ bool ll128_load_row(const RunParams& P, const char* row,
-                                               uint4& ln, int lane, int nl,
-                                               uint64_t seq, uint32_t rank,
-                                               int64_t row_line) {
-  const int i = lane >> 3, k = lane & 7;
-  const bool valid = i < nl;
-  const char* p = row + 16 * lane;
-  bool ok = true;
-  if (!kConc) {
-    ln = valid ? ld_v4(p) : make_uint4(0, 0, 0, 0);
-    bool ready = !(valid && k == 7) ||
-                 (((uint64_t)ln.w << 32) | ln.z) == seq;
-    if (__all_sync(0xFFFFFFFFu, ready)) return true;
-    if (!ready) {
-      ok = ll128_wait_seq(P, p + 8, seq, rank, row_line + i);
-      fence_acq_rel_gpu();
-    }
-    __syncwarp();
-    if (__all_sync(0xFFFFFFFFu, ok)) {
-      if (valid) ln = ld_v4(p);
-      return true;
-    }
-    return false;
-  }
-  if (valid && k == 7) {
-    if (ld_relaxed_u64(p + 8) != seq) ok = ll128_wait_seq(P, p + 8, seq, rank, row_line + i);
-    fence_acq_rel_gpu();
-  }
-  __syncwarp();
-  if (!__all_sync(0xFFFFFFFFu, ok)) return false;
-  if (valid) {
-    uint64_t a, b;
-    ld_relaxed_v2u64(p, a, b);
-    ln = make_uint4((uint32_t)a, (uint32_t)(a >> 32), (uint32_t)b, (uint32_t)(b >> 32));
-  } else {
-    ln = make_uint4(0, 0, 0, 0);
-  }
-  return true;
-}
+// Rows a warp keeps in flight per step (copy and stage: one load per row).
+constexpr int kRowsInFlight = 4;
 
-// Stage one tile: rows of 240 input elements -> rows of four lines.
+// Stage one tile: rows of 240 input elements -> rows of four lines.  A warp
+// loads kRowsInFlight rows of input before it re-aligns and stores them.
 template <bool kConc>
 __device__ __forceinline__ void ll128_stage_tile(const RunParams& P, const StageItem& it,
                                                  uint64_t epoch) {
@@ -178,14 +138,76 @@ __device__ __forceinline__ void ll128_stage_tile(const RunParams& P, const Stage
   const uint16_t* in = P.in[it.rank] + it.in_elem;
   char* img = image_bytes(P, P.P, epoch, it.rank) + it.dst_line * kLL128LineBytes;
   const uint32_t nrows = (it.nlines + kLL128RowLines - 1) / kLL128RowLines;
-  for (uint32_t r = warp; r < nrows; r += nwarps) {
-    const int64_t left = (int64_t)it.nelems - (int64_t)r * kRowElems;
-    uint4 pay = make_uint4(0, 0, 0, 0);
-    if (lane < 30 && 8 * lane < left) pay = ld_stream_v4(in + (size_t)r * kRowElems + 8 * lane);
-    uint4 ln = payload_to_lines(pay, lane);
-    const int nl = min((int)kLL128RowLines, (int)(it.nlines - r * kLL128RowLines));
-    ll128_store_row<kConc>(img + (size_t)r * kRowBytes, ln, lane, nl, epoch);
+  for (uint32_t r0 = warp; r0 < nrows; r0 += nwarps * kRowsInFlight) {
+    uint4 pay[kRowsInFlight];
+#pragma unroll
+    for (int j = 0; j < kRowsInFlight; ++j) {
+      const uint32_t r = r0 + j * nwarps;
+      const int64_t left = (int64_t)it.nelems - (int64_t)r * kRowElems;
+      pay[j] = make_uint4(0, 0, 0, 0);
+      if (r < nrows && lane < 30 && 8 * lane < left)
+        pay[j] = ld_stream_v4(in + (size_t)r * kRowElems + 8 * lane);
+    }
+#pragma unroll
+    for (int j = 0; j < kRowsInFlight; ++j) {
+      const uint32_t r = r0 + j * nwarps;
+      if (r >= nrows) break;
+      uint4 ln = payload_to_lines(pay[j], lane);
+      const int nl = min((int)kLL128RowLines, (int)(it.nlines - r * kLL128RowLines));
+      ll128_store_row<kConc>(img + (size_t)r * kRowBytes, ln, lane, nl, epoch);
+    }
   }
+}
+
+__device__ __forceinline__ bool ll128_chunk_ready(const uint4& v, int lane, bool valid,
+                                                  uint64_t seq) {
+  return !(valid && (lane & 7) == 7) || ((((uint64_t)v.w) << 32) | v.z) == seq;
+}
+
+// Stream-ordered slow path: a chunk loaded optimistically did not carry the
+// epoch.  The lane waits (bounded) for the number and fences; the caller
+// reloads the chunk when every lane of the warp succeeded.  Warp-collective.
+__device__ __noinline__ bool ll128_wait_chunk(const RunParams& P, const char* row, int lane,
+                                              bool ready, uint64_t seq, uint32_t rank,
+                                              int64_t row_line) {
+  bool ok = true;
+  if (!ready) {
+    ok = ll128_wait_seq(P, row + 16 * lane + 8, seq, rank, row_line + (lane >> 3));
+    fence_acq_rel_gpu();
+  }
+  __syncwarp();
+  return __all_sync(0xFFFFFFFFu, ok);
+}
+
+// Concurrent path: the lanes holding sequence numbers read them for `cnt`
+// rows first (relaxed), wait for the missing ones, then one acquire fence;
+// after __syncwarp every lane may load the data of those rows.
+template <int CNT>
+__device__ __forceinline__ bool ll128_acquire_rows(const RunParams& P, const char* const* rows,
+                                                   const int* nls, int cnt, int lane,
+                                                   uint64_t seq, const uint32_t* ranks,
+                                                   const int64_t* row_lines) {
+  bool ok = true;
+  if ((lane & 7) == 7) {
+    uint64_t v[CNT];
+#pragma unroll
+    for (int j = 0; j < CNT; ++j)
+      if (j < cnt && (lane >> 3) < nls[j]) v[j] = ld_relaxed_u64(rows[j] + 16 * lane + 8);
+#pragma unroll
+    for (int j = 0; j < CNT; ++j)
+      if (j < cnt && (lane >> 3) < nls[j] && v[j] != seq)
+        ok = ok && ll128_wait_seq(P, rows[j] + 16 * lane + 8, seq, ranks[j],
+                                  row_lines[j] + (lane >> 3));
+    fence_acq_rel_gpu();
+  }
+  __syncwarp();
+  return __all_sync(0xFFFFFFFFu, ok);
+}
+
+__device__ __forceinline__ uint4 ld_relaxed_v4(const char* p) {
+  uint64_t a, b;
+  ld_relaxed_v2u64(p, a, b);
+  return make_uint4((uint32_t)a, (uint32_t)(a >> 32), (uint32_t)b, (uint32_t)(b >> 32));
 }
 
 // Fold the 8 (k < 7) or 4 (k = 7) bf16 of this lane's chunk over n images.
@@ -220,43 +242,138 @@ __device__ __forceinline__ void ll128_write_payload(uint16_t* out_row, uint4 ln,
 }
 
 // Process one consume item (see ll8_consume_item); `R` = source region.
+// Fold: a warp loads the row of all n images before it validates them.
+// Copy: a warp loads kRowsInFlight rows before it validates them.
 template <bool kConc>
 __device__ __forceinline__ void ll128_consume_item(const RunParams& P, const Region& R,
                                                    const Item& it, uint64_t epoch) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
   const int n = P.nranks;
-  const bool reduce = it.kind == IK_REDUCE;
   const bool publish = (it.flags & IF_PUBLISH) != 0;
   const uint32_t nrows = (it.nlines + kLL128RowLines - 1) / kLL128RowLines;
-  for (uint32_t r = warp; r < nrows; r += nwarps) {
-    const int nl = min((int)kLL128RowLines, (int)(it.nlines - r * kLL128RowLines));
-    const uint64_t row_line = it.src_line + (uint64_t)r * kLL128RowLines;
-    const int64_t left = (int64_t)it.nelems - (int64_t)r * kRowElems;
-    uint4 res;
-    bool ok = true;
-    if (reduce) {
+  const int li = lane >> 3;
+  if (it.kind == IK_REDUCE) {
+    for (uint32_t r = warp; r < nrows; r += nwarps) {
+      const int nl = min((int)kLL128RowLines, (int)(it.nlines - r * kLL128RowLines));
+      const bool valid = li < nl;
+      const uint64_t row_line = it.src_line + (uint64_t)r * kLL128RowLines;
+      const uint64_t roff = row_line * kLL128LineBytes;
       uint4 s[kMaxRanks];
+      if (!kConc) {
 #pragma unroll
-      for (int p = 0; p < kMaxRanks; ++p)
-        if (p < n)
-          ok = ok && ll128_load_row<kConc>(P, image_bytes(P, R, epoch, p) +
-                                                  row_line * kLL128LineBytes,
-                                           s[p], lane, nl, epoch, p, (int64_t)row_line);
-      if (!ok) return;
-      res = ll128_fold(s, n);
-    } else {
-      ok = ll128_load_row<kConc>(P, image_bytes(P, R, epoch, it.src) +
-                                        row_line * kLL128LineBytes,
-                                 res, lane, nl, epoch, it.src, (int64_t)row_line);
-      if (!ok) return;
+        for (int p = 0; p < kMaxRanks; ++p)
+          if (p < n) s[p] = valid ? ld_v4(image_bytes(P, R, epoch, p) + roff + 16 * lane)
+                                  : make_uint4(0, 0, 0, 0);
+        bool ready = true;
+#pragma unroll
+        for (int p = 0; p < kMaxRanks; ++p)
+          if (p < n) ready = ready && ll128_chunk_ready(s[p], lane, valid, epoch);
+        if (!__all_sync(0xFFFFFFFFu, ready)) {
+#pragma unroll
+          for (int p = 0; p < kMaxRanks; ++p) {
+            if (p < n) {
+              const bool rp = ll128_chunk_ready(s[p], lane, valid, epoch);
+              if (!__all_sync(0xFFFFFFFFu, rp)) {
+                const char* row = image_bytes(P, R, epoch, p) + roff;
+                if (!ll128_wait_chunk(P, row, lane, rp, epoch, p, (int64_t)row_line)) return;
+                if (valid) s[p] = ld_v4(row + 16 * lane);
+              }
+            }
+          }
+        }
+      } else {
+        const char* rows[kMaxRanks];
+        int nls[kMaxRanks];
+        uint32_t ranks[kMaxRanks];
+        int64_t rls[kMaxRanks];
+#pragma unroll
+        for (int p = 0; p < kMaxRanks; ++p) {
+          rows[p] = image_bytes(P, R, epoch, p < n ? p : 0) + roff;
+          nls[p] = nl;
+          ranks[p] = p;
+          rls[p] = (int64_t)row_line;
+        }
+        if (!ll128_acquire_rows<kMaxRanks>(P, rows, nls, n, lane, epoch, ranks, rls)) return;
+#pragma unroll
+        for (int p = 0; p < kMaxRanks; ++p)
+          if (p < n) s[p] = valid ? ld_relaxed_v4(rows[p] + 16 * lane) : make_uint4(0, 0, 0, 0);
+      }
+      const uint4 res = ll128_fold(s, n);
+      if (publish) {
+        char* dst = image_bytes(P, P.AG, epoch, it.dst) +
+                    (it.out_off + (uint64_t)r * kLL128RowLines) * kLL128LineBytes;
+        ll128_store_row<kConc>(dst, res, lane, nl, epoch);
+      } else {
+        const int64_t left = (int64_t)it.nelems - (int64_t)r * kRowElems;
+        ll128_write_payload(P.out[it.dst] + it.out_off + (uint64_t)r * kRowElems, res, lane,
+                            left);
+      }
     }
-    if (publish) {
-      char* dst = image_bytes(P, P.AG, epoch, it.dst) +
-                  (it.out_off + (uint64_t)r * kLL128RowLines) * kLL128LineBytes;
-      ll128_store_row<kConc>(dst, res, lane, nl, epoch);
+    return;
+  }
+  // copy
+  const char* src = image_bytes(P, R, epoch, it.src) + it.src_line * kLL128LineBytes;
+  for (uint32_t r0 = warp; r0 < nrows; r0 += nwarps * kRowsInFlight) {
+    uint4 v[kRowsInFlight];
+    int nls[kRowsInFlight];
+    if (!kConc) {
+#pragma unroll
+      for (int j = 0; j < kRowsInFlight; ++j) {
+        const uint32_t r = r0 + j * nwarps;
+        nls[j] = r < nrows ? min((int)kLL128RowLines, (int)(it.nlines - r * kLL128RowLines)) : 0;
+        v[j] = li < nls[j] ? ld_v4(src + (size_t)r * kRowBytes + 16 * lane)
+                           : make_uint4(0, 0, 0, 0);
+      }
+      bool ready = true;
+#pragma unroll
+      for (int j = 0; j < kRowsInFlight; ++j)
+        ready = ready && ll128_chunk_ready(v[j], lane, li < nls[j], epoch);
+      if (!__all_sync(0xFFFFFFFFu, ready)) {
+#pragma unroll
+        for (int j = 0; j < kRowsInFlight; ++j) {
+          const uint32_t r = r0 + j * nwarps;
+          const bool rj = ll128_chunk_ready(v[j], lane, li < nls[j], epoch);
+          if (!__all_sync(0xFFFFFFFFu, rj)) {
+            const char* row = src + (size_t)r * kRowBytes;
+            if (!ll128_wait_chunk(P, row, lane, rj, epoch, it.src,
+                                  (int64_t)(it.src_line + r * kLL128RowLines)))
+              return;
+            if (li < nls[j]) v[j] = ld_v4(row + 16 * lane);
+          }
+        }
+      }
     } else {
-      ll128_write_payload(P.out[it.dst] + it.out_off + (uint64_t)r * kRowElems, res,
-                          lane, left);
+      const char* rows[kRowsInFlight];
+      uint32_t ranks[kRowsInFlight];
+      int64_t rls[kRowsInFlight];
+#pragma unroll
+      for (int j = 0; j < kRowsInFlight; ++j) {
+        const uint32_t r = r0 + j * nwarps;
+        nls[j] = r < nrows ? min((int)kLL128RowLines, (int)(it.nlines - r * kLL128RowLines)) : 0;
+        rows[j] = src + (size_t)(r < nrows ? r : 0) * kRowBytes;
+        ranks[j] = it.src;
+        rls[j] = (int64_t)(it.src_line + (uint64_t)r * kLL128RowLines);
+      }
+      if (!ll128_acquire_rows<kRowsInFlight>(P, rows, nls, kRowsInFlight, lane, epoch, ranks,
+                                             rls))
+        return;
+#pragma unroll
+      for (int j = 0; j < kRowsInFlight; ++j)
+        v[j] = li < nls[j] ? ld_relaxed_v4(rows[j] + 16 * lane) : make_uint4(0, 0, 0, 0);
+    }
+#pragma unroll
+    for (int j = 0; j < kRowsInFlight; ++j) {
+      const uint32_t r = r0 + j * nwarps;
+      if (r >= nrows) break;
+      if (publish) {
+        char* dst = image_bytes(P, P.AG, epoch, it.dst) +
+                    (it.out_off + (uint64_t)r * kLL128RowLines) * kLL128LineBytes;
+        ll128_store_row<kConc>(dst, v[j], lane, nls[j], epoch);
+      } else {
+        const int64_t left = (int64_t)it.nelems - (int64_t)r * kRowElems;
+        ll128_write_payload(P.out[it.dst] + it.out_off + (uint64_t)r * kRowElems, v[j], lane,
+                            left);
+      }
     }
   }
 }

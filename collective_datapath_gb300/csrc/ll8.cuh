@@ -63,16 +63,35 @@ __device__ __forceinline__ uint64_t* image_lines(const RunParams& P, const Regio
                                      (uint64_t)rank * R.rank_bytes);
 }
 
+// Groups a thread keeps in flight per step (stage and copy).
+constexpr int kGroupsInFlight = 4;
+
 // Encode one staging tile (nlines is a multiple of 4 for LL8).
 __device__ __forceinline__ void ll8_stage_tile(const RunParams& P, const StageItem& it,
                                                uint64_t epoch) {
   const uint16_t* in = P.in[it.rank] + it.in_elem;
   uint64_t* img = image_lines(P, P.P, epoch, it.rank) + it.dst_line;
+  // Deferred re-arm: the same lines of the other slot were consumed by the
+  // previous run, which has completed.
+  const bool deferred = P.reset_mode == kResetDeferred;
+  uint64_t* other = image_lines(P, P.P, epoch + 1, it.rank) + it.dst_line;
   const uint32_t flag = (uint32_t)epoch;
   const uint32_t ngroups = it.nlines / kLL8GroupLines;
-  for (uint32_t g = threadIdx.x; g < ngroups; g += blockDim.x) {
-    uint4 v = ld_stream_v4(in + 8 * (size_t)g);
-    ll8_store(img + 4 * (size_t)g, v, flag);
+  for (uint32_t g0 = threadIdx.x; g0 < ngroups; g0 += blockDim.x * kGroupsInFlight) {
+    uint4 v[kGroupsInFlight];
+#pragma unroll
+    for (int j = 0; j < kGroupsInFlight; ++j) {
+      const uint32_t g = g0 + j * blockDim.x;
+      if (g < ngroups) v[j] = ld_stream_v4(in + 8 * (size_t)g);
+    }
+#pragma unroll
+    for (int j = 0; j < kGroupsInFlight; ++j) {
+      const uint32_t g = g0 + j * blockDim.x;
+      if (g < ngroups) {
+        ll8_store(img + 4 * (size_t)g, v[j], flag);
+        if (deferred) ll8_rearm(other + 4 * (size_t)g);
+      }
+    }
   }
 }
 
@@ -111,7 +130,9 @@ __device__ __forceinline__ uint4 ll8_fold(const LL8Group* s, int n) {
 }
 
 // Process one consume item: validate + unpack (+ fold) + write (+ re-arm).
-// `R` is the source region (P for phase 1, AG for twoshot phase 2).
+// `R` is the source region (P for phase 1, AG for twoshot phase 2).  A fold
+// loads the group of all n images before it checks them; a copy loads
+// kGroupsInFlight groups before it checks them.
 __device__ __forceinline__ void ll8_consume_item(const RunParams& P, const Region& R,
                                                  const Item& it, uint64_t epoch) {
   const uint32_t flag = (uint32_t)epoch;
@@ -119,12 +140,12 @@ __device__ __forceinline__ void ll8_consume_item(const RunParams& P, const Regio
   const uint32_t ngroups = it.nlines / kLL8GroupLines;
   const bool reduce = it.kind == IK_REDUCE;
   const bool publish = (it.flags & IF_PUBLISH) != 0;
-  const bool sole = (it.flags & IF_RESET_SOLE) != 0 && P.reset_mode == 0;
+  const bool sole = (it.flags & IF_RESET_SOLE) != 0 && P.reset_mode == kResetLastReader;
+  const bool deferred = P.reset_mode == kResetDeferred;
   bool ok = true;
-  for (uint32_t g = threadIdx.x; g < ngroups; g += blockDim.x) {
-    const uint64_t line = it.src_line + 4 * (uint64_t)g;
-    uint4 res;
-    if (reduce) {
+  if (reduce) {
+    for (uint32_t g = threadIdx.x; g < ngroups && ok; g += blockDim.x) {
+      const uint64_t line = it.src_line + 4 * (uint64_t)g;
       LL8Group s[kMaxRanks];
 #pragma unroll
       for (int p = 0; p < kMaxRanks; ++p)
@@ -136,32 +157,60 @@ __device__ __forceinline__ void ll8_consume_item(const RunParams& P, const Regio
           ok = ok && ll8_wait(P, src, flag, p, (int64_t)line);
           ll8_load(src, s[p]);
         }
-      res = ll8_fold(s, n);
+      if (!ok) break;
+      const uint4 res = ll8_fold(s, n);
       if (sole) {
 #pragma unroll
         for (int p = 0; p < kMaxRanks; ++p)
           if (p < n) ll8_rearm(image_lines(P, R, epoch, p) + line);
       }
-    } else {
-      LL8Group s;
-      uint64_t* src = image_lines(P, R, epoch, it.src) + line;
-      ll8_load(src, s);
-      if (!ll8_ready(s, flag)) {
-        ok = ok && ll8_wait(P, src, flag, it.src, (int64_t)line);
-        ll8_load(src, s);
+      if (publish) {
+        ll8_store(image_lines(P, P.AG, epoch, it.dst) + it.out_off + 4 * (uint64_t)g, res,
+                  flag);
+        if (deferred)
+          ll8_rearm(image_lines(P, P.AG, epoch + 1, it.dst) + it.out_off + 4 * (uint64_t)g);
+      } else {
+        st_v4(P.out[it.dst] + it.out_off + 8 * (uint64_t)g, res);
       }
-      res = make_uint4((uint32_t)s.l0, (uint32_t)s.l1, (uint32_t)s.l2, (uint32_t)s.l3);
-      if (sole) ll8_rearm(src);
     }
-    if (!ok) break;
-    if (publish) {
-      ll8_store(image_lines(P, P.AG, epoch, it.dst) + it.out_off + 4 * (uint64_t)g, res,
-                flag);
-    } else {
-      st_v4(P.out[it.dst] + it.out_off + 8 * (uint64_t)g, res);
+  } else {
+    uint64_t* src0 = image_lines(P, R, epoch, it.src) + it.src_line;
+    for (uint32_t g0 = threadIdx.x; g0 < ngroups && ok; g0 += blockDim.x * kGroupsInFlight) {
+      LL8Group s[kGroupsInFlight];
+#pragma unroll
+      for (int j = 0; j < kGroupsInFlight; ++j) {
+        const uint32_t g = g0 + j * blockDim.x;
+        if (g < ngroups) ll8_load(src0 + 4 * (size_t)g, s[j]);
+      }
+#pragma unroll
+      for (int j = 0; j < kGroupsInFlight; ++j) {
+        const uint32_t g = g0 + j * blockDim.x;
+        if (g < ngroups && !ll8_ready(s[j], flag)) {
+          ok = ok && ll8_wait(P, src0 + 4 * (size_t)g, flag, it.src,
+                              (int64_t)(it.src_line + 4 * (uint64_t)g));
+          ll8_load(src0 + 4 * (size_t)g, s[j]);
+        }
+      }
+      if (!ok) break;
+#pragma unroll
+      for (int j = 0; j < kGroupsInFlight; ++j) {
+        const uint32_t g = g0 + j * blockDim.x;
+        if (g >= ngroups) break;
+        const uint4 res =
+            make_uint4((uint32_t)s[j].l0, (uint32_t)s[j].l1, (uint32_t)s[j].l2, (uint32_t)s[j].l3);
+        if (sole) ll8_rearm(src0 + 4 * (size_t)g);
+        if (publish) {
+          ll8_store(image_lines(P, P.AG, epoch, it.dst) + it.out_off + 4 * (uint64_t)g, res,
+                    flag);
+          if (deferred)
+            ll8_rearm(image_lines(P, P.AG, epoch + 1, it.dst) + it.out_off + 4 * (uint64_t)g);
+        } else {
+          st_v4(P.out[it.dst] + it.out_off + 8 * (uint64_t)g, res);
+        }
+      }
     }
   }
-  if ((it.flags & IF_RESET_COUNTED) && P.reset_mode == 0) {
+  if ((it.flags & IF_RESET_COUNTED) && P.reset_mode == kResetLastReader) {
     // The last of `readers` items over these lines re-arms them.
     __shared__ uint32_t last;
     __syncthreads();

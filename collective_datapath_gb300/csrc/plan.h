@@ -70,9 +70,8 @@ struct WsHeader {
   uint32_t status_rank;
   int64_t status_line;
   uint32_t abort;          // nonzero after an error: waits give up at once
-  uint32_t done_ctas;      // last-CTA counter of the run's final kernel
-  uint32_t started;        // fused late runs: consumer CTAs that started
-  uint32_t pad0;
+  uint32_t arrived;        // CTAs of the run's final launch that read the epoch
+  uint32_t started[2];     // fused runs: worker CTAs that started, by slot
   uint64_t rejections;     // stale lines observed (diagnostic)
   uint64_t pad1[26];
 };
@@ -92,7 +91,7 @@ struct RunParams {
   uint16_t* out[kMaxRanks];       // rank outputs
   int nranks;
   int enc;
-  int reset_mode;                 // COLL_RESET_*
+  int reset_mode;                 // COLL_RESET_* (LL8 only; LL128 needs none)
   int ctas_per_rank;              // fused path: CTAs bound to each rank
   uint64_t timeout_ns;
   Region P;                       // rank images written by stage
@@ -111,6 +110,7 @@ struct RunParams {
   uint64_t seg_line0[kMaxRanks];
   uint64_t seg_elems[kMaxRanks];
   uint64_t seg_in0[kMaxRanks];
+  int interleave1, interleave2;   // streamed consume walks ranks interleaved
   int stage_rank;                 // streamed stage of one rank, -1 = all
   int advance_epoch;              // this launch ends the run
   // late producers (fault-injection runs)

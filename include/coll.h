@@ -108,11 +108,19 @@ enum { COLL_LL8 = 0, COLL_LL128 = 1 };
  * allGather>; SiFAR §3.1; flash-comm §4.3 (one-hop / sharded two-hop). */
 enum { COLL_ALGO_AUTO = 0, COLL_ONESHOT = 1, COLL_TWOSHOT = 2 };
 
-/* Flag re-arm (LL8 only; LL128 lines need none): after every reader of a
- * line consumed it, its flag word is set back to 0 -- by the last reader
- * (FUSED), by a separate kernel at the end of the run (KERNEL), or never
- * (NONE).  flash-comm §3.1 / Table 2 (checking and re-arming). */
-enum { COLL_RESET_FUSED = 0, COLL_RESET_KERNEL = 1, COLL_RESET_NONE = 2 };
+/* Flag re-arm (LL8 only; LL128 sequence numbers need none, flash-comm §3.1
+ * Table 2): after every reader of a line consumed it, its flag word is set
+ * back to 0 --
+ *   FUSED:    by the last reader, counted per tile inside the consume kernel;
+ *   KERNEL:   by a separate kernel at the end of the run;
+ *   DEFERRED: (default) by the owning rank during the next epoch, in the slot
+ *             that epoch does not use: the completed previous run is the
+ *             evidence that every reader consumed it (the dual-buffering
+ *             argument of SiFAR §3.3), so no counter or barrier is needed;
+ *   NONE:     never (flags are epoch values, so a stale line never matches).
+ */
+enum { COLL_RESET_FUSED = 0, COLL_RESET_KERNEL = 1, COLL_RESET_NONE = 2,
+       COLL_RESET_DEFERRED = 3 };
 
 /* Launch path: FUSED = stage and consume inside one cooperative kernel
  * (all CTAs co-resident; a CTA serves one emulated rank); STREAMED =
@@ -123,7 +131,7 @@ enum { COLL_PATH_AUTO = 0, COLL_PATH_FUSED = 1, COLL_PATH_STREAMED = 2 };
 typedef struct {
     int encoding;        /* COLL_LL8 | COLL_LL128 (default LL8) */
     int algorithm;       /* COLL_ALGO_AUTO | COLL_ONESHOT | COLL_TWOSHOT */
-    int reset_mode;      /* COLL_RESET_* (default FUSED) */
+    int reset_mode;      /* COLL_RESET_* (default DEFERRED) */
     int path;            /* COLL_PATH_* (default AUTO) */
     int ctas;            /* CTAs of the consume grid, 0 = auto */
     int tile_lines;      /* lines per work item, 0 = auto */

@@ -126,16 +126,22 @@ def test_staged_lines_match_the_oracle_encoding(cd, enc):
 
 
 @pytest.mark.parametrize("algo", [1, 2])
-@pytest.mark.parametrize("reset", [0, 1])
+@pytest.mark.parametrize("reset", [0, 1, 3])
 @pytest.mark.parametrize("path", [1, 2])
 def test_flags_rearmed_after_run(cd, algo, reset, path):
-    """LL8: after a run every flag word of the slot it used is 0."""
+    """LL8 re-arm: every flag word of a consumed slot is 0 afterwards -- the
+    slot of the run itself for the last-reader (0) and kernel (1) modes; for
+    the deferred mode (3) the slot of the previous run, re-armed while the
+    next run uses the other slot."""
     n, count = 8, 8 * 512
     coll = make(cd, cd.ALLREDUCE, n, count, encoding=0, algorithm=algo,
                 reset_mode=reset, path=path)
     xs, ins, outs = buffers(coll, n, seed=6)
-    coll.run(ins, outs)
+    coll.run(ins, outs)                      # epoch 1 -> slot 1
     check(coll, outs, oracle.allreduce(xs), n)
+    if reset == 3:
+        coll.run(ins, outs)                  # epoch 2 -> slot 0, re-arms slot 1
+        check(coll, outs, oracle.allreduce(xs), n)
     regions = (0, 1) if algo == 2 else (0,)
     for region in regions:
         for r in range(n):
@@ -143,6 +149,10 @@ def test_flags_rearmed_after_run(cd, algo, reset, path):
                 raw, lines, lb = read_lines(coll, region, 1, r, k)
                 flags = raw.view(np.uint32)[1::2]
                 assert np.all(flags == 0), f"region {region} rank {r} seg {k}"
+    if reset == 3:
+        # the slot in use still carries this run's flags until the next run
+        raw, _, _ = read_lines(coll, 0, 0, 0, 0)
+        assert np.all(raw.view(np.uint32)[1::2] == 2)
 
 
 @pytest.mark.parametrize("enc", [0, 1])
