@@ -114,6 +114,30 @@ cudaError_t launched(coll_spec* s, cudaError_t e, cudaStream_t st) {
   return cudaSuccess;
 }
 
+// One stream-ordered consume phase: LL128 phases made only of folds or only
+// of plain-output copies run through the shared-memory pipelines; anything
+// else through the generic consume kernel.
+cudaError_t launch_phase(const Plan& p, const RunParams& P, int phase,
+                         const std::vector<Item>& items, cudaStream_t st) {
+  if (p.enc == ENC_LL128 && !items.empty()) {
+    bool all_fold = true, all_copy = true;
+    for (const Item& it : items) {
+      all_fold = all_fold && it.kind == IK_REDUCE;
+      all_copy = all_copy && it.kind == IK_COPY && !(it.flags & IF_PUBLISH);
+    }
+    if (all_fold && phase == 1)
+      return launch_fold(P, std::min<int>((int)items.size(), device_sms() * 2), st);
+    if (all_copy)
+      return launch_copy(P, phase, std::min<int>((int)items.size(), device_sms() * 4), st);
+  }
+  return launch_consume(P, phase, p.consume_grid, st);
+}
+
+cudaError_t launch_stager(const Plan& p, const RunParams& P, int items, cudaStream_t st) {
+  if (p.enc == ENC_LL128) return launch_stage_pipe(P, std::min(items, device_sms() * 4), st);
+  return launch_stage(P, std::min(items, device_sms() * 8), st);
+}
+
 // Consume phase(s) of a run whose inputs are staged; the last launch
 // advances the epoch.
 coll_status_t launch_consumers(coll_spec* s, RunParams P, cudaStream_t st) {
@@ -125,17 +149,11 @@ coll_status_t launch_consumers(coll_spec* s, RunParams P, cudaStream_t st) {
     if (cudaError_t e = launched(s, launch_advance(P, st), st)) return cuda_status(e);
   } else {
     P.advance_epoch = !two && !rearm_kernel;
-    bool all_fold = p.enc == ENC_LL128 && !p.items1.empty();
-    for (const Item& it : p.items1) all_fold = all_fold && it.kind == IK_REDUCE;
-    if (all_fold) {
-      const int grid = std::min<int>((int)p.items1.size(), device_sms() * 2);
-      if (cudaError_t e = launched(s, launch_fold(P, grid, st), st)) return cuda_status(e);
-    } else if (cudaError_t e = launched(s, launch_consume(P, 1, p.consume_grid, st), st)) {
+    if (cudaError_t e = launched(s, launch_phase(p, P, 1, p.items1, st), st))
       return cuda_status(e);
-    }
     if (two) {
       P.advance_epoch = !rearm_kernel;
-      if (cudaError_t e = launched(s, launch_consume(P, 2, p.consume_grid, st), st))
+      if (cudaError_t e = launched(s, launch_phase(p, P, 2, p.items2, st), st))
         return cuda_status(e);
     }
   }
@@ -266,8 +284,7 @@ coll_status_t coll_stage(coll_spec_t* s, int rank, const void* dev_in,
   P.in[rank] = static_cast<const uint16_t*>(dev_in);
   P.stage_rank = rank;
   const int items = P.sbeg[rank + 1] - P.sbeg[rank];
-  const int grid = std::min(items, device_sms() * 8);
-  return cuda_status(launch_stage(P, grid, as_stream(stream)));
+  return cuda_status(launch_stager(s->plan, P, items, as_stream(stream)));
 }
 
 coll_status_t coll_run(coll_spec_t* s, const void* const* dev_ins, void* const* dev_outs,
@@ -293,8 +310,8 @@ coll_status_t coll_run(coll_spec_t* s, const void* const* dev_ins, void* const* 
   }
   if (dev_ins != nullptr && !p.sitems.empty()) {
     P.stage_rank = -1;
-    const int grid = std::min((int)p.sitems.size(), device_sms() * 8);
-    if (cudaError_t e = launched(s, launch_stage(P, grid, st), st)) return cuda_status(e);
+    if (cudaError_t e = launched(s, launch_stager(p, P, (int)p.sitems.size(), st), st))
+      return cuda_status(e);
   }
   return launch_consumers(s, P, st);
 }

@@ -158,8 +158,13 @@ struct Waiter {
   }
 };
 
+// One atomic per warp for the stale lines its active lanes observed.
 __device__ __forceinline__ void count_rejection(char* ws) {
-  atomicAdd(reinterpret_cast<unsigned long long*>(&header(ws)->rejections), 1ull);
+  const unsigned mask = __activemask();
+  const int leader = __ffs(mask) - 1;
+  if ((int)(threadIdx.x & 31) == leader)
+    atomicAdd(reinterpret_cast<unsigned long long*>(&header(ws)->rejections),
+              (unsigned long long)__popc(mask));
 }
 
 // Epoch protocol of a launch.  Thread 0 reads the device epoch once and

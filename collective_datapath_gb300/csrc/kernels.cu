@@ -175,6 +175,145 @@ __global__ void __launch_bounds__(kThreads, 2) k_fold_ll128(RunParams P) {
   finish_run(P, e);
 }
 
+// ---- LL128 copy and stage through cp.async rings --------------------------------
+// Copy (all-gather, all-to-all, twoshot phase 2): each warp keeps kCopyStages
+// source rows (512 bytes of lines) in flight in shared memory; after a row
+// lands the warp validates its sequence numbers and every lane q < 30 gathers
+// the two 8-byte payload granules of output chunk q straight from shared
+// memory (payload granule G of a row sits in line G / 15 at byte 8 (G % 15)).
+// Stage: the same ring holds input rows (480 payload bytes); lane L gathers
+// the granules of its line chunk and adds the sequence number.
+constexpr int kCopyStages = 8;
+
+size_t copy_smem_bytes() { return (size_t)(kThreads / 32) * kCopyStages * kRowBytes; }
+
+__device__ __forceinline__ uint2 lds_v2(uint32_t saddr) {
+  uint2 v;
+  asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(saddr) : "memory");
+  return v;
+}
+__device__ __forceinline__ void sts_v4(uint32_t saddr, uint4 v) {
+  asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(saddr), "r"(v.x), "r"(v.y),
+               "r"(v.z), "r"(v.w)
+               : "memory");
+}
+__device__ __forceinline__ uint64_t lds_u64(uint32_t saddr) {
+  uint64_t v;
+  asm volatile("ld.shared.u64 %0, [%1];" : "=l"(v) : "r"(saddr) : "memory");
+  return v;
+}
+
+__global__ void __launch_bounds__(kThreads, 4) k_copy_ll128(RunParams P, int phase) {
+  extern __shared__ __align__(128) char smem[];
+  const uint64_t e = begin_run(P);
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
+  const int li = lane >> 3;
+  const Item* items = phase == 1 ? P.items1 : P.items2;
+  const int* beg = phase == 1 ? P.beg1 : P.beg2;
+  const bool inter = phase == 1 ? P.interleave1 : P.interleave2;
+  const Region& R = phase == 1 ? P.P : P.AG;
+  const int n_items = beg[P.nranks];
+  const uint32_t wbase =
+      (uint32_t)__cvta_generic_to_shared(smem) + (uint32_t)(warp * kCopyStages * kRowBytes);
+  // output chunk q = lane: its two granules
+  const int q = lane < 30 ? lane : 29;
+  const uint32_t g0off = 128 * ((2 * q) / 15) + 8 * ((2 * q) % 15);
+  const uint32_t g1off = 128 * ((2 * q + 1) / 15) + 8 * ((2 * q + 1) % 15);
+  for (int v = blockIdx.x; v < n_items; v += gridDim.x) {
+    if (aborted(P.ws)) break;
+    const int i = inter ? beg[v % P.nranks] + v / P.nranks : v;
+    const Item it = items[i];
+    const char* src = image_bytes(P, R, e, it.src) + it.src_line * kLL128LineBytes;
+    const uint32_t nrows = (it.nlines + kLL128RowLines - 1) / kLL128RowLines;
+    const int nj = (uint32_t)warp < nrows ? (int)((nrows - warp + nwarps - 1) / nwarps) : 0;
+    auto issue = [&](int j) {
+      if (j < nj) {
+        const uint32_t r = warp + j * nwarps;
+        const int nl = min((int)kLL128RowLines, (int)(it.nlines - r * kLL128RowLines));
+        cp_async16(wbase + (j % kCopyStages) * kRowBytes + 16 * lane,
+                   src + (size_t)r * kRowBytes + 16 * lane, li < nl);
+      }
+      cp_async_commit();
+    };
+#pragma unroll
+    for (int j = 0; j < kCopyStages; ++j) issue(j);
+    for (int j = 0; j < nj; ++j) {
+      cp_async_wait<kCopyStages - 1>();
+      __syncwarp();
+      const uint32_t row = wbase + (j % kCopyStages) * kRowBytes;
+      const uint32_t r = warp + j * nwarps;
+      const int nl = min((int)kLL128RowLines, (int)(it.nlines - r * kLL128RowLines));
+      const bool valid = li < nl;
+      const bool ready = !(valid && (lane & 7) == 7) || lds_u64(row + 16 * lane + 8) == e;
+      if (!__all_sync(0xFFFFFFFFu, ready)) {
+        const char* grow = src + (size_t)r * kRowBytes;
+        if (!ll128_wait_chunk(P, grow, lane, ready, e, it.src,
+                              (int64_t)(it.src_line + r * kLL128RowLines)))
+          break;
+        if (valid) sts_v4(row + 16 * lane, ld_v4(grow + 16 * lane));
+        __syncwarp();
+      }
+      const uint2 a = lds_v2(row + g0off), b = lds_v2(row + g1off);
+      __syncwarp();  // every lane read the slot before it is refilled
+      issue(j + kCopyStages);
+      const int64_t left = (int64_t)it.nelems - (int64_t)r * kRowElems;
+      if (lane < 30 && 8 * lane < left)
+        st_v4(P.out[it.dst] + it.out_off + (uint64_t)r * kRowElems + 8 * lane,
+              make_uint4(a.x, a.y, b.x, b.y));
+    }
+    cp_async_wait<0>();
+    __syncwarp();
+  }
+  finish_run(P, e);
+}
+
+__global__ void __launch_bounds__(kThreads, 4) k_stage_ll128(RunParams P) {
+  extern __shared__ __align__(128) char smem[];
+  const uint64_t e = begin_run(P);
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
+  const int li = lane >> 3, k = lane & 7;
+  const int lo = P.stage_rank < 0 ? 0 : P.stage_rank;
+  const int hi = P.stage_rank < 0 ? P.nranks : P.stage_rank + 1;
+  const uint32_t wbase =
+      (uint32_t)__cvta_generic_to_shared(smem) + (uint32_t)(warp * kCopyStages * kRowBytes);
+  const int G = 15 * li + 2 * k;  // first payload granule of this lane's line chunk
+  for (int v = P.sbeg[lo] + blockIdx.x; v < P.sbeg[hi]; v += gridDim.x) {
+    const StageItem it = P.sitems[v];
+    const uint16_t* in = P.in[it.rank] + it.in_elem;
+    char* img = image_bytes(P, P.P, e, it.rank) + it.dst_line * kLL128LineBytes;
+    const uint32_t nrows = (it.nlines + kLL128RowLines - 1) / kLL128RowLines;
+    const int nj = (uint32_t)warp < nrows ? (int)((nrows - warp + nwarps - 1) / nwarps) : 0;
+    auto issue = [&](int j) {
+      if (j < nj) {
+        const uint32_t r = warp + j * nwarps;
+        const int64_t left = (int64_t)it.nelems - (int64_t)r * kRowElems;
+        const bool valid = lane < 30 && 8 * lane < left;
+        cp_async16(wbase + (j % kCopyStages) * kRowBytes + 16 * lane,
+                   in + (size_t)r * kRowElems + (valid ? 8 * lane : 0), valid);
+      }
+      cp_async_commit();
+    };
+#pragma unroll
+    for (int j = 0; j < kCopyStages; ++j) issue(j);
+    for (int j = 0; j < nj; ++j) {
+      cp_async_wait<kCopyStages - 1>();
+      __syncwarp();
+      const uint32_t row = wbase + (j % kCopyStages) * kRowBytes;
+      // lanes 30, 31 hold no input: their slot bytes [480, 512) stay unread
+      const uint2 a = lds_v2(row + 8 * G);
+      const uint2 b = k == 7 ? make_uint2(0, 0) : lds_v2(row + 8 * (G + 1));
+      __syncwarp();
+      issue(j + kCopyStages);
+      const uint32_t r = warp + j * nwarps;
+      const int nl = min((int)kLL128RowLines, (int)(it.nlines - r * kLL128RowLines));
+      ll128_store_row<false>(img + (size_t)r * kRowBytes, make_uint4(a.x, a.y, b.x, b.y), lane,
+                             nl, e);
+    }
+    cp_async_wait<0>();
+    __syncwarp();
+  }
+}
+
 // Late producer: publish rank p's withheld lines in the given order, after
 // every consumer CTA has started polling.  One warp publishes, in order.
 template <int ENC>
@@ -400,6 +539,17 @@ cudaError_t launch_fold(const RunParams& P, int grid, cudaStream_t s) {
     configured = fold_smem_bytes(kMaxRanks);
   }
   k_fold_ll128<<<grid, kThreads, bytes, s>>>(P);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_copy(const RunParams& P, int phase, int grid, cudaStream_t s) {
+  k_copy_ll128<<<grid, kThreads, copy_smem_bytes(), s>>>(P, phase);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_stage_pipe(const RunParams& P, int grid, cudaStream_t s) {
+  if (grid <= 0) return cudaSuccess;
+  k_stage_ll128<<<grid, kThreads, copy_smem_bytes(), s>>>(P);
   return cudaGetLastError();
 }
 

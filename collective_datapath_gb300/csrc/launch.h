@@ -17,6 +17,10 @@ cudaError_t launch_consume(const RunParams& P, int phase, int grid, cudaStream_t
 cudaError_t launch_fused(const RunParams& P, int grid, cudaStream_t s);
 // LL128 phase-1 folds through the shared-memory pipeline (all items IK_REDUCE).
 cudaError_t launch_fold(const RunParams& P, int grid, cudaStream_t s);
+// LL128 copy phases (all items IK_COPY, plain outputs) and LL128 staging
+// through cp.async shared-memory rings.
+cudaError_t launch_copy(const RunParams& P, int phase, int grid, cudaStream_t s);
+cudaError_t launch_stage_pipe(const RunParams& P, int grid, cudaStream_t s);
 cudaError_t launch_withhold(const RunParams& P, cudaStream_t s);
 cudaError_t launch_rearm(const RunParams& P, int grid, cudaStream_t s);
 cudaError_t launch_advance(const RunParams& P, cudaStream_t s);
