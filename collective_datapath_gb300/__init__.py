@@ -41,8 +41,8 @@ EXPORTS = [
     "coll_run_host", "coll_get_counts", "coll_query_status", "coll_get_epoch",
     "coll_staging_layout", "coll_stage_withheld", "coll_run_late",
     "coll_get_rejections", "coll_debug_items", "coll_debug_plan",
-    "coll_set_profile_events", "coll_last_launches", "coll_destroy",
-    "coll_status_string",
+    "coll_set_profile_events", "coll_last_launches", "coll_allreduce_static",
+    "coll_destroy", "coll_status_string",
 ]
 
 
@@ -93,6 +93,7 @@ _sig("coll_debug_plan", _st, _vp, _P(ctypes.c_int), _P(ctypes.c_int),
      _P(ctypes.c_int), _P(ctypes.c_int))
 _sig("coll_set_profile_events", _st, _vp, _P(_vp), ctypes.c_int)
 _sig("coll_last_launches", _st, _vp, _P(ctypes.c_int))
+_sig("coll_allreduce_static", _st, ctypes.c_int, _sz, _P(_vp), _P(_vp), _vp)
 _sig("coll_destroy", _st, _vp)
 _sig("coll_status_string", ctypes.c_char_p, ctypes.c_int)
 
@@ -289,6 +290,12 @@ def coll_last_launches(spec: int) -> int:
     n = ctypes.c_int()
     _check(_lib.coll_last_launches(spec, ctypes.byref(n)), "coll_last_launches")
     return n.value
+
+
+def coll_allreduce_static(ins: Sequence, outs: Sequence, count: int, stream=None) -> None:
+    """All-reduce in the library's fixed scratch (no workspace, no allocation)."""
+    _check(_lib.coll_allreduce_static(len(ins), count, _ptr_array(ins), _ptr_array(outs),
+                                      _stream_handle(stream)), "coll_allreduce_static")
 
 
 def coll_destroy(spec: int) -> None:

@@ -129,7 +129,7 @@ __device__ __forceinline__ WsHeader* header(char* ws) {
 
 // Latch the first device error (later ones are dropped) and raise `abort`
 // so that every other wait of the run gives up promptly.
-__device__ __noinline__ void latch_error(char* ws, uint32_t code, uint32_t rank,
+static __device__ __noinline__ void latch_error(char* ws, uint32_t code, uint32_t rank,
                                          int64_t line) {
   WsHeader* h = header(ws);
   if (atomicCAS(&h->status_code, 0u, code) == 0u) {

@@ -112,7 +112,7 @@ __device__ __forceinline__ void ll128_store_row(char* row, uint4 ln, int lane, i
 }
 
 // Bounded wait for the sequence number at `p` (a lane with k = 7).
-__device__ __noinline__ bool ll128_wait_seq(const RunParams& P, const char* p,
+static __device__ __noinline__ bool ll128_wait_seq(const RunParams& P, const char* p,
                                             uint64_t seq, uint32_t rank, int64_t line) {
   count_rejection(P.ws);
   Waiter w;
@@ -167,7 +167,7 @@ __device__ __forceinline__ bool ll128_chunk_ready(const uint4& v, int lane, bool
 // Stream-ordered slow path: a chunk loaded optimistically did not carry the
 // epoch.  The lane waits (bounded) for the number and fences; the caller
 // reloads the chunk when every lane of the warp succeeded.  Warp-collective.
-__device__ __noinline__ bool ll128_wait_chunk(const RunParams& P, const char* row, int lane,
+static __device__ __noinline__ bool ll128_wait_chunk(const RunParams& P, const char* row, int lane,
                                               bool ready, uint64_t seq, uint32_t rank,
                                               int64_t row_line) {
   bool ok = true;

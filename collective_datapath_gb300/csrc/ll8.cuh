@@ -41,7 +41,7 @@ __device__ __forceinline__ void ll8_rearm(uint64_t* p) {
 
 // Poll a group until every line carries `flag` (bounded); the caller then
 // reloads it.  Returns false on timeout or abort (the error is latched).
-__device__ __noinline__ bool ll8_wait(const RunParams& P, const uint64_t* p, uint32_t flag,
+static __device__ __noinline__ bool ll8_wait(const RunParams& P, const uint64_t* p, uint32_t flag,
                                       uint32_t rank, int64_t line) {
   count_rejection(P.ws);
   Waiter w;

@@ -288,6 +288,33 @@ coll_status_t coll_set_profile_events(coll_spec_t *spec, void *const *events, in
 /* Number of kernel launches the last coll_run issued. */
 coll_status_t coll_last_launches(const coll_spec_t *spec, int *launches);
 
+/* All-reduce without any allocation.  The pages have no counterpart: this is
+ * an entry point for callers that cannot allocate device memory when they
+ * need the collective -- code running under a stream capture that must not
+ * allocate, inside an allocator's own callback, or in a process whose device
+ * memory another runtime has fully reserved -- and so cannot provide the
+ * workspace that coll_bind takes.
+ * It runs the oneshot LL8 all-reduce (stage, validate, fold in rank order
+ * 0..nranks-1 in fp32, one rounding to bf16) of nranks buffers of `count`
+ * bf16 each into nranks outputs, like coll_run on an (SCATTERED, SCATTERED,
+ * REDUCE) spec with COLL_LL8 and COLL_ONESHOT, and gives the same bytes.
+ * Its scratch is a fixed array inside the library (8 MiB + 4 KiB), held by
+ * every GPU that loads the library until the process exits:
+ *   - nranks * count must not exceed 1,048,576 elements: larger requests
+ *     return COLL_ERR_NOMEM and enqueue nothing; count % 8 != 0 returns
+ *     COLL_ERR_ALIGN; count == 0 does nothing;
+ *   - the first call on a device sets that device up (looks up the scratch
+ *     address, clears its header, sets the first epoch) with blocking CUDA
+ *     calls, so make it before any stream capture that includes this call;
+ *   - every call on a device shares the one scratch array, which keeps the
+ *     previous call's contents; calls that overlap on the GPU (other streams,
+ *     other host threads) race and give undefined outputs;
+ *   - a device-side wait that exceeds its bound (200 ms) leaves the outputs
+ *     undefined; this entry point reports only host-side errors.
+ * It calls no cudaMalloc, cudaFree or other allocating routine. */
+coll_status_t coll_allreduce_static(int nranks, size_t count, const void *const *dev_ins,
+                                    void *const *dev_outs, coll_stream_t stream);
+
 /* Release the spec's host state (never the caller's device memory). */
 coll_status_t coll_destroy(coll_spec_t *spec);
 
