@@ -92,6 +92,10 @@ def _declare(L: ctypes.CDLL) -> None:
                                    ctypes.POINTER(_u16p),
                                    ctypes.POINTER(_u16p), _i32p, _i64p]
     L.orc_moe_dispatch.restype = ctypes.c_int
+    L.orc_moe_row_sources.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                      ctypes.c_int, ctypes.POINTER(_i32p),
+                                      ctypes.c_int, _i32p, _i32p]
+    L.orc_moe_row_sources.restype = ctypes.c_int64
     L.orc_ll8_lines.argtypes = [_sz]
     L.orc_ll8_lines.restype = _sz
     L.orc_ll8_encode.argtypes = [_u16p, _sz, ctypes.c_uint64, _u64p]
@@ -241,6 +245,21 @@ def moe_dispatch(ins: Sequence[np.ndarray], topk: Sequence[np.ndarray],
     if outs is not None:
         outs = [o[:rows[d]] for d, o in enumerate(outs)]
     return outs, counts, rows
+
+
+def moe_row_sources(topk: Sequence[np.ndarray], experts: int, d: int):
+    """(src_rank, src_token) int32 arrays of destination d's output rows."""
+    n = len(topk)
+    tokens, k = np.asarray(topk[0]).shape
+    tks = [_c(t, np.int32) for t in topk]
+    cap = tokens * n * min(k, experts // n)
+    sr = np.zeros(max(cap, 1), dtype=np.int32)
+    st = np.zeros(max(cap, 1), dtype=np.int32)
+    rows = lib().orc_moe_row_sources(n, tokens, k, experts, _ptr_array(tks, ctypes.c_int32),
+                                     d, _ptr(sr, ctypes.c_int32), _ptr(st, ctypes.c_int32))
+    if rows < 0:
+        raise ValueError("orc_moe_row_sources: invalid arguments")
+    return sr[:rows], st[:rows]
 
 
 # ---- encodings ---------------------------------------------------------------

@@ -202,6 +202,29 @@ int orc_moe_dispatch(int n, int tokens, int hidden, int k, int experts,
     return 0;
 }
 
+int64_t orc_moe_row_sources(int n, int tokens, int k, int experts,
+                            const int32_t *const *topk, int d, int32_t *src_rank,
+                            int32_t *src_token)
+{
+    if (n < 1 || experts < n || experts % n != 0 || d < 0 || d >= n ||
+        topk == NULL || src_rank == NULL || src_token == NULL)
+        return -1;
+    int el = experts / n;
+    int64_t row = 0;
+    for (int le = 0; le < el; ++le) {
+        int e = d * el + le;
+        for (int p = 0; p < n; ++p)
+            for (int t = 0; t < tokens; ++t)
+                for (int j = 0; j < k; ++j)
+                    if (topk[p][(size_t)t * (size_t)k + (size_t)j] == e) {
+                        src_rank[row] = p;
+                        src_token[row] = t;
+                        row += 1;
+                    }
+    }
+    return row;
+}
+
 /* ---- readiness encodings ---------------------------------------------- */
 
 size_t orc_ll8_lines(size_t elems) { return (elems + 1u) / 2u; }

@@ -135,6 +135,15 @@ int orc_moe_dispatch(int n, int tokens, int hidden, int k, int experts,
                      const int32_t *const *topk, const uint16_t *const *in,
                      uint16_t *const *out, int32_t *counts, int64_t *out_rows);
 
+/* Source of every output row of destination d under the same definition as
+ * orc_moe_dispatch: src_rank[row], src_token[row] for row < rows (the
+ * return value), in the (local expert, source rank, token) order.  Lets a
+ * test check a full-size dispatch row by row without materialising it.
+ * Returns -1 on invalid arguments. */
+int64_t orc_moe_row_sources(int n, int tokens, int k, int experts,
+                            const int32_t *const *topk, int d, int32_t *src_rank,
+                            int32_t *src_token);
+
 /* ---- readiness encodings ---------------------------------------------- */
 /* LL8 line (8 bytes, a little-endian uint64):
  *   bits  0..15 = element 2j, bits 16..31 = element 2j+1 (0 past the end),

@@ -392,3 +392,25 @@ def test_moe_counts_and_rows_invariants(orc):
                     r += 1
         assert r == rows[d]
     assert len(seen) == n * tokens * k and set(seen.values()) == {1}
+
+
+def test_moe_row_sources_agree_with_the_materialised_dispatch(orc):
+    """The row-source listing names exactly the rows orc_moe_dispatch copies
+    (hand-derived tiny case, then a random case)."""
+    spec = json.load(open(os.path.join(GOLDEN, "moe_tiny.json")))
+    topk = [np.array(spec["topk"][str(p)], dtype=np.int32) for p in range(2)]
+    ins = [_bits(spec["rows"][str(p)]) for p in range(2)]
+    for d in range(2):
+        sr, st = orc.moe_row_sources(topk, spec["experts"], d)
+        want = _bits(spec["expected_out"][str(d)])
+        got = np.stack([ins[p][t] for p, t in zip(sr, st)])
+        assert np.array_equal(got, want)
+    n, tokens, hidden, k, experts = 4, 128, 16, 3, 16
+    ins = [synth.random_bits16(8, tokens * hidden, p).reshape(tokens, hidden)
+           for p in range(n)]
+    topk = [synth.topk_experts(8, tokens, k, experts, p) for p in range(n)]
+    outs, counts, rows = orc.moe_dispatch(ins, topk, experts)
+    for d in range(n):
+        sr, st = orc.moe_row_sources(topk, experts, d)
+        assert sr.size == rows[d]
+        assert np.array_equal(np.stack([ins[p][t] for p, t in zip(sr, st)]), outs[d])
