@@ -52,7 +52,7 @@ class coll_options_t(ctypes.Structure):
                 ("ctas", ctypes.c_int), ("tile_lines", ctypes.c_int),
                 ("timeout_ns", ctypes.c_uint64), ("tokens", ctypes.c_int),
                 ("hidden", ctypes.c_int), ("topk", ctypes.c_int),
-                ("experts", ctypes.c_int)]
+                ("experts", ctypes.c_int), ("max_rows", ctypes.c_int)]
 
 
 _vp = ctypes.c_void_p

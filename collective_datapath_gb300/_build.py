@@ -17,8 +17,9 @@ ROOT = os.path.dirname(HERE)
 BUILD_DIR = os.path.join(ROOT, "_build")
 LIB = os.path.join(HERE, "libcoll.so")
 
-SOURCES = ["kernels.cu", "api.cpp", "derive.cpp", "static_ws.cu"]
-HEADERS = ["plan.h", "derive.h", "launch.h", "dev_common.cuh", "ll8.cuh", "ll128.cuh"]
+SOURCES = ["kernels.cu", "api.cpp", "derive.cpp", "static_ws.cu", "moe.cu"]
+HEADERS = ["plan.h", "derive.h", "launch.h", "dev_common.cuh", "ll8.cuh", "ll128.cuh",
+           "pipe.cuh"]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 # No fast math: IEEE division/sqrt, no flush-to-zero (the fold is bit-exact).

@@ -20,6 +20,7 @@ struct coll_spec {
   RunParams base{};
   std::vector<cudaEvent_t> events;  // optional per-launch timing events
   int launches = 0;                 // launches of the current / last run
+  const int32_t* topk[kMaxRanks] = {};  // MoE routing per source rank
 };
 
 namespace {
@@ -80,6 +81,26 @@ void fill_base(coll_spec* s) {
   };
   P.interleave1 = equal_lists(p.beg1);
   P.interleave2 = equal_lists(p.beg2);
+  if (p.kind == CK_MOE) {
+    MoeParams& M = P.moe;
+    M.tokens = p.moe_tokens;
+    M.hidden = p.moe_hidden;
+    M.k = p.moe_k;
+    M.experts = p.moe_experts;
+    M.el = p.moe_el;
+    M.nblocks = p.moe_nblocks;
+    M.row_lines = p.moe_row_lines;
+    M.max_rows = p.moe_max_rows;
+    M.entry_rank = reinterpret_cast<uint32_t*>(s->ws + p.off_entry_rank);
+    M.block_off = reinterpret_cast<uint32_t*>(s->ws + p.off_block_off);
+    M.cnt = reinterpret_cast<uint32_t*>(s->ws + p.off_cnt);
+    M.stage_off = reinterpret_cast<uint32_t*>(s->ws + p.off_stage_off);
+    M.out_off = reinterpret_cast<uint32_t*>(s->ws + p.off_out_off);
+    M.rows_dest = reinterpret_cast<uint32_t*>(s->ws + p.off_rows_dest);
+    M.counts_out = reinterpret_cast<int32_t*>(s->ws + p.off_counts_out);
+    P.sitems = nullptr;
+    P.items1 = nullptr;
+  }
   P.stage_rank = -1;
   P.advance_epoch = 0;
 }
@@ -204,6 +225,7 @@ coll_status_t coll_spec_create(coll_layout_t in_layout, coll_layout_t out_layout
   d.hidden = o.hidden;
   d.topk = o.topk;
   d.experts = o.experts;
+  d.max_rows = o.max_rows;
   device_shape(o.encoding, &d.sms, &d.fused_capacity);
   coll_spec* s = new (std::nothrow) coll_spec();
   if (s == nullptr) return COLL_ERR_INVALID;
@@ -271,7 +293,10 @@ coll_status_t coll_set_routing(coll_spec_t* s, int rank, const int32_t* dev_topk
   (void)stream;
   if (s == nullptr || dev_topk == nullptr || rank < 0 || rank >= s->plan.n)
     return COLL_ERR_INVALID;
-  return COLL_ERR_UNSUPPORTED;
+  if (s->plan.kind != CK_MOE) return COLL_ERR_UNSUPPORTED;
+  if ((reinterpret_cast<uintptr_t>(dev_topk) & 3u) != 0) return COLL_ERR_ALIGN;
+  s->topk[rank] = dev_topk;
+  return COLL_OK;
 }
 
 coll_status_t coll_stage(coll_spec_t* s, int rank, const void* dev_in,
@@ -283,6 +308,11 @@ coll_status_t coll_stage(coll_spec_t* s, int rank, const void* dev_in,
   RunParams P = s->base;
   P.in[rank] = static_cast<const uint16_t*>(dev_in);
   P.stage_rank = rank;
+  if (s->plan.kind == CK_MOE) {
+    if (s->topk[rank] == nullptr) return COLL_ERR_STATE;
+    for (int r = 0; r < s->plan.n; ++r) P.moe.topk[r] = s->topk[r];
+    return cuda_status(launch_moe_stage_all(P, as_stream(stream)));
+  }
   const int items = P.sbeg[rank + 1] - P.sbeg[rank];
   return cuda_status(launch_stager(s->plan, P, items, as_stream(stream)));
 }
@@ -301,8 +331,20 @@ coll_status_t coll_run(coll_spec_t* s, const void* const* dev_ins, void* const* 
     P.out[r] = static_cast<uint16_t*>(dev_outs[r]);
     if (dev_ins) P.in[r] = static_cast<const uint16_t*>(dev_ins[r]);
   }
-  const bool empty = p.items1.empty() && p.items2.empty();
   run_begin(s, st);
+  if (p.kind == CK_MOE) {
+    for (int r = 0; r < p.n; ++r) {
+      if (s->topk[r] == nullptr) return COLL_ERR_STATE;
+      P.moe.topk[r] = s->topk[r];
+    }
+    if (dev_ins != nullptr) {
+      P.stage_rank = -1;
+      if (cudaError_t e = launched(s, launch_moe_stage_all(P, st), st)) return cuda_status(e);
+    }
+    P.advance_epoch = 1;
+    return cuda_status(launched(s, launch_moe_consume(P, st), st));
+  }
+  const bool empty = p.items1.empty() && p.items2.empty();
   if (dev_ins != nullptr && p.path == COLL_PATH_FUSED && !empty &&
       !(p.enc == ENC_LL8 && p.reset_mode == COLL_RESET_KERNEL)) {
     P.advance_epoch = 1;
@@ -343,9 +385,13 @@ coll_status_t coll_run_host(coll_spec_t* s, const void* const* host_ins,
 
 coll_status_t coll_get_counts(const coll_spec_t* s, int32_t* dev_counts,
                               coll_stream_t stream) {
-  (void)stream;
   if (s == nullptr || dev_counts == nullptr) return COLL_ERR_INVALID;
-  return COLL_ERR_UNSUPPORTED;
+  if (s->plan.kind != CK_MOE) return COLL_ERR_UNSUPPORTED;
+  if (!s->bound) return COLL_ERR_STATE;
+  const Plan& p = s->plan;
+  const size_t bytes = 4 * ((size_t)p.n * p.moe_el * p.n + p.n);
+  return cuda_status(cudaMemcpyAsync(dev_counts, s->ws + p.off_counts_out, bytes,
+                                     cudaMemcpyDeviceToDevice, as_stream(stream)));
 }
 
 coll_status_t coll_query_status(coll_spec_t* s, coll_stream_t stream, int* code, int* rank,

@@ -115,6 +115,65 @@ void group_by_dst(std::vector<Item>& items, int n, int* beg) {
 
 }  // namespace
 
+// MoE dispatch: no work lists (the routing is only known on the device);
+// the plan fixes the staging geometry and the device tables.
+static int derive_moe(const DeriveInput& in, Plan& p) {
+  const int n = in.nranks;
+  if (in.encoding != COLL_LL128) return COLL_ERR_UNSUPPORTED;
+  if (in.tokens < 0 || in.hidden <= 0 || in.topk < 1 || in.topk > 64 || in.experts < n ||
+      in.experts % n != 0 || in.experts > 1024 || in.max_rows < 0)
+    return COLL_ERR_INVALID;
+  if (in.hidden % 8 != 0) return COLL_ERR_ALIGN;
+  if (in.hidden > 48 * 1024) return COLL_ERR_UNSUPPORTED;  // two rows in shared memory
+  p.kind = CK_MOE;
+  p.enc = ENC_LL128;
+  p.n = n;
+  p.algorithm = 0;
+  p.path = COLL_PATH_STREAMED;
+  p.reset_mode = COLL_RESET_NONE;
+  p.timeout_ns = in.timeout_ns ? in.timeout_ns : 200000000ull;
+  p.moe_tokens = in.tokens;
+  p.moe_hidden = in.hidden;
+  p.moe_k = in.topk;
+  p.moe_experts = in.experts;
+  p.moe_el = in.experts / n;
+  p.moe_nblocks = (in.tokens + 127) / 128;
+  p.moe_row_lines = (uint32_t)round_up(lines_for(ENC_LL128, (uint64_t)in.hidden), 4);
+  const uint64_t worst = (uint64_t)in.tokens * n * std::min(in.topk, p.moe_el);
+  p.moe_max_rows = (uint32_t)(in.max_rows > 0 ? std::min<uint64_t>(in.max_rows, worst) : worst);
+  for (int r = 0; r < n; ++r) {
+    p.in_elems[r] = (uint64_t)in.tokens * in.hidden;
+    p.out_elems[r] = (uint64_t)p.moe_max_rows * in.hidden;
+  }
+  for (int r = 0; r <= kMaxRanks; ++r) p.sbeg[r] = p.beg1[r] = p.beg2[r] = 0;
+  p.ctas_per_rank = 1;
+  p.consume_grid = 1;
+  uint64_t off = round_up(sizeof(WsHeader), 256);
+  p.off_sitems = p.off_items1 = p.off_items2 = off;
+  auto table = [&](uint64_t bytes) {
+    const uint64_t o = off;
+    off = round_up(off + std::max<uint64_t>(bytes, 4), 256);
+    return o;
+  };
+  const uint64_t tk = (uint64_t)in.tokens * in.topk;
+  p.off_entry_rank = table(4 * n * tk);
+  p.off_block_off = table(4ull * n * p.moe_nblocks * in.experts);
+  p.off_cnt = table(4ull * n * in.experts);
+  p.off_stage_off = table(4ull * n * in.experts);
+  p.off_out_off = table(4ull * n * p.moe_el * n);
+  p.off_rows_dest = table(4ull * n);
+  p.off_counts_out = table(4ull * (n * p.moe_el * n + n));
+  p.off_counters = table(4);
+  off = round_up(off, 4096);
+  p.p_rank_lines = tk * p.moe_row_lines;
+  p.P.rank_bytes = round_up(p.p_rank_lines * kLL128LineBytes, 4096);
+  p.P.slot_bytes = p.P.rank_bytes * (uint64_t)n;
+  p.P.base = off;
+  off += 2 * p.P.slot_bytes;
+  p.ws_bytes = off;
+  return COLL_OK;
+}
+
 int derive(const DeriveInput& in, Plan& p) {
   p = Plan{};
   const int n = in.nranks;
@@ -134,6 +193,8 @@ int derive(const DeriveInput& in, Plan& p) {
     p.kind = CK_ALLGATHER;
   else if (L == COLL_SCATTERED && O == COLL_TRANSPOSED && in.op == COLL_COPY)
     p.kind = CK_ALLTOALL;
+  else if (L == COLL_SCATTERED_V && O == COLL_TRANSPOSED_V && in.op == COLL_COPY)
+    return derive_moe(in, p);
   else
     return COLL_ERR_UNSUPPORTED;
 

@@ -35,7 +35,7 @@ struct DeriveInput {
   uint64_t count;
   int encoding, algorithm, reset_mode, path, ctas, tile_lines;
   uint64_t timeout_ns;
-  int tokens, hidden, topk, experts;
+  int tokens, hidden, topk, experts, max_rows;
   int sms;             // device SM count (a default when no device is present)
   int fused_capacity;  // co-resident CTAs of the fused kernel
 };
@@ -60,6 +60,11 @@ struct Plan {
   std::vector<Item> items1, items2;
   int sbeg[kMaxRanks + 1], beg1[kMaxRanks + 1], beg2[kMaxRanks + 1];
   uint32_t ncounters;
+  // MoE dispatch geometry and table offsets
+  int moe_tokens = 0, moe_hidden = 0, moe_k = 0, moe_experts = 0, moe_el = 0, moe_nblocks = 0;
+  uint32_t moe_row_lines = 0, moe_max_rows = 0;
+  uint64_t off_entry_rank = 0, off_block_off = 0, off_cnt = 0, off_stage_off = 0,
+           off_out_off = 0, off_rows_dest = 0, off_counts_out = 0;
   // workspace layout (byte offsets from the workspace base)
   uint64_t off_sitems, off_items1, off_items2, off_counters;
   Region P, AG;

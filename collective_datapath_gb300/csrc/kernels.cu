@@ -13,6 +13,7 @@
 #include "launch.h"
 #include "ll128.cuh"
 #include "ll8.cuh"
+#include "pipe.cuh"
 
 namespace coll {
 
@@ -72,27 +73,6 @@ __global__ void __launch_bounds__(kThreads, 2) k_consume(RunParams P, int phase)
 // and reads its own 16-byte chunks, so the per-thread cp.async groups need no
 // warp synchronisation.  Stream-ordered launches only.
 constexpr int kFoldStages = 3;
-
-__device__ __forceinline__ void cp_async16(uint32_t saddr, const void* g, bool valid) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(saddr), "l"(g),
-               "r"(valid ? 16 : 0)
-               : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() {
-  asm volatile("cp.async.commit_group;" ::: "memory");
-}
-template <int N>
-__device__ __forceinline__ void cp_async_wait() {
-  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
-}
-__device__ __forceinline__ uint4 lds_v4(uint32_t saddr) {
-  uint4 v;
-  asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
-               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-               : "r"(saddr)
-               : "memory");
-  return v;
-}
 
 size_t fold_smem_bytes(int nranks) {
   return (size_t)(kThreads / 32) * kFoldStages * nranks * kRowBytes;
@@ -186,22 +166,6 @@ __global__ void __launch_bounds__(kThreads, 2) k_fold_ll128(RunParams P) {
 constexpr int kCopyStages = 8;
 
 size_t copy_smem_bytes() { return (size_t)(kThreads / 32) * kCopyStages * kRowBytes; }
-
-__device__ __forceinline__ uint2 lds_v2(uint32_t saddr) {
-  uint2 v;
-  asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(saddr) : "memory");
-  return v;
-}
-__device__ __forceinline__ void sts_v4(uint32_t saddr, uint4 v) {
-  asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(saddr), "r"(v.x), "r"(v.y),
-               "r"(v.z), "r"(v.w)
-               : "memory");
-}
-__device__ __forceinline__ uint64_t lds_u64(uint32_t saddr) {
-  uint64_t v;
-  asm volatile("ld.shared.u64 %0, [%1];" : "=l"(v) : "r"(saddr) : "memory");
-  return v;
-}
 
 __global__ void __launch_bounds__(kThreads, 4) k_copy_ll128(RunParams P, int phase) {
   extern __shared__ __align__(128) char smem[];

@@ -84,6 +84,22 @@ struct Region {
   uint64_t rank_bytes;  // bytes between consecutive rank images
 };
 
+// MoE dispatch (scatteredV -> transposedV): routing inputs and the device
+// tables the routing kernels fill (all inside the workspace).
+struct MoeParams {
+  const int32_t* topk[kMaxRanks];  // [tokens * k] expert ids per source
+  int tokens, hidden, k, experts, el, nblocks;
+  uint32_t row_lines;   // LL128 lines per staged row (a multiple of 4)
+  uint32_t max_rows;    // output rows per destination
+  uint32_t* entry_rank; // [N][tokens * k] rank among the block's rows of one expert
+  uint32_t* block_off;  // [N][nblocks][experts] block counts, then prefixes
+  uint32_t* cnt;        // [N][experts]
+  uint32_t* stage_off;  // [N][experts] first staged row of (source, expert)
+  uint32_t* out_off;    // [N dest][el][N src] first output row of the block
+  uint32_t* rows_dest;  // [N]
+  int32_t* counts_out;  // [N dest][el][N src] counts, then rows per destination
+};
+
 // Everything a kernel launch needs; passed by value (captured by graphs).
 struct RunParams {
   char* ws;                       // workspace base
@@ -117,6 +133,7 @@ struct RunParams {
   const int64_t* late_order[kMaxRanks];
   int64_t late_n[kMaxRanks];
   int late_ctas;                  // extra CTAs at the end of the grid
+  MoeParams moe;
   // withheld staging (fault-injection runs)
   const int64_t* wh_lines;
   const int32_t* wh_kind;

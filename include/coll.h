@@ -140,7 +140,9 @@ typedef struct {
     int tokens;          /* rows per source rank */
     int hidden;          /* bf16 elements per row */
     int topk;            /* experts per token */
-    int experts;         /* total experts, a multiple of nranks */
+    int experts;         /* total experts, a multiple of nranks (<= 1024) */
+    int max_rows;        /* output rows each destination can hold, 0 = the
+                            worst case tokens * nranks * min(topk, experts/nranks) */
 } coll_options_t;
 
 typedef struct coll_spec coll_spec_t;
@@ -179,8 +181,13 @@ coll_status_t coll_bind(coll_spec_t *spec, void *dev_workspace, size_t bytes,
                         coll_stream_t stream);
 
 /* MoE dispatch only: give source rank `rank`'s routing, dev_topk[tokens*topk]
- * (int32 expert ids, distinct per token).  Counting, the prefix sums and the
- * row placement run on the device at the next coll_stage / coll_run. */
+ * (int32 expert ids, distinct per token; the array must stay valid and
+ * unchanged until the run that uses it completes).  Counting, the prefix
+ * sums and the row placement run on the device at the next coll_stage /
+ * coll_run.  Output of destination d: its rows in the order (local expert,
+ * source rank, token), each the source's token row; an expert id outside
+ * [0, experts) latches COLL_ERR_INVALID and the row is dropped; more rows
+ * than max_rows latch COLL_ERR_NOMEM and the excess rows are dropped. */
 coll_status_t coll_set_routing(coll_spec_t *spec, int rank,
                                const int32_t *dev_topk, coll_stream_t stream);
 
@@ -209,8 +216,8 @@ coll_status_t coll_run_host(coll_spec_t *spec, const void *const *host_ins,
                             void *const *host_outs, coll_stream_t stream);
 
 /* MoE dispatch only: copy counts[dest][local expert][source] (int32,
- * nranks * experts) and, after it, rows per destination (nranks int32) of
- * the last run into dev_counts. */
+ * nranks * experts entries) and, after them, the rows of each destination
+ * (nranks int32) of the last run into dev_counts (stream-ordered). */
 coll_status_t coll_get_counts(const coll_spec_t *spec, int32_t *dev_counts,
                               coll_stream_t stream);
 
