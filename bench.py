@@ -345,6 +345,59 @@ def bandwidth_row(cd, triple, count_in_out, kind, stream, steps=5) -> dict:
             "status": st}
 
 
+def moe_row(cd, stream, steps=5) -> dict:
+    """MoE dispatch: 8 ranks x 4096 tokens x 7168 bf16, top-8 of 256 experts
+    (routing drawn on the device from a seeded generator)."""
+    import torch
+
+    n, tokens, hidden, k, experts = N_RANKS, 4096, 7168, 8, 256
+    coll = cd.Collective(cd.MOE_DISPATCH, n, 0, encoding=cd.COLL_LL128, tokens=tokens,
+                         hidden=hidden, topk=k, experts=experts, max_rows=40000)
+    ins = make_inputs(tokens * hidden, 13)
+    topk = []
+    for r in range(n):
+        g = torch.Generator(device="cuda")
+        g.manual_seed(5000 + r)
+        keys = torch.rand(tokens, experts, generator=g, device="cuda")
+        topk.append(keys.argsort(dim=1)[:, :k].to(torch.int32).contiguous())
+        cd.coll_set_routing(coll.spec, r, topk[r])
+    outs = [torch.empty(coll.elems(r)[1], dtype=torch.int16, device="cuda") for r in range(n)]
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+    for e in ev:
+        e.record(stream)
+    with torch.cuda.stream(stream):
+        for _ in range(2):
+            coll.run(ins, outs, stream)
+        stream.synchronize()
+        cd.coll_set_profile_events(coll.spec, ev)
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        times = [0.0, 0.0]
+        for _ in range(steps):
+            coll.run(ins, outs, stream)
+            stream.synchronize()
+            times[0] += ev[0].elapsed_time(ev[1])
+            times[1] += ev[1].elapsed_time(ev[2])
+        e1.record(stream)
+        stream.synchronize()
+        cd.coll_set_profile_events(coll.spec, [])
+    st = coll.status(stream)[0]
+    rows = n * tokens * k
+    row_b, line_b = hidden * 2, ((hidden + 59) // 60 + 3) // 4 * 4 * 128
+    unique = n * tokens * row_b + rows * line_b + rows * line_b + rows * row_b
+    issue = rows * row_b + rows * line_b + rows * line_b + rows * row_b
+    ms = e0.elapsed_time(e1) / steps
+    coll.close()
+    del coll, ins, outs, topk
+    torch.cuda.empty_cache()
+    return {"ms": round(ms, 4), "GB/s": round(unique / ms / 1e6, 1),
+            "algorithmic_bytes": unique, "issue_level_bytes": issue,
+            "stage_ms": round(times[0] / steps, 4), "copy_ms": round(times[1] / steps, 4),
+            "note": "bytes: each token row read once, staged K times as LL128, "
+                    "every routed row read and unpacked once", "status": st}
+
+
 def main() -> int:
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -429,12 +482,16 @@ def main() -> int:
     dom = max(range(nk), key=lambda k: dur[k])
     achieved = kb[dom] / dur[dom] / 1e6
     traffic = None
-    prof = os.path.join(ROOT, "profiles", "traffic.json")
+    prof = os.path.join(ROOT, "profiles", "traffic.md")
     if os.path.exists(prof):
-        with open(prof) as f:
-            t = json.load(f)
         key = f"allreduce_twoshot_ll128_{args.mib}mib"
-        traffic = t.get(key, {}).get(["stage", "rs", "ag"][dom])
+        want = ["stage", "rs", "ag"][dom]
+        with open(prof) as f:
+            for ln in f:
+                parts = ln.split()
+                if len(parts) == 4 and parts[0] == "traffic" and parts[1] == key \
+                        and parts[2] == want:
+                    traffic = int(parts[3])
 
     line = {
         "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world,
@@ -504,6 +561,7 @@ def main() -> int:
         line["rows"] = {
             "reduce_scatter_256MiB": bandwidth_row(cd, cd.REDUCE_SCATTER, count, "rs", stream),
             "all_gather_256MiB": bandwidth_row(cd, cd.ALLGATHER, count, "ag", stream),
+            "moe_dispatch_8x4096x7168_top8of256": moe_row(cd, stream),
         }
         line["latency_us_per_op"] = latency_sweep(cd, stream)
         if world == 1:
