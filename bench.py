@@ -161,6 +161,12 @@ def barrier_max(value: float, world: int) -> float:
     return float(t.item())
 
 
+def replica_value(world: int, bytes_per_replica: float, ms_max: float) -> float:
+    """Whole-job GB/s: every replica moves the same bytes; the job takes the
+    slowest replica's time."""
+    return world * bytes_per_replica / (ms_max * 1e-3) / 1e9
+
+
 def barrier(world: int) -> None:
     if world > 1:
         import torch.distributed as dist
@@ -470,7 +476,7 @@ def main() -> int:
         raise RuntimeError(f"device status {code} during the timed steps")
     ms_step = barrier_max(ms_total / K, world)
     algo_bytes = bytes_allreduce_twoshot(N_RANKS, s_bytes, EPS_LL128)
-    value = world * algo_bytes / (ms_step * 1e-3) / 1e9
+    value = replica_value(world, algo_bytes, ms_step)
 
     # per-kernel durations over the timed steps
     names = ["stage (LL128 encode)", "reduce-scatter fold + publish", "all-gather unpack"]
