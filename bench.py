@@ -260,19 +260,23 @@ def timed(step, k: int, w: int, stream, world: int) -> float:
     return e0.elapsed_time(e1)
 
 
-def latency_sweep(cd, stream) -> dict:
+def latency_sweep(cd, stream, only_T=None, only_variant=None) -> dict:
     """8 ranks x [T x 4096] bf16, LL8 (config of the decode-time sweep)."""
     import torch
 
     out = {}
     flush = torch.empty(int(2 * L2_BYTES), dtype=torch.uint8, device="cuda")
     for T in (1, 2, 4, 8, 16, 32, 64, 128):
+        if only_T is not None and T != only_T:
+            continue
         count = T * 4096
         row = {}
         for algo, path, name in ((cd.COLL_ONESHOT, cd.COLL_PATH_FUSED, "oneshot_fused"),
                                  (cd.COLL_ONESHOT, cd.COLL_PATH_STREAMED, "oneshot_streamed"),
                                  (cd.COLL_TWOSHOT, cd.COLL_PATH_FUSED, "twoshot_fused"),
                                  (cd.COLL_TWOSHOT, cd.COLL_PATH_STREAMED, "twoshot_streamed")):
+            if only_variant is not None and name != only_variant:
+                continue
             coll = cd.Collective(cd.ALLREDUCE, N_RANKS, count, encoding=cd.COLL_LL8,
                                  algorithm=algo, path=path)
             ins = make_inputs(count, 7 + T)
@@ -414,6 +418,9 @@ def main() -> int:
     ap.add_argument("--quick", action="store_true", help="skip sweep, extra rows and CPU leg")
     ap.add_argument("--sweep-only", action="store_true",
                     help="only the small-message latency sweep (profiling runs)")
+    ap.add_argument("--sweep-T", type=int, default=None, help="sweep only this T")
+    ap.add_argument("--sweep-variant", default=None,
+                    help="sweep only this variant, e.g. twoshot_fused")
     args = ap.parse_args()
     if args.impl == "reference":
         return run_reference(args)
@@ -438,7 +445,8 @@ def main() -> int:
     peaks = load_peaks()
     stream = torch.cuda.Stream()
     if args.sweep_only:
-        print(json.dumps({"latency_us_per_op": latency_sweep(cd, stream)}))
+        print(json.dumps({"latency_us_per_op": latency_sweep(cd, stream, args.sweep_T,
+                                                             args.sweep_variant)}))
         return 0
     count = args.mib * 2**20 // 2
     s_bytes = count * 2.0

@@ -140,7 +140,9 @@ cudaError_t launched(coll_spec* s, cudaError_t e, cudaStream_t st) {
 // else through the generic consume kernel.
 cudaError_t launch_phase(const Plan& p, const RunParams& P, int phase,
                          const std::vector<Item>& items, cudaStream_t st) {
-  if (p.enc == ENC_LL128 && !items.empty()) {
+  const bool pipelined = p.enc == ENC_LL128 || p.reset_mode == COLL_RESET_DEFERRED ||
+                         p.reset_mode == COLL_RESET_NONE;
+  if (pipelined && !items.empty()) {
     bool all_fold = true, all_copy = true;
     for (const Item& it : items) {
       all_fold = all_fold && it.kind == IK_REDUCE;

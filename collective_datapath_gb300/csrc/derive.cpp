@@ -221,16 +221,22 @@ int derive(const DeriveInput& in, Plan& p) {
     in_bytes_per_rank = std::max<uint64_t>(in_bytes_per_rank, 2 * p.in_elems[r]);
   }
 
-  // Algorithm and path.
+  // Algorithm and path (AUTO): boundaries placed on measured points of the
+  // 8-rank LL8 sweep on GB300 (flash-comm §3.2: fit, then put the boundary on
+  // a measured size).  Oneshot up to 512 KiB per rank (it reads N^2 S of
+  // lines but has one phase), twoshot above; one fused cooperative kernel up
+  // to 256 KiB per rank, stream-ordered pipelined kernels above.  Two ranks
+  // always use oneshot (both move S per rank).
   p.algorithm = 0;
   if (p.kind == CK_ALLREDUCE) {
     p.algorithm = in.algorithm;
     if (p.algorithm == COLL_ALGO_AUTO)
-      p.algorithm = (n <= 2 || in_bytes_per_rank <= 64 * 1024) ? COLL_ONESHOT : COLL_TWOSHOT;
+      p.algorithm = (n <= 2 || in_bytes_per_rank <= 512 * 1024) ? COLL_ONESHOT : COLL_TWOSHOT;
   }
   p.path = in.path;
   if (p.path == COLL_PATH_AUTO)
-    p.path = in_bytes_per_rank <= 64 * 1024 ? COLL_PATH_FUSED : COLL_PATH_STREAMED;
+    p.path = (in_bytes_per_rank <= 256 * 1024 && p.enc == ENC_LL8) ? COLL_PATH_FUSED
+                                                                  : COLL_PATH_STREAMED;
 
   // Rank images of region P.
   for (int r = 0; r < n; ++r) {

@@ -145,7 +145,9 @@ __device__ __forceinline__ bool aborted(char* ws) {
 }
 
 // Bounded wait bookkeeping: the first failed check starts the clock; the
-// wait gives up when the bound passes or another wait of the run failed.
+// wait gives up when the bound passes, or -- checked only once the wait is
+// older than 20 us, to keep the common short poll to one load -- when
+// another wait of the run failed.
 struct Waiter {
   uint64_t t0 = 0;
   __device__ __forceinline__ bool expired(char* ws, uint64_t timeout_ns) {
@@ -154,7 +156,8 @@ struct Waiter {
       t0 = now;
       return false;
     }
-    return (now - t0) > timeout_ns || aborted(ws);
+    const uint64_t waited = now - t0;
+    return waited > timeout_ns || (waited > 20000 && aborted(ws));
   }
 };
 
@@ -167,32 +170,31 @@ __device__ __forceinline__ void count_rejection(char* ws) {
               (unsigned long long)__popc(mask));
 }
 
-// Epoch protocol of a launch.  Thread 0 reads the device epoch once and
-// shares it with the CTA; in the launch that ends a run every CTA then adds
-// one to `arrived` (fire-and-forget).  The last CTA of the grid advances the
-// epoch once every CTA has read it (arrived == grid), so the next run uses
+// Epoch protocol of a launch.  Every thread reads the device epoch itself
+// (one L2 request per warp, issued next to the launch's first data loads, no
+// CTA barrier); in the launch that ends a run each warp then adds one to
+// `arrived` (fire-and-forget).  The last CTA of the grid advances the epoch
+// once every warp has read it (arrived == all warps), so the next run uses
 // the other staging slot; no CTA waits at the end of its own work.
 __device__ __forceinline__ uint64_t begin_run(const RunParams& P) {
-  __shared__ uint64_t s_epoch;
-  if (threadIdx.x == 0) {
-    WsHeader* h = header(P.ws);
-    s_epoch = ld_relaxed_u64(&h->epoch);
-    if (P.advance_epoch) {
+  WsHeader* h = header(P.ws);
+  const uint64_t e = ld_relaxed_u64(&h->epoch);
+  if (P.advance_epoch) {
+    __syncwarp();
+    if ((threadIdx.x & 31) == 0)
       asm volatile("red.relaxed.gpu.global.add.u32 [%0], 1;" ::"l"(&h->arrived) : "memory");
-    }
   }
-  __syncthreads();
-  return s_epoch;
+  return e;
 }
 
 __device__ __forceinline__ void finish_run(const RunParams& P, uint64_t epoch) {
   if (!P.advance_epoch || threadIdx.x != 0) return;
-  const uint32_t total = gridDim.x * gridDim.y * gridDim.z;
+  const uint32_t total = gridDim.x * gridDim.y * gridDim.z * ((blockDim.x + 31) / 32);
   if (blockIdx.x != gridDim.x - 1) return;
   WsHeader* h = header(P.ws);
-  // Every CTA has started (and read the epoch) long before the last CTA
+  // Every warp has started (and read the epoch) long before the last CTA
   // finishes; the 10 s bound only guards against a broken launch.  This wait
-  // ignores `abort`: the epoch must not move before every CTA has read it.
+  // ignores `abort`: the epoch must not move before every warp has read it.
   const uint64_t t0 = globaltimer_ns();
   while (ld_relaxed_u32(&h->arrived) < total) {
     if (globaltimer_ns() - t0 > 10000000000ull) {

@@ -278,6 +278,169 @@ __global__ void __launch_bounds__(kThreads, 4) k_stage_ll128(RunParams P) {
   }
 }
 
+// ---- LL8 fold and copy through cp.async rings ------------------------------------
+// The same pipelines for 8-byte lines: a warp row is 512 bytes = 64 lines =
+// 128 elements; lane L holds lines 2L and 2L+1 (elements 4L..4L+3).  Used on
+// the stream-ordered path when re-arming is deferred or off (the last-reader
+// re-arm needs the generic kernel's counters).
+
+__device__ __forceinline__ bool ll8_pair_ready(const uint4& v, uint32_t flag) {
+  return v.y == flag && v.w == flag;
+}
+
+constexpr int kLL8RowLines = 64;
+
+__global__ void __launch_bounds__(kThreads, 2) k_fold_ll8(RunParams P) {
+  extern __shared__ __align__(128) char smem[];
+  const uint64_t e = begin_run(P);
+  const uint32_t flag = (uint32_t)e;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
+  const int n = P.nranks;
+  const uint32_t wbase = (uint32_t)__cvta_generic_to_shared(smem) +
+                         (uint32_t)(warp * kFoldStages * n * kRowBytes + 16 * lane);
+  const bool deferred = P.reset_mode == kResetDeferred;
+  const int n_items = P.beg1[P.nranks];
+  for (int v = blockIdx.x; v < n_items; v += gridDim.x) {
+    if (aborted(P.ws)) break;
+    const int i = P.interleave1 ? P.beg1[v % P.nranks] + v / P.nranks : v;
+    const Item it = P.items1[i];
+    const bool publish = (it.flags & IF_PUBLISH) != 0;
+    const uint32_t nrows = (it.nlines + kLL8RowLines - 1) / kLL8RowLines;
+    const int nj = (uint32_t)warp < nrows ? (int)((nrows - warp + nwarps - 1) / nwarps) : 0;
+    auto issue = [&](int j) {
+      if (j < nj) {
+        const uint32_t r = warp + j * nwarps;
+        const bool valid = r * kLL8RowLines + 2 * lane < it.nlines;
+        const uint64_t off = (it.src_line + (uint64_t)r * kLL8RowLines) * kLL8LineBytes + 16 * lane;
+        const uint32_t slot = wbase + (uint32_t)((j % kFoldStages) * n * kRowBytes);
+        for (int p = 0; p < n; ++p)
+          cp_async16(slot + p * kRowBytes, P.ws + P.P.base + (e & 1) * P.P.slot_bytes +
+                                               (uint64_t)p * P.P.rank_bytes + off,
+                     valid);
+      }
+      cp_async_commit();
+    };
+#pragma unroll
+    for (int j = 0; j < kFoldStages; ++j) issue(j);
+    bool ok = true;
+    for (int j = 0; j < nj; ++j) {
+      cp_async_wait<kFoldStages - 1>();
+      const uint32_t slot = wbase + (uint32_t)((j % kFoldStages) * n * kRowBytes);
+      uint4 s[kMaxRanks];
+#pragma unroll
+      for (int p = 0; p < kMaxRanks; ++p)
+        if (p < n) s[p] = lds_v4(slot + p * kRowBytes);
+      issue(j + kFoldStages);
+      const uint32_t r = warp + j * nwarps;
+      const uint64_t line = it.src_line + (uint64_t)r * kLL8RowLines + 2 * lane;
+      const bool valid = r * kLL8RowLines + 2 * lane < it.nlines;
+      if (valid) {
+#pragma unroll
+        for (int p = 0; p < kMaxRanks; ++p) {
+          if (p < n && ok && !ll8_pair_ready(s[p], flag)) {
+            const uint64_t* g = reinterpret_cast<const uint64_t*>(
+                                    P.ws + P.P.base + (e & 1) * P.P.slot_bytes +
+                                    (uint64_t)p * P.P.rank_bytes) + line;
+            ok = ll8_wait_lines(P, g, 2, flag, p, (int64_t)line);
+            uint64_t a, b;
+            ld_relaxed_v2u64(g, a, b);
+            s[p] = make_uint4((uint32_t)a, (uint32_t)(a >> 32), (uint32_t)b, (uint32_t)(b >> 32));
+          }
+        }
+        float a0 = bf16_lo_to_f32(s[0].x), a1 = bf16_hi_to_f32(s[0].x);
+        float a2 = bf16_lo_to_f32(s[0].z), a3 = bf16_hi_to_f32(s[0].z);
+#pragma unroll
+        for (int p = 1; p < kMaxRanks; ++p) {
+          if (p < n) {
+            a0 = __fadd_rn(a0, bf16_lo_to_f32(s[p].x));
+            a1 = __fadd_rn(a1, bf16_hi_to_f32(s[p].x));
+            a2 = __fadd_rn(a2, bf16_lo_to_f32(s[p].z));
+            a3 = __fadd_rn(a3, bf16_hi_to_f32(s[p].z));
+          }
+        }
+        const uint32_t w0 = pack_bf16x2(a0, a1), w1 = pack_bf16x2(a2, a3);
+        if (publish) {
+          uint64_t* dst = reinterpret_cast<uint64_t*>(P.ws + P.AG.base + (e & 1) * P.AG.slot_bytes +
+                                                      (uint64_t)it.dst * P.AG.rank_bytes) +
+                          it.out_off + (uint64_t)r * kLL8RowLines + 2 * lane;
+          const uint64_t f = (uint64_t)flag << 32;
+          st_relaxed_v2u64(dst, (uint64_t)w0 | f, (uint64_t)w1 | f);
+          if (deferred) {
+            uint64_t* other = reinterpret_cast<uint64_t*>(
+                                  P.ws + P.AG.base + ((e + 1) & 1) * P.AG.slot_bytes +
+                                  (uint64_t)it.dst * P.AG.rank_bytes) +
+                              it.out_off + (uint64_t)r * kLL8RowLines + 2 * lane;
+            st_relaxed_v2u64(other, 0ull, 0ull);
+          }
+        } else {
+          st_v2u32(P.out[it.dst] + it.out_off + (uint64_t)r * 2 * kLL8RowLines + 4 * lane, w0, w1);
+        }
+      }
+      if (!__all_sync(0xFFFFFFFFu, ok)) break;
+    }
+    cp_async_wait<0>();
+    if (!ok) break;
+  }
+  finish_run(P, e);
+}
+
+__global__ void __launch_bounds__(kThreads, 4) k_copy_ll8(RunParams P, int phase) {
+  extern __shared__ __align__(128) char smem[];
+  const uint64_t e = begin_run(P);
+  const uint32_t flag = (uint32_t)e;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
+  const Item* items = phase == 1 ? P.items1 : P.items2;
+  const int* beg = phase == 1 ? P.beg1 : P.beg2;
+  const bool inter = phase == 1 ? P.interleave1 : P.interleave2;
+  const Region& R = phase == 1 ? P.P : P.AG;
+  const int n_items = beg[P.nranks];
+  const uint32_t wbase = (uint32_t)__cvta_generic_to_shared(smem) +
+                         (uint32_t)(warp * kCopyStages * kRowBytes + 16 * lane);
+  for (int v = blockIdx.x; v < n_items; v += gridDim.x) {
+    if (aborted(P.ws)) break;
+    const int i = inter ? beg[v % P.nranks] + v / P.nranks : v;
+    const Item it = items[i];
+    const uint64_t* src = reinterpret_cast<const uint64_t*>(
+                              P.ws + R.base + (e & 1) * R.slot_bytes +
+                              (uint64_t)it.src * R.rank_bytes) +
+                          it.src_line;
+    const uint32_t nrows = (it.nlines + kLL8RowLines - 1) / kLL8RowLines;
+    const int nj = (uint32_t)warp < nrows ? (int)((nrows - warp + nwarps - 1) / nwarps) : 0;
+    auto issue = [&](int j) {
+      if (j < nj) {
+        const uint32_t r = warp + j * nwarps;
+        cp_async16(wbase + (j % kCopyStages) * kRowBytes, src + (size_t)r * kLL8RowLines + 2 * lane,
+                   r * kLL8RowLines + 2 * lane < it.nlines);
+      }
+      cp_async_commit();
+    };
+#pragma unroll
+    for (int j = 0; j < kCopyStages; ++j) issue(j);
+    bool ok = true;
+    for (int j = 0; j < nj; ++j) {
+      cp_async_wait<kCopyStages - 1>();
+      uint4 s = lds_v4(wbase + (j % kCopyStages) * kRowBytes);
+      issue(j + kCopyStages);
+      const uint32_t r = warp + j * nwarps;
+      if (r * kLL8RowLines + 2 * lane < it.nlines) {
+        if (!ll8_pair_ready(s, flag)) {
+          const uint64_t* g = src + (size_t)r * kLL8RowLines + 2 * lane;
+          ok = ll8_wait_lines(P, g, 2, flag, it.src,
+                              (int64_t)(it.src_line + r * kLL8RowLines + 2 * lane));
+          uint64_t a, b;
+          ld_relaxed_v2u64(g, a, b);
+          s = make_uint4((uint32_t)a, (uint32_t)(a >> 32), (uint32_t)b, (uint32_t)(b >> 32));
+        }
+        st_v2u32(P.out[it.dst] + it.out_off + (uint64_t)r * 2 * kLL8RowLines + 4 * lane, s.x, s.z);
+      }
+      if (!__all_sync(0xFFFFFFFFu, ok)) break;
+    }
+    cp_async_wait<0>();
+    if (!ok) break;
+  }
+  finish_run(P, e);
+}
+
 // Late producer: publish rank p's withheld lines in the given order, after
 // every consumer CTA has started polling.  One warp publishes, in order.
 template <int ENC>
@@ -365,7 +528,7 @@ __device__ void late_producer(const RunParams& P, uint64_t e, int p, int workers
 }
 
 template <int ENC>
-__global__ void __launch_bounds__(kThreads) k_fused(RunParams P) {
+__global__ void __launch_bounds__(kThreads, 2) k_fused(RunParams P) {
   const uint64_t e = begin_run(P);
   const int B = P.ctas_per_rank;
   const int workers = P.nranks * B;
@@ -493,21 +656,29 @@ cudaError_t launch_fused(const RunParams& P, int grid, cudaStream_t s) {
 }
 
 cudaError_t launch_fold(const RunParams& P, int grid, cudaStream_t s) {
-  static size_t configured = 0;
+  static bool configured = false;
   const size_t bytes = fold_smem_bytes(P.nranks);
-  if (bytes > configured) {
+  if (!configured) {
+    const int most = (int)fold_smem_bytes(kMaxRanks);
     cudaError_t e = cudaFuncSetAttribute(k_fold_ll128,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)fold_smem_bytes(kMaxRanks));
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, most);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(k_fold_ll8, cudaFuncAttributeMaxDynamicSharedMemorySize, most);
     if (e != cudaSuccess) return e;
-    configured = fold_smem_bytes(kMaxRanks);
+    configured = true;
   }
-  k_fold_ll128<<<grid, kThreads, bytes, s>>>(P);
+  if (P.enc == ENC_LL8)
+    k_fold_ll8<<<grid, kThreads, bytes, s>>>(P);
+  else
+    k_fold_ll128<<<grid, kThreads, bytes, s>>>(P);
   return cudaGetLastError();
 }
 
 cudaError_t launch_copy(const RunParams& P, int phase, int grid, cudaStream_t s) {
-  k_copy_ll128<<<grid, kThreads, copy_smem_bytes(), s>>>(P, phase);
+  if (P.enc == ENC_LL8)
+    k_copy_ll8<<<grid, kThreads, copy_smem_bytes(), s>>>(P, phase);
+  else
+    k_copy_ll128<<<grid, kThreads, copy_smem_bytes(), s>>>(P, phase);
   return cudaGetLastError();
 }
 

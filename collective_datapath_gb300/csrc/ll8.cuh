@@ -39,10 +39,12 @@ __device__ __forceinline__ void ll8_rearm(uint64_t* p) {
   st_relaxed_v2u64(p + 2, 0ull, 0ull);
 }
 
-// Poll a group until every line carries `flag` (bounded); the caller then
-// reloads it.  Returns false on timeout or abort (the error is latched).
-static __device__ __noinline__ bool ll8_wait(const RunParams& P, const uint64_t* p, uint32_t flag,
-                                      uint32_t rank, int64_t line) {
+// Poll `lines` (2 or 4) consecutive lines until every one carries `flag`
+// (bounded); the caller then reloads them.  Returns false on timeout or
+// abort (the error is latched).
+static __device__ __noinline__ bool ll8_wait_lines(const RunParams& P, const uint64_t* p,
+                                                   int lines, uint32_t flag, uint32_t rank,
+                                                   int64_t line) {
   count_rejection(P.ws);
   Waiter w;
   for (;;) {
@@ -51,9 +53,13 @@ static __device__ __noinline__ bool ll8_wait(const RunParams& P, const uint64_t*
       return false;
     }
     __nanosleep(64);
-    LL8Group g;
-    ll8_load(p, g);
-    if (ll8_ready(g, flag)) return true;
+    bool ready = true;
+    for (int j = 0; j < lines; j += 2) {
+      uint64_t a, b;
+      ld_relaxed_v2u64(p + j, a, b);
+      ready = ready && (uint32_t)(a >> 32) == flag && (uint32_t)(b >> 32) == flag;
+    }
+    if (ready) return true;
   }
 }
 
@@ -95,40 +101,6 @@ __device__ __forceinline__ void ll8_stage_tile(const RunParams& P, const StageIt
   }
 }
 
-// Fold one group of every rank in rank order (fp32, one rounding).
-__device__ __forceinline__ uint4 ll8_fold(const LL8Group* s, int n) {
-  float a[8];
-  {
-    const uint32_t w0 = (uint32_t)s[0].l0, w1 = (uint32_t)s[0].l1,
-                   w2 = (uint32_t)s[0].l2, w3 = (uint32_t)s[0].l3;
-    a[0] = bf16_lo_to_f32(w0); a[1] = bf16_hi_to_f32(w0);
-    a[2] = bf16_lo_to_f32(w1); a[3] = bf16_hi_to_f32(w1);
-    a[4] = bf16_lo_to_f32(w2); a[5] = bf16_hi_to_f32(w2);
-    a[6] = bf16_lo_to_f32(w3); a[7] = bf16_hi_to_f32(w3);
-  }
-#pragma unroll
-  for (int p = 1; p < kMaxRanks; ++p) {
-    if (p < n) {
-      const uint32_t w0 = (uint32_t)s[p].l0, w1 = (uint32_t)s[p].l1,
-                     w2 = (uint32_t)s[p].l2, w3 = (uint32_t)s[p].l3;
-      a[0] = __fadd_rn(a[0], bf16_lo_to_f32(w0));
-      a[1] = __fadd_rn(a[1], bf16_hi_to_f32(w0));
-      a[2] = __fadd_rn(a[2], bf16_lo_to_f32(w1));
-      a[3] = __fadd_rn(a[3], bf16_hi_to_f32(w1));
-      a[4] = __fadd_rn(a[4], bf16_lo_to_f32(w2));
-      a[5] = __fadd_rn(a[5], bf16_hi_to_f32(w2));
-      a[6] = __fadd_rn(a[6], bf16_lo_to_f32(w3));
-      a[7] = __fadd_rn(a[7], bf16_hi_to_f32(w3));
-    }
-  }
-  uint4 r;
-  r.x = pack_bf16x2(a[0], a[1]);
-  r.y = pack_bf16x2(a[2], a[3]);
-  r.z = pack_bf16x2(a[4], a[5]);
-  r.w = pack_bf16x2(a[6], a[7]);
-  return r;
-}
-
 // Process one consume item: validate + unpack (+ fold) + write (+ re-arm).
 // `R` is the source region (P for phase 1, AG for twoshot phase 2).  A fold
 // loads the group of all n images before it checks them; a copy loads
@@ -144,33 +116,49 @@ __device__ __forceinline__ void ll8_consume_item(const RunParams& P, const Regio
   const bool deferred = P.reset_mode == kResetDeferred;
   bool ok = true;
   if (reduce) {
-    for (uint32_t g = threadIdx.x; g < ngroups && ok; g += blockDim.x) {
-      const uint64_t line = it.src_line + 4 * (uint64_t)g;
-      LL8Group s[kMaxRanks];
+    // Pairs of lines (16 bytes, 4 elements) per source per step: the N
+    // sources' pairs are loaded before any is checked.
+    const uint32_t npairs = it.nlines / 2;
+    for (uint32_t q = threadIdx.x; q < npairs && ok; q += blockDim.x) {
+      const uint64_t line = it.src_line + 2 * (uint64_t)q;
+      uint64_t lo[kMaxRanks], hi[kMaxRanks];
 #pragma unroll
       for (int p = 0; p < kMaxRanks; ++p)
-        if (p < n) ll8_load(image_lines(P, R, epoch, p) + line, s[p]);
+        if (p < n) ld_relaxed_v2u64(image_lines(P, R, epoch, p) + line, lo[p], hi[p]);
 #pragma unroll
       for (int p = 0; p < kMaxRanks; ++p)
-        if (p < n && !ll8_ready(s[p], flag)) {
+        if (p < n && ((uint32_t)(lo[p] >> 32) != flag || (uint32_t)(hi[p] >> 32) != flag)) {
           const uint64_t* src = image_lines(P, R, epoch, p) + line;
-          ok = ok && ll8_wait(P, src, flag, p, (int64_t)line);
-          ll8_load(src, s[p]);
+          ok = ok && ll8_wait_lines(P, src, 2, flag, p, (int64_t)line);
+          ld_relaxed_v2u64(src, lo[p], hi[p]);
         }
       if (!ok) break;
-      const uint4 res = ll8_fold(s, n);
+      float a0 = bf16_lo_to_f32((uint32_t)lo[0]), a1 = bf16_hi_to_f32((uint32_t)lo[0]);
+      float a2 = bf16_lo_to_f32((uint32_t)hi[0]), a3 = bf16_hi_to_f32((uint32_t)hi[0]);
+#pragma unroll
+      for (int p = 1; p < kMaxRanks; ++p) {
+        if (p < n) {
+          a0 = __fadd_rn(a0, bf16_lo_to_f32((uint32_t)lo[p]));
+          a1 = __fadd_rn(a1, bf16_hi_to_f32((uint32_t)lo[p]));
+          a2 = __fadd_rn(a2, bf16_lo_to_f32((uint32_t)hi[p]));
+          a3 = __fadd_rn(a3, bf16_hi_to_f32((uint32_t)hi[p]));
+        }
+      }
+      const uint32_t w0 = pack_bf16x2(a0, a1), w1 = pack_bf16x2(a2, a3);
       if (sole) {
 #pragma unroll
         for (int p = 0; p < kMaxRanks; ++p)
-          if (p < n) ll8_rearm(image_lines(P, R, epoch, p) + line);
+          if (p < n) st_relaxed_v2u64(image_lines(P, R, epoch, p) + line, 0ull, 0ull);
       }
       if (publish) {
-        ll8_store(image_lines(P, P.AG, epoch, it.dst) + it.out_off + 4 * (uint64_t)g, res,
-                  flag);
+        const uint64_t f = (uint64_t)flag << 32;
+        st_relaxed_v2u64(image_lines(P, P.AG, epoch, it.dst) + it.out_off + 2 * (uint64_t)q,
+                         (uint64_t)w0 | f, (uint64_t)w1 | f);
         if (deferred)
-          ll8_rearm(image_lines(P, P.AG, epoch + 1, it.dst) + it.out_off + 4 * (uint64_t)g);
+          st_relaxed_v2u64(image_lines(P, P.AG, epoch + 1, it.dst) + it.out_off + 2 * (uint64_t)q,
+                           0ull, 0ull);
       } else {
-        st_v4(P.out[it.dst] + it.out_off + 8 * (uint64_t)g, res);
+        st_v2u32(P.out[it.dst] + it.out_off + 4 * (uint64_t)q, w0, w1);
       }
     }
   } else {
@@ -186,8 +174,8 @@ __device__ __forceinline__ void ll8_consume_item(const RunParams& P, const Regio
       for (int j = 0; j < kGroupsInFlight; ++j) {
         const uint32_t g = g0 + j * blockDim.x;
         if (g < ngroups && !ll8_ready(s[j], flag)) {
-          ok = ok && ll8_wait(P, src0 + 4 * (size_t)g, flag, it.src,
-                              (int64_t)(it.src_line + 4 * (uint64_t)g));
+          ok = ok && ll8_wait_lines(P, src0 + 4 * (size_t)g, 4, flag, it.src,
+                                    (int64_t)(it.src_line + 4 * (uint64_t)g));
           ll8_load(src0 + 4 * (size_t)g, s[j]);
         }
       }

@@ -125,7 +125,8 @@ enum { COLL_RESET_FUSED = 0, COLL_RESET_KERNEL = 1, COLL_RESET_NONE = 2,
 /* Launch path: FUSED = stage and consume inside one cooperative kernel
  * (all CTAs co-resident; a CTA serves one emulated rank); STREAMED =
  * separate stage and consume kernels ordered by the stream.  AUTO picks
- * FUSED up to 64 KiB per rank. */
+ * FUSED for LL8 up to 256 KiB per rank and, for all-reduce, ONESHOT up to
+ * 512 KiB per rank (boundaries on measured GB300 points). */
 enum { COLL_PATH_AUTO = 0, COLL_PATH_FUSED = 1, COLL_PATH_STREAMED = 2 };
 
 typedef struct {
