@@ -415,6 +415,8 @@ def main() -> int:
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--mib", type=int, default=256, help="per-rank MiB of the main workload")
+    ap.add_argument("--path", default="streamed", choices=["streamed", "composed"],
+                    help="launch path of the main all-reduce")
     ap.add_argument("--quick", action="store_true", help="skip sweep, extra rows and CPU leg")
     ap.add_argument("--sweep-only", action="store_true",
                     help="only the small-message latency sweep (profiling runs)")
@@ -450,12 +452,14 @@ def main() -> int:
         return 0
     count = args.mib * 2**20 // 2
     s_bytes = count * 2.0
+    composed = args.path == "composed"
     coll = cd.Collective(cd.ALLREDUCE, N_RANKS, count, encoding=cd.COLL_LL128,
-                         algorithm=cd.COLL_TWOSHOT, path=cd.COLL_PATH_STREAMED)
+                         algorithm=cd.COLL_TWOSHOT,
+                         path=cd.COLL_PATH_COMPOSED if composed else cd.COLL_PATH_STREAMED)
     ins = make_inputs(count, 4)
     outs = [torch.empty(count, dtype=torch.int16, device="cuda") for _ in range(N_RANKS)]
     K, W = args.steps, args.warmup
-    nk = 3
+    nk = 1 if composed else 3
     events = [[torch.cuda.Event(enable_timing=True) for _ in range(nk + 1)]
               for _ in range(W + K)]
     for evs in events:          # torch creates the CUDA event on first record
@@ -487,8 +491,12 @@ def main() -> int:
     value = replica_value(world, algo_bytes, ms_step)
 
     # per-kernel durations over the timed steps
-    names = ["stage (LL128 encode)", "reduce-scatter fold + publish", "all-gather unpack"]
-    kb = kernel_bytes_allreduce_twoshot(N_RANKS, s_bytes, EPS_LL128)
+    if composed:
+        names = ["composed twoshot (stage / fold + publish / gather CTA groups)"]
+        kb = [bytes_allreduce_twoshot(N_RANKS, s_bytes, EPS_LL128)]
+    else:
+        names = ["stage (LL128 encode)", "reduce-scatter fold + publish", "all-gather unpack"]
+        kb = kernel_bytes_allreduce_twoshot(N_RANKS, s_bytes, EPS_LL128)
     dur = [statistics.mean(events[W + i][k].elapsed_time(events[W + i][k + 1])
                            for i in range(K)) for k in range(nk)]
     kernels = [{"name": names[k], "ms": round(dur[k], 4), "bytes": kb[k],
@@ -499,7 +507,7 @@ def main() -> int:
     prof = os.path.join(ROOT, "profiles", "traffic.md")
     if os.path.exists(prof):
         key = f"allreduce_twoshot_ll128_{args.mib}mib"
-        want = ["stage", "rs", "ag"][dom]
+        want = "composed" if composed else ["stage", "rs", "ag"][dom]
         with open(prof) as f:
             for ln in f:
                 parts = ln.split()
@@ -515,7 +523,8 @@ def main() -> int:
         "config": {"workload": f"all-reduce, {N_RANKS} emulated ranks, {args.mib} MiB bf16 "
                                f"per rank, LL128 lines, twoshot (bandwidth regime)",
                    "n_ranks": N_RANKS, "per_rank_mib": args.mib, "encoding": "LL128",
-                   "algorithm": "twoshot", "parallelism": f"replicas{world}",
+                   "algorithm": "twoshot", "path": args.path,
+                   "parallelism": f"replicas{world}",
                    "l2": "inputs (2 GiB) and staging larger than L2; no flush"},
         "roofline": {"bound": "hbm", "kernel": names[dom], "achieved": round(achieved, 1),
                      "peak": peaks["hbm_gbs"], "unit": "GB/s",

@@ -17,7 +17,7 @@ ROOT = os.path.dirname(HERE)
 BUILD_DIR = os.path.join(ROOT, "_build")
 LIB = os.path.join(HERE, "libcoll.so")
 
-SOURCES = ["kernels.cu", "api.cpp", "derive.cpp", "static_ws.cu", "moe.cu"]
+SOURCES = ["kernels.cu", "api.cpp", "derive.cpp", "static_ws.cu", "moe.cu", "composed.cu"]
 HEADERS = ["plan.h", "derive.h", "launch.h", "dev_common.cuh", "ll8.cuh", "ll128.cuh",
            "pipe.cuh"]
 

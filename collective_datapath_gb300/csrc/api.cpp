@@ -2,6 +2,8 @@
 // and kernel launches.  No device allocation anywhere in this file.
 #include <cuda_runtime.h>
 
+#include <cstdio>
+#include <cstdlib>
 #include <cstring>
 #include <new>
 #include <vector>
@@ -133,6 +135,29 @@ cudaError_t launched(coll_spec* s, cudaError_t e, cudaStream_t st) {
   s->launches += 1;
   if (s->launches < (int)s->events.size()) return cudaEventRecord(s->events[s->launches], st);
   return cudaSuccess;
+}
+
+// Shape of the composed twoshot launch: chunks of 256 lines of every
+// partition, CTA groups split 40 % stage / 25 % fold / 35 % gather of the
+// co-resident grid, a window of 24 chunks (~50 MB of staging in L2 at 8
+// ranks), staging dropped from L2 once folded.  COLL_COMPOSED_SHAPE =
+// "chunk_lines,stage%,fold%,window,discard" overrides it (benchmark sweeps).
+ComposedParams composed_shape(const Plan& p, int grid) {
+  ComposedParams q{};
+  int chunk = 256, stage_pct = 40, fold_pct = 25, window = 24, discard = 1;
+  if (const char* env = std::getenv("COLL_COMPOSED_SHAPE"))
+    std::sscanf(env, "%d,%d,%d,%d,%d", &chunk, &stage_pct, &fold_pct, &window, &discard);
+  chunk = std::max(4, chunk / 4 * 4);
+  uint64_t max_lines = 0;
+  for (const Seg& sg : p.pseg[0]) max_lines = std::max<uint64_t>(max_lines, sg.lines);
+  q.chunk_lines = (uint32_t)chunk;
+  q.nchunks = (uint32_t)((max_lines + chunk - 1) / chunk);
+  q.n_stage = std::max(1, grid * stage_pct / 100);
+  q.n_fold = std::max(1, grid * fold_pct / 100);
+  if (q.n_stage + q.n_fold >= grid) q.n_fold = std::max(1, grid - q.n_stage - 1);
+  q.window = std::max(1, window);
+  q.discard = discard;
+  return q;
 }
 
 // One stream-ordered consume phase: LL128 phases made only of folds or only
@@ -347,6 +372,13 @@ coll_status_t coll_run(coll_spec_t* s, const void* const* dev_ins, void* const* 
     return cuda_status(launched(s, launch_moe_consume(P, st), st));
   }
   const bool empty = p.items1.empty() && p.items2.empty();
+  if (dev_ins != nullptr && p.path == COLL_PATH_COMPOSED && !empty) {
+    const int cap = composed_capacity();
+    if (cap < 3) return COLL_ERR_CUDA;
+    P.cp = composed_shape(p, cap);
+    P.advance_epoch = 1;
+    return cuda_status(launched(s, launch_composed(P, cap, st), st));
+  }
   if (dev_ins != nullptr && p.path == COLL_PATH_FUSED && !empty &&
       !(p.enc == ENC_LL8 && p.reset_mode == COLL_RESET_KERNEL)) {
     P.advance_epoch = 1;

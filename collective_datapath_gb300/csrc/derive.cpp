@@ -180,7 +180,7 @@ int derive(const DeriveInput& in, Plan& p) {
   if (n < 1 || n > kMaxRanks) return COLL_ERR_UNSUPPORTED;
   if (in.dtype != COLL_BF16) return COLL_ERR_UNSUPPORTED;
   if (in.encoding != COLL_LL8 && in.encoding != COLL_LL128) return COLL_ERR_UNSUPPORTED;
-  if (in.reset_mode < 0 || in.reset_mode > 3 || in.path < 0 || in.path > 2 ||
+  if (in.reset_mode < 0 || in.reset_mode > 3 || in.path < 0 || in.path > 3 ||
       in.algorithm < 0 || in.algorithm > 2 || in.ctas < 0 || in.tile_lines < 0)
     return COLL_ERR_INVALID;
 
@@ -237,6 +237,10 @@ int derive(const DeriveInput& in, Plan& p) {
   if (p.path == COLL_PATH_AUTO)
     p.path = (in_bytes_per_rank <= 256 * 1024 && p.enc == ENC_LL8) ? COLL_PATH_FUSED
                                                                   : COLL_PATH_STREAMED;
+
+  if (p.path == COLL_PATH_COMPOSED &&
+      !(p.kind == CK_ALLREDUCE && p.algorithm == COLL_TWOSHOT && p.enc == ENC_LL128))
+    return COLL_ERR_UNSUPPORTED;
 
   // Rank images of region P.
   for (int r = 0; r < n; ++r) {

@@ -73,7 +73,10 @@ struct WsHeader {
   uint32_t arrived;        // warps of the run's final launch that read the epoch
   uint32_t started[2];     // fused runs: worker CTAs that started, by slot
   uint64_t rejections;     // stale lines observed (diagnostic)
-  uint64_t pad1[26];
+  // composed twoshot: completed units per role, by slot (flow control only)
+  uint32_t fold_done[2];
+  uint32_t gather_done[2];
+  uint64_t pad1[24];
 };
 static_assert(sizeof(WsHeader) == 256, "WsHeader layout");
 
@@ -98,6 +101,16 @@ struct MoeParams {
   uint32_t* out_off;    // [N dest][el][N src] first output row of the block
   uint32_t* rows_dest;  // [N]
   int32_t* counts_out;  // [N dest][el][N src] counts, then rows per destination
+};
+
+// Composed twoshot all-reduce (one persistent launch, Purlin Algorithm 1):
+// CTA roles and the chunking of every partition.
+struct ComposedParams {
+  uint32_t chunk_lines;  // lines of one partition per chunk (multiple of 4)
+  uint32_t nchunks;
+  int n_stage, n_fold;   // CTAs of the stage and fold groups; the rest gather
+  int window;            // a role may run this many chunks ahead of the next one
+  int discard;           // drop consumed staging lines from L2 (no write-back)
 };
 
 // Everything a kernel launch needs; passed by value (captured by graphs).
@@ -134,6 +147,7 @@ struct RunParams {
   int64_t late_n[kMaxRanks];
   int late_ctas;                  // extra CTAs at the end of the grid
   MoeParams moe;
+  ComposedParams cp;
   // withheld staging (fault-injection runs)
   const int64_t* wh_lines;
   const int32_t* wh_kind;

@@ -130,3 +130,36 @@ def test_config4_reduce_scatter_and_all_gather(cd, inputs, mib):
     assert torch.equal(ar_outs[5], gathered[0])
     del ar, ar_outs, outs, gathered
     torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("mib", [32, 256])
+def test_config4_allreduce_composed_twoshot(cd, inputs, mib):
+    """The one-launch twoshot at full size: sampled against the oracle, and
+    byte-identical to the stream-ordered twoshot on every element."""
+    import torch
+
+    count = mib * 1024 * 1024 // 2
+    ins = [x[:count] for x in inputs]
+    comp = cd.Collective(cd.ALLREDUCE, N, count, encoding=cd.COLL_LL128,
+                         algorithm=cd.COLL_TWOSHOT, path=cd.COLL_PATH_COMPOSED)
+    outs = [torch.empty(count, dtype=torch.int16, device="cuda") for _ in range(N)]
+    for _ in range(2):
+        comp.run(ins, outs)
+    code, rank, line = comp.status()
+    assert code == cd.COLL_OK, (code, rank, line)
+    pos = sample_positions(count, 50 + mib)
+    want = sampled_reference(inputs, count, pos)
+    got = outs[0][torch.from_numpy(pos).cuda()].cpu().numpy().view(np.uint16)
+    assert np.array_equal(got, want)
+    del comp
+    ref = cd.Collective(cd.ALLREDUCE, N, count, encoding=cd.COLL_LL128,
+                        algorithm=cd.COLL_TWOSHOT, path=cd.COLL_PATH_STREAMED)
+    ref_out = torch.empty(count, dtype=torch.int16, device="cuda")
+    tmp = [ref_out] + [torch.empty(count, dtype=torch.int16, device="cuda")
+                       for _ in range(N - 1)]
+    ref.run(ins, tmp)
+    assert ref.status()[0] == cd.COLL_OK
+    for r in range(N):
+        assert torch.equal(outs[r], ref_out), f"rank {r}"
+    del ref, tmp, outs
+    torch.cuda.empty_cache()

@@ -229,3 +229,25 @@ def test_graph_replay_advances_epoch_on_device(cd, enc):
         torch.cuda.synchronize()
         check(coll, outs, oracle.allreduce(xs), n)
     assert coll.epoch() == 5
+
+
+@pytest.mark.parametrize("n,count", [(8, 8 * 1000), (8, 8 * 60 * 1024 + 64), (3, 3000),
+                                     (2, 2 * 4096), (8, 8 * 60 * 300)])
+@pytest.mark.parametrize("shape", [None, "8,30,30,2,1", "64,40,25,1,0", "4,20,20,3,1"])
+def test_composed_twoshot_matches_the_oracle(cd, n, count, shape, monkeypatch):
+    """The one-launch twoshot (stage / fold / gather CTA groups pipelined by
+    chunk): bit-exact against the oracle over several epochs, for several
+    chunk sizes, group splits and windows, with and without dropping the
+    folded staging lines from L2."""
+    if shape is not None:
+        monkeypatch.setenv("COLL_COMPOSED_SHAPE", shape)
+    coll = make(cd, cd.ALLREDUCE, n, count, encoding=cd.COLL_LL128,
+                algorithm=cd.COLL_TWOSHOT, path=cd.COLL_PATH_COMPOSED)
+    _, ins, outs = buffers(coll, n, seed=10)
+    for e in range(1, 4):
+        xs = [synth.normal_bf16(100 + e, count, n, r) for r in range(n)]
+        for r in range(n):
+            ins[r].copy_(to_dev(xs[r]))
+        coll.run(ins, outs)
+        check(coll, outs, oracle.allreduce(xs), n)
+        assert coll.epoch() == e + 1
