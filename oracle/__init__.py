@@ -86,6 +86,11 @@ def _declare(L: ctypes.CDLL) -> None:
                                          ctypes.POINTER(_u16p),
                                          ctypes.POINTER(_u16p)]
     L.orc_allreduce_composed.restype = ctypes.c_int
+    for name in ("orc_reduce_scatter_v", "orc_all_gather_v", "orc_all_to_all_v"):
+        f = getattr(L, name)
+        f.argtypes = [ctypes.c_int, ctypes.POINTER(_sz), ctypes.POINTER(_u16p),
+                      ctypes.POINTER(_u16p)]
+        f.restype = ctypes.c_int
     L.orc_moe_dispatch.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                    ctypes.c_int, ctypes.c_int,
                                    ctypes.POINTER(_i32p),
@@ -197,6 +202,35 @@ def all_gather(ins: Sequence[np.ndarray], count: int) -> list[np.ndarray]:
 def all_to_all(ins: Sequence[np.ndarray]) -> list[np.ndarray]:
     count = int(np.asarray(ins[0]).size)
     return _collective("orc_all_to_all", ins, count, count)
+
+
+def _v_call(name, ins, lens, out_sizes):
+    n = len(ins)
+    arrs = [_c(np.asarray(x).ravel(), np.uint16) for x in ins]
+    arrs = [a if a.size else np.zeros(1, np.uint16) for a in arrs]
+    outs = [np.zeros(max(int(o), 1), dtype=np.uint16) for o in out_sizes]
+    ln = (_sz * len(lens))(*[int(v) for v in lens])
+    rc = getattr(lib(), name)(n, ln, _ptr_array(arrs, ctypes.c_uint16),
+                              _ptr_array(outs, ctypes.c_uint16))
+    if rc != 0:
+        raise ValueError(f"{name}: invalid arguments")
+    return [o[:int(sz)] for o, sz in zip(outs, out_sizes)]
+
+
+def reduce_scatter_v(ins: Sequence[np.ndarray], lens: Sequence[int]) -> list[np.ndarray]:
+    return _v_call("orc_reduce_scatter_v", ins, lens, lens)
+
+
+def all_gather_v(ins: Sequence[np.ndarray], lens: Sequence[int]) -> list[np.ndarray]:
+    return _v_call("orc_all_gather_v", ins, lens, [sum(lens)] * len(ins))
+
+
+def all_to_all_v(ins: Sequence[np.ndarray], lens: Sequence[Sequence[int]]) -> list[np.ndarray]:
+    """lens[p][d] = elements source p sends to destination d."""
+    n = len(ins)
+    flat = [int(lens[p][d]) for p in range(n) for d in range(n)]
+    return _v_call("orc_all_to_all_v", ins, flat,
+                   [sum(lens[p][d] for p in range(n)) for d in range(n)])
 
 
 def allreduce_composed(ins: Sequence[np.ndarray]) -> list[np.ndarray]:

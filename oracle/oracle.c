@@ -149,6 +149,55 @@ int orc_all_to_all(int n, size_t count, const uint16_t *const *in,
     return 0;
 }
 
+int orc_reduce_scatter_v(int n, const size_t *len, const uint16_t *const *in,
+                         uint16_t *const *out)
+{
+    if (bad_args(n, in, out) || len == NULL)
+        return -1;
+    size_t off = 0;
+    for (int r = 0; r < n; ++r) {
+        for (size_t j = 0; j < len[r]; ++j)
+            out[r][j] = orc_fold(in, n, off + j);
+        off += len[r];
+    }
+    return 0;
+}
+
+int orc_all_gather_v(int n, const size_t *len, const uint16_t *const *in,
+                     uint16_t *const *out)
+{
+    if (bad_args(n, in, out) || len == NULL)
+        return -1;
+    for (int d = 0; d < n; ++d) {
+        size_t off = 0;
+        for (int p = 0; p < n; ++p) {
+            for (size_t j = 0; j < len[p]; ++j)
+                out[d][off + j] = in[p][j];
+            off += len[p];
+        }
+    }
+    return 0;
+}
+
+int orc_all_to_all_v(int n, const size_t *len, const uint16_t *const *in,
+                     uint16_t *const *out)
+{
+    if (bad_args(n, in, out) || len == NULL)
+        return -1;
+    for (int d = 0; d < n; ++d) {
+        size_t dst = 0;
+        for (int p = 0; p < n; ++p) {
+            size_t src = 0;
+            for (int k = 0; k < d; ++k)
+                src += len[(size_t)p * n + k];
+            for (size_t j = 0; j < len[(size_t)p * n + d]; ++j)
+                out[d][dst + j] = in[p][src + j];
+            dst += len[(size_t)p * n + d];
+        }
+    }
+    return 0;
+}
+
 int orc_allreduce_composed(int n, size_t count, const uint16_t *const *in,
                            uint16_t *const *out, uint16_t *const *tmp)
 {

@@ -109,6 +109,23 @@ int orc_all_gather(int n, size_t count, const uint16_t *const *in,
 int orc_all_to_all(int n, size_t count, const uint16_t *const *in,
                    uint16_t *const *out);
 
+/* Variable-length (V) collectives ([Purlin] §3.1: the V variants keep the
+ * layouts' relations but take partition sizes at runtime; §2.1 contracts).
+ * len[] are element counts; offsets are their prefix sums.
+ * RSV: every rank holds sum(len) elements partitioned by len;
+ *      out_r[j] = fold over p of in_p[off_r + j], j < len[r].
+ * AGV: rank p contributes len[p] elements; out_d = in_0 | in_1 | ... in rank
+ *      order (sum(len) elements).
+ * A2AV: len[p*n + d] = elements source p sends to destination d; source p's
+ *      buffer holds its partitions in destination order; out_d = partition d
+ *      of source 0 | of source 1 | ... in source-rank order. */
+int orc_reduce_scatter_v(int n, const size_t *len, const uint16_t *const *in,
+                         uint16_t *const *out);
+int orc_all_gather_v(int n, const size_t *len, const uint16_t *const *in,
+                     uint16_t *const *out);
+int orc_all_to_all_v(int n, const size_t *len, const uint16_t *const *in,
+                     uint16_t *const *out);
+
 /* Twoshot all-reduce written as the composition of [Purlin] §3.1
  * "Composing transformations": reduce-scatter into a packed intermediate,
  * then all-gather of that intermediate.  `tmp` holds n intermediates of

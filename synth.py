@@ -18,6 +18,8 @@ Recipe (every stream is independent and reproducible):
 * top-k experts without replacement: per token, the first k entries of an
   argsort of independent uniform keys (a uniformly random k-subset, in
   random order).
+* variable-length splits (V collectives): the Zipf split with exponent s of
+  the Purlin page's Eq. (4) (see ``zipf_split``), in bytes, 128-byte units.
 * stale lines of an epoch: exactly ``round(frac * lines)`` distinct line
   indices (the first of a random permutation), a random publication order of
   them, a stale-kind per line (0: previous epoch's flag e-1, 1: the slot's
@@ -112,3 +114,28 @@ def stale_plan(seed: int, lines: int, frac: float, *index: int):
     mant = g.integers(0, 128, size=m).astype(np.uint16)
     poison = (sign | np.uint16(0x90 << 7) | mant).astype(np.uint16)
     return idx, order, kind, poison
+
+
+def zipf_split(total_bytes: int, ranks: int = 8, s: float = 0.125) -> list[int]:
+    """Bytes per rank of a Zipf split of ``total_bytes`` (Purlin, appendix
+    "Variable-length splits", Eq. (4)): with u = max(128, T / (8 W)) bytes
+    and x_r = (T / u) (r+1)^-s / sum_k (k+1)^-s, rank r gets u (floor(x_r) +
+    d_r), the remaining units going one each to the ranks with the largest
+    fractional parts of x_r (ties to the lower rank)."""
+    u = max(128, total_bytes // (8 * ranks))
+    units = total_bytes // u
+    w = [(r + 1) ** -s for r in range(ranks)]
+    tot = sum(w)
+    x = [units * wr / tot for wr in w]
+    fl = [int(np.floor(v)) for v in x]
+    left = units - sum(fl)
+    order = sorted(range(ranks), key=lambda r: (-(x[r] - fl[r]), r))
+    for r in order[:left]:
+        fl[r] += 1
+    return [u * f for f in fl]
+
+
+def rotate_right(v: list, k: int) -> list:
+    """The vector v rotated right by k positions (A2AV partition vectors)."""
+    k %= len(v)
+    return v[-k:] + v[:-k] if k else list(v)

@@ -35,6 +35,9 @@ MUTANTS = [
     ("ll128_big_endian_seq", "line[120 + b] = (uint8_t)((epoch >> (8 * b)) & 0xFFu);", "line[120 + b] = (uint8_t)((epoch >> (8 * (7 - b))) & 0xFFu);"),
     ("ll128_59_per_line", "size_t idx = j * 60u + q;\n            uint16_t v", "size_t idx = j * 59u + q;\n            uint16_t v"),
     ("moe_source_transposed", "counts[e * n + p] += 1;", "counts[e * n + (n - 1 - p)] += 1;"),
+    ("rsv_offset_not_advanced", "            out[r][j] = orc_fold(in, n, off + j);\n        off += len[r];", "            out[r][j] = orc_fold(in, n, off + j);\n        off += 0;"),
+    ("a2av_source_offset", "                src += len[(size_t)p * n + k];", "                src += len[(size_t)k * n + p];"),
+    ("agv_rank_order", "                out[d][off + j] = in[p][j];\n            off += len[p];", "                out[d][off + j] = in[n - 1 - p][j];\n            off += len[p];"),
     ("moe_source_major_order", "for (int le = 0; le < el; ++le) {\n            int e = d * el + le;\n            for (int p = 0; p < n; ++p)",
      "for (int le = 0; le < el; ++le) {\n            int e = d * el + le;\n            for (int p = n - 1; p >= 0; --p)"),
 ]
@@ -60,6 +63,8 @@ PINS = [
     pins.test_ll128_line_layout_hand_case,
     pins.test_ll128_rejects_other_sequence_numbers,
     pins.test_moe_tiny_hand_derived_layout,
+    pins.test_v_collectives_invariants_on_zipf_splits,
+    pins.test_all_to_all_v_hand_case,
     pins.test_moe_counts_and_rows_invariants,
 ]
 

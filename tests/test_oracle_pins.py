@@ -414,3 +414,61 @@ def test_moe_row_sources_agree_with_the_materialised_dispatch(orc):
         sr, st = orc.moe_row_sources(topk, experts, d)
         assert sr.size == rows[d]
         assert np.array_equal(np.stack([ins[p][t] for p, t in zip(sr, st)]), outs[d])
+
+
+# ---- variable-length (V) collectives and the Zipf split ----------------------------
+
+def test_zipf_split_matches_the_worked_values_and_stated_bounds():
+    spec = json.load(open(os.path.join(GOLDEN, "zipf_split.json")))
+    for t, want in spec["cases"].items():
+        assert synth.zipf_split(int(t)) == want
+    for e in range(13, 31):                       # 8 KiB .. 1 GiB
+        t = 1 << e
+        v = synth.zipf_split(t)
+        assert sum(v) == t and all(x % 128 == 0 for x in v)
+        assert max(v) == 1.125 * t / 8
+        assert v == sorted(v, reverse=True)
+    assert synth.rotate_right([0, 1, 2, 3], 1) == [3, 0, 1, 2]
+
+
+def test_v_collectives_reduce_to_the_fixed_ones_on_equal_partitions(orc):
+    n, m = 8, 64
+    xs = [synth.normal_bf16(21, n * m, p) for p in range(n)]
+    eq = [m] * n
+    assert all(np.array_equal(a, b) for a, b in
+               zip(orc.reduce_scatter_v(xs, eq), orc.reduce_scatter(xs)))
+    assert all(np.array_equal(a, b) for a, b in
+               zip(orc.all_to_all_v(xs, [[m] * n for _ in range(n)]), orc.all_to_all(xs)))
+    shards = [x[:m] for x in xs]
+    assert all(np.array_equal(a, b) for a, b in
+               zip(orc.all_gather_v(shards, eq), orc.all_gather(shards, n * m)))
+
+
+def test_v_collectives_invariants_on_zipf_splits(orc):
+    n = 8
+    lens = [b // 2 for b in synth.zipf_split(8192)]          # elements
+    t = sum(lens)
+    xs = [synth.normal_bf16(22, t, p) for p in range(n)]
+    rs = orc.reduce_scatter_v(xs, lens)
+    assert [r.size for r in rs] == lens
+    ar = orc.allreduce(xs)
+    ag = orc.all_gather_v(rs, lens)
+    for a in ag:
+        assert np.array_equal(a, ar[0])                     # AGV o RSV == AR
+    # A2AV with the rotated vectors (rank r sends rotate_right(lens, r+1)),
+    # then back with the transposed sizes, is the identity
+    send = [synth.rotate_right(lens, r + 1) for r in range(n)]
+    ys = [synth.random_bits16(23, t, p) for p in range(n)]
+    fwd = orc.all_to_all_v(ys, send)
+    assert all(f.size == t for f in fwd)                     # every rank receives T
+    back = orc.all_to_all_v(fwd, [[send[d][p] for d in range(n)] for p in range(n)])
+    for p in range(n):
+        assert np.array_equal(back[p], ys[p])
+
+
+def test_all_to_all_v_hand_case(orc):
+    a = np.arange(1, 25, dtype=np.uint16)          # source 0: 8 for d0, 16 for d1
+    b = np.arange(101, 125, dtype=np.uint16)       # source 1: 24 for d0, 0 for d1
+    out = orc.all_to_all_v([a, b], [[8, 16], [24, 0]])
+    assert out[0].tolist() == list(range(1, 9)) + list(range(101, 125))
+    assert out[1].tolist() == list(range(9, 25))
