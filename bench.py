@@ -355,6 +355,54 @@ def bandwidth_row(cd, triple, count_in_out, kind, stream, steps=5) -> dict:
             "status": st}
 
 
+def v_row(cd, name, total_bytes, stream, steps=5) -> dict:
+    """Variable-length collective on a Zipf split (exponent 0.125) of a total
+    of `total_bytes` over 8 ranks, LL128 lines, streamed path.  all-to-all V
+    rotates each source's split right by (source + 1).  `algbw` is the
+    total T over the time, as the variable-length experiment reports it."""
+    import torch
+
+    import synth
+
+    n = N_RANKS
+    base = [b // 2 for b in synth.zipf_split(total_bytes, n)]
+    if name == "ALLTOALL_V":
+        v = [synth.rotate_right(base, p + 1) for p in range(n)]
+        count = 0
+    else:
+        v, count = base, sum(base)
+    coll = cd.Collective(getattr(cd, name), n, count, encoding=cd.COLL_LL128,
+                         path=cd.COLL_PATH_STREAMED, vcounts=v)
+    ins = make_inputs(max(max(coll.elems(r)[0] for r in range(n)), 8), 12)
+    ins = [x[:coll.elems(r)[0]] for r, x in enumerate(ins)]
+    outs = [torch.empty(max(coll.elems(r)[1], 8), dtype=torch.int16, device="cuda")
+            for r in range(n)]
+    with torch.cuda.stream(stream):
+        for _ in range(2):
+            coll.run(ins, outs, stream)
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(steps):
+            coll.run(ins, outs, stream)
+        e1.record(stream)
+        stream.synchronize()
+    ms = e0.elapsed_time(e1) / steps
+    t = float(total_bytes)
+    if name == "REDUCE_SCATTER_V":
+        b = bytes_reduce_scatter(n, t, EPS_LL128)
+    elif name == "ALLGATHER_V":
+        b = bytes_all_gather(n, t, EPS_LL128)
+    else:
+        b = 2 * n * t * (1 + EPS_LL128)
+    st = coll.status(stream)[0]
+    coll.close()
+    del coll, ins, outs
+    torch.cuda.empty_cache()
+    return {"ms": round(ms, 4), "GB/s": round(b / ms / 1e6, 1), "algbw_GB/s": round(t / ms / 1e6, 1),
+            "algorithmic_bytes": b, "status": st}
+
+
 def moe_row(cd, stream, steps=5) -> dict:
     """MoE dispatch: 8 ranks x 4096 tokens x 7168 bf16, top-8 of 256 experts
     (routing drawn on the device from a seeded generator)."""
@@ -585,6 +633,9 @@ def main() -> int:
             "reduce_scatter_256MiB": bandwidth_row(cd, cd.REDUCE_SCATTER, count, "rs", stream),
             "all_gather_256MiB": bandwidth_row(cd, cd.ALLGATHER, count, "ag", stream),
             "moe_dispatch_8x4096x7168_top8of256": moe_row(cd, stream),
+            "reduce_scatter_v_zipf_256MiB": v_row(cd, "REDUCE_SCATTER_V", 256 << 20, stream),
+            "all_gather_v_zipf_256MiB": v_row(cd, "ALLGATHER_V", 256 << 20, stream),
+            "all_to_all_v_zipf_256MiB": v_row(cd, "ALLTOALL_V", 256 << 20, stream),
         }
         line["latency_us_per_op"] = latency_sweep(cd, stream)
         if world == 1:

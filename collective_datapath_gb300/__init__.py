@@ -52,7 +52,8 @@ class coll_options_t(ctypes.Structure):
                 ("ctas", ctypes.c_int), ("tile_lines", ctypes.c_int),
                 ("timeout_ns", ctypes.c_uint64), ("tokens", ctypes.c_int),
                 ("hidden", ctypes.c_int), ("topk", ctypes.c_int),
-                ("experts", ctypes.c_int), ("max_rows", ctypes.c_int)]
+                ("experts", ctypes.c_int), ("max_rows", ctypes.c_int),
+                ("vcounts", ctypes.POINTER(ctypes.c_uint64)), ("nvcounts", ctypes.c_int)]
 
 
 _vp = ctypes.c_void_p
@@ -144,10 +145,17 @@ def _ptr_array(ts: Sequence) -> ctypes.Array:
 def options(**kw) -> coll_options_t:
     o = coll_options_t()
     _lib.coll_options_default(ctypes.byref(o))
+    vc = kw.pop("vcounts", None)
     for k, v in kw.items():
         if not hasattr(o, k):
             raise TypeError(f"unknown option {k}")
         setattr(o, k, v)
+    if vc is not None:
+        flat = [int(x) for row in vc for x in (row if hasattr(row, "__len__") else [row])]
+        arr = (ctypes.c_uint64 * len(flat))(*flat)
+        o._vcounts_keepalive = arr
+        o.vcounts = ctypes.cast(arr, ctypes.POINTER(ctypes.c_uint64))
+        o.nvcounts = len(flat)
     return o
 
 
@@ -312,6 +320,9 @@ ALLREDUCE = (COLL_SCATTERED, COLL_SCATTERED, COLL_REDUCE)
 REDUCE_SCATTER = (COLL_SCATTERED, COLL_PACKED, COLL_REDUCE)
 ALLGATHER = (COLL_PACKED, COLL_SCATTERED, COLL_COPY)
 ALLTOALL = (COLL_SCATTERED, COLL_TRANSPOSED, COLL_COPY)
+REDUCE_SCATTER_V = (COLL_SCATTERED_V, COLL_PACKED_V, COLL_REDUCE)
+ALLGATHER_V = (COLL_PACKED_V, COLL_SCATTERED_V, COLL_COPY)
+ALLTOALL_V = (COLL_SCATTERED_V, COLL_TRANSPOSED_V, COLL_COPY)
 MOE_DISPATCH = (COLL_SCATTERED_V, COLL_TRANSPOSED_V, COLL_COPY)
 
 

@@ -253,6 +253,8 @@ coll_status_t coll_spec_create(coll_layout_t in_layout, coll_layout_t out_layout
   d.topk = o.topk;
   d.experts = o.experts;
   d.max_rows = o.max_rows;
+  if (o.vcounts != nullptr && o.nvcounts > 0)
+    d.vcounts.assign(o.vcounts, o.vcounts + o.nvcounts);
   device_shape(o.encoding, &d.sms, &d.fused_capacity);
   coll_spec* s = new (std::nothrow) coll_spec();
   if (s == nullptr) return COLL_ERR_INVALID;
@@ -523,7 +525,8 @@ coll_status_t coll_run_late(coll_spec_t* s, const void* const* dev_ins, void* co
     return COLL_ERR_INVALID;
   if (!s->bound) return COLL_ERR_STATE;
   const Plan& p = s->plan;
-  if (p.kind == CK_ALLGATHER || p.enc == ENC_LL8 && p.reset_mode == COLL_RESET_KERNEL)
+  if (p.kind == CK_ALLGATHER || p.kind == CK_ALLGATHER_V || p.kind == CK_ALLTOALL_V ||
+      (p.enc == ENC_LL8 && p.reset_mode == COLL_RESET_KERNEL))
     return COLL_ERR_UNSUPPORTED;  // late producers need identical rank images
   if (coll_status_t e = check_outs(s, dev_outs)) return e;
   if (coll_status_t e = check_ins(s, dev_ins)) return e;

@@ -193,22 +193,47 @@ int derive(const DeriveInput& in, Plan& p) {
     p.kind = CK_ALLGATHER;
   else if (L == COLL_SCATTERED && O == COLL_TRANSPOSED && in.op == COLL_COPY)
     p.kind = CK_ALLTOALL;
-  else if (L == COLL_SCATTERED_V && O == COLL_TRANSPOSED_V && in.op == COLL_COPY)
-    return derive_moe(in, p);
-  else
+  else if (L == COLL_SCATTERED_V && O == COLL_PACKED_V && in.op == COLL_REDUCE)
+    p.kind = CK_REDUCE_SCATTER_V;
+  else if (L == COLL_PACKED_V && O == COLL_SCATTERED_V && in.op == COLL_COPY)
+    p.kind = CK_ALLGATHER_V;
+  else if (L == COLL_SCATTERED_V && O == COLL_TRANSPOSED_V && in.op == COLL_COPY) {
+    if (in.experts > 0) return derive_moe(in, p);
+    p.kind = CK_ALLTOALL_V;
+  } else
     return COLL_ERR_UNSUPPORTED;
 
-  if (in.count % 8 != 0) return COLL_ERR_ALIGN;
+  // V collectives: runtime sizes (Purlin §3.1, V layouts), each a multiple
+  // of 8 elements so that every segment starts 16-byte aligned.
+  const bool vkind = p.kind == CK_REDUCE_SCATTER_V || p.kind == CK_ALLGATHER_V ||
+                     p.kind == CK_ALLTOALL_V;
+  std::vector<uint64_t> V;  // [n] or [n * n]
+  uint64_t count_in = in.count;
+  if (vkind) {
+    const size_t want = p.kind == CK_ALLTOALL_V ? (size_t)n * n : (size_t)n;
+    if (in.vcounts.size() != want) return COLL_ERR_INVALID;
+    V = in.vcounts;
+    uint64_t sum = 0;
+    for (uint64_t v : V) {
+      if (v % 8 != 0) return COLL_ERR_ALIGN;
+      if (v > (1ull << 40)) return COLL_ERR_INVALID;
+      sum += v;
+    }
+    if (p.kind != CK_ALLTOALL_V && sum != in.count) return COLL_ERR_INVALID;
+    if (p.kind == CK_ALLTOALL_V) count_in = 0;
+  }
+
+  if (count_in % 8 != 0) return COLL_ERR_ALIGN;
   p.enc = in.encoding;
   p.n = n;
-  p.count = in.count;
-  p.shard = shard_elems(in.count, n);
+  p.count = count_in;
+  p.shard = shard_elems(count_in, n);
   p.reset_mode = p.enc == ENC_LL8 ? in.reset_mode : COLL_RESET_NONE;
   p.timeout_ns = in.timeout_ns ? in.timeout_ns : 200000000ull;
   if (p.kind == CK_ALLTOALL && p.shard * (uint64_t)n != in.count)
     return COLL_ERR_ALIGN;  // the exchange needs equal partitions
 
-  const uint64_t count = in.count, M = p.shard;
+  const uint64_t count = count_in, M = p.shard;
   uint64_t in_bytes_per_rank = 0;
   for (int r = 0; r < n; ++r) {
     switch (p.kind) {
@@ -216,6 +241,15 @@ int derive(const DeriveInput& in, Plan& p) {
       case CK_REDUCE_SCATTER: p.in_elems[r] = count; p.out_elems[r] = shard_len(count, n, r); break;
       case CK_ALLGATHER: p.in_elems[r] = shard_len(count, n, r); p.out_elems[r] = count; break;
       case CK_ALLTOALL: p.in_elems[r] = count; p.out_elems[r] = count; break;
+      case CK_REDUCE_SCATTER_V: p.in_elems[r] = count; p.out_elems[r] = V[r]; break;
+      case CK_ALLGATHER_V: p.in_elems[r] = V[r]; p.out_elems[r] = count; break;
+      case CK_ALLTOALL_V:
+        p.in_elems[r] = p.out_elems[r] = 0;
+        for (int k = 0; k < n; ++k) {
+          p.in_elems[r] += V[(size_t)r * n + k];
+          p.out_elems[r] += V[(size_t)k * n + r];
+        }
+        break;
       default: break;
     }
     in_bytes_per_rank = std::max<uint64_t>(in_bytes_per_rank, 2 * p.in_elems[r]);
@@ -245,7 +279,16 @@ int derive(const DeriveInput& in, Plan& p) {
   // Rank images of region P.
   for (int r = 0; r < n; ++r) {
     std::vector<std::pair<uint64_t, uint64_t>> parts;
-    if (L == COLL_SCATTERED) {
+    if (p.kind == CK_REDUCE_SCATTER_V || p.kind == CK_ALLTOALL_V) {
+      // partition k of rank r: V[k] (RS-V) or V[r][k] (A2A-V) elements,
+      // packed back to back in the input
+      uint64_t at = 0;
+      for (int k = 0; k < n; ++k) {
+        const uint64_t len = p.kind == CK_REDUCE_SCATTER_V ? V[k] : V[(size_t)r * n + k];
+        parts.push_back({len, at});
+        at += len;
+      }
+    } else if (L == COLL_SCATTERED) {
       for (int k = 0; k < n; ++k) parts.push_back({shard_len(count, n, k), shard_begin(count, n, k)});
     } else {
       parts.push_back({p.in_elems[r], 0});
@@ -296,7 +339,11 @@ int derive(const DeriveInput& in, Plan& p) {
     for (auto& s : segs) v.push_back(s.lines);
     return v;
   };
-  const Tiler stage_tiler{pick_tile(seg_lines(p.pseg[0])), p.enc};
+  // Rank images may differ (V layouts, a ragged last partition): the stage
+  // tile is the largest any rank needs.
+  uint64_t stile = 4;
+  for (int r = 0; r < n; ++r) stile = std::max(stile, pick_tile(seg_lines(p.pseg[r])));
+  const Tiler stage_tiler{stile, p.enc};
   const uint64_t epl = (uint64_t)line_elems(p.enc);
 
   // Stage items.
@@ -400,6 +447,66 @@ int derive(const DeriveInput& in, Plan& p) {
             p.items1.push_back(it);
           });
         }
+      break;
+    }
+    case CK_REDUCE_SCATTER_V: {
+      // every rank's image has the same segments; owner r folds segment r
+      std::vector<uint64_t> mine;
+      for (int r = 0; r < n; ++r) mine.push_back(p.pseg[0][r].lines);
+      uint64_t tile = 4;
+      for (uint64_t l : mine) tile = std::max(tile, pick_tile({l}));
+      const Tiler t{tile, p.enc};
+      for (int r = 0; r < n; ++r) {
+        const Seg& s = p.pseg[0][r];
+        t.over(s, [&](uint64_t t0, uint64_t nl, uint64_t ne) {
+          Item it = make_item(IK_REDUCE, r, 0, s.line0 + t0, nl, ne, t0 * epl);
+          set_reset(it, 1, 0);
+          p.items1.push_back(it);
+        });
+      }
+      break;
+    }
+    case CK_ALLGATHER_V: {
+      // every rank copies every contribution q to offset sum_{q'<q} V[q']
+      std::vector<uint64_t> all;
+      for (int q = 0; q < n; ++q) all.push_back(p.pseg[q][0].lines);
+      const Tiler t{pick_tile(all), p.enc};
+      for (int d = 0; d < n; ++d) {
+        uint64_t at = 0;
+        for (int q = 0; q < n; ++q) {
+          const Seg& s = p.pseg[q][0];
+          t.over(s, [&](uint64_t t0, uint64_t nl, uint64_t ne) {
+            Item it = make_item(IK_COPY, d, q, s.line0 + t0, nl, ne, at + t0 * epl);
+            set_reset(it, n, ctr.get(3, ((uint64_t)q << 40) | (s.line0 + t0)));
+            p.items1.push_back(it);
+          });
+          at += V[q];
+        }
+      }
+      break;
+    }
+    case CK_ALLTOALL_V: {
+      // destination d copies segment d of every source q, in source order,
+      // to offset sum_{q'<q} V[q'][d]
+      uint64_t tile = 4;
+      for (int d = 0; d < n; ++d) {
+        std::vector<uint64_t> mine;
+        for (int q = 0; q < n; ++q) mine.push_back(p.pseg[q][d].lines);
+        tile = std::max(tile, pick_tile(mine));
+      }
+      const Tiler t{tile, p.enc};
+      for (int d = 0; d < n; ++d) {
+        uint64_t at = 0;
+        for (int q = 0; q < n; ++q) {
+          const Seg& s = p.pseg[q][d];
+          t.over(s, [&](uint64_t t0, uint64_t nl, uint64_t ne) {
+            Item it = make_item(IK_COPY, d, q, s.line0 + t0, nl, ne, at + t0 * epl);
+            set_reset(it, 1, 0);
+            p.items1.push_back(it);
+          });
+          at += V[(size_t)q * n + d];
+        }
+      }
       break;
     }
     default:

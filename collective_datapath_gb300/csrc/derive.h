@@ -20,7 +20,8 @@
 
 namespace coll {
 
-enum CollKind { CK_ALLREDUCE, CK_REDUCE_SCATTER, CK_ALLGATHER, CK_ALLTOALL, CK_MOE };
+enum CollKind { CK_ALLREDUCE, CK_REDUCE_SCATTER, CK_ALLGATHER, CK_ALLTOALL, CK_MOE,
+                CK_REDUCE_SCATTER_V, CK_ALLGATHER_V, CK_ALLTOALL_V };
 
 struct Seg {
   uint64_t line0;    // first line in the rank image
@@ -36,6 +37,7 @@ struct DeriveInput {
   int encoding, algorithm, reset_mode, path, ctas, tile_lines;
   uint64_t timeout_ns;
   int tokens, hidden, topk, experts, max_rows;
+  std::vector<uint64_t> vcounts;  // V collectives (see coll.h)
   int sms;             // device SM count (a default when no device is present)
   int fused_capacity;  // co-resident CTAs of the fused kernel
 };

@@ -25,7 +25,12 @@
  *   (SCATTERED,   PACKED,      REDUCE)  reduce-scatter  in = count, out = len(r)
  *   (PACKED,      SCATTERED,   COPY)    all-gather      in = len(p), out = count
  *   (SCATTERED,   TRANSPOSED,  COPY)    all-to-all      in = out = count
- *   (SCATTERED_V, TRANSPOSED_V,COPY)    MoE dispatch    (rows routed by top-k)
+ *   (SCATTERED_V, PACKED_V,    REDUCE)  reduce-scatter V  in = count, out = vcounts[r]
+ *   (PACKED_V,    SCATTERED_V, COPY)    all-gather V      in = vcounts[p], out = count
+ *   (SCATTERED_V, TRANSPOSED_V,COPY)    all-to-all V      sizes from vcounts[p][d];
+ *                                       MoE dispatch      when experts > 0 (rows
+ *                                       routed by top-k)
+ * V variants keep the layouts' relations with runtime sizes (Purlin §3.1).
  * Partition r of a scattered buffer covers [r*M, min(count, (r+1)*M)) with
  * M = roundup(ceil(count / nranks), 8) elements (equal partitions when
  * 8*nranks divides count).  Every other triple returns COLL_ERR_UNSUPPORTED.
@@ -149,6 +154,16 @@ typedef struct {
     int experts;         /* total experts, a multiple of nranks (<= 1024) */
     int max_rows;        /* output rows each destination can hold, 0 = the
                             worst case tokens * nranks * min(topk, experts/nranks) */
+    /* Variable-length collectives (V layouts, MoE dispatch excepted): element
+     * counts, each a multiple of 8, copied at coll_spec_create.
+     *   reduce-scatter V: nranks entries, the output of each rank (their sum
+     *     is every rank's input, `count` of the spec);
+     *   all-gather V: nranks entries, the contribution of each rank (their sum
+     *     is every rank's output, `count`);
+     *   all-to-all V: nranks * nranks entries, [p * nranks + d] = elements
+     *     source p sends to destination d (count is ignored). */
+    const uint64_t *vcounts;
+    int nvcounts;
 } coll_options_t;
 
 typedef struct coll_spec coll_spec_t;

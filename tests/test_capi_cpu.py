@@ -180,3 +180,63 @@ def test_reset_counters_match_reader_counts(cd):
                 readers = counted[counted[:, 9] == cid][:, 4]
                 assert np.all(readers == u)
         cd.coll_destroy(spec)
+
+
+# ---- variable-length (V) collectives ---------------------------------------
+
+def zipf_elems(total_bytes, n):
+    return [b // 2 for b in synth.zipf_split(total_bytes, n)]
+
+
+V_CASES = [
+    # (triple name, n, per-rank vector or matrix, enc, path)
+    ("REDUCE_SCATTER_V", 8, zipf_elems(8 * 2048 * 2, 8), 1, 2),
+    ("REDUCE_SCATTER_V", 8, zipf_elems(8 * 2048 * 2, 8), 0, 1),
+    ("REDUCE_SCATTER_V", 3, [8, 0, 488], 1, 1),            # an empty partition
+    ("ALLGATHER_V", 8, zipf_elems(8 * 1024 * 2, 8), 0, 2),
+    ("ALLGATHER_V", 8, zipf_elems(8 * 1024 * 2, 8), 1, 1),
+    ("ALLGATHER_V", 4, [64, 8, 0, 1208], 1, 2),
+    ("ALLTOALL_V", 8, [synth.rotate_right(zipf_elems(8 * 960 * 2, 8), p + 1)
+                       for p in range(8)], 1, 2),
+    ("ALLTOALL_V", 8, [synth.rotate_right(zipf_elems(8 * 512 * 2, 8), p + 1)
+                       for p in range(8)], 0, 1),
+    ("ALLTOALL_V", 3, [[8, 0, 240], [0, 0, 16], [128, 64, 8]], 0, 2),
+]
+
+
+@pytest.mark.parametrize("name,n,v,enc,path", V_CASES)
+def test_derived_v_schedule_computes_the_oracle_result(cd, name, n, v, enc, path):
+    triple = getattr(cd, name)
+    count = 0 if name == "ALLTOALL_V" else int(sum(v))
+    spec = cd.coll_spec_create(*triple, n, count, encoding=enc, path=path, vcounts=v)
+    try:
+        ins = [synth.normal_bf16(9, cd.coll_buffer_elems(spec, r)[0], n, r) for r in range(n)]
+        got = interpret(cd, spec, enc, n, ins)
+        if name == "REDUCE_SCATTER_V":
+            want = oracle.reduce_scatter_v(ins, v)
+        elif name == "ALLGATHER_V":
+            want = oracle.all_gather_v(ins, v)
+        else:
+            want = oracle.all_to_all_v(ins, v)
+        for r in range(n):
+            assert got[r].size == want[r].size
+            assert np.array_equal(got[r], want[r]), f"rank {r}"
+    finally:
+        cd.coll_destroy(spec)
+
+
+def test_v_argument_validation(cd):
+    def status_of(*a, **kw):
+        with pytest.raises(cd.CollError) as e:
+            cd.coll_spec_create(*a, **kw)
+        return e.value.status
+
+    assert status_of(*cd.REDUCE_SCATTER_V, 4, 64, vcounts=[16, 16, 16]) == cd.COLL_ERR_INVALID
+    assert status_of(*cd.REDUCE_SCATTER_V, 4, 64, vcounts=[16, 16, 16, 8]) == cd.COLL_ERR_INVALID
+    assert status_of(*cd.ALLGATHER_V, 4, 64, vcounts=[16, 16, 20, 12]) == cd.COLL_ERR_ALIGN
+    assert status_of(*cd.ALLTOALL_V, 2, 0, vcounts=[8, 8, 8]) == cd.COLL_ERR_INVALID
+    assert status_of(*cd.ALLGATHER_V, 2, 16) == cd.COLL_ERR_INVALID   # no vcounts
+    s = cd.coll_spec_create(*cd.ALLTOALL_V, 2, 0, vcounts=[[8, 16], [0, 24]])
+    assert cd.coll_buffer_elems(s, 0) == (24, 8)
+    assert cd.coll_buffer_elems(s, 1) == (24, 40)
+    cd.coll_destroy(s)
