@@ -113,6 +113,16 @@ def _declare(L: ctypes.CDLL) -> None:
     L.orc_ll128_encode.restype = None
     L.orc_ll128_decode.argtypes = [_u8p, _sz, ctypes.c_uint64, _u16p]
     L.orc_ll128_decode.restype = _sz
+    L.orc_sent_sanitize.argtypes = [ctypes.c_uint16]
+    L.orc_sent_sanitize.restype = ctypes.c_uint16
+    L.orc_sent_sanitize_buf.argtypes = [_u16p, _sz, _u16p]
+    L.orc_sent_sanitize_buf.restype = None
+    L.orc_sent_packs.argtypes = [_sz]
+    L.orc_sent_packs.restype = _sz
+    L.orc_sent_encode.argtypes = [_u16p, _sz, _u64p]
+    L.orc_sent_encode.restype = None
+    L.orc_sent_decode.argtypes = [_u64p, _sz, _u16p]
+    L.orc_sent_decode.restype = _sz
 
 
 # ---- marshalling helpers -------------------------------------------------
@@ -338,3 +348,37 @@ def ll128_decode(lines: np.ndarray, elems: int, epoch: int,
     rej = lib().orc_ll128_decode(_ptr(lines, ctypes.c_uint8), elems, epoch,
                                  _ptr(out, ctypes.c_uint16))
     return out[:elems], int(rej)
+
+
+# ---- sentinel readiness --------------------------------------------------------
+
+SENT_BF16 = 0xFFFF
+CANONICAL_NAN = 0x7FC0
+
+
+def sent_sanitize(x: np.ndarray) -> np.ndarray:
+    """Every element equal to the reserved pattern replaced by the canonical
+    quiet NaN (what a sentinel-encoded copy delivers)."""
+    x = _c(np.asarray(x).ravel(), np.uint16)
+    out = np.zeros(max(x.size, 1), dtype=np.uint16)
+    lib().orc_sent_sanitize_buf(_ptr(x, ctypes.c_uint16), x.size, _ptr(out, ctypes.c_uint16))
+    return out[:x.size]
+
+
+def sent_packs(elems: int) -> int:
+    return int(lib().orc_sent_packs(elems))
+
+
+def sent_encode(x: np.ndarray) -> np.ndarray:
+    x = _c(np.asarray(x).ravel(), np.uint16)
+    out = np.zeros(max(sent_packs(x.size), 1), dtype=np.uint64)
+    lib().orc_sent_encode(_ptr(x, ctypes.c_uint16), x.size, _ptr(out, ctypes.c_uint64))
+    return out[:sent_packs(x.size)]
+
+
+def sent_decode(packs: np.ndarray, elems: int, fill: int = 0) -> tuple[np.ndarray, int]:
+    packs = _c(packs, np.uint64)
+    out = np.full(max(elems, 1), fill, dtype=np.uint16)
+    skipped = lib().orc_sent_decode(_ptr(packs, ctypes.c_uint64), elems,
+                                    _ptr(out, ctypes.c_uint16))
+    return out[:elems], int(skipped)

@@ -349,3 +349,51 @@ size_t orc_ll128_decode(const uint8_t *lines, size_t elems, uint64_t epoch,
     }
     return rejected;
 }
+
+uint16_t orc_sent_sanitize(uint16_t x)
+{
+    if (x == ORC_SENT_BF16)
+        return (uint16_t)ORC_CANONICAL_NAN;
+    return x;
+}
+
+void orc_sent_sanitize_buf(const uint16_t *in, size_t elems, uint16_t *out)
+{
+    for (size_t i = 0; i < elems; ++i)
+        out[i] = orc_sent_sanitize(in[i]);
+}
+
+size_t orc_sent_packs(size_t elems) { return (elems + 3u) / 4u; }
+
+void orc_sent_encode(const uint16_t *in, size_t elems, uint64_t *packs)
+{
+    size_t np = orc_sent_packs(elems);
+    for (size_t j = 0; j < np; ++j) {
+        uint64_t pack = 0;
+        for (size_t q = 0; q < 4; ++q) {
+            size_t idx = 4 * j + q;
+            uint64_t v = idx < elems ? orc_sent_sanitize(in[idx]) : 0u;
+            pack |= v << (16 * q);
+        }
+        packs[j] = pack;
+    }
+}
+
+size_t orc_sent_decode(const uint64_t *packs, size_t elems, uint16_t *out)
+{
+    size_t np = orc_sent_packs(elems);
+    size_t skipped = 0;
+    for (size_t j = 0; j < np; ++j) {
+        uint64_t pack = packs[j];
+        if (pack == ~(uint64_t)0) {
+            skipped += 1;
+            continue;
+        }
+        for (size_t q = 0; q < 4; ++q) {
+            size_t idx = 4 * j + q;
+            if (idx < elems)
+                out[idx] = (uint16_t)((pack >> (16 * q)) & 0xFFFFu);
+        }
+    }
+    return skipped;
+}

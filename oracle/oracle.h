@@ -191,6 +191,28 @@ void orc_ll128_encode(const uint16_t *in, size_t elems, uint64_t epoch,
 size_t orc_ll128_decode(const uint8_t *lines, size_t elems, uint64_t epoch,
                         uint16_t *out);
 
+/* Sentinel readiness: [flash] §3.1 "Sentinel readiness".  Receive storage is
+ * pre-filled with a reserved bit pattern; a producer publishes a pack by
+ * overwriting it, so a pack that differs from the sentinel has arrived, and
+ * no flag travels with the payload.  A value that equals the reserved
+ * pattern is replaced by the canonical quiet NaN before publication, so it
+ * can never look unready.
+ * Readings (the pages fix neither): the reserved bf16 pattern is 0xFFFF (a
+ * NaN, so only a NaN input changes, and it stays a NaN); the canonical
+ * quiet NaN is 0x7FC0 (the NaN the fold's rounding produces); a pack is 8
+ * bytes = 4 elements, little-endian (element 4j in bits 0..15), 0 past the
+ * end; the sentinel pack is all ones (four sentinel elements). */
+#define ORC_SENT_BF16 0xFFFFu
+#define ORC_CANONICAL_NAN 0x7FC0u
+uint16_t orc_sent_sanitize(uint16_t x);
+void orc_sent_sanitize_buf(const uint16_t *in, size_t elems, uint16_t *out);
+size_t orc_sent_packs(size_t elems);
+void orc_sent_encode(const uint16_t *in, size_t elems, uint64_t *packs);
+/* Decode packs that are not the sentinel pack; a sentinel pack has not
+ * arrived and is skipped (its elements are not written).  Returns the number
+ * of packs skipped. */
+size_t orc_sent_decode(const uint64_t *packs, size_t elems, uint16_t *out);
+
 #ifdef __cplusplus
 }
 #endif

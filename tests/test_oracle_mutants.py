@@ -38,6 +38,11 @@ MUTANTS = [
     ("rsv_offset_not_advanced", "            out[r][j] = orc_fold(in, n, off + j);\n        off += len[r];", "            out[r][j] = orc_fold(in, n, off + j);\n        off += 0;"),
     ("a2av_source_offset", "                src += len[(size_t)p * n + k];", "                src += len[(size_t)k * n + p];"),
     ("agv_rank_order", "                out[d][off + j] = in[p][j];\n            off += len[p];", "                out[d][off + j] = in[n - 1 - p][j];\n            off += len[p];"),
+    ("sent_sanitizes_wrong_pattern", "if (x == ORC_SENT_BF16)", "if (x == 0x7FFFu)"),
+    ("sent_packs_big_endian", "pack |= v << (16 * q);", "pack |= v << (16 * (3 - q));"),
+    ("sent_decode_accepts_sentinel", "if (pack == ~(uint64_t)0) {", "if (0) {"),
+    ("sent_not_sanitized_in_encode", "uint64_t v = idx < elems ? orc_sent_sanitize(in[idx]) : 0u;",
+     "uint64_t v = idx < elems ? in[idx] : 0u;"),
     ("moe_source_major_order", "for (int le = 0; le < el; ++le) {\n            int e = d * el + le;\n            for (int p = 0; p < n; ++p)",
      "for (int le = 0; le < el; ++le) {\n            int e = d * el + le;\n            for (int p = n - 1; p >= 0; --p)"),
 ]
@@ -66,6 +71,10 @@ PINS = [
     pins.test_v_collectives_invariants_on_zipf_splits,
     pins.test_all_to_all_v_hand_case,
     pins.test_moe_counts_and_rows_invariants,
+    pins.test_sentinel_sanitize_changes_only_the_reserved_nan,
+    pins.test_sentinel_pack_layout_hand_case,
+    pins.test_sentinel_roundtrip_every_pattern_in_every_position,
+    pins.test_sentinel_pack_is_not_ready,
 ]
 
 

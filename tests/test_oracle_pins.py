@@ -352,6 +352,82 @@ def test_ll128_rejects_other_sequence_numbers(orc):
     assert np.array_equal(back[:240], x[:240])
 
 
+# ---- sentinel readiness (flash-comm §3.1) ---------------------------------------------
+
+def _is_bf16_nan(v: np.ndarray) -> np.ndarray:
+    """IEEE binary16-brain layout: exponent all ones and a nonzero fraction."""
+    return ((v & 0x7F80) == 0x7F80) & ((v & 0x007F) != 0)
+
+
+def test_sentinel_sanitize_changes_only_the_reserved_nan(orc):
+    pats = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    out = orc.sent_sanitize(pats)
+    changed = np.nonzero(out != pats)[0]
+    assert changed.tolist() == [0xFFFF]
+    assert out[0xFFFF] == 0x7FC0
+    # the reserved pattern and its replacement are both NaNs: no number changes
+    assert _is_bf16_nan(np.array([0xFFFF, 0x7FC0], np.uint16)).all()
+    # 0x7FC0 is the canonical quiet NaN: sign 0, exponent all ones, only the
+    # quiet bit of the fraction set
+    assert (0x7FC0 >> 15) == 0 and (0x7FC0 & 0x7F80) == 0x7F80 and (0x7FC0 & 0x7F) == 0x40
+    # the fold's rounding yields the same NaN, so partial sums never carry
+    # the reserved pattern
+    assert orc.f32_to_bf16(float("nan")) == 0x7FC0
+    assert orc.f32_to_bf16(-float("nan")) == 0x7FC0
+
+
+def test_sentinel_pack_layout_hand_case(orc):
+    x = np.array([0x0001, 0xFFFF, 0x1234, 0x8000, 0x7F80], dtype=np.uint16)
+    packs = orc.sent_encode(x)
+    assert packs.tolist() == [0x800012347FC00001, 0x0000000000007F80]
+    assert orc.sent_packs(0) == 0 and orc.sent_packs(4) == 1 and orc.sent_packs(9) == 3
+
+
+def test_sentinel_roundtrip_every_pattern_in_every_position(orc):
+    pats = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    for pos in range(4):
+        x = np.zeros(65536 * 4, dtype=np.uint16)
+        x[pos::4] = pats
+        packs = orc.sent_encode(x)
+        assert packs.size == 65536
+        assert not np.any(packs == np.uint64(0xFFFFFFFFFFFFFFFF))   # never looks unready
+        back, skipped = orc.sent_decode(packs, x.size)
+        assert skipped == 0
+        want = x.copy()
+        want[want == 0xFFFF] = 0x7FC0
+        assert np.array_equal(back, want)
+
+
+def test_sentinel_pack_is_not_ready(orc):
+    x = synth.random_bits16(9, 100, 2)
+    packs = orc.sent_encode(x)
+    packs[[3, 20]] = np.uint64(0xFFFFFFFFFFFFFFFF)
+    back, skipped = orc.sent_decode(packs, x.size, fill=0xDEAD)
+    assert skipped == 2
+    assert np.all(back[12:16] == 0xDEAD) and np.all(back[80:84] == 0xDEAD)
+    assert np.array_equal(back[:12], orc.sent_sanitize(x[:12]))
+    # one sentinel element next to data is data, not a missing pack
+    one = np.array([0xFFFF, 0xFFFF, 0xFFFF, 0x0001], dtype=np.uint64)
+    mixed = np.array([int(one[0] | (one[1] << 16) | (one[2] << 32) | (one[3] << 48))],
+                     dtype=np.uint64)
+    back, skipped = orc.sent_decode(mixed, 4)
+    assert skipped == 0 and back.tolist() == [0xFFFF, 0xFFFF, 0xFFFF, 0x0001]
+
+
+def test_sentinel_sanitize_does_not_change_a_fold(orc):
+    """NaN in, NaN out: folding sanitized inputs gives the bits of folding the
+    raw ones, so reductions are unaffected by the sanitisation."""
+    n, count = 8, 4096
+    xs = [synth.random_bits16(10, count, r) for r in range(n)]
+    g = np.random.Generator(np.random.Philox(3))
+    for r in range(n):
+        xs[r][g.integers(0, count, 200)] = 0xFFFF
+    raw = orc.allreduce(xs)[0]
+    san = orc.allreduce([orc.sent_sanitize(x) for x in xs])[0]
+    assert np.array_equal(raw, san)
+    assert not np.any(raw == 0xFFFF)
+
+
 # ---- C11 MoE dispatch ------------------------------------------------------------------
 
 def test_moe_tiny_hand_derived_layout(orc):
