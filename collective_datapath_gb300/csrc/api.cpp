@@ -165,8 +165,9 @@ ComposedParams composed_shape(const Plan& p, int grid) {
 // else through the generic consume kernel.
 cudaError_t launch_phase(const Plan& p, const RunParams& P, int phase,
                          const std::vector<Item>& items, cudaStream_t st) {
-  const bool pipelined = p.enc == ENC_LL128 || p.reset_mode == COLL_RESET_DEFERRED ||
-                         p.reset_mode == COLL_RESET_NONE;
+  const bool pipelined = p.enc == ENC_LL128 ||
+                         (p.enc == ENC_LL8 && (p.reset_mode == COLL_RESET_DEFERRED ||
+                                               p.reset_mode == COLL_RESET_NONE));
   if (pipelined && !items.empty()) {
     bool all_fold = true, all_copy = true;
     for (const Item& it : items) {
@@ -190,7 +191,7 @@ cudaError_t launch_stager(const Plan& p, const RunParams& P, int items, cudaStre
 // advances the epoch.
 coll_status_t launch_consumers(coll_spec* s, RunParams P, cudaStream_t st) {
   const Plan& p = s->plan;
-  const bool rearm_kernel = p.enc == ENC_LL8 && p.reset_mode == COLL_RESET_KERNEL;
+  const bool rearm_kernel = p.enc != ENC_LL128 && p.reset_mode == COLL_RESET_KERNEL;
   const bool two = !p.items2.empty();
   if (p.items1.empty() && !two) {
     P.advance_epoch = !rearm_kernel;
@@ -291,6 +292,13 @@ coll_status_t coll_bind(coll_spec_t* s, void* dev_workspace, size_t bytes,
   s->ws = static_cast<char*>(dev_workspace);
   s->ws_bytes = bytes;
   if (cudaError_t e = cudaMemsetAsync(s->ws, 0, p.ws_bytes, st)) return cuda_status(e);
+  if (p.enc == ENC_SENT) {
+    // flash-comm §4.2: arrival-checked storage starts out holding the pattern
+    for (const Region* R : {&p.P, &p.AG})
+      if (R->slot_bytes > 0)
+        if (cudaError_t e = cudaMemsetAsync(s->ws + R->base, 0xFF, 2 * R->slot_bytes, st))
+          return cuda_status(e);
+  }
   WsHeader h{};
   h.epoch = 1;
   // Pageable sources: the runtime copies them before returning.
@@ -382,7 +390,7 @@ coll_status_t coll_run(coll_spec_t* s, const void* const* dev_ins, void* const* 
     return cuda_status(launched(s, launch_composed(P, cap, st), st));
   }
   if (dev_ins != nullptr && p.path == COLL_PATH_FUSED && !empty &&
-      !(p.enc == ENC_LL8 && p.reset_mode == COLL_RESET_KERNEL)) {
+      !(p.enc != ENC_LL128 && p.reset_mode == COLL_RESET_KERNEL)) {
     P.advance_epoch = 1;
     return cuda_status(launched(s, launch_fused(P, p.n * p.ctas_per_rank, st), st));
   }
@@ -526,7 +534,7 @@ coll_status_t coll_run_late(coll_spec_t* s, const void* const* dev_ins, void* co
   if (!s->bound) return COLL_ERR_STATE;
   const Plan& p = s->plan;
   if (p.kind == CK_ALLGATHER || p.kind == CK_ALLGATHER_V || p.kind == CK_ALLTOALL_V ||
-      (p.enc == ENC_LL8 && p.reset_mode == COLL_RESET_KERNEL))
+      (p.enc != ENC_LL128 && p.reset_mode == COLL_RESET_KERNEL))
     return COLL_ERR_UNSUPPORTED;  // late producers need identical rank images
   if (coll_status_t e = check_outs(s, dev_outs)) return e;
   if (coll_status_t e = check_ins(s, dev_ins)) return e;

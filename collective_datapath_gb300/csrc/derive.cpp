@@ -9,8 +9,12 @@
 
 namespace coll {
 
-int line_bytes(int enc) { return enc == ENC_LL8 ? kLL8LineBytes : kLL128LineBytes; }
-int line_elems(int enc) { return enc == ENC_LL8 ? kLL8Elems : kLL128Elems; }
+int line_bytes(int enc) {
+  return enc == ENC_LL8 ? kLL8LineBytes : (enc == ENC_SENT ? kSentLineBytes : kLL128LineBytes);
+}
+int line_elems(int enc) {
+  return enc == ENC_LL8 ? kLL8Elems : (enc == ENC_SENT ? kSentElems : kLL128Elems);
+}
 
 uint64_t lines_for(int enc, uint64_t elems) {
   const uint64_t e = (uint64_t)line_elems(enc);
@@ -179,7 +183,8 @@ int derive(const DeriveInput& in, Plan& p) {
   const int n = in.nranks;
   if (n < 1 || n > kMaxRanks) return COLL_ERR_UNSUPPORTED;
   if (in.dtype != COLL_BF16) return COLL_ERR_UNSUPPORTED;
-  if (in.encoding != COLL_LL8 && in.encoding != COLL_LL128) return COLL_ERR_UNSUPPORTED;
+  if (in.encoding != COLL_LL8 && in.encoding != COLL_LL128 && in.encoding != COLL_SENT)
+    return COLL_ERR_UNSUPPORTED;
   if (in.reset_mode < 0 || in.reset_mode > 3 || in.path < 0 || in.path > 3 ||
       in.algorithm < 0 || in.algorithm > 2 || in.ctas < 0 || in.tile_lines < 0)
     return COLL_ERR_INVALID;
@@ -228,7 +233,10 @@ int derive(const DeriveInput& in, Plan& p) {
   p.n = n;
   p.count = count_in;
   p.shard = shard_elems(count_in, n);
-  p.reset_mode = p.enc == ENC_LL8 ? in.reset_mode : COLL_RESET_NONE;
+  p.reset_mode = p.enc == ENC_LL128 ? COLL_RESET_NONE : in.reset_mode;
+  // Sentinel packs carry no epoch: without a re-arm a consumed pack would
+  // look published to the next run of its slot.
+  if (p.enc == ENC_SENT && p.reset_mode == COLL_RESET_NONE) return COLL_ERR_UNSUPPORTED;
   p.timeout_ns = in.timeout_ns ? in.timeout_ns : 200000000ull;
   if (p.kind == CK_ALLTOALL && p.shard * (uint64_t)n != in.count)
     return COLL_ERR_ALIGN;  // the exchange needs equal partitions
@@ -269,8 +277,8 @@ int derive(const DeriveInput& in, Plan& p) {
   }
   p.path = in.path;
   if (p.path == COLL_PATH_AUTO)
-    p.path = (in_bytes_per_rank <= 256 * 1024 && p.enc == ENC_LL8) ? COLL_PATH_FUSED
-                                                                  : COLL_PATH_STREAMED;
+    p.path = (in_bytes_per_rank <= 256 * 1024 && p.enc != ENC_LL128) ? COLL_PATH_FUSED
+                                                                     : COLL_PATH_STREAMED;
 
   if (p.path == COLL_PATH_COMPOSED &&
       !(p.kind == CK_ALLREDUCE && p.algorithm == COLL_TWOSHOT && p.enc == ENC_LL128))
@@ -314,7 +322,7 @@ int derive(const DeriveInput& in, Plan& p) {
   auto fused = p.path == COLL_PATH_FUSED;
   // Streamed tiles: a 256-thread CTA moves 4 LL8 groups per thread or 4
   // LL128 rows per warp per step.
-  const uint64_t max_tile = p.enc == ENC_LL8 ? 4096 : 1024;
+  const uint64_t max_tile = p.enc == ENC_LL128 ? 1024 : 4096;
   // Fused tiles: the smallest tile (multiple of 4 lines) that gives every
   // CTA of a rank at most one item of the phase.
   auto pick_tile = [&](const std::vector<uint64_t>& seg_lines) -> uint64_t {

@@ -6,7 +6,7 @@
 //              stages its tiles, then polls and consumes; optional late
 //              producer CTAs publish withheld lines while consumers poll
 //  k_withhold  fault injection: overwrite listed lines with stale content
-//  k_rearm     LL8 re-arm of a whole slot by a separate kernel
+//  k_rearm     LL8 / sentinel re-arm of a whole slot by a separate kernel
 //  k_advance   an empty run: only the epoch advances
 #include <cuda_runtime.h>
 
@@ -14,6 +14,7 @@
 #include "ll128.cuh"
 #include "ll8.cuh"
 #include "pipe.cuh"
+#include "sent.cuh"
 
 namespace coll {
 
@@ -24,6 +25,8 @@ __device__ __forceinline__ void stage_item(const RunParams& P, const StageItem& 
                                            uint64_t e) {
   if (ENC == ENC_LL8)
     ll8_stage_tile(P, it, e);
+  else if (ENC == ENC_SENT)
+    sent_stage_tile(P, it, e);
   else
     ll128_stage_tile<kConc>(P, it, e);
 }
@@ -33,6 +36,8 @@ __device__ __forceinline__ void consume_item(const RunParams& P, const Region& R
                                              const Item& it, uint64_t e) {
   if (ENC == ENC_LL8)
     ll8_consume_item(P, R, it, e);
+  else if (ENC == ENC_SENT)
+    sent_consume_item(P, R, it, e);
   else
     ll128_consume_item<kConc>(P, R, it, e);
 }
@@ -470,12 +475,27 @@ __device__ void late_producer(const RunParams& P, uint64_t e, int p, int workers
     // segment containing `line` (segments are in image order)
     int k = 0;
     while (k + 1 < P.nseg && (uint64_t)line >= P.seg_line0[k + 1]) ++k;
-    const int epl = ENC == ENC_LL8 ? kLL8Elems : kLL128Elems;
+    const int epl = ENC == ENC_LL8 ? kLL8Elems : (ENC == ENC_SENT ? kSentElems : kLL128Elems);
     const uint64_t off = ((uint64_t)line - P.seg_line0[k]) * epl;
     elem0 = P.seg_in0[k] + off;
     elems = (int64_t)P.seg_elems[k] - (int64_t)off;  // elements left in segment
   };
-  if (ENC == ENC_LL8) {
+  if (ENC == ENC_SENT) {
+    uint64_t* img = image_lines(P, P.P, e, p);
+    for (int64_t j = 0; j < n; j += 32) {
+      if (j + lane < n) {
+        const int64_t line = order[j + lane];
+        uint64_t elem0;
+        int64_t left;
+        locate(line, elem0, left);
+        const uint2 d = *reinterpret_cast<const uint2*>(in + elem0);
+        st_relaxed_u64(img + line, (uint64_t)sent_sanitize2(d.x) |
+                                       ((uint64_t)sent_sanitize2(d.y) << 32));
+      }
+      __syncwarp();
+      __nanosleep(500);
+    }
+  } else if (ENC == ENC_LL8) {
     uint64_t* img = image_lines(P, P.P, e, p);
     for (int64_t j = 0; j < n; j += 32) {
       if (j + lane < n) {
@@ -567,7 +587,10 @@ __global__ void k_withhold(RunParams P) {
     const uint64_t stale = kind == 0 ? e - 1 : (kind == 1 ? e - 2 : 0);
     const uint64_t pz = P.wh_poison[j];
     const uint64_t pw = pz | (pz << 16) | (pz << 32) | (pz << 48);
-    if (ENC == ENC_LL8) {
+    if (ENC == ENC_SENT) {
+      // a pack that was never published still holds the pattern
+      st_relaxed_u64(image_lines(P, P.P, e, p) + line, kSentPack);
+    } else if (ENC == ENC_LL8) {
       uint64_t* img = image_lines(P, P.P, e, p);
       st_relaxed_u64(img + line, (pw & 0xFFFFFFFFull) | ((uint64_t)(uint32_t)stale << 32));
     } else {
@@ -578,9 +601,11 @@ __global__ void k_withhold(RunParams P) {
   }
 }
 
-// Re-arm every LL8 line of the current slot (both regions), then end the run.
+// Re-arm every LL8 line (flag 0) or sentinel pack (the pattern) of the
+// current slot (both regions), then end the run.
 __global__ void __launch_bounds__(kThreads) k_rearm(RunParams P) {
   const uint64_t e = begin_run(P);
+  const uint64_t fill = P.enc == ENC_SENT ? kSentPack : 0ull;
   for (int region = 0; region < 2; ++region) {
     const Region& R = region == 0 ? P.P : P.AG;
     if (R.rank_bytes == 0) continue;
@@ -588,7 +613,7 @@ __global__ void __launch_bounds__(kThreads) k_rearm(RunParams P) {
     uint4* base = reinterpret_cast<uint4*>(P.ws + R.base + (e & 1) * R.slot_bytes);
     for (uint64_t i = blockIdx.x * (uint64_t)blockDim.x + threadIdx.x; i < words;
          i += (uint64_t)gridDim.x * blockDim.x)
-      st_relaxed_v2u64(base + i, 0ull, 0ull);
+      st_relaxed_v2u64(base + i, fill, fill);
   }
   finish_run(P, e);
 }
@@ -611,9 +636,11 @@ int device_sms() {
 
 int fused_capacity(int enc) {
   int per_sm = 0;
-  cudaError_t err = enc == ENC_LL8
-                        ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+  cudaError_t err =
+      enc == ENC_LL8    ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(
                               &per_sm, k_fused<ENC_LL8>, kThreads, 0)
+      : enc == ENC_SENT ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+                              &per_sm, k_fused<ENC_SENT>, kThreads, 0)
                         : cudaOccupancyMaxActiveBlocksPerMultiprocessor(
                               &per_sm, k_fused<ENC_LL128>, kThreads, 0);
   if (err != cudaSuccess || per_sm <= 0) return 0;
@@ -626,6 +653,8 @@ cudaError_t launch_stage(const RunParams& P, int grid, cudaStream_t s) {
   if (grid <= 0) return cudaSuccess;
   if (P.enc == ENC_LL8)
     k_stage<ENC_LL8><<<grid, kThreads, 0, s>>>(P);
+  else if (P.enc == ENC_SENT)
+    k_stage<ENC_SENT><<<grid, kThreads, 0, s>>>(P);
   else
     k_stage<ENC_LL128><<<grid, kThreads, 0, s>>>(P);
   return cudaGetLastError();
@@ -635,6 +664,8 @@ cudaError_t launch_consume(const RunParams& P, int phase, int grid, cudaStream_t
   if (grid <= 0) grid = 1;
   if (P.enc == ENC_LL8)
     k_consume<ENC_LL8><<<grid, kThreads, 0, s>>>(P, phase);
+  else if (P.enc == ENC_SENT)
+    k_consume<ENC_SENT><<<grid, kThreads, 0, s>>>(P, phase);
   else
     k_consume<ENC_LL128><<<grid, kThreads, 0, s>>>(P, phase);
   return cudaGetLastError();
@@ -652,6 +683,7 @@ cudaError_t launch_fused(const RunParams& P, int grid, cudaStream_t s) {
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   if (P.enc == ENC_LL8) return cudaLaunchKernelEx(&cfg, k_fused<ENC_LL8>, P);
+  if (P.enc == ENC_SENT) return cudaLaunchKernelEx(&cfg, k_fused<ENC_SENT>, P);
   return cudaLaunchKernelEx(&cfg, k_fused<ENC_LL128>, P);
 }
 
@@ -693,6 +725,8 @@ cudaError_t launch_withhold(const RunParams& P, cudaStream_t s) {
   const int grid = (int)((P.wh_n + kThreads - 1) / kThreads);
   if (P.enc == ENC_LL8)
     k_withhold<ENC_LL8><<<grid, kThreads, 0, s>>>(P);
+  else if (P.enc == ENC_SENT)
+    k_withhold<ENC_SENT><<<grid, kThreads, 0, s>>>(P);
   else
     k_withhold<ENC_LL128><<<grid, kThreads, 0, s>>>(P);
   return cudaGetLastError();

@@ -10,12 +10,13 @@ namespace coll {
 
 constexpr int kMaxRanks = 8;
 
-// Readiness encodings (values match COLL_LL8 / COLL_LL128 of coll.h).
-enum Encoding : int { ENC_LL8 = 0, ENC_LL128 = 1 };
+// Readiness encodings (values match COLL_LL8 / COLL_LL128 / COLL_SENT of coll.h).
+enum Encoding : int { ENC_LL8 = 0, ENC_LL128 = 1, ENC_SENT = 2 };
 
 // Bytes per line and bf16 payload elements per line of each encoding.
 constexpr int kLL8LineBytes = 8, kLL8Elems = 2;
 constexpr int kLL128LineBytes = 128, kLL128Elems = 60;
+constexpr int kSentLineBytes = 8, kSentElems = 4;  // one sentinel pack
 // Lines of one 16-byte LL8 input chunk / one 512-byte LL128 warp row.
 constexpr int kLL8GroupLines = 4;
 constexpr int kLL128RowLines = 4;

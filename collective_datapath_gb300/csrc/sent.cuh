@@ -1,0 +1,224 @@
+// sent.cuh -- sentinel readiness: 8-byte packs of four bf16 and no flag.
+//
+// flash-comm §3.1 "Sentinel readiness": staging storage holds a reserved
+// pattern until a producer overwrites it with data, so a pack that differs
+// from the pattern has arrived and nothing but payload is moved.  The
+// reserved bf16 pattern is 0xFFFF (a NaN), the unready pack is all ones,
+// and an input element equal to 0xFFFF is published as the canonical quiet
+// NaN 0x7FC0.  A fold's result needs no such step: its rounding maps every
+// NaN to 0x7FC0 already.  Once read, a pack is re-armed with the pattern by
+// the rule of the spec's re-arm mode (sole or last reader, a re-arm kernel,
+// or the owner during the next epoch).
+//
+// A thread moves groups of two packs (one 16-byte input chunk, eight
+// elements) with one 16-byte access.  Each 8-byte pack is single-copy atomic,
+// so a pack that is not the pattern holds the whole published payload; no
+// fence is needed on either side (the LL8 argument with the flag replaced by
+// the pattern test).
+#pragma once
+
+#include "dev_common.cuh"
+#include "ll8.cuh"
+
+namespace coll {
+
+constexpr uint64_t kSentPack = ~0ull;
+constexpr int kSentGroupLines = 2;  // packs per 16-byte group
+
+// Both bf16 halves of w, each 0xFFFF replaced by 0x7FC0.
+__device__ __forceinline__ uint32_t sent_sanitize2(uint32_t w) {
+  const uint32_t lo = (w & 0xFFFFu) == 0xFFFFu ? 0x7FC0u : (w & 0xFFFFu);
+  const uint32_t hi = (w >> 16) == 0xFFFFu ? 0x7FC0u : (w >> 16);
+  return lo | (hi << 16);
+}
+
+__device__ __forceinline__ void sent_store(uint64_t* p, uint4 v) {
+  st_relaxed_v2u64(p, (uint64_t)sent_sanitize2(v.x) | ((uint64_t)sent_sanitize2(v.y) << 32),
+                   (uint64_t)sent_sanitize2(v.z) | ((uint64_t)sent_sanitize2(v.w) << 32));
+}
+
+__device__ __forceinline__ void sent_rearm(uint64_t* p) {
+  st_relaxed_v2u64(p, kSentPack, kSentPack);
+}
+
+// Poll the two packs at p until neither is the pattern (bounded); the caller
+// then reloads them.  Returns false on timeout or abort (error latched).
+static __device__ __noinline__ bool sent_wait_pair(const RunParams& P, const uint64_t* p,
+                                                   uint32_t rank, int64_t line) {
+  count_rejection(P.ws);
+  Waiter w;
+  for (;;) {
+    if (w.expired(P.ws, P.timeout_ns)) {
+      latch_error(P.ws, kStatusTimeout, rank, line);
+      return false;
+    }
+    __nanosleep(64);
+    uint64_t a, b;
+    ld_relaxed_v2u64(p, a, b);
+    if (a != kSentPack && b != kSentPack) return true;
+  }
+}
+
+// Encode one staging tile (nlines is even: segments hold multiples of 8
+// elements).  Deferred re-arm writes the pattern over the same packs of the
+// other slot, which the completed previous run consumed.
+__device__ __forceinline__ void sent_stage_tile(const RunParams& P, const StageItem& it,
+                                                uint64_t epoch) {
+  const uint16_t* in = P.in[it.rank] + it.in_elem;
+  uint64_t* img = image_lines(P, P.P, epoch, it.rank) + it.dst_line;
+  const bool deferred = P.reset_mode == kResetDeferred;
+  uint64_t* other = image_lines(P, P.P, epoch + 1, it.rank) + it.dst_line;
+  const uint32_t ngroups = it.nlines / kSentGroupLines;
+  for (uint32_t g0 = threadIdx.x; g0 < ngroups; g0 += blockDim.x * kGroupsInFlight) {
+    uint4 v[kGroupsInFlight];
+#pragma unroll
+    for (int j = 0; j < kGroupsInFlight; ++j) {
+      const uint32_t g = g0 + j * blockDim.x;
+      if (g < ngroups) v[j] = ld_stream_v4(in + 8 * (size_t)g);
+    }
+#pragma unroll
+    for (int j = 0; j < kGroupsInFlight; ++j) {
+      const uint32_t g = g0 + j * blockDim.x;
+      if (g < ngroups) {
+        sent_store(img + 2 * (size_t)g, v[j]);
+        if (deferred) sent_rearm(other + 2 * (size_t)g);
+      }
+    }
+  }
+}
+
+// Fold of eight elements (four words) of every source, rank order, fp32,
+// one rounding.
+__device__ __forceinline__ uint4 sent_fold8(const uint64_t* lo, const uint64_t* hi, int n) {
+  float a[8];
+  const uint32_t w0[4] = {(uint32_t)lo[0], (uint32_t)(lo[0] >> 32), (uint32_t)hi[0],
+                          (uint32_t)(hi[0] >> 32)};
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    a[2 * k] = bf16_lo_to_f32(w0[k]);
+    a[2 * k + 1] = bf16_hi_to_f32(w0[k]);
+  }
+#pragma unroll
+  for (int p = 1; p < kMaxRanks; ++p) {
+    if (p < n) {
+      const uint32_t w[4] = {(uint32_t)lo[p], (uint32_t)(lo[p] >> 32), (uint32_t)hi[p],
+                             (uint32_t)(hi[p] >> 32)};
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        a[2 * k] = __fadd_rn(a[2 * k], bf16_lo_to_f32(w[k]));
+        a[2 * k + 1] = __fadd_rn(a[2 * k + 1], bf16_hi_to_f32(w[k]));
+      }
+    }
+  }
+  return make_uint4(pack_bf16x2(a[0], a[1]), pack_bf16x2(a[2], a[3]), pack_bf16x2(a[4], a[5]),
+                    pack_bf16x2(a[6], a[7]));
+}
+
+// Process one consume item: validate + unpack (+ fold) + write (+ re-arm).
+__device__ __forceinline__ void sent_consume_item(const RunParams& P, const Region& R,
+                                                  const Item& it, uint64_t epoch) {
+  const int n = P.nranks;
+  const uint32_t ngroups = it.nlines / kSentGroupLines;
+  const bool reduce = it.kind == IK_REDUCE;
+  const bool publish = (it.flags & IF_PUBLISH) != 0;
+  const bool sole = (it.flags & IF_RESET_SOLE) != 0 && P.reset_mode == kResetLastReader;
+  const bool deferred = P.reset_mode == kResetDeferred;
+  bool ok = true;
+  if (reduce) {
+    // One group (two packs) of every source per step, all loaded before any
+    // is checked.
+    for (uint32_t g = threadIdx.x; g < ngroups && ok; g += blockDim.x) {
+      const uint64_t line = it.src_line + 2 * (uint64_t)g;
+      uint64_t lo[kMaxRanks], hi[kMaxRanks];
+#pragma unroll
+      for (int p = 0; p < kMaxRanks; ++p)
+        if (p < n) ld_relaxed_v2u64(image_lines(P, R, epoch, p) + line, lo[p], hi[p]);
+#pragma unroll
+      for (int p = 0; p < kMaxRanks; ++p)
+        if (p < n && (lo[p] == kSentPack || hi[p] == kSentPack)) {
+          const uint64_t* src = image_lines(P, R, epoch, p) + line;
+          ok = ok && sent_wait_pair(P, src, p, (int64_t)line);
+          ld_relaxed_v2u64(src, lo[p], hi[p]);
+        }
+      if (!ok) break;
+      const uint4 res = sent_fold8(lo, hi, n);
+      if (sole) {
+#pragma unroll
+        for (int p = 0; p < kMaxRanks; ++p)
+          if (p < n) sent_rearm(image_lines(P, R, epoch, p) + line);
+      }
+      if (publish) {
+        uint64_t* dst = image_lines(P, P.AG, epoch, it.dst) + it.out_off + 2 * (uint64_t)g;
+        st_relaxed_v2u64(dst, (uint64_t)res.x | ((uint64_t)res.y << 32),
+                         (uint64_t)res.z | ((uint64_t)res.w << 32));
+        if (deferred)
+          sent_rearm(image_lines(P, P.AG, epoch + 1, it.dst) + it.out_off + 2 * (uint64_t)g);
+      } else {
+        st_v4(P.out[it.dst] + it.out_off + 8 * (uint64_t)g, res);
+      }
+    }
+  } else {
+    uint64_t* src0 = image_lines(P, R, epoch, it.src) + it.src_line;
+    for (uint32_t g0 = threadIdx.x; g0 < ngroups && ok; g0 += blockDim.x * kGroupsInFlight) {
+      uint64_t a[kGroupsInFlight], b[kGroupsInFlight];
+#pragma unroll
+      for (int j = 0; j < kGroupsInFlight; ++j) {
+        const uint32_t g = g0 + j * blockDim.x;
+        if (g < ngroups) ld_relaxed_v2u64(src0 + 2 * (size_t)g, a[j], b[j]);
+      }
+#pragma unroll
+      for (int j = 0; j < kGroupsInFlight; ++j) {
+        const uint32_t g = g0 + j * blockDim.x;
+        if (g < ngroups && (a[j] == kSentPack || b[j] == kSentPack)) {
+          ok = ok && sent_wait_pair(P, src0 + 2 * (size_t)g, it.src,
+                                    (int64_t)(it.src_line + 2 * (uint64_t)g));
+          ld_relaxed_v2u64(src0 + 2 * (size_t)g, a[j], b[j]);
+        }
+      }
+      if (!ok) break;
+#pragma unroll
+      for (int j = 0; j < kGroupsInFlight; ++j) {
+        const uint32_t g = g0 + j * blockDim.x;
+        if (g >= ngroups) break;
+        if (sole) sent_rearm(src0 + 2 * (size_t)g);
+        if (publish) {
+          st_relaxed_v2u64(image_lines(P, P.AG, epoch, it.dst) + it.out_off + 2 * (uint64_t)g,
+                           a[j], b[j]);
+          if (deferred)
+            sent_rearm(image_lines(P, P.AG, epoch + 1, it.dst) + it.out_off + 2 * (uint64_t)g);
+        } else {
+          st_v4(P.out[it.dst] + it.out_off + 8 * (uint64_t)g,
+                make_uint4((uint32_t)a[j], (uint32_t)(a[j] >> 32), (uint32_t)b[j],
+                           (uint32_t)(b[j] >> 32)));
+        }
+      }
+    }
+  }
+  if ((it.flags & IF_RESET_COUNTED) && P.reset_mode == kResetLastReader) {
+    // The last of `readers` items over these packs re-arms them.
+    __shared__ uint32_t last;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      __threadfence();
+      const uint32_t old = atomicAdd(&P.counters[it.counter], 1u);
+      last = (old == (uint32_t)it.readers - 1u);
+      if (last) {
+        P.counters[it.counter] = 0u;
+        __threadfence();
+      }
+    }
+    __syncthreads();
+    if (last) {
+      for (uint32_t g = threadIdx.x; g < ngroups; g += blockDim.x) {
+        const uint64_t line = it.src_line + 2 * (uint64_t)g;
+        if (reduce) {
+          for (int p = 0; p < n; ++p) sent_rearm(image_lines(P, R, epoch, p) + line);
+        } else {
+          sent_rearm(image_lines(P, R, epoch, it.src) + line);
+        }
+      }
+    }
+  }
+}
+
+}  // namespace coll

@@ -104,8 +104,15 @@ typedef enum {
  *   flash-comm §4.3 sequence-numbered packet.
  * COLL_LL128: 128-byte line = 120 bytes of data (60 bf16) + 8-byte sequence
  *   number = the epoch (bytes 120..127).  flash-comm §3.1 sequence-number
- *   readiness, at 128-byte granularity. */
-enum { COLL_LL8 = 0, COLL_LL128 = 1 };
+ *   readiness, at 128-byte granularity.
+ * COLL_SENT: 8-byte pack = four bf16 and nothing else.  flash-comm §3.1
+ *   sentinel readiness: staging holds the all-ones pattern until a producer
+ *   overwrites it, so no byte beyond the payload moves.  An input element
+ *   equal to 0xFFFF (a NaN) is delivered as the canonical quiet NaN 0x7FC0;
+ *   all other bit patterns pass unchanged, and reductions are unaffected
+ *   (NaN in, NaN out).  Consumed packs must be re-armed: any reset mode but
+ *   COLL_RESET_NONE (which gets COLL_ERR_UNSUPPORTED). */
+enum { COLL_LL8 = 0, COLL_LL128 = 1, COLL_SENT = 2 };
 
 /* All-reduce algorithm: oneshot (every rank folds all N inputs), twoshot
  * (reduce-scatter to an owner per partition, which publishes its reduced
@@ -113,16 +120,17 @@ enum { COLL_LL8 = 0, COLL_LL128 = 1 };
  * allGather>; SiFAR §3.1; flash-comm §4.3 (one-hop / sharded two-hop). */
 enum { COLL_ALGO_AUTO = 0, COLL_ONESHOT = 1, COLL_TWOSHOT = 2 };
 
-/* Flag re-arm (LL8 only; LL128 sequence numbers need none, flash-comm §3.1
- * Table 2): after every reader of a line consumed it, its flag word is set
- * back to 0 --
+/* Re-arm (LL8 and sentinel; LL128 sequence numbers need none, flash-comm
+ * §3.1 Table 2): after every reader of a line consumed it, its LL8 flag word
+ * is set back to 0, or a sentinel pack back to the pattern --
  *   FUSED:    by the last reader, counted per tile inside the consume kernel;
  *   KERNEL:   by a separate kernel at the end of the run;
  *   DEFERRED: (default) by the owning rank during the next epoch, in the slot
  *             that epoch does not use: the completed previous run is the
  *             evidence that every reader consumed it (the dual-buffering
  *             argument of SiFAR §3.3), so no counter or barrier is needed;
- *   NONE:     never (flags are epoch values, so a stale line never matches).
+ *   NONE:     never (LL8 flags are epoch values, so a stale line never
+ *             matches; not allowed with COLL_SENT).
  */
 enum { COLL_RESET_FUSED = 0, COLL_RESET_KERNEL = 1, COLL_RESET_NONE = 2,
        COLL_RESET_DEFERRED = 3 };
@@ -140,7 +148,7 @@ enum { COLL_PATH_AUTO = 0, COLL_PATH_FUSED = 1, COLL_PATH_STREAMED = 2,
        COLL_PATH_COMPOSED = 3 };
 
 typedef struct {
-    int encoding;        /* COLL_LL8 | COLL_LL128 (default LL8) */
+    int encoding;        /* COLL_LL8 | COLL_LL128 | COLL_SENT (default LL8) */
     int algorithm;       /* COLL_ALGO_AUTO | COLL_ONESHOT | COLL_TWOSHOT */
     int reset_mode;      /* COLL_RESET_* (default DEFERRED) */
     int path;            /* COLL_PATH_* (default AUTO) */

@@ -75,13 +75,18 @@ def test_argument_validation(cd):
 # ---- CPU interpretation of the derived schedule --------------------------------
 
 def _encode(enc, x, epoch):
+    if enc == 2:
+        return oracle.sent_encode(x)
     return oracle.ll8_encode(x, epoch) if enc == 0 else \
         oracle.ll128_encode(x, epoch).reshape(-1, 128)
 
 
 def _decode(enc, lines, elems, epoch):
-    out, rej = (oracle.ll8_decode(lines, elems, epoch) if enc == 0 else
-                oracle.ll128_decode(np.ascontiguousarray(lines).ravel(), elems, epoch))
+    if enc == 2:
+        out, rej = oracle.sent_decode(lines, elems)
+    else:
+        out, rej = (oracle.ll8_decode(lines, elems, epoch) if enc == 0 else
+                    oracle.ll128_decode(np.ascontiguousarray(lines).ravel(), elems, epoch))
     assert rej == 0
     return out
 
@@ -91,12 +96,12 @@ def interpret(cd, spec, enc, n, ins, epoch=5):
     st = cd.coll_debug_items(spec, 0)
     p1 = cd.coll_debug_items(spec, 1)
     p2 = cd.coll_debug_items(spec, 2)
-    width = 1 if enc == 0 else 128
-    dt = np.uint64 if enc == 0 else np.uint8
+    width = 1 if enc != 1 else 128
+    dt = np.uint64 if enc != 1 else np.uint8
     img_lines = int(max([r[7] + r[5] for r in st] + [4]))
     ag_lines = int(max([r[8] + r[5] for r in p1 if r[1] & 1] + [4]))
-    P = [np.zeros((img_lines, width) if enc else img_lines, dtype=dt) for _ in range(n)]
-    AG = [np.zeros((ag_lines, width) if enc else ag_lines, dtype=dt) for _ in range(n)]
+    P = [np.zeros((img_lines, width) if enc == 1 else img_lines, dtype=dt) for _ in range(n)]
+    AG = [np.zeros((ag_lines, width) if enc == 1 else ag_lines, dtype=dt) for _ in range(n)]
     for rank, _, _, _, _, nl, ne, dst_line, in_elem, _ in st:
         assert dst_line % 4 == 0
         P[rank][dst_line:dst_line + nl] = _encode(enc, ins[rank][in_elem:in_elem + ne], epoch)
@@ -141,6 +146,12 @@ CASES = [
     ("ALLGATHER", 4, 4 * 104 + 8, 1, 0, 1),
     ("ALLTOALL", 8, 8 * 960, 1, 0, 2),
     ("ALLTOALL", 4, 4 * 64, 0, 0, 1),
+    ("ALLREDUCE", 8, 8 * 4096, 2, 1, 1),   # sentinel packs
+    ("ALLREDUCE", 8, 8 * 4096, 2, 2, 2),
+    ("ALLREDUCE", 3, 1000, 2, 2, 1),
+    ("REDUCE_SCATTER", 5, 5 * 8 * 7 + 16, 2, 0, 2),
+    ("ALLGATHER", 4, 4 * 104 + 8, 2, 0, 1),
+    ("ALLTOALL", 8, 8 * 960, 2, 0, 2),
 ]
 
 
@@ -151,15 +162,18 @@ def test_derived_schedule_computes_the_oracle_result(cd, name, n, count, enc, al
     try:
         ins = [synth.normal_bf16(3, cd.coll_buffer_elems(spec, r)[0], n, count, r)
                for r in range(n)]
+        if enc == 2:                       # a copy delivers the sanitised input
+            ins[0][::97] = 0xFFFF
         got = interpret(cd, spec, enc, n, ins)
+        san = [oracle.sent_sanitize(x) for x in ins] if enc == 2 else ins
         if name == "ALLREDUCE":
             want = oracle.allreduce(ins)
         elif name == "REDUCE_SCATTER":
             want = oracle.reduce_scatter(ins)
         elif name == "ALLGATHER":
-            want = oracle.all_gather(ins, count)
+            want = oracle.all_gather(san, count)
         else:
-            want = oracle.all_to_all(ins)
+            want = oracle.all_to_all(san)
         for r in range(n):
             assert np.array_equal(got[r], want[r]), f"rank {r}"
     finally:
@@ -240,3 +254,13 @@ def test_v_argument_validation(cd):
     assert cd.coll_buffer_elems(s, 0) == (24, 8)
     assert cd.coll_buffer_elems(s, 1) == (24, 40)
     cd.coll_destroy(s)
+
+
+def test_sentinel_needs_a_rearm(cd):
+    with pytest.raises(cd.CollError) as e:
+        cd.coll_spec_create(*cd.ALLREDUCE, 8, 64, encoding=cd.COLL_SENT,
+                            reset_mode=cd.COLL_RESET_NONE)
+    assert e.value.status == cd.COLL_ERR_UNSUPPORTED
+    for mode in (cd.COLL_RESET_FUSED, cd.COLL_RESET_KERNEL, cd.COLL_RESET_DEFERRED):
+        s = cd.coll_spec_create(*cd.ALLREDUCE, 8, 64, encoding=cd.COLL_SENT, reset_mode=mode)
+        cd.coll_destroy(s)
