@@ -260,9 +260,12 @@ def timed(step, k: int, w: int, stream, world: int) -> float:
     return e0.elapsed_time(e1)
 
 
-def latency_sweep(cd, stream, only_T=None, only_variant=None) -> dict:
-    """8 ranks x [T x 4096] bf16, LL8 (config of the decode-time sweep)."""
+def latency_sweep(cd, stream, only_T=None, only_variant=None, encoding=None) -> dict:
+    """8 ranks x [T x 4096] bf16, LL8 (config of the decode-time sweep), or
+    another readiness encoding."""
     import torch
+
+    enc = cd.COLL_LL8 if encoding is None else encoding
 
     out = {}
     flush = torch.empty(int(2 * L2_BYTES), dtype=torch.uint8, device="cuda")
@@ -277,7 +280,7 @@ def latency_sweep(cd, stream, only_T=None, only_variant=None) -> dict:
                                  (cd.COLL_TWOSHOT, cd.COLL_PATH_STREAMED, "twoshot_streamed")):
             if only_variant is not None and name != only_variant:
                 continue
-            coll = cd.Collective(cd.ALLREDUCE, N_RANKS, count, encoding=cd.COLL_LL8,
+            coll = cd.Collective(cd.ALLREDUCE, N_RANKS, count, encoding=enc,
                                  algorithm=algo, path=path)
             ins = make_inputs(count, 7 + T)
             outs = [torch.empty(count, dtype=torch.int16, device="cuda")
@@ -403,6 +406,39 @@ def v_row(cd, name, total_bytes, stream, steps=5) -> dict:
             "algorithmic_bytes": b, "status": st}
 
 
+def sentinel_row(cd, count, stream, steps=5) -> dict:
+    """8 ranks x `count` bf16 all-reduce, twoshot, sentinel packs, streamed.
+    Algorithmic bytes are the LL form with epsilon = 1 (no readiness bytes);
+    the re-arm writes (N S for the staging slot, S for the reduced
+    partitions) are reported beside them, not in them."""
+    import torch
+
+    n = N_RANKS
+    coll = cd.Collective(cd.ALLREDUCE, n, count, encoding=cd.COLL_SENT,
+                         algorithm=cd.COLL_TWOSHOT, path=cd.COLL_PATH_STREAMED)
+    ins = make_inputs(count, 13)
+    outs = [torch.empty(count, dtype=torch.int16, device="cuda") for _ in range(n)]
+    with torch.cuda.stream(stream):
+        for _ in range(2):
+            coll.run(ins, outs, stream)
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(steps):
+            coll.run(ins, outs, stream)
+        e1.record(stream)
+        stream.synchronize()
+    ms = e0.elapsed_time(e1) / steps
+    s = count * 2.0
+    b = bytes_allreduce_twoshot(n, s, 1.0)
+    st = coll.status(stream)[0]
+    coll.close()
+    del coll, ins, outs
+    torch.cuda.empty_cache()
+    return {"ms": round(ms, 4), "GB/s": round(b / ms / 1e6, 1), "algorithmic_bytes": b,
+            "rearm_bytes": (n + 1) * s, "status": st}
+
+
 def moe_row(cd, stream, steps=5) -> dict:
     """MoE dispatch: 8 ranks x 4096 tokens x 7168 bf16, top-8 of 256 experts
     (routing drawn on the device from a seeded generator)."""
@@ -471,6 +507,8 @@ def main() -> int:
     ap.add_argument("--sweep-T", type=int, default=None, help="sweep only this T")
     ap.add_argument("--sweep-variant", default=None,
                     help="sweep only this variant, e.g. twoshot_fused")
+    ap.add_argument("--sweep-enc", default="ll8", choices=["ll8", "ll128", "sent"],
+                    help="readiness encoding of the sweep")
     args = ap.parse_args()
     if args.impl == "reference":
         return run_reference(args)
@@ -495,8 +533,10 @@ def main() -> int:
     peaks = load_peaks()
     stream = torch.cuda.Stream()
     if args.sweep_only:
-        print(json.dumps({"latency_us_per_op": latency_sweep(cd, stream, args.sweep_T,
-                                                             args.sweep_variant)}))
+        enc = {"ll8": cd.COLL_LL8, "ll128": cd.COLL_LL128, "sent": cd.COLL_SENT}[args.sweep_enc]
+        print(json.dumps({"encoding": args.sweep_enc,
+                          "latency_us_per_op": latency_sweep(cd, stream, args.sweep_T,
+                                                             args.sweep_variant, enc)}))
         return 0
     count = args.mib * 2**20 // 2
     s_bytes = count * 2.0
@@ -636,6 +676,7 @@ def main() -> int:
             "reduce_scatter_v_zipf_256MiB": v_row(cd, "REDUCE_SCATTER_V", 256 << 20, stream),
             "all_gather_v_zipf_256MiB": v_row(cd, "ALLGATHER_V", 256 << 20, stream),
             "all_to_all_v_zipf_256MiB": v_row(cd, "ALLTOALL_V", 256 << 20, stream),
+            "allreduce_256MiB_sentinel_twoshot": sentinel_row(cd, count, stream),
         }
         line["latency_us_per_op"] = latency_sweep(cd, stream)
         if world == 1:
