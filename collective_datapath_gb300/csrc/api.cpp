@@ -137,26 +137,33 @@ cudaError_t launched(coll_spec* s, cudaError_t e, cudaStream_t st) {
   return cudaSuccess;
 }
 
-// Shape of the composed twoshot launch: chunks of 256 lines of every
-// partition, CTA groups split 40 % stage / 25 % fold / 35 % gather of the
-// co-resident grid, a window of 24 chunks (~50 MB of staging in L2 at 8
-// ranks), staging dropped from L2 once folded.  COLL_COMPOSED_SHAPE =
-// "chunk_lines,stage%,fold%,window,discard" overrides it (benchmark sweeps).
-ComposedParams composed_shape(const Plan& p, int grid) {
+// Shape of the composed twoshot launch: chunks of 128 lines of every
+// partition, a lag of 64 queue steps between a chunk's stage, fold and
+// gather tasks, consumed lines dropped from L2.  COLL_COMPOSED_SHAPE =
+// "chunk_lines,lag,discard" overrides it (benchmark sweeps); chunks are a
+// power of two of at least kComposedMinChunk lines, the size the completion
+// flags were laid out for.
+ComposedParams composed_shape(const coll_spec* s) {
+  const Plan& p = s->plan;
   ComposedParams q{};
-  int chunk = 256, stage_pct = 40, fold_pct = 25, window = 24, discard = 1;
+  int chunk = 128, lag = 64, discard = 1;
   if (const char* env = std::getenv("COLL_COMPOSED_SHAPE"))
-    std::sscanf(env, "%d,%d,%d,%d,%d", &chunk, &stage_pct, &fold_pct, &window, &discard);
-  chunk = std::max(4, chunk / 4 * 4);
+    std::sscanf(env, "%d,%d,%d", &chunk, &lag, &discard);
+  // a power of two of at least kComposedMinChunk lines (rows per chunk are
+  // counted with shifts)
+  int c2 = (int)kComposedMinChunk;
+  while (c2 * 2 <= chunk && c2 < (1 << 20)) c2 *= 2;
+  chunk = c2;
   uint64_t max_lines = 0;
   for (const Seg& sg : p.pseg[0]) max_lines = std::max<uint64_t>(max_lines, sg.lines);
   q.chunk_lines = (uint32_t)chunk;
-  q.nchunks = (uint32_t)((max_lines + chunk - 1) / chunk);
-  q.n_stage = std::max(1, grid * stage_pct / 100);
-  q.n_fold = std::max(1, grid * fold_pct / 100);
-  if (q.n_stage + q.n_fold >= grid) q.n_fold = std::max(1, grid - q.n_stage - 1);
-  q.window = std::max(1, window);
+  q.nchunks = (uint32_t)std::max<uint64_t>(1, (max_lines + chunk - 1) / chunk);
+  q.lag = std::max(1, lag);
   q.discard = discard;
+  char* f = s->ws + p.off_cflags;
+  q.flag_stage = reinterpret_cast<uint64_t*>(f);
+  q.flag_fold = q.flag_stage + p.composed_max_chunks * p.n;
+  q.gather_cnt = q.flag_fold + p.composed_max_chunks * p.n;
   return q;
 }
 
@@ -385,7 +392,7 @@ coll_status_t coll_run(coll_spec_t* s, const void* const* dev_ins, void* const* 
   if (dev_ins != nullptr && p.path == COLL_PATH_COMPOSED && !empty) {
     const int cap = composed_capacity();
     if (cap < 3) return COLL_ERR_CUDA;
-    P.cp = composed_shape(p, cap);
+    P.cp = composed_shape(s);
     P.advance_epoch = 1;
     return cuda_status(launched(s, launch_composed(P, cap, st), st));
   }

@@ -1,26 +1,32 @@
 // composed.cu -- the twoshot all-reduce as one persistent cooperative launch.
 //
-// Purlin §3.2 ("Extending the execution to AllReduce", Figure 5, Algorithm 1):
-// three CTA groups run concurrently at the granularity of a chunk -- staging
-// CTAs, reducer CTAs that fold partition r of every rank and publish it, and
-// gather CTAs that copy every published partition into every output.  Here
-// the notification between the groups is the LL128 sequence number carried
-// by every line (flash-comm §3.1), so the groups need no counters to be
-// correct; two counters only keep each group within `window` chunks of the
-// next one, so that a chunk's staged and published lines are still in L2 when
-// their reader comes (the 126 MiB L2 stands in for the interconnect).
+// Purlin §3.2 ("Extending the execution to AllReduce", Figure 5, Algorithm 1)
+// runs the reduce-scatter and the all-gather of a twoshot all-reduce as
+// concurrent stage, reduce and gather work at chunk granularity, with chunk
+// completion signalled to the next role.  Here every partition is cut into
+// chunks of `chunk_lines` LL128 lines and the run is a queue of tasks:
+//   stage  S(c, p): rank p's input -> its staged lines of chunk c (all N
+//                   partitions);
+//   fold   F(c, r): chunk c of partition r from all N staged images ->
+//                   folded in rank order, published as lines of owner r;
+//   gather G(c, d): chunk c of every owner's published partition -> rank d's
+//                   output.
+// Queue step t holds S(t, *), then F(t - lag, *), then G(t - 2 lag, *).  CTAs
+// take tasks in queue order from one counter, so a task only ever waits for
+// tasks that are earlier in the queue and already taken by co-resident CTAs:
+// the earliest unfinished task waits for nothing, so the launch always
+// progresses.  The lag keeps a chunk's staged and published lines in L2
+// between producer and reader (the working set is about `lag` steps of
+// chunks, a few tens of MB at most), and a staged line's only reader drops
+// it from L2 once folded, so staging does not reach HBM.
 //
-// Units (c = chunk, one chunk = chunk_lines lines of every partition):
-//   stage  (c, p): rank p's input -> the chunk's lines of its N partitions
-//   fold   (c, r): partition r's chunk lines of all N ranks -> folded, published
-//   gather (c, d): every owner's published chunk lines -> rank d's output
-// Memory ordering per unit: a producer CTA stores all data, __syncthreads,
-// every thread fence.acq_rel.gpu, then the sequence numbers (a release
-// pattern); a consumer CTA polls every sequence number of the unit, every
-// thread fence.acq_rel.gpu, __syncthreads, then reads the data (an acquire
-// pattern).  Each line is still checked; the fence is paid once per unit.
-// A staged line has exactly one reader (its fold unit), which drops it from
-// L2 after reading it (discard.global.L2), so staging never reaches HBM.
+// Readiness: a producer task stores its lines (data and the epoch as the
+// LL128 sequence number), then __syncthreads, one fence.acq_rel.gpu and the
+// task's flag = epoch (release); a consumer task waits for the flags of the
+// N tasks it reads (acquire fence, __syncthreads), loads the lines and still
+// checks every line's number.  Flags hold epochs, so they never need a
+// reset.  The gather count of a chunk carries the epoch in its high bits; the
+// N-th gather of a chunk drops the published lines of that chunk from L2.
 #include <cuda_runtime.h>
 
 #include "launch.h"
@@ -31,8 +37,8 @@ namespace coll {
 
 constexpr int kCThreads = 256;
 constexpr int kCWarps = kCThreads / 32;
-constexpr int kCFoldStages = 3;                      // rows of all N images per warp
-constexpr int kCRing = kCFoldStages * kMaxRanks;     // rows per warp (stage / gather)
+constexpr int kCRing = 16;                         // rows in flight per warp
+constexpr int kCFoldStages = kCRing / kMaxRanks;   // rows of all N images per warp
 
 size_t composed_smem_bytes() { return (size_t)kCWarps * kCRing * kRowBytes; }
 
@@ -44,289 +50,317 @@ __device__ __forceinline__ int seg_lines_of(const RunParams& P, int k) {
   return (int)((P.seg_elems[k] + kLL128Elems - 1) / kLL128Elems);
 }
 
-// Bounded wait for a counter to reach `target` (flow control).
-__device__ __forceinline__ bool wait_counter(const RunParams& P, const uint32_t* ctr,
-                                             uint32_t target) {
-  if (ld_relaxed_u32(ctr) >= target) return true;
-  Waiter w;
-  while (ld_relaxed_u32(ctr) < target) {
-    if (w.expired(P.ws, P.timeout_ns)) {
-      latch_error(P.ws, kStatusTimeout, 0xFFFFFFFEu, -3);
-      return false;
-    }
-    __nanosleep(200);
-  }
-  return true;
+// Lines of segment k inside the chunk starting at line t0 (0 past its end).
+__device__ __forceinline__ int chunk_lines_of(const RunParams& P, int k, uint32_t t0) {
+  return max(0, min((int)P.cp.chunk_lines, seg_lines_of(P, k) - (int)t0));
 }
 
-// Every thread polls its share of a unit's sequence numbers -- all loads
-// issued before any is checked -- then fences; the caller's __syncthreads
-// completes the acquire for the whole CTA.  `line_addr(i)` gives line i of
-// the unit (i < total); at most kPollPerThread lines per thread per batch.
-constexpr int kPollPerThread = 8;
-
-template <class F>
-__device__ __forceinline__ bool poll_unit(const RunParams& P, int total, uint64_t seq, F line_addr) {
+// Threads 0..n-1 wait (bounded) for flags[thread] == e, each then fences
+// (acquire); the caller's __syncthreads hands the ordering to the CTA.
+__device__ __forceinline__ bool acquire_flags(const RunParams& P, const uint64_t* flags, int n,
+                                              uint64_t e) {
   bool ok = true;
-  for (int base = 0; base < total; base += kPollPerThread * (int)blockDim.x) {
-    uint64_t v[kPollPerThread];
-#pragma unroll
-    for (int j = 0; j < kPollPerThread; ++j) {
-      const int i = base + j * (int)blockDim.x + (int)threadIdx.x;
-      v[j] = i < total ? ld_relaxed_u64(line_addr(i) + 120) : seq;
+  if ((int)threadIdx.x < n) {
+    const uint64_t* f = flags + threadIdx.x;
+    if (ld_relaxed_u64(f) != e) {
+      Waiter w;
+      while (ld_relaxed_u64(f) != e) {
+        if (w.expired(P.ws, P.timeout_ns)) {
+          latch_error(P.ws, kStatusTimeout, threadIdx.x, -3);
+          ok = false;
+          break;
+        }
+        __nanosleep(64);
+      }
     }
-#pragma unroll
-    for (int j = 0; j < kPollPerThread; ++j) {
-      const int i = base + j * (int)blockDim.x + (int)threadIdx.x;
-      if (ok && v[j] != seq) ok = ll128_wait_seq(P, line_addr(i) + 120, seq, 0, i);
-    }
+    fence_acq_rel_gpu();
   }
   return ok;
 }
 
-__global__ void __launch_bounds__(kCThreads, 2) k_composed_ll128(RunParams P) {
+// After every data store of the CTA: one release of the task's flag, unless
+// the task failed.
+__device__ __forceinline__ void release_flag(uint64_t* flag, uint64_t e, const int& s_ok) {
+  __syncthreads();
+  if (threadIdx.x == 0 && s_ok) {
+    fence_acq_rel_gpu();
+    st_relaxed_u64(flag, e);
+  }
+}
+
+// Per-task descriptors of the N pieces a stage or gather task moves (one
+// per partition), filled by threads 0..n-1 before the task's first barrier.
+// Rows of the task are numbered i = piece * R + row, R = chunk_lines / 4 a
+// power of two; rows past a short piece are skipped.
+struct Piece {
+  const char* src;  // first source byte of the piece in this chunk
+  char* dst;        // first destination byte
+  int nl;           // lines of the piece in this chunk
+  int left;         // payload elements of the piece from the chunk start
+};
+
+__device__ __forceinline__ void fill_stage_piece(const RunParams& P, Piece* pc, int c, int p,
+                                                 uint64_t e) {
+  const int k = threadIdx.x;
+  const uint32_t t0 = (uint32_t)c * P.cp.chunk_lines;
+  pc[k].src = reinterpret_cast<const char*>(P.in[p] + P.seg_in0[k] + (uint64_t)t0 * kLL128Elems);
+  pc[k].dst = image_bytes(P, P.P, e, p) + (P.seg_line0[k] + t0) * kLL128LineBytes;
+  pc[k].nl = chunk_lines_of(P, k, t0);
+  const int64_t lk = (int64_t)P.seg_elems[k] - (int64_t)t0 * kLL128Elems;
+  pc[k].left = (int)(lk < (int64_t)P.cp.chunk_lines * kLL128Elems ? lk
+                                                                  : (int64_t)P.cp.chunk_lines * kLL128Elems);
+}
+
+__device__ __forceinline__ void fill_gather_piece(const RunParams& P, Piece* pc, int c, int d,
+                                                  uint64_t e) {
+  const int r = threadIdx.x;
+  const uint32_t t0 = (uint32_t)c * P.cp.chunk_lines;
+  pc[r].src = image_bytes(P, P.AG, e, r) + (uint64_t)t0 * kLL128LineBytes;
+  pc[r].dst = reinterpret_cast<char*>(P.out[d] + P.seg_in0[r] + (uint64_t)t0 * kLL128Elems);
+  pc[r].nl = chunk_lines_of(P, r, t0);
+  const int64_t lr = (int64_t)P.seg_elems[r] - (int64_t)t0 * kLL128Elems;
+  pc[r].left = (int)(lr < (int64_t)P.cp.chunk_lines * kLL128Elems ? lr
+                                                                  : (int64_t)P.cp.chunk_lines * kLL128Elems);
+}
+
+__device__ __forceinline__ void stage_task(const Piece* pc, uint32_t wbase, int lane, int warp,
+                                           int n, int rsh, uint64_t e) {
+  const int li = lane >> 3, kk = lane & 7;
+  const int G = 15 * li + 2 * kk;  // first payload granule of this lane's line chunk
+  const int rmask = (1 << rsh) - 1;
+  const int nrows = n << rsh;
+  const int nj = warp < nrows ? (nrows - warp + kCWarps - 1) / kCWarps : 0;
+  auto issue = [&](int j) {
+    if (j < nj) {
+      const int i = warp + j * kCWarps, k = i >> rsh, r = i & rmask;
+      const int left = pc[k].left - r * kRowElems;
+      const bool valid = 4 * r < pc[k].nl && lane < 30 && 8 * lane < left;
+      cp_async16(wbase + (j % kCRing) * kRowBytes + 16 * lane,
+                 pc[k].src + (size_t)r * (2 * kRowElems) + (valid ? 16 * lane : 0), valid);
+    }
+    cp_async_commit();
+  };
+#pragma unroll 1
+  for (int j = 0; j < kCRing; ++j) issue(j);
+  for (int j = 0; j < nj; ++j) {
+    cp_async_wait<kCRing - 1>();
+    __syncwarp();
+    const uint32_t row = wbase + (j % kCRing) * kRowBytes;
+    // lanes 30, 31 hold no input: their slot bytes [480, 512) stay unread
+    const uint2 a = lds_v2(row + 8 * G);
+    const uint2 b = kk == 7 ? make_uint2(0, 0) : lds_v2(row + 8 * (G + 1));
+    __syncwarp();
+    issue(j + kCRing);
+    const int i = warp + j * kCWarps, k = i >> rsh, r = i & rmask;
+    const int nl_row = pc[k].nl - 4 * r;
+    if (nl_row > 0)
+      ll128_store_row<false>(pc[k].dst + (size_t)r * kRowBytes, make_uint4(a.x, a.y, b.x, b.y),
+                             lane, min((int)kLL128RowLines, nl_row), e);
+  }
+  cp_async_wait<0>();
+  __syncwarp();
+}
+
+__device__ __forceinline__ bool fold_task(const RunParams& P, uint32_t wbase, int lane, int warp,
+                                          int c, int r, uint64_t e) {
+  const int n = P.nranks;
+  const uint32_t t0 = (uint32_t)c * P.cp.chunk_lines;
+  const int nl = chunk_lines_of(P, r, t0);
+  const int li = lane >> 3;
+  const uint64_t src_line = P.seg_line0[r] + t0;
+  // rank p's rows of this piece start at src0 + p * rank_bytes
+  const char* src0 = image_bytes(P, P.P, e, 0) + src_line * kLL128LineBytes;
+  const uint64_t rb = P.P.rank_bytes;
+  const int nrows = (nl + kLL128RowLines - 1) / kLL128RowLines;
+  const int nj = warp < nrows ? (nrows - warp + kCWarps - 1) / kCWarps : 0;
+  auto issue = [&](int j) {
+    if (j < nj) {
+      const int rr = warp + j * kCWarps;
+      const bool valid = li < nl - rr * kLL128RowLines;
+      const uint32_t sl = wbase + (uint32_t)((j % kCFoldStages) * kMaxRanks * kRowBytes) + 16 * lane;
+#pragma unroll
+      for (int p = 0; p < kMaxRanks; ++p)
+        if (p < n)
+          cp_async16(sl + p * kRowBytes, src0 + p * rb + (size_t)rr * kRowBytes + 16 * lane, valid);
+    }
+    cp_async_commit();
+  };
+#pragma unroll
+  for (int j = 0; j < kCFoldStages; ++j) issue(j);
+  char* ag = image_bytes(P, P.AG, e, r) + (uint64_t)t0 * kLL128LineBytes;
+  bool ok = true;
+  for (int j = 0; j < nj; ++j) {
+    cp_async_wait<kCFoldStages - 1>();
+    const uint32_t sl = wbase + (uint32_t)((j % kCFoldStages) * kMaxRanks * kRowBytes) + 16 * lane;
+    const int rr = warp + j * kCWarps;
+    const int nl_row = min((int)kLL128RowLines, nl - rr * kLL128RowLines);
+    const bool valid = li < nl_row;
+    uint4 s[kMaxRanks];
+#pragma unroll
+    for (int p = 0; p < kMaxRanks; ++p)
+      if (p < n) s[p] = lds_v4(sl + p * kRowBytes);
+    bool ready = true;
+#pragma unroll
+    for (int p = 0; p < kMaxRanks; ++p)
+      if (p < n) ready = ready && ll128_chunk_ready(s[p], lane, valid, e);
+    if (!__all_sync(0xFFFFFFFFu, ready)) {
+      // the producer's flag was set, so this only happens if the protocol
+      // is broken: wait for the numbers on global memory, bounded
+      const uint64_t row_line = src_line + (uint64_t)rr * kLL128RowLines;
+#pragma unroll
+      for (int p = 0; p < kMaxRanks; ++p) {
+        if (p < n && ok) {
+          const bool rp = ll128_chunk_ready(s[p], lane, valid, e);
+          if (!__all_sync(0xFFFFFFFFu, rp)) {
+            const char* grow = src0 + p * rb + (size_t)rr * kRowBytes;
+            ok = ll128_wait_chunk(P, grow, lane, rp, e, p, (int64_t)row_line);
+            if (ok && valid) s[p] = ld_v4(grow + 16 * lane);
+          }
+        }
+      }
+      if (!ok) break;
+    }
+    issue(j + kCFoldStages);
+    // the staged lines of this row have no other reader: drop them
+    if (P.cp.discard && lane < 4 * n && (lane & 3) < nl_row) {
+      discard_l2_line(src0 + (lane >> 2) * rb + (size_t)rr * kRowBytes +
+                      (size_t)(lane & 3) * kLL128LineBytes);
+    }
+    const uint4 res = ll128_fold(s, n);
+    ll128_store_row<false>(ag + (size_t)rr * kRowBytes, res, lane, nl_row, e);
+  }
+  cp_async_wait<0>();
+  __syncwarp();
+  return ok;
+}
+
+__device__ __forceinline__ bool gather_task(const RunParams& P, const Piece* pc, uint32_t wbase,
+                                            int lane, int warp, int rsh, uint64_t e) {
+  const int n = P.nranks;
+  const int li = lane >> 3;
+  // output chunk q = lane: its two payload granules in the row
+  const int q = lane < 30 ? lane : 29;
+  const uint32_t g0off = 128 * ((2 * q) / 15) + 8 * ((2 * q) % 15);
+  const uint32_t g1off = 128 * ((2 * q + 1) / 15) + 8 * ((2 * q + 1) % 15);
+  const int rmask = (1 << rsh) - 1;
+  const int nrows = n << rsh;
+  const int nj = warp < nrows ? (nrows - warp + kCWarps - 1) / kCWarps : 0;
+  auto issue = [&](int j) {
+    if (j < nj) {
+      const int i = warp + j * kCWarps, r = i >> rsh, rr = i & rmask;
+      cp_async16(wbase + (j % kCRing) * kRowBytes + 16 * lane,
+                 pc[r].src + (size_t)rr * kRowBytes + 16 * lane, li < pc[r].nl - 4 * rr);
+    }
+    cp_async_commit();
+  };
+#pragma unroll 1
+  for (int j = 0; j < kCRing; ++j) issue(j);
+  bool ok = true;
+  for (int j = 0; j < nj; ++j) {
+    cp_async_wait<kCRing - 1>();
+    __syncwarp();
+    const uint32_t row = wbase + (j % kCRing) * kRowBytes;
+    const int i = warp + j * kCWarps, r = i >> rsh, rr = i & rmask;
+    const int nl_row = pc[r].nl - 4 * rr;
+    const bool valid = li < nl_row;
+    const bool ready = !(valid && (lane & 7) == 7) || lds_u64(row + 16 * lane + 8) == e;
+    if (!__all_sync(0xFFFFFFFFu, ready)) {
+      const char* grow = pc[r].src + (size_t)rr * kRowBytes;
+      ok = ll128_wait_chunk(P, grow, lane, ready, e, r, (int64_t)rr * kLL128RowLines);
+      if (!ok) break;
+      if (valid) sts_v4(row + 16 * lane, ld_v4(grow + 16 * lane));
+      __syncwarp();
+    }
+    const uint2 a = lds_v2(row + g0off), b = lds_v2(row + g1off);
+    __syncwarp();  // every lane read the slot before it is refilled
+    issue(j + kCRing);
+    const int left = pc[r].left - rr * kRowElems;
+    if (nl_row > 0 && lane < 30 && 8 * lane < left)
+      st_v4(pc[r].dst + (size_t)rr * (2 * kRowElems) + 16 * lane, make_uint4(a.x, a.y, b.x, b.y));
+  }
+  cp_async_wait<0>();
+  __syncwarp();
+  return ok;
+}
+
+// Counts one finished gather of chunk c in this epoch; true for the N-th.
+// Called by one thread after its CTA's reads of the chunk completed.
+__device__ __forceinline__ bool last_gather(const RunParams& P, int c, uint64_t e) {
+  unsigned long long* cnt = reinterpret_cast<unsigned long long*>(P.cp.gather_cnt + c);
+  unsigned long long old = ld_relaxed_u64(cnt), want;
+  for (;;) {
+    want = (old >> 8) == e ? old + 1 : ((e << 8) | 1ull);
+    const unsigned long long seen = atomicCAS(cnt, old, want);
+    if (seen == old) break;
+    old = seen;
+  }
+  return (int)(want & 0xFFull) == P.nranks;
+}
+
+__global__ void __launch_bounds__(kCThreads, 3) k_composed_ll128(RunParams P) {
   extern __shared__ __align__(128) char smem[];
-  __shared__ int s_ok;
+  __shared__ Piece s_piece[kMaxRanks];
+  __shared__ int s_task[2];
+  __shared__ int s_ok, s_last;
   const uint64_t e = begin_run(P);
   const ComposedParams& Q = P.cp;
   WsHeader* h = header(P.ws);
   const int n = P.nranks;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int li = lane >> 3, kk = lane & 7;
-  const uint32_t Lc = Q.chunk_lines;
-  const int units = (int)Q.nchunks * n;
   const int slot = (int)(e & 1);
+  const int per_step = 3 * n;
+  const int ntasks = ((int)Q.nchunks + 2 * Q.lag) * per_step;
+  const int rsh = __ffs((int)Q.chunk_lines / kLL128RowLines) - 1;  // rows per chunk = 2^rsh
   const uint32_t wbase =
       (uint32_t)__cvta_generic_to_shared(smem) + (uint32_t)(warp * kCRing * kRowBytes);
-  int role, first, stride;
-  if ((int)blockIdx.x < Q.n_stage) {
-    role = 0; first = blockIdx.x; stride = Q.n_stage;
-  } else if ((int)blockIdx.x < Q.n_stage + Q.n_fold) {
-    role = 1; first = blockIdx.x - Q.n_stage; stride = Q.n_fold;
-  } else {
-    role = 2; first = blockIdx.x - Q.n_stage - Q.n_fold;
-    stride = gridDim.x - Q.n_stage - Q.n_fold;
+  if (threadIdx.x == 0) {
+    s_task[0] = (int)atomicAdd(&h->task_next[slot], 1u);
+    s_ok = 1;
   }
-  // payload granules of output chunk q (gather) and of line chunk (li, kk) (stage)
-  const int q = lane < 30 ? lane : 29;
-  const uint32_t g0off = 128 * ((2 * q) / 15) + 8 * ((2 * q) % 15);
-  const uint32_t g1off = 128 * ((2 * q + 1) / 15) + 8 * ((2 * q + 1) % 15);
-  const int G = 15 * li + 2 * kk;
-
-  for (int u = first; u < units; u += stride) {
-    if (aborted(P.ws)) break;
-    const int c = u / n, x = u % n;  // x = rank p (stage), owner r (fold), rank d (gather)
-    const uint32_t t0 = (uint32_t)c * Lc;
-    if (role == 0) {
-      // ---- stage (c, p = x) ------------------------------------------------------
-      if (threadIdx.x == 0) {
-        s_ok = c < Q.window ||
-               wait_counter(P, &h->fold_done[slot], (uint32_t)(c - Q.window + 1) * n);
-      }
-      __syncthreads();
-      if (!s_ok) break;
-      // the unit's rows (all N partition tiles) as one stream per warp
-      int rows_before[kMaxRanks + 1];
-      rows_before[0] = 0;
-      for (int k = 0; k < n; ++k) {
-        const int nl = max(0, min((int)Lc, seg_lines_of(P, k) - (int)t0));
-        rows_before[k + 1] = rows_before[k] + (nl + kLL128RowLines - 1) / kLL128RowLines;
-      }
-      const int nrows = rows_before[n];
-      const int nj = warp < nrows ? (nrows - warp + kCWarps - 1) / kCWarps : 0;
-      auto locate = [&](int gr, int& k, int& r) {
-        k = 0;
-        while (k + 1 < n && gr >= rows_before[k + 1]) ++k;
-        r = gr - rows_before[k];
-      };
-      auto issue = [&](int j) {
-        if (j < nj) {
-          int k, r;
-          locate(warp + j * kCWarps, k, r);
-          const int64_t left =
-              (int64_t)P.seg_elems[k] - ((int64_t)t0 * kLL128Elems + (int64_t)r * kRowElems);
-          const bool valid = lane < 30 && 8 * lane < left;
-          const uint16_t* src = P.in[x] + P.seg_in0[k] + (uint64_t)t0 * kLL128Elems +
-                                (uint64_t)r * kRowElems + (valid ? 8 * lane : 0);
-          cp_async16(wbase + (j % kCRing) * kRowBytes + 16 * lane, src, valid);
-        }
-        cp_async_commit();
-      };
-#pragma unroll 1
-      for (int j = 0; j < kCRing; ++j) issue(j);
-      for (int j = 0; j < nj; ++j) {
-        cp_async_wait<kCRing - 1>();
-        __syncwarp();
-        const uint32_t row = wbase + (j % kCRing) * kRowBytes;
-        const uint2 a = lds_v2(row + 8 * G);
-        const uint2 b = kk == 7 ? make_uint2(0, 0) : lds_v2(row + 8 * (G + 1));
-        __syncwarp();
-        issue(j + kCRing);
-        int k, r;
-        locate(warp + j * kCWarps, k, r);
-        const int nl = min((int)Lc, seg_lines_of(P, k) - (int)t0);
-        const int nl_row = min((int)kLL128RowLines, nl - r * kLL128RowLines);
-        if (li < nl_row) {
-          char* dst = image_bytes(P, P.P, e, x) +
-                      (P.seg_line0[k] + t0 + (uint64_t)r * kLL128RowLines) * kLL128LineBytes +
-                      16 * lane;
-          if (kk == 7)
-            st_v2u32(dst, a.x, a.y);
-          else
-            st_v4(dst, make_uint4(a.x, a.y, b.x, b.y));
-        }
-      }
-      cp_async_wait<0>();
-      // release: every data store of the CTA, then the numbers
-      __syncthreads();
-      fence_acq_rel_gpu();
-      for (int k = 0; k < n; ++k) {
-        const int nl = min((int)Lc, seg_lines_of(P, k) - (int)t0);
-        char* img = image_bytes(P, P.P, e, x) + (P.seg_line0[k] + t0) * kLL128LineBytes;
-        for (int j = threadIdx.x; j < nl; j += blockDim.x)
-          st_relaxed_u64(img + (size_t)j * kLL128LineBytes + 120, e);
-      }
-    } else if (role == 1) {
-      // ---- fold (c, r = x) ---------------------------------------------------------
-      const int r = x;
-      const int nl = min((int)Lc, seg_lines_of(P, r) - (int)t0);
-      if (threadIdx.x == 0) {
-        s_ok = c < Q.window ||
-               wait_counter(P, &h->gather_done[slot], (uint32_t)(c - Q.window + 1) * n);
-      }
-      __syncthreads();
-      if (!s_ok) break;
-      if (nl > 0) {
-        const uint64_t src_line = P.seg_line0[r] + t0;
-        // acquire every line of the unit
-        const bool ok = poll_unit(P, n * nl, e, [&](int idx) {
-          return (const char*)image_bytes(P, P.P, e, idx / nl) +
-                 (src_line + (uint64_t)(idx % nl)) * kLL128LineBytes;
-        });
-        fence_acq_rel_gpu();
-        if (threadIdx.x == 0) s_ok = 1;
+  __syncthreads();
+  for (int it = 0;; ++it) {
+    const int t = s_task[it & 1];
+    if (t >= ntasks) break;
+    // take the next task now; it is needed only after this one
+    if (threadIdx.x == 0)
+      s_task[(it + 1) & 1] = aborted(P.ws) ? ntasks : (int)atomicAdd(&h->task_next[slot], 1u);
+    const int step = t / per_step, rem = t % per_step;
+    const int kind = rem / n, x = rem % n;
+    const int c = step - kind * Q.lag;
+    if (c >= 0 && c < (int)Q.nchunks) {
+      if (kind == 0) {
+        if ((int)threadIdx.x < n) fill_stage_piece(P, s_piece, c, x, e);
         __syncthreads();
-        if (!ok) s_ok = 0;
+        stage_task(s_piece, wbase, lane, warp, n, rsh, e);
+        release_flag(Q.flag_stage + (size_t)c * n + x, e, s_ok);
+      } else if (kind == 1) {
+        if (!acquire_flags(P, Q.flag_stage + (size_t)c * n, n, e)) s_ok = 0;
         __syncthreads();
-        if (!s_ok) break;
-        const int nrows = (nl + kLL128RowLines - 1) / kLL128RowLines;
-        const int nj = warp < nrows ? (nrows - warp + kCWarps - 1) / kCWarps : 0;
-        auto issue = [&](int j) {
-          if (j < nj) {
-            const int rr = warp + j * kCWarps;
-            const int nl_row = min((int)kLL128RowLines, nl - rr * kLL128RowLines);
-            const uint64_t off =
-                (src_line + (uint64_t)rr * kLL128RowLines) * kLL128LineBytes + 16 * lane;
-            const uint32_t sl = wbase + (uint32_t)((j % kCFoldStages) * n * kRowBytes);
-            for (int p = 0; p < n; ++p)
-              cp_async16(sl + p * kRowBytes + 16 * lane, image_bytes(P, P.P, e, p) + off,
-                         li < nl_row);
-          }
-          cp_async_commit();
-        };
-#pragma unroll
-        for (int j = 0; j < kCFoldStages; ++j) issue(j);
-        char* ag = image_bytes(P, P.AG, e, r) + (uint64_t)t0 * kLL128LineBytes;
-        for (int j = 0; j < nj; ++j) {
-          cp_async_wait<kCFoldStages - 1>();
-          const uint32_t sl = wbase + (uint32_t)((j % kCFoldStages) * n * kRowBytes);
-          uint4 s[kMaxRanks];
-#pragma unroll
-          for (int p = 0; p < kMaxRanks; ++p)
-            if (p < n) s[p] = lds_v4(sl + p * kRowBytes + 16 * lane);
-          issue(j + kCFoldStages);
-          const int rr = warp + j * kCWarps;
-          const int nl_row = min((int)kLL128RowLines, nl - rr * kLL128RowLines);
-          // the staged lines of this row have no other reader: drop them
-          if (Q.discard && lane < 4 * n && (lane & 3) < nl_row)
-            discard_l2_line(image_bytes(P, P.P, e, lane >> 2) +
-                            (src_line + (uint64_t)rr * kLL128RowLines + (lane & 3)) *
-                                kLL128LineBytes);
-          const uint4 res = ll128_fold(s, n);
-          if (li < nl_row) {
-            char* dst = ag + (size_t)rr * kRowBytes + 16 * lane;
-            if (kk == 7)
-              st_v2u32(dst, res.x, res.y);
-            else
-              st_v4(dst, res);
+        if (s_ok) {
+          if (!fold_task(P, wbase, lane, warp, c, x, e)) s_ok = 0;
+          release_flag(Q.flag_fold + (size_t)c * n + x, e, s_ok);
+        }
+      } else {
+        if ((int)threadIdx.x < n) fill_gather_piece(P, s_piece, c, x, e);
+        if (!acquire_flags(P, Q.flag_fold + (size_t)c * n, n, e)) s_ok = 0;
+        __syncthreads();
+        if (s_ok) {
+          if (!gather_task(P, s_piece, wbase, lane, warp, rsh, e)) s_ok = 0;
+          __syncthreads();
+          if (threadIdx.x == 0) s_last = s_ok && Q.discard && last_gather(P, c, e);
+          __syncthreads();
+          if (s_last) {
+            for (int r = 0; r < n; ++r) {
+              const int nl = s_piece[r].nl;
+              for (int j = threadIdx.x; j < nl; j += blockDim.x)
+                discard_l2_line(s_piece[r].src + (size_t)j * kLL128LineBytes);
+            }
           }
         }
-        cp_async_wait<0>();
-        __syncthreads();
-        fence_acq_rel_gpu();
-        for (int j = threadIdx.x; j < nl; j += blockDim.x)
-          st_relaxed_u64(ag + (size_t)j * kLL128LineBytes + 120, e);
       }
-      __syncthreads();
-      if (threadIdx.x == 0) {
-        __threadfence();
-        atomicAdd(&h->fold_done[slot], 1u);
-      }
-    } else {
-      // ---- gather (c, d = x) -------------------------------------------------------
-      const int d = x;
-      int rows_before[kMaxRanks + 1];
-      rows_before[0] = 0;
-      for (int r = 0; r < n; ++r) {
-        const int nl = max(0, min((int)Lc, seg_lines_of(P, r) - (int)t0));
-        rows_before[r + 1] = rows_before[r] + (nl + kLL128RowLines - 1) / kLL128RowLines;
-      }
-      // owners' chunk tiles have Lc lines except in the last chunk; lines
-      // past a shorter tile are skipped by pointing them at a ready line
-      const bool ok = poll_unit(P, n * (int)Lc, e, [&](int idx) {
-        const int r = idx / (int)Lc, j = idx % (int)Lc;
-        const int nl = min((int)Lc, seg_lines_of(P, r) - (int)t0);
-        const int jj = j < nl ? j : 0;
-        return (const char*)image_bytes(P, P.AG, e, nl > 0 ? r : 0) +
-               ((uint64_t)(nl > 0 ? t0 : 0) + jj) * kLL128LineBytes;
-      });
-      fence_acq_rel_gpu();
-      if (threadIdx.x == 0) s_ok = 1;
-      __syncthreads();
-      if (!ok) s_ok = 0;
-      __syncthreads();
-      if (!s_ok) break;
-      const int nrows = rows_before[n];
-      const int nj = warp < nrows ? (nrows - warp + kCWarps - 1) / kCWarps : 0;
-      auto locate = [&](int gr, int& r, int& rr) {
-        r = 0;
-        while (r + 1 < n && gr >= rows_before[r + 1]) ++r;
-        rr = gr - rows_before[r];
-      };
-      auto issue = [&](int j) {
-        if (j < nj) {
-          int r, rr;
-          locate(warp + j * kCWarps, r, rr);
-          const int nl = min((int)Lc, seg_lines_of(P, r) - (int)t0);
-          const int nl_row = min((int)kLL128RowLines, nl - rr * kLL128RowLines);
-          const char* src = image_bytes(P, P.AG, e, r) +
-                            ((uint64_t)t0 + (uint64_t)rr * kLL128RowLines) * kLL128LineBytes;
-          cp_async16(wbase + (j % kCRing) * kRowBytes + 16 * lane, src + 16 * lane,
-                     li < nl_row);
-        }
-        cp_async_commit();
-      };
-#pragma unroll 1
-      for (int j = 0; j < kCRing; ++j) issue(j);
-      for (int j = 0; j < nj; ++j) {
-        cp_async_wait<kCRing - 1>();
-        __syncwarp();
-        const uint32_t row = wbase + (j % kCRing) * kRowBytes;
-        const uint2 a = lds_v2(row + g0off), b = lds_v2(row + g1off);
-        __syncwarp();
-        issue(j + kCRing);
-        int r, rr;
-        locate(warp + j * kCWarps, r, rr);
-        const int64_t left = (int64_t)P.seg_elems[r] - (int64_t)(t0 + rr * kLL128RowLines) * kLL128Elems;
-        if (lane < 30 && 8 * lane < left)
-          st_v4(P.out[d] + P.seg_in0[r] + (uint64_t)(t0 + rr * kLL128RowLines) * kLL128Elems +
-                    8 * lane,
-                make_uint4(a.x, a.y, b.x, b.y));
-      }
-      cp_async_wait<0>();
-      __syncthreads();
-      if (threadIdx.x == 0) atomicAdd(&h->gather_done[slot], 1u);
     }
+    __syncthreads();  // the next task index, s_ok and s_piece are final
+    if (!s_ok) break;
   }
   finish_run(P, e);
 }

@@ -545,7 +545,15 @@ int derive(const DeriveInput& in, Plan& p) {
   p.off_items2 = off;
   off = round_up(off + p.items2.size() * sizeof(Item), 256);
   p.off_counters = off;
-  off = round_up(off + (uint64_t)std::max<uint32_t>(p.ncounters, 1) * 4, 4096);
+  off = round_up(off + (uint64_t)std::max<uint32_t>(p.ncounters, 1) * 4, 256);
+  if (p.path == COLL_PATH_COMPOSED) {
+    uint64_t most = 0;
+    for (const Seg& sg : p.pseg[0]) most = std::max<uint64_t>(most, sg.lines);
+    p.composed_max_chunks = std::max<uint64_t>(1, (most + kComposedMinChunk - 1) / kComposedMinChunk);
+    p.off_cflags = off;
+    off += p.composed_max_chunks * ((uint64_t)n * 16 + 8);
+  }
+  off = round_up(off, 4096);
   const uint64_t lb = (uint64_t)line_bytes(p.enc);
   p.P.rank_bytes = round_up(p.p_rank_lines * lb, 4096);
   p.P.slot_bytes = p.P.rank_bytes * (uint64_t)n;

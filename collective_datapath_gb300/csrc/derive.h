@@ -69,9 +69,14 @@ struct Plan {
            off_out_off = 0, off_rows_dest = 0, off_counts_out = 0;
   // workspace layout (byte offsets from the workspace base)
   uint64_t off_sitems, off_items1, off_items2, off_counters;
+  // composed twoshot: completion flags for chunks of at least
+  // kComposedMinChunk lines (stage, fold: [chunks][N] u64; gather: [chunks] u64)
+  uint64_t off_cflags = 0, composed_max_chunks = 0;
   Region P, AG;
   uint64_t ws_bytes;
 };
+
+constexpr uint32_t kComposedMinChunk = 16;
 
 // Returns a coll_status_t value (0 = ok).
 int derive(const DeriveInput& in, Plan& plan);

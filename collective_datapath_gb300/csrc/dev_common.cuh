@@ -206,8 +206,7 @@ __device__ __forceinline__ void finish_run(const RunParams& P, uint64_t epoch) {
   st_relaxed_u32(&h->arrived, 0u);
   // the next run's counters
   st_relaxed_u32(&h->started[(epoch + 1) & 1], 0u);
-  st_relaxed_u32(&h->fold_done[(epoch + 1) & 1], 0u);
-  st_relaxed_u32(&h->gather_done[(epoch + 1) & 1], 0u);
+  st_relaxed_u32(&h->task_next[(epoch + 1) & 1], 0u);
   st_relaxed_u64(&h->epoch, epoch + 1);
 }
 

@@ -74,9 +74,9 @@ struct WsHeader {
   uint32_t arrived;        // warps of the run's final launch that read the epoch
   uint32_t started[2];     // fused runs: worker CTAs that started, by slot
   uint64_t rejections;     // stale lines observed (diagnostic)
-  // composed twoshot: completed units per role, by slot (flow control only)
-  uint32_t fold_done[2];
-  uint32_t gather_done[2];
+  // composed twoshot: next task of the run's queue, by slot
+  uint32_t task_next[2];
+  uint32_t pad0[2];
   uint64_t pad1[24];
 };
 static_assert(sizeof(WsHeader) == 256, "WsHeader layout");
@@ -105,13 +105,16 @@ struct MoeParams {
 };
 
 // Composed twoshot all-reduce (one persistent launch, Purlin Algorithm 1):
-// CTA roles and the chunking of every partition.
+// the chunking of every partition, the task queue's lag and the per-task
+// completion flags (epoch values, in the workspace).
 struct ComposedParams {
   uint32_t chunk_lines;  // lines of one partition per chunk (multiple of 4)
   uint32_t nchunks;
-  int n_stage, n_fold;   // CTAs of the stage and fold groups; the rest gather
-  int window;            // a role may run this many chunks ahead of the next one
-  int discard;           // drop consumed staging lines from L2 (no write-back)
+  int lag;               // queue steps between a chunk's stage, fold and gather
+  int discard;           // drop consumed lines from L2 (no write-back)
+  uint64_t* flag_stage;  // [nchunks][N]: epoch once rank p staged chunk c
+  uint64_t* flag_fold;   // [nchunks][N]: epoch once owner r published chunk c
+  uint64_t* gather_cnt;  // [nchunks]: (epoch << 8) | gathers of chunk c done
 };
 
 // Everything a kernel launch needs; passed by value (captured by graphs).

@@ -233,12 +233,12 @@ def test_graph_replay_advances_epoch_on_device(cd, enc):
 
 @pytest.mark.parametrize("n,count", [(8, 8 * 1000), (8, 8 * 60 * 1024 + 64), (3, 3000),
                                      (2, 2 * 4096), (8, 8 * 60 * 300)])
-@pytest.mark.parametrize("shape", [None, "8,30,30,2,1", "64,40,25,1,0", "4,20,20,3,1"])
+@pytest.mark.parametrize("shape", [None, "16,1,1", "64,3,0", "32,40,1", "256,8,1"])
 def test_composed_twoshot_matches_the_oracle(cd, n, count, shape, monkeypatch):
-    """The one-launch twoshot (stage / fold / gather CTA groups pipelined by
+    """The one-launch twoshot (a queue of stage / fold / gather tasks per
     chunk): bit-exact against the oracle over several epochs, for several
-    chunk sizes, group splits and windows, with and without dropping the
-    folded staging lines from L2."""
+    chunk sizes and queue lags, with and without dropping consumed lines
+    from L2."""
     if shape is not None:
         monkeypatch.setenv("COLL_COMPOSED_SHAPE", shape)
     coll = make(cd, cd.ALLREDUCE, n, count, encoding=cd.COLL_LL128,
