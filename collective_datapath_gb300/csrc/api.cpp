@@ -137,18 +137,19 @@ cudaError_t launched(coll_spec* s, cudaError_t e, cudaStream_t st) {
   return cudaSuccess;
 }
 
-// Shape of the composed twoshot launch: chunks of 128 lines of every
-// partition, a lag of 64 queue steps between a chunk's stage, fold and
-// gather tasks, consumed lines dropped from L2.  COLL_COMPOSED_SHAPE =
-// "chunk_lines,lag,discard" overrides it (benchmark sweeps); chunks are a
+// Shape of the composed twoshot launch: chunks of 256 lines of every
+// partition, a lag of 28 queue steps between a chunk's stage, fold and
+// gather tasks, consumed lines dropped from L2, launch variant 0.
+// COLL_COMPOSED_SHAPE = "chunk_lines,lag,discard,variant" overrides it
+// (benchmark sweeps); chunks are a
 // power of two of at least kComposedMinChunk lines, the size the completion
 // flags were laid out for.
 ComposedParams composed_shape(const coll_spec* s) {
   const Plan& p = s->plan;
   ComposedParams q{};
-  int chunk = 128, lag = 64, discard = 1;
+  int chunk = 256, lag = 28, discard = 1, variant = 0;
   if (const char* env = std::getenv("COLL_COMPOSED_SHAPE"))
-    std::sscanf(env, "%d,%d,%d", &chunk, &lag, &discard);
+    std::sscanf(env, "%d,%d,%d,%d", &chunk, &lag, &discard, &variant);
   // a power of two of at least kComposedMinChunk lines (rows per chunk are
   // counted with shifts)
   int c2 = (int)kComposedMinChunk;
@@ -160,6 +161,7 @@ ComposedParams composed_shape(const coll_spec* s) {
   q.nchunks = (uint32_t)std::max<uint64_t>(1, (max_lines + chunk - 1) / chunk);
   q.lag = std::max(1, lag);
   q.discard = discard;
+  q.variant = variant == 1 ? 1 : 0;
   char* f = s->ws + p.off_cflags;
   q.flag_stage = reinterpret_cast<uint64_t*>(f);
   q.flag_fold = q.flag_stage + p.composed_max_chunks * p.n;
@@ -390,9 +392,9 @@ coll_status_t coll_run(coll_spec_t* s, const void* const* dev_ins, void* const* 
   }
   const bool empty = p.items1.empty() && p.items2.empty();
   if (dev_ins != nullptr && p.path == COLL_PATH_COMPOSED && !empty) {
-    const int cap = composed_capacity();
-    if (cap < 3) return COLL_ERR_CUDA;
     P.cp = composed_shape(s);
+    const int cap = composed_capacity(P.cp.variant);
+    if (cap < 3) return COLL_ERR_CUDA;
     P.advance_epoch = 1;
     return cuda_status(launched(s, launch_composed(P, cap, st), st));
   }

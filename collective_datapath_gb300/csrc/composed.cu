@@ -37,10 +37,16 @@ namespace coll {
 
 constexpr int kCThreads = 256;
 constexpr int kCWarps = kCThreads / 32;
-constexpr int kCRing = 16;                         // rows in flight per warp
-constexpr int kCFoldStages = kCRing / kMaxRanks;   // rows of all N images per warp
+// Two launch shapes: RING rows in flight per warp (stage, gather; the fold
+// keeps RING / 8 rows of all N images), MINB CTAs per SM.
+//   variant 0: 16 rows, 3 CTAs per SM (64 KB of shared memory each)
+//   variant 1: 24 rows, 2 CTAs per SM (96 KB each)
+constexpr int kCRing0 = 16, kCMinBlocks0 = 3;
+constexpr int kCRing1 = 24, kCMinBlocks1 = 2;
 
-size_t composed_smem_bytes() { return (size_t)kCWarps * kCRing * kRowBytes; }
+size_t composed_smem_bytes(int variant) {
+  return (size_t)kCWarps * (variant == 1 ? kCRing1 : kCRing0) * kRowBytes;
+}
 
 __device__ __forceinline__ void discard_l2_line(const void* p) {
   asm volatile("discard.global.L2 [%0], 128;" ::"l"(p) : "memory");
@@ -123,6 +129,7 @@ __device__ __forceinline__ void fill_gather_piece(const RunParams& P, Piece* pc,
                                                                   : (int64_t)P.cp.chunk_lines * kLL128Elems);
 }
 
+template <int kCRing>
 __device__ __forceinline__ void stage_task(const Piece* pc, uint32_t wbase, int lane, int warp,
                                            int n, int rsh, uint64_t e) {
   const int li = lane >> 3, kk = lane & 7;
@@ -130,13 +137,15 @@ __device__ __forceinline__ void stage_task(const Piece* pc, uint32_t wbase, int 
   const int rmask = (1 << rsh) - 1;
   const int nrows = n << rsh;
   const int nj = warp < nrows ? (nrows - warp + kCWarps - 1) / kCWarps : 0;
+  const uint64_t pol = l2_evict_first_policy();  // inputs are read once
   auto issue = [&](int j) {
     if (j < nj) {
       const int i = warp + j * kCWarps, k = i >> rsh, r = i & rmask;
       const int left = pc[k].left - r * kRowElems;
       const bool valid = 4 * r < pc[k].nl && lane < 30 && 8 * lane < left;
-      cp_async16(wbase + (j % kCRing) * kRowBytes + 16 * lane,
-                 pc[k].src + (size_t)r * (2 * kRowElems) + (valid ? 16 * lane : 0), valid);
+      cp_async16_hint(wbase + (j % kCRing) * kRowBytes + 16 * lane,
+                      pc[k].src + (size_t)r * (2 * kRowElems) + (valid ? 16 * lane : 0), valid,
+                      pol);
     }
     cp_async_commit();
   };
@@ -161,8 +170,10 @@ __device__ __forceinline__ void stage_task(const Piece* pc, uint32_t wbase, int 
   __syncwarp();
 }
 
+template <int kCRing>
 __device__ __forceinline__ bool fold_task(const RunParams& P, uint32_t wbase, int lane, int warp,
                                           int c, int r, uint64_t e) {
+  constexpr int kCFoldStages = kCRing / kMaxRanks;  // rows of all N images per warp
   const int n = P.nranks;
   const uint32_t t0 = (uint32_t)c * P.cp.chunk_lines;
   const int nl = chunk_lines_of(P, r, t0);
@@ -234,6 +245,7 @@ __device__ __forceinline__ bool fold_task(const RunParams& P, uint32_t wbase, in
   return ok;
 }
 
+template <int kCRing>
 __device__ __forceinline__ bool gather_task(const RunParams& P, const Piece* pc, uint32_t wbase,
                                             int lane, int warp, int rsh, uint64_t e) {
   const int n = P.nranks;
@@ -245,6 +257,7 @@ __device__ __forceinline__ bool gather_task(const RunParams& P, const Piece* pc,
   const int rmask = (1 << rsh) - 1;
   const int nrows = n << rsh;
   const int nj = warp < nrows ? (nrows - warp + kCWarps - 1) / kCWarps : 0;
+  const uint64_t pol = l2_evict_first_policy();  // outputs are written once
   auto issue = [&](int j) {
     if (j < nj) {
       const int i = warp + j * kCWarps, r = i >> rsh, rr = i & rmask;
@@ -276,7 +289,8 @@ __device__ __forceinline__ bool gather_task(const RunParams& P, const Piece* pc,
     issue(j + kCRing);
     const int left = pc[r].left - rr * kRowElems;
     if (nl_row > 0 && lane < 30 && 8 * lane < left)
-      st_v4(pc[r].dst + (size_t)rr * (2 * kRowElems) + 16 * lane, make_uint4(a.x, a.y, b.x, b.y));
+      st_v4_hint(pc[r].dst + (size_t)rr * (2 * kRowElems) + 16 * lane,
+                 make_uint4(a.x, a.y, b.x, b.y), pol);
   }
   cp_async_wait<0>();
   __syncwarp();
@@ -297,11 +311,12 @@ __device__ __forceinline__ bool last_gather(const RunParams& P, int c, uint64_t 
   return (int)(want & 0xFFull) == P.nranks;
 }
 
-__global__ void __launch_bounds__(kCThreads, 3) k_composed_ll128(RunParams P) {
+template <int kCRing, int kMinBlocks>
+__global__ void __launch_bounds__(kCThreads, kMinBlocks) k_composed_ll128(RunParams P) {
   extern __shared__ __align__(128) char smem[];
   __shared__ Piece s_piece[kMaxRanks];
   __shared__ int s_task[2];
-  __shared__ int s_ok, s_last;
+  __shared__ int s_ok;
   const uint64_t e = begin_run(P);
   const ComposedParams& Q = P.cp;
   WsHeader* h = header(P.ws);
@@ -318,6 +333,9 @@ __global__ void __launch_bounds__(kCThreads, 3) k_composed_ll128(RunParams P) {
     s_ok = 1;
   }
   __syncthreads();
+  // Barriers per task: two.  The first publishes the task's descriptors or
+  // its acquired flags; the second ends the task's reads and writes (and
+  // publishes the next task index and s_ok, written before it).
   for (int it = 0;; ++it) {
     const int t = s_task[it & 1];
     if (t >= ntasks) break;
@@ -327,71 +345,79 @@ __global__ void __launch_bounds__(kCThreads, 3) k_composed_ll128(RunParams P) {
     const int step = t / per_step, rem = t % per_step;
     const int kind = rem / n, x = rem % n;
     const int c = step - kind * Q.lag;
-    if (c >= 0 && c < (int)Q.nchunks) {
-      if (kind == 0) {
-        if ((int)threadIdx.x < n) fill_stage_piece(P, s_piece, c, x, e);
-        __syncthreads();
-        stage_task(s_piece, wbase, lane, warp, n, rsh, e);
-        release_flag(Q.flag_stage + (size_t)c * n + x, e, s_ok);
-      } else if (kind == 1) {
-        if (!acquire_flags(P, Q.flag_stage + (size_t)c * n, n, e)) s_ok = 0;
-        __syncthreads();
-        if (s_ok) {
-          if (!fold_task(P, wbase, lane, warp, c, x, e)) s_ok = 0;
-          release_flag(Q.flag_fold + (size_t)c * n + x, e, s_ok);
-        }
-      } else {
-        if ((int)threadIdx.x < n) fill_gather_piece(P, s_piece, c, x, e);
-        if (!acquire_flags(P, Q.flag_fold + (size_t)c * n, n, e)) s_ok = 0;
-        __syncthreads();
-        if (s_ok) {
-          if (!gather_task(P, s_piece, wbase, lane, warp, rsh, e)) s_ok = 0;
-          __syncthreads();
-          if (threadIdx.x == 0) s_last = s_ok && Q.discard && last_gather(P, c, e);
-          __syncthreads();
-          if (s_last) {
-            for (int r = 0; r < n; ++r) {
-              const int nl = s_piece[r].nl;
-              for (int j = threadIdx.x; j < nl; j += blockDim.x)
-                discard_l2_line(s_piece[r].src + (size_t)j * kLL128LineBytes);
-            }
+    if (c < 0 || c >= (int)Q.nchunks) {
+      __syncthreads();
+      continue;
+    }
+    if (kind == 0) {
+      if ((int)threadIdx.x < n) fill_stage_piece(P, s_piece, c, x, e);
+      __syncthreads();
+      stage_task<kCRing>(s_piece, wbase, lane, warp, n, rsh, e);
+      release_flag(Q.flag_stage + (size_t)c * n + x, e, s_ok);
+    } else if (kind == 1) {
+      if (!acquire_flags(P, Q.flag_stage + (size_t)c * n, n, e)) s_ok = 0;
+      __syncthreads();
+      if (!s_ok) break;
+      if (!fold_task<kCRing>(P, wbase, lane, warp, c, x, e)) s_ok = 0;
+      release_flag(Q.flag_fold + (size_t)c * n + x, e, s_ok);
+    } else {
+      if ((int)threadIdx.x < n) fill_gather_piece(P, s_piece, c, x, e);
+      if (!acquire_flags(P, Q.flag_fold + (size_t)c * n, n, e)) s_ok = 0;
+      __syncthreads();
+      if (!s_ok) break;
+      if (!gather_task<kCRing>(P, s_piece, wbase, lane, warp, rsh, e)) s_ok = 0;
+      __syncthreads();
+      if (warp == 0 && s_ok && Q.discard == 1) {
+        // warp 0 alone: it also fills the next task's descriptors, so it
+        // is done with these before anyone reads the next ones
+        const bool last = __shfl_sync(0xFFFFFFFFu, lane == 0 ? (int)last_gather(P, c, e) : 0, 0);
+        if (last)
+          for (int r = 0; r < n; ++r) {
+            const int nl = s_piece[r].nl;
+            for (int j = lane; j < nl; j += 32)
+              discard_l2_line(s_piece[r].src + (size_t)j * kLL128LineBytes);
           }
-        }
       }
     }
-    __syncthreads();  // the next task index, s_ok and s_piece are final
     if (!s_ok) break;
   }
   finish_run(P, e);
 }
 
-int composed_capacity() {
-  int per_sm = 0;
+template <int R, int B>
+static int capacity_of() {
   static bool configured = false;
+  const int bytes = (int)((size_t)kCWarps * R * kRowBytes);
   if (!configured) {
-    if (cudaFuncSetAttribute(k_composed_ll128, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)composed_smem_bytes()) != cudaSuccess)
+    if (cudaFuncSetAttribute(k_composed_ll128<R, B>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             bytes) != cudaSuccess)
       return 0;
     configured = true;
   }
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_composed_ll128, kCThreads,
-                                                    composed_smem_bytes()) != cudaSuccess)
+  int per_sm = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_composed_ll128<R, B>, kCThreads,
+                                                    bytes) != cudaSuccess)
     return 0;
   return per_sm * device_sms();
+}
+
+int composed_capacity(int variant) {
+  return variant == 1 ? capacity_of<kCRing1, kCMinBlocks1>() : capacity_of<kCRing0, kCMinBlocks0>();
 }
 
 cudaError_t launch_composed(const RunParams& P, int grid, cudaStream_t s) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(kCThreads);
-  cfg.dynamicSmemBytes = composed_smem_bytes();
+  cfg.dynamicSmemBytes = composed_smem_bytes(P.cp.variant);
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeCooperative;
   attr[0].val.cooperative = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, k_composed_ll128, P);
+  if (P.cp.variant == 1) return cudaLaunchKernelEx(&cfg, k_composed_ll128<kCRing1, kCMinBlocks1>, P);
+  return cudaLaunchKernelEx(&cfg, k_composed_ll128<kCRing0, kCMinBlocks0>, P);
 }
 
 }  // namespace coll

@@ -12,6 +12,24 @@ __device__ __forceinline__ void cp_async16(uint32_t saddr, const void* g, bool v
                "r"(valid ? 16 : 0)
                : "memory");
 }
+// L2 eviction policies (createpolicy): data streamed once is marked
+// evict-first so that it does not push out lines another CTA still needs.
+__device__ __forceinline__ uint64_t l2_evict_first_policy() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+__device__ __forceinline__ void cp_async16_hint(uint32_t saddr, const void* g, bool valid,
+                                                uint64_t pol) {
+  asm volatile("cp.async.cg.shared.global.L2::cache_hint [%0], [%1], 16, %2, %3;" ::"r"(saddr),
+               "l"(g), "r"(valid ? 16 : 0), "l"(pol)
+               : "memory");
+}
+__device__ __forceinline__ void st_v4_hint(void* p, uint4 v, uint64_t pol) {
+  asm volatile("st.global.L2::cache_hint.v4.u32 [%0], {%1, %2, %3, %4}, %5;" ::"l"(p),
+               "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w), "l"(pol)
+               : "memory");
+}
 __device__ __forceinline__ void cp_async_commit() {
   asm volatile("cp.async.commit_group;" ::: "memory");
 }

@@ -111,7 +111,9 @@ struct ComposedParams {
   uint32_t chunk_lines;  // lines of one partition per chunk (multiple of 4)
   uint32_t nchunks;
   int lag;               // queue steps between a chunk's stage, fold and gather
-  int discard;           // drop consumed lines from L2 (no write-back)
+  int discard;           // drop consumed lines from L2 (no write-back):
+                         // 1 = staged and published lines, 2 = staged only
+  int variant;           // launch shape (ring depth and CTAs per SM)
   uint64_t* flag_stage;  // [nchunks][N]: epoch once rank p staged chunk c
   uint64_t* flag_fold;   // [nchunks][N]: epoch once owner r published chunk c
   uint64_t* gather_cnt;  // [nchunks]: (epoch << 8) | gathers of chunk c done
