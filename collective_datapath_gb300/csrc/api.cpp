@@ -161,7 +161,7 @@ ComposedParams composed_shape(const coll_spec* s) {
   q.nchunks = (uint32_t)std::max<uint64_t>(1, (max_lines + chunk - 1) / chunk);
   q.lag = std::max(1, lag);
   q.discard = discard;
-  q.variant = variant == 1 ? 1 : 0;
+  q.variant = variant >= 0 && variant <= 2 ? variant : 0;
   char* f = s->ws + p.off_cflags;
   q.flag_stage = reinterpret_cast<uint64_t*>(f);
   q.flag_fold = q.flag_stage + p.composed_max_chunks * p.n;

@@ -35,17 +35,20 @@
 
 namespace coll {
 
-constexpr int kCThreads = 256;
-constexpr int kCWarps = kCThreads / 32;
-// Two launch shapes: RING rows in flight per warp (stage, gather; the fold
-// keeps RING / 8 rows of all N images), MINB CTAs per SM.
-//   variant 0: 16 rows, 3 CTAs per SM (64 KB of shared memory each)
-//   variant 1: 24 rows, 2 CTAs per SM (96 KB each)
-constexpr int kCRing0 = 16, kCMinBlocks0 = 3;
-constexpr int kCRing1 = 24, kCMinBlocks1 = 2;
+// Launch shapes: kW warps per CTA, kCRing rows in flight per warp (stage,
+// gather; the fold keeps kCRing / 8 rows of all N images), kMinBlocks CTAs
+// per SM.
+//   variant 0: 8 warps, 16 rows, 3 CTAs per SM (64 KB of shared memory each)
+//   variant 1: 8 warps, 24 rows, 2 CTAs per SM (96 KB each)
+//   variant 2: 4 warps, 16 rows, 6 CTAs per SM (32 KB each)
+struct CVariant {
+  int warps, ring;
+};
+constexpr CVariant kCVariants[3] = {{8, 16}, {8, 24}, {4, 16}};
 
 size_t composed_smem_bytes(int variant) {
-  return (size_t)kCWarps * (variant == 1 ? kCRing1 : kCRing0) * kRowBytes;
+  const CVariant v = kCVariants[variant];
+  return (size_t)v.warps * v.ring * kRowBytes;
 }
 
 __device__ __forceinline__ void discard_l2_line(const void* p) {
@@ -129,7 +132,7 @@ __device__ __forceinline__ void fill_gather_piece(const RunParams& P, Piece* pc,
                                                                   : (int64_t)P.cp.chunk_lines * kLL128Elems);
 }
 
-template <int kCRing>
+template <int kCWarps, int kCRing>
 __device__ __forceinline__ void stage_task(const Piece* pc, uint32_t wbase, int lane, int warp,
                                            int n, int rsh, uint64_t e) {
   const int li = lane >> 3, kk = lane & 7;
@@ -170,7 +173,7 @@ __device__ __forceinline__ void stage_task(const Piece* pc, uint32_t wbase, int 
   __syncwarp();
 }
 
-template <int kCRing>
+template <int kCWarps, int kCRing>
 __device__ __forceinline__ bool fold_task(const RunParams& P, uint32_t wbase, int lane, int warp,
                                           int c, int r, uint64_t e) {
   constexpr int kCFoldStages = kCRing / kMaxRanks;  // rows of all N images per warp
@@ -245,7 +248,7 @@ __device__ __forceinline__ bool fold_task(const RunParams& P, uint32_t wbase, in
   return ok;
 }
 
-template <int kCRing>
+template <int kCWarps, int kCRing>
 __device__ __forceinline__ bool gather_task(const RunParams& P, const Piece* pc, uint32_t wbase,
                                             int lane, int warp, int rsh, uint64_t e) {
   const int n = P.nranks;
@@ -311,8 +314,8 @@ __device__ __forceinline__ bool last_gather(const RunParams& P, int c, uint64_t 
   return (int)(want & 0xFFull) == P.nranks;
 }
 
-template <int kCRing, int kMinBlocks>
-__global__ void __launch_bounds__(kCThreads, kMinBlocks) k_composed_ll128(RunParams P) {
+template <int kCWarps, int kCRing, int kMinBlocks>
+__global__ void __launch_bounds__(kCWarps * 32, kMinBlocks) k_composed_ll128(RunParams P) {
   extern __shared__ __align__(128) char smem[];
   __shared__ Piece s_piece[kMaxRanks];
   __shared__ int s_task[2];
@@ -352,20 +355,20 @@ __global__ void __launch_bounds__(kCThreads, kMinBlocks) k_composed_ll128(RunPar
     if (kind == 0) {
       if ((int)threadIdx.x < n) fill_stage_piece(P, s_piece, c, x, e);
       __syncthreads();
-      stage_task<kCRing>(s_piece, wbase, lane, warp, n, rsh, e);
+      stage_task<kCWarps, kCRing>(s_piece, wbase, lane, warp, n, rsh, e);
       release_flag(Q.flag_stage + (size_t)c * n + x, e, s_ok);
     } else if (kind == 1) {
       if (!acquire_flags(P, Q.flag_stage + (size_t)c * n, n, e)) s_ok = 0;
       __syncthreads();
       if (!s_ok) break;
-      if (!fold_task<kCRing>(P, wbase, lane, warp, c, x, e)) s_ok = 0;
+      if (!fold_task<kCWarps, kCRing>(P, wbase, lane, warp, c, x, e)) s_ok = 0;
       release_flag(Q.flag_fold + (size_t)c * n + x, e, s_ok);
     } else {
       if ((int)threadIdx.x < n) fill_gather_piece(P, s_piece, c, x, e);
       if (!acquire_flags(P, Q.flag_fold + (size_t)c * n, n, e)) s_ok = 0;
       __syncthreads();
       if (!s_ok) break;
-      if (!gather_task<kCRing>(P, s_piece, wbase, lane, warp, rsh, e)) s_ok = 0;
+      if (!gather_task<kCWarps, kCRing>(P, s_piece, wbase, lane, warp, rsh, e)) s_ok = 0;
       __syncthreads();
       if (warp == 0 && s_ok && Q.discard == 1) {
         // warp 0 alone: it also fills the next task's descriptors, so it
@@ -384,40 +387,44 @@ __global__ void __launch_bounds__(kCThreads, kMinBlocks) k_composed_ll128(RunPar
   finish_run(P, e);
 }
 
-template <int R, int B>
+template <int W, int R, int B>
 static int capacity_of() {
   static bool configured = false;
-  const int bytes = (int)((size_t)kCWarps * R * kRowBytes);
+  const int bytes = (int)((size_t)W * R * kRowBytes);
   if (!configured) {
-    if (cudaFuncSetAttribute(k_composed_ll128<R, B>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             bytes) != cudaSuccess)
+    if (cudaFuncSetAttribute(k_composed_ll128<W, R, B>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) != cudaSuccess)
       return 0;
     configured = true;
   }
   int per_sm = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_composed_ll128<R, B>, kCThreads,
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_composed_ll128<W, R, B>, W * 32,
                                                     bytes) != cudaSuccess)
     return 0;
   return per_sm * device_sms();
 }
 
 int composed_capacity(int variant) {
-  return variant == 1 ? capacity_of<kCRing1, kCMinBlocks1>() : capacity_of<kCRing0, kCMinBlocks0>();
+  if (variant == 1) return capacity_of<8, 24, 2>();
+  if (variant == 2) return capacity_of<4, 16, 6>();
+  return capacity_of<8, 16, 3>();
 }
 
 cudaError_t launch_composed(const RunParams& P, int grid, cudaStream_t s) {
+  const int v = P.cp.variant;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
-  cfg.blockDim = dim3(kCThreads);
-  cfg.dynamicSmemBytes = composed_smem_bytes(P.cp.variant);
+  cfg.blockDim = dim3(kCVariants[v].warps * 32);
+  cfg.dynamicSmemBytes = composed_smem_bytes(v);
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeCooperative;
   attr[0].val.cooperative = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  if (P.cp.variant == 1) return cudaLaunchKernelEx(&cfg, k_composed_ll128<kCRing1, kCMinBlocks1>, P);
-  return cudaLaunchKernelEx(&cfg, k_composed_ll128<kCRing0, kCMinBlocks0>, P);
+  if (v == 1) return cudaLaunchKernelEx(&cfg, k_composed_ll128<8, 24, 2>, P);
+  if (v == 2) return cudaLaunchKernelEx(&cfg, k_composed_ll128<4, 16, 6>, P);
+  return cudaLaunchKernelEx(&cfg, k_composed_ll128<8, 16, 3>, P);
 }
 
 }  // namespace coll

@@ -233,7 +233,7 @@ def test_graph_replay_advances_epoch_on_device(cd, enc):
 
 @pytest.mark.parametrize("n,count", [(8, 8 * 1000), (8, 8 * 60 * 1024 + 64), (3, 3000),
                                      (2, 2 * 4096), (8, 8 * 60 * 300)])
-@pytest.mark.parametrize("shape", [None, "16,1,1", "64,3,0", "32,40,1", "256,8,1", "64,4,1,1", "16,2,0,1"])
+@pytest.mark.parametrize("shape", [None, "16,1,1", "64,3,0", "32,40,1", "256,8,1", "64,4,1,1", "16,2,0,1", "32,4,1,2", "128,6,2,2"])
 def test_composed_twoshot_matches_the_oracle(cd, n, count, shape, monkeypatch):
     """The one-launch twoshot (a queue of stage / fold / gather tasks per
     chunk): bit-exact against the oracle over several epochs, for several
