@@ -138,18 +138,19 @@ cudaError_t launched(coll_spec* s, cudaError_t e, cudaStream_t st) {
 }
 
 // Shape of the composed twoshot launch: chunks of 256 lines of every
-// partition, a lag of 28 queue steps between a chunk's stage, fold and
-// gather tasks, consumed lines dropped from L2, launch variant 0.
-// COLL_COMPOSED_SHAPE = "chunk_lines,lag,discard,variant" overrides it
+// partition, a lag of 28 queue steps from a chunk's stage to its fold and
+// from its fold to its gather, consumed lines dropped from L2, launch
+// variant 0.  COLL_COMPOSED_SHAPE = "chunk_lines,lag,discard,variant,lag2"
+// overrides it
 // (benchmark sweeps); chunks are a
 // power of two of at least kComposedMinChunk lines, the size the completion
 // flags were laid out for.
 ComposedParams composed_shape(const coll_spec* s) {
   const Plan& p = s->plan;
   ComposedParams q{};
-  int chunk = 256, lag = 28, discard = 1, variant = 0;
+  int chunk = 256, lag = 28, discard = 1, variant = 0, lag2 = -1;
   if (const char* env = std::getenv("COLL_COMPOSED_SHAPE"))
-    std::sscanf(env, "%d,%d,%d,%d", &chunk, &lag, &discard, &variant);
+    std::sscanf(env, "%d,%d,%d,%d,%d", &chunk, &lag, &discard, &variant, &lag2);
   // a power of two of at least kComposedMinChunk lines (rows per chunk are
   // counted with shifts)
   int c2 = (int)kComposedMinChunk;
@@ -160,6 +161,7 @@ ComposedParams composed_shape(const coll_spec* s) {
   q.chunk_lines = (uint32_t)chunk;
   q.nchunks = (uint32_t)std::max<uint64_t>(1, (max_lines + chunk - 1) / chunk);
   q.lag = std::max(1, lag);
+  q.lag2 = lag2 < 1 ? q.lag : lag2;
   q.discard = discard;
   q.variant = variant >= 0 && variant <= 2 ? variant : 0;
   char* f = s->ws + p.off_cflags;

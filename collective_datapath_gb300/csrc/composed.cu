@@ -11,7 +11,7 @@
 //                   folded in rank order, published as lines of owner r;
 //   gather G(c, d): chunk c of every owner's published partition -> rank d's
 //                   output.
-// Queue step t holds S(t, *), then F(t - lag, *), then G(t - 2 lag, *).  CTAs
+// Queue step t holds S(t, *), then F(t - lag, *), then G(t - lag - lag2, *).  CTAs
 // take tasks in queue order from one counter, so a task only ever waits for
 // tasks that are earlier in the queue and already taken by co-resident CTAs:
 // the earliest unfinished task waits for nothing, so the launch always
@@ -327,7 +327,7 @@ __global__ void __launch_bounds__(kCWarps * 32, kMinBlocks) k_composed_ll128(Run
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int slot = (int)(e & 1);
   const int per_step = 3 * n;
-  const int ntasks = ((int)Q.nchunks + 2 * Q.lag) * per_step;
+  const int ntasks = ((int)Q.nchunks + Q.lag + Q.lag2) * per_step;
   const int rsh = __ffs((int)Q.chunk_lines / kLL128RowLines) - 1;  // rows per chunk = 2^rsh
   const uint32_t wbase =
       (uint32_t)__cvta_generic_to_shared(smem) + (uint32_t)(warp * kCRing * kRowBytes);
@@ -347,7 +347,7 @@ __global__ void __launch_bounds__(kCWarps * 32, kMinBlocks) k_composed_ll128(Run
       s_task[(it + 1) & 1] = aborted(P.ws) ? ntasks : (int)atomicAdd(&h->task_next[slot], 1u);
     const int step = t / per_step, rem = t % per_step;
     const int kind = rem / n, x = rem % n;
-    const int c = step - kind * Q.lag;
+    const int c = step - (kind == 0 ? 0 : (kind == 1 ? Q.lag : Q.lag + Q.lag2));
     if (c < 0 || c >= (int)Q.nchunks) {
       __syncthreads();
       continue;

@@ -110,7 +110,8 @@ struct MoeParams {
 struct ComposedParams {
   uint32_t chunk_lines;  // lines of one partition per chunk (multiple of 4)
   uint32_t nchunks;
-  int lag;               // queue steps between a chunk's stage, fold and gather
+  int lag;               // queue steps between a chunk's stage and its fold
+  int lag2;              // queue steps between a chunk's fold and its gather
   int discard;           // drop consumed lines from L2 (no write-back):
                          // 1 = staged and published lines, 2 = staged only
   int variant;           // launch shape (ring depth and CTAs per SM)
