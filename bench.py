@@ -277,10 +277,13 @@ def latency_sweep(cd, stream, only_T=None, only_variant=None, encoding=None) -> 
         for algo, path, name in ((cd.COLL_ONESHOT, cd.COLL_PATH_FUSED, "oneshot_fused"),
                                  (cd.COLL_ONESHOT, cd.COLL_PATH_STREAMED, "oneshot_streamed"),
                                  (cd.COLL_TWOSHOT, cd.COLL_PATH_FUSED, "twoshot_fused"),
-                                 (cd.COLL_TWOSHOT, cd.COLL_PATH_STREAMED, "twoshot_streamed")):
+                                 (cd.COLL_TWOSHOT, cd.COLL_PATH_STREAMED, "twoshot_streamed"),
+                                 (cd.COLL_ALGO_AUTO, cd.COLL_PATH_AUTO, "policy")):
             if only_variant is not None and name != only_variant:
                 continue
-            coll = cd.Collective(cd.ALLREDUCE, N_RANKS, count, encoding=enc,
+            # "policy": encoding, algorithm and path from the calibrated table
+            coll = cd.Collective(cd.ALLREDUCE, N_RANKS, count,
+                                 encoding=cd.COLL_ENC_AUTO if name == "policy" else enc,
                                  algorithm=algo, path=path)
             ins = make_inputs(count, 7 + T)
             outs = [torch.empty(count, dtype=torch.int16, device="cuda")
@@ -318,6 +321,10 @@ def latency_sweep(cd, stream, only_T=None, only_variant=None, encoding=None) -> 
             st = coll.status(stream)
             row[name] = {"warm_us": round(warm, 3), "cold_us": round(cold, 3),
                          "status": st[0]}
+            if name == "policy":
+                pl = coll.plan()
+                row[name]["choice"] = {"encoding": pl["encoding"], "algorithm": pl["algorithm"],
+                                       "path": pl["path"]}
             coll.close()
             del coll, ins, outs, g
         out[f"T={T}"] = {"bytes_per_rank": count * 2, **row}

@@ -29,7 +29,7 @@ COLL_COPY, COLL_REDUCE = 0, 1
 COLL_BF16 = 0
 COLL_OK, COLL_ERR_INVALID, COLL_ERR_UNSUPPORTED, COLL_ERR_ALIGN = 0, 1, 2, 3
 COLL_ERR_NOMEM, COLL_ERR_CUDA, COLL_ERR_TIMEOUT, COLL_ERR_STATE = 4, 5, 6, 7
-COLL_LL8, COLL_LL128, COLL_SENT = 0, 1, 2
+COLL_LL8, COLL_LL128, COLL_SENT, COLL_ENC_AUTO = 0, 1, 2, 3
 COLL_ALGO_AUTO, COLL_ONESHOT, COLL_TWOSHOT = 0, 1, 2
 COLL_RESET_FUSED, COLL_RESET_KERNEL, COLL_RESET_NONE, COLL_RESET_DEFERRED = 0, 1, 2, 3
 COLL_PATH_AUTO, COLL_PATH_FUSED, COLL_PATH_STREAMED, COLL_PATH_COMPOSED = 0, 1, 2, 3
@@ -53,7 +53,8 @@ class coll_options_t(ctypes.Structure):
                 ("timeout_ns", ctypes.c_uint64), ("tokens", ctypes.c_int),
                 ("hidden", ctypes.c_int), ("topk", ctypes.c_int),
                 ("experts", ctypes.c_int), ("max_rows", ctypes.c_int),
-                ("vcounts", ctypes.POINTER(ctypes.c_uint64)), ("nvcounts", ctypes.c_int)]
+                ("vcounts", ctypes.POINTER(ctypes.c_uint64)), ("nvcounts", ctypes.c_int),
+                ("slots", ctypes.c_int)]
 
 
 _vp = ctypes.c_void_p

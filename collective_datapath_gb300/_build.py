@@ -19,7 +19,7 @@ LIB = os.path.join(HERE, "libcoll.so")
 
 SOURCES = ["kernels.cu", "api.cpp", "derive.cpp", "static_ws.cu", "moe.cu", "composed.cu"]
 HEADERS = ["plan.h", "derive.h", "launch.h", "dev_common.cuh", "ll8.cuh", "ll128.cuh",
-           "pipe.cuh", "sent.cuh"]
+           "pipe.cuh", "sent.cuh", "policy_table.h"]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 # No fast math: IEEE division/sqrt, no flush-to-zero (the fold is bit-exact).

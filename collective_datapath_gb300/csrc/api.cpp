@@ -265,6 +265,7 @@ coll_status_t coll_spec_create(coll_layout_t in_layout, coll_layout_t out_layout
   d.topk = o.topk;
   d.experts = o.experts;
   d.max_rows = o.max_rows;
+  d.slots = o.slots;
   if (o.vcounts != nullptr && o.nvcounts > 0)
     d.vcounts.assign(o.vcounts, o.vcounts + o.nvcounts);
   device_shape(o.encoding, &d.sms, &d.fused_capacity);
@@ -307,7 +308,8 @@ coll_status_t coll_bind(coll_spec_t* s, void* dev_workspace, size_t bytes,
     // flash-comm §4.2: arrival-checked storage starts out holding the pattern
     for (const Region* R : {&p.P, &p.AG})
       if (R->slot_bytes > 0)
-        if (cudaError_t e = cudaMemsetAsync(s->ws + R->base, 0xFF, 2 * R->slot_bytes, st))
+        if (cudaError_t e = cudaMemsetAsync(s->ws + R->base, 0xFF,
+                                            (R->slot_mask + 1) * R->slot_bytes, st))
           return cuda_status(e);
   }
   WsHeader h{};
@@ -497,7 +499,7 @@ coll_status_t coll_get_rejections(coll_spec_t* s, coll_stream_t stream,
 coll_status_t coll_staging_layout(const coll_spec_t* s, int region, int slot, int rank,
                                   int seg, uint64_t* byte_offset, uint64_t* lines,
                                   int* line_bytes_out) {
-  if (s == nullptr || rank < 0 || rank >= s->plan.n || slot < 0 || slot > 1)
+  if (s == nullptr || rank < 0 || rank >= s->plan.n || slot < 0 || slot >= s->plan.slots)
     return COLL_ERR_INVALID;
   const Plan& p = s->plan;
   const std::vector<Seg>* segs;

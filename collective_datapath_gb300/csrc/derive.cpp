@@ -6,6 +6,7 @@
 #include <utility>
 
 #include "../../include/coll.h"
+#include "policy_table.h"
 
 namespace coll {
 
@@ -123,7 +124,7 @@ void group_by_dst(std::vector<Item>& items, int n, int* beg) {
 // the plan fixes the staging geometry and the device tables.
 static int derive_moe(const DeriveInput& in, Plan& p) {
   const int n = in.nranks;
-  if (in.encoding != COLL_LL128) return COLL_ERR_UNSUPPORTED;
+  if (in.encoding != COLL_LL128 && in.encoding != COLL_ENC_AUTO) return COLL_ERR_UNSUPPORTED;
   if (in.tokens < 0 || in.hidden <= 0 || in.topk < 1 || in.topk > 64 || in.experts < n ||
       in.experts % n != 0 || in.experts > 1024 || in.max_rows < 0)
     return COLL_ERR_INVALID;
@@ -172,18 +173,41 @@ static int derive_moe(const DeriveInput& in, Plan& p) {
   p.p_rank_lines = tk * p.moe_row_lines;
   p.P.rank_bytes = round_up(p.p_rank_lines * kLL128LineBytes, 4096);
   p.P.slot_bytes = p.P.rank_bytes * (uint64_t)n;
+  p.P.slot_mask = (uint64_t)p.slots - 1;
   p.P.base = off;
-  off += 2 * p.P.slot_bytes;
+  off += (uint64_t)p.slots * p.P.slot_bytes;
   p.ws_bytes = off;
   return COLL_OK;
+}
+
+// The calibrated entry for `n` ranks and `bytes` per rank: the table of the
+// smallest calibrated group of at least n ranks (the largest one past it).
+static const PolicyEntry* policy_lookup(int n, uint64_t bytes) {
+  int group = kPolicyGroups[sizeof(kPolicyGroups) / sizeof(int) - 1];
+  for (int g : kPolicyGroups)
+    if (g >= n) {
+      group = g;
+      break;
+    }
+  int len = 0;
+  const PolicyEntry* t = policy_table(group, &len);
+  for (int i = 0; i < len; ++i)
+    if (bytes <= t[i].max_bytes) return &t[i];
+  return &t[len - 1];
 }
 
 int derive(const DeriveInput& in, Plan& p) {
   p = Plan{};
   const int n = in.nranks;
+  // flash-comm §4.2: slots rotate with a device-side call counter; two
+  // suffice here (a run starts after the previous one ended), four delay a
+  // slot's reuse by three more runs
+  if (in.slots != 0 && in.slots != 2 && in.slots != 4) return COLL_ERR_INVALID;
+  p.slots = in.slots == 0 ? 2 : in.slots;
   if (n < 1 || n > kMaxRanks) return COLL_ERR_UNSUPPORTED;
   if (in.dtype != COLL_BF16) return COLL_ERR_UNSUPPORTED;
-  if (in.encoding != COLL_LL8 && in.encoding != COLL_LL128 && in.encoding != COLL_SENT)
+  if (in.encoding != COLL_LL8 && in.encoding != COLL_LL128 && in.encoding != COLL_SENT &&
+      in.encoding != COLL_ENC_AUTO)
     return COLL_ERR_UNSUPPORTED;
   if (in.reset_mode < 0 || in.reset_mode > 3 || in.path < 0 || in.path > 3 ||
       in.algorithm < 0 || in.algorithm > 2 || in.ctas < 0 || in.tile_lines < 0)
@@ -229,14 +253,9 @@ int derive(const DeriveInput& in, Plan& p) {
   }
 
   if (count_in % 8 != 0) return COLL_ERR_ALIGN;
-  p.enc = in.encoding;
   p.n = n;
   p.count = count_in;
   p.shard = shard_elems(count_in, n);
-  p.reset_mode = p.enc == ENC_LL128 ? COLL_RESET_NONE : in.reset_mode;
-  // Sentinel packs carry no epoch: without a re-arm a consumed pack would
-  // look published to the next run of its slot.
-  if (p.enc == ENC_SENT && p.reset_mode == COLL_RESET_NONE) return COLL_ERR_UNSUPPORTED;
   p.timeout_ns = in.timeout_ns ? in.timeout_ns : 200000000ull;
   if (p.kind == CK_ALLTOALL && p.shard * (uint64_t)n != in.count)
     return COLL_ERR_ALIGN;  // the exchange needs equal partitions
@@ -263,22 +282,51 @@ int derive(const DeriveInput& in, Plan& p) {
     in_bytes_per_rank = std::max<uint64_t>(in_bytes_per_rank, 2 * p.in_elems[r]);
   }
 
-  // Algorithm and path (AUTO): boundaries placed on measured points of the
-  // 8-rank LL8 sweep on GB300 (flash-comm §3.2: fit, then put the boundary on
-  // a measured size).  Oneshot up to 512 KiB per rank (it reads N^2 S of
-  // lines but has one phase), twoshot above; one fused cooperative kernel up
-  // to 256 KiB per rank, stream-ordered pipelined kernels above.  Two ranks
-  // always use oneshot (both move S per rank).
+  // Encoding, algorithm and path.  An all-reduce with all three on AUTO
+  // takes the calibrated policy entry for its group and size (flash-comm
+  // §3.2 and §4.1: a constant-time lookup in a table measured offline).
+  int enc = in.encoding, algo = in.algorithm, path = in.path;
+  if (p.kind == CK_ALLREDUCE && enc == COLL_ENC_AUTO && algo == COLL_ALGO_AUTO &&
+      path == COLL_PATH_AUTO) {
+    const PolicyEntry* e = policy_lookup(n, in_bytes_per_rank);
+    enc = e->enc;
+    algo = e->algo;
+    path = e->path;
+  }
+  // Otherwise an AUTO encoding halves the bytes of small messages with
+  // sentinel packs and uses LL128 lines above 1 MiB per rank.
+  if (enc == COLL_ENC_AUTO) enc = in_bytes_per_rank <= (1u << 20) ? COLL_SENT : COLL_LL128;
+  // Sentinel packs carry no epoch: without a re-arm a consumed pack would
+  // look published to the next run of its slot.
+  if (enc == COLL_SENT && in.reset_mode == COLL_RESET_NONE) {
+    if (in.encoding == COLL_SENT) return COLL_ERR_UNSUPPORTED;
+    enc = COLL_LL8;
+  }
+  p.enc = enc;
+  p.reset_mode = p.enc == ENC_LL128 ? COLL_RESET_NONE : in.reset_mode;
+
+  // Algorithm and path left on AUTO: boundaries placed on measured points
+  // of the 8-rank sweeps on GB300.  Oneshot up to 512 KiB per rank (it reads
+  // N^2 S of lines but has one phase), twoshot above; one fused cooperative
+  // kernel up to 256 KiB per rank for LL8 and sentinel packs; the composed
+  // launch for LL128 twoshot from 8 MiB per rank; stream-ordered kernels
+  // otherwise.  Two ranks always use oneshot (both move S per rank).
   p.algorithm = 0;
   if (p.kind == CK_ALLREDUCE) {
-    p.algorithm = in.algorithm;
+    p.algorithm = algo;
     if (p.algorithm == COLL_ALGO_AUTO)
       p.algorithm = (n <= 2 || in_bytes_per_rank <= 512 * 1024) ? COLL_ONESHOT : COLL_TWOSHOT;
   }
-  p.path = in.path;
-  if (p.path == COLL_PATH_AUTO)
-    p.path = (in_bytes_per_rank <= 256 * 1024 && p.enc != ENC_LL128) ? COLL_PATH_FUSED
-                                                                     : COLL_PATH_STREAMED;
+  p.path = path;
+  if (p.path == COLL_PATH_AUTO) {
+    if (in_bytes_per_rank <= 256 * 1024 && p.enc != ENC_LL128)
+      p.path = COLL_PATH_FUSED;
+    else if (p.kind == CK_ALLREDUCE && p.algorithm == COLL_TWOSHOT && p.enc == ENC_LL128 &&
+             in_bytes_per_rank >= (8u << 20))
+      p.path = COLL_PATH_COMPOSED;
+    else
+      p.path = COLL_PATH_STREAMED;
+  }
 
   if (p.path == COLL_PATH_COMPOSED &&
       !(p.kind == CK_ALLREDUCE && p.algorithm == COLL_TWOSHOT && p.enc == ENC_LL128))
@@ -557,12 +605,14 @@ int derive(const DeriveInput& in, Plan& p) {
   const uint64_t lb = (uint64_t)line_bytes(p.enc);
   p.P.rank_bytes = round_up(p.p_rank_lines * lb, 4096);
   p.P.slot_bytes = p.P.rank_bytes * (uint64_t)n;
+  p.P.slot_mask = (uint64_t)p.slots - 1;
   p.P.base = off;
-  off += 2 * p.P.slot_bytes;
+  off += (uint64_t)p.slots * p.P.slot_bytes;
   p.AG.rank_bytes = round_up(p.ag_rank_lines * lb, 4096);
   p.AG.slot_bytes = p.AG.rank_bytes * (uint64_t)n;
+  p.AG.slot_mask = (uint64_t)p.slots - 1;
   p.AG.base = off;
-  off += 2 * p.AG.slot_bytes;
+  off += (uint64_t)p.slots * p.AG.slot_bytes;
   p.ws_bytes = off;
   return COLL_OK;
 }

@@ -38,6 +38,7 @@ struct DeriveInput {
   uint64_t timeout_ns;
   int tokens, hidden, topk, experts, max_rows;
   std::vector<uint64_t> vcounts;  // V collectives (see coll.h)
+  int slots;                      // staging slots: 2 or 4 (0 = 2)
   int sms;             // device SM count (a default when no device is present)
   int fused_capacity;  // co-resident CTAs of the fused kernel
 };
@@ -52,6 +53,7 @@ struct Plan {
   int path;        // COLL_PATH_FUSED / COLL_PATH_STREAMED (when inputs are given)
   int reset_mode;
   uint64_t timeout_ns;
+  int slots = 2;      // staging slots per region
   int ctas_per_rank;  // fused path
   int consume_grid;   // streamed consume grid
   uint64_t in_elems[kMaxRanks], out_elems[kMaxRanks];

@@ -319,7 +319,7 @@ __global__ void __launch_bounds__(kThreads, 2) k_fold_ll8(RunParams P) {
         const uint64_t off = (it.src_line + (uint64_t)r * kLL8RowLines) * kLL8LineBytes + 16 * lane;
         const uint32_t slot = wbase + (uint32_t)((j % kFoldStages) * n * kRowBytes);
         for (int p = 0; p < n; ++p)
-          cp_async16(slot + p * kRowBytes, P.ws + P.P.base + (e & 1) * P.P.slot_bytes +
+          cp_async16(slot + p * kRowBytes, P.ws + P.P.base + (e & P.P.slot_mask) * P.P.slot_bytes +
                                                (uint64_t)p * P.P.rank_bytes + off,
                      valid);
       }
@@ -344,7 +344,7 @@ __global__ void __launch_bounds__(kThreads, 2) k_fold_ll8(RunParams P) {
         for (int p = 0; p < kMaxRanks; ++p) {
           if (p < n && ok && !ll8_pair_ready(s[p], flag)) {
             const uint64_t* g = reinterpret_cast<const uint64_t*>(
-                                    P.ws + P.P.base + (e & 1) * P.P.slot_bytes +
+                                    P.ws + P.P.base + (e & P.P.slot_mask) * P.P.slot_bytes +
                                     (uint64_t)p * P.P.rank_bytes) + line;
             ok = ll8_wait_lines(P, g, 2, flag, p, (int64_t)line);
             uint64_t a, b;
@@ -365,14 +365,14 @@ __global__ void __launch_bounds__(kThreads, 2) k_fold_ll8(RunParams P) {
         }
         const uint32_t w0 = pack_bf16x2(a0, a1), w1 = pack_bf16x2(a2, a3);
         if (publish) {
-          uint64_t* dst = reinterpret_cast<uint64_t*>(P.ws + P.AG.base + (e & 1) * P.AG.slot_bytes +
+          uint64_t* dst = reinterpret_cast<uint64_t*>(P.ws + P.AG.base + (e & P.AG.slot_mask) * P.AG.slot_bytes +
                                                       (uint64_t)it.dst * P.AG.rank_bytes) +
                           it.out_off + (uint64_t)r * kLL8RowLines + 2 * lane;
           const uint64_t f = (uint64_t)flag << 32;
           st_relaxed_v2u64(dst, (uint64_t)w0 | f, (uint64_t)w1 | f);
           if (deferred) {
             uint64_t* other = reinterpret_cast<uint64_t*>(
-                                  P.ws + P.AG.base + ((e + 1) & 1) * P.AG.slot_bytes +
+                                  P.ws + P.AG.base + ((e + 1) & P.AG.slot_mask) * P.AG.slot_bytes +
                                   (uint64_t)it.dst * P.AG.rank_bytes) +
                               it.out_off + (uint64_t)r * kLL8RowLines + 2 * lane;
             st_relaxed_v2u64(other, 0ull, 0ull);
@@ -406,7 +406,7 @@ __global__ void __launch_bounds__(kThreads, 4) k_copy_ll8(RunParams P, int phase
     const int i = inter ? beg[v % P.nranks] + v / P.nranks : v;
     const Item it = items[i];
     const uint64_t* src = reinterpret_cast<const uint64_t*>(
-                              P.ws + R.base + (e & 1) * R.slot_bytes +
+                              P.ws + R.base + (e & R.slot_mask) * R.slot_bytes +
                               (uint64_t)it.src * R.rank_bytes) +
                           it.src_line;
     const uint32_t nrows = (it.nlines + kLL8RowLines - 1) / kLL8RowLines;
@@ -610,7 +610,7 @@ __global__ void __launch_bounds__(kThreads) k_rearm(RunParams P) {
     const Region& R = region == 0 ? P.P : P.AG;
     if (R.rank_bytes == 0) continue;
     const uint64_t words = (uint64_t)P.nranks * R.rank_bytes / 16;
-    uint4* base = reinterpret_cast<uint4*>(P.ws + R.base + (e & 1) * R.slot_bytes);
+    uint4* base = reinterpret_cast<uint4*>(P.ws + R.base + (e & R.slot_mask) * R.slot_bytes);
     for (uint64_t i = blockIdx.x * (uint64_t)blockDim.x + threadIdx.x; i < words;
          i += (uint64_t)gridDim.x * blockDim.x)
       st_relaxed_v2u64(base + i, fill, fill);

@@ -32,7 +32,7 @@ constexpr int kRowBytes = kLL128RowLines * kLL128LineBytes;  // 512
 
 __device__ __forceinline__ char* image_bytes(const RunParams& P, const Region& R,
                                              uint64_t epoch, int rank) {
-  return P.ws + R.base + (epoch & 1) * R.slot_bytes + (uint64_t)rank * R.rank_bytes;
+  return P.ws + R.base + (epoch & R.slot_mask) * R.slot_bytes + (uint64_t)rank * R.rank_bytes;
 }
 
 __device__ __forceinline__ uint4 shfl4(uint4 v, int src) {

@@ -65,7 +65,7 @@ static __device__ __noinline__ bool ll8_wait_lines(const RunParams& P, const uin
 
 __device__ __forceinline__ uint64_t* image_lines(const RunParams& P, const Region& R,
                                                  uint64_t epoch, int rank) {
-  return reinterpret_cast<uint64_t*>(P.ws + R.base + (epoch & 1) * R.slot_bytes +
+  return reinterpret_cast<uint64_t*>(P.ws + R.base + (epoch & R.slot_mask) * R.slot_bytes +
                                      (uint64_t)rank * R.rank_bytes);
 }
 

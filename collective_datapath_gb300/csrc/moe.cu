@@ -206,7 +206,7 @@ __global__ void __launch_bounds__(kMoeThreads) k_moe_stage(RunParams P) {
     int p, t;
     unit_src(u, p, t);
     const uint32_t row = sbuf + cur * buf_stride;
-    char* img = P.ws + P.P.base + (e & 1) * P.P.slot_bytes + (uint64_t)p * P.P.rank_bytes;
+    char* img = P.ws + P.P.base + (e & P.P.slot_mask) * P.P.slot_bytes + (uint64_t)p * P.P.rank_bytes;
     for (int j = warp; j < M.k; j += nwarps) {
       const size_t ent = (size_t)t * M.k + j;
       const int ex = M.topk[p][ent];
@@ -287,7 +287,7 @@ __global__ void __launch_bounds__(kMoeThreads, 4) k_moe_copy(RunParams P) {
     const int le = idx / n, p = idx % n;
     const int ex = d * M.el + le;
     const uint32_t s = s_stage[p * M.experts + ex] + (o - tab[idx]);
-    const char* src = P.ws + P.P.base + (e & 1) * P.P.slot_bytes + (uint64_t)p * P.P.rank_bytes +
+    const char* src = P.ws + P.P.base + (e & P.P.slot_mask) * P.P.slot_bytes + (uint64_t)p * P.P.rank_bytes +
                       (uint64_t)s * M.row_lines * kLL128LineBytes;
     uint16_t* dst = P.out[d] + (uint64_t)o * M.hidden;
     auto issue = [&](int j) {

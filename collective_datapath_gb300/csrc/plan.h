@@ -66,7 +66,7 @@ static_assert(sizeof(StageItem) == 32, "StageItem layout");
 
 // Device-resident control block at the start of the workspace.
 struct WsHeader {
-  uint64_t epoch;          // current epoch; slot = epoch & 1
+  uint64_t epoch;          // current epoch; staging slot = epoch & slot_mask
   uint32_t status_code;    // 0 or a coll_status_t latched by a kernel
   uint32_t status_rank;
   int64_t status_line;
@@ -81,10 +81,12 @@ struct WsHeader {
 };
 static_assert(sizeof(WsHeader) == 256, "WsHeader layout");
 
-// A staging region: two slots, each holding one image per rank.
+// A staging region: two or four slots (used in turn by consecutive epochs:
+// slot = epoch & slot_mask), each holding one image per rank.
 struct Region {
   uint64_t base;        // byte offset of slot 0 from the workspace base
-  uint64_t slot_bytes;  // bytes between slot 0 and slot 1
+  uint64_t slot_bytes;  // bytes between consecutive slots
+  uint64_t slot_mask;   // slots - 1 (1 or 3)
   uint64_t rank_bytes;  // bytes between consecutive rank images
 };
 

@@ -1,0 +1,51 @@
+// policy_table.h -- all-reduce policy per group size, written by
+// collective_datapath_gb300/tune.py from measurements; do not edit by hand.
+// measured on NVIDIA GB300, warm (CUDA graph) us per op, sizes 8 KiB - 64 MiB per rank
+// Entries: bytes per rank up to max_bytes use (encoding, algorithm, path).
+#pragma once
+
+#include <cstdint>
+
+namespace coll {
+
+struct PolicyEntry {
+  uint64_t max_bytes;
+  int enc, algo, path;
+};
+
+constexpr PolicyEntry kPolicy2[] = {
+    {8192ull, 2, 1, 1},  // SENT/oneshot/fused
+    {65536ull, 0, 1, 1},  // LL8/oneshot/fused
+    {2113536ull, 2, 1, 1},  // SENT/oneshot/fused
+    {4456448ull, 2, 2, 1},  // SENT/twoshot/fused
+    {17121280ull, 1, 1, 2},  // LL128/oneshot/streamed
+    {UINT64_MAX, 1, 2, 2},  // LL128/twoshot/streamed
+};
+constexpr PolicyEntry kPolicy4[] = {
+    {8192ull, 0, 1, 1},  // LL8/oneshot/fused
+    {851968ull, 2, 1, 1},  // SENT/oneshot/fused
+    {4456448ull, 2, 2, 1},  // SENT/twoshot/fused
+    {8994816ull, 1, 1, 2},  // LL128/oneshot/streamed
+    {UINT64_MAX, 1, 2, 2},  // LL128/twoshot/streamed
+};
+constexpr PolicyEntry kPolicy8[] = {
+    {8192ull, 0, 1, 1},  // LL8/oneshot/fused
+    {475136ull, 2, 1, 1},  // SENT/oneshot/fused
+    {4456448ull, 2, 2, 1},  // SENT/twoshot/fused
+    {33554432ull, 1, 2, 2},  // LL128/twoshot/streamed
+    {UINT64_MAX, 1, 2, 3},  // LL128/twoshot/composed
+};
+
+// group sizes with a table, in increasing order
+constexpr int kPolicyGroups[] = {2, 4, 8};
+
+inline const PolicyEntry* policy_table(int group, int* len) {
+  switch (group) {
+    case 2: *len = (int)(sizeof(kPolicy2) / sizeof(PolicyEntry)); return kPolicy2;
+    case 4: *len = (int)(sizeof(kPolicy4) / sizeof(PolicyEntry)); return kPolicy4;
+    case 8: *len = (int)(sizeof(kPolicy8) / sizeof(PolicyEntry)); return kPolicy8;
+    default: *len = 0; return nullptr;
+  }
+}
+
+}  // namespace coll

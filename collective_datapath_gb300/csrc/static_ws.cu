@@ -139,6 +139,7 @@ extern "C" coll_status_t coll_allreduce_static(int nranks, size_t count,
   P.P.base = kStaticHeaderBytes;
   P.P.rank_bytes = (uint64_t)rank_lines * kLL8LineBytes;
   P.P.slot_bytes = P.P.rank_bytes * (uint64_t)nranks;
+  P.P.slot_mask = 1;
   P.stage_rank = -1;
   P.advance_epoch = 1;
 

@@ -112,7 +112,13 @@ typedef enum {
  *   all other bit patterns pass unchanged, and reductions are unaffected
  *   (NaN in, NaN out).  Consumed packs must be re-armed: any reset mode but
  *   COLL_RESET_NONE (which gets COLL_ERR_UNSUPPORTED). */
-enum { COLL_LL8 = 0, COLL_LL128 = 1, COLL_SENT = 2 };
+enum { COLL_LL8 = 0, COLL_LL128 = 1, COLL_SENT = 2, COLL_ENC_AUTO = 3 };
+/* COLL_ENC_AUTO: for an all-reduce whose algorithm and path are AUTO too,
+ * encoding, algorithm and path come from a policy table calibrated on GB300
+ * per group size and bytes per rank (flash-comm §3.2 cost-guided selection,
+ * §4.1 table lookup; the table is csrc/policy_table.h, written by tune.py).
+ * Otherwise sentinel packs up to 1 MiB per rank (LL8 when the reset mode is
+ * COLL_RESET_NONE) and LL128 lines above. */
 
 /* All-reduce algorithm: oneshot (every rank folds all N inputs), twoshot
  * (reduce-scatter to an owner per partition, which publishes its reduced
@@ -148,7 +154,8 @@ enum { COLL_PATH_AUTO = 0, COLL_PATH_FUSED = 1, COLL_PATH_STREAMED = 2,
        COLL_PATH_COMPOSED = 3 };
 
 typedef struct {
-    int encoding;        /* COLL_LL8 | COLL_LL128 | COLL_SENT (default LL8) */
+    int encoding;        /* COLL_LL8 | COLL_LL128 | COLL_SENT | COLL_ENC_AUTO
+                            (default LL8) */
     int algorithm;       /* COLL_ALGO_AUTO | COLL_ONESHOT | COLL_TWOSHOT */
     int reset_mode;      /* COLL_RESET_* (default DEFERRED) */
     int path;            /* COLL_PATH_* (default AUTO) */
@@ -172,6 +179,9 @@ typedef struct {
      *     source p sends to destination d (count is ignored). */
     const uint64_t *vcounts;
     int nvcounts;
+    int slots;           /* staging slots used in turn by consecutive runs:
+                            2 (default, 0 means 2) or 4 (flash-comm §4.2
+                            rotating slots; twice the staging memory) */
 } coll_options_t;
 
 typedef struct coll_spec coll_spec_t;
@@ -262,7 +272,8 @@ coll_status_t coll_get_epoch(coll_spec_t *spec, coll_stream_t stream,
 /* Staging geometry, for inspection: region 0 = the rank images written by
  * coll_stage, region 1 = the reduced partitions published by twoshot owners.
  * Returns the byte offset (from the workspace base) of segment `seg` of rank
- * `rank` in slot `slot`, its line count and the line size in bytes. */
+ * `rank` in slot `slot` (0 .. slots-1; run e uses slot e mod slots), its line
+ * count and the line size in bytes. */
 coll_status_t coll_staging_layout(const coll_spec_t *spec, int region, int slot,
                                   int rank, int seg, uint64_t *byte_offset,
                                   uint64_t *lines, int *line_bytes);

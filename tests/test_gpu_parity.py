@@ -251,3 +251,28 @@ def test_composed_twoshot_matches_the_oracle(cd, n, count, shape, monkeypatch):
         coll.run(ins, outs)
         check(coll, outs, oracle.allreduce(xs), n)
         assert coll.epoch() == e + 1
+
+
+@pytest.mark.parametrize("enc,reset", [(0, 0), (0, 1), (0, 3), (1, 2), (2, 0), (2, 1), (2, 3)])
+@pytest.mark.parametrize("path", [1, 2, 3])
+def test_four_rotating_slots(cd, enc, reset, path):
+    """Four staging slots (flash-comm §4.2): run e stages into slot e mod 4
+    (the slot's lines carry epoch e), every run stays bit-exact, and the
+    re-arm rules hold with the longer rotation."""
+    if path == 3 and enc != 1:
+        pytest.skip("the composed launch is LL128 only")
+    n, count = 8, 8 * 1200
+    coll = make(cd, cd.ALLREDUCE, n, count, encoding=enc, algorithm=cd.COLL_TWOSHOT,
+                path=path, reset_mode=reset, slots=4)
+    _, ins, outs = buffers(coll, n, seed=30)
+    for e in range(1, 10):
+        xs = [synth.normal_bf16(300 + e, count, r) for r in range(n)]
+        for r in range(n):
+            ins[r].copy_(to_dev(xs[r]))
+        coll.run(ins, outs)
+        check(coll, outs, oracle.allreduce(xs), n)
+        assert coll.epoch() == e + 1
+        if enc == 1:
+            raw, lines, lb = read_lines(coll, 0, e % 4, 3, 5)
+            seqs = raw.reshape(lines, lb)[:, 120:128].copy().view(np.uint64).ravel()
+            assert np.all(seqs == e), f"epoch {e}: slot {e % 4} holds {set(seqs.tolist())}"
