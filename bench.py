@@ -229,6 +229,9 @@ def run_reference(args) -> int:
 # ---- GPU measurements ---------------------------------------------------------------
 
 def make_inputs(count: int, seed: int):
+    """Seeded uniform[-4, 4] bf16 inputs, one per rank, drawn on the device;
+    returns once they are written (they are drawn on torch's current stream,
+    the collectives run on another)."""
     import torch
 
     xs = []
@@ -237,6 +240,7 @@ def make_inputs(count: int, seed: int):
         g.manual_seed(seed * 1000 + r)
         u = torch.rand(count, generator=g, device="cuda", dtype=torch.float32)
         xs.append((u * 8.0 - 4.0).to(torch.bfloat16).view(torch.int16))
+    torch.cuda.synchronize()
     return xs
 
 
@@ -504,6 +508,7 @@ def moe_row(cd, stream, steps=5) -> dict:
         keys = torch.rand(tokens, experts, generator=g, device="cuda")
         topk.append(keys.argsort(dim=1)[:, :k].to(torch.int32).contiguous())
         cd.coll_set_routing(coll.spec, r, topk[r])
+    torch.cuda.synchronize()  # routing is drawn on torch's stream
     outs = [torch.empty(coll.elems(r)[1], dtype=torch.int16, device="cuda") for r in range(n)]
     ev = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
     for e in ev:

@@ -215,6 +215,7 @@ def time_op(cd, n: int, nbytes: int, cand: Candidate, stream) -> float:
     ins = [(torch.rand(count, generator=g, device="cuda") * 8 - 4).to(torch.bfloat16)
            .view(torch.int16) for _ in range(n)]
     outs = [torch.empty(count, dtype=torch.int16, device="cuda") for _ in range(n)]
+    torch.cuda.synchronize()  # inputs are drawn on torch's stream
     k = 64 if nbytes <= (1 << 20) else (16 if nbytes <= (16 << 20) else 4)
     with torch.cuda.stream(stream):
         for _ in range(3):
