@@ -171,30 +171,32 @@ __device__ __forceinline__ void count_rejection(char* ws) {
 }
 
 // Epoch protocol of a launch.  Every thread reads the device epoch itself
-// (one L2 request per warp, issued next to the launch's first data loads, no
-// CTA barrier); in the launch that ends a run each warp then adds one to
-// `arrived` (fire-and-forget).  The last CTA of the grid advances the epoch
-// once every warp has read it (arrived == all warps), so the next run uses
-// the other staging slot; no CTA waits at the end of its own work.
+// (one L2 request per warp, issued next to the launch's first data loads); in
+// the launch that ends a run each CTA then adds one to `arrived` once all its
+// threads hold the value (the barrier's predicate consumes it).  The last CTA
+// of the grid advances the epoch once every CTA has arrived, so the next run
+// uses the other staging slot; no CTA waits at the end of its own work.
 __device__ __forceinline__ uint64_t begin_run(const RunParams& P) {
   WsHeader* h = header(P.ws);
   const uint64_t e = ld_relaxed_u64(&h->epoch);
   if (P.advance_epoch) {
-    __syncwarp();
-    if ((threadIdx.x & 31) == 0)
-      asm volatile("red.relaxed.gpu.global.add.u32 [%0], 1;" ::"l"(&h->arrived) : "memory");
+    const int z = __syncthreads_or((int)(e >> 63));  // 0: the epoch never gets there
+    if (threadIdx.x == 0)
+      asm volatile("red.relaxed.gpu.global.add.u32 [%0], %1;" ::"l"(&h->arrived),
+                   "r"(1u + (uint32_t)z)
+                   : "memory");
   }
   return e;
 }
 
 __device__ __forceinline__ void finish_run(const RunParams& P, uint64_t epoch) {
   if (!P.advance_epoch || threadIdx.x != 0) return;
-  const uint32_t total = gridDim.x * gridDim.y * gridDim.z * ((blockDim.x + 31) / 32);
+  const uint32_t total = gridDim.x * gridDim.y * gridDim.z;
   if (blockIdx.x != gridDim.x - 1) return;
   WsHeader* h = header(P.ws);
-  // Every warp has started (and read the epoch) long before the last CTA
+  // Every CTA has started (and read the epoch) long before the last CTA
   // finishes; the 10 s bound only guards against a broken launch.  This wait
-  // ignores `abort`: the epoch must not move before every warp has read it.
+  // ignores `abort`: the epoch must not move before every CTA has read it.
   const uint64_t t0 = globaltimer_ns();
   while (ld_relaxed_u32(&h->arrived) < total) {
     if (globaltimer_ns() - t0 > 10000000000ull) {

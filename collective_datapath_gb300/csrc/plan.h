@@ -71,7 +71,7 @@ struct WsHeader {
   uint32_t status_rank;
   int64_t status_line;
   uint32_t abort;          // nonzero after an error: waits give up at once
-  uint32_t arrived;        // warps of the run's final launch that read the epoch
+  uint32_t arrived;        // CTAs of the run's final launch that read the epoch
   uint32_t started[2];     // fused runs: worker CTAs that started, by slot
   uint64_t rejections;     // stale lines observed (diagnostic)
   // composed twoshot: next task of the run's queue, by slot
