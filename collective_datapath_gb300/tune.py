@@ -85,9 +85,24 @@ def crossing(fa: tuple[float, float], fb: tuple[float, float]) -> float | None:
     return (ab - aa) / (ba - bb)
 
 
-def winners(times: dict[int, dict[Candidate, float]]) -> list[tuple[int, Candidate]]:
-    """Fastest candidate at every measured size, in increasing size."""
-    return [(s, min(times[s], key=lambda c: (times[s][c], c))) for s in sorted(times)]
+# A protocol keeps its band while it is within this fraction of the fastest
+# (flash-comm §3.2 "stable protocol band"): measurement noise of a few
+# percent does not flip the choice back and forth between neighbours.
+TOLERANCE = 0.03
+
+
+def winners(times: dict[int, dict[Candidate, float]],
+            tol: float = TOLERANCE) -> list[tuple[int, Candidate]]:
+    """Winner at every measured size, in increasing size: the fastest, unless
+    the previous size's winner is within `tol` of it."""
+    out: list[tuple[int, Candidate]] = []
+    for s in sorted(times):
+        best = min(times[s], key=lambda c: (times[s][c], c))
+        if out and out[-1][1] in times[s] and \
+                times[s][out[-1][1]] <= (1.0 + tol) * times[s][best]:
+            best = out[-1][1]
+        out.append((s, best))
+    return out
 
 
 def probe_sizes(s0: int, s1: int, s_cross: float | None, k: int = 4) -> list[int]:
@@ -105,10 +120,11 @@ def probe_sizes(s0: int, s1: int, s_cross: float | None, k: int = 4) -> list[int
 
 
 def build_policy(times: dict[int, dict[Candidate, float]],
-                 measure: Callable[[int, Candidate], float]) -> list[tuple[int, Candidate]]:
+                 measure: Callable[[int, Candidate], float],
+                 tol: float = TOLERANCE) -> list[tuple[int, Candidate]]:
     """Entries (max bytes per rank, candidate) in increasing size, the last
     open-ended (max = 2^64 - 1).  `measure(size, cand)` times one more point."""
-    win = winners(times)
+    win = winners(times, tol)
     entries: list[tuple[int, Candidate]] = []
     for (s0, c0), (s1, c1) in zip(win, win[1:]):
         if c0 == c1:
@@ -118,8 +134,8 @@ def build_policy(times: dict[int, dict[Candidate, float]],
         s_cross = crossing(fa, fb) if fa and fb else None
         boundary = s0
         for s in probe_sizes(s0, s1, s_cross):
-            if measure(s, c0) <= measure(s, c1):
-                boundary = s          # the left candidate still wins here
+            if measure(s, c0) <= (1.0 + tol) * measure(s, c1):
+                boundary = s          # the left candidate still holds its band here
             else:
                 break
         entries.append((boundary, c0))

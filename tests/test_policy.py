@@ -51,7 +51,7 @@ def test_two_protocols_switch_at_the_measured_point_below_the_crossing():
     costs = {A: (5.0, 1e-5), B: (20.0, 2e-6)}      # cross at 1.875e6 bytes
     measure, calls = lines_model(costs)
     times = {s: {A: measure(s, A), B: measure(s, B)} for s in GRID}
-    table = tune.build_policy(times, measure)
+    table = tune.build_policy(times, measure, tol=0.0)
     assert [c for _, c in table] == [A, B]
     boundary = table[0][0]
     s_star = 15 / 8e-6
@@ -75,7 +75,7 @@ def test_three_bands_and_a_candidate_that_never_wins():
     costs = {A: (3.0, 4e-5), B: (8.0, 1e-5), D: (40.0, 1.5e-6), X: (50.0, 5e-5)}
     measure, _ = lines_model(costs)
     times = {s: {c: measure(s, c) for c in costs} for s in GRID}
-    table = tune.build_policy(times, measure)
+    table = tune.build_policy(times, measure, tol=0.0)
     assert [c for _, c in table] == [A, B, D]
     assert table[-1][0] == (1 << 64) - 1
     assert table[0][0] < table[1][0]
@@ -148,3 +148,22 @@ def test_auto_encoding_outside_the_table(cd):
                             reset_mode=cd.COLL_RESET_NONE)
     assert cd.coll_debug_plan(s)["encoding"] == cd.COLL_LL8
     cd.coll_destroy(s)
+
+
+def test_noise_within_the_tolerance_does_not_flip_the_choice():
+    A, B = C(tune.LL8, tune.ONESHOT, tune.FUSED), C(tune.SENT, tune.ONESHOT, tune.FUSED)
+    # B is 1 % faster at 16 KiB only (noise), then clearly faster from 64 KiB
+    t = {8 << 10: {A: 5.00, B: 5.10}, 16 << 10: {A: 5.05, B: 5.00},
+         32 << 10: {A: 5.15, B: 5.20}, 64 << 10: {A: 6.50, B: 5.40}}
+
+    def measure(s, c):                     # linear between the grid points
+        lo = max(k for k in t if k <= s)
+        hi = min(k for k in t if k >= s)
+        if lo == hi:
+            return t[lo][c]
+        return t[lo][c] + (t[hi][c] - t[lo][c]) * (s - lo) / (hi - lo)
+
+    table = tune.build_policy(t, measure)
+    assert [c for _, c in table] == [A, B]
+    assert (32 << 10) <= table[0][0] < (64 << 10)
+    assert [c for _, c in tune.build_policy(t, measure, tol=0.0)] == [A, B, A, B]
