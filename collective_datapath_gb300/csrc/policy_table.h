@@ -14,25 +14,24 @@ struct PolicyEntry {
 };
 
 constexpr PolicyEntry kPolicy2[] = {
-    {8192ull, 2, 1, 1},  // SENT/oneshot/fused
-    {65536ull, 0, 1, 1},  // LL8/oneshot/fused
-    {2113536ull, 2, 1, 1},  // SENT/oneshot/fused
+    {98304ull, 0, 1, 1},  // LL8/oneshot/fused
+    {2097152ull, 2, 1, 1},  // SENT/oneshot/fused
     {4456448ull, 2, 2, 1},  // SENT/twoshot/fused
-    {17121280ull, 1, 1, 2},  // LL128/oneshot/streamed
+    {16777216ull, 1, 1, 2},  // LL128/oneshot/streamed
     {UINT64_MAX, 1, 2, 2},  // LL128/twoshot/streamed
 };
 constexpr PolicyEntry kPolicy4[] = {
-    {8192ull, 0, 1, 1},  // LL8/oneshot/fused
-    {851968ull, 2, 1, 1},  // SENT/oneshot/fused
+    {16384ull, 0, 1, 1},  // LL8/oneshot/fused
+    {884736ull, 2, 1, 1},  // SENT/oneshot/fused
     {4456448ull, 2, 2, 1},  // SENT/twoshot/fused
     {8994816ull, 1, 1, 2},  // LL128/oneshot/streamed
     {UINT64_MAX, 1, 2, 2},  // LL128/twoshot/streamed
 };
 constexpr PolicyEntry kPolicy8[] = {
-    {8192ull, 0, 1, 1},  // LL8/oneshot/fused
-    {475136ull, 2, 1, 1},  // SENT/oneshot/fused
+    {16384ull, 0, 1, 1},  // LL8/oneshot/fused
+    {491520ull, 2, 1, 1},  // SENT/oneshot/fused
     {4456448ull, 2, 2, 1},  // SENT/twoshot/fused
-    {33554432ull, 1, 2, 2},  // LL128/twoshot/streamed
+    {35520512ull, 1, 2, 2},  // LL128/twoshot/streamed
     {UINT64_MAX, 1, 2, 3},  // LL128/twoshot/composed
 };
 
