@@ -65,7 +65,7 @@ def sampled_reference(inputs, count, pos):
 
 
 @pytest.mark.parametrize("mib", [32, 128, 256])
-def test_config4_allreduce_twoshot_ll128(cd, inputs, mib):
+def test_bandwidth_allreduce_twoshot_ll128(cd, inputs, mib):
     import torch
 
     count = mib * 1024 * 1024 // 2
@@ -88,7 +88,7 @@ def test_config4_allreduce_twoshot_ll128(cd, inputs, mib):
 
 
 @pytest.mark.parametrize("mib", [32, 256])
-def test_config4_reduce_scatter_and_all_gather(cd, inputs, mib):
+def test_bandwidth_reduce_scatter_and_all_gather(cd, inputs, mib):
     import torch
 
     count = mib * 1024 * 1024 // 2
@@ -133,7 +133,7 @@ def test_config4_reduce_scatter_and_all_gather(cd, inputs, mib):
 
 
 @pytest.mark.parametrize("mib", [32, 256])
-def test_config4_allreduce_composed_twoshot(cd, inputs, mib):
+def test_bandwidth_allreduce_composed_twoshot(cd, inputs, mib):
     """The one-launch twoshot at full size: sampled against the oracle, and
     byte-identical to the stream-ordered twoshot on every element."""
     import torch

@@ -80,7 +80,7 @@ def test_moe_dispatch_small_cases_match_the_oracle(cd, n, tokens, hidden, k, exp
             assert np.array_equal(got, want[d]), f"epoch {epoch} destination {d}"
 
 
-def test_config5_moe_dispatch_full_size(cd):
+def test_moe_dispatch_8x4096x7168_full_size(cd):
     """8 ranks x 4096 tokens x 7168 bf16 normal(0,1), top-8 of 256 experts:
     every output row of every destination equals its source row as listed
     by the oracle, and the counts equal the oracle's."""

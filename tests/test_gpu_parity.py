@@ -47,7 +47,7 @@ def check(coll, outs, want, n):
                                  f"got {got[bad[0]]:#06x} want {want[r][bad[0]]:#06x}")
 
 
-def test_config1_oneshot_two_ranks_1kib(cd):
+def test_oneshot_two_ranks_512_elements(cd):
     """2 ranks x 512 bf16 uniform[-1,1] seed 0, LL8, oneshot, one epoch."""
     n, count = 2, 512
     coll = make(cd, cd.ALLREDUCE, n, count, encoding=cd.COLL_LL8,
@@ -63,7 +63,7 @@ def test_config1_oneshot_two_ranks_1kib(cd):
 @pytest.mark.parametrize("algo", [1, 2])
 @pytest.mark.parametrize("path", [1, 2])
 @pytest.mark.parametrize("T", [1, 2, 4, 8, 16, 32, 64, 128])
-def test_config2_decode_allreduce(cd, T, path, algo):
+def test_decode_allreduce_8_ranks(cd, T, path, algo):
     """8 ranks x [T x 4096] normal(0,1), LL8, oneshot and twoshot; all 8
     output copies identical and equal to the oracle."""
     n, count = 8, T * 4096

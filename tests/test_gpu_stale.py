@@ -42,7 +42,7 @@ def image_lines_of_real_lines(cd, coll, n_seg):
 
 
 @pytest.mark.parametrize("enc,algo,epochs", [(0, 1, 64), (1, 1, 64), (0, 2, 8), (1, 2, 8)])
-def test_config3_stale_lines_rejected_across_64_epochs(cd, enc, algo, epochs):
+def test_stale_lines_rejected_across_64_epochs(cd, enc, algo, epochs):
     import torch
 
     n, count = 8, 16 * 7168

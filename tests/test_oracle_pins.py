@@ -30,7 +30,7 @@ def _bits(vals) -> np.ndarray:
     return (f >> 16).astype(np.uint16)
 
 
-# ---- C0 widening -------------------------------------------------------------
+# ---- widening bf16 -> fp32 -------------------------------------------------------------
 
 def test_widening_all_patterns_match_field_decoding(orc):
     for b in list(range(0, 65536, 7)) + [0x0000, 0x8000, 0x0001, 0x8001,
@@ -62,7 +62,7 @@ def test_widening_matches_torch_for_all_patterns(orc):
     assert np.all(np.isnan(got) == np.isnan(ref))
 
 
-# ---- C2 rounding ----------------------------------------------------------------
+# ---- rounding fp32 -> bf16 ----------------------------------------------------------------
 
 @pytest.fixture(scope="module")
 def round_checker(orc, tmp_path_factory):
@@ -120,7 +120,7 @@ def test_rounding_matches_torch_cast_on_finite_values(orc):
     assert np.array_equal(got, ref[:20000])
 
 
-# ---- C1 fold ---------------------------------------------------------------------
+# ---- fold in rank order ---------------------------------------------------------------------
 
 @pytest.mark.parametrize("n", [1, 2, 3, 5, 8])
 def test_fold_integer_inputs_sum_exactly(orc, n):
@@ -208,7 +208,7 @@ def test_fold_overflow_and_subnormals(orc):
     assert exact.fold_bits([0x0001, 0x0001]) == 0x0002
 
 
-# ---- C3 / C4 collectives -----------------------------------------------------------
+# ---- collectives -----------------------------------------------------------
 
 def test_figure4_worked_example(orc):
     spec = json.load(open(os.path.join(GOLDEN, "fig4_layouts.json")))
@@ -283,7 +283,7 @@ def test_all_gather_is_rank_ordered_concatenation(orc):
         assert np.array_equal(o, np.concatenate(xs))
 
 
-# ---- C5 / C6 encodings ---------------------------------------------------------------
+# ---- line encodings ---------------------------------------------------------------
 
 def test_ll8_line_layout_hand_case(orc):
     lines = orc.ll8_encode(np.array([0x3F80, 0xC000, 0x1234], dtype=np.uint16), 5)
@@ -428,7 +428,7 @@ def test_sentinel_sanitize_does_not_change_a_fold(orc):
     assert not np.any(raw == 0xFFFF)
 
 
-# ---- C11 MoE dispatch ------------------------------------------------------------------
+# ---- MoE dispatch ------------------------------------------------------------------
 
 def test_moe_tiny_hand_derived_layout(orc):
     spec = json.load(open(os.path.join(GOLDEN, "moe_tiny.json")))
