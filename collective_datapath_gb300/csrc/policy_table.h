@@ -14,24 +14,23 @@ struct PolicyEntry {
 };
 
 constexpr PolicyEntry kPolicy2[] = {
-    {98304ull, 0, 1, 1},  // LL8/oneshot/fused
-    {2097152ull, 2, 1, 1},  // SENT/oneshot/fused
-    {4456448ull, 2, 2, 1},  // SENT/twoshot/fused
+    {16384ull, 0, 1, 1},  // LL8/oneshot/fused
+    {1097728ull, 2, 1, 1},  // SENT/oneshot/fused
+    {5931008ull, 2, 2, 1},  // SENT/twoshot/fused
     {16777216ull, 1, 1, 2},  // LL128/oneshot/streamed
     {UINT64_MAX, 1, 2, 2},  // LL128/twoshot/streamed
 };
 constexpr PolicyEntry kPolicy4[] = {
-    {16384ull, 0, 1, 1},  // LL8/oneshot/fused
-    {884736ull, 2, 1, 1},  // SENT/oneshot/fused
+    {8192ull, 0, 1, 1},  // LL8/oneshot/fused
+    {802816ull, 2, 1, 1},  // SENT/oneshot/fused
     {4456448ull, 2, 2, 1},  // SENT/twoshot/fused
-    {8994816ull, 1, 1, 2},  // LL128/oneshot/streamed
+    {9011200ull, 1, 1, 2},  // LL128/oneshot/streamed
     {UINT64_MAX, 1, 2, 2},  // LL128/twoshot/streamed
 };
 constexpr PolicyEntry kPolicy8[] = {
-    {16384ull, 0, 1, 1},  // LL8/oneshot/fused
-    {491520ull, 2, 1, 1},  // SENT/oneshot/fused
-    {4456448ull, 2, 2, 1},  // SENT/twoshot/fused
-    {35520512ull, 1, 2, 2},  // LL128/twoshot/streamed
+    {376832ull, 2, 1, 1},  // SENT/oneshot/fused
+    {4194304ull, 2, 2, 1},  // SENT/twoshot/fused
+    {34619392ull, 1, 2, 2},  // LL128/twoshot/streamed
     {UINT64_MAX, 1, 2, 3},  // LL128/twoshot/composed
 };
 
