@@ -54,6 +54,7 @@ def lib() -> ctypes.CDLL:
 
 _u16p = ctypes.POINTER(ctypes.c_uint16)
 _u64p = ctypes.POINTER(ctypes.c_uint64)
+_u32p = ctypes.POINTER(ctypes.c_uint32)
 _u8p = ctypes.POINTER(ctypes.c_uint8)
 _i32p = ctypes.POINTER(ctypes.c_int32)
 _i64p = ctypes.POINTER(ctypes.c_int64)
@@ -113,6 +114,18 @@ def _declare(L: ctypes.CDLL) -> None:
     L.orc_ll128_encode.restype = None
     L.orc_ll128_decode.argtypes = [_u8p, _sz, ctypes.c_uint64, _u16p]
     L.orc_ll128_decode.restype = _sz
+    L.orc_fold_f32.argtypes = [ctypes.POINTER(_u32p), ctypes.c_int, _sz]
+    L.orc_fold_f32.restype = ctypes.c_uint32
+    for name in ("orc_allreduce_f32", "orc_reduce_scatter_f32"):
+        f = getattr(L, name)
+        f.argtypes = [ctypes.c_int, _sz, ctypes.POINTER(_u32p), ctypes.POINTER(_u32p)]
+        f.restype = ctypes.c_int
+    L.orc_sent_sanitize_f32.argtypes = [ctypes.c_uint32]
+    L.orc_sent_sanitize_f32.restype = ctypes.c_uint32
+    L.orc_sent_encode_f32.argtypes = [_u32p, _sz, _u64p]
+    L.orc_sent_encode_f32.restype = None
+    L.orc_sent_decode_f32.argtypes = [_u64p, _sz, _u32p]
+    L.orc_sent_decode_f32.restype = _sz
     L.orc_sent_sanitize.argtypes = [ctypes.c_uint16]
     L.orc_sent_sanitize.restype = ctypes.c_uint16
     L.orc_sent_sanitize_buf.argtypes = [_u16p, _sz, _u16p]
@@ -381,4 +394,62 @@ def sent_decode(packs: np.ndarray, elems: int, fill: int = 0) -> tuple[np.ndarra
     out = np.full(max(elems, 1), fill, dtype=np.uint16)
     skipped = lib().orc_sent_decode(_ptr(packs, ctypes.c_uint64), elems,
                                     _ptr(out, ctypes.c_uint16))
+    return out[:elems], int(skipped)
+
+
+# ---- fp32 tensors (uint32 bit patterns) -------------------------------------------
+
+CANONICAL_NAN_F32 = 0x7FC00000
+
+
+def _f32_collective(name, ins, out_sizes):
+    n, count = len(ins), int(np.asarray(ins[0]).size)
+    arrs = [_c(np.asarray(x).ravel(), np.uint32) for x in ins]
+    arrs = [a if a.size else np.zeros(1, np.uint32) for a in arrs]
+    outs = [np.zeros(max(int(o), 1), dtype=np.uint32) for o in out_sizes]
+    rc = getattr(lib(), name)(n, count, _ptr_array(arrs, ctypes.c_uint32),
+                              _ptr_array(outs, ctypes.c_uint32))
+    if rc != 0:
+        raise ValueError(f"{name} rejected its arguments")
+    return [o[:int(m)] for o, m in zip(outs, out_sizes)]
+
+
+def fold_f32(xs: Sequence[int]) -> int:
+    """The fold of one position whose N contributions are the fp32 patterns xs."""
+    arrs = [np.array([v], dtype=np.uint32) for v in xs]
+    return int(lib().orc_fold_f32(_ptr_array(arrs, ctypes.c_uint32), len(arrs), 0))
+
+
+def allreduce_f32(ins: Sequence[np.ndarray]) -> list[np.ndarray]:
+    count = int(np.asarray(ins[0]).size)
+    return _f32_collective("orc_allreduce_f32", ins, [count] * len(ins))
+
+
+def reduce_scatter_f32(ins: Sequence[np.ndarray]) -> list[np.ndarray]:
+    n, count = len(ins), int(np.asarray(ins[0]).size)
+    return _f32_collective("orc_reduce_scatter_f32", ins,
+                           [shard_len(count, n, r) for r in range(n)])
+
+
+def sent_sanitize_f32(x: np.ndarray) -> np.ndarray:
+    x = _c(np.asarray(x).ravel(), np.uint32)
+    out = x.copy()
+    for i in np.flatnonzero(x == np.uint32(0xFFFFFFFF)):
+        out[i] = lib().orc_sent_sanitize_f32(int(x[i]))
+    return out
+
+
+def sent_encode_f32(x: np.ndarray) -> np.ndarray:
+    x = _c(np.asarray(x).ravel(), np.uint32)
+    np_ = (x.size + 1) // 2
+    out = np.zeros(max(np_, 1), dtype=np.uint64)
+    lib().orc_sent_encode_f32(_ptr(x, ctypes.c_uint32), x.size, _ptr(out, ctypes.c_uint64))
+    return out[:np_]
+
+
+def sent_decode_f32(packs: np.ndarray, elems: int, fill: int = 0) -> tuple[np.ndarray, int]:
+    packs = _c(packs, np.uint64)
+    out = np.full(max(elems, 1), fill, dtype=np.uint32)
+    skipped = lib().orc_sent_decode_f32(_ptr(packs, ctypes.c_uint64), elems,
+                                        _ptr(out, ctypes.c_uint32))
     return out[:elems], int(skipped)

@@ -397,3 +397,98 @@ size_t orc_sent_decode(const uint64_t *packs, size_t elems, uint16_t *out)
     }
     return skipped;
 }
+
+/* ---- fp32 tensors -------------------------------------------------------- */
+
+static float f32_of(uint32_t u)
+{
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return f;
+}
+
+static uint32_t bits_of(float f)
+{
+    uint32_t u;
+    if (f != f)
+        return 0x7FC00000u; /* any NaN: the canonical quiet NaN */
+    memcpy(&u, &f, sizeof u);
+    return u;
+}
+
+uint32_t orc_fold_f32(const uint32_t *const *x, int n, size_t i)
+{
+    float acc = f32_of(x[0][i]);
+    for (int p = 1; p < n; ++p)
+        acc = acc + f32_of(x[p][i]);
+    return bits_of(acc);
+}
+
+static int bad_args_f32(int n, const uint32_t *const *in, uint32_t *const *out)
+{
+    if (n < 1 || in == NULL || out == NULL)
+        return 1;
+    for (int p = 0; p < n; ++p)
+        if (in[p] == NULL || out[p] == NULL)
+            return 1;
+    return 0;
+}
+
+int orc_allreduce_f32(int n, size_t count, const uint32_t *const *in,
+                      uint32_t *const *out)
+{
+    if (bad_args_f32(n, in, out))
+        return -1;
+    for (int d = 0; d < n; ++d)
+        for (size_t i = 0; i < count; ++i)
+            out[d][i] = orc_fold_f32(in, n, i);
+    return 0;
+}
+
+int orc_reduce_scatter_f32(int n, size_t count, const uint32_t *const *in,
+                           uint32_t *const *out)
+{
+    if (bad_args_f32(n, in, out))
+        return -1;
+    for (int r = 0; r < n; ++r) {
+        size_t b = orc_shard_begin(count, n, r);
+        size_t len = orc_shard_len(count, n, r);
+        for (size_t j = 0; j < len; ++j)
+            out[r][j] = orc_fold_f32(in, n, b + j);
+    }
+    return 0;
+}
+
+uint32_t orc_sent_sanitize_f32(uint32_t x)
+{
+    if (x == 0xFFFFFFFFu)
+        return 0x7FC00000u;
+    return x;
+}
+
+void orc_sent_encode_f32(const uint32_t *in, size_t elems, uint64_t *packs)
+{
+    size_t np = (elems + 1u) / 2u;
+    for (size_t j = 0; j < np; ++j) {
+        uint64_t lo = orc_sent_sanitize_f32(in[2 * j]);
+        uint64_t hi = 2 * j + 1 < elems ? orc_sent_sanitize_f32(in[2 * j + 1]) : 0u;
+        packs[j] = lo | (hi << 32);
+    }
+}
+
+size_t orc_sent_decode_f32(const uint64_t *packs, size_t elems, uint32_t *out)
+{
+    size_t np = (elems + 1u) / 2u;
+    size_t skipped = 0;
+    for (size_t j = 0; j < np; ++j) {
+        uint64_t pack = packs[j];
+        if (pack == 0xFFFFFFFFFFFFFFFFull) { /* not yet published */
+            skipped += 1;
+            continue;
+        }
+        out[2 * j] = (uint32_t)(pack & 0xFFFFFFFFu);
+        if (2 * j + 1 < elems)
+            out[2 * j + 1] = (uint32_t)(pack >> 32);
+    }
+    return skipped;
+}

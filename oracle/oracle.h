@@ -213,6 +213,29 @@ void orc_sent_encode(const uint16_t *in, size_t elems, uint64_t *packs);
  * of packs skipped. */
 size_t orc_sent_decode(const uint64_t *packs, size_t elems, uint16_t *out);
 
+/* ---- fp32 tensors -------------------------------------------------------
+ * [flash] §4.1 admits bf16 and fp32 tensors.  For fp32 the fold is the same
+ * left fold in rank order, in binary32 with round-to-nearest-even, and there
+ * is no final narrowing: acc = x_0; acc = acc + x_p for p = 1..N-1.
+ * Readings: elements are uint32 bit patterns; a NaN result is written as the
+ * canonical quiet NaN 0x7FC00000 (the pages fix no NaN payload; this is the
+ * binary32 counterpart of the bf16 rule, whose 0x7FC0 is its upper half).
+ * Partitions are counted in fp32 elements with the same rule as bf16.
+ * Copies (all-gather, all-to-all and their V forms) move bytes and need no
+ * fp32 form: they are the bf16 ones on the same bytes. */
+uint32_t orc_fold_f32(const uint32_t *const *x, int n, size_t i);
+int orc_allreduce_f32(int n, size_t count, const uint32_t *const *in,
+                      uint32_t *const *out);
+int orc_reduce_scatter_f32(int n, size_t count, const uint32_t *const *in,
+                           uint32_t *const *out);
+
+/* Sentinel packs of fp32: 8 bytes = 2 elements (element 2j in the low
+ * word), the reserved pattern 0xFFFFFFFF (a NaN), published as 0x7FC00000;
+ * the unready pack is all ones. */
+uint32_t orc_sent_sanitize_f32(uint32_t x);
+void orc_sent_encode_f32(const uint32_t *in, size_t elems, uint64_t *packs);
+size_t orc_sent_decode_f32(const uint64_t *packs, size_t elems, uint32_t *out);
+
 #ifdef __cplusplus
 }
 #endif

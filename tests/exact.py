@@ -125,3 +125,63 @@ def fold_bits(values: list[int]) -> int:
     for b in values[1:]:
         acc = add32(acc, decode_bf16(b))
     return to_bf16_bits(acc)
+
+
+def decode_f32(bits: int):
+    """binary32 pattern -> (Fraction value, is_negative_zero) or INF/NINF/None(NaN)."""
+    s = (bits >> 31) & 1
+    e = (bits >> 23) & 0xFF
+    f = bits & 0x7FFFFF
+    if e == 0xFF:
+        if f:
+            return None
+        return NINF if s else INF
+    if e == 0:
+        mag = Fraction(f, 1 << 23) * Fraction(2) ** -126
+    else:
+        mag = (1 + Fraction(f, 1 << 23)) * Fraction(2) ** (e - 127)
+    if mag == 0:
+        return (Fraction(0), bool(s))
+    return (-mag if s else mag, False)
+
+
+def encode_f32(v) -> int:
+    """Exact binary32-representable value (Fraction, neg-zero flag) -> pattern."""
+    if v == INF:
+        return 0x7F800000
+    if v == NINF:
+        return 0xFF800000
+    val, negzero = v
+    if val == 0:
+        return 0x80000000 if negzero else 0
+    s = 1 if val < 0 else 0
+    a = -val if s else val
+    e = _floor_log2(a)
+    if e < -126:
+        f = a / Fraction(2) ** -126 * (1 << 23)
+        assert f.denominator == 1
+        return (s << 31) | int(f)
+    f = (a / Fraction(2) ** e - 1) * (1 << 23)
+    assert f.denominator == 1
+    return (s << 31) | ((e + 127) << 23) | int(f)
+
+
+def add_exact(x, y):
+    """IEEE-754 binary32 addition of two decoded operands (§6.1, §6.3):
+    infinities, signed zeros under round-to-nearest, and one rounding of the
+    exact sum.  None stands for NaN."""
+    if x is None or y is None:
+        return None
+    if x in (INF, NINF) or y in (INF, NINF):
+        if x in (INF, NINF) and y in (INF, NINF) and x != y:
+            return None
+        return x if x in (INF, NINF) else y
+    (vx, zx), (vy, zy) = x, y
+    t = vx + vy
+    if t == 0:
+        # exact zero sum: -0 only when both operands are -0 (§6.3)
+        return (Fraction(0), vx == 0 and vy == 0 and zx and zy)
+    r = round_to(t, BINARY32)
+    if r in (INF, NINF):
+        return r
+    return (r, r == 0 and t < 0)

@@ -43,6 +43,14 @@ MUTANTS = [
     ("sent_decode_accepts_sentinel", "if (pack == ~(uint64_t)0) {", "if (0) {"),
     ("sent_not_sanitized_in_encode", "uint64_t v = idx < elems ? orc_sent_sanitize(in[idx]) : 0u;",
      "uint64_t v = idx < elems ? in[idx] : 0u;"),
+    ("f32_nan_keeps_payload", "        return 0x7FC00000u; /* any NaN: the canonical quiet NaN */",
+     "        memcpy(&u, &f, sizeof u); return u;"),
+    ("f32_fold_drops_rank0", "    float acc = f32_of(x[0][i]);\n    for (int p = 1; p < n; ++p)\n        acc = acc + f32_of(x[p][i]);",
+     "    float acc = 0.0f;\n    for (int p = 1; p < n; ++p)\n        acc = acc + f32_of(x[p][i]);"),
+    ("f32_rs_wrong_offset", "            out[r][j] = orc_fold_f32(in, n, b + j);", "            out[r][j] = orc_fold_f32(in, n, j);"),
+    ("f32_sent_pack_swapped", "        packs[j] = lo | (hi << 32);", "        packs[j] = hi | (lo << 32);"),
+    ("f32_sent_decode_accepts_sentinel", "        if (pack == 0xFFFFFFFFFFFFFFFFull) { /* not yet published */", "        if (0) {"),
+    ("f32_sent_wrong_pattern", "    if (x == 0xFFFFFFFFu)\n        return 0x7FC00000u;", "    if (x == 0xFFFF0000u)\n        return 0x7FC00000u;"),
     ("moe_source_major_order", "for (int le = 0; le < el; ++le) {\n            int e = d * el + le;\n            for (int p = 0; p < n; ++p)",
      "for (int le = 0; le < el; ++le) {\n            int e = d * el + le;\n            for (int p = n - 1; p >= 0; --p)"),
 ]
@@ -75,6 +83,10 @@ PINS = [
     pins.test_sentinel_pack_layout_hand_case,
     pins.test_sentinel_roundtrip_every_pattern_in_every_position,
     pins.test_sentinel_pack_is_not_ready,
+    pins.test_fold_f32_special_values,
+    pins.test_fold_f32_n1_is_identity,
+    pins.test_reduce_scatter_f32_is_the_allreduce_partition,
+    pins.test_sentinel_f32_sanitize_and_layout,
 ]
 
 

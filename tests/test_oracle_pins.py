@@ -548,3 +548,103 @@ def test_all_to_all_v_hand_case(orc):
     out = orc.all_to_all_v([a, b], [[8, 16], [24, 0]])
     assert out[0].tolist() == list(range(1, 9)) + list(range(101, 125))
     assert out[1].tolist() == list(range(9, 25))
+
+
+# ---- fp32 tensors ---------------------------------------------------------------
+
+def _f32_patterns(seed, size):
+    """fp32 patterns spread over every exponent, with zeros, subnormals,
+    infinities and the largest finite values mixed in."""
+    g = np.random.Generator(np.random.Philox(seed))
+    bits = g.integers(0, 1 << 32, size, dtype=np.uint64).astype(np.uint32)
+    special = np.array([0, 0x80000000, 1, 0x80000001, 0x007FFFFF, 0x00800000, 0x7F7FFFFF,
+                        0xFF7FFFFF, 0x7F800000, 0xFF800000, 0x3F800000, 0xBF800000],
+                       dtype=np.uint32)
+    bits[:: 7] = special[g.integers(0, special.size, bits[:: 7].size)]
+    # narrow the exponent range on half the entries so sums round often
+    half = g.random(size) < 0.5
+    bits[half] = (bits[half] & np.uint32(0x807FFFFF)) | \
+        (g.integers(100, 140, int(half.sum())).astype(np.uint32) << np.uint32(23))
+    nan = ((bits >> 23) & 0xFF) == 0xFF
+    nan &= (bits & 0x7FFFFF) != 0
+    bits[nan] = np.uint32(0x3F800000)          # NaN inputs are pinned separately
+    return bits
+
+
+def _fold_f32_exact(vals):
+    acc = exact.decode_f32(int(vals[0]))
+    for v in vals[1:]:
+        acc = exact.add_exact(acc, exact.decode_f32(int(v)))
+    return 0x7FC00000 if acc is None else exact.encode_f32(acc)
+
+
+def test_fold_f32_against_exact_rationals(orc):
+    for n in (2, 3, 5, 8):
+        xs = [_f32_patterns(70 + n * 10 + p, 700) for p in range(n)]
+        got = orc.allreduce_f32(xs)[0]
+        for i in range(700):
+            assert got[i] == _fold_f32_exact([x[i] for x in xs]), (n, i)
+
+
+def test_fold_f32_integer_sums_are_exact(orc):
+    g = np.random.Generator(np.random.Philox(77))
+    for n in (2, 8):
+        ints = [g.integers(-(1 << 20), 1 << 20, 4096) for _ in range(n)]
+        xs = [np.asarray(v, dtype=np.float32).view(np.uint32) for v in ints]
+        got = orc.allreduce_f32(xs)[0].view(np.float32)
+        assert np.array_equal(got, np.sum(ints, axis=0).astype(np.float32))
+
+
+def test_fold_f32_special_values(orc):
+    f = orc.fold_f32
+    assert f([0x7F800000, 0xFF800000]) == 0x7FC00000          # inf + -inf: NaN
+    assert f([0x7FC00001, 0x3F800000]) == 0x7FC00000          # NaN in: canonical NaN out
+    assert f([0xFFFFFFFF]) == 0x7FC00000                      # N = 1 keeps no NaN payload
+    assert f([0x80000000, 0x80000000]) == 0x80000000          # -0 + -0 = -0
+    assert f([0x80000000, 0x00000000]) == 0x00000000          # -0 + +0 = +0
+    assert f([0x7F7FFFFF, 0x7F7FFFFF]) == 0x7F800000          # overflow to +inf
+    assert f([0x00000001, 0x00000001]) == 0x00000002          # subnormals kept
+    assert f([0x3F800000, 0x33800000]) == 0x3F800000          # 1 + 2^-24: tie to even
+    assert f([0x3F800001, 0x33800000]) == 0x3F800002          # tie to even, upwards
+    # rank order is observable: (big + 1) - big vs (big - big) + 1
+    big, one = 0x4B800000, 0x3F800000                         # 2^24, 1
+    assert f([big, one, big | 0x80000000]) == 0
+    assert f([big, big | 0x80000000, one]) == one
+
+
+def test_fold_f32_n1_is_identity(orc):
+    x = _f32_patterns(79, 20000)
+    x[:4] = [0x80000000, 0x00000001, 0x7F800000, 0xFF7FFFFF]
+    assert np.array_equal(orc.allreduce_f32([x])[0], x)
+
+
+def test_reduce_scatter_f32_is_the_allreduce_partition(orc):
+    n, count = 5, 5 * 40 + 16
+    xs = [_f32_patterns(90 + p, count) for p in range(n)]
+    ar = orc.allreduce_f32(xs)[0]
+    rs = orc.reduce_scatter_f32(xs)
+    for r in range(n):
+        b, ln = orc.shard_begin(count, n, r), orc.shard_len(count, n, r)
+        assert np.array_equal(rs[r], ar[b:b + ln])
+
+
+def test_sentinel_f32_sanitize_and_layout(orc):
+    x = np.array([0xFFFFFFFF, 0x3F800000, 0xFFFF0000, 0x0000FFFF, 0x7FC00001], dtype=np.uint32)
+    assert orc.sent_sanitize_f32(x).tolist() == [0x7FC00000, 0x3F800000, 0xFFFF0000,
+                                                 0x0000FFFF, 0x7FC00001]
+    packs = orc.sent_encode_f32(x)
+    assert packs.tolist() == [0x3F8000007FC00000, 0x0000FFFFFFFF0000, 0x000000007FC00001]
+    # only the all-ones pattern changes, wherever it sits
+    g = np.random.Generator(np.random.Philox(5))
+    y = g.integers(0, 1 << 32, 50000, dtype=np.uint64).astype(np.uint32)
+    y[::97] = 0xFFFFFFFF
+    s = orc.sent_sanitize_f32(y)
+    changed = np.flatnonzero(s != y)
+    assert np.array_equal(changed, np.flatnonzero(y == 0xFFFFFFFF))
+    assert np.all(s[changed] == 0x7FC00000)
+    back, skipped = orc.sent_decode_f32(orc.sent_encode_f32(y), y.size)
+    assert skipped == 0 and np.array_equal(back, s)
+    p = orc.sent_encode_f32(y)
+    p[3] = np.uint64(0xFFFFFFFFFFFFFFFF)
+    back, skipped = orc.sent_decode_f32(p, y.size, fill=7)
+    assert skipped == 1 and back[6] == 7 and back[7] == 7
