@@ -27,6 +27,7 @@ COLL_PACKED, COLL_SCATTERED, COLL_TRANSPOSED = 0, 1, 2
 COLL_PACKED_V, COLL_SCATTERED_V, COLL_TRANSPOSED_V = 3, 4, 5
 COLL_COPY, COLL_REDUCE = 0, 1
 COLL_BF16 = 0
+COLL_F32 = 1
 COLL_OK, COLL_ERR_INVALID, COLL_ERR_UNSUPPORTED, COLL_ERR_ALIGN = 0, 1, 2, 3
 COLL_ERR_NOMEM, COLL_ERR_CUDA, COLL_ERR_TIMEOUT, COLL_ERR_STATE = 4, 5, 6, 7
 COLL_LL8, COLL_LL128, COLL_SENT, COLL_ENC_AUTO = 0, 1, 2, 3

@@ -57,6 +57,7 @@ void fill_base(coll_spec* s) {
   P.nranks = p.n;
   P.enc = p.enc;
   P.reset_mode = p.reset_mode;
+  P.dtype = p.dtype;
   P.ctas_per_rank = p.ctas_per_rank;
   P.timeout_ns = p.timeout_ns;
   P.P = p.P;
@@ -289,8 +290,9 @@ coll_status_t coll_workspace_bytes(const coll_spec_t* s, size_t* bytes) {
 coll_status_t coll_buffer_elems(const coll_spec_t* s, int rank, size_t* in_elems,
                                 size_t* out_elems) {
   if (s == nullptr || rank < 0 || rank >= s->plan.n) return COLL_ERR_INVALID;
-  if (in_elems) *in_elems = (size_t)s->plan.in_elems[rank];
-  if (out_elems) *out_elems = (size_t)s->plan.out_elems[rank];
+  const uint64_t eu = s->plan.dtype == COLL_F32 ? 2 : 1;  // the plan counts 16-bit units
+  if (in_elems) *in_elems = (size_t)(s->plan.in_elems[rank] / eu);
+  if (out_elems) *out_elems = (size_t)(s->plan.out_elems[rank] / eu);
   return COLL_OK;
 }
 

@@ -240,7 +240,7 @@ __device__ __forceinline__ bool fold_task(const RunParams& P, uint32_t wbase, in
       discard_l2_line(src0 + (lane >> 2) * rb + (size_t)rr * kRowBytes +
                       (size_t)(lane & 3) * kLL128LineBytes);
     }
-    const uint4 res = ll128_fold(s, n);
+    const uint4 res = ll128_fold(s, n, P.dtype);
     ll128_store_row<false>(ag + (size_t)rr * kRowBytes, res, lane, nl_row, e);
   }
   cp_async_wait<0>();

@@ -205,7 +205,11 @@ int derive(const DeriveInput& in, Plan& p) {
   if (in.slots != 0 && in.slots != 2 && in.slots != 4) return COLL_ERR_INVALID;
   p.slots = in.slots == 0 ? 2 : in.slots;
   if (n < 1 || n > kMaxRanks) return COLL_ERR_UNSUPPORTED;
-  if (in.dtype != COLL_BF16) return COLL_ERR_UNSUPPORTED;
+  if (in.dtype != COLL_BF16 && in.dtype != COLL_F32) return COLL_ERR_UNSUPPORTED;
+  // Sizes below are kept in 16-bit units: an fp32 element is two of them.
+  // Counts and partitions are given and cut in elements of the dtype.
+  const uint64_t eu = in.dtype == COLL_F32 ? 2 : 1;
+  p.dtype = in.dtype;
   if (in.encoding != COLL_LL8 && in.encoding != COLL_LL128 && in.encoding != COLL_SENT &&
       in.encoding != COLL_ENC_AUTO)
     return COLL_ERR_UNSUPPORTED;
@@ -227,7 +231,7 @@ int derive(const DeriveInput& in, Plan& p) {
   else if (L == COLL_PACKED_V && O == COLL_SCATTERED_V && in.op == COLL_COPY)
     p.kind = CK_ALLGATHER_V;
   else if (L == COLL_SCATTERED_V && O == COLL_TRANSPOSED_V && in.op == COLL_COPY) {
-    if (in.experts > 0) return derive_moe(in, p);
+    if (in.experts > 0) return in.dtype == COLL_BF16 ? derive_moe(in, p) : COLL_ERR_UNSUPPORTED;
     p.kind = CK_ALLTOALL_V;
   } else
     return COLL_ERR_UNSUPPORTED;
@@ -250,23 +254,27 @@ int derive(const DeriveInput& in, Plan& p) {
     }
     if (p.kind != CK_ALLTOALL_V && sum != in.count) return COLL_ERR_INVALID;
     if (p.kind == CK_ALLTOALL_V) count_in = 0;
+    for (uint64_t& v : V) v *= eu;
   }
 
   if (count_in % 8 != 0) return COLL_ERR_ALIGN;
   p.n = n;
-  p.count = count_in;
-  p.shard = shard_elems(count_in, n);
+  p.count = count_in * eu;
+  p.shard = shard_elems(count_in, n) * eu;
   p.timeout_ns = in.timeout_ns ? in.timeout_ns : 200000000ull;
-  if (p.kind == CK_ALLTOALL && p.shard * (uint64_t)n != in.count)
+  if (p.kind == CK_ALLTOALL && shard_elems(count_in, n) * (uint64_t)n != in.count)
     return COLL_ERR_ALIGN;  // the exchange needs equal partitions
 
-  const uint64_t count = count_in, M = p.shard;
+  const uint64_t count = p.count, M = p.shard;
+  // partition k of the (elementwise) partition rule, in 16-bit units
+  auto SB = [&](int k) { return shard_begin(count_in, n, k) * eu; };
+  auto SL = [&](int k) { return shard_len(count_in, n, k) * eu; };
   uint64_t in_bytes_per_rank = 0;
   for (int r = 0; r < n; ++r) {
     switch (p.kind) {
       case CK_ALLREDUCE: p.in_elems[r] = count; p.out_elems[r] = count; break;
-      case CK_REDUCE_SCATTER: p.in_elems[r] = count; p.out_elems[r] = shard_len(count, n, r); break;
-      case CK_ALLGATHER: p.in_elems[r] = shard_len(count, n, r); p.out_elems[r] = count; break;
+      case CK_REDUCE_SCATTER: p.in_elems[r] = count; p.out_elems[r] = SL(r); break;
+      case CK_ALLGATHER: p.in_elems[r] = SL(r); p.out_elems[r] = count; break;
       case CK_ALLTOALL: p.in_elems[r] = count; p.out_elems[r] = count; break;
       case CK_REDUCE_SCATTER_V: p.in_elems[r] = count; p.out_elems[r] = V[r]; break;
       case CK_ALLGATHER_V: p.in_elems[r] = V[r]; p.out_elems[r] = count; break;
@@ -345,7 +353,7 @@ int derive(const DeriveInput& in, Plan& p) {
         at += len;
       }
     } else if (L == COLL_SCATTERED) {
-      for (int k = 0; k < n; ++k) parts.push_back({shard_len(count, n, k), shard_begin(count, n, k)});
+      for (int k = 0; k < n; ++k) parts.push_back({SL(k), SB(k)});
     } else {
       parts.push_back({p.in_elems[r], 0});
     }
@@ -354,7 +362,7 @@ int derive(const DeriveInput& in, Plan& p) {
   const bool twoshot = p.kind == CK_ALLREDUCE && p.algorithm == COLL_TWOSHOT;
   if (twoshot) {
     for (int r = 0; r < n; ++r) {
-      std::vector<std::pair<uint64_t, uint64_t>> parts{{shard_len(count, n, r), 0}};
+      std::vector<std::pair<uint64_t, uint64_t>> parts{{SL(r), 0}};
       p.ag_rank_lines = std::max<uint64_t>(p.ag_rank_lines, build_image(p.enc, parts, p.agseg[r]));
     }
   }
@@ -438,7 +446,7 @@ int derive(const DeriveInput& in, Plan& p) {
             const Seg& s = p.pseg[0][k];
             t.over(s, [&](uint64_t t0, uint64_t nl, uint64_t ne) {
               Item it = make_item(IK_REDUCE, d, 0, s.line0 + t0, nl, ne,
-                                  shard_begin(count, n, k) + t0 * epl);
+                                  SB(k) + t0 * epl);
               set_reset(it, n, ctr.get(1, s.line0 + t0));
               p.items1.push_back(it);
             });
@@ -463,7 +471,7 @@ int derive(const DeriveInput& in, Plan& p) {
             const Seg& s = p.agseg[r][0];
             t2.over(s, [&](uint64_t t0, uint64_t nl, uint64_t ne) {
               Item it = make_item(IK_COPY, d, r, s.line0 + t0, nl, ne,
-                                  shard_begin(count, n, r) + t0 * epl);
+                                  SB(r) + t0 * epl);
               set_reset(it, n, ctr.get(2, ((uint64_t)r << 40) | (s.line0 + t0)));
               p.items2.push_back(it);
             });
@@ -489,7 +497,7 @@ int derive(const DeriveInput& in, Plan& p) {
           const Seg& s = p.pseg[q][0];
           t.over(s, [&](uint64_t t0, uint64_t nl, uint64_t ne) {
             Item it = make_item(IK_COPY, d, q, s.line0 + t0, nl, ne,
-                                shard_begin(count, n, q) + t0 * epl);
+                                SB(q) + t0 * epl);
             set_reset(it, n, ctr.get(3, ((uint64_t)q << 40) | (s.line0 + t0)));
             p.items1.push_back(it);
           });

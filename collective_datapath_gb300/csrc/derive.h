@@ -45,6 +45,7 @@ struct DeriveInput {
 
 struct Plan {
   CollKind kind;
+  int dtype = 0;  // COLL_BF16 / COLL_F32; element counts below are 16-bit units
   int algorithm;  // COLL_ONESHOT / COLL_TWOSHOT for all-reduce, else 0
   int enc;
   int n;

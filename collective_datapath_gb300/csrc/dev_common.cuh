@@ -121,6 +121,32 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return f32_to_bf16_rne(lo) | (f32_to_bf16_rne(hi) << 16);
 }
 
+// Element types (values match COLL_BF16 / COLL_F32 of coll.h).  A 32-bit
+// word holds two bf16 or one fp32.
+constexpr int kDtBF16 = 0, kDtF32 = 1;
+
+// An fp32 result as written: any NaN becomes the canonical quiet NaN.
+__device__ __forceinline__ uint32_t f32_bits(float a) {
+  return a != a ? 0x7FC00000u : __float_as_uint(a);
+}
+
+// Fold of K 32-bit words of every source as fp32, in rank order, binary32
+// round-to-nearest-even, no narrowing.  w[p * K + k] = word k of source p.
+template <int K>
+__device__ __forceinline__ void fold_f32_words(const uint32_t* w, int n, uint32_t* out) {
+  float a[K];
+#pragma unroll
+  for (int k = 0; k < K; ++k) a[k] = __uint_as_float(w[k]);
+#pragma unroll
+  for (int p = 1; p < kMaxRanks; ++p)
+    if (p < n) {
+#pragma unroll
+      for (int k = 0; k < K; ++k) a[k] = __fadd_rn(a[k], __uint_as_float(w[p * K + k]));
+    }
+#pragma unroll
+  for (int k = 0; k < K; ++k) out[k] = f32_bits(a[k]);
+}
+
 // ---- status -----------------------------------------------------------------
 
 __device__ __forceinline__ WsHeader* header(char* ws) {

@@ -144,7 +144,7 @@ __global__ void __launch_bounds__(kThreads, 2) k_fold_ll128(RunParams P) {
         }
         if (!ok) break;
       }
-      const uint4 res = ll128_fold(s, n);
+      const uint4 res = ll128_fold(s, n, P.dtype);
       if (publish) {
         char* dst = image_bytes(P, P.AG, e, it.dst) +
                     (it.out_off + (uint64_t)r * kLL128RowLines) * kLL128LineBytes;
@@ -352,18 +352,14 @@ __global__ void __launch_bounds__(kThreads, 2) k_fold_ll8(RunParams P) {
             s[p] = make_uint4((uint32_t)a, (uint32_t)(a >> 32), (uint32_t)b, (uint32_t)(b >> 32));
           }
         }
-        float a0 = bf16_lo_to_f32(s[0].x), a1 = bf16_hi_to_f32(s[0].x);
-        float a2 = bf16_lo_to_f32(s[0].z), a3 = bf16_hi_to_f32(s[0].z);
+        uint64_t lo[kMaxRanks], hi[kMaxRanks];
 #pragma unroll
-        for (int p = 1; p < kMaxRanks; ++p) {
-          if (p < n) {
-            a0 = __fadd_rn(a0, bf16_lo_to_f32(s[p].x));
-            a1 = __fadd_rn(a1, bf16_hi_to_f32(s[p].x));
-            a2 = __fadd_rn(a2, bf16_lo_to_f32(s[p].z));
-            a3 = __fadd_rn(a3, bf16_hi_to_f32(s[p].z));
-          }
+        for (int p = 0; p < kMaxRanks; ++p) {
+          lo[p] = s[p].x;   // payload words of the two lines
+          hi[p] = s[p].z;
         }
-        const uint32_t w0 = pack_bf16x2(a0, a1), w1 = pack_bf16x2(a2, a3);
+        uint32_t w0, w1;
+        ll8_fold_pair(lo, hi, n, P.dtype, w0, w1);
         if (publish) {
           uint64_t* dst = reinterpret_cast<uint64_t*>(P.ws + P.AG.base + (e & P.AG.slot_mask) * P.AG.slot_bytes +
                                                       (uint64_t)it.dst * P.AG.rank_bytes) +
@@ -489,8 +485,8 @@ __device__ void late_producer(const RunParams& P, uint64_t e, int p, int workers
         int64_t left;
         locate(line, elem0, left);
         const uint2 d = *reinterpret_cast<const uint2*>(in + elem0);
-        st_relaxed_u64(img + line, (uint64_t)sent_sanitize2(d.x) |
-                                       ((uint64_t)sent_sanitize2(d.y) << 32));
+        st_relaxed_u64(img + line, (uint64_t)sent_word(d.x, P.dtype) |
+                                       ((uint64_t)sent_word(d.y, P.dtype) << 32));
       }
       __syncwarp();
       __nanosleep(500);

@@ -210,8 +210,23 @@ __device__ __forceinline__ uint4 ld_relaxed_v4(const char* p) {
   return make_uint4((uint32_t)a, (uint32_t)(a >> 32), (uint32_t)b, (uint32_t)(b >> 32));
 }
 
-// Fold the 8 (k < 7) or 4 (k = 7) bf16 of this lane's chunk over n images.
-__device__ __forceinline__ uint4 ll128_fold(const uint4* s, int n) {
+// Fold the 8 (k < 7) or 4 (k = 7) bf16, or 4 (2) fp32, of this lane's chunk
+// over n images.
+__device__ __forceinline__ uint4 ll128_fold_f32(const uint4* s, int n) {
+  uint32_t w[kMaxRanks * 4], r[4];
+#pragma unroll
+  for (int p = 0; p < kMaxRanks; ++p) {
+    w[4 * p] = s[p].x;
+    w[4 * p + 1] = s[p].y;
+    w[4 * p + 2] = s[p].z;
+    w[4 * p + 3] = s[p].w;
+  }
+  fold_f32_words<4>(w, n, r);
+  return make_uint4(r[0], r[1], r[2], r[3]);
+}
+
+__device__ __forceinline__ uint4 ll128_fold(const uint4* s, int n, int dtype) {
+  if (dtype == kDtF32) return ll128_fold_f32(s, n);
   float a[8];
   a[0] = bf16_lo_to_f32(s[0].x); a[1] = bf16_hi_to_f32(s[0].x);
   a[2] = bf16_lo_to_f32(s[0].y); a[3] = bf16_hi_to_f32(s[0].y);
@@ -298,7 +313,7 @@ __device__ __forceinline__ void ll128_consume_item(const RunParams& P, const Reg
         for (int p = 0; p < kMaxRanks; ++p)
           if (p < n) s[p] = valid ? ld_relaxed_v4(rows[p] + 16 * lane) : make_uint4(0, 0, 0, 0);
       }
-      const uint4 res = ll128_fold(s, n);
+      const uint4 res = ll128_fold(s, n, P.dtype);
       if (publish) {
         char* dst = image_bytes(P, P.AG, epoch, it.dst) +
                     (it.out_off + (uint64_t)r * kLL128RowLines) * kLL128LineBytes;

@@ -69,6 +69,37 @@ __device__ __forceinline__ uint64_t* image_lines(const RunParams& P, const Regio
                                      (uint64_t)rank * R.rank_bytes);
 }
 
+// Fold of the payload words of two lines of every source (lo[p], hi[p]):
+// 4 bf16 or 2 fp32, rank order, fp32 accumulation.
+__device__ __forceinline__ void ll8_fold_pair(const uint64_t* lo, const uint64_t* hi, int n,
+                                              int dtype, uint32_t& w0, uint32_t& w1) {
+  if (dtype == kDtF32) {
+    uint32_t w[kMaxRanks * 2], r[2];
+#pragma unroll
+    for (int p = 0; p < kMaxRanks; ++p) {
+      w[2 * p] = (uint32_t)lo[p];
+      w[2 * p + 1] = (uint32_t)hi[p];
+    }
+    fold_f32_words<2>(w, n, r);
+    w0 = r[0];
+    w1 = r[1];
+    return;
+  }
+  float a0 = bf16_lo_to_f32((uint32_t)lo[0]), a1 = bf16_hi_to_f32((uint32_t)lo[0]);
+  float a2 = bf16_lo_to_f32((uint32_t)hi[0]), a3 = bf16_hi_to_f32((uint32_t)hi[0]);
+#pragma unroll
+  for (int p = 1; p < kMaxRanks; ++p) {
+    if (p < n) {
+      a0 = __fadd_rn(a0, bf16_lo_to_f32((uint32_t)lo[p]));
+      a1 = __fadd_rn(a1, bf16_hi_to_f32((uint32_t)lo[p]));
+      a2 = __fadd_rn(a2, bf16_lo_to_f32((uint32_t)hi[p]));
+      a3 = __fadd_rn(a3, bf16_hi_to_f32((uint32_t)hi[p]));
+    }
+  }
+  w0 = pack_bf16x2(a0, a1);
+  w1 = pack_bf16x2(a2, a3);
+}
+
 // Groups a thread keeps in flight per step (stage and copy).
 constexpr int kGroupsInFlight = 4;
 
@@ -133,18 +164,8 @@ __device__ __forceinline__ void ll8_consume_item(const RunParams& P, const Regio
           ld_relaxed_v2u64(src, lo[p], hi[p]);
         }
       if (!ok) break;
-      float a0 = bf16_lo_to_f32((uint32_t)lo[0]), a1 = bf16_hi_to_f32((uint32_t)lo[0]);
-      float a2 = bf16_lo_to_f32((uint32_t)hi[0]), a3 = bf16_hi_to_f32((uint32_t)hi[0]);
-#pragma unroll
-      for (int p = 1; p < kMaxRanks; ++p) {
-        if (p < n) {
-          a0 = __fadd_rn(a0, bf16_lo_to_f32((uint32_t)lo[p]));
-          a1 = __fadd_rn(a1, bf16_hi_to_f32((uint32_t)lo[p]));
-          a2 = __fadd_rn(a2, bf16_lo_to_f32((uint32_t)hi[p]));
-          a3 = __fadd_rn(a3, bf16_hi_to_f32((uint32_t)hi[p]));
-        }
-      }
-      const uint32_t w0 = pack_bf16x2(a0, a1), w1 = pack_bf16x2(a2, a3);
+      uint32_t w0, w1;
+      ll8_fold_pair(lo, hi, n, P.dtype, w0, w1);
       if (sole) {
 #pragma unroll
         for (int p = 0; p < kMaxRanks; ++p)

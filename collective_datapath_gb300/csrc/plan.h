@@ -129,6 +129,7 @@ struct RunParams {
   uint16_t* out[kMaxRanks];       // rank outputs
   int nranks;
   int enc;
+  int dtype;                      // kDtBF16 / kDtF32: how folds read a 32-bit word
   int reset_mode;                 // COLL_RESET_* (LL8 only; LL128 needs none)
   int ctas_per_rank;              // fused path: CTAs bound to each rank
   uint64_t timeout_ns;

@@ -32,9 +32,19 @@ __device__ __forceinline__ uint32_t sent_sanitize2(uint32_t w) {
   return lo | (hi << 16);
 }
 
-__device__ __forceinline__ void sent_store(uint64_t* p, uint4 v) {
-  st_relaxed_v2u64(p, (uint64_t)sent_sanitize2(v.x) | ((uint64_t)sent_sanitize2(v.y) << 32),
-                   (uint64_t)sent_sanitize2(v.z) | ((uint64_t)sent_sanitize2(v.w) << 32));
+// An fp32 element equal to the reserved word 0xFFFFFFFF becomes 0x7FC00000.
+__device__ __forceinline__ uint32_t sent_sanitize_f32(uint32_t w) {
+  return w == 0xFFFFFFFFu ? 0x7FC00000u : w;
+}
+
+// A 32-bit input word as published: two bf16 or one fp32 sanitised.
+__device__ __forceinline__ uint32_t sent_word(uint32_t w, int dtype) {
+  return dtype == kDtF32 ? sent_sanitize_f32(w) : sent_sanitize2(w);
+}
+
+__device__ __forceinline__ void sent_store(uint64_t* p, uint4 v, int dtype) {
+  st_relaxed_v2u64(p, (uint64_t)sent_word(v.x, dtype) | ((uint64_t)sent_word(v.y, dtype) << 32),
+                   (uint64_t)sent_word(v.z, dtype) | ((uint64_t)sent_word(v.w, dtype) << 32));
 }
 
 __device__ __forceinline__ void sent_rearm(uint64_t* p) {
@@ -80,16 +90,29 @@ __device__ __forceinline__ void sent_stage_tile(const RunParams& P, const StageI
     for (int j = 0; j < kGroupsInFlight; ++j) {
       const uint32_t g = g0 + j * blockDim.x;
       if (g < ngroups) {
-        sent_store(img + 2 * (size_t)g, v[j]);
+        sent_store(img + 2 * (size_t)g, v[j], P.dtype);
         if (deferred) sent_rearm(other + 2 * (size_t)g);
       }
     }
   }
 }
 
-// Fold of eight elements (four words) of every source, rank order, fp32,
-// one rounding.
-__device__ __forceinline__ uint4 sent_fold8(const uint64_t* lo, const uint64_t* hi, int n) {
+// Fold of four words of every source (eight bf16 or four fp32), rank
+// order, fp32 accumulation; bf16 is rounded once at the end.
+__device__ __forceinline__ uint4 sent_fold8(const uint64_t* lo, const uint64_t* hi, int n,
+                                            int dtype) {
+  if (dtype == kDtF32) {
+    uint32_t w[kMaxRanks * 4], r[4];
+#pragma unroll
+    for (int p = 0; p < kMaxRanks; ++p) {
+      w[4 * p] = (uint32_t)lo[p];
+      w[4 * p + 1] = (uint32_t)(lo[p] >> 32);
+      w[4 * p + 2] = (uint32_t)hi[p];
+      w[4 * p + 3] = (uint32_t)(hi[p] >> 32);
+    }
+    fold_f32_words<4>(w, n, r);
+    return make_uint4(r[0], r[1], r[2], r[3]);
+  }
   float a[8];
   const uint32_t w0[4] = {(uint32_t)lo[0], (uint32_t)(lo[0] >> 32), (uint32_t)hi[0],
                           (uint32_t)(hi[0] >> 32)};
@@ -141,7 +164,7 @@ __device__ __forceinline__ void sent_consume_item(const RunParams& P, const Regi
           ld_relaxed_v2u64(src, lo[p], hi[p]);
         }
       if (!ok) break;
-      const uint4 res = sent_fold8(lo, hi, n);
+      const uint4 res = sent_fold8(lo, hi, n, P.dtype);
       if (sole) {
 #pragma unroll
         for (int p = 0; p < kMaxRanks; ++p)

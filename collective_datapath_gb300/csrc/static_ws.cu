@@ -133,6 +133,7 @@ extern "C" coll_status_t coll_allreduce_static(int nranks, size_t count,
   }
   P.nranks = nranks;
   P.enc = ENC_LL8;
+  P.dtype = kDtBF16;
   P.reset_mode = kResetNone;
   P.ctas_per_rank = B;
   P.timeout_ns = 200000000ull;

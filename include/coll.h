@@ -85,7 +85,14 @@ typedef enum {
  * or reduce corresponding elements. */
 typedef enum { COLL_COPY = 0, COLL_REDUCE = 1 } coll_op_t;
 
-typedef enum { COLL_BF16 = 0 } coll_dtype_t;
+typedef enum { COLL_BF16 = 0, COLL_F32 = 1 } coll_dtype_t;
+/* COLL_F32 (flash-comm §4.1 admits bf16 and fp32 tensors): the fold is the
+ * same left fold in rank order in binary32 with no final narrowing; a NaN
+ * result is written as 0x7FC00000.  `count`, `vcounts` and the element
+ * counts of coll_buffer_elems are fp32 elements; every count is still a
+ * multiple of 8.  Lines carry the same bytes as for bf16 (an LL8 line one
+ * fp32, an LL128 line 30, a sentinel pack 2, whose reserved pattern is
+ * 0xFFFFFFFF, published as 0x7FC00000).  MoE dispatch is bf16 only. */
 
 typedef enum {
     COLL_OK = 0,

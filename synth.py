@@ -36,6 +36,8 @@ TAG_INTEGER = 3
 TAG_TOPK = 4
 TAG_STALE = 5
 TAG_BITS = 6
+TAG_NORMAL_F32 = 7
+TAG_BITS32 = 8
 
 
 def _gen(seed: int, tag: int, *index: int) -> np.random.Generator:
@@ -77,6 +79,26 @@ def integer_bf16(seed: int, n: int, lo: int, hi: int, *index: int) -> np.ndarray
     g = _gen(seed, TAG_INTEGER, *index)
     v = g.integers(lo, hi + 1, size=n).astype(np.float32)
     return _f32_to_bf16_bits(v)
+
+
+def normal_f32(seed: int, n: int, *index: int) -> np.ndarray:
+    """n fp32 bit patterns (uint32) drawn i.i.d. normal(0, 1) (Box-Muller),
+    rounded to binary32 by numpy's cast."""
+    g = _gen(seed, TAG_NORMAL_F32, *index)
+    half = (n + 1) // 2
+    u1 = 1.0 - g.random(half)
+    u2 = g.random(half)
+    r = np.sqrt(-2.0 * np.log(u1))
+    z = np.empty(2 * half, dtype=np.float64)
+    z[0::2] = r * np.cos(2.0 * np.pi * u2)
+    z[1::2] = r * np.sin(2.0 * np.pi * u2)
+    return z[:n].astype(np.float32).view(np.uint32)
+
+
+def random_bits32(seed: int, n: int, *index: int) -> np.ndarray:
+    """n arbitrary 32-bit patterns (any fp32 value, NaN and Inf included)."""
+    g = _gen(seed, TAG_BITS32, *index)
+    return g.integers(0, 1 << 32, size=n, dtype=np.uint64).astype(np.uint32)
 
 
 def random_bits16(seed: int, n: int, *index: int) -> np.ndarray:

@@ -91,8 +91,31 @@ def _decode(enc, lines, elems, epoch):
     return out
 
 
-def interpret(cd, spec, enc, n, ins, epoch=5):
-    """Run the derived items on the CPU: stage, phase 1, phase 2."""
+def _fold_units(xs, f32):
+    """Oracle fold of decoded 16-bit units (fp32: pairs of units)."""
+    if not f32:
+        return oracle.allreduce(xs)[0]
+    ys = [np.ascontiguousarray(x).view(np.uint32) for x in xs]
+    return oracle.allreduce_f32(ys)[0].view(np.uint16)
+
+
+def _encode_units(enc, x, epoch, f32):
+    if enc == 2 and f32:
+        return oracle.sent_encode_f32(np.ascontiguousarray(x).view(np.uint32))
+    return _encode(enc, x, epoch)
+
+
+def _decode_units(enc, lines, elems, epoch, f32):
+    if enc == 2 and f32:
+        out, rej = oracle.sent_decode_f32(lines, elems // 2)
+        assert rej == 0
+        return out.view(np.uint16)
+    return _decode(enc, lines, elems, epoch)
+
+
+def interpret(cd, spec, enc, n, ins, epoch=5, f32=False):
+    """Run the derived items on the CPU: stage, phase 1, phase 2.  `ins` are
+    16-bit units (an fp32 element is two of them)."""
     st = cd.coll_debug_items(spec, 0)
     p1 = cd.coll_debug_items(spec, 1)
     p2 = cd.coll_debug_items(spec, 2)
@@ -104,21 +127,22 @@ def interpret(cd, spec, enc, n, ins, epoch=5):
     AG = [np.zeros((ag_lines, width) if enc == 1 else ag_lines, dtype=dt) for _ in range(n)]
     for rank, _, _, _, _, nl, ne, dst_line, in_elem, _ in st:
         assert dst_line % 4 == 0
-        P[rank][dst_line:dst_line + nl] = _encode(enc, ins[rank][in_elem:in_elem + ne], epoch)
-    outs = [np.full(cd.coll_buffer_elems(spec, r)[1], 0xDEAD, dtype=np.uint16)
-            for r in range(n)]
+        P[rank][dst_line:dst_line + nl] = _encode_units(enc, ins[rank][in_elem:in_elem + ne],
+                                                        epoch, f32)
+    outs = [np.full(cd.coll_buffer_elems(spec, r)[1] * (2 if f32 else 1), 0xDEAD,
+                    dtype=np.uint16) for r in range(n)]
     written = [np.zeros(o.size, dtype=np.int32) for o in outs]
 
     def run(items, images):
         for kind, flags, dst, src, readers, nl, ne, sl, off, ctr in items:
             assert sl % 4 == 0
             if kind == 0:
-                xs = [_decode(enc, images[q][sl:sl + nl], ne, epoch) for q in range(n)]
-                res = oracle.allreduce(xs)[0]
+                xs = [_decode_units(enc, images[q][sl:sl + nl], ne, epoch, f32) for q in range(n)]
+                res = _fold_units(xs, f32)
             else:
-                res = _decode(enc, images[src][sl:sl + nl], ne, epoch)
+                res = _decode_units(enc, images[src][sl:sl + nl], ne, epoch, f32)
             if flags & 1:
-                AG[dst][off:off + nl] = _encode(enc, res, epoch)
+                AG[dst][off:off + nl] = _encode_units(enc, res, epoch, f32)
             else:
                 outs[dst][off:off + ne] = res
                 written[dst][off:off + ne] += 1
@@ -264,3 +288,58 @@ def test_sentinel_needs_a_rearm(cd):
     for mode in (cd.COLL_RESET_FUSED, cd.COLL_RESET_KERNEL, cd.COLL_RESET_DEFERRED):
         s = cd.coll_spec_create(*cd.ALLREDUCE, 8, 64, encoding=cd.COLL_SENT, reset_mode=mode)
         cd.coll_destroy(s)
+
+
+
+# ---- fp32 tensors ---------------------------------------------------------------
+
+F32_CASES = [
+    ("ALLREDUCE", 8, 8 * 1024, 0, 1, 1), ("ALLREDUCE", 8, 8 * 1024, 0, 2, 2),
+    ("ALLREDUCE", 3, 600, 1, 2, 2), ("ALLREDUCE", 8, 8 * 480, 1, 2, 1),
+    ("ALLREDUCE", 5, 5 * 96 + 8, 2, 1, 1), ("ALLREDUCE", 8, 8 * 512, 2, 2, 2),
+    ("REDUCE_SCATTER", 8, 8 * 600, 1, 0, 2), ("REDUCE_SCATTER", 3, 3 * 40 + 16, 2, 0, 1),
+    ("ALLGATHER", 4, 4 * 104 + 8, 1, 0, 1), ("ALLGATHER", 8, 8 * 256, 2, 0, 2),
+    ("ALLTOALL", 8, 8 * 240, 1, 0, 2), ("ALLTOALL", 4, 4 * 64, 0, 0, 1),
+]
+
+
+@pytest.mark.parametrize("name,n,count,enc,algo,path", F32_CASES)
+def test_derived_f32_schedule_computes_the_oracle_result(cd, name, n, count, enc, algo, path):
+    spec = cd.coll_spec_create(*getattr(cd, name), n, count, dtype=cd.COLL_F32, encoding=enc,
+                               algorithm=algo, path=path)
+    try:
+        ins32 = [synth.normal_f32(3, cd.coll_buffer_elems(spec, r)[0], n, count, r)
+                 for r in range(n)]
+        ins32[0][::37] = 0xFFFFFFFF                       # the reserved sentinel word
+        ins32[1 % n][5::41] = 0x7FC00123                  # a NaN with a payload
+        got = interpret(cd, spec, enc, n, [x.view(np.uint16) for x in ins32], f32=True)
+        san = [oracle.sent_sanitize_f32(x) for x in ins32] if enc == 2 else ins32
+        if name == "ALLREDUCE":
+            want = oracle.allreduce_f32(ins32)
+        elif name == "REDUCE_SCATTER":
+            want = oracle.reduce_scatter_f32(ins32)
+        elif name == "ALLGATHER":
+            want = [np.concatenate(san) for _ in range(n)]
+        else:
+            m = oracle.shard_elems(count, n)
+            want = [np.concatenate([san[p][d * m:(d + 1) * m] for p in range(n)]) for d in range(n)]
+        for r in range(n):
+            assert np.array_equal(got[r].view(np.uint32), want[r]), f"rank {r}"
+    finally:
+        cd.coll_destroy(spec)
+
+
+def test_f32_element_counts_and_admission(cd):
+    s = cd.coll_spec_create(*cd.REDUCE_SCATTER, 3, 3 * 40 + 16, dtype=cd.COLL_F32)
+    assert [cd.coll_buffer_elems(s, r) for r in range(3)] == [(136, 48), (136, 48), (136, 40)]
+    cd.coll_destroy(s)
+    with pytest.raises(cd.CollError) as e:
+        cd.coll_spec_create(*cd.ALLREDUCE, 8, 12, dtype=cd.COLL_F32)
+    assert e.value.status == cd.COLL_ERR_ALIGN
+    with pytest.raises(cd.CollError) as e:
+        cd.coll_spec_create(*cd.MOE_DISPATCH, 2, 0, dtype=cd.COLL_F32, encoding=cd.COLL_LL128,
+                            tokens=4, hidden=8, topk=1, experts=2)
+    assert e.value.status == cd.COLL_ERR_UNSUPPORTED
+    with pytest.raises(cd.CollError) as e:
+        cd.coll_spec_create(*cd.ALLREDUCE, 8, 64, dtype=7)
+    assert e.value.status == cd.COLL_ERR_UNSUPPORTED
