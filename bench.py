@@ -489,6 +489,38 @@ def streamed_row(cd, count, stream, steps=5) -> dict:
                         for k in range(3)]}
 
 
+def f32_row(cd, nbytes, stream, steps=5) -> dict:
+    """8 ranks x `nbytes` of fp32 per rank: twoshot all-reduce, LL128 lines,
+    the composed launch (the bench workload with fp32 elements: the same
+    bytes, folds in binary32 with no narrowing)."""
+    import torch
+
+    n = N_RANKS
+    count = nbytes // 4
+    coll = cd.Collective(cd.ALLREDUCE, n, count, dtype=cd.COLL_F32, encoding=cd.COLL_LL128,
+                         algorithm=cd.COLL_TWOSHOT, path=cd.COLL_PATH_COMPOSED)
+    ins = [x.view(torch.int32) for x in make_inputs(2 * count, 14)]
+    outs = [torch.empty(count, dtype=torch.int32, device="cuda") for _ in range(n)]
+    with torch.cuda.stream(stream):
+        for _ in range(2):
+            coll.run(ins, outs, stream)
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(steps):
+            coll.run(ins, outs, stream)
+        e1.record(stream)
+        stream.synchronize()
+    ms = e0.elapsed_time(e1) / steps
+    b = bytes_allreduce_twoshot(n, float(nbytes), EPS_LL128)
+    st = coll.status(stream)[0]
+    coll.close()
+    del coll, ins, outs
+    torch.cuda.empty_cache()
+    return {"ms": round(ms, 4), "GB/s": round(b / ms / 1e6, 1), "algorithmic_bytes": b,
+            "status": st}
+
+
 def sentinel_row(cd, count, stream, steps=5) -> dict:
     """8 ranks x `count` bf16 all-reduce, twoshot, sentinel packs, streamed.
     Algorithmic bytes are the LL form with epsilon = 1 (no readiness bytes);
@@ -768,6 +800,7 @@ def main() -> int:
             "all_gather_v_zipf_256MiB": v_row(cd, "ALLGATHER_V", 256 << 20, stream),
             "all_to_all_v_zipf_256MiB": v_row(cd, "ALLTOALL_V", 256 << 20, stream),
             "allreduce_256MiB_sentinel_twoshot": sentinel_row(cd, count, stream),
+            "allreduce_256MiB_f32_composed": f32_row(cd, 256 << 20, stream),
         }
         line["latency_us_per_op"] = latency_sweep(cd, stream)
         if world == 1:
