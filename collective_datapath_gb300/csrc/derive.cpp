@@ -294,12 +294,14 @@ int derive(const DeriveInput& in, Plan& p) {
   // takes the calibrated policy entry for its group and size (flash-comm
   // §3.2 and §4.1: a constant-time lookup in a table measured offline).
   int enc = in.encoding, algo = in.algorithm, path = in.path;
+  int ctas = in.ctas;  // the launch shape: 0 = the default width
   if (p.kind == CK_ALLREDUCE && enc == COLL_ENC_AUTO && algo == COLL_ALGO_AUTO &&
       path == COLL_PATH_AUTO) {
     const PolicyEntry* e = policy_lookup(n, in_bytes_per_rank);
     enc = e->enc;
     algo = e->algo;
     path = e->path;
+    if (ctas == 0) ctas = e->ctas;
   }
   // Otherwise an AUTO encoding halves the bytes of small messages with
   // sentinel packs and uses LL128 lines above 1 MiB per rank.
@@ -369,14 +371,21 @@ int derive(const DeriveInput& in, Plan& p) {
 
   // CTAs per rank on the fused path: every worker CTA plus one late producer
   // per rank must be co-resident (cooperative launch).
-  const int sms = in.sms > 0 ? in.sms : 152;
-  int cap = in.fused_capacity > 0 ? std::min(in.fused_capacity, sms) : sms;
-  // A power of two: the twoshot's published tiles then line up with the
-  // tiles its gathers read (on GB300, 16 CTAs per rank at 8 ranks run a
+  // By default one CTA per SM; a requested `ctas` (the option, or the policy
+  // entry's launch shape) may go up to every co-resident CTA.  Always a
+  // power of two per rank: the twoshot's published tiles then line up with
+  // the tiles its gathers read (on GB300, 16 CTAs per rank at 8 ranks run a
   // 1 MiB twoshot in 13.5 us, 17 or 18 CTAs in 19-20 us).
-  int B = std::max(1, cap / n - 1);
-  while (B & (B - 1)) B &= B - 1;
-  if (in.ctas > 0) B = std::max(1, std::min(B, in.ctas / n));
+  const int sms = in.sms > 0 ? in.sms : 152;
+  const int cap = in.fused_capacity > 0 ? in.fused_capacity : sms;
+  auto pow2_floor = [](int v) {
+    v = std::max(1, v);
+    while (v & (v - 1)) v &= v - 1;
+    return v;
+  };
+  const int B_all = pow2_floor(cap / n - 1);
+  int B = std::min(B_all, pow2_floor(std::min(cap, sms) / n - 1));
+  if (ctas > 0) B = std::min(B_all, pow2_floor(ctas / n));
 
   // Tile sizes (lines, multiples of 4).
   auto fused = p.path == COLL_PATH_FUSED;

@@ -11,27 +11,28 @@ namespace coll {
 struct PolicyEntry {
   uint64_t max_bytes;
   int enc, algo, path;
+  int ctas;  // launch shape of the one-launch path (0 = one CTA per SM)
 };
 
 constexpr PolicyEntry kPolicy2[] = {
-    {16384ull, 0, 1, 1},  // LL8/oneshot/fused
-    {1097728ull, 2, 1, 1},  // SENT/oneshot/fused
-    {5931008ull, 2, 2, 1},  // SENT/twoshot/fused
-    {16777216ull, 1, 1, 2},  // LL128/oneshot/streamed
-    {UINT64_MAX, 1, 2, 2},  // LL128/twoshot/streamed
+    {16384ull, 0, 1, 1, 0},  // LL8/oneshot/fused
+    {1097728ull, 2, 1, 1, 0},  // SENT/oneshot/fused
+    {5931008ull, 2, 2, 1, 0},  // SENT/twoshot/fused
+    {16777216ull, 1, 1, 2, 0},  // LL128/oneshot/streamed
+    {UINT64_MAX, 1, 2, 2, 0},  // LL128/twoshot/streamed
 };
 constexpr PolicyEntry kPolicy4[] = {
-    {8192ull, 0, 1, 1},  // LL8/oneshot/fused
-    {802816ull, 2, 1, 1},  // SENT/oneshot/fused
-    {4456448ull, 2, 2, 1},  // SENT/twoshot/fused
-    {9011200ull, 1, 1, 2},  // LL128/oneshot/streamed
-    {UINT64_MAX, 1, 2, 2},  // LL128/twoshot/streamed
+    {8192ull, 0, 1, 1, 0},  // LL8/oneshot/fused
+    {802816ull, 2, 1, 1, 0},  // SENT/oneshot/fused
+    {4456448ull, 2, 2, 1, 0},  // SENT/twoshot/fused
+    {9011200ull, 1, 1, 2, 0},  // LL128/oneshot/streamed
+    {UINT64_MAX, 1, 2, 2, 0},  // LL128/twoshot/streamed
 };
 constexpr PolicyEntry kPolicy8[] = {
-    {376832ull, 2, 1, 1},  // SENT/oneshot/fused
-    {4194304ull, 2, 2, 1},  // SENT/twoshot/fused
-    {34619392ull, 1, 2, 2},  // LL128/twoshot/streamed
-    {UINT64_MAX, 1, 2, 3},  // LL128/twoshot/composed
+    {376832ull, 2, 1, 1, 0},  // SENT/oneshot/fused
+    {4194304ull, 2, 2, 1, 0},  // SENT/twoshot/fused
+    {34619392ull, 1, 2, 2, 0},  // LL128/twoshot/streamed
+    {UINT64_MAX, 1, 2, 3, 0},  // LL128/twoshot/composed
 };
 
 // group sizes with a table, in increasing order

@@ -42,19 +42,27 @@ ALGO_NAMES = {ONESHOT: "oneshot", TWOSHOT: "twoshot"}
 PATH_NAMES = {FUSED: "fused", STREAMED: "streamed", COMPOSED: "composed"}
 
 
+# Launch shape of the one-launch path: 0 = one CTA per SM (the default),
+# WIDE = every co-resident CTA (the library clamps the request).
+WIDE = 1024
+
+
 @dataclass(frozen=True, order=True)
 class Candidate:
     enc: int
     algo: int
     path: int
+    ctas: int = 0
 
     def name(self) -> str:
-        return f"{ENC_NAMES[self.enc]}/{ALGO_NAMES[self.algo]}/{PATH_NAMES[self.path]}"
+        shape = "/wide" if self.ctas else ""
+        return f"{ENC_NAMES[self.enc]}/{ALGO_NAMES[self.algo]}/{PATH_NAMES[self.path]}{shape}"
 
 
 def candidates_for(nbytes: int) -> list[Candidate]:
     """The protocols worth measuring at one size (bytes per rank): one
-    cooperative launch only up to 4 MiB, the composed launch from 1 MiB."""
+    cooperative launch only up to 4 MiB (in two launch shapes), the composed
+    launch from 1 MiB."""
     out = []
     for enc in (LL8, SENT, LL128):
         for algo in (ONESHOT, TWOSHOT):
@@ -66,6 +74,8 @@ def candidates_for(nbytes: int) -> list[Candidate]:
                 if enc == LL128 and path == FUSED:
                     continue
                 out.append(Candidate(enc, algo, path))
+                if path == FUSED:
+                    out.append(Candidate(enc, algo, path, WIDE))
     return out
 
 
@@ -172,6 +182,7 @@ def header_text(tables: dict[int, list[tuple[int, Candidate]]], note: str) -> st
         "struct PolicyEntry {",
         "  uint64_t max_bytes;",
         "  int enc, algo, path;",
+        "  int ctas;  // launch shape of the one-launch path (0 = one CTA per SM)",
         "};",
         "",
     ]
@@ -179,7 +190,7 @@ def header_text(tables: dict[int, list[tuple[int, Candidate]]], note: str) -> st
         lines.append(f"constexpr PolicyEntry kPolicy{n}[] = {{")
         for m, c in tables[n]:
             mx = "UINT64_MAX" if m >= (1 << 64) - 1 else f"{m}ull"
-            lines.append(f"    {{{mx}, {c.enc}, {c.algo}, {c.path}}},  // {c.name()}")
+            lines.append(f"    {{{mx}, {c.enc}, {c.algo}, {c.path}, {c.ctas}}},  // {c.name()}")
         lines.append("};")
     lines.append("")
     lines.append("// group sizes with a table, in increasing order")
@@ -209,9 +220,11 @@ def parse_header(text: str) -> dict[int, list[tuple[int, Candidate]]]:
             tables[cur] = []
         elif cur is not None and ln.startswith("{"):
             body = ln[1:ln.index("}")]
-            m, e, a, p = (x.strip() for x in body.split(","))
+            fields = [x.strip() for x in body.split(",")]
+            m, e, a, p = fields[:4]
+            w = int(fields[4]) if len(fields) > 4 else 0
             mx = (1 << 64) - 1 if m == "UINT64_MAX" else int(m.rstrip("ul"))
-            tables[cur].append((mx, Candidate(int(e), int(a), int(p))))
+            tables[cur].append((mx, Candidate(int(e), int(a), int(p), w)))
         elif ln.startswith("};"):
             cur = None
     return tables
@@ -225,7 +238,7 @@ def time_op(cd, n: int, nbytes: int, cand: Candidate, stream) -> float:
 
     count = nbytes // 2
     coll = cd.Collective(cd.ALLREDUCE, n, count, encoding=cand.enc, algorithm=cand.algo,
-                         path=cand.path)
+                         path=cand.path, ctas=cand.ctas)
     g = torch.Generator(device="cuda")
     g.manual_seed(nbytes + n)
     ins = [(torch.rand(count, generator=g, device="cuda") * 8 - 4).to(torch.bfloat16)
