@@ -362,13 +362,13 @@ def latency_sweep(cd, stream, only_T=None, only_variant=None, encoding=None) -> 
     return out
 
 
-def bandwidth_row(cd, triple, count_in_out, kind, stream, steps=5) -> dict:
+def bandwidth_row(cd, triple, count_in_out, kind, stream, steps=5, path=None) -> dict:
     import torch
 
     n = N_RANKS
     count = count_in_out
     coll = cd.Collective(triple, n, count, encoding=cd.COLL_LL128,
-                         path=cd.COLL_PATH_STREAMED)
+                         path=cd.COLL_PATH_STREAMED if path is None else path)
     ins = make_inputs(max(coll.elems(r)[0] for r in range(n)), 11)
     ins = [x[:coll.elems(r)[0]] for r, x in enumerate(ins)]
     outs = [torch.empty(max(coll.elems(r)[1], 8), dtype=torch.int16, device="cuda")
@@ -385,7 +385,12 @@ def bandwidth_row(cd, triple, count_in_out, kind, stream, steps=5) -> dict:
         stream.synchronize()
     ms = e0.elapsed_time(e1) / steps
     s = count * 2.0
-    b = bytes_reduce_scatter(n, s, EPS_LL128) if kind == "rs" else bytes_all_gather(n, s, EPS_LL128)
+    if kind == "rs":
+        b = bytes_reduce_scatter(n, s, EPS_LL128)
+    elif kind == "a2a":
+        b = 2 * n * s * (1 + EPS_LL128)
+    else:
+        b = bytes_all_gather(n, s, EPS_LL128)
     st = coll.status(stream)[0]
     coll.close()
     del coll, ins, outs
@@ -794,7 +799,12 @@ def main() -> int:
             **({"allreduce_256MiB_streamed_three_launches": streamed_row(cd, count, stream)}
                if composed else {}),
             "reduce_scatter_256MiB": bandwidth_row(cd, cd.REDUCE_SCATTER, count, "rs", stream),
+            "reduce_scatter_256MiB_composed": bandwidth_row(cd, cd.REDUCE_SCATTER, count, "rs",
+                                                            stream, path=cd.COLL_PATH_COMPOSED),
             "all_gather_256MiB": bandwidth_row(cd, cd.ALLGATHER, count, "ag", stream),
+            "all_to_all_256MiB": bandwidth_row(cd, cd.ALLTOALL, count, "a2a", stream),
+            "all_to_all_256MiB_composed": bandwidth_row(cd, cd.ALLTOALL, count, "a2a", stream,
+                                                        path=cd.COLL_PATH_COMPOSED),
             "moe_dispatch_8x4096x7168_top8of256": moe_row(cd, stream),
             "reduce_scatter_v_zipf_256MiB": v_row(cd, "REDUCE_SCATTER_V", 256 << 20, stream),
             "all_gather_v_zipf_256MiB": v_row(cd, "ALLGATHER_V", 256 << 20, stream),

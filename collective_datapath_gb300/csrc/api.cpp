@@ -149,7 +149,10 @@ cudaError_t launched(coll_spec* s, cudaError_t e, cudaStream_t st) {
 ComposedParams composed_shape(const coll_spec* s) {
   const Plan& p = s->plan;
   ComposedParams q{};
-  int chunk = 256, lag = 28, discard = 1, variant = 0, lag2 = -1;
+  // defaults measured at 8 x 256 MiB: all-reduce 256-line chunks, lag 28;
+  // reduce-scatter and all-to-all 128-line chunks, lag 40
+  const bool ar = p.kind == CK_ALLREDUCE;
+  int chunk = ar ? 256 : 128, lag = ar ? 28 : 40, discard = 1, variant = 0, lag2 = -1;
   if (const char* env = std::getenv("COLL_COMPOSED_SHAPE"))
     std::sscanf(env, "%d,%d,%d,%d,%d", &chunk, &lag, &discard, &variant, &lag2);
   // a power of two of at least kComposedMinChunk lines (rows per chunk are
@@ -165,6 +168,7 @@ ComposedParams composed_shape(const coll_spec* s) {
   q.lag2 = lag2 < 1 ? q.lag : lag2;
   q.discard = discard;
   q.variant = variant >= 0 && variant <= 2 ? variant : 0;
+  q.mode = p.kind == CK_REDUCE_SCATTER ? 1 : (p.kind == CK_ALLTOALL ? 2 : 0);
   char* f = s->ws + p.off_cflags;
   q.flag_stage = reinterpret_cast<uint64_t*>(f);
   q.flag_fold = q.flag_stage + p.composed_max_chunks * p.n;

@@ -132,6 +132,20 @@ __device__ __forceinline__ void fill_gather_piece(const RunParams& P, Piece* pc,
                                                                   : (int64_t)P.cp.chunk_lines * kLL128Elems);
 }
 
+// All-to-all: destination d copies segment d of every source r.
+__device__ __forceinline__ void fill_a2a_piece(const RunParams& P, Piece* pc, int c, int d,
+                                               uint64_t e) {
+  const int r = threadIdx.x;
+  const uint32_t t0 = (uint32_t)c * P.cp.chunk_lines;
+  pc[r].src = image_bytes(P, P.P, e, r) + (P.seg_line0[d] + t0) * kLL128LineBytes;
+  pc[r].dst = reinterpret_cast<char*>(P.out[d] + P.seg_in0[r] + (uint64_t)t0 * kLL128Elems);
+  pc[r].nl = chunk_lines_of(P, d, t0);
+  const int64_t ld = (int64_t)P.seg_elems[d] - (int64_t)t0 * kLL128Elems;
+  pc[r].left = (int)(ld < (int64_t)P.cp.chunk_lines * kLL128Elems
+                         ? ld
+                         : (int64_t)P.cp.chunk_lines * kLL128Elems);
+}
+
 template <int kCWarps, int kCRing>
 __device__ __forceinline__ void stage_task(const Piece* pc, uint32_t wbase, int lane, int warp,
                                            int n, int rsh, uint64_t e) {
@@ -173,9 +187,11 @@ __device__ __forceinline__ void stage_task(const Piece* pc, uint32_t wbase, int 
   __syncwarp();
 }
 
+// Fold chunk c of partition r over the N staged images; publish it as lines
+// of owner r (all-reduce) or write it into rank r's output (reduce-scatter).
 template <int kCWarps, int kCRing>
 __device__ __forceinline__ bool fold_task(const RunParams& P, uint32_t wbase, int lane, int warp,
-                                          int c, int r, uint64_t e) {
+                                          int c, int r, uint64_t e, bool to_out) {
   constexpr int kCFoldStages = kCRing / kMaxRanks;  // rows of all N images per warp
   const int n = P.nranks;
   const uint32_t t0 = (uint32_t)c * P.cp.chunk_lines;
@@ -241,7 +257,13 @@ __device__ __forceinline__ bool fold_task(const RunParams& P, uint32_t wbase, in
                       (size_t)(lane & 3) * kLL128LineBytes);
     }
     const uint4 res = ll128_fold(s, n, P.dtype);
-    ll128_store_row<false>(ag + (size_t)rr * kRowBytes, res, lane, nl_row, e);
+    if (to_out) {
+      const uint64_t line = (uint64_t)t0 + (uint64_t)rr * kLL128RowLines;
+      ll128_write_payload(P.out[r] + line * kLL128Elems, res, lane,
+                          (int64_t)P.seg_elems[r] - (int64_t)line * kLL128Elems);
+    } else {
+      ll128_store_row<false>(ag + (size_t)rr * kRowBytes, res, lane, nl_row, e);
+    }
   }
   cp_async_wait<0>();
   __syncwarp();
@@ -326,8 +348,11 @@ __global__ void __launch_bounds__(kCWarps * 32, kMinBlocks) k_composed_ll128(Run
   const int n = P.nranks;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int slot = (int)(e & 1);
-  const int per_step = 3 * n;
-  const int ntasks = ((int)Q.nchunks + Q.lag + Q.lag2) * per_step;
+  // all-reduce: stage, fold + publish, gather; reduce-scatter: stage, fold
+  // into the outputs; all-to-all: stage, copy into the outputs
+  const int kinds = Q.mode == 0 ? 3 : 2;
+  const int per_step = kinds * n;
+  const int ntasks = ((int)Q.nchunks + Q.lag + (kinds == 3 ? Q.lag2 : 0)) * per_step;
   const int rsh = __ffs((int)Q.chunk_lines / kLL128RowLines) - 1;  // rows per chunk = 2^rsh
   const uint32_t wbase =
       (uint32_t)__cvta_generic_to_shared(smem) + (uint32_t)(warp * kCRing * kRowBytes);
@@ -357,12 +382,28 @@ __global__ void __launch_bounds__(kCWarps * 32, kMinBlocks) k_composed_ll128(Run
       __syncthreads();
       stage_task<kCWarps, kCRing>(s_piece, wbase, lane, warp, n, rsh, e);
       release_flag(Q.flag_stage + (size_t)c * n + x, e, s_ok);
-    } else if (kind == 1) {
+    } else if (kind == 1 && Q.mode != 2) {
       if (!acquire_flags(P, Q.flag_stage + (size_t)c * n, n, e)) s_ok = 0;
       __syncthreads();
       if (!s_ok) break;
-      if (!fold_task<kCWarps, kCRing>(P, wbase, lane, warp, c, x, e)) s_ok = 0;
+      if (!fold_task<kCWarps, kCRing>(P, wbase, lane, warp, c, x, e, Q.mode == 1)) s_ok = 0;
       release_flag(Q.flag_fold + (size_t)c * n + x, e, s_ok);
+    } else if (kind == 1) {
+      // all-to-all: segment x of every source's chunk c into rank x's output;
+      // each staged line has this one reader, which drops it once copied
+      if ((int)threadIdx.x < n) fill_a2a_piece(P, s_piece, c, x, e);
+      if (!acquire_flags(P, Q.flag_stage + (size_t)c * n, n, e)) s_ok = 0;
+      __syncthreads();
+      if (!s_ok) break;
+      if (!gather_task<kCWarps, kCRing>(P, s_piece, wbase, lane, warp, rsh, e)) s_ok = 0;
+      __syncthreads();
+      if (s_ok && Q.discard)
+        for (int r = 0; r < n; ++r) {
+          const int nl = s_piece[r].nl;
+          for (int j = threadIdx.x; j < nl; j += blockDim.x)
+            discard_l2_line(s_piece[r].src + (size_t)j * kLL128LineBytes);
+        }
+      __syncthreads();  // s_piece is refilled by the next task
     } else {
       if ((int)threadIdx.x < n) fill_gather_piece(P, s_piece, c, x, e);
       if (!acquire_flags(P, Q.flag_fold + (size_t)c * n, n, e)) s_ok = 0;

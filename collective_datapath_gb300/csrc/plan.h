@@ -117,6 +117,9 @@ struct ComposedParams {
   int discard;           // drop consumed lines from L2 (no write-back):
                          // 1 = staged and published lines, 2 = staged only
   int variant;           // launch shape (ring depth and CTAs per SM)
+  int mode;              // 0 all-reduce: stage, fold + publish, gather;
+                         // 1 reduce-scatter: stage, fold into the outputs;
+                         // 2 all-to-all: stage, copy into the outputs
   uint64_t* flag_stage;  // [nchunks][N]: epoch once rank p staged chunk c
   uint64_t* flag_fold;   // [nchunks][N]: epoch once owner r published chunk c
   uint64_t* gather_cnt;  // [nchunks]: (epoch << 8) | gathers of chunk c done

@@ -151,12 +151,14 @@ enum { COLL_RESET_FUSED = 0, COLL_RESET_KERNEL = 1, COLL_RESET_NONE = 2,
 /* Launch path: FUSED = stage and consume inside one cooperative kernel
  * (all CTAs co-resident; a CTA serves one emulated rank); STREAMED =
  * separate stage and consume kernels ordered by the stream; COMPOSED
- * (twoshot all-reduce with LL128 only) = one persistent cooperative kernel
- * whose stage, fold and gather CTA groups work through the partitions chunk
- * by chunk, each chunk's lines staying in L2 between its producer and its
- * reader (Purlin §3.2 Algorithm 1, Figure 5).  AUTO picks
- * FUSED for LL8 up to 256 KiB per rank and, for all-reduce, ONESHOT up to
- * 512 KiB per rank (boundaries on measured GB300 points). */
+ * (LL128 only: the twoshot all-reduce, reduce-scatter and all-to-all) = one
+ * persistent cooperative kernel that runs stage, fold (+ publish) and
+ * gather or copy tasks chunk by chunk from one queue, each chunk's lines
+ * staying in L2 between its producer and its reader (Purlin §3.2,
+ * Algorithm 1, Figure 5).  AUTO picks FUSED for LL8 and sentinel packs up
+ * to 256 KiB per rank, COMPOSED for LL128 from 32 MiB per rank and, for
+ * all-reduce, ONESHOT up to 512 KiB per rank (boundaries on measured GB300
+ * points); with COLL_ENC_AUTO the all-reduce takes the calibrated table. */
 enum { COLL_PATH_AUTO = 0, COLL_PATH_FUSED = 1, COLL_PATH_STREAMED = 2,
        COLL_PATH_COMPOSED = 3 };
 

@@ -163,3 +163,50 @@ def test_bandwidth_allreduce_composed_twoshot(cd, inputs, mib):
         assert torch.equal(outs[r], ref_out), f"rank {r}"
     del ref, tmp, outs
     torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("mib", [32, 256])
+def test_bandwidth_composed_reduce_scatter_and_all_to_all(cd, inputs, mib):
+    """The one-launch reduce-scatter (sampled against the oracle, and equal
+    to the stream-ordered one on every element) and all-to-all (equal to the
+    stream-ordered one on every element)."""
+    import torch
+
+    count = mib * 1024 * 1024 // 2
+    m = count // N
+    ins = [x[:count] for x in inputs]
+    results = {}
+    for path in (cd.COLL_PATH_COMPOSED, cd.COLL_PATH_STREAMED):
+        rs = cd.Collective(cd.REDUCE_SCATTER, N, count, encoding=cd.COLL_LL128, path=path)
+        shards = [torch.empty(m, dtype=torch.int16, device="cuda") for _ in range(N)]
+        for _ in range(2):
+            rs.run(ins, shards)
+        assert rs.status()[0] == cd.COLL_OK
+        del rs
+        results[("rs", path)] = shards
+    pos = sample_positions(count, 90 + mib)
+    want = sampled_reference(inputs, count, pos)
+    for r in range(N):
+        sel = pos[(pos >= r * m) & (pos < (r + 1) * m)]
+        got = results[("rs", cd.COLL_PATH_COMPOSED)][r][torch.from_numpy(sel - r * m).cuda()]
+        assert np.array_equal(got.cpu().numpy().view(np.uint16), want[np.searchsorted(pos, sel)])
+        assert torch.equal(results[("rs", cd.COLL_PATH_COMPOSED)][r],
+                           results[("rs", cd.COLL_PATH_STREAMED)][r])
+    del results
+    outs = {}
+    for path in (cd.COLL_PATH_COMPOSED, cd.COLL_PATH_STREAMED):
+        a2a = cd.Collective(cd.ALLTOALL, N, count, encoding=cd.COLL_LL128, path=path)
+        o = [torch.empty(count, dtype=torch.int16, device="cuda") for _ in range(N)]
+        for _ in range(2):
+            a2a.run(ins, o)
+        assert a2a.status()[0] == cd.COLL_OK
+        del a2a
+        outs[path] = o
+    for d in range(N):
+        assert torch.equal(outs[cd.COLL_PATH_COMPOSED][d], outs[cd.COLL_PATH_STREAMED][d])
+        # block p of destination d is block d of source p
+        for p in (0, 3, N - 1):
+            assert torch.equal(outs[cd.COLL_PATH_COMPOSED][d][p * m:(p + 1) * m],
+                               ins[p][d * m:(d + 1) * m])
+    del outs
+    torch.cuda.empty_cache()

@@ -276,3 +276,26 @@ def test_four_rotating_slots(cd, enc, reset, path):
             raw, lines, lb = read_lines(coll, 0, e % 4, 3, 5)
             seqs = raw.reshape(lines, lb)[:, 120:128].copy().view(np.uint64).ravel()
             assert np.all(seqs == e), f"epoch {e}: slot {e % 4} holds {set(seqs.tolist())}"
+
+
+@pytest.mark.parametrize("name,n,count", [("REDUCE_SCATTER", 8, 8 * 60 * 1024 + 64),
+                                          ("REDUCE_SCATTER", 3, 3000), ("REDUCE_SCATTER", 8, 24),
+                                          ("ALLTOALL", 8, 8 * 60 * 512), ("ALLTOALL", 4, 4 * 1000),
+                                          ("ALLTOALL", 2, 2 * 8)])
+@pytest.mark.parametrize("shape", [None, "16,1,1", "64,3,0", "32,5,1,2"])
+def test_composed_reduce_scatter_and_all_to_all(cd, name, n, count, shape, monkeypatch):
+    """The one-launch form of reduce-scatter (stage, fold into the outputs)
+    and all-to-all (stage, copy), bit-exact over several epochs."""
+    if shape is not None:
+        monkeypatch.setenv("COLL_COMPOSED_SHAPE", shape)
+    triple = getattr(cd, name)
+    coll = make(cd, triple, n, count, encoding=cd.COLL_LL128, path=cd.COLL_PATH_COMPOSED)
+    _, ins, outs = buffers(coll, n, seed=41)
+    for e in range(1, 4):
+        xs = [synth.random_bits16(400 + e, count, n, r) if name == "ALLTOALL"
+              else synth.normal_bf16(400 + e, count, n, r) for r in range(n)]
+        for r in range(n):
+            ins[r].copy_(to_dev(xs[r]))
+        coll.run(ins, outs)
+        check(coll, outs, expected(cd, triple, xs, count), n)
+        assert coll.epoch() == e + 1
