@@ -559,14 +559,16 @@ def sentinel_row(cd, count, stream, steps=5) -> dict:
             "rearm_bytes": (n + 1) * s, "status": st}
 
 
-def moe_row(cd, stream, steps=5) -> dict:
+def moe_row(cd, stream, steps=5, path=None) -> dict:
     """MoE dispatch: 8 ranks x 4096 tokens x 7168 bf16, top-8 of 256 experts
     (routing drawn on the device from a seeded generator)."""
     import torch
 
     n, tokens, hidden, k, experts = N_RANKS, 4096, 7168, 8, 256
     coll = cd.Collective(cd.MOE_DISPATCH, n, 0, encoding=cd.COLL_LL128, tokens=tokens,
-                         hidden=hidden, topk=k, experts=experts, max_rows=40000)
+                         hidden=hidden, topk=k, experts=experts, max_rows=40000,
+                         path=cd.COLL_PATH_AUTO if path is None else path)
+    composed = coll.plan()["path"] == cd.COLL_PATH_COMPOSED
     ins = make_inputs(tokens * hidden, 13)
     topk = []
     for r in range(n):
@@ -584,18 +586,23 @@ def moe_row(cd, stream, steps=5) -> dict:
         for _ in range(2):
             coll.run(ins, outs, stream)
         stream.synchronize()
-        cd.coll_set_profile_events(coll.spec, ev)
         e0 = torch.cuda.Event(enable_timing=True)
         e1 = torch.cuda.Event(enable_timing=True)
         e0.record(stream)
+        for _ in range(steps):
+            coll.run(ins, outs, stream)
+        e1.record(stream)
+        stream.synchronize()
+        # the split between the two launch groups, from events the library
+        # records after each launch (separate runs, so the total above is
+        # not perturbed)
+        cd.coll_set_profile_events(coll.spec, ev)
         times = [0.0, 0.0]
         for _ in range(steps):
             coll.run(ins, outs, stream)
             stream.synchronize()
             times[0] += ev[0].elapsed_time(ev[1])
             times[1] += ev[1].elapsed_time(ev[2])
-        e1.record(stream)
-        stream.synchronize()
         cd.coll_set_profile_events(coll.spec, [])
     st = coll.status(stream)[0]
     rows = n * tokens * k
@@ -606,9 +613,12 @@ def moe_row(cd, stream, steps=5) -> dict:
     coll.close()
     del coll, ins, outs, topk
     torch.cuda.empty_cache()
+    split = ({"routing_ms": round(times[0] / steps, 4),
+              "stage_and_copy_ms": round(times[1] / steps, 4)} if composed else
+             {"stage_ms": round(times[0] / steps, 4), "copy_ms": round(times[1] / steps, 4)})
     return {"ms": round(ms, 4), "GB/s": round(unique / ms / 1e6, 1),
-            "algorithmic_bytes": unique, "issue_level_bytes": issue,
-            "stage_ms": round(times[0] / steps, 4), "copy_ms": round(times[1] / steps, 4),
+            "path": "composed" if composed else "streamed",
+            "algorithmic_bytes": unique, "issue_level_bytes": issue, **split,
             "note": "bytes: each token row read once, staged K times as LL128, "
                     "every routed row read and unpacked once", "status": st}
 
@@ -806,6 +816,8 @@ def main() -> int:
             "all_to_all_256MiB_composed": bandwidth_row(cd, cd.ALLTOALL, count, "a2a", stream,
                                                         path=cd.COLL_PATH_COMPOSED),
             "moe_dispatch_8x4096x7168_top8of256": moe_row(cd, stream),
+            "moe_dispatch_8x4096x7168_top8of256_streamed": moe_row(cd, stream,
+                                                                   path=cd.COLL_PATH_STREAMED),
             "reduce_scatter_v_zipf_256MiB": v_row(cd, "REDUCE_SCATTER_V", 256 << 20, stream),
             "all_gather_v_zipf_256MiB": v_row(cd, "ALLGATHER_V", 256 << 20, stream),
             "all_to_all_v_zipf_256MiB": v_row(cd, "ALLTOALL_V", 256 << 20, stream),

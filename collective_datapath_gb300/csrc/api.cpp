@@ -101,6 +101,9 @@ void fill_base(coll_spec* s) {
     M.out_off = reinterpret_cast<uint32_t*>(s->ws + p.off_out_off);
     M.rows_dest = reinterpret_cast<uint32_t*>(s->ws + p.off_rows_dest);
     M.counts_out = reinterpret_cast<int32_t*>(s->ws + p.off_counts_out);
+    M.flag_stage = reinterpret_cast<uint64_t*>(s->ws + p.off_moe_flags);
+    M.lag = 6;
+    if (const char* env = std::getenv("COLL_MOE_LAG")) M.lag = std::max(1, std::atoi(env));
     P.sitems = nullptr;
     P.items1 = nullptr;
   }
@@ -392,6 +395,13 @@ coll_status_t coll_run(coll_spec_t* s, const void* const* dev_ins, void* const* 
     for (int r = 0; r < p.n; ++r) {
       if (s->topk[r] == nullptr) return COLL_ERR_STATE;
       P.moe.topk[r] = s->topk[r];
+    }
+    if (dev_ins != nullptr && p.path == COLL_PATH_COMPOSED) {
+      // routing, then stage and copy tasks in one launch
+      P.stage_rank = -1;
+      if (cudaError_t e = launched(s, launch_moe_routing(P, st), st)) return cuda_status(e);
+      P.advance_epoch = 1;
+      return cuda_status(launched(s, launch_moe_composed(P, st), st));
     }
     if (dev_ins != nullptr) {
       P.stage_rank = -1;

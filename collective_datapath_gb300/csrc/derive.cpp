@@ -134,7 +134,11 @@ static int derive_moe(const DeriveInput& in, Plan& p) {
   p.enc = ENC_LL128;
   p.n = n;
   p.algorithm = 0;
-  p.path = COLL_PATH_STREAMED;
+  // streamed: routing, stage, copy launches; composed: routing, then one
+  // launch of stage and copy tasks (staged rows read from L2)
+  if (in.path != COLL_PATH_AUTO && in.path != COLL_PATH_STREAMED && in.path != COLL_PATH_COMPOSED)
+    return COLL_ERR_UNSUPPORTED;
+  p.path = in.path == COLL_PATH_AUTO ? COLL_PATH_COMPOSED : in.path;
   p.reset_mode = COLL_RESET_NONE;
   p.timeout_ns = in.timeout_ns ? in.timeout_ns : 200000000ull;
   p.moe_tokens = in.tokens;
@@ -142,7 +146,7 @@ static int derive_moe(const DeriveInput& in, Plan& p) {
   p.moe_k = in.topk;
   p.moe_experts = in.experts;
   p.moe_el = in.experts / n;
-  p.moe_nblocks = (in.tokens + 127) / 128;
+  p.moe_nblocks = (in.tokens + kMoeBlockTokens - 1) / kMoeBlockTokens;
   p.moe_row_lines = (uint32_t)round_up(lines_for(ENC_LL128, (uint64_t)in.hidden), 4);
   const uint64_t worst = (uint64_t)in.tokens * n * std::min(in.topk, p.moe_el);
   p.moe_max_rows = (uint32_t)(in.max_rows > 0 ? std::min<uint64_t>(in.max_rows, worst) : worst);
@@ -168,6 +172,7 @@ static int derive_moe(const DeriveInput& in, Plan& p) {
   p.off_out_off = table(4ull * n * p.moe_el * n);
   p.off_rows_dest = table(4ull * n);
   p.off_counts_out = table(4ull * (n * p.moe_el * n + n));
+  p.off_moe_flags = table(8ull * n * p.moe_nblocks * kMoeSubs);
   p.off_counters = table(4);
   off = round_up(off, 4096);
   p.p_rank_lines = tk * p.moe_row_lines;

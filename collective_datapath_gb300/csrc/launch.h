@@ -30,6 +30,8 @@ cudaError_t launch_composed(const RunParams& P, int grid, cudaStream_t s);
 // then the destination scan + validated copy (ends the run).
 cudaError_t launch_moe_stage_all(const RunParams& P, cudaStream_t s);
 cudaError_t launch_moe_consume(const RunParams& P, cudaStream_t s);
+cudaError_t launch_moe_routing(const RunParams& P, cudaStream_t s);
+cudaError_t launch_moe_composed(const RunParams& P, cudaStream_t s);
 cudaError_t launch_rearm(const RunParams& P, int grid, cudaStream_t s);
 cudaError_t launch_advance(const RunParams& P, cudaStream_t s);
 

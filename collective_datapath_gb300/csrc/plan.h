@@ -92,9 +92,17 @@ struct Region {
 
 // MoE dispatch (scatteredV -> transposedV): routing inputs and the device
 // tables the routing kernels fill (all inside the workspace).
+// Tokens per routing block (per-block counts and prefixes) and, in the
+// composed dispatch, per stage task.
+constexpr int kMoeBlockTokens = 16;
+constexpr int kMoeSubTokens = 2;
+constexpr int kMoeSubs = kMoeBlockTokens / kMoeSubTokens;
+
 struct MoeParams {
   const int32_t* topk[kMaxRanks];  // [tokens * k] expert ids per source
   int tokens, hidden, k, experts, el, nblocks;
+  int lag;              // composed dispatch: queue steps from a block's stage to its copies
+  uint64_t* flag_stage; // composed dispatch: [N][nblocks * kMoeSubs] epoch once staged
   uint32_t row_lines;   // LL128 lines per staged row (a multiple of 4)
   uint32_t max_rows;    // output rows per destination
   uint32_t* entry_rank; // [N][tokens * k] rank among the block's rows of one expert

@@ -46,16 +46,23 @@ def counts_of(cd, coll, n, experts):
     return c[:n * el * n].reshape(n, el, n), c[n * el * n:]
 
 
+@pytest.mark.parametrize("path", [2, 3])
 @pytest.mark.parametrize("n,tokens,hidden,k,experts,staged", [
     (4, 300, 64, 3, 16, False),
     (2, 128, 136, 2, 4, True),
     (8, 257, 7168, 8, 256, False),
     (3, 50, 120, 4, 9, True),
+    (8, 33, 960, 8, 512, False),
+    (1, 17, 64, 2, 2, False),
 ])
-def test_moe_dispatch_small_cases_match_the_oracle(cd, n, tokens, hidden, k, experts, staged):
+def test_moe_dispatch_small_cases_match_the_oracle(cd, n, tokens, hidden, k, experts, staged,
+                                                   path):
+    """Both launch forms: routing, stage and copy launches (2), and routing
+    plus one launch of stage and copy tasks (3); staged runs take the first
+    form's copy."""
     import torch
 
-    coll = make_moe(cd, n, tokens, hidden, k, experts)
+    coll = make_moe(cd, n, tokens, hidden, k, experts, path=path)
     xs = [synth.normal_bf16(5, tokens * hidden, n, r).reshape(tokens, hidden) for r in range(n)]
     tk = [synth.topk_experts(5, tokens, k, experts, n, r) for r in range(n)]
     ins = [to_dev(x.ravel()) for x in xs]
@@ -80,14 +87,15 @@ def test_moe_dispatch_small_cases_match_the_oracle(cd, n, tokens, hidden, k, exp
             assert np.array_equal(got, want[d]), f"epoch {epoch} destination {d}"
 
 
-def test_moe_dispatch_8x4096x7168_full_size(cd):
+@pytest.mark.parametrize("path", [2, 3])
+def test_moe_dispatch_8x4096x7168_full_size(cd, path):
     """8 ranks x 4096 tokens x 7168 bf16 normal(0,1), top-8 of 256 experts:
     every output row of every destination equals its source row as listed
-    by the oracle, and the counts equal the oracle's."""
+    by the oracle, and the counts equal the oracle's (both launch forms)."""
     import torch
 
     n, tokens, hidden, k, experts = 8, 4096, 7168, 8, 256
-    coll = make_moe(cd, n, tokens, hidden, k, experts, max_rows=40000)
+    coll = make_moe(cd, n, tokens, hidden, k, experts, max_rows=40000, path=path)
     xs = [synth.normal_bf16(6, tokens * hidden, r) for r in range(n)]
     tk = [synth.topk_experts(6, tokens, k, experts, r) for r in range(n)]
     x_dev = torch.stack([torch.from_numpy(x.view(np.int16)) for x in xs]).cuda()  # [n, T*H]
