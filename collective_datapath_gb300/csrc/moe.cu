@@ -12,7 +12,7 @@
 // contiguous).
 //
 // Steps, all on the device:
-//  k_moe_count    per (source, block of 128 tokens): per-expert counts and
+//  k_moe_count    per (source, block of 16 tokens): per-expert counts and
 //                 the stable rank of every (token, choice) among the block's
 //                 tokens routed to the same expert
 //  k_moe_scan_src per source: block prefixes, cnt[p][e], and stage_off[p][e]
@@ -23,6 +23,8 @@
 //  k_moe_scan_dst per destination: out_off[d][le][p], counts, rows
 //  k_moe_copy     one warp per output row: validate the row's LL128 lines
 //                 through a cp.async ring and unpack them
+//  k_moe_composed the stage and copy steps as tasks of one launch (after the
+//                 routing kernels), staged rows read back mostly from L2
 #include <cuda_runtime.h>
 
 #include "launch.h"
