@@ -526,6 +526,62 @@ def f32_row(cd, nbytes, stream, steps=5) -> dict:
             "status": st}
 
 
+def atom_ablation(cd, stream, nbytes=256 << 20, stage_bytes=16384, ctas_list=None,
+                  steps=5, engines=("bulk", "lsu"), stages=range(1, 9)) -> dict:
+    """Pipeline-depth ablation of the one-sided copy (Purlin §5.2, Figure 9;
+    capacity Q_cap = C * S * B_stage of §3.3 Eq. (3)), against HBM: a copy of
+    `nbytes` with the CTA count C fixed, S = 1..8 stages of `stage_bytes`,
+    for both load engines.  copy_GBps = message bytes / time (the figure's
+    quantity); hbm_GBps counts the read and the write (the HBM roofline);
+    latency_ns = Q_cap / copy rate, the latency the bytes in flight cover by
+    Little's law.  Median of `steps` launches, each timed alone."""
+    import torch
+
+    sms = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
+    ctas_list = ctas_list or (16, 32, 64, sms)
+    src = torch.randint(-2**31, 2**31 - 1, (nbytes // 4,), dtype=torch.int32, device="cuda")
+    dst = torch.empty_like(src)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    torch.cuda.synchronize()
+    out = {"bytes": nbytes, "stage_bytes": stage_bytes, "threads_per_cta": 256,
+           "l2": "source and destination (512 MiB together) larger than L2; no flush"}
+    for name, engine in (("bulk", cd.COLL_ATOM_BULK), ("lsu", cd.COLL_ATOM_LSU)):
+        if name not in engines:
+            continue
+        for C in ctas_list:
+            pts = []
+            for S in stages:
+                def launch():
+                    cd.coll_atom_copy(dst, src, nbytes, engine=engine, ctas=C, stages=S,
+                                      stage_bytes=stage_bytes, status=status, stream=stream)
+                with torch.cuda.stream(stream):
+                    for _ in range(2):
+                        launch()
+                    ms = []
+                    for _ in range(steps):
+                        e0 = torch.cuda.Event(enable_timing=True)
+                        e1 = torch.cuda.Event(enable_timing=True)
+                        e0.record(stream)
+                        launch()
+                        e1.record(stream)
+                        stream.synchronize()
+                        ms.append(e0.elapsed_time(e1))
+                t = statistics.median(ms)
+                rate = nbytes / t / 1e6
+                q = C * S * stage_bytes
+                pts.append({"S": S, "q_cap_bytes": q, "ms": round(t, 4),
+                            "copy_GBps": round(rate, 1), "hbm_GBps": round(2 * rate, 1),
+                            "latency_ns": round(q / rate, 1)})
+            out[f"{name}_C{C}"] = pts
+    torch.cuda.synchronize()
+    out["status"] = int(status.item())
+    ok = bool(torch.equal(dst, src))
+    out["last_copy_exact"] = ok
+    del src, dst
+    torch.cuda.empty_cache()
+    return out
+
+
 def sentinel_row(cd, count, stream, steps=5) -> dict:
     """8 ranks x `count` bf16 all-reduce, twoshot, sentinel packs, streamed.
     Algorithmic bytes are the LL form with epsilon = 1 (no readiness bytes);
@@ -640,6 +696,10 @@ def main() -> int:
                     help="sweep only this variant, e.g. twoshot_fused")
     ap.add_argument("--sweep-enc", default="ll8", choices=["ll8", "ll128", "sent"],
                     help="readiness encoding of the sweep")
+    ap.add_argument("--atom-only", action="store_true",
+                    help="only the pipeline-depth ablation of the one-sided copy")
+    ap.add_argument("--atom-case", default=None,
+                    help="with --atom-only: one point ENGINE,C,S (e.g. bulk,16,8)")
     args = ap.parse_args()
     if args.impl == "reference":
         return run_reference(args)
@@ -668,6 +728,13 @@ def main() -> int:
         print(json.dumps({"encoding": args.sweep_enc,
                           "latency_us_per_op": latency_sweep(cd, stream, args.sweep_T,
                                                              args.sweep_variant, enc)}))
+        return 0
+    if args.atom_only:
+        kw = {}
+        if args.atom_case:
+            eng, c, st = args.atom_case.split(",")
+            kw = {"engines": (eng,), "ctas_list": (int(c),), "stages": (int(st),)}
+        print(json.dumps({"pipeline_depth_ablation_256MiB": atom_ablation(cd, stream, **kw)}))
         return 0
     count = args.mib * 2**20 // 2
     s_bytes = count * 2.0
@@ -823,6 +890,7 @@ def main() -> int:
             "all_to_all_v_zipf_256MiB": v_row(cd, "ALLTOALL_V", 256 << 20, stream),
             "allreduce_256MiB_sentinel_twoshot": sentinel_row(cd, count, stream),
             "allreduce_256MiB_f32_composed": f32_row(cd, 256 << 20, stream),
+            "pipeline_depth_ablation_256MiB": atom_ablation(cd, stream),
         }
         line["latency_us_per_op"] = latency_sweep(cd, stream)
         if world == 1:

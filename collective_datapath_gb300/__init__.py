@@ -34,6 +34,7 @@ COLL_LL8, COLL_LL128, COLL_SENT, COLL_ENC_AUTO = 0, 1, 2, 3
 COLL_ALGO_AUTO, COLL_ONESHOT, COLL_TWOSHOT = 0, 1, 2
 COLL_RESET_FUSED, COLL_RESET_KERNEL, COLL_RESET_NONE, COLL_RESET_DEFERRED = 0, 1, 2, 3
 COLL_PATH_AUTO, COLL_PATH_FUSED, COLL_PATH_STREAMED, COLL_PATH_COMPOSED = 0, 1, 2, 3
+COLL_ATOM_BULK, COLL_ATOM_LSU = 0, 1
 
 # Every symbol include/coll.h declares (checked by the tests).
 EXPORTS = [
@@ -43,7 +44,7 @@ EXPORTS = [
     "coll_staging_layout", "coll_stage_withheld", "coll_run_late",
     "coll_get_rejections", "coll_debug_items", "coll_debug_plan",
     "coll_set_profile_events", "coll_last_launches", "coll_allreduce_static",
-    "coll_destroy", "coll_status_string",
+    "coll_atom_copy", "coll_destroy", "coll_status_string",
 ]
 
 
@@ -97,6 +98,8 @@ _sig("coll_debug_plan", _st, _vp, _P(ctypes.c_int), _P(ctypes.c_int),
 _sig("coll_set_profile_events", _st, _vp, _P(_vp), ctypes.c_int)
 _sig("coll_last_launches", _st, _vp, _P(ctypes.c_int))
 _sig("coll_allreduce_static", _st, ctypes.c_int, _sz, _P(_vp), _P(_vp), _vp)
+_sig("coll_atom_copy", _st, _vp, _vp, _sz, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+     ctypes.c_int, _vp, _vp)
 _sig("coll_destroy", _st, _vp)
 _sig("coll_status_string", ctypes.c_char_p, ctypes.c_int)
 
@@ -306,6 +309,15 @@ def coll_allreduce_static(ins: Sequence, outs: Sequence, count: int, stream=None
     """All-reduce in the library's fixed scratch (no workspace, no allocation)."""
     _check(_lib.coll_allreduce_static(len(ins), count, _ptr_array(ins), _ptr_array(outs),
                                       _stream_handle(stream)), "coll_allreduce_static")
+
+
+def coll_atom_copy(dst, src, nbytes: int, engine: int = COLL_ATOM_BULK, ctas: int = 0,
+                   stages: int = 8, stage_bytes: int = 16384, status=None,
+                   stream=None) -> None:
+    """One-sided copy of `nbytes` from `src` to `dst` (device tensors) with
+    `ctas` CTAs of `stages` pipeline stages of `stage_bytes` each."""
+    _check(_lib.coll_atom_copy(_ptr(dst), _ptr(src), nbytes, engine, ctas, stages, stage_bytes,
+                               _ptr(status), _stream_handle(stream)), "coll_atom_copy")
 
 
 def coll_destroy(spec: int) -> None:

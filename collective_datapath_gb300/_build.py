@@ -17,9 +17,10 @@ ROOT = os.path.dirname(HERE)
 BUILD_DIR = os.path.join(ROOT, "_build")
 LIB = os.path.join(HERE, "libcoll.so")
 
-SOURCES = ["kernels.cu", "api.cpp", "derive.cpp", "static_ws.cu", "moe.cu", "composed.cu"]
+SOURCES = ["kernels.cu", "api.cpp", "derive.cpp", "static_ws.cu", "moe.cu", "composed.cu",
+           "atom.cu"]
 HEADERS = ["plan.h", "derive.h", "launch.h", "dev_common.cuh", "ll8.cuh", "ll128.cuh",
-           "pipe.cuh", "sent.cuh", "policy_table.h"]
+           "pipe.cuh", "sent.cuh", "policy_table.h", "tma.cuh"]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 # No fast math: IEEE division/sqrt, no flush-to-zero (the fold is bit-exact).

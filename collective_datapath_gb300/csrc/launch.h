@@ -32,6 +32,13 @@ cudaError_t launch_moe_stage_all(const RunParams& P, cudaStream_t s);
 cudaError_t launch_moe_consume(const RunParams& P, cudaStream_t s);
 cudaError_t launch_moe_routing(const RunParams& P, cudaStream_t s);
 cudaError_t launch_moe_composed(const RunParams& P, cudaStream_t s);
+// One-sided copy with an explicit pipeline (atom.cu): engine 0 = TMA bulk
+// ring, 1 = cp.async ring; `stages` in 1..kAtomMaxStages of `stage_bytes`.
+constexpr int kAtomMaxStages = 8;
+constexpr int kAtomMaxSmem = 192 * 1024;
+cudaError_t launch_atom_copy(void* dst, const void* src, uint64_t bytes, int engine, int ctas,
+                             int stages, uint32_t stage_bytes, int32_t* status,
+                             cudaStream_t st);
 cudaError_t launch_rearm(const RunParams& P, int grid, cudaStream_t s);
 cudaError_t launch_advance(const RunParams& P, cudaStream_t s);
 

@@ -30,6 +30,7 @@
 #include "launch.h"
 #include "ll128.cuh"
 #include "pipe.cuh"
+#include "tma.cuh"
 
 namespace coll {
 
@@ -126,46 +127,6 @@ __global__ void __launch_bounds__(kMoeThreads) k_moe_scan_dst(RunParams P) {
 
 // ---- gather-stage with a TMA bulk load per token row ----------------------------
 
-__device__ __forceinline__ void mbar_init(uint32_t mbar, uint32_t count) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(mbar), "r"(count) : "memory");
-}
-__device__ __forceinline__ void mbar_expect_tx(uint32_t mbar, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(mbar), "r"(bytes)
-               : "memory");
-}
-__device__ __forceinline__ bool mbar_try_wait(uint32_t mbar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n .reg .pred p;\n"
-      " mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
-      " selp.u32 %0, 1, 0, p;\n}"
-      : "=r"(ok)
-      : "r"(mbar), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-// Wait for phase `parity` of an mbarrier, giving up after timeout_ns.
-__device__ __forceinline__ bool mbar_wait_bounded(uint32_t mbar, uint32_t parity,
-                                                  uint64_t timeout_ns) {
-  const uint64_t t0 = globaltimer_ns();
-  while (!mbar_try_wait(mbar, parity))
-    if (globaltimer_ns() - t0 > timeout_ns) return false;
-  return true;
-}
-__device__ __forceinline__ void tma_load_1d(uint32_t dst, const void* src, uint32_t bytes,
-                                            uint32_t mbar) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
-          "r"(dst),
-      "l"(src), "r"(bytes), "r"(mbar)
-      : "memory");
-}
-__device__ __forceinline__ void fence_proxy_async_smem() {
-  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
-__device__ __forceinline__ void fence_mbarrier_init() {
-  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-}
 size_t moe_stage_smem_bytes(int hidden) {
   return 2 * (((size_t)hidden * 2 + 127) / 128 * 128);
 }

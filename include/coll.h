@@ -371,6 +371,33 @@ coll_status_t coll_last_launches(const coll_spec_t *spec, int *launches);
 coll_status_t coll_allreduce_static(int nranks, size_t count, const void *const *dev_ins,
                                     void *const *dev_outs, coll_stream_t stream);
 
+/* One-sided copy with an explicit pipeline depth -- Purlin §3.3, Eq. (3):
+ * `ctas` transfer CTAs (C), each with `stages` pipeline stages (S) of
+ * `stage_bytes` bytes (B_stage), keep at most Q_cap = C * S * B_stage bytes
+ * of loads in flight; §5.2 (Figure 9) ablates S at fixed C and message size.
+ * dev_dst[0 .. bytes) <- dev_src[0 .. bytes), byte for byte.  Both pointers
+ * are device addresses of this GPU, 16-byte aligned; the ranges must not
+ * overlap.  Chunk c (stage_bytes each, the last one shorter) is copied by
+ * CTA c mod C.  Engines:
+ *   COLL_ATOM_BULK: one thread per CTA drives S shared-memory stages with
+ *     TMA bulk loads (mbarrier completion) and TMA bulk stores;
+ *   COLL_ATOM_LSU: 256 threads per CTA keep S stages of cp.async granules in
+ *     flight and store them from registers.
+ * Arguments: stages 1..8; stage_bytes a positive multiple of 16 with
+ * stages * stage_bytes <= 196,608 (shared memory per CTA); ctas 0..65535,
+ * 0 = one per SM; bytes a multiple of 16, 0 = nothing to do.  Out-of-range
+ * arguments, null pointers or overlapping ranges return COLL_ERR_INVALID,
+ * misaligned pointers, sizes or stage_bytes COLL_ERR_ALIGN, and in each case
+ * nothing is enqueued.  The copy is asynchronous on `stream`.
+ * dev_status (a device int32, may be NULL) is set to COLL_ERR_TIMEOUT if a
+ * stage waits longer than one second for its load (the CTA then drains its
+ * copies and stops); it is never cleared by the library. */
+typedef enum { COLL_ATOM_BULK = 0, COLL_ATOM_LSU = 1 } coll_atom_engine_t;
+
+coll_status_t coll_atom_copy(void *dev_dst, const void *dev_src, size_t bytes, int engine,
+                             int ctas, int stages, int stage_bytes, int32_t *dev_status,
+                             coll_stream_t stream);
+
 /* Release the spec's host state (never the caller's device memory). */
 coll_status_t coll_destroy(coll_spec_t *spec);
 

@@ -124,6 +124,9 @@ def _declare(L: ctypes.CDLL) -> None:
     L.orc_sent_sanitize_f32.restype = ctypes.c_uint32
     L.orc_sent_encode_f32.argtypes = [_u32p, _sz, _u64p]
     L.orc_sent_encode_f32.restype = None
+    L.orc_one_sided_copy.argtypes = [ctypes.POINTER(ctypes.c_uint8), _sz,
+                                     ctypes.POINTER(ctypes.c_uint8)]
+    L.orc_one_sided_copy.restype = None
     L.orc_sent_decode_f32.argtypes = [_u64p, _sz, _u32p]
     L.orc_sent_decode_f32.restype = _sz
     L.orc_sent_sanitize.argtypes = [ctypes.c_uint16]
@@ -453,3 +456,12 @@ def sent_decode_f32(packs: np.ndarray, elems: int, fill: int = 0) -> tuple[np.nd
     skipped = lib().orc_sent_decode_f32(_ptr(packs, ctypes.c_uint64), elems,
                                         _ptr(out, ctypes.c_uint32))
     return out[:elems], int(skipped)
+
+
+def one_sided_copy(src: np.ndarray) -> np.ndarray:
+    """The bytes a one-sided copy (Purlin §3.3 Atom::copy) delivers: those
+    of `src`, in order, as uint8."""
+    b = _c(np.asarray(src).reshape(-1).view(np.uint8), np.uint8)
+    out = np.zeros_like(b)
+    lib().orc_one_sided_copy(_ptr(b, ctypes.c_uint8), b.size, _ptr(out, ctypes.c_uint8))
+    return out

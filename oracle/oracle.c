@@ -492,3 +492,9 @@ size_t orc_sent_decode_f32(const uint64_t *packs, size_t elems, uint32_t *out)
     }
     return skipped;
 }
+
+void orc_one_sided_copy(const uint8_t *src, size_t bytes, uint8_t *dst)
+{
+    for (size_t i = 0; i < bytes; ++i)
+        dst[i] = src[i];
+}

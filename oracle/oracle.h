@@ -236,6 +236,11 @@ uint32_t orc_sent_sanitize_f32(uint32_t x);
 void orc_sent_encode_f32(const uint32_t *in, size_t elems, uint64_t *packs);
 size_t orc_sent_decode_f32(const uint64_t *packs, size_t elems, uint32_t *out);
 
+/* One-sided copy -- Purlin §3.3 (Atom::copy): dst[i] = src[i] for every
+ * byte i < bytes.  Pipeline depth, stage size and CTA count change how the
+ * bytes move, never which bytes arrive, so none of them is a parameter. */
+void orc_one_sided_copy(const uint8_t *src, size_t bytes, uint8_t *dst);
+
 #ifdef __cplusplus
 }
 #endif

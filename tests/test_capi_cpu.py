@@ -343,3 +343,31 @@ def test_f32_element_counts_and_admission(cd):
     with pytest.raises(cd.CollError) as e:
         cd.coll_spec_create(*cd.ALLREDUCE, 8, 64, dtype=7)
     assert e.value.status == cd.COLL_ERR_UNSUPPORTED
+
+
+def test_atom_copy_argument_validation(cd):
+    """coll_atom_copy rejects every bad argument on the host, before any CUDA
+    call (the pointers here are never dereferenced)."""
+    def status_of(dst, src, nbytes, **kw):
+        try:
+            cd.coll_atom_copy(dst, src, nbytes, stream=0, **kw)
+        except cd.CollError as e:
+            return e.status
+        return cd.COLL_OK
+
+    a, b = 0x10000000, 0x20000000
+    assert status_of(a, b, 0) == cd.COLL_OK                       # nothing to copy
+    assert status_of(a, b, 4096, stages=0) == cd.COLL_ERR_INVALID
+    assert status_of(a, b, 4096, stages=9) == cd.COLL_ERR_INVALID
+    assert status_of(a, b, 4096, stage_bytes=0) == cd.COLL_ERR_INVALID
+    assert status_of(a, b, 4096, stages=8, stage_bytes=32768) == cd.COLL_ERR_INVALID
+    assert status_of(a, b, 4096, engine=2) == cd.COLL_ERR_INVALID
+    assert status_of(a, b, 4096, ctas=-1) == cd.COLL_ERR_INVALID
+    assert status_of(a, b, 4096, ctas=65536) == cd.COLL_ERR_INVALID
+    assert status_of(a, b, 4096, stage_bytes=24) == cd.COLL_ERR_ALIGN
+    assert status_of(a, b, 4104) == cd.COLL_ERR_ALIGN
+    assert status_of(a + 8, b, 4096) == cd.COLL_ERR_ALIGN
+    assert status_of(a, b + 4, 4096) == cd.COLL_ERR_ALIGN
+    assert status_of(None, b, 4096) == cd.COLL_ERR_INVALID
+    assert status_of(a, a + 4080, 4096) == cd.COLL_ERR_INVALID     # overlapping ranges
+    assert status_of(a + 4080, a, 4096) == cd.COLL_ERR_INVALID

@@ -51,6 +51,9 @@ MUTANTS = [
     ("f32_sent_pack_swapped", "        packs[j] = lo | (hi << 32);", "        packs[j] = hi | (lo << 32);"),
     ("f32_sent_decode_accepts_sentinel", "        if (pack == 0xFFFFFFFFFFFFFFFFull) { /* not yet published */", "        if (0) {"),
     ("f32_sent_wrong_pattern", "    if (x == 0xFFFFFFFFu)\n        return 0x7FC00000u;", "    if (x == 0xFFFF0000u)\n        return 0x7FC00000u;"),
+    ("copy_drops_first_byte", "    for (size_t i = 0; i < bytes; ++i)\n        dst[i] = src[i];",
+     "    for (size_t i = 1; i < bytes; ++i)\n        dst[i] = src[i];"),
+    ("copy_reversed", "        dst[i] = src[i];", "        dst[i] = src[bytes - 1 - i];"),
     ("moe_source_major_order", "for (int le = 0; le < el; ++le) {\n            int e = d * el + le;\n            for (int p = 0; p < n; ++p)",
      "for (int le = 0; le < el; ++le) {\n            int e = d * el + le;\n            for (int p = n - 1; p >= 0; --p)"),
 ]
@@ -87,6 +90,7 @@ PINS = [
     pins.test_fold_f32_n1_is_identity,
     pins.test_reduce_scatter_f32_is_the_allreduce_partition,
     pins.test_sentinel_f32_sanitize_and_layout,
+    pins.test_one_sided_copy_delivers_every_byte_in_order,
 ]
 
 

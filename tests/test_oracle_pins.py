@@ -648,3 +648,18 @@ def test_sentinel_f32_sanitize_and_layout(orc):
     p[3] = np.uint64(0xFFFFFFFFFFFFFFFF)
     back, skipped = orc.sent_decode_f32(p, y.size, fill=7)
     assert skipped == 1 and back[6] == 7 and back[7] == 7
+
+
+# ---- one-sided copy (Purlin §3.3, Atom::copy) ------------------------------------
+
+def test_one_sided_copy_delivers_every_byte_in_order(orc):
+    # every byte value once, in an order that no shift, reversal or stride
+    # of the input reproduces (a permutation written out by hand:
+    # 37 i + 11 mod 256, no byte zero at either end)
+    x = np.array([(37 * i + 11) % 256 for i in range(256)], dtype=np.uint8)
+    assert orc.one_sided_copy(x).tolist() == [(37 * i + 11) % 256 for i in range(256)]
+    assert orc.one_sided_copy(np.zeros(0, dtype=np.uint8)).size == 0
+    assert orc.one_sided_copy(np.array([7], dtype=np.uint8)).tolist() == [7]
+    # wider elements travel as their little-endian bytes
+    w = np.array([0x04030201, 0x08070605], dtype=np.uint32)
+    assert orc.one_sided_copy(w).tolist() == [1, 2, 3, 4, 5, 6, 7, 8]
