@@ -615,14 +615,15 @@ def sentinel_row(cd, count, stream, steps=5) -> dict:
             "rearm_bytes": (n + 1) * s, "status": st}
 
 
-def moe_row(cd, stream, steps=5, path=None) -> dict:
-    """MoE dispatch: 8 ranks x 4096 tokens x 7168 bf16, top-8 of 256 experts
-    (routing drawn on the device from a seeded generator)."""
+def moe_row(cd, stream, steps=5, path=None, tokens=4096) -> dict:
+    """MoE dispatch: 8 ranks x `tokens` tokens x 7168 bf16, top-8 of 256
+    experts (routing drawn on the device from a seeded generator)."""
     import torch
 
-    n, tokens, hidden, k, experts = N_RANKS, 4096, 7168, 8, 256
+    n, hidden, k, experts = N_RANKS, 7168, 8, 256
     coll = cd.Collective(cd.MOE_DISPATCH, n, 0, encoding=cd.COLL_LL128, tokens=tokens,
-                         hidden=hidden, topk=k, experts=experts, max_rows=40000,
+                         hidden=hidden, topk=k, experts=experts,
+                         max_rows=(tokens * k * 40000 + 32767) // 32768,
                          path=cd.COLL_PATH_AUTO if path is None else path)
     composed = coll.plan()["path"] == cd.COLL_PATH_COMPOSED
     ins = make_inputs(tokens * hidden, 13)
@@ -698,6 +699,12 @@ def main() -> int:
                     help="readiness encoding of the sweep")
     ap.add_argument("--atom-only", action="store_true",
                     help="only the pipeline-depth ablation of the one-sided copy")
+    ap.add_argument("--row", default=None,
+                    help="run one extra row alone and print it (profiling runs): "
+                         "moe, moe_streamed, rs, rs_composed, ag, a2a, a2a_composed, "
+                         "sentinel, f32, rsv, agv, a2av")
+    ap.add_argument("--moe-tokens", type=int, default=4096,
+                    help="tokens per rank of the MoE rows (the bench line uses 4096)")
     ap.add_argument("--atom-case", default=None,
                     help="with --atom-only: one point ENGINE,C,S (e.g. bulk,16,8)")
     args = ap.parse_args()
@@ -737,6 +744,28 @@ def main() -> int:
         print(json.dumps({"pipeline_depth_ablation_256MiB": atom_ablation(cd, stream, **kw)}))
         return 0
     count = args.mib * 2**20 // 2
+    if args.row:
+        rows = {
+            "moe": lambda: moe_row(cd, stream, tokens=args.moe_tokens),
+            "moe_streamed": lambda: moe_row(cd, stream, path=cd.COLL_PATH_STREAMED,
+                                            tokens=args.moe_tokens),
+            "rs": lambda: bandwidth_row(cd, cd.REDUCE_SCATTER, count, "rs", stream),
+            "rs_composed": lambda: bandwidth_row(cd, cd.REDUCE_SCATTER, count, "rs", stream,
+                                                 path=cd.COLL_PATH_COMPOSED),
+            "ag": lambda: bandwidth_row(cd, cd.ALLGATHER, count, "ag", stream),
+            "a2a": lambda: bandwidth_row(cd, cd.ALLTOALL, count, "a2a", stream),
+            "a2a_composed": lambda: bandwidth_row(cd, cd.ALLTOALL, count, "a2a", stream,
+                                                  path=cd.COLL_PATH_COMPOSED),
+            "sentinel": lambda: sentinel_row(cd, count, stream),
+            "f32": lambda: f32_row(cd, args.mib << 20, stream),
+            "rsv": lambda: v_row(cd, "REDUCE_SCATTER_V", args.mib << 20, stream),
+            "agv": lambda: v_row(cd, "ALLGATHER_V", args.mib << 20, stream),
+            "a2av": lambda: v_row(cd, "ALLTOALL_V", args.mib << 20, stream),
+        }
+        if args.row not in rows:
+            raise SystemExit(f"unknown row {args.row}")
+        print(json.dumps({"rows": {args.row: rows[args.row]()}}))
+        return 0
     s_bytes = count * 2.0
     composed = args.path == "composed"
     coll = cd.Collective(cd.ALLREDUCE, N_RANKS, count, encoding=cd.COLL_LL128,
