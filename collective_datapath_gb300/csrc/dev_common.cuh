@@ -71,6 +71,14 @@ __device__ __forceinline__ uint4 ld_stream_v4(const void* p) {
   return v;
 }
 
+__device__ __forceinline__ uint2 ld_stream_v2(const void* p) {
+  uint2 v;
+  asm volatile("ld.global.nc.L1::no_allocate.v2.u32 {%0, %1}, [%2];"
+               : "=r"(v.x), "=r"(v.y)
+               : "l"(p));
+  return v;
+}
+
 // Plain 16-byte accesses for data no other CTA of the same launch touches.
 __device__ __forceinline__ uint4 ld_v4(const void* p) {
   uint4 v;

@@ -1,6 +1,7 @@
 // ll8.cuh -- LL8 datapath: 8-byte lines of 4 data bytes (two bf16) and a
-// 4-byte flag equal to the epoch's low 32 bits.  A thread handles groups of
-// four lines (one 16-byte input chunk, 32 bytes of lines, two 16-byte stores).
+// 4-byte flag equal to the epoch's low 32 bits.  Staging moves line pairs
+// (8 input bytes -> one 16-byte store); consumers read pairs or groups of four
+// lines.
 //
 // The line is the notification: Purlin §3.2 "Specializing for latency"
 // packs payload and flag in one packet written by a single store; flash-comm
@@ -104,6 +105,11 @@ __device__ __forceinline__ void ll8_fold_pair(const uint64_t* lo, const uint64_t
 constexpr int kGroupsInFlight = 4;
 
 // Encode one staging tile (nlines is a multiple of 4 for LL8).
+// Staging moves line pairs: a lane loads 8 input bytes (four bf16) and
+// stores the two lines they make as one 16-byte store, so a warp's store
+// covers 512 contiguous bytes (16 fully written sectors).
+constexpr int kPairsInFlight = 8;
+
 __device__ __forceinline__ void ll8_stage_tile(const RunParams& P, const StageItem& it,
                                                uint64_t epoch) {
   const uint16_t* in = P.in[it.rank] + it.in_elem;
@@ -112,21 +118,21 @@ __device__ __forceinline__ void ll8_stage_tile(const RunParams& P, const StageIt
   // previous run, which has completed.
   const bool deferred = P.reset_mode == kResetDeferred;
   uint64_t* other = image_lines(P, P.P, epoch + 1, it.rank) + it.dst_line;
-  const uint32_t flag = (uint32_t)epoch;
-  const uint32_t ngroups = it.nlines / kLL8GroupLines;
-  for (uint32_t g0 = threadIdx.x; g0 < ngroups; g0 += blockDim.x * kGroupsInFlight) {
-    uint4 v[kGroupsInFlight];
+  const uint64_t f = (uint64_t)(uint32_t)epoch << 32;
+  const uint32_t npairs = it.nlines / 2;
+  for (uint32_t q0 = threadIdx.x; q0 < npairs; q0 += blockDim.x * kPairsInFlight) {
+    uint2 v[kPairsInFlight];
 #pragma unroll
-    for (int j = 0; j < kGroupsInFlight; ++j) {
-      const uint32_t g = g0 + j * blockDim.x;
-      if (g < ngroups) v[j] = ld_stream_v4(in + 8 * (size_t)g);
+    for (int j = 0; j < kPairsInFlight; ++j) {
+      const uint32_t q = q0 + j * blockDim.x;
+      if (q < npairs) v[j] = ld_stream_v2(in + 4 * (size_t)q);
     }
 #pragma unroll
-    for (int j = 0; j < kGroupsInFlight; ++j) {
-      const uint32_t g = g0 + j * blockDim.x;
-      if (g < ngroups) {
-        ll8_store(img + 4 * (size_t)g, v[j], flag);
-        if (deferred) ll8_rearm(other + 4 * (size_t)g);
+    for (int j = 0; j < kPairsInFlight; ++j) {
+      const uint32_t q = q0 + j * blockDim.x;
+      if (q < npairs) {
+        st_relaxed_v2u64(img + 2 * (size_t)q, (uint64_t)v[j].x | f, (uint64_t)v[j].y | f);
+        if (deferred) st_relaxed_v2u64(other + 2 * (size_t)q, 0ull, 0ull);
       }
     }
   }
