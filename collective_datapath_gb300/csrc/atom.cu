@@ -167,11 +167,9 @@ __global__ void __launch_bounds__(kAtomThreads) k_atom_lsu(AtomArgs a) {
 template <int S>
 static cudaError_t launch_atom_s(const AtomArgs& a, int engine, int ctas, cudaStream_t st) {
   const size_t smem = (size_t)S * a.stage_bytes;
+  static size_t memo[2][kMaxDevices];
   auto* fn = engine == 0 ? k_atom_bulk<S> : k_atom_lsu<S>;
-  // per call: the attribute belongs to the current device
-  cudaError_t err =
-      cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kAtomMaxSmem);
-  if (err != cudaSuccess) return err;
+  if (cudaError_t err = raise_smem_limit(fn, (size_t)kAtomMaxSmem, memo[engine])) return err;
   fn<<<ctas, kAtomThreads, smem, st>>>(a);
   return cudaGetLastError();
 }

@@ -430,14 +430,9 @@ __global__ void __launch_bounds__(kCWarps * 32, kMinBlocks) k_composed_ll128(Run
 
 template <int W, int R, int B>
 static int capacity_of() {
-  static bool configured = false;
+  static size_t memo[kMaxDevices];
   const int bytes = (int)((size_t)W * R * kRowBytes);
-  if (!configured) {
-    if (cudaFuncSetAttribute(k_composed_ll128<W, R, B>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) != cudaSuccess)
-      return 0;
-    configured = true;
-  }
+  if (raise_smem_limit(k_composed_ll128<W, R, B>, (size_t)bytes, memo) != cudaSuccess) return 0;
   int per_sm = 0;
   if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_composed_ll128<W, R, B>, W * 32,
                                                     bytes) != cudaSuccess)

@@ -618,16 +618,26 @@ __global__ void k_advance(RunParams P) { finish_run(P, begin_run(P)); }
 
 // ---- launchers ---------------------------------------------------------------
 
-static int g_num_sms = 0;
+int current_device() {
+  int dev = 0;
+  return cudaGetDevice(&dev) == cudaSuccess ? dev : 0;
+}
+
+static int g_num_sms[kMaxDevices];
 
 int device_sms() {
-  if (g_num_sms == 0) {
-    int dev = 0;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&g_num_sms, cudaDevAttrMultiProcessorCount, dev);
-    if (g_num_sms <= 0) g_num_sms = 1;
+  const int dev = current_device();
+  if (dev < 0 || dev >= kMaxDevices) {
+    int n = 0;
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    return n > 0 ? n : 1;
   }
-  return g_num_sms;
+  if (g_num_sms[dev] == 0) {
+    int n = 0;
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    g_num_sms[dev] = n > 0 ? n : 1;
+  }
+  return g_num_sms[dev];
 }
 
 int fused_capacity(int enc) {
@@ -684,17 +694,11 @@ cudaError_t launch_fused(const RunParams& P, int grid, cudaStream_t s) {
 }
 
 cudaError_t launch_fold(const RunParams& P, int grid, cudaStream_t s) {
-  static bool configured = false;
+  static size_t memo128[kMaxDevices], memo8[kMaxDevices];
   const size_t bytes = fold_smem_bytes(P.nranks);
-  if (!configured) {
-    const int most = (int)fold_smem_bytes(kMaxRanks);
-    cudaError_t e = cudaFuncSetAttribute(k_fold_ll128,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, most);
-    if (e == cudaSuccess)
-      e = cudaFuncSetAttribute(k_fold_ll8, cudaFuncAttributeMaxDynamicSharedMemorySize, most);
-    if (e != cudaSuccess) return e;
-    configured = true;
-  }
+  if (cudaError_t e = P.enc == ENC_LL8 ? raise_smem_limit(k_fold_ll8, bytes, memo8)
+                                       : raise_smem_limit(k_fold_ll128, bytes, memo128))
+    return e;
   if (P.enc == ENC_LL8)
     k_fold_ll8<<<grid, kThreads, bytes, s>>>(P);
   else

@@ -7,7 +7,26 @@
 
 namespace coll {
 
+// Device ordinals a process can drive; per-device host caches are this long.
+constexpr int kMaxDevices = 64;
+// The device current on the calling host thread (0 if it cannot be read).
+int current_device();
+// SM count of the current device (cached per device).
 int device_sms();
+// Raise a kernel's dynamic shared-memory limit on the current device to at
+// least `bytes`; `memo` (kMaxDevices entries, zero-initialised, owned by the
+// caller) remembers what each device was given, so the driver call is made
+// once per kernel and device.  The attribute belongs to the device that is
+// current at the call, so one process driving several GPUs sets it on each.
+template <typename K>
+cudaError_t raise_smem_limit(K* kernel, size_t bytes, size_t* memo) {
+  const int d = current_device();
+  if (d >= 0 && d < kMaxDevices && memo[d] >= bytes) return cudaSuccess;
+  const cudaError_t e =
+      cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+  if (e == cudaSuccess && d >= 0 && d < kMaxDevices) memo[d] = bytes;
+  return e;
+}
 int block_threads();
 // Co-resident CTAs of the fused kernel on this device (0 if unknown).
 int fused_capacity(int enc);

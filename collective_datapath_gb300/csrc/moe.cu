@@ -553,14 +553,9 @@ cudaError_t launch_moe_stage_all(const RunParams& P, cudaStream_t s) {
   k_moe_scan_src<<<nsrc, kMoeThreads, 0, s>>>(P);
   if (cudaError_t e = cudaGetLastError()) return e;
   const size_t bytes = moe_stage_smem_bytes(M.hidden);
-  static size_t configured = 0;
-  if (bytes > 48 * 1024 && bytes > configured) {
-    if (cudaError_t e = cudaFuncSetAttribute(k_moe_stage,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             (int)bytes))
-      return e;
-    configured = bytes;
-  }
+  static size_t memo[kMaxDevices];
+  if (bytes > 48 * 1024)
+    if (cudaError_t e = raise_smem_limit(k_moe_stage, bytes, memo)) return e;
   const int64_t units = (int64_t)nsrc * M.tokens;
   const int grid = (int)std::min<int64_t>(std::max<int64_t>(units, 1), device_sms() * 8);
   k_moe_stage<<<grid, kMoeThreads, bytes, s>>>(P);
@@ -584,14 +579,8 @@ cudaError_t launch_moe_routing(const RunParams& P, cudaStream_t s) {
 
 cudaError_t launch_moe_composed(const RunParams& P, cudaStream_t s) {
   const size_t bytes = moe_composed_smem_bytes(P.moe.hidden);
-  static size_t configured = 0;
-  if (bytes > configured) {
-    if (cudaError_t e = cudaFuncSetAttribute(k_moe_composed,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             (int)bytes))
-      return e;
-    configured = bytes;
-  }
+  static size_t memo[kMaxDevices];
+  if (cudaError_t e = raise_smem_limit(k_moe_composed, bytes, memo)) return e;
   int per_sm = 0;
   if (cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_moe_composed,
                                                                     kMcWarps * 32, bytes))
@@ -615,14 +604,9 @@ cudaError_t launch_moe_consume(const RunParams& P, cudaStream_t s) {
   k_moe_scan_dst<<<P.nranks, kMoeThreads, sizeof(uint32_t) * M.el * P.nranks, s>>>(P);
   if (cudaError_t e = cudaGetLastError()) return e;
   const size_t bytes = moe_copy_smem_bytes(P.nranks, M.experts);
-  static size_t configured = 0;
-  if (bytes > 48 * 1024 && bytes > configured) {
-    if (cudaError_t e = cudaFuncSetAttribute(k_moe_copy,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             (int)bytes))
-      return e;
-    configured = bytes;
-  }
+  static size_t memo[kMaxDevices];
+  if (bytes > 48 * 1024)
+    if (cudaError_t e = raise_smem_limit(k_moe_copy, bytes, memo)) return e;
   k_moe_copy<<<device_sms() * 4, kMoeThreads, bytes, s>>>(P);
   return cudaGetLastError();
 }

@@ -33,7 +33,6 @@ constexpr size_t kStaticMaxElems = size_t(1) << 20;
 constexpr size_t kStaticBytes = kStaticHeaderBytes + 2 * kStaticMaxElems * 4;
 constexpr int kStaticThreads = 256;
 constexpr uint32_t kStaticTileLines = 4 * kStaticThreads;  // one LL8 group per thread
-constexpr int kMaxDevices = 64;
 
 static __device__ __align__(256) char g_static_scratch[kStaticBytes];
 
