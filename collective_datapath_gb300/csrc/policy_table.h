@@ -15,9 +15,8 @@ struct PolicyEntry {
 };
 
 constexpr PolicyEntry kPolicy2[] = {
-    {131072ull, 0, 1, 1, 0},  // LL8/oneshot/fused
-    {671744ull, 2, 1, 1, 0},  // SENT/oneshot/fused
-    {3571712ull, 2, 1, 1, 1024},  // SENT/oneshot/fused/wide
+    {737280ull, 2, 1, 1, 0},  // SENT/oneshot/fused
+    {2506752ull, 2, 1, 1, 1024},  // SENT/oneshot/fused/wide
     {7421952ull, 2, 2, 1, 1024},  // SENT/twoshot/fused/wide
     {16777216ull, 1, 1, 2, 0},  // LL128/oneshot/streamed
     {UINT64_MAX, 1, 2, 2, 0},  // LL128/twoshot/streamed
@@ -25,18 +24,18 @@ constexpr PolicyEntry kPolicy2[] = {
 constexpr PolicyEntry kPolicy4[] = {
     {49152ull, 0, 1, 1, 0},  // LL8/oneshot/fused
     {311296ull, 2, 1, 1, 0},  // SENT/oneshot/fused
-    {2048000ull, 2, 1, 1, 1024},  // SENT/oneshot/fused/wide
+    {1753088ull, 2, 1, 1, 1024},  // SENT/oneshot/fused/wide
     {7421952ull, 2, 2, 1, 1024},  // SENT/twoshot/fused/wide
-    {9060352ull, 1, 1, 2, 0},  // LL128/oneshot/streamed
+    {9125888ull, 1, 1, 2, 0},  // LL128/oneshot/streamed
     {UINT64_MAX, 1, 2, 2, 0},  // LL128/twoshot/streamed
 };
 constexpr PolicyEntry kPolicy8[] = {
-    {16384ull, 0, 1, 1, 0},  // LL8/oneshot/fused
+    {32768ull, 0, 1, 1, 0},  // LL8/oneshot/fused
     {180224ull, 2, 1, 1, 0},  // SENT/oneshot/fused
-    {786432ull, 2, 1, 1, 1024},  // SENT/oneshot/fused/wide
-    {1048576ull, 2, 2, 1, 0},  // SENT/twoshot/fused
+    {425984ull, 2, 1, 1, 1024},  // SENT/oneshot/fused/wide
+    {1425408ull, 2, 2, 1, 0},  // SENT/twoshot/fused
     {5931008ull, 2, 2, 1, 1024},  // SENT/twoshot/fused/wide
-    {33554432ull, 1, 2, 2, 0},  // LL128/twoshot/streamed
+    {51052544ull, 1, 2, 2, 0},  // LL128/twoshot/streamed
     {UINT64_MAX, 1, 2, 3, 0},  // LL128/twoshot/composed
 };
 
