@@ -214,6 +214,15 @@ def cpu_oracle_allreduce(per_rank_mib: int, seed: int = 4, runs: int = 1) -> dic
                       f"counted with the same algorithmic bytes as the GPU line"}
 
 
+def workload_config(mib: int, path: str, world: int) -> dict:
+    """The bench workload, named the same way by both arms."""
+    return {"workload": f"all-reduce, {N_RANKS} emulated ranks, {mib} MiB bf16 per rank, "
+                        f"LL128 lines, twoshot (bandwidth regime)",
+            "n_ranks": N_RANKS, "per_rank_mib": mib, "encoding": "LL128",
+            "algorithm": "twoshot", "path": path, "parallelism": f"replicas{world}",
+            "l2": "inputs (2 GiB) and staging larger than L2; no flush"}
+
+
 def run_reference(args) -> int:
     world, rank, _ = dist_setup()
     if rank != 0:
@@ -232,13 +241,13 @@ def run_reference(args) -> int:
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(sec * 1e3, 3), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": f"all-reduce, {N_RANKS} emulated ranks, {per_rank_mib} MiB "
-                               f"bf16 per rank per step (a bounded sample of the 256 MiB "
-                               f"workload), CPU oracle",
-                   "parallelism": "replicas"},
+        "config": workload_config(args.mib, args.path, world),
         "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1,
                          "kind": "oracle", "host": host_cpu(),
-                         "sample": f"{N_RANKS} ranks x {per_rank_mib} MiB per step"},
+                         "sample": f"each step: the plain C oracle (single thread) on a "
+                                   f"bounded sample of the workload, {N_RANKS} ranks x "
+                                   f"{per_rank_mib} MiB bf16 instead of {args.mib} MiB; GB/s "
+                                   f"counted with the same algorithmic bytes per element"},
         "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
@@ -835,12 +844,7 @@ def main() -> int:
         "steps": K, "warmup": W, "ms_per_step": round(ms_step, 4),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": f"all-reduce, {N_RANKS} emulated ranks, {args.mib} MiB bf16 "
-                               f"per rank, LL128 lines, twoshot (bandwidth regime)",
-                   "n_ranks": N_RANKS, "per_rank_mib": args.mib, "encoding": "LL128",
-                   "algorithm": "twoshot", "path": args.path,
-                   "parallelism": f"replicas{world}",
-                   "l2": "inputs (2 GiB) and staging larger than L2; no flush"},
+        "config": workload_config(args.mib, args.path, world),
         "roofline": {"bound": "hbm", "kernel": names[dom], "achieved": round(achieved, 1),
                      "peak": peaks["hbm_gbs"], "unit": "GB/s",
                      "frac": round(achieved / peaks["hbm_gbs"], 4), "traffic": traffic,
