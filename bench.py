@@ -591,6 +591,44 @@ def atom_ablation(cd, stream, nbytes=256 << 20, stage_bytes=16384, ctas_list=Non
     return out
 
 
+def bounded_staging_row(cd, count, stream, staging_mib=16, steps=5) -> dict:
+    """The bench workload (8 ranks x 256 MiB, LL128 twoshot, composed launch)
+    with each rank's staging image bounded to `staging_mib` MiB per slot:
+    chunks cycle through the chunk slots that fit (Purlin §4.1)."""
+    import torch
+
+    n = N_RANKS
+    coll = cd.Collective(cd.ALLREDUCE, n, count, encoding=cd.COLL_LL128,
+                         algorithm=cd.COLL_TWOSHOT, path=cd.COLL_PATH_COMPOSED,
+                         staging_bytes=staging_mib << 20)
+    full = cd.coll_spec_create(*cd.ALLREDUCE, n, count, encoding=cd.COLL_LL128,
+                               algorithm=cd.COLL_TWOSHOT, path=cd.COLL_PATH_COMPOSED)
+    full_ws = cd.coll_workspace_bytes(full)
+    cd.coll_destroy(full)
+    ins = make_inputs(count, 4)
+    outs = [torch.empty(count, dtype=torch.int16, device="cuda") for _ in range(n)]
+    with torch.cuda.stream(stream):
+        for _ in range(2):
+            coll.run(ins, outs, stream)
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(steps):
+            coll.run(ins, outs, stream)
+        e1.record(stream)
+        stream.synchronize()
+    ms = e0.elapsed_time(e1) / steps
+    b = bytes_allreduce_twoshot(n, count * 2.0, EPS_LL128)
+    st = coll.status(stream)[0]
+    ws = cd.coll_workspace_bytes(coll.spec)
+    coll.close()
+    del coll, ins, outs
+    torch.cuda.empty_cache()
+    return {"ms": round(ms, 4), "GB/s": round(b / ms / 1e6, 1), "algorithmic_bytes": b,
+            "staging_mib_per_rank": staging_mib, "workspace_bytes": ws,
+            "workspace_bytes_unbounded": full_ws, "status": st}
+
+
 def sentinel_row(cd, count, stream, steps=5) -> dict:
     """8 ranks x `count` bf16 all-reduce, twoshot, sentinel packs, streamed.
     Algorithmic bytes are the LL form with epsilon = 1 (no readiness bytes);
@@ -711,7 +749,7 @@ def main() -> int:
     ap.add_argument("--row", default=None,
                     help="run one extra row alone and print it (profiling runs): "
                          "moe, moe_streamed, rs, rs_composed, ag, a2a, a2a_composed, "
-                         "sentinel, f32, rsv, agv, a2av")
+                         "sentinel, f32, staging16, rsv, agv, a2av")
     ap.add_argument("--moe-tokens", type=int, default=4096,
                     help="tokens per rank of the MoE rows (the bench line uses 4096)")
     ap.add_argument("--atom-case", default=None,
@@ -767,6 +805,7 @@ def main() -> int:
                                                   path=cd.COLL_PATH_COMPOSED),
             "sentinel": lambda: sentinel_row(cd, count, stream),
             "f32": lambda: f32_row(cd, args.mib << 20, stream),
+            "staging16": lambda: bounded_staging_row(cd, count, stream),
             "rsv": lambda: v_row(cd, "REDUCE_SCATTER_V", args.mib << 20, stream),
             "agv": lambda: v_row(cd, "ALLGATHER_V", args.mib << 20, stream),
             "a2av": lambda: v_row(cd, "ALLTOALL_V", args.mib << 20, stream),
@@ -923,6 +962,7 @@ def main() -> int:
             "all_to_all_v_zipf_256MiB": v_row(cd, "ALLTOALL_V", 256 << 20, stream),
             "allreduce_256MiB_sentinel_twoshot": sentinel_row(cd, count, stream),
             "allreduce_256MiB_f32_composed": f32_row(cd, 256 << 20, stream),
+            "allreduce_256MiB_composed_staging_16MiB": bounded_staging_row(cd, count, stream),
             "pipeline_depth_ablation_256MiB": atom_ablation(cd, stream),
         }
         line["latency_us_per_op"] = latency_sweep(cd, stream)

@@ -56,7 +56,7 @@ class coll_options_t(ctypes.Structure):
                 ("hidden", ctypes.c_int), ("topk", ctypes.c_int),
                 ("experts", ctypes.c_int), ("max_rows", ctypes.c_int),
                 ("vcounts", ctypes.POINTER(ctypes.c_uint64)), ("nvcounts", ctypes.c_int),
-                ("slots", ctypes.c_int)]
+                ("slots", ctypes.c_int), ("staging_bytes", ctypes.c_uint64)]
 
 
 _vp = ctypes.c_void_p

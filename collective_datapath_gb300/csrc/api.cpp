@@ -169,6 +169,22 @@ ComposedParams composed_shape(const coll_spec* s) {
   q.nchunks = (uint32_t)std::max<uint64_t>(1, (max_lines + chunk - 1) / chunk);
   q.lag = std::max(1, lag);
   q.lag2 = lag2 < 1 ? q.lag : lag2;
+  // Bounded staging (Purlin §4.1): chunk c uses chunk slot c mod W of the
+  // staging images.  A stage waits for the folds (copies) that read the
+  // slot's previous chunk and a fold for the gathers of its published slot,
+  // so both lags stay below W: every task then waits only for tasks earlier
+  // in the queue.  The chunk shrinks (to no less than kComposedMinChunk)
+  // until the images hold two slots.
+  q.ring = 0;
+  if (p.ring_lines > 0) {
+    while (q.chunk_lines > kComposedMinChunk &&
+           p.ring_lines / ((uint64_t)p.n * q.chunk_lines) < 2)
+      q.chunk_lines /= 2;
+    q.nchunks = (uint32_t)std::max<uint64_t>(1, (max_lines + q.chunk_lines - 1) / q.chunk_lines);
+    q.ring = (uint32_t)(p.ring_lines / ((uint64_t)p.n * q.chunk_lines));
+    q.lag = std::min(q.lag, (int)q.ring - 1);
+    q.lag2 = std::min(q.lag2, (int)q.ring - 1);
+  }
   q.discard = discard;
   q.variant = variant >= 0 && variant <= 2 ? variant : 0;
   q.mode = p.kind == CK_REDUCE_SCATTER ? 1 : (p.kind == CK_ALLTOALL ? 2 : 0);
@@ -274,6 +290,7 @@ coll_status_t coll_spec_create(coll_layout_t in_layout, coll_layout_t out_layout
   d.experts = o.experts;
   d.max_rows = o.max_rows;
   d.slots = o.slots;
+  d.staging_bytes = o.staging_bytes;
   if (o.vcounts != nullptr && o.nvcounts > 0)
     d.vcounts.assign(o.vcounts, o.vcounts + o.nvcounts);
   device_shape(o.encoding, &d.sms, &d.fused_capacity);
@@ -361,6 +378,7 @@ coll_status_t coll_set_routing(coll_spec_t* s, int rank, const int32_t* dev_topk
 coll_status_t coll_stage(coll_spec_t* s, int rank, const void* dev_in,
                          coll_stream_t stream) {
   if (s == nullptr || rank < 0 || rank >= s->plan.n) return COLL_ERR_INVALID;
+  if (s->plan.ring_lines > 0) return COLL_ERR_UNSUPPORTED;  // staging cycles inside the run
   if (!s->bound) return COLL_ERR_STATE;
   if (s->plan.in_elems[rank] > 0 && dev_in == nullptr) return COLL_ERR_INVALID;
   if (!aligned16(dev_in)) return COLL_ERR_ALIGN;
@@ -380,6 +398,7 @@ coll_status_t coll_run(coll_spec_t* s, const void* const* dev_ins, void* const* 
                        coll_stream_t stream) {
   if (s == nullptr) return COLL_ERR_INVALID;
   if (!s->bound) return COLL_ERR_STATE;
+  if (dev_ins == nullptr && s->plan.ring_lines > 0) return COLL_ERR_UNSUPPORTED;
   if (coll_status_t e = check_outs(s, dev_outs)) return e;
   if (dev_ins != nullptr)
     if (coll_status_t e = check_ins(s, dev_ins)) return e;
@@ -413,9 +432,11 @@ coll_status_t coll_run(coll_spec_t* s, const void* const* dev_ins, void* const* 
   const bool empty = p.items1.empty() && p.items2.empty();
   if (dev_ins != nullptr && p.path == COLL_PATH_COMPOSED && !empty) {
     P.cp = composed_shape(s);
-    const int cap = composed_capacity(P.cp.variant);
+    const int cap = composed_capacity(P.cp.variant, P.cp.ring > 0);
     if (cap < 3) return COLL_ERR_CUDA;
-    P.advance_epoch = 1;
+    // cycling staging: chunk c is notified with epoch + c, so the run moves
+    // the epoch past all of them, by an odd step (Purlin §4.2)
+    P.advance_epoch = P.cp.ring > 0 ? (int)(P.cp.nchunks | 1u) : 1;
     return cuda_status(launched(s, launch_composed(P, cap, st), st));
   }
   if (dev_ins != nullptr && p.path == COLL_PATH_FUSED && !empty &&
@@ -518,6 +539,7 @@ coll_status_t coll_staging_layout(const coll_spec_t* s, int region, int slot, in
   if (s == nullptr || rank < 0 || rank >= s->plan.n || slot < 0 || slot >= s->plan.slots)
     return COLL_ERR_INVALID;
   const Plan& p = s->plan;
+  if (p.ring_lines > 0) return COLL_ERR_UNSUPPORTED;  // chunk slots, not segments
   const std::vector<Seg>* segs;
   const Region* R;
   if (region == 0) {
@@ -560,6 +582,7 @@ coll_status_t coll_run_late(coll_spec_t* s, const void* const* dev_ins, void* co
                             coll_stream_t stream) {
   if (s == nullptr || dev_ins == nullptr || dev_order == nullptr || n_late == nullptr)
     return COLL_ERR_INVALID;
+  if (s->plan.ring_lines > 0) return COLL_ERR_UNSUPPORTED;
   if (!s->bound) return COLL_ERR_STATE;
   const Plan& p = s->plan;
   if (p.kind == CK_ALLGATHER || p.kind == CK_ALLGATHER_V || p.kind == CK_ALLTOALL_V ||

@@ -109,11 +109,15 @@ struct Piece {
 };
 
 __device__ __forceinline__ void fill_stage_piece(const RunParams& P, Piece* pc, int c, int p,
-                                                 uint64_t e) {
+                                                 uint64_t e, uint32_t W) {
   const int k = threadIdx.x;
   const uint32_t t0 = (uint32_t)c * P.cp.chunk_lines;
   pc[k].src = reinterpret_cast<const char*>(P.in[p] + P.seg_in0[k] + (uint64_t)t0 * kLL128Elems);
-  pc[k].dst = image_bytes(P, P.P, e, p) + (P.seg_line0[k] + t0) * kLL128LineBytes;
+  // cycling staging: chunk slot c mod W holds the N partitions' lines of the
+  // chunk, partition-major; otherwise each partition's lines sit in place
+  const uint64_t line = W ? ((uint64_t)(c % W) * P.nranks + k) * P.cp.chunk_lines
+                         : P.seg_line0[k] + t0;
+  pc[k].dst = image_bytes(P, P.P, e, p) + line * kLL128LineBytes;
   pc[k].nl = chunk_lines_of(P, k, t0);
   const int64_t lk = (int64_t)P.seg_elems[k] - (int64_t)t0 * kLL128Elems;
   pc[k].left = (int)(lk < (int64_t)P.cp.chunk_lines * kLL128Elems ? lk
@@ -121,10 +125,11 @@ __device__ __forceinline__ void fill_stage_piece(const RunParams& P, Piece* pc, 
 }
 
 __device__ __forceinline__ void fill_gather_piece(const RunParams& P, Piece* pc, int c, int d,
-                                                  uint64_t e) {
+                                                  uint64_t e, uint32_t W) {
   const int r = threadIdx.x;
   const uint32_t t0 = (uint32_t)c * P.cp.chunk_lines;
-  pc[r].src = image_bytes(P, P.AG, e, r) + (uint64_t)t0 * kLL128LineBytes;
+  const uint64_t line = W ? (uint64_t)(c % W) * P.cp.chunk_lines : t0;
+  pc[r].src = image_bytes(P, P.AG, e, r) + line * kLL128LineBytes;
   pc[r].dst = reinterpret_cast<char*>(P.out[d] + P.seg_in0[r] + (uint64_t)t0 * kLL128Elems);
   pc[r].nl = chunk_lines_of(P, r, t0);
   const int64_t lr = (int64_t)P.seg_elems[r] - (int64_t)t0 * kLL128Elems;
@@ -134,10 +139,12 @@ __device__ __forceinline__ void fill_gather_piece(const RunParams& P, Piece* pc,
 
 // All-to-all: destination d copies segment d of every source r.
 __device__ __forceinline__ void fill_a2a_piece(const RunParams& P, Piece* pc, int c, int d,
-                                               uint64_t e) {
+                                               uint64_t e, uint32_t W) {
   const int r = threadIdx.x;
   const uint32_t t0 = (uint32_t)c * P.cp.chunk_lines;
-  pc[r].src = image_bytes(P, P.P, e, r) + (P.seg_line0[d] + t0) * kLL128LineBytes;
+  const uint64_t line = W ? ((uint64_t)(c % W) * P.nranks + d) * P.cp.chunk_lines
+                         : P.seg_line0[d] + t0;
+  pc[r].src = image_bytes(P, P.P, e, r) + line * kLL128LineBytes;
   pc[r].dst = reinterpret_cast<char*>(P.out[d] + P.seg_in0[r] + (uint64_t)t0 * kLL128Elems);
   pc[r].nl = chunk_lines_of(P, d, t0);
   const int64_t ld = (int64_t)P.seg_elems[d] - (int64_t)t0 * kLL128Elems;
@@ -191,13 +198,15 @@ __device__ __forceinline__ void stage_task(const Piece* pc, uint32_t wbase, int 
 // of owner r (all-reduce) or write it into rank r's output (reduce-scatter).
 template <int kCWarps, int kCRing>
 __device__ __forceinline__ bool fold_task(const RunParams& P, uint32_t wbase, int lane, int warp,
-                                          int c, int r, uint64_t e, bool to_out) {
+                                          int c, int r, uint64_t e, uint64_t seq, bool to_out,
+                                          uint32_t W) {
   constexpr int kCFoldStages = kCRing / kMaxRanks;  // rows of all N images per warp
   const int n = P.nranks;
   const uint32_t t0 = (uint32_t)c * P.cp.chunk_lines;
   const int nl = chunk_lines_of(P, r, t0);
   const int li = lane >> 3;
-  const uint64_t src_line = P.seg_line0[r] + t0;
+  const uint64_t src_line =
+      W ? ((uint64_t)(c % W) * n + r) * P.cp.chunk_lines : P.seg_line0[r] + t0;
   // rank p's rows of this piece start at src0 + p * rank_bytes
   const char* src0 = image_bytes(P, P.P, e, 0) + src_line * kLL128LineBytes;
   const uint64_t rb = P.P.rank_bytes;
@@ -217,7 +226,8 @@ __device__ __forceinline__ bool fold_task(const RunParams& P, uint32_t wbase, in
   };
 #pragma unroll
   for (int j = 0; j < kCFoldStages; ++j) issue(j);
-  char* ag = image_bytes(P, P.AG, e, r) + (uint64_t)t0 * kLL128LineBytes;
+  char* ag = image_bytes(P, P.AG, e, r) +
+             (W ? (uint64_t)(c % W) * P.cp.chunk_lines : (uint64_t)t0) * kLL128LineBytes;
   bool ok = true;
   for (int j = 0; j < nj; ++j) {
     cp_async_wait<kCFoldStages - 1>();
@@ -232,7 +242,7 @@ __device__ __forceinline__ bool fold_task(const RunParams& P, uint32_t wbase, in
     bool ready = true;
 #pragma unroll
     for (int p = 0; p < kMaxRanks; ++p)
-      if (p < n) ready = ready && ll128_chunk_ready(s[p], lane, valid, e);
+      if (p < n) ready = ready && ll128_chunk_ready(s[p], lane, valid, seq);
     if (!__all_sync(0xFFFFFFFFu, ready)) {
       // the producer's flag was set, so this only happens if the protocol
       // is broken: wait for the numbers on global memory, bounded
@@ -240,10 +250,10 @@ __device__ __forceinline__ bool fold_task(const RunParams& P, uint32_t wbase, in
 #pragma unroll
       for (int p = 0; p < kMaxRanks; ++p) {
         if (p < n && ok) {
-          const bool rp = ll128_chunk_ready(s[p], lane, valid, e);
+          const bool rp = ll128_chunk_ready(s[p], lane, valid, seq);
           if (!__all_sync(0xFFFFFFFFu, rp)) {
             const char* grow = src0 + p * rb + (size_t)rr * kRowBytes;
-            ok = ll128_wait_chunk(P, grow, lane, rp, e, p, (int64_t)row_line);
+            ok = ll128_wait_chunk(P, grow, lane, rp, seq, p, (int64_t)row_line);
             if (ok && valid) s[p] = ld_v4(grow + 16 * lane);
           }
         }
@@ -262,7 +272,7 @@ __device__ __forceinline__ bool fold_task(const RunParams& P, uint32_t wbase, in
       ll128_write_payload(P.out[r] + line * kLL128Elems, res, lane,
                           (int64_t)P.seg_elems[r] - (int64_t)line * kLL128Elems);
     } else {
-      ll128_store_row<false>(ag + (size_t)rr * kRowBytes, res, lane, nl_row, e);
+      ll128_store_row<false>(ag + (size_t)rr * kRowBytes, res, lane, nl_row, seq);
     }
   }
   cp_async_wait<0>();
@@ -324,8 +334,11 @@ __device__ __forceinline__ bool gather_task(const RunParams& P, const Piece* pc,
 
 // Counts one finished gather of chunk c in this epoch; true for the N-th.
 // Called by one thread after its CTA's reads of the chunk completed.
-__device__ __forceinline__ bool last_gather(const RunParams& P, int c, uint64_t e) {
+__device__ __forceinline__ bool last_gather(const RunParams& P, int c, uint64_t e, bool release) {
   unsigned long long* cnt = reinterpret_cast<unsigned long long*>(P.cp.gather_cnt + c);
+  // cycling staging: the count frees the published slot, so the CTA's reads
+  // of the chunk must come before it
+  if (release) fence_acq_rel_gpu();
   unsigned long long old = ld_relaxed_u64(cnt), want;
   for (;;) {
     want = (old >> 8) == e ? old + 1 : ((e << 8) | 1ull);
@@ -336,7 +349,34 @@ __device__ __forceinline__ bool last_gather(const RunParams& P, int c, uint64_t 
   return (int)(want & 0xFFull) == P.nranks;
 }
 
-template <int kCWarps, int kCRing, int kMinBlocks>
+// Thread 0 waits (bounded) until all N gathers of chunk c finished in this
+// epoch, then fences (acquire); the caller's __syncthreads hands the order
+// to the CTA.  Cycling staging: the fold that reuses the chunk's published
+// slot waits for this.
+__device__ __forceinline__ bool acquire_gathers(const RunParams& P, int c, uint64_t e) {
+  bool ok = true;
+  if (threadIdx.x == 0) {
+    const uint64_t want = (e << 8) | (uint64_t)P.nranks;
+    const uint64_t* cnt = P.cp.gather_cnt + c;
+    if (ld_relaxed_u64(cnt) != want) {
+      Waiter w;
+      while (ld_relaxed_u64(cnt) != want) {
+        if (w.expired(P.ws, P.timeout_ns)) {
+          latch_error(P.ws, kStatusTimeout, 0xFFFFFFFFu, -5);
+          ok = false;
+          break;
+        }
+        __nanosleep(64);
+      }
+    }
+    fence_acq_rel_gpu();
+  }
+  return ok;
+}
+
+// kCycle: the staging images cycle through P.cp.ring chunk slots (a
+// separate instantiation, so the default launch carries none of it)
+template <int kCWarps, int kCRing, int kMinBlocks, bool kCycle>
 __global__ void __launch_bounds__(kCWarps * 32, kMinBlocks) k_composed_ll128(RunParams P) {
   extern __shared__ __align__(128) char smem[];
   __shared__ Piece s_piece[kMaxRanks];
@@ -377,25 +417,35 @@ __global__ void __launch_bounds__(kCWarps * 32, kMinBlocks) k_composed_ll128(Run
       __syncthreads();
       continue;
     }
+    // cycling staging: chunk c's lines carry e + c, and its chunk slot was
+    // last used by chunk c - W, whose readers must be done with it
+    const uint32_t W = kCycle ? Q.ring : 0u;
+    const uint64_t seq = W ? e + (uint64_t)c : e;
+    const bool reuse = W && c >= (int)W;
     if (kind == 0) {
-      if ((int)threadIdx.x < n) fill_stage_piece(P, s_piece, c, x, e);
+      if ((int)threadIdx.x < n) fill_stage_piece(P, s_piece, c, x, e, W);
+      if (reuse && !acquire_flags(P, Q.flag_fold + (size_t)(c - (int)W) * n, n, e))
+        s_ok = 0;
       __syncthreads();
-      stage_task<kCWarps, kCRing>(s_piece, wbase, lane, warp, n, rsh, e);
+      if (!s_ok) break;
+      stage_task<kCWarps, kCRing>(s_piece, wbase, lane, warp, n, rsh, seq);
       release_flag(Q.flag_stage + (size_t)c * n + x, e, s_ok);
     } else if (kind == 1 && Q.mode != 2) {
       if (!acquire_flags(P, Q.flag_stage + (size_t)c * n, n, e)) s_ok = 0;
+      if (reuse && Q.mode == 0 && !acquire_gathers(P, c - (int)W, e)) s_ok = 0;
       __syncthreads();
       if (!s_ok) break;
-      if (!fold_task<kCWarps, kCRing>(P, wbase, lane, warp, c, x, e, Q.mode == 1)) s_ok = 0;
+      if (!fold_task<kCWarps, kCRing>(P, wbase, lane, warp, c, x, e, seq, Q.mode == 1, W))
+        s_ok = 0;
       release_flag(Q.flag_fold + (size_t)c * n + x, e, s_ok);
     } else if (kind == 1) {
       // all-to-all: segment x of every source's chunk c into rank x's output;
       // each staged line has this one reader, which drops it once copied
-      if ((int)threadIdx.x < n) fill_a2a_piece(P, s_piece, c, x, e);
+      if ((int)threadIdx.x < n) fill_a2a_piece(P, s_piece, c, x, e, W);
       if (!acquire_flags(P, Q.flag_stage + (size_t)c * n, n, e)) s_ok = 0;
       __syncthreads();
       if (!s_ok) break;
-      if (!gather_task<kCWarps, kCRing>(P, s_piece, wbase, lane, warp, rsh, e)) s_ok = 0;
+      if (!gather_task<kCWarps, kCRing>(P, s_piece, wbase, lane, warp, rsh, seq)) s_ok = 0;
       __syncthreads();
       if (s_ok && Q.discard)
         for (int r = 0; r < n; ++r) {
@@ -403,19 +453,28 @@ __global__ void __launch_bounds__(kCWarps * 32, kMinBlocks) k_composed_ll128(Run
           for (int j = threadIdx.x; j < nl; j += blockDim.x)
             discard_l2_line(s_piece[r].src + (size_t)j * kLL128LineBytes);
         }
-      __syncthreads();  // s_piece is refilled by the next task
+      // cycling staging: the copy's completion (a stage reusing the chunk
+      // slot waits for it); either barrier keeps s_piece until every thread
+      // is done with it
+      if (W)
+        release_flag(Q.flag_fold + (size_t)c * n + x, e, s_ok);
+      else
+        __syncthreads();
     } else {
-      if ((int)threadIdx.x < n) fill_gather_piece(P, s_piece, c, x, e);
+      if ((int)threadIdx.x < n) fill_gather_piece(P, s_piece, c, x, e, W);
       if (!acquire_flags(P, Q.flag_fold + (size_t)c * n, n, e)) s_ok = 0;
       __syncthreads();
       if (!s_ok) break;
-      if (!gather_task<kCWarps, kCRing>(P, s_piece, wbase, lane, warp, rsh, e)) s_ok = 0;
+      if (!gather_task<kCWarps, kCRing>(P, s_piece, wbase, lane, warp, rsh, seq)) s_ok = 0;
       __syncthreads();
-      if (warp == 0 && s_ok && Q.discard == 1) {
+      if (warp == 0 && s_ok && (Q.discard == 1 || W)) {
         // warp 0 alone: it also fills the next task's descriptors, so it
         // is done with these before anyone reads the next ones
-        const bool last = __shfl_sync(0xFFFFFFFFu, lane == 0 ? (int)last_gather(P, c, e) : 0, 0);
-        if (last)
+        // with cycling staging the count frees the published slot for the fold
+        // of chunk c + W, so a discard after it could drop that fold's lines:
+        // published lines are then left in place to be overwritten
+        const bool last = __shfl_sync(0xFFFFFFFFu, lane == 0 ? (int)last_gather(P, c, e, W != 0) : 0, 0);
+        if (last && Q.discard == 1 && !W)
           for (int r = 0; r < n; ++r) {
             const int nl = s_piece[r].nl;
             for (int j = lane; j < nl; j += 32)
@@ -428,22 +487,27 @@ __global__ void __launch_bounds__(kCWarps * 32, kMinBlocks) k_composed_ll128(Run
   finish_run(P, e);
 }
 
-template <int W, int R, int B>
+template <int W, int R, int B, bool C>
 static int capacity_of() {
   static size_t memo[kMaxDevices];
   const int bytes = (int)((size_t)W * R * kRowBytes);
-  if (raise_smem_limit(k_composed_ll128<W, R, B>, (size_t)bytes, memo) != cudaSuccess) return 0;
+  if (raise_smem_limit(k_composed_ll128<W, R, B, C>, (size_t)bytes, memo) != cudaSuccess) return 0;
   int per_sm = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_composed_ll128<W, R, B>, W * 32,
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_composed_ll128<W, R, B, C>, W * 32,
                                                     bytes) != cudaSuccess)
     return 0;
   return per_sm * device_sms();
 }
 
-int composed_capacity(int variant) {
-  if (variant == 1) return capacity_of<8, 24, 2>();
-  if (variant == 2) return capacity_of<4, 16, 6>();
-  return capacity_of<8, 16, 3>();
+int composed_capacity(int variant, bool cycle) {
+  if (cycle) {
+    if (variant == 1) return capacity_of<8, 24, 2, true>();
+    if (variant == 2) return capacity_of<4, 16, 6, true>();
+    return capacity_of<8, 16, 3, true>();
+  }
+  if (variant == 1) return capacity_of<8, 24, 2, false>();
+  if (variant == 2) return capacity_of<4, 16, 6, false>();
+  return capacity_of<8, 16, 3, false>();
 }
 
 cudaError_t launch_composed(const RunParams& P, int grid, cudaStream_t s) {
@@ -458,9 +522,14 @@ cudaError_t launch_composed(const RunParams& P, int grid, cudaStream_t s) {
   attr[0].val.cooperative = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  if (v == 1) return cudaLaunchKernelEx(&cfg, k_composed_ll128<8, 24, 2>, P);
-  if (v == 2) return cudaLaunchKernelEx(&cfg, k_composed_ll128<4, 16, 6>, P);
-  return cudaLaunchKernelEx(&cfg, k_composed_ll128<8, 16, 3>, P);
+  if (P.cp.ring > 0) {
+    if (v == 1) return cudaLaunchKernelEx(&cfg, k_composed_ll128<8, 24, 2, true>, P);
+    if (v == 2) return cudaLaunchKernelEx(&cfg, k_composed_ll128<4, 16, 6, true>, P);
+    return cudaLaunchKernelEx(&cfg, k_composed_ll128<8, 16, 3, true>, P);
+  }
+  if (v == 1) return cudaLaunchKernelEx(&cfg, k_composed_ll128<8, 24, 2, false>, P);
+  if (v == 2) return cudaLaunchKernelEx(&cfg, k_composed_ll128<4, 16, 6, false>, P);
+  return cudaLaunchKernelEx(&cfg, k_composed_ll128<8, 16, 3, false>, P);
 }
 
 }  // namespace coll

@@ -334,6 +334,14 @@ int derive(const DeriveInput& in, Plan& p) {
       p.algorithm = (n <= 2 || in_bytes_per_rank <= 512 * 1024) ? COLL_ONESHOT : COLL_TWOSHOT;
   }
   p.path = path;
+  // Bounded staging (Purlin §4.1) is a mode of the composed launch: with a
+  // capacity below the message, AUTO takes the composed launch and any
+  // other path is refused (its kernels address the whole message).
+  const bool composable = p.enc == ENC_LL128 &&
+                          ((p.kind == CK_ALLREDUCE && p.algorithm == COLL_TWOSHOT) ||
+                           p.kind == CK_REDUCE_SCATTER || p.kind == CK_ALLTOALL);
+  const bool capped = in.staging_bytes > 0;
+  if (capped && p.path == COLL_PATH_AUTO && composable) p.path = COLL_PATH_COMPOSED;
   if (p.path == COLL_PATH_AUTO) {
     if (in_bytes_per_rank <= 256 * 1024 && p.enc != ENC_LL128)
       p.path = COLL_PATH_FUSED;
@@ -635,6 +643,16 @@ int derive(const DeriveInput& in, Plan& p) {
   }
   off = round_up(off, 4096);
   const uint64_t lb = (uint64_t)line_bytes(p.enc);
+  if (capped && in.staging_bytes < p.p_rank_lines * lb) {
+    if (p.path != COLL_PATH_COMPOSED) return COLL_ERR_UNSUPPORTED;
+    // chunk slots of N partitions x chunk lines; at least two slots of the
+    // smallest chunk
+    p.ring_lines = in.staging_bytes / lb / ((uint64_t)n * kComposedMinChunk) *
+                   ((uint64_t)n * kComposedMinChunk);
+    if (p.ring_lines < 2ull * n * kComposedMinChunk) return COLL_ERR_INVALID;
+    p.p_rank_lines = p.ring_lines;
+    if (p.ag_rank_lines > 0) p.ag_rank_lines = std::min(p.ag_rank_lines, p.ring_lines / n);
+  }
   p.P.rank_bytes = round_up(p.p_rank_lines * lb, 4096);
   p.P.slot_bytes = p.P.rank_bytes * (uint64_t)n;
   p.P.slot_mask = (uint64_t)p.slots - 1;

@@ -39,6 +39,7 @@ struct DeriveInput {
   int tokens, hidden, topk, experts, max_rows;
   std::vector<uint64_t> vcounts;  // V collectives (see coll.h)
   int slots;                      // staging slots: 2 or 4 (0 = 2)
+  uint64_t staging_bytes;         // per rank image and slot; 0 = whole message
   int sms;             // device SM count (a default when no device is present)
   int fused_capacity;  // co-resident CTAs of the fused kernel
 };
@@ -75,6 +76,9 @@ struct Plan {
   // composed twoshot: completion flags for chunks of at least
   // kComposedMinChunk lines (stage, fold: [chunks][N] u64; gather: [chunks] u64)
   uint64_t off_cflags = 0, composed_max_chunks = 0;
+  // composed launch with bounded staging: lines of each rank's staging
+  // image per slot (chunks cycle through it); 0 = one place per chunk
+  uint64_t ring_lines = 0;
   Region P, AG;
   uint64_t ws_bytes;
 };

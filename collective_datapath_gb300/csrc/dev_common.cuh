@@ -243,7 +243,7 @@ __device__ __forceinline__ void finish_run(const RunParams& P, uint64_t epoch) {
   // the next run's counters
   st_relaxed_u32(&h->started[(epoch + 1) & 1], 0u);
   st_relaxed_u32(&h->task_next[(epoch + 1) & 1], 0u);
-  st_relaxed_u64(&h->epoch, epoch + 1);
+  st_relaxed_u64(&h->epoch, epoch + (uint64_t)P.advance_epoch);
 }
 
 }  // namespace coll

@@ -43,7 +43,7 @@ cudaError_t launch_stage_pipe(const RunParams& P, int grid, cudaStream_t s);
 cudaError_t launch_withhold(const RunParams& P, cudaStream_t s);
 // Composed twoshot all-reduce: co-resident CTAs of the persistent kernel, and
 // the launch (P.cp filled in).
-int composed_capacity(int variant);
+int composed_capacity(int variant, bool cycle);
 cudaError_t launch_composed(const RunParams& P, int grid, cudaStream_t s);
 // MoE dispatch: routing + gather-stage of one source (P.stage_rank) or all,
 // then the destination scan + validated copy (ends the run).

@@ -128,6 +128,9 @@ struct ComposedParams {
   int mode;              // 0 all-reduce: stage, fold + publish, gather;
                          // 1 reduce-scatter: stage, fold into the outputs;
                          // 2 all-to-all: stage, copy into the outputs
+  uint32_t ring;         // chunk slots the staging images cycle through (0: none,
+                         // every chunk has its own place); staged and published
+                         // lines of chunk c then carry epoch + c
   uint64_t* flag_stage;  // [nchunks][N]: epoch once rank p staged chunk c
   uint64_t* flag_fold;   // [nchunks][N]: epoch once owner r published chunk c
   uint64_t* gather_cnt;  // [nchunks]: (epoch << 8) | gathers of chunk c done
@@ -162,7 +165,9 @@ struct RunParams {
   uint64_t seg_in0[kMaxRanks];
   int interleave1, interleave2;   // streamed consume walks ranks interleaved
   int stage_rank;                 // streamed stage of one rank, -1 = all
-  int advance_epoch;              // this launch ends the run
+  int advance_epoch;              // > 0: this launch ends the run and adds
+                                  // this much to the epoch (odd; 1 but for
+                                  // the composed launch with cycling staging)
   // late producers (fault-injection runs)
   const int64_t* late_order[kMaxRanks];
   int64_t late_n[kMaxRanks];

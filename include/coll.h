@@ -191,6 +191,25 @@ typedef struct {
     int slots;           /* staging slots used in turn by consecutive runs:
                             2 (default, 0 means 2) or 4 (flash-comm §4.2
                             rotating slots; twice the staging memory) */
+    uint64_t staging_bytes; /* capacity of each rank's staging image per
+                            slot, in bytes; 0 (default) = the whole message.
+                            Purlin §4.1: when the staging a collective needs
+                            exceeds the capacity, chunks cycle through a
+                            fixed number of chunk slots.  A capacity below
+                            the message requires the composed launch (the
+                            LL128 twoshot all-reduce, reduce-scatter or
+                            all-to-all; path AUTO selects it) and must hold
+                            at least 4096 * nranks bytes (two chunk slots of
+                            the smallest chunk), else COLL_ERR_UNSUPPORTED /
+                            COLL_ERR_INVALID.  Such a spec runs only through
+                            coll_run with inputs (and coll_run_host):
+                            coll_stage, coll_run without inputs,
+                            coll_stage_withheld, coll_run_late and
+                            coll_staging_layout return COLL_ERR_UNSUPPORTED.
+                            Staged lines of chunk c carry epoch + c, and a
+                            run advances the epoch by its chunk count
+                            rounded up to an odd number (Purlin §4.2), so
+                            consecutive runs still alternate slots. */
 } coll_options_t;
 
 typedef struct coll_spec coll_spec_t;

@@ -371,3 +371,47 @@ def test_atom_copy_argument_validation(cd):
     assert status_of(None, b, 4096) == cd.COLL_ERR_INVALID
     assert status_of(a, a + 4080, 4096) == cd.COLL_ERR_INVALID     # overlapping ranges
     assert status_of(a + 4080, a, 4096) == cd.COLL_ERR_INVALID
+
+
+def test_bounded_staging_validation(cd):
+    """Purlin §4.1 staging capacity: only the composed launch cycles chunk
+    slots; a capacity below two slots of the smallest chunk, another path or
+    a non-composable collective is refused, and a ring-mode spec refuses the
+    entry points that address the whole message (all on the host)."""
+    n, count = 8, 8 * 60 * 4096
+    kw = dict(encoding=cd.COLL_LL128, algorithm=cd.COLL_TWOSHOT)
+
+    def status_of(triple, **opts):
+        try:
+            s = cd.coll_spec_create(*triple, n, count, **opts)
+        except cd.CollError as e:
+            return e.status
+        cd.coll_destroy(s)
+        return cd.COLL_OK
+
+    assert status_of(cd.ALLREDUCE, staging_bytes=1 << 20, path=cd.COLL_PATH_STREAMED,
+                     **kw) == cd.COLL_ERR_UNSUPPORTED
+    assert status_of(cd.ALLREDUCE, staging_bytes=4096 * n - 128, path=cd.COLL_PATH_COMPOSED,
+                     **kw) == cd.COLL_ERR_INVALID
+    assert status_of(cd.ALLGATHER, staging_bytes=1 << 16,
+                     encoding=cd.COLL_LL128) == cd.COLL_ERR_UNSUPPORTED
+    assert status_of(cd.ALLREDUCE, staging_bytes=4096 * n, path=cd.COLL_PATH_COMPOSED,
+                     **kw) == cd.COLL_OK
+
+    def ws(**opts):
+        s = cd.coll_spec_create(*cd.ALLREDUCE, n, count, **kw, **opts)
+        b = cd.coll_workspace_bytes(s)
+        cd.coll_destroy(s)
+        return b
+
+    full = ws(path=cd.COLL_PATH_COMPOSED)
+    assert ws(staging_bytes=1 << 40, path=cd.COLL_PATH_COMPOSED) == full  # no cycling needed
+    assert ws(staging_bytes=1 << 20) < ws(staging_bytes=1 << 21) < full   # AUTO -> composed
+    s = cd.coll_spec_create(*cd.ALLREDUCE, n, count, staging_bytes=1 << 20, **kw)
+    assert cd.coll_debug_plan(s)["path"] == cd.COLL_PATH_COMPOSED
+    for call in (lambda: cd.coll_stage(s, 0, 0x1000, stream=0),
+                 lambda: cd.coll_staging_layout(s, 0, 0, 0, 0)):
+        with pytest.raises(cd.CollError) as e:
+            call()
+        assert e.value.status == cd.COLL_ERR_UNSUPPORTED
+    cd.coll_destroy(s)

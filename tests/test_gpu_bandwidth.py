@@ -132,16 +132,18 @@ def test_bandwidth_reduce_scatter_and_all_gather(cd, inputs, mib):
     torch.cuda.empty_cache()
 
 
-@pytest.mark.parametrize("mib", [32, 256])
-def test_bandwidth_allreduce_composed_twoshot(cd, inputs, mib):
+@pytest.mark.parametrize("mib,staging_mib", [(32, 0), (256, 0), (256, 8)])
+def test_bandwidth_allreduce_composed_twoshot(cd, inputs, mib, staging_mib):
     """The one-launch twoshot at full size: sampled against the oracle, and
-    byte-identical to the stream-ordered twoshot on every element."""
+    byte-identical to the stream-ordered twoshot on every element; also with
+    the staging images bounded to a few MiB, chunks cycling through them."""
     import torch
 
     count = mib * 1024 * 1024 // 2
     ins = [x[:count] for x in inputs]
     comp = cd.Collective(cd.ALLREDUCE, N, count, encoding=cd.COLL_LL128,
-                         algorithm=cd.COLL_TWOSHOT, path=cd.COLL_PATH_COMPOSED)
+                         algorithm=cd.COLL_TWOSHOT, path=cd.COLL_PATH_COMPOSED,
+                         staging_bytes=staging_mib << 20)
     outs = [torch.empty(count, dtype=torch.int16, device="cuda") for _ in range(N)]
     for _ in range(2):
         comp.run(ins, outs)

@@ -253,6 +253,42 @@ def test_composed_twoshot_matches_the_oracle(cd, n, count, shape, monkeypatch):
         assert coll.epoch() == e + 1
 
 
+@pytest.mark.parametrize("name,n,count", [("ALLREDUCE", 8, 8 * 60 * 1024 + 64),
+                                          ("ALLREDUCE", 3, 3 * 60 * 700),
+                                          ("REDUCE_SCATTER", 8, 8 * 60 * 1024 + 64),
+                                          ("ALLTOALL", 8, 8 * 60 * 512), ("ALLTOALL", 4, 4 * 1000)])
+@pytest.mark.parametrize("min_chunk_slots,shape", [(2, "16,1,1"), (3, "16,2,1"), (5, "64,40,1"),
+                                                   (4, "32,3,0"), (9, None), (40, "16,8,1,2")])
+def test_composed_cycling_staging(cd, name, n, count, min_chunk_slots, shape, monkeypatch):
+    """Purlin §4.1 bounded staging: each rank's staging image holds only a few
+    chunk slots (min_chunk_slots of the 16-line chunk) and chunks cycle through
+    them -- a stage waits for the readers of its slot's previous chunk, a fold
+    for the gathers of its published slot's previous chunk.  Staged lines of
+    chunk c carry epoch + c (§4.2).  Bit-exact over several epochs, every run
+    advances the epoch by an odd step, and stale lines from the previous
+    cycles and runs are never taken."""
+    if shape is not None:
+        monkeypatch.setenv("COLL_COMPOSED_SHAPE", shape)
+    triple = getattr(cd, name)
+    opts = dict(encoding=cd.COLL_LL128, path=cd.COLL_PATH_COMPOSED,
+                staging_bytes=min_chunk_slots * n * 16 * 128)
+    if name == "ALLREDUCE":
+        opts["algorithm"] = cd.COLL_TWOSHOT
+    coll = make(cd, triple, n, count, **opts)
+    _, ins, outs = buffers(coll, n, seed=43)
+    last = coll.epoch()
+    for e in range(1, 5):
+        xs = [synth.random_bits16(500 + e, count, n, r) if name == "ALLTOALL"
+              else synth.normal_bf16(500 + e, count, n, r) for r in range(n)]
+        for r in range(n):
+            ins[r].copy_(to_dev(xs[r]))
+        coll.run(ins, outs)
+        check(coll, outs, expected(cd, triple, xs, count), n)
+        now = coll.epoch()
+        assert (now - last) % 2 == 1, (last, now)
+        last = now
+
+
 @pytest.mark.parametrize("enc,reset", [(0, 0), (0, 1), (0, 3), (1, 2), (2, 0), (2, 1), (2, 3)])
 @pytest.mark.parametrize("path", [1, 2, 3])
 def test_four_rotating_slots(cd, enc, reset, path):
