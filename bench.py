@@ -750,6 +750,8 @@ def main() -> int:
                     help="run one extra row alone and print it (profiling runs): "
                          "moe, moe_streamed, rs, rs_composed, ag, a2a, a2a_composed, "
                          "sentinel, f32, staging16, rsv, agv, a2av")
+    ap.add_argument("--staging-mib", type=int, default=16,
+                    help="staging MiB per rank of the bounded-staging row run alone")
     ap.add_argument("--moe-tokens", type=int, default=4096,
                     help="tokens per rank of the MoE rows (the bench line uses 4096)")
     ap.add_argument("--atom-case", default=None,
@@ -805,7 +807,7 @@ def main() -> int:
                                                   path=cd.COLL_PATH_COMPOSED),
             "sentinel": lambda: sentinel_row(cd, count, stream),
             "f32": lambda: f32_row(cd, args.mib << 20, stream),
-            "staging16": lambda: bounded_staging_row(cd, count, stream),
+            "staging16": lambda: bounded_staging_row(cd, count, stream, args.staging_mib),
             "rsv": lambda: v_row(cd, "REDUCE_SCATTER_V", args.mib << 20, stream),
             "agv": lambda: v_row(cd, "ALLGATHER_V", args.mib << 20, stream),
             "a2av": lambda: v_row(cd, "ALLTOALL_V", args.mib << 20, stream),
