@@ -41,10 +41,12 @@
  * memory and frees nothing of the caller's.  A spec holds host state only;
  * it is not thread-safe and must be used from one stream at a time.
  *
- * Asynchrony.  coll_bind, coll_stage, coll_run and coll_set_routing only
- * enqueue work on the given stream and may be captured in a CUDA graph: the
- * epoch that selects the staging slot and the readiness value lives in the
- * workspace, on the device, and advances on the device.
+ * Asynchrony.  coll_bind, coll_stage and coll_run only enqueue work on the
+ * given stream (coll_set_routing records a pointer on the host).  coll_stage
+ * and coll_run may be captured in a CUDA graph and replayed: the epoch that
+ * selects the staging slot and the readiness value lives in the workspace,
+ * on the device, and advances on the device.  coll_bind copies the spec's
+ * work lists from host memory and is made once, outside any capture.
  *
  * Errors.  Host-side argument errors return a status immediately and enqueue
  * nothing.  Device-side errors (a wait that exceeded its time bound) are
@@ -240,10 +242,11 @@ coll_status_t coll_buffer_elems(const coll_spec_t *spec, int rank,
                                 size_t *in_elems, size_t *out_elems);
 
 /* Hand the caller-allocated workspace (device memory, 256-byte aligned) to
- * the spec and initialise it on `stream`: every readiness word = 0, epoch =
- * 1, status clear, work lists uploaded.  Purlin §4 "Initialization": buffers
- * are given once and reused for every call.  COLL_ERR_NOMEM if bytes is
- * smaller than coll_workspace_bytes. */
+ * the spec and initialise it on `stream`: every readiness word = 0 (sentinel
+ * staging: the all-ones pattern), epoch = 1, status clear, work lists
+ * uploaded from host memory (not capturable in a CUDA graph).  Purlin §4
+ * "Initialization": buffers are given once and reused for every call.
+ * COLL_ERR_NOMEM if bytes is smaller than coll_workspace_bytes. */
 coll_status_t coll_bind(coll_spec_t *spec, void *dev_workspace, size_t bytes,
                         coll_stream_t stream);
 
