@@ -262,17 +262,19 @@ coll_status_t coll_set_routing(coll_spec_t *spec, int rank,
                                const int32_t *dev_topk, coll_stream_t stream);
 
 /* Stage rank `rank`'s input for the current epoch e: encode it as lines with
- * readiness value e into staging slot e & 1 of that rank.  The store of a
+ * readiness value e into staging slot e mod slots (2 or 4) of that rank.  The store of a
  * line is its notification (no separate notify step): Purlin §3.2 latency
  * path, flash-comm §3.1.  All ranks must be staged before coll_run(ins=NULL)
  * of the same epoch, in stream order. */
 coll_status_t coll_stage(coll_spec_t *spec, int rank, const void *dev_in,
                          coll_stream_t stream);
 
-/* Run the collective for the current epoch, then advance the epoch.
+/* Run the collective for the current epoch, then advance the epoch (by 1;
+ * with bounded staging by the run's chunk count rounded up to odd).
  * dev_ins == NULL: every rank was staged by coll_stage; the consume kernels
  * validate and consume.  dev_ins != NULL (nranks input pointers): staging is
- * done here too -- inside the same cooperative kernel on the FUSED path.
+ * done here too -- inside the same cooperative kernel on the FUSED path, as
+ * the stage tasks of the one persistent launch on the COMPOSED path.
  * dev_outs: nranks output pointers (16-byte aligned).  Consumers reduce in
  * rank order 0..N-1 whatever order lines become ready in (flash-comm §3.3). */
 coll_status_t coll_run(coll_spec_t *spec, const void *const *dev_ins,
