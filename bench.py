@@ -889,7 +889,11 @@ def main() -> int:
         "roofline": {"bound": "hbm", "kernel": names[dom], "achieved": round(achieved, 1),
                      "peak": peaks["hbm_gbs"], "unit": "GB/s",
                      "frac": round(achieved / peaks["hbm_gbs"], 4), "traffic": traffic,
-                     "peak_source": peaks["source"]},
+                     "peak_source": peaks["source"],
+                     # DRAM side: the ncu traffic per launch over this run's launch time
+                     **({"dram_achieved": round(traffic / dur[dom] / 1e6, 1),
+                         "dram_frac": round(traffic / dur[dom] / 1e6 / peaks["hbm_gbs"], 4)}
+                        if traffic else {})},
         **({"roofline_note": "achieved counts every emulated rank's reads and writes "
                              "(issue-level, as for the three-launch path); the staged and "
                              "published lines stay in L2 and are dropped once read, so the "
