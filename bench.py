@@ -5,7 +5,8 @@ Default workload (one step = one all-reduce through the whole datapath:
 stage as LL128 lines, validate + fold the partitions at their owners,
 publish, validate + unpack at every rank):
     8 emulated ranks, 256 MiB of bf16 per rank (uniform[-4, 4], seeded),
-    LL128 sequence-number lines, twoshot, stream-ordered kernels.
+    LL128 sequence-number lines, twoshot, one composed launch
+    (``--path streamed``: the three stream-ordered launches).
 The inputs (2 GiB) and staging (4.8 GiB) exceed the 126 MiB L2, so no L2
 flush is needed between steps.
 
@@ -14,12 +15,16 @@ summed over replicas for --gpus N (one independent replica per GPU: the
 single-GPU emulation does not shard across GPUs).
 
 The same JSON line carries the roofline of the dominant kernel (per-launch
-CUDA events around each kernel of every timed step), the end-to-end number
-through coll_run_host (pinned host buffers, copies in the timed region), the
-small-message latency sweep (8 ranks x [T x 4096] bf16, LL8, oneshot and
-twoshot; warm = 128 ops per CUDA graph, cold = L2 flushed before every op),
-reduce-scatter and all-gather at 256 MiB, and the CPU oracle timed on a
-bounded sample.  ``--impl reference`` times the CPU oracle instead.
+CUDA events around each kernel of every timed step, with the DRAM-side rate
+from the committed ncu traffic figure), the end-to-end number from pinned
+host buffers, ``rows`` for the other collectives and paths (streamed
+all-reduce, reduce-scatter, all-gather, all-to-all, MoE dispatch, the V
+collectives, sentinel packs, fp32, bounded staging, and the pipeline-depth
+ablation of the one-sided copy), the small-message latency sweep (8 ranks x
+[T x 4096] bf16; warm = 128 ops per CUDA graph, cold = L2 flushed before
+every op) and the CPU oracle timed on a bounded sample.  ``--impl
+reference`` times the CPU oracle instead; ``--row``, ``--sweep-only`` and
+``--atom-only`` run one part alone (profiling runs).
 """
 from __future__ import annotations
 
