@@ -2,6 +2,12 @@
 //
 //  k_stage     stream-ordered staging of rank inputs into LL lines
 //  k_consume   stream-ordered validate + unpack + (fold) + write, per phase
+//  k_fold_ll128 / k_copy_ll128 / k_stage_ll128
+//              the LL128 fold, copy and stage through per-warp cp.async
+//              rings of 512-byte rows (stream-ordered path)
+//  k_fold_ll8 / k_copy_ll8
+//              the same rings for LL8 lines (stream-ordered path with the
+//              deferred or no re-arm)
 //  k_fused     one cooperative launch: each CTA serves one emulated rank,
 //              stages its tiles, then polls and consumes; optional late
 //              producer CTAs publish withheld lines while consumers poll
