@@ -236,7 +236,15 @@ int derive(const DeriveInput& in, Plan& p) {
   else if (L == COLL_PACKED_V && O == COLL_SCATTERED_V && in.op == COLL_COPY)
     p.kind = CK_ALLGATHER_V;
   else if (L == COLL_SCATTERED_V && O == COLL_TRANSPOSED_V && in.op == COLL_COPY) {
-    if (in.experts > 0) return in.dtype == COLL_BF16 ? derive_moe(in, p) : COLL_ERR_UNSUPPORTED;
+    if (in.experts > 0) {
+      // a dispatch copies rows: an fp32 row is 2 * hidden 16-bit units, and
+      // the plan's element counts are those units (coll_buffer_elems
+      // divides them back)
+      if (in.hidden % 8 != 0) return COLL_ERR_ALIGN;
+      DeriveInput m = in;
+      m.hidden = in.hidden * (int)eu;
+      return derive_moe(m, p);
+    }
     p.kind = CK_ALLTOALL_V;
   } else
     return COLL_ERR_UNSUPPORTED;

@@ -94,7 +94,8 @@ typedef enum { COLL_BF16 = 0, COLL_F32 = 1 } coll_dtype_t;
  * counts of coll_buffer_elems are fp32 elements; every count is still a
  * multiple of 8.  Lines carry the same bytes as for bf16 (an LL8 line one
  * fp32, an LL128 line 30, a sentinel pack 2, whose reserved pattern is
- * 0xFFFFFFFF, published as 0x7FC00000).  MoE dispatch is bf16 only. */
+ * 0xFFFFFFFF, published as 0x7FC00000).  MoE dispatch copies fp32 rows
+ * byte for byte (`hidden` fp32 elements per row, at most 24,576). */
 
 typedef enum {
     COLL_OK = 0,
@@ -175,7 +176,8 @@ typedef struct {
     uint64_t timeout_ns; /* bound on every device wait, 0 = 200 ms */
     /* MoE dispatch (SCATTERED_V -> TRANSPOSED_V) only: */
     int tokens;          /* rows per source rank */
-    int hidden;          /* bf16 elements per row */
+    int hidden;          /* elements per row (of the dtype; a multiple of 8,
+                            at most 49,152 bf16 or 24,576 fp32) */
     int topk;            /* experts per token */
     int experts;         /* total experts, a multiple of nranks (<= 1024) */
     int max_rows;        /* output rows each destination can hold, 0 = the

@@ -336,9 +336,15 @@ def test_f32_element_counts_and_admission(cd):
     with pytest.raises(cd.CollError) as e:
         cd.coll_spec_create(*cd.ALLREDUCE, 8, 12, dtype=cd.COLL_F32)
     assert e.value.status == cd.COLL_ERR_ALIGN
+    # MoE dispatch copies fp32 rows: element counts stay in fp32 elements,
+    # rows wider than 24,576 fp32 do not fit the two staged rows in shared memory
+    s = cd.coll_spec_create(*cd.MOE_DISPATCH, 2, 0, dtype=cd.COLL_F32, encoding=cd.COLL_LL128,
+                            tokens=4, hidden=8, topk=1, experts=2)
+    assert cd.coll_buffer_elems(s, 0) == (32, 4 * 2 * 1 * 8)
+    cd.coll_destroy(s)
     with pytest.raises(cd.CollError) as e:
         cd.coll_spec_create(*cd.MOE_DISPATCH, 2, 0, dtype=cd.COLL_F32, encoding=cd.COLL_LL128,
-                            tokens=4, hidden=8, topk=1, experts=2)
+                            tokens=4, hidden=24576 + 8, topk=1, experts=2)
     assert e.value.status == cd.COLL_ERR_UNSUPPORTED
     with pytest.raises(cd.CollError) as e:
         cd.coll_spec_create(*cd.ALLREDUCE, 8, 64, dtype=7)

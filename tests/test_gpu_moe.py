@@ -88,6 +88,37 @@ def test_moe_dispatch_small_cases_match_the_oracle(cd, n, tokens, hidden, k, exp
 
 
 @pytest.mark.parametrize("path", [2, 3])
+@pytest.mark.parametrize("n,tokens,hidden,k,experts", [(4, 300, 64, 3, 16), (8, 129, 3584, 8, 256),
+                                                      (2, 40, 8, 2, 4)])
+def test_moe_dispatch_f32_rows(cd, n, tokens, hidden, k, experts, path):
+    """fp32 rows (random bit patterns, NaN payloads included) dispatched byte
+    for byte: the oracle's dispatch of the same bytes seen as 2 * hidden
+    16-bit units, rows and counts, both launch forms, two epochs."""
+    import torch
+
+    coll = make_moe(cd, n, tokens, hidden, k, experts, path=path, dtype=cd.COLL_F32)
+    xs = [synth.random_bits32(7, tokens * hidden, n, r) for r in range(n)]
+    tk = [synth.topk_experts(7, tokens, k, experts, n, r) for r in range(n)]
+    ins = [torch.from_numpy(x.view(np.int32)).cuda() for x in xs]
+    topk_dev = [torch.from_numpy(t.ravel()).cuda() for t in tk]
+    route(cd, coll, topk_dev)
+    assert coll.elems(0) == (tokens * hidden, coll.elems(0)[1])
+    outs = [torch.zeros(coll.elems(r)[1], dtype=torch.int32, device="cuda") for r in range(n)]
+    want, wcounts, wrows = oracle.moe_dispatch(
+        [x.view(np.uint16).reshape(tokens, 2 * hidden) for x in xs], tk, experts)
+    for epoch in range(2):
+        coll.run(ins, outs)
+        code, rank, line = coll.status()
+        assert code == cd.COLL_OK, (code, rank, line)
+        counts, rows = counts_of(cd, coll, n, experts)
+        assert np.array_equal(counts, wcounts)
+        assert np.array_equal(rows, wrows)
+        for d in range(n):
+            got = outs[d].cpu().numpy().view(np.uint16)[:wrows[d] * 2 * hidden]
+            assert np.array_equal(got.reshape(-1, 2 * hidden), want[d]), (epoch, d)
+
+
+@pytest.mark.parametrize("path", [2, 3])
 def test_moe_dispatch_8x4096x7168_full_size(cd, path):
     """8 ranks x 4096 tokens x 7168 bf16 normal(0,1), top-8 of 256 experts:
     every output row of every destination equals its source row as listed
