@@ -43,8 +43,11 @@ PATH_NAMES = {FUSED: "fused", STREAMED: "streamed", COMPOSED: "composed"}
 
 
 # Launch shape of the one-launch path: 0 = one CTA per SM (the default),
-# WIDE = every co-resident CTA (the library clamps the request).
+# WIDE = every co-resident CTA (the library clamps the request); NARROW = 64
+# CTAs in all (8 per rank at 8 ranks: for the smallest messages, fewer CTAs
+# mean fewer arrivals and cross-CTA line polls).
 WIDE = 1024
+NARROW = 64
 
 
 @dataclass(frozen=True, order=True)
@@ -55,14 +58,14 @@ class Candidate:
     ctas: int = 0
 
     def name(self) -> str:
-        shape = "/wide" if self.ctas else ""
+        shape = {0: "", WIDE: "/wide", NARROW: "/narrow"}.get(self.ctas, f"/ctas{self.ctas}")
         return f"{ENC_NAMES[self.enc]}/{ALGO_NAMES[self.algo]}/{PATH_NAMES[self.path]}{shape}"
 
 
 def candidates_for(nbytes: int) -> list[Candidate]:
     """The protocols worth measuring at one size (bytes per rank): one
-    cooperative launch only up to 4 MiB (in two launch shapes), the composed
-    launch from 1 MiB."""
+    cooperative launch only up to 4 MiB (in two launch shapes, three up to
+    256 KiB), the composed launch from 1 MiB."""
     out = []
     for enc in (LL8, SENT, LL128):
         for algo in (ONESHOT, TWOSHOT):
@@ -76,6 +79,8 @@ def candidates_for(nbytes: int) -> list[Candidate]:
                 out.append(Candidate(enc, algo, path))
                 if path == FUSED:
                     out.append(Candidate(enc, algo, path, WIDE))
+                    if nbytes <= (256 << 10):
+                        out.append(Candidate(enc, algo, path, NARROW))
     return out
 
 
