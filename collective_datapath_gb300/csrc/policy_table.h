@@ -15,27 +15,31 @@ struct PolicyEntry {
 };
 
 constexpr PolicyEntry kPolicy2[] = {
-    {737280ull, 2, 1, 1, 0},  // SENT/oneshot/fused
-    {2506752ull, 2, 1, 1, 1024},  // SENT/oneshot/fused/wide
+    {65536ull, 0, 1, 1, 64},  // LL8/oneshot/fused/narrow
+    {131072ull, 2, 1, 1, 64},  // SENT/oneshot/fused/narrow
+    {770048ull, 2, 1, 1, 0},  // SENT/oneshot/fused
+    {2998272ull, 2, 1, 1, 1024},  // SENT/oneshot/fused/wide
     {7421952ull, 2, 2, 1, 1024},  // SENT/twoshot/fused/wide
-    {16777216ull, 1, 1, 2, 0},  // LL128/oneshot/streamed
+    {17432576ull, 1, 1, 2, 0},  // LL128/oneshot/streamed
     {UINT64_MAX, 1, 2, 2, 0},  // LL128/twoshot/streamed
 };
 constexpr PolicyEntry kPolicy4[] = {
-    {49152ull, 0, 1, 1, 0},  // LL8/oneshot/fused
+    {32768ull, 0, 1, 1, 64},  // LL8/oneshot/fused/narrow
     {311296ull, 2, 1, 1, 0},  // SENT/oneshot/fused
-    {1753088ull, 2, 1, 1, 1024},  // SENT/oneshot/fused/wide
+    {983040ull, 2, 1, 1, 1024},  // SENT/oneshot/fused/wide
+    {1900544ull, 2, 2, 1, 0},  // SENT/twoshot/fused
     {7421952ull, 2, 2, 1, 1024},  // SENT/twoshot/fused/wide
-    {9125888ull, 1, 1, 2, 0},  // LL128/oneshot/streamed
+    {9109504ull, 1, 1, 2, 0},  // LL128/oneshot/streamed
     {UINT64_MAX, 1, 2, 2, 0},  // LL128/twoshot/streamed
 };
 constexpr PolicyEntry kPolicy8[] = {
-    {32768ull, 0, 1, 1, 0},  // LL8/oneshot/fused
+    {8192ull, 0, 1, 1, 64},  // LL8/oneshot/fused/narrow
+    {32768ull, 2, 1, 1, 64},  // SENT/oneshot/fused/narrow
     {180224ull, 2, 1, 1, 0},  // SENT/oneshot/fused
-    {425984ull, 2, 1, 1, 1024},  // SENT/oneshot/fused/wide
-    {1425408ull, 2, 2, 1, 0},  // SENT/twoshot/fused
-    {5931008ull, 2, 2, 1, 1024},  // SENT/twoshot/fused/wide
-    {51052544ull, 1, 2, 2, 0},  // LL128/twoshot/streamed
+    {819200ull, 2, 1, 1, 1024},  // SENT/oneshot/fused/wide
+    {1835008ull, 2, 2, 1, 0},  // SENT/twoshot/fused
+    {7421952ull, 2, 2, 1, 1024},  // SENT/twoshot/fused/wide
+    {51150848ull, 1, 2, 2, 0},  // LL128/twoshot/streamed
     {UINT64_MAX, 1, 2, 3, 0},  // LL128/twoshot/composed
 };
 
