@@ -421,3 +421,26 @@ def test_bounded_staging_validation(cd):
             call()
         assert e.value.status == cd.COLL_ERR_UNSUPPORTED
     cd.coll_destroy(s)
+
+
+@pytest.mark.parametrize("T", [64, 68, 96, 136, 200])
+def test_fused_phases_fill_whole_rounds(cd, T):
+    """A fused phase with more items than CTAs per rank gets whole rounds of
+    items of about equal size: no CTA b of a rank (items b, b + B, ...)
+    moves much more than its share of the lines (with the largest tile, a
+    few CTAs moved twice the others).  Schedule only (host)."""
+    n = 8
+    s = cd.coll_spec_create(*cd.ALLREDUCE, n, T * 4096, encoding=cd.COLL_SENT,
+                            algorithm=cd.COLL_TWOSHOT, path=cd.COLL_PATH_FUSED)
+    B = cd.coll_debug_plan(s)["ctas_per_rank"]
+    for which in (1, 2):
+        items = cd.coll_debug_items(s, which)
+        per_rank = len(items) // n
+        if per_rank > B:
+            assert per_rank % B == 0, (which, per_rank, B)
+        for d in range(n):
+            mine = [it for it in items if int(it[2]) == d]
+            load = [sum(int(it[5]) for it in mine[b::B]) for b in range(B)]
+            fair = -(-sum(load) // B)  # no CTA carries much more than its share
+            assert max(load) <= 1.02 * fair + 8, (which, d, load)
+    cd.coll_destroy(s)
