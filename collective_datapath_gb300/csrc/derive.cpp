@@ -429,7 +429,11 @@ int derive(const DeriveInput& in, Plan& p) {
   auto pick_tile = [&](const std::vector<uint64_t>& seg_lines) -> uint64_t {
     if (in.tile_lines > 0) return round_up((uint64_t)in.tile_lines, 4);
     if (!fused) return max_tile;
-    uint64_t lo = 4, hi = max_tile;
+    // The one-launch twoshot takes tiles of up to 16384 lines: one round of
+    // larger tiles beat two balanced rounds from 128 tokens up (8 x [136 x
+    // 4096]: 16.2 against 19.4 us); the oneshot keeps 4096 (larger tiles cost
+    // it 5-7 % at 96-112 tokens).
+    uint64_t lo = 4, hi = twoshot && p.enc != ENC_LL128 ? 16384 : max_tile;
     auto items_for = [&](uint64_t t) {
       uint64_t c = 0;
       for (uint64_t l : seg_lines) c += (l + t - 1) / t;
