@@ -142,7 +142,8 @@ cudaError_t launched(coll_spec* s, cudaError_t e, cudaStream_t st) {
 }
 
 // Shape of the composed twoshot launch: chunks of 256 lines of every
-// partition, a lag of 28 queue steps from a chunk's stage to its fold and
+// partition (fewer for short runs, see below), a lag of 28 queue steps from
+// a chunk's stage to its fold and
 // from its fold to its gather, consumed lines dropped from L2, launch
 // variant 0.  COLL_COMPOSED_SHAPE = "chunk_lines,lag,discard,variant,lag2"
 // overrides it
@@ -156,15 +157,22 @@ ComposedParams composed_shape(const coll_spec* s) {
   // reduce-scatter and all-to-all 128-line chunks, lag 40
   const bool ar = p.kind == CK_ALLREDUCE;
   int chunk = ar ? 256 : 128, lag = ar ? 28 : 40, discard = 1, variant = 0, lag2 = -1;
-  if (const char* env = std::getenv("COLL_COMPOSED_SHAPE"))
+  uint64_t most = 0;
+  for (const Seg& sg : p.pseg[0]) most = std::max<uint64_t>(most, sg.lines);
+  if (const char* env = std::getenv("COLL_COMPOSED_SHAPE")) {
     std::sscanf(env, "%d,%d,%d,%d,%d", &chunk, &lag, &discard, &variant, &lag2);
+  } else if (ar) {
+    // The queue fills and drains over 2 * lag steps; the chunk is the largest
+    // of 256, 128 and 64 lines that still gives eight lags' worth of chunks
+    // (measured at 8 x 8 / 32 / 128 MiB: 64, 128 and 256 lines were best).
+    while (chunk > 64 && (most + chunk - 1) / chunk < 8ull * (uint64_t)lag) chunk /= 2;
+  }
   // a power of two of at least kComposedMinChunk lines (rows per chunk are
   // counted with shifts)
   int c2 = (int)kComposedMinChunk;
   while (c2 * 2 <= chunk && c2 < (1 << 20)) c2 *= 2;
   chunk = c2;
-  uint64_t max_lines = 0;
-  for (const Seg& sg : p.pseg[0]) max_lines = std::max<uint64_t>(max_lines, sg.lines);
+  const uint64_t max_lines = most;
   q.chunk_lines = (uint32_t)chunk;
   q.nchunks = (uint32_t)std::max<uint64_t>(1, (max_lines + chunk - 1) / chunk);
   q.lag = std::max(1, lag);
