@@ -159,7 +159,8 @@ enum { COLL_RESET_FUSED = 0, COLL_RESET_KERNEL = 1, COLL_RESET_NONE = 2,
  * gather or copy tasks chunk by chunk from one queue, each chunk's lines
  * staying in L2 between its producer and its reader (Purlin §3.2,
  * Algorithm 1, Figure 5).  AUTO picks FUSED for LL8 and sentinel packs up
- * to 256 KiB per rank, COMPOSED for LL128 from 32 MiB per rank and, for
+ * to 256 KiB per rank, COMPOSED for LL128 from 32 MiB per rank (all-to-all:
+ * from 16 MiB) and, for
  * all-reduce, ONESHOT up to 512 KiB per rank (boundaries on measured GB300
  * points); with COLL_ENC_AUTO the all-reduce takes the calibrated table. */
 enum { COLL_PATH_AUTO = 0, COLL_PATH_FUSED = 1, COLL_PATH_STREAMED = 2,
