@@ -381,8 +381,10 @@ def bandwidth_row(cd, triple, count_in_out, kind, stream, steps=5, path=None) ->
 
     n = N_RANKS
     count = count_in_out
+    extra = {"algorithm": cd.COLL_TWOSHOT} if kind == "ar" else {}
     coll = cd.Collective(triple, n, count, encoding=cd.COLL_LL128,
-                         path=cd.COLL_PATH_STREAMED if path is None else path)
+                         path=cd.COLL_PATH_STREAMED if path is None else path, **extra)
+    chosen = coll.plan()["path"]
     ins = make_inputs(max(coll.elems(r)[0] for r in range(n)), 11)
     ins = [x[:coll.elems(r)[0]] for r, x in enumerate(ins)]
     outs = [torch.empty(max(coll.elems(r)[1], 8), dtype=torch.int16, device="cuda")
@@ -399,7 +401,9 @@ def bandwidth_row(cd, triple, count_in_out, kind, stream, steps=5, path=None) ->
         stream.synchronize()
     ms = e0.elapsed_time(e1) / steps
     s = count * 2.0
-    if kind == "rs":
+    if kind == "ar":
+        b = bytes_allreduce_twoshot(n, s, EPS_LL128)
+    elif kind == "rs":
         b = bytes_reduce_scatter(n, s, EPS_LL128)
     elif kind == "a2a":
         b = 2 * n * s * (1 + EPS_LL128)
@@ -410,7 +414,26 @@ def bandwidth_row(cd, triple, count_in_out, kind, stream, steps=5, path=None) ->
     del coll, ins, outs
     torch.cuda.empty_cache()
     return {"ms": round(ms, 4), "GB/s": round(b / ms / 1e6, 1), "algorithmic_bytes": b,
+            "path": {1: "fused", 2: "streamed", 3: "composed"}.get(chosen, chosen),
             "status": st}
+
+
+def sizes_row(cd, stream, sizes_mib=(32, 128)) -> dict:
+    """The bandwidth regime at the smaller per-rank sizes: all-reduce (LL128
+    twoshot), reduce-scatter and all-gather (gathered output per rank) at each
+    size, each on the launch path AUTO picks."""
+    out = {}
+    for mib in sizes_mib:
+        count = mib * 2**20 // 2
+        out[f"{mib}MiB"] = {
+            "allreduce": bandwidth_row(cd, cd.ALLREDUCE, count, "ar", stream,
+                                       path=cd.COLL_PATH_AUTO),
+            "reduce_scatter": bandwidth_row(cd, cd.REDUCE_SCATTER, count, "rs", stream,
+                                            path=cd.COLL_PATH_AUTO),
+            "all_gather": bandwidth_row(cd, cd.ALLGATHER, count, "ag", stream,
+                                        path=cd.COLL_PATH_AUTO),
+        }
+    return out
 
 
 def v_row(cd, name, total_bytes, stream, steps=5) -> dict:
@@ -754,7 +777,7 @@ def main() -> int:
     ap.add_argument("--row", default=None,
                     help="run one extra row alone and print it (profiling runs): "
                          "moe, moe_streamed, rs, rs_composed, ag, a2a, a2a_composed, "
-                         "sentinel, f32, staging16, rsv, agv, a2av")
+                         "sentinel, f32, staging16, sizes, rsv, agv, a2av")
     ap.add_argument("--staging-mib", type=int, default=16,
                     help="staging MiB per rank of the bounded-staging row run alone")
     ap.add_argument("--moe-tokens", type=int, default=4096,
@@ -813,6 +836,7 @@ def main() -> int:
             "sentinel": lambda: sentinel_row(cd, count, stream),
             "f32": lambda: f32_row(cd, args.mib << 20, stream),
             "staging16": lambda: bounded_staging_row(cd, count, stream, args.staging_mib),
+            "sizes": lambda: sizes_row(cd, stream),
             "rsv": lambda: v_row(cd, "REDUCE_SCATTER_V", args.mib << 20, stream),
             "agv": lambda: v_row(cd, "ALLGATHER_V", args.mib << 20, stream),
             "a2av": lambda: v_row(cd, "ALLTOALL_V", args.mib << 20, stream),
@@ -974,6 +998,7 @@ def main() -> int:
             "allreduce_256MiB_sentinel_twoshot": sentinel_row(cd, count, stream),
             "allreduce_256MiB_f32_composed": f32_row(cd, 256 << 20, stream),
             "allreduce_256MiB_composed_staging_16MiB": bounded_staging_row(cd, count, stream),
+            "bandwidth_regime_32_128MiB": sizes_row(cd, stream),
             "pipeline_depth_ablation_256MiB": atom_ablation(cd, stream),
         }
         line["latency_us_per_op"] = latency_sweep(cd, stream)
