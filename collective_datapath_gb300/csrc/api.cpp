@@ -195,7 +195,10 @@ ComposedParams composed_shape(const coll_spec* s) {
   }
   q.discard = discard;
   q.variant = variant >= 0 && variant <= 2 ? variant : 0;
-  q.mode = p.kind == CK_REDUCE_SCATTER ? 1 : (p.kind == CK_ALLTOALL ? 2 : 0);
+  q.mode = p.kind == CK_REDUCE_SCATTER ? 1
+           : p.kind == CK_ALLTOALL      ? 2
+           : p.kind == CK_ALLGATHER     ? 3
+                                        : 0;
   char* f = s->ws + p.off_cflags;
   q.flag_stage = reinterpret_cast<uint64_t*>(f);
   q.flag_fold = q.flag_stage + p.composed_max_chunks * p.n;
@@ -440,6 +443,15 @@ coll_status_t coll_run(coll_spec_t* s, const void* const* dev_ins, void* const* 
   const bool empty = p.items1.empty() && p.items2.empty();
   if (dev_ins != nullptr && p.path == COLL_PATH_COMPOSED && !empty) {
     P.cp = composed_shape(s);
+    if (P.cp.mode == 3) {
+      // all-gather: each source stages its own packed segment; the kernel
+      // takes source k's segment and its offset in the gathered output
+      for (int k = 0; k < p.n; ++k) {
+        P.seg_line0[k] = p.pseg[k][0].line0;
+        P.seg_elems[k] = p.pseg[k][0].elems;
+        P.seg_in0[k] = p.shard * (uint64_t)k;
+      }
+    }
     const int cap = composed_capacity(P.cp.variant, P.cp.ring > 0);
     if (cap < 3) return COLL_ERR_CUDA;
     // cycling staging: chunk c is notified with epoch + c, so the run moves

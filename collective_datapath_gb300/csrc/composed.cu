@@ -153,6 +153,35 @@ __device__ __forceinline__ void fill_a2a_piece(const RunParams& P, Piece* pc, in
                          : (int64_t)P.cp.chunk_lines * kLL128Elems);
 }
 
+// All-gather (mode 3): rank p stages chunk c of its one packed segment;
+// the seg_* fields hold each source's segment and its output offset.
+__device__ __forceinline__ void fill_ag_stage_piece(const RunParams& P, Piece* pc, int c, int p,
+                                                    uint64_t e) {
+  const uint32_t t0 = (uint32_t)c * P.cp.chunk_lines;
+  pc[0].src = reinterpret_cast<const char*>(P.in[p] + (uint64_t)t0 * kLL128Elems);
+  pc[0].dst = image_bytes(P, P.P, e, p) + (P.seg_line0[p] + t0) * kLL128LineBytes;
+  pc[0].nl = chunk_lines_of(P, p, t0);
+  const int64_t lk = (int64_t)P.seg_elems[p] - (int64_t)t0 * kLL128Elems;
+  pc[0].left = (int)(lk < (int64_t)P.cp.chunk_lines * kLL128Elems
+                         ? lk
+                         : (int64_t)P.cp.chunk_lines * kLL128Elems);
+}
+
+// All-gather copy: destination d copies chunk c of every source r's staged
+// segment into partition r of its output.
+__device__ __forceinline__ void fill_ag_copy_piece(const RunParams& P, Piece* pc, int c, int d,
+                                                   uint64_t e) {
+  const int r = threadIdx.x;
+  const uint32_t t0 = (uint32_t)c * P.cp.chunk_lines;
+  pc[r].src = image_bytes(P, P.P, e, r) + (P.seg_line0[r] + t0) * kLL128LineBytes;
+  pc[r].dst = reinterpret_cast<char*>(P.out[d] + P.seg_in0[r] + (uint64_t)t0 * kLL128Elems);
+  pc[r].nl = chunk_lines_of(P, r, t0);
+  const int64_t lr = (int64_t)P.seg_elems[r] - (int64_t)t0 * kLL128Elems;
+  pc[r].left = (int)(lr < (int64_t)P.cp.chunk_lines * kLL128Elems
+                         ? lr
+                         : (int64_t)P.cp.chunk_lines * kLL128Elems);
+}
+
 template <int kCWarps, int kCRing>
 __device__ __forceinline__ void stage_task(const Piece* pc, uint32_t wbase, int lane, int warp,
                                            int n, int rsh, uint64_t e) {
@@ -423,14 +452,18 @@ __global__ void __launch_bounds__(kCWarps * 32, kMinBlocks) k_composed_ll128(Run
     const uint64_t seq = W ? e + (uint64_t)c : e;
     const bool reuse = W && c >= (int)W;
     if (kind == 0) {
-      if ((int)threadIdx.x < n) fill_stage_piece(P, s_piece, c, x, e, W);
+      if (Q.mode == 3) {
+        if (threadIdx.x == 0) fill_ag_stage_piece(P, s_piece, c, x, e);
+      } else if ((int)threadIdx.x < n) {
+        fill_stage_piece(P, s_piece, c, x, e, W);
+      }
       if (reuse && !acquire_flags(P, Q.flag_fold + (size_t)(c - (int)W) * n, n, e))
         s_ok = 0;
       __syncthreads();
       if (!s_ok) break;
-      stage_task<kCWarps, kCRing>(s_piece, wbase, lane, warp, n, rsh, seq);
+      stage_task<kCWarps, kCRing>(s_piece, wbase, lane, warp, Q.mode == 3 ? 1 : n, rsh, seq);
       release_flag(Q.flag_stage + (size_t)c * n + x, e, s_ok);
-    } else if (kind == 1 && Q.mode != 2) {
+    } else if (kind == 1 && (Q.mode == 0 || Q.mode == 1)) {
       if (!acquire_flags(P, Q.flag_stage + (size_t)c * n, n, e)) s_ok = 0;
       if (reuse && Q.mode == 0 && !acquire_gathers(P, c - (int)W, e)) s_ok = 0;
       __syncthreads();
@@ -438,6 +471,26 @@ __global__ void __launch_bounds__(kCWarps * 32, kMinBlocks) k_composed_ll128(Run
       if (!fold_task<kCWarps, kCRing>(P, wbase, lane, warp, c, x, e, seq, Q.mode == 1, W))
         s_ok = 0;
       release_flag(Q.flag_fold + (size_t)c * n + x, e, s_ok);
+    } else if (kind == 1 && Q.mode == 3) {
+      // all-gather: chunk c of every source's segment into rank x's output;
+      // the N-th copy of a chunk drops its staged lines from L2
+      if ((int)threadIdx.x < n) fill_ag_copy_piece(P, s_piece, c, x, e);
+      if (!acquire_flags(P, Q.flag_stage + (size_t)c * n, n, e)) s_ok = 0;
+      __syncthreads();
+      if (!s_ok) break;
+      if (!gather_task<kCWarps, kCRing>(P, s_piece, wbase, lane, warp, rsh, seq)) s_ok = 0;
+      __syncthreads();
+      if (warp == 0 && s_ok && Q.discard == 1) {
+        // warp 0 alone, as for the all-reduce's gathers
+        const bool last =
+            __shfl_sync(0xFFFFFFFFu, lane == 0 ? (int)last_gather(P, c, e, false) : 0, 0);
+        if (last)
+          for (int r = 0; r < n; ++r) {
+            const int nl = s_piece[r].nl;
+            for (int j = lane; j < nl; j += 32)
+              discard_l2_line(s_piece[r].src + (size_t)j * kLL128LineBytes);
+          }
+      }
     } else if (kind == 1) {
       // all-to-all: segment x of every source's chunk c into rank x's output;
       // each staged line has this one reader, which drops it once copied

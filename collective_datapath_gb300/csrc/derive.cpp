@@ -364,12 +364,13 @@ int derive(const DeriveInput& in, Plan& p) {
       p.path = COLL_PATH_STREAMED;
   }
 
-  // The composed launch: the LL128 twoshot all-reduce, reduce-scatter and
-  // all-to-all (stage plus one or two consuming kinds of task per chunk).
+  // The composed launch: the LL128 twoshot all-reduce, reduce-scatter,
+  // all-to-all and all-gather (stage plus one or two consuming kinds of task
+  // per chunk).
   if (p.path == COLL_PATH_COMPOSED &&
       !(p.enc == ENC_LL128 &&
         ((p.kind == CK_ALLREDUCE && p.algorithm == COLL_TWOSHOT) ||
-         p.kind == CK_REDUCE_SCATTER || p.kind == CK_ALLTOALL)))
+         p.kind == CK_REDUCE_SCATTER || p.kind == CK_ALLTOALL || p.kind == CK_ALLGATHER)))
     return COLL_ERR_UNSUPPORTED;
 
   // Rank images of region P.
@@ -665,7 +666,9 @@ int derive(const DeriveInput& in, Plan& p) {
   off = round_up(off, 4096);
   const uint64_t lb = (uint64_t)line_bytes(p.enc);
   if (capped && in.staging_bytes < p.p_rank_lines * lb) {
-    if (p.path != COLL_PATH_COMPOSED) return COLL_ERR_UNSUPPORTED;
+    // cycling needs the composed launch of a collective whose chunk slots
+    // hold all N partitions of a chunk (not the all-gather's one segment)
+    if (p.path != COLL_PATH_COMPOSED || !composable) return COLL_ERR_UNSUPPORTED;
     // chunk slots of N partitions x chunk lines; at least two slots of the
     // smallest chunk
     p.ring_lines = in.staging_bytes / lb / ((uint64_t)n * kComposedMinChunk) *

@@ -154,7 +154,9 @@ enum { COLL_RESET_FUSED = 0, COLL_RESET_KERNEL = 1, COLL_RESET_NONE = 2,
 /* Launch path: FUSED = stage and consume inside one cooperative kernel
  * (all CTAs co-resident; a CTA serves one emulated rank); STREAMED =
  * separate stage and consume kernels ordered by the stream; COMPOSED
- * (LL128 only: the twoshot all-reduce, reduce-scatter and all-to-all) = one
+ * (LL128 only: the twoshot all-reduce, reduce-scatter, all-to-all and
+ * all-gather; AUTO never takes it for the all-gather, whose stream-ordered
+ * copy measured faster at every size) = one
  * persistent cooperative kernel that runs stage, fold (+ publish) and
  * gather or copy tasks chunk by chunk from one queue, each chunk's lines
  * staying in L2 between its producer and its reader (Purlin §3.2,

@@ -168,6 +168,34 @@ def test_bandwidth_allreduce_composed_twoshot(cd, inputs, mib, staging_mib):
 
 
 @pytest.mark.parametrize("mib", [32, 256])
+def test_bandwidth_composed_all_gather(cd, inputs, mib):
+    """The one-launch all-gather at full size (gathered output `mib` MiB per
+    rank): byte-identical to the stream-ordered all-gather, and every
+    destination holds each source's segment in its partition."""
+    import torch
+
+    count = mib * 1024 * 1024 // 2
+    res = {}
+    for path in (cd.COLL_PATH_COMPOSED, cd.COLL_PATH_STREAMED):
+        coll = cd.Collective(cd.ALLGATHER, N, count, encoding=cd.COLL_LL128, path=path)
+        ins = [inputs[r][:coll.elems(r)[0]] for r in range(N)]
+        outs = [torch.empty(count, dtype=torch.int16, device="cuda") for _ in range(N)]
+        for _ in range(2):
+            coll.run(ins, outs)
+        code, rank, line = coll.status()
+        assert code == cd.COLL_OK, (path, code, rank, line)
+        res[path] = outs
+        del coll
+    m = count // N
+    for d in range(N):
+        assert torch.equal(res[cd.COLL_PATH_COMPOSED][d], res[cd.COLL_PATH_STREAMED][d])
+        for p in (0, N - 1):
+            assert torch.equal(res[cd.COLL_PATH_COMPOSED][d][p * m:(p + 1) * m], inputs[p][:m])
+    del res
+    torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("mib", [32, 256])
 def test_bandwidth_composed_reduce_scatter_and_all_to_all(cd, inputs, mib):
     """The one-launch reduce-scatter (sampled against the oracle, and equal
     to the stream-ordered one on every element) and all-to-all (equal to the
