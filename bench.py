@@ -710,6 +710,10 @@ def moe_row(cd, stream, steps=5, path=None, tokens=4096) -> dict:
         topk.append(keys.argsort(dim=1)[:, :k].to(torch.int32).contiguous())
         cd.coll_set_routing(coll.spec, r, topk[r])
     torch.cuda.synchronize()  # routing is drawn on torch's stream
+    # staged rows: one per (token, destination rank holding one of its experts)
+    el = experts // n
+    staged = sum(int(torch.zeros(tokens, n, dtype=torch.bool, device="cuda")
+                     .scatter_(1, topk[r].long() // el, True).sum()) for r in range(n))
     outs = [torch.empty(coll.elems(r)[1], dtype=torch.int16, device="cuda") for r in range(n)]
     ev = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
     for e in ev:
@@ -739,8 +743,8 @@ def moe_row(cd, stream, steps=5, path=None, tokens=4096) -> dict:
     st = coll.status(stream)[0]
     rows = n * tokens * k
     row_b, line_b = hidden * 2, ((hidden + 59) // 60 + 3) // 4 * 4 * 128
-    unique = n * tokens * row_b + rows * line_b + rows * line_b + rows * row_b
-    issue = rows * row_b + rows * line_b + rows * line_b + rows * row_b
+    unique = n * tokens * row_b + staged * line_b + staged * line_b + rows * row_b
+    issue = rows * row_b + rows * line_b + rows * line_b + rows * row_b  # a row per choice
     ms = e0.elapsed_time(e1) / steps
     coll.close()
     del coll, ins, outs, topk
@@ -750,9 +754,11 @@ def moe_row(cd, stream, steps=5, path=None, tokens=4096) -> dict:
              {"stage_ms": round(times[0] / steps, 4), "copy_ms": round(times[1] / steps, 4)})
     return {"ms": round(ms, 4), "GB/s": round(unique / ms / 1e6, 1),
             "path": "composed" if composed else "streamed",
-            "algorithmic_bytes": unique, "issue_level_bytes": issue, **split,
-            "note": "bytes: each token row read once, staged K times as LL128, "
-                    "every routed row read and unpacked once", "status": st}
+            "algorithmic_bytes": unique, "issue_level_bytes": issue, "staged_rows": staged,
+            "routed_rows": rows, **split,
+            "note": "bytes: each token row read once, staged as LL128 once per destination "
+                    "rank it is routed to, each staged row read once and unpacked into "
+                    "every routed row", "status": st}
 
 
 def main() -> int:

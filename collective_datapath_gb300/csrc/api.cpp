@@ -97,6 +97,8 @@ void fill_base(coll_spec* s) {
     M.entry_rank = reinterpret_cast<uint32_t*>(s->ws + p.off_entry_rank);
     M.block_off = reinterpret_cast<uint32_t*>(s->ws + p.off_block_off);
     M.cnt = reinterpret_cast<uint32_t*>(s->ws + p.off_cnt);
+    M.tok_rank = reinterpret_cast<uint32_t*>(s->ws + p.off_tok_rank);
+    M.dblock_off = reinterpret_cast<uint32_t*>(s->ws + p.off_dblock_off);
     M.stage_off = reinterpret_cast<uint32_t*>(s->ws + p.off_stage_off);
     M.out_off = reinterpret_cast<uint32_t*>(s->ws + p.off_out_off);
     M.rows_dest = reinterpret_cast<uint32_t*>(s->ws + p.off_rows_dest);

@@ -168,14 +168,17 @@ static int derive_moe(const DeriveInput& in, Plan& p) {
   p.off_entry_rank = table(4 * n * tk);
   p.off_block_off = table(4ull * n * p.moe_nblocks * in.experts);
   p.off_cnt = table(4ull * n * in.experts);
-  p.off_stage_off = table(4ull * n * in.experts);
+  p.off_tok_rank = table(4ull * n * in.tokens * n);
+  p.off_dblock_off = table(4ull * n * p.moe_nblocks * n);
+  p.off_stage_off = table(4ull * n * n);
   p.off_out_off = table(4ull * n * p.moe_el * n);
   p.off_rows_dest = table(4ull * n);
   p.off_counts_out = table(4ull * (n * p.moe_el * n + n));
   p.off_moe_flags = table(8ull * n * p.moe_nblocks * kMoeSubs);
   p.off_counters = table(4);
   off = round_up(off, 4096);
-  p.p_rank_lines = tk * p.moe_row_lines;
+  // one staged row per (token, destination holding one of its experts)
+  p.p_rank_lines = (uint64_t)in.tokens * std::min(in.topk, n) * p.moe_row_lines;
   p.P.rank_bytes = round_up(p.p_rank_lines * kLL128LineBytes, 4096);
   p.P.slot_bytes = p.P.rank_bytes * (uint64_t)n;
   p.P.slot_mask = (uint64_t)p.slots - 1;

@@ -69,7 +69,8 @@ struct Plan {
   // MoE dispatch geometry and table offsets
   int moe_tokens = 0, moe_hidden = 0, moe_k = 0, moe_experts = 0, moe_el = 0, moe_nblocks = 0;
   uint32_t moe_row_lines = 0, moe_max_rows = 0;
-  uint64_t off_entry_rank = 0, off_block_off = 0, off_cnt = 0, off_stage_off = 0,
+  uint64_t off_entry_rank = 0, off_block_off = 0, off_cnt = 0, off_tok_rank = 0,
+           off_dblock_off = 0, off_stage_off = 0,
            off_out_off = 0, off_rows_dest = 0, off_counts_out = 0, off_moe_flags = 0;
   // workspace layout (byte offsets from the workspace base)
   uint64_t off_sitems, off_items1, off_items2, off_counters;

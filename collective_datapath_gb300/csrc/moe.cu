@@ -14,15 +14,19 @@
 // Steps, all on the device:
 //  k_moe_count    per (source, block of 16 tokens): per-expert counts and
 //                 the stable rank of every (token, choice) among the block's
-//                 tokens routed to the same expert
-//  k_moe_scan_src per source: block prefixes, cnt[p][e], and stage_off[p][e]
-//                 (the source's staging image = rows ordered by expert, then
-//                 token: one contiguous partition per destination)
+//                 tokens routed to the same expert; per destination, the rank
+//                 of every token with a choice there among the block's tokens
+//  k_moe_scan_src per source (two CTAs: expert columns, destination columns):
+//                 block prefixes, cnt[p][e], and stage_off[p][d]
+//                 (the source's staging image = rows ordered by destination,
+//                 then token: one contiguous partition per destination, each
+//                 token staged once for every destination it is routed to)
 //  k_moe_stage    per token row: one 1-D TMA bulk copy of the row into shared
-//                 memory, then K LL128 copies of it into the staging image
+//                 memory, then one LL128 copy of it per destination
 //  k_moe_scan_dst per destination: out_off[d][le][p], counts, rows
-//  k_moe_copy     one warp per output row: validate the row's LL128 lines
-//                 through a cp.async ring and unpack them
+//  k_moe_copy     one warp per staged row: validate its LL128 lines through a
+//                 cp.async ring and unpack them into each of the token's
+//                 output rows on that destination (one per choice there)
 //  k_moe_composed the stage and copy steps as tasks of one launch (after the
 //                 routing kernels), staged rows read back mostly from L2
 #include <cuda_runtime.h>
@@ -57,6 +61,19 @@ __global__ void __launch_bounds__(kMoeThreads) k_moe_count(RunParams P) {
     s_topk[i] = e;
   }
   __syncthreads();
+  // per (token, destination): does one of the token's choices live there
+  const int n = P.nranks;
+  __shared__ uint8_t s_on[kMoeBlockTokens * kMaxRanks];
+  for (int i = threadIdx.x; i < nt * n; i += blockDim.x) {
+    const int tok = i / n, d = i % n;
+    bool on = false;
+    for (int j = 0; j < M.k; ++j) {
+      const int32_t e = s_topk[tok * M.k + j];
+      on |= e >= 0 && e / M.el == d;
+    }
+    s_on[i] = on;
+  }
+  __syncthreads();
   uint32_t* rank_out = M.entry_rank + (size_t)p * M.tokens * M.k + (size_t)t0 * M.k;
   uint32_t* bcnt = M.block_off + ((size_t)p * M.nblocks + blockIdx.x) * M.experts;
   for (int e = threadIdx.x; e < M.experts; e += blockDim.x) {
@@ -65,37 +82,58 @@ __global__ void __launch_bounds__(kMoeThreads) k_moe_count(RunParams P) {
       if (s_topk[i] == e) rank_out[i] = c++;
     bcnt[e] = c;
   }
+  // per destination: the block's tokens with at least one choice there, in
+  // token order (each is staged once for that destination)
+  uint32_t* trank = M.tok_rank + ((size_t)p * M.tokens + t0) * n;
+  uint32_t* dcnt = M.dblock_off + ((size_t)p * M.nblocks + blockIdx.x) * n;
+  const int d = (int)blockDim.x - 1 - (int)threadIdx.x;  // the last threads: n <= blockDim
+  if (d < n) {
+    uint32_t c = 0;
+    for (int i = 0; i < nt; ++i) trank[(size_t)i * n + d] = s_on[i * n + d] ? c++ : ~0u;
+    dcnt[d] = c;
+  }
+}
+
+// Exclusive prefix over the blocks of one column of a [nblocks][stride]
+// table of block counts, in place; returns the column's total.
+__device__ uint32_t prefix_blocks(uint32_t* col, size_t stride, int nblocks) {
+  constexpr int kBatch = 16;  // block counts loaded before any is rewritten
+  uint32_t run = 0;
+  for (int b0 = 0; b0 < nblocks; b0 += kBatch) {
+    uint32_t v[kBatch];
+#pragma unroll
+    for (int j = 0; j < kBatch; ++j) v[j] = b0 + j < nblocks ? col[(size_t)(b0 + j) * stride] : 0u;
+#pragma unroll
+    for (int j = 0; j < kBatch; ++j)
+      if (b0 + j < nblocks) {
+        col[(size_t)(b0 + j) * stride] = run;
+        run += v[j];
+      }
+  }
+  return run;
 }
 
 __global__ void __launch_bounds__(kMoeThreads) k_moe_scan_src(RunParams P) {
+  __shared__ uint32_t s_dcnt[kMaxRanks];
   const MoeParams& M = P.moe;
   const int p = P.stage_rank >= 0 ? P.stage_rank : (int)blockIdx.x;
-  uint32_t* cnt = M.cnt + (size_t)p * M.experts;
-  constexpr int kBatch = 16;  // block counts loaded before any is rewritten
-  for (int e = threadIdx.x; e < M.experts; e += blockDim.x) {
-    uint32_t run = 0;
-    uint32_t* col = M.block_off + (size_t)p * M.nblocks * M.experts + e;
-    for (int b0 = 0; b0 < M.nblocks; b0 += kBatch) {
-      uint32_t v[kBatch];
-#pragma unroll
-      for (int j = 0; j < kBatch; ++j)
-        v[j] = b0 + j < M.nblocks ? col[(size_t)(b0 + j) * M.experts] : 0u;
-#pragma unroll
-      for (int j = 0; j < kBatch; ++j)
-        if (b0 + j < M.nblocks) {
-          col[(size_t)(b0 + j) * M.experts] = run;  // exclusive prefix over blocks
-          run += v[j];
-        }
-    }
-    cnt[e] = run;
+  const int n = P.nranks;
+  if (blockIdx.y == 0) {  // a thread per expert column
+    for (int c = threadIdx.x; c < M.experts; c += blockDim.x)
+      M.cnt[(size_t)p * M.experts + c] =
+          prefix_blocks(M.block_off + (size_t)p * M.nblocks * M.experts + c, M.experts, M.nblocks);
+    return;
   }
+  // a second CTA per source: a thread per destination column
+  for (int d = threadIdx.x; d < n; d += blockDim.x)
+    s_dcnt[d] = prefix_blocks(M.dblock_off + (size_t)p * M.nblocks * n + d, n, M.nblocks);
   __syncthreads();
   if (threadIdx.x == 0) {
+    // the staging image: one partition per destination, in rank order
     uint32_t run = 0;
-    uint32_t* off = M.stage_off + (size_t)p * M.experts;
-    for (int e = 0; e < M.experts; ++e) {
-      off[e] = run;
-      run += cnt[e];
+    for (int d = 0; d < n; ++d) {
+      M.stage_off[(size_t)p * n + d] = run;
+      run += s_dcnt[d];
     }
   }
 }
@@ -131,6 +169,34 @@ size_t moe_stage_smem_bytes(int hidden) {
   return 2 * (((size_t)hidden * 2 + 127) / 128 * 128);
 }
 
+// First staged row of (source p, token t) for destination d in p's staging
+// image, or -1 when none of the token's choices lives on d.
+__device__ __forceinline__ int64_t moe_staged_row(const MoeParams& M, int n, int p, int t, int d) {
+  const uint32_t r = M.tok_rank[((size_t)p * M.tokens + t) * n + d];
+  if (r == ~0u) return -1;
+  return (int64_t)M.stage_off[(size_t)p * n + d] +
+         M.dblock_off[((size_t)p * M.nblocks + t / kMoeBlockTokens) * n + d] + r;
+}
+
+// Writes the token row at `row` (shared memory, row_bytes) as one staged
+// LL128 row at `dst`: every 128-byte line holds 60 16-bit units and the
+// epoch; a warp writes four lines per step, one 16-byte store per lane.
+__device__ __forceinline__ void moe_write_row(char* dst, uint32_t row, uint32_t row_bytes,
+                                              uint32_t row_lines, int lane, uint64_t e) {
+  const int li = lane >> 3, kk = lane & 7;
+  for (uint32_t r = 0; r < row_lines / kLL128RowLines; ++r) {
+    const uint32_t off = (uint32_t)kRowElems * 2 * r + 120 * li + 16 * kk;
+    const uint2 a = off < row_bytes ? lds_v2(row + off) : make_uint2(0, 0);
+    const uint2 b = (kk < 7 && off + 8 < row_bytes) ? lds_v2(row + off + 8) : make_uint2(0, 0);
+    uint4 v = make_uint4(a.x, a.y, b.x, b.y);
+    if (kk == 7) {
+      v.z = (uint32_t)e;
+      v.w = (uint32_t)(e >> 32);
+    }
+    st_v4(dst + (size_t)r * kRowBytes + 16 * lane, v);
+  }
+}
+
 __global__ void __launch_bounds__(kMoeThreads) k_moe_stage(RunParams P) {
   extern __shared__ __align__(128) char smem[];
   __shared__ __align__(8) uint64_t mbar[2];
@@ -138,7 +204,6 @@ __global__ void __launch_bounds__(kMoeThreads) k_moe_stage(RunParams P) {
   const uint64_t e = begin_run(P);
   const MoeParams& M = P.moe;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
-  const int li = lane >> 3, kk = lane & 7;
   const uint32_t row_bytes = (uint32_t)M.hidden * 2;
   const uint32_t buf_stride = (row_bytes + 127) / 128 * 128;
   const uint32_t sbuf = (uint32_t)__cvta_generic_to_shared(smem);
@@ -184,124 +249,142 @@ __global__ void __launch_bounds__(kMoeThreads) k_moe_stage(RunParams P) {
     unit_src(u, p, t);
     const uint32_t row = sbuf + cur * buf_stride;
     char* img = P.ws + P.P.base + (e & P.P.slot_mask) * P.P.slot_bytes + (uint64_t)p * P.P.rank_bytes;
-    for (int j = warp; j < M.k; j += nwarps) {
-      const size_t ent = (size_t)t * M.k + j;
-      const int ex = M.topk[p][ent];
-      if (ex < 0 || ex >= M.experts) continue;
-      const uint32_t s = M.stage_off[(size_t)p * M.experts + ex] +
-                         M.block_off[((size_t)p * M.nblocks + t / kMoeBlockTokens) * M.experts + ex] +
-                         M.entry_rank[(size_t)p * M.tokens * M.k + ent];
-      char* dst = img + (uint64_t)s * M.row_lines * kLL128LineBytes;
-      for (uint32_t r = 0; r < M.row_lines / kLL128RowLines; ++r) {
-        const uint32_t off = (uint32_t)kRowElems * 2 * r + 120 * li + 16 * kk;
-        const uint2 a = off < row_bytes ? lds_v2(row + off) : make_uint2(0, 0);
-        const uint2 b = (kk < 7 && off + 8 < row_bytes) ? lds_v2(row + off + 8) : make_uint2(0, 0);
-        uint4 v = make_uint4(a.x, a.y, b.x, b.y);
-        if (kk == 7) {
-          v.z = (uint32_t)e;
-          v.w = (uint32_t)(e >> 32);
-        }
-        st_v4(dst + (size_t)r * kRowBytes + 16 * lane, v);
-      }
+    for (int d = warp; d < P.nranks; d += nwarps) {  // one staged row per destination
+      const int64_t srow = moe_staged_row(M, P.nranks, p, t, d);
+      if (srow >= 0)
+        moe_write_row(img + (uint64_t)srow * M.row_lines * kLL128LineBytes, row, row_bytes,
+                      M.row_lines, lane, e);
     }
     __syncthreads();  // the buffer is free for the load after next
   }
   finish_run(P, e);
 }
 
-// ---- copy: one warp per output row ----------------------------------------------
+// ---- copy: one warp per staged row ---------------------------------------------
 
 constexpr int kMoeRing = 8;
 
-size_t moe_copy_smem_bytes(int nranks, int experts) {
-  const int el = experts / nranks;
-  return (size_t)(kMoeThreads / 32) * kMoeRing * kRowBytes +
-         sizeof(uint32_t) * ((size_t)nranks * el * nranks + (size_t)nranks * experts +
-                             kMaxRanks + 1);
+// The output rows of destination d that (source p, token t) fills: lane j
+// holds the row of choice j in o0 (choice j + 32 in o1), and the warp-uniform
+// masks name the choices that live on d.  Rows past the capacity are left
+// out (the routing latched that error).
+struct MoeFan {
+  uint32_t mask0, mask1, o0, o1;
+};
+
+__device__ __forceinline__ MoeFan moe_dest_rows(const MoeParams& M, int n, int p, int t, int d,
+                                                int lane) {
+  uint32_t o[2] = {0, 0};
+  bool on[2] = {false, false};
+#pragma unroll
+  for (int c = 0; c < 2; ++c) {
+    const int j = lane + 32 * c;
+    if (j >= M.k) continue;
+    const size_t ent = (size_t)t * M.k + j;
+    const int ex = M.topk[p][ent];
+    if (ex < 0 || ex >= M.experts || ex / M.el != d) continue;
+    const int le = ex - d * M.el;
+    o[c] = M.out_off[((size_t)d * M.el + le) * n + p] +
+           M.block_off[((size_t)p * M.nblocks + t / kMoeBlockTokens) * M.experts + ex] +
+           M.entry_rank[(size_t)p * M.tokens * M.k + ent];
+    on[c] = o[c] < M.max_rows;
+  }
+  MoeFan f;
+  f.mask0 = __ballot_sync(0xFFFFFFFFu, on[0]);
+  f.mask1 = __ballot_sync(0xFFFFFFFFu, on[1]);
+  f.o0 = o[0];
+  f.o1 = o[1];
+  return f;
 }
 
+// Validates one staged row (src: epoch-e LL128 lines staged by source p, the
+// first of them line0 of p's image) through the warp's cp.async ring at
+// wbase, and stores each 512-byte step's 240 units into every output row of
+// f.  discard: the row has no other reader, so each step's lines leave L2
+// once read.  false: a line's wait ran out (error latched).
+template <int kRing>
+__device__ __forceinline__ bool moe_copy_row(const RunParams& P, const char* src, int64_t line0,
+                                             int p, uint16_t* out_d, int nrows_w, const MoeFan& f,
+                                             uint32_t wbase, int lane, uint64_t e, bool discard) {
+  const int hidden = P.moe.hidden;
+  const uint64_t pol = l2_evict_first_policy();  // output rows are written once
+  const int q = lane < 30 ? lane : 29;
+  const uint32_t g0off = 128 * ((2 * q) / 15) + 8 * ((2 * q) % 15);
+  const uint32_t g1off = 128 * ((2 * q + 1) / 15) + 8 * ((2 * q + 1) % 15);
+  auto issue = [&](int r) {
+    if (r < nrows_w)
+      cp_async16(wbase + (r % kRing) * kRowBytes + 16 * lane, src + (size_t)r * kRowBytes + 16 * lane,
+                 true);
+    cp_async_commit();
+  };
+#pragma unroll
+  for (int r = 0; r < kRing; ++r) issue(r);
+  bool ok = true;
+  for (int r = 0; r < nrows_w; ++r) {
+    cp_async_wait<kRing - 1>();
+    __syncwarp();
+    const uint32_t slot = wbase + (r % kRing) * kRowBytes;
+    const bool ready = (lane & 7) != 7 || lds_u64(slot + 16 * lane + 8) == e;
+    if (!__all_sync(0xFFFFFFFFu, ready)) {
+      const char* grow = src + (size_t)r * kRowBytes;
+      if (!ll128_wait_chunk(P, grow, lane, ready, e, p, line0 + (int64_t)r * kLL128RowLines)) {
+        ok = false;
+        break;
+      }
+      sts_v4(slot + 16 * lane, ld_v4(grow + 16 * lane));
+      __syncwarp();
+    }
+    const uint2 a = lds_v2(slot + g0off), c = lds_v2(slot + g1off);
+    __syncwarp();
+    issue(r + kRing);
+    if (discard && lane < 4)
+      asm volatile("discard.global.L2 [%0], 128;" ::"l"(src + (size_t)r * kRowBytes + 128 * lane)
+                   : "memory");
+    const int64_t left = (int64_t)hidden - (int64_t)r * kRowElems;
+    const bool mine = lane < 30 && 8 * lane < left;
+    const uint4 v = make_uint4(a.x, a.y, c.x, c.y);
+    uint16_t* col = out_d + (size_t)r * kRowElems + 8 * lane;
+    for (uint32_t m = f.mask0; m; m &= m - 1) {
+      const uint32_t o = __shfl_sync(0xFFFFFFFFu, f.o0, __ffs(m) - 1);
+      if (mine) st_v4_hint(col + (uint64_t)o * hidden, v, pol);
+    }
+    for (uint32_t m = f.mask1; m; m &= m - 1) {
+      const uint32_t o = __shfl_sync(0xFFFFFFFFu, f.o1, __ffs(m) - 1);
+      if (mine) st_v4_hint(col + (uint64_t)o * hidden, v, pol);
+    }
+  }
+  cp_async_wait<0>();
+  __syncwarp();
+  return ok;
+}
+
+size_t moe_copy_smem_bytes() { return (size_t)(kMoeThreads / 32) * kMoeRing * kRowBytes; }
+
+// One warp per (source, destination, token) unit, in that order, so each
+// warp takes the staged rows of one partition in token order; units whose
+// token has no choice on the destination are skipped.
 __global__ void __launch_bounds__(kMoeThreads, 4) k_moe_copy(RunParams P) {
   extern __shared__ __align__(128) char smem[];
   const uint64_t e = begin_run(P);
   const MoeParams& M = P.moe;
   const int n = P.nranks;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
-  const int ntab = n * M.el * n;
-  uint32_t* s_out = reinterpret_cast<uint32_t*>(smem + (size_t)nwarps * kMoeRing * kRowBytes);
-  uint32_t* s_stage = s_out + ntab;
-  uint32_t* s_pre = s_stage + n * M.experts;
-  for (int i = threadIdx.x; i < ntab; i += blockDim.x) s_out[i] = M.out_off[i];
-  for (int i = threadIdx.x; i < n * M.experts; i += blockDim.x) s_stage[i] = M.stage_off[i];
-  if (threadIdx.x == 0) {
-    uint32_t run = 0;
-    for (int d = 0; d < n; ++d) {
-      s_pre[d] = run;
-      run += min(M.rows_dest[d], M.max_rows);
-    }
-    s_pre[n] = run;
-  }
-  __syncthreads();
-  const uint32_t total = s_pre[n];
   const uint32_t wbase = (uint32_t)__cvta_generic_to_shared(smem) +
                          (uint32_t)(warp * kMoeRing * kRowBytes);
-  const int q = lane < 30 ? lane : 29;
-  const uint32_t g0off = 128 * ((2 * q) / 15) + 8 * ((2 * q) % 15);
-  const uint32_t g1off = 128 * ((2 * q + 1) / 15) + 8 * ((2 * q + 1) % 15);
-  const int nrows = (int)(M.row_lines / kLL128RowLines);
-  for (uint32_t v = blockIdx.x * nwarps + warp; v < total; v += gridDim.x * nwarps) {
+  const int nrows_w = (int)(M.row_lines / kLL128RowLines);
+  const char* img0 = P.ws + P.P.base + (e & P.P.slot_mask) * P.P.slot_bytes;
+  const uint64_t units = (uint64_t)n * n * M.tokens;
+  for (uint64_t v = (uint64_t)blockIdx.x * nwarps + warp; v < units; v += (uint64_t)gridDim.x * nwarps) {
     if (aborted(P.ws)) break;
-    int d = 0;
-    while (d + 1 < n && v >= s_pre[d + 1]) ++d;
-    const uint32_t o = v - s_pre[d];
-    // last (le, p) block whose first row is <= o: it holds row o
-    const uint32_t* tab = s_out + (size_t)d * M.el * n;
-    int lo = 0, hi = M.el * n;  // upper_bound
-    while (lo < hi) {
-      const int mid = (lo + hi) >> 1;
-      if (tab[mid] <= o) lo = mid + 1; else hi = mid;
-    }
-    const int idx = lo - 1;
-    const int le = idx / n, p = idx % n;
-    const int ex = d * M.el + le;
-    const uint32_t s = s_stage[p * M.experts + ex] + (o - tab[idx]);
-    const char* src = P.ws + P.P.base + (e & P.P.slot_mask) * P.P.slot_bytes + (uint64_t)p * P.P.rank_bytes +
-                      (uint64_t)s * M.row_lines * kLL128LineBytes;
-    uint16_t* dst = P.out[d] + (uint64_t)o * M.hidden;
-    auto issue = [&](int j) {
-      if (j < nrows)
-        cp_async16(wbase + (j % kMoeRing) * kRowBytes + 16 * lane,
-                   src + (size_t)j * kRowBytes + 16 * lane, true);
-      cp_async_commit();
-    };
-#pragma unroll
-    for (int j = 0; j < kMoeRing; ++j) issue(j);
-    bool ok = true;
-    for (int j = 0; j < nrows; ++j) {
-      cp_async_wait<kMoeRing - 1>();
-      __syncwarp();
-      const uint32_t slot = wbase + (j % kMoeRing) * kRowBytes;
-      const bool ready =
-          (lane & 7) != 7 || lds_u64(slot + 16 * lane + 8) == e;
-      if (!__all_sync(0xFFFFFFFFu, ready)) {
-        const char* grow = src + (size_t)j * kRowBytes;
-        if (!ll128_wait_chunk(P, grow, lane, ready, e, p,
-                              (int64_t)s * M.row_lines + (int64_t)j * kLL128RowLines)) {
-          ok = false;
-          break;
-        }
-        sts_v4(slot + 16 * lane, ld_v4(grow + 16 * lane));
-        __syncwarp();
-      }
-      const uint2 a = lds_v2(slot + g0off), b = lds_v2(slot + g1off);
-      __syncwarp();
-      issue(j + kMoeRing);
-      const int64_t left = (int64_t)M.hidden - (int64_t)j * kRowElems;
-      if (lane < 30 && 8 * lane < left)
-        st_v4(dst + (size_t)j * kRowElems + 8 * lane, make_uint4(a.x, a.y, b.x, b.y));
-    }
-    cp_async_wait<0>();
-    __syncwarp();
-    if (!ok) break;
+    const int t = (int)(v % (uint64_t)M.tokens);
+    const int pd = (int)(v / (uint64_t)M.tokens), p = pd / n, d = pd % n;
+    const int64_t srow = moe_staged_row(M, n, p, t, d);
+    if (srow < 0) continue;
+    const MoeFan f = moe_dest_rows(M, n, p, t, d, lane);
+    const char* src = img0 + (uint64_t)p * P.P.rank_bytes + (uint64_t)srow * M.row_lines * kLL128LineBytes;
+    if (!moe_copy_row<kMoeRing>(P, src, srow * M.row_lines, p, P.out[d], nrows_w, f, wbase, lane, e,
+                                false))
+      break;
   }
   finish_run(P, e);
 }
@@ -309,52 +392,24 @@ __global__ void __launch_bounds__(kMoeThreads, 4) k_moe_copy(RunParams P) {
 // ---- composed dispatch: stage and copy tasks in one launch ---------------------
 // The queue of the composed twoshot (composed.cu) applied to the dispatch:
 // step b holds the stage tasks of routing block b (source p, kMoeSubTokens
-// tokens each: one TMA row load, K LL128 copies) and the copy tasks of block
-// b - lag (destination d, source p: every row source p's block routed to an
-// expert of d, one warp per row).  A copy task waits for the flags of its
-// block's stage tasks; each staged row has exactly that one reader, which
-// drops it from L2 once copied, so staged rows rarely reach HBM.
+// tokens each: one TMA row load, one LL128 copy per destination) and the copy
+// tasks of block b - lag (destination d, source p: the staged rows of source
+// p's block for d, one warp per staged row, each unpacked into all of the
+// token's output rows on d).  A copy task waits for the flags of its block's
+// stage tasks; each staged row has exactly that one reader, which drops it
+// from L2 once copied.
 constexpr int kMcWarps = 8, kMcRing = 8;
 
-// Two row buffers, the warps' copy rings, and a prefix table of the local
-// experts' row counts (up to 1024 local experts).
+// Two row buffers and the warps' copy rings.
 size_t moe_composed_smem_bytes(int hidden) {
-  return moe_stage_smem_bytes(hidden) + (size_t)kMcWarps * kMcRing * kRowBytes + 4 * 1028;
-}
-
-// K LL128 copies of one token row (in shared memory at `row`) into the
-// source's staging image; warp j writes choice j.
-__device__ __forceinline__ void moe_write_copies(const RunParams& P, const MoeParams& M, int p,
-                                                 int t, uint32_t row, uint32_t row_bytes,
-                                                 char* img, int lane, int warp, uint64_t e) {
-  const int li = lane >> 3, kk = lane & 7;
-  for (int j = warp; j < M.k; j += kMcWarps) {
-    const size_t ent = (size_t)t * M.k + j;
-    const int ex = M.topk[p][ent];
-    if (ex < 0 || ex >= M.experts) continue;
-    const uint32_t srow = M.stage_off[(size_t)p * M.experts + ex] +
-                          M.block_off[((size_t)p * M.nblocks + t / kMoeBlockTokens) * M.experts + ex] +
-                          M.entry_rank[(size_t)p * M.tokens * M.k + ent];
-    char* dst = img + (uint64_t)srow * M.row_lines * kLL128LineBytes;
-    for (uint32_t r = 0; r < M.row_lines / kLL128RowLines; ++r) {
-      const uint32_t off = (uint32_t)kRowElems * 2 * r + 120 * li + 16 * kk;
-      const uint2 a = off < row_bytes ? lds_v2(row + off) : make_uint2(0, 0);
-      const uint2 b = (kk < 7 && off + 8 < row_bytes) ? lds_v2(row + off + 8) : make_uint2(0, 0);
-      uint4 v = make_uint4(a.x, a.y, b.x, b.y);
-      if (kk == 7) {
-        v.z = (uint32_t)e;
-        v.w = (uint32_t)(e >> 32);
-      }
-      st_v4(dst + (size_t)r * kRowBytes + 16 * lane, v);
-    }
-  }
+  return moe_stage_smem_bytes(hidden) + (size_t)kMcWarps * kMcRing * kRowBytes;
 }
 
 __global__ void __launch_bounds__(kMcWarps * 32, 3) k_moe_composed(RunParams P) {
   extern __shared__ __align__(128) char smem[];
   __shared__ __align__(8) uint64_t mbar[2];
   __shared__ int s_task[2], s_ok;
-  __shared__ uint32_t s_rows;                   // rows of the current copy task
+  __shared__ int s_tok[kMoeBlockTokens];        // copy task: its staged rows' tokens
   const uint64_t e = begin_run(P);
   const MoeParams& M = P.moe;
   WsHeader* h = header(P.ws);
@@ -365,8 +420,6 @@ __global__ void __launch_bounds__(kMcWarps * 32, 3) k_moe_composed(RunParams P) 
   const uint32_t sbuf = (uint32_t)__cvta_generic_to_shared(smem);
   const uint32_t sbar = (uint32_t)__cvta_generic_to_shared(mbar);
   const uint32_t wbase = sbuf + 2 * buf_stride + (uint32_t)(warp * kMcRing * kRowBytes);
-  uint32_t* s_pre = reinterpret_cast<uint32_t*>(smem + 2 * buf_stride +
-                                                 (size_t)kMcWarps * kMcRing * kRowBytes);
   const int slot = (int)(e & 1);
   const int per_step = n * kMoeSubs + n * n;
   const int ntasks = (M.nblocks + M.lag) * per_step;
@@ -382,9 +435,6 @@ __global__ void __launch_bounds__(kMcWarps * 32, 3) k_moe_composed(RunParams P) 
     s_ok = 1;
   }
   __syncthreads();
-  const int q = lane < 30 ? lane : 29;
-  const uint32_t g0off = 128 * ((2 * q) / 15) + 8 * ((2 * q) % 15);
-  const uint32_t g1off = 128 * ((2 * q + 1) / 15) + 8 * ((2 * q + 1) % 15);
   const int nrows_w = (int)(M.row_lines / kLL128RowLines);
   for (int it = 0;; ++it) {
     const int t = s_task[it & 1];
@@ -402,29 +452,41 @@ __global__ void __launch_bounds__(kMcWarps * 32, 3) k_moe_composed(RunParams P) 
         continue;
       }
       if (threadIdx.x == 0) {
+        const uint64_t in_pol = l2_evict_first_policy();  // token rows are read once
         for (int k = 0; k < nt; ++k) {
           fence_proxy_async_smem();
           mbar_expect_tx(sbar + 8 * k, row_bytes);
-          tma_load_1d(sbuf + k * buf_stride, P.in[p] + (size_t)(t0 + k) * M.hidden, row_bytes,
-                      sbar + 8 * k);
+          tma_load_1d_hint(sbuf + k * buf_stride, P.in[p] + (size_t)(t0 + k) * M.hidden, row_bytes,
+                           sbar + 8 * k, in_pol);
         }
       }
       char* img = img0 + (uint64_t)p * img_stride;
-      for (int k = 0; k < nt; ++k) {
-        if (threadIdx.x == 0) {
+      if (threadIdx.x == 0) {
+        for (int k = 0; k < nt; ++k) {  // every load is waited for (bounded), even after a timeout
           if (!mbar_wait_bounded(sbar + 8 * k, uses[k] & 1, P.timeout_ns)) {
             latch_error(P.ws, kStatusTimeout, p, (int64_t)(t0 + k));
             s_ok = 0;
-            for (int k2 = k + 1; k2 < nt; ++k2)   // let the other load land, bounded
-              mbar_wait_bounded(sbar + 8 * k2, uses[k2] & 1, P.timeout_ns);
           }
+          uses[k] += 1;
         }
-        __syncthreads();
-        if (!s_ok) break;
-        moe_write_copies(P, M, p, t0 + k, sbuf + k * buf_stride, row_bytes, img, lane, warp, e);
       }
-      if (threadIdx.x == 0)
-        for (int k = 0; k < nt; ++k) uses[k] += 1;
+      __syncthreads();
+      if (s_ok) {
+        // the sub-block's staged rows, one per (token, destination with a
+        // choice of it), spread over the warps: warp w writes the w-th, the
+        // (w + kMcWarps)-th ... of them
+        static_assert(kMoeSubTokens * kMaxRanks <= 32, "a lane per (token, destination)");
+        int64_t srow = -1;
+        if (lane < nt * n) srow = moe_staged_row(M, n, p, t0 + lane / n, lane % n);
+        uint32_t real = __ballot_sync(0xFFFFFFFFu, srow >= 0);
+        for (int i = 0; real; ++i, real &= real - 1) {
+          const int q = __ffs(real) - 1;
+          const int64_t sr = __shfl_sync(0xFFFFFFFFu, srow, q);
+          if (i % kMcWarps == warp)
+            moe_write_row(img + (uint64_t)sr * M.row_lines * kLL128LineBytes,
+                          sbuf + (q / n) * buf_stride, row_bytes, M.row_lines, lane, e);
+        }
+      }
       // release: every row of the sub-block is written
       __syncthreads();
       if (threadIdx.x == 0 && s_ok) {
@@ -461,80 +523,34 @@ __global__ void __launch_bounds__(kMcWarps * 32, 3) k_moe_composed(RunParams P) 
         fence_acq_rel_gpu();
       }
     }
-    // rows of each local expert of d in this block, prefix-summed
-    for (int le = threadIdx.x; le < M.el; le += blockDim.x) {
-      const int ex = d * M.el + le;
-      const uint32_t b0 = M.block_off[((size_t)p * M.nblocks + b) * M.experts + ex];
-      const uint32_t b1 = b + 1 < M.nblocks
-                              ? M.block_off[((size_t)p * M.nblocks + b + 1) * M.experts + ex]
-                              : M.cnt[(size_t)p * M.experts + ex];
-      s_pre[le + 1] = b1 - b0;
-    }
-    __syncthreads();
-    if (threadIdx.x == 0) {
-      s_pre[0] = 0;
-      for (int le = 0; le < M.el; ++le) s_pre[le + 1] += s_pre[le];
-      s_rows = s_pre[M.el];
-    }
-    __syncthreads();
-    if (!s_ok) break;
-    const uint32_t rows = s_rows;
-    for (uint32_t j = warp; j < rows; j += kMcWarps) {
-      int lo = 0, hi = M.el;  // last le with s_pre[le] <= j
-      while (hi - lo > 1) {
-        const int mid = (lo + hi) >> 1;
-        if (s_pre[mid] <= j) lo = mid; else hi = mid;
-      }
-      const int le = lo, ex = d * M.el + le;
-      const uint32_t i = j - s_pre[le];
-      const uint32_t boff = M.block_off[((size_t)p * M.nblocks + b) * M.experts + ex];
-      const uint32_t o = M.out_off[((size_t)d * M.el + le) * n + p] + boff + i;
-      if (o >= M.max_rows) continue;  // capacity error, latched by the routing
-      const uint32_t srow = M.stage_off[(size_t)p * M.experts + ex] + boff + i;
-      const char* src = img0 + (uint64_t)p * img_stride + (uint64_t)srow * M.row_lines * kLL128LineBytes;
-      uint16_t* dst = P.out[d] + (uint64_t)o * M.hidden;
-      auto issue = [&](int r) {
-        if (r < nrows_w)
-          cp_async16(wbase + (r % kMcRing) * kRowBytes + 16 * lane, src + (size_t)r * kRowBytes + 16 * lane,
-                     true);
-        cp_async_commit();
-      };
-#pragma unroll
-      for (int r = 0; r < kMcRing; ++r) issue(r);
-      bool ok = true;
-      for (int r = 0; r < nrows_w; ++r) {
-        cp_async_wait<kMcRing - 1>();
-        __syncwarp();
-        const uint32_t ring = wbase + (r % kMcRing) * kRowBytes;
-        const bool ready = (lane & 7) != 7 || lds_u64(ring + 16 * lane + 8) == e;
-        if (!__all_sync(0xFFFFFFFFu, ready)) {
-          const char* grow = src + (size_t)r * kRowBytes;
-          if (!ll128_wait_chunk(P, grow, lane, ready, e, p,
-                                (int64_t)srow * M.row_lines + (int64_t)r * kLL128RowLines)) {
-            ok = false;
-            break;
-          }
-          sts_v4(ring + 16 * lane, ld_v4(grow + 16 * lane));
-          __syncwarp();
+    // the block's tokens bound for d: consecutive staged rows, in token order
+    bool mine = false;
+    if ((int)threadIdx.x < kMoeBlockTokens) {
+      const int t = b * kMoeBlockTokens + threadIdx.x;
+      if (t < M.tokens) {
+        const uint32_t r = M.tok_rank[((size_t)p * M.tokens + t) * n + d];
+        if (r != ~0u) {
+          s_tok[r] = t;
+          mine = true;
         }
-        const uint2 a = lds_v2(ring + g0off), c = lds_v2(ring + g1off);
-        __syncwarp();
-        issue(r + kMcRing);
-        if (lane < 4)  // the row's four lines have no other reader
-          asm volatile("discard.global.L2 [%0], 128;" ::"l"(src + (size_t)r * kRowBytes + 128 * lane)
-                       : "memory");
-        const int64_t left = (int64_t)M.hidden - (int64_t)r * kRowElems;
-        if (lane < 30 && 8 * lane < left)
-          st_v4(dst + (size_t)r * kRowElems + 8 * lane, make_uint4(a.x, a.y, c.x, c.y));
       }
-      cp_async_wait<0>();
-      __syncwarp();
-      if (!ok) {
+    }
+    const int rows = __syncthreads_count(mine);
+    if (!s_ok) break;
+    const int64_t row0 = (int64_t)M.stage_off[(size_t)p * n + d] +
+                         M.dblock_off[((size_t)p * M.nblocks + b) * n + d];
+    for (int j = warp; j < rows; j += kMcWarps) {
+      const int tok = s_tok[j];
+      const MoeFan f = moe_dest_rows(M, n, p, tok, d, lane);
+      const int64_t srow = row0 + j;
+      const char* src = img0 + (uint64_t)p * img_stride + (uint64_t)srow * M.row_lines * kLL128LineBytes;
+      if (!moe_copy_row<kMcRing>(P, src, srow * M.row_lines, p, P.out[d], nrows_w, f, wbase, lane, e,
+                                 true)) {
         s_ok = 0;
         break;
       }
     }
-    __syncthreads();  // s_pre, s_task and s_ok are final
+    __syncthreads();  // s_tok, s_task and s_ok are final
     if (!s_ok) break;
   }
   finish_run(P, e);
@@ -550,7 +566,7 @@ cudaError_t launch_moe_stage_all(const RunParams& P, cudaStream_t s) {
     k_moe_count<<<dim3(M.nblocks, nsrc), kMoeThreads, smem, s>>>(P);
     if (cudaError_t e = cudaGetLastError()) return e;
   }
-  k_moe_scan_src<<<nsrc, kMoeThreads, 0, s>>>(P);
+  k_moe_scan_src<<<dim3(nsrc, 2), kMoeThreads, 0, s>>>(P);
   if (cudaError_t e = cudaGetLastError()) return e;
   const size_t bytes = moe_stage_smem_bytes(M.hidden);
   static size_t memo[kMaxDevices];
@@ -571,7 +587,7 @@ cudaError_t launch_moe_routing(const RunParams& P, cudaStream_t s) {
     k_moe_count<<<dim3(M.nblocks, P.nranks), kMoeThreads, smem, s>>>(P);
     if (cudaError_t e = cudaGetLastError()) return e;
   }
-  k_moe_scan_src<<<P.nranks, kMoeThreads, 0, s>>>(P);
+  k_moe_scan_src<<<dim3(P.nranks, 2), kMoeThreads, 0, s>>>(P);
   if (cudaError_t e = cudaGetLastError()) return e;
   k_moe_scan_dst<<<P.nranks, kMoeThreads, sizeof(uint32_t) * M.el * P.nranks, s>>>(P);
   return cudaGetLastError();
@@ -603,7 +619,7 @@ cudaError_t launch_moe_consume(const RunParams& P, cudaStream_t s) {
   const MoeParams& M = P.moe;
   k_moe_scan_dst<<<P.nranks, kMoeThreads, sizeof(uint32_t) * M.el * P.nranks, s>>>(P);
   if (cudaError_t e = cudaGetLastError()) return e;
-  const size_t bytes = moe_copy_smem_bytes(P.nranks, M.experts);
+  const size_t bytes = moe_copy_smem_bytes();
   static size_t memo[kMaxDevices];
   if (bytes > 48 * 1024)
     if (cudaError_t e = raise_smem_limit(k_moe_copy, bytes, memo)) return e;

@@ -108,7 +108,10 @@ struct MoeParams {
   uint32_t* entry_rank; // [N][tokens * k] rank among the block's rows of one expert
   uint32_t* block_off;  // [N][nblocks][experts] block counts, then prefixes
   uint32_t* cnt;        // [N][experts]
-  uint32_t* stage_off;  // [N][experts] first staged row of (source, expert)
+  uint32_t* tok_rank;   // [N][tokens][N] rank among the block's tokens bound for
+                        // one destination, ~0u if none of its choices lives there
+  uint32_t* dblock_off; // [N][nblocks][N] the same per destination: counts, then prefixes
+  uint32_t* stage_off;  // [N][N] first staged row of (source, destination)
   uint32_t* out_off;    // [N dest][el][N src] first output row of the block
   uint32_t* rows_dest;  // [N]
   int32_t* counts_out;  // [N dest][el][N src] counts, then rows per destination

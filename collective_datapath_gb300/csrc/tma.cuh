@@ -50,6 +50,15 @@ __device__ __forceinline__ void tma_load_1d(uint32_t dst, const void* src, uint3
       "l"(src), "r"(bytes), "r"(mbar)
       : "memory");
 }
+// The same with an L2 eviction policy (createpolicy) for the source lines.
+__device__ __forceinline__ void tma_load_1d_hint(uint32_t dst, const void* src, uint32_t bytes,
+                                                 uint32_t mbar, uint64_t pol) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], "
+      "%2, [%3], %4;" ::"r"(dst),
+      "l"(src), "r"(bytes), "r"(mbar), "l"(pol)
+      : "memory");
+}
 // Shared -> global bulk store, tracked by the issuing thread's bulk groups.
 __device__ __forceinline__ void tma_store_1d(void* dst, uint32_t src, uint32_t bytes) {
   asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst),
