@@ -180,11 +180,12 @@ __device__ __forceinline__ int64_t moe_staged_row(const MoeParams& M, int n, int
 
 // Writes the token row at `row` (shared memory, row_bytes) as one staged
 // LL128 row at `dst`: every 128-byte line holds 60 16-bit units and the
-// epoch; a warp writes four lines per step, one 16-byte store per lane.
+// epoch; a warp writes four lines per step, one 16-byte store per lane,
+// steps r0 .. r1-1 of the row.
 __device__ __forceinline__ void moe_write_row(char* dst, uint32_t row, uint32_t row_bytes,
-                                              uint32_t row_lines, int lane, uint64_t e) {
+                                              uint32_t r0, uint32_t r1, int lane, uint64_t e) {
   const int li = lane >> 3, kk = lane & 7;
-  for (uint32_t r = 0; r < row_lines / kLL128RowLines; ++r) {
+  for (uint32_t r = r0; r < r1; ++r) {
     const uint32_t off = (uint32_t)kRowElems * 2 * r + 120 * li + 16 * kk;
     const uint2 a = off < row_bytes ? lds_v2(row + off) : make_uint2(0, 0);
     const uint2 b = (kk < 7 && off + 8 < row_bytes) ? lds_v2(row + off + 8) : make_uint2(0, 0);
@@ -252,8 +253,8 @@ __global__ void __launch_bounds__(kMoeThreads) k_moe_stage(RunParams P) {
     for (int d = warp; d < P.nranks; d += nwarps) {  // one staged row per destination
       const int64_t srow = moe_staged_row(M, P.nranks, p, t, d);
       if (srow >= 0)
-        moe_write_row(img + (uint64_t)srow * M.row_lines * kLL128LineBytes, row, row_bytes,
-                      M.row_lines, lane, e);
+        moe_write_row(img + (uint64_t)srow * M.row_lines * kLL128LineBytes, row, row_bytes, 0,
+                      M.row_lines / kLL128RowLines, lane, e);
     }
     __syncthreads();  // the buffer is free for the load after next
   }
@@ -297,14 +298,15 @@ __device__ __forceinline__ MoeFan moe_dest_rows(const MoeParams& M, int n, int p
   return f;
 }
 
-// Validates one staged row (src: epoch-e LL128 lines staged by source p, the
-// first of them line0 of p's image) through the warp's cp.async ring at
-// wbase, and stores each 512-byte step's 240 units into every output row of
-// f.  discard: the row has no other reader, so each step's lines leave L2
-// once read.  false: a line's wait ran out (error latched).
+// Validates steps r0 .. r1-1 (512 bytes, four lines each) of one staged row
+// (src: epoch-e LL128 lines staged by source p, the first of them line0 of
+// p's image) through the warp's cp.async ring at wbase, and stores each
+// step's 240 units into every output row of f.  discard: the row has no
+// other reader, so each step's lines leave L2 once read.  false: a line's
+// wait ran out (error latched).
 template <int kRing>
 __device__ __forceinline__ bool moe_copy_row(const RunParams& P, const char* src, int64_t line0,
-                                             int p, uint16_t* out_d, int nrows_w, const MoeFan& f,
+                                             int p, uint16_t* out_d, int r0, int r1, const MoeFan& f,
                                              uint32_t wbase, int lane, uint64_t e, bool discard) {
   const int hidden = P.moe.hidden;
   const uint64_t pol = l2_evict_first_policy();  // output rows are written once
@@ -312,18 +314,18 @@ __device__ __forceinline__ bool moe_copy_row(const RunParams& P, const char* src
   const uint32_t g0off = 128 * ((2 * q) / 15) + 8 * ((2 * q) % 15);
   const uint32_t g1off = 128 * ((2 * q + 1) / 15) + 8 * ((2 * q + 1) % 15);
   auto issue = [&](int r) {
-    if (r < nrows_w)
-      cp_async16(wbase + (r % kRing) * kRowBytes + 16 * lane, src + (size_t)r * kRowBytes + 16 * lane,
-                 true);
+    if (r < r1)
+      cp_async16(wbase + ((r - r0) % kRing) * kRowBytes + 16 * lane,
+                 src + (size_t)r * kRowBytes + 16 * lane, true);
     cp_async_commit();
   };
 #pragma unroll
-  for (int r = 0; r < kRing; ++r) issue(r);
+  for (int i = 0; i < kRing; ++i) issue(r0 + i);
   bool ok = true;
-  for (int r = 0; r < nrows_w; ++r) {
+  for (int r = r0; r < r1; ++r) {
     cp_async_wait<kRing - 1>();
     __syncwarp();
-    const uint32_t slot = wbase + (r % kRing) * kRowBytes;
+    const uint32_t slot = wbase + ((r - r0) % kRing) * kRowBytes;
     const bool ready = (lane & 7) != 7 || lds_u64(slot + 16 * lane + 8) == e;
     if (!__all_sync(0xFFFFFFFFu, ready)) {
       const char* grow = src + (size_t)r * kRowBytes;
@@ -382,8 +384,8 @@ __global__ void __launch_bounds__(kMoeThreads, 4) k_moe_copy(RunParams P) {
     if (srow < 0) continue;
     const MoeFan f = moe_dest_rows(M, n, p, t, d, lane);
     const char* src = img0 + (uint64_t)p * P.P.rank_bytes + (uint64_t)srow * M.row_lines * kLL128LineBytes;
-    if (!moe_copy_row<kMoeRing>(P, src, srow * M.row_lines, p, P.out[d], nrows_w, f, wbase, lane, e,
-                                false))
+    if (!moe_copy_row<kMoeRing>(P, src, srow * M.row_lines, p, P.out[d], 0, nrows_w, f, wbase, lane,
+                                e, false))
       break;
   }
   finish_run(P, e);
@@ -399,6 +401,10 @@ __global__ void __launch_bounds__(kMoeThreads, 4) k_moe_copy(RunParams P) {
 // stage tasks; each staged row has exactly that one reader, which drops it
 // from L2 once copied.
 constexpr int kMcWarps = 8, kMcRing = 8;
+// Each staged row is written and copied as kMcSplit ranges of its 512-byte
+// steps, so a task's warps get near-equal shares (the task ends at a CTA
+// barrier, where its busiest warp sets the pace).
+constexpr int kMcSplit = 2;
 
 // Two row buffers and the warps' copy rings.
 size_t moe_composed_smem_bytes(int hidden) {
@@ -482,9 +488,11 @@ __global__ void __launch_bounds__(kMcWarps * 32, 3) k_moe_composed(RunParams P) 
         for (int i = 0; real; ++i, real &= real - 1) {
           const int q = __ffs(real) - 1;
           const int64_t sr = __shfl_sync(0xFFFFFFFFu, srow, q);
-          if (i % kMcWarps == warp)
-            moe_write_row(img + (uint64_t)sr * M.row_lines * kLL128LineBytes,
-                          sbuf + (q / n) * buf_stride, row_bytes, M.row_lines, lane, e);
+          for (int part = 0; part < kMcSplit; ++part)
+            if ((i * kMcSplit + part) % kMcWarps == warp)
+              moe_write_row(img + (uint64_t)sr * M.row_lines * kLL128LineBytes,
+                            sbuf + (q / n) * buf_stride, row_bytes, part * nrows_w / kMcSplit,
+                            (part + 1) * nrows_w / kMcSplit, lane, e);
         }
       }
       // release: every row of the sub-block is written
@@ -539,13 +547,13 @@ __global__ void __launch_bounds__(kMcWarps * 32, 3) k_moe_composed(RunParams P) 
     if (!s_ok) break;
     const int64_t row0 = (int64_t)M.stage_off[(size_t)p * n + d] +
                          M.dblock_off[((size_t)p * M.nblocks + b) * n + d];
-    for (int j = warp; j < rows; j += kMcWarps) {
-      const int tok = s_tok[j];
-      const MoeFan f = moe_dest_rows(M, n, p, tok, d, lane);
+    for (int u = warp; u < rows * kMcSplit; u += kMcWarps) {
+      const int j = u / kMcSplit, part = u % kMcSplit;
+      const MoeFan f = moe_dest_rows(M, n, p, s_tok[j], d, lane);
       const int64_t srow = row0 + j;
       const char* src = img0 + (uint64_t)p * img_stride + (uint64_t)srow * M.row_lines * kLL128LineBytes;
-      if (!moe_copy_row<kMcRing>(P, src, srow * M.row_lines, p, P.out[d], nrows_w, f, wbase, lane, e,
-                                 true)) {
+      if (!moe_copy_row<kMcRing>(P, src, srow * M.row_lines, p, P.out[d], part * nrows_w / kMcSplit,
+                                 (part + 1) * nrows_w / kMcSplit, f, wbase, lane, e, true)) {
         s_ok = 0;
         break;
       }
