@@ -94,7 +94,7 @@ _sig("coll_run_late", _st, _vp, _P(_vp), _P(_vp), _P(_vp), _P(ctypes.c_int64), _
 _sig("coll_get_rejections", _st, _vp, _vp, _P(ctypes.c_uint64))
 _sig("coll_debug_items", _st, _vp, ctypes.c_int, _P(ctypes.c_int64), _sz, _P(_sz))
 _sig("coll_debug_plan", _st, _vp, _P(ctypes.c_int), _P(ctypes.c_int),
-     _P(ctypes.c_int), _P(ctypes.c_int))
+     _P(ctypes.c_int), _P(ctypes.c_int), _P(ctypes.c_int))
 _sig("coll_set_profile_events", _st, _vp, _P(_vp), ctypes.c_int)
 _sig("coll_last_launches", _st, _vp, _P(ctypes.c_int))
 _sig("coll_allreduce_static", _st, ctypes.c_int, _sz, _P(_vp), _P(_vp), _vp)
@@ -282,11 +282,11 @@ def coll_debug_items(spec: int, which: int):
 
 
 def coll_debug_plan(spec: int) -> dict:
-    a, p, c, e = (ctypes.c_int() for _ in range(4))
+    a, p, c, e, d = (ctypes.c_int() for _ in range(5))
     _check(_lib.coll_debug_plan(spec, ctypes.byref(a), ctypes.byref(p), ctypes.byref(c),
-                                ctypes.byref(e)), "coll_debug_plan")
+                                ctypes.byref(e), ctypes.byref(d)), "coll_debug_plan")
     return {"algorithm": a.value, "path": p.value, "ctas_per_rank": c.value,
-            "encoding": e.value}
+            "encoding": e.value, "dependent_launch": d.value}
 
 
 def coll_set_profile_events(spec: int, events: Sequence) -> None:

@@ -464,7 +464,8 @@ coll_status_t coll_run(coll_spec_t* s, const void* const* dev_ins, void* const* 
   if (dev_ins != nullptr && p.path == COLL_PATH_FUSED && !empty &&
       !(p.enc != ENC_LL128 && p.reset_mode == COLL_RESET_KERNEL)) {
     P.advance_epoch = 1;
-    return cuda_status(launched(s, launch_fused(P, p.n * p.ctas_per_rank, st), st));
+    return cuda_status(
+        launched(s, launch_fused(P, p.n * p.ctas_per_rank, st, p.dependent_launch), st));
   }
   if (dev_ins != nullptr && !p.sitems.empty()) {
     P.stage_rank = -1;
@@ -623,7 +624,7 @@ coll_status_t coll_run_late(coll_spec_t* s, const void* const* dev_ins, void* co
   P.sitems = nullptr;  // inputs were staged (with lines withheld)
   P.late_ctas = p.n;
   P.advance_epoch = 1;
-  return cuda_status(launch_fused(P, p.n * p.ctas_per_rank + p.n, as_stream(stream)));
+  return cuda_status(launch_fused(P, p.n * p.ctas_per_rank + p.n, as_stream(stream), false));
 }
 
 coll_status_t coll_debug_items(const coll_spec_t* s, int which, int64_t* buf, size_t cap,
@@ -654,8 +655,9 @@ coll_status_t coll_debug_items(const coll_spec_t* s, int which, int64_t* buf, si
 }
 
 coll_status_t coll_debug_plan(const coll_spec_t* s, int* algorithm, int* path,
-                              int* ctas_per_rank, int* encoding) {
+                              int* ctas_per_rank, int* encoding, int* dependent_launch) {
   if (s == nullptr) return COLL_ERR_INVALID;
+  if (dependent_launch) *dependent_launch = s->plan.dependent_launch ? 1 : 0;
   if (algorithm) *algorithm = s->plan.algorithm;
   if (path) *path = s->plan.path;
   if (ctas_per_rank) *ctas_per_rank = s->plan.ctas_per_rank;

@@ -212,7 +212,13 @@ __device__ __forceinline__ void count_rejection(char* ws) {
 // uses the other staging slot; no CTA waits at the end of its own work.
 __device__ __forceinline__ uint64_t begin_run(const RunParams& P) {
   WsHeader* h = header(P.ws);
+  // Under programmatic stream serialization the CTAs may start before the
+  // previous kernel in the stream has completed: wait for it (and for its
+  // writes) before reading anything; without that launch attribute the wait
+  // returns at once.  Then let a dependent launch place its CTAs.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const uint64_t e = ld_relaxed_u64(&h->epoch);
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   if (P.advance_epoch) {
     const int z = __syncthreads_or((int)(e >> 63));  // 0: the epoch never gets there
     if (threadIdx.x == 0)

@@ -683,17 +683,19 @@ cudaError_t launch_consume(const RunParams& P, int phase, int grid, cudaStream_t
   return cudaGetLastError();
 }
 
-cudaError_t launch_fused(const RunParams& P, int grid, cudaStream_t s) {
+cudaError_t launch_fused(const RunParams& P, int grid, cudaStream_t s, bool dependent) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = 0;
   cfg.stream = s;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeCooperative;
   attr[0].val.cooperative = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = dependent ? 2 : 1;
   if (P.enc == ENC_LL8) return cudaLaunchKernelEx(&cfg, k_fused<ENC_LL8>, P);
   if (P.enc == ENC_SENT) return cudaLaunchKernelEx(&cfg, k_fused<ENC_SENT>, P);
   return cudaLaunchKernelEx(&cfg, k_fused<ENC_LL128>, P);

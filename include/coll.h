@@ -152,7 +152,15 @@ enum { COLL_RESET_FUSED = 0, COLL_RESET_KERNEL = 1, COLL_RESET_NONE = 2,
        COLL_RESET_DEFERRED = 3 };
 
 /* Launch path: FUSED = stage and consume inside one cooperative kernel
- * (all CTAs co-resident; a CTA serves one emulated rank); STREAMED =
+ * (all CTAs co-resident; a CTA serves one emulated rank).  Up to 512 KiB per
+ * rank (input or output, whichever is larger) that kernel is a dependent
+ * launch: it carries programmatic stream serialization, so its CTAs can be
+ * placed while the previous kernel in the stream finishes, and they wait
+ * for that kernel to complete, with its writes visible, before reading the
+ * workspace or any input (griddepcontrol.wait).  Each of the library's
+ * kernels allows the next dependent launch to be placed once it has read
+ * the epoch; a caller's kernel launched that way must wait the same way
+ * before it reads the outputs.  STREAMED =
  * separate stage and consume kernels ordered by the stream; COMPOSED
  * (LL128 only: the twoshot all-reduce, reduce-scatter, all-to-all and
  * all-gather; AUTO never takes it for the all-gather, whose stream-ordered
@@ -358,10 +366,12 @@ coll_status_t coll_debug_items(const coll_spec_t *spec, int which, int64_t *buf,
 
 /* Summary of the derived plan: all-reduce algorithm (COLL_ONESHOT /
  * COLL_TWOSHOT, 0 for other collectives), launch path used when inputs are
- * given to coll_run (COLL_PATH_FUSED / COLL_PATH_STREAMED), CTAs per rank of
- * the fused path, and the encoding. */
+ * given to coll_run (COLL_PATH_*), CTAs per rank of the fused path, the
+ * encoding, and whether the fused launch is a dependent launch (1: launched
+ * with programmatic stream serialization; see COLL_PATH_FUSED).  Any output
+ * pointer may be NULL. */
 coll_status_t coll_debug_plan(const coll_spec_t *spec, int *algorithm, int *path,
-                              int *ctas_per_rank, int *encoding);
+                              int *ctas_per_rank, int *encoding, int *dependent_launch);
 
 /* Per-launch timing: when set, every following coll_run records events[0]
  * on its stream before its first launch and events[k] after its k-th launch

@@ -444,3 +444,25 @@ def test_fused_phases_fill_whole_rounds(cd, T):
             fair = -(-sum(load) // B)  # no CTA carries much more than its share
             assert max(load) <= 1.02 * fair + 8, (which, d, load)
     cd.coll_destroy(s)
+
+
+def test_dependent_launch_rule(cd):
+    """One-launch (fused) runs up to 512 KiB per rank, input or output, are
+    dependent launches; larger ones, and every other path, are not.  Plan
+    only (host)."""
+    def dep(triple, n, count, **kw):
+        s = cd.coll_spec_create(*triple, n, count, **kw)
+        try:
+            return cd.coll_debug_plan(s)["dependent_launch"]
+        finally:
+            cd.coll_destroy(s)
+
+    fused = dict(encoding=cd.COLL_LL8, path=cd.COLL_PATH_FUSED)
+    assert dep(cd.ALLREDUCE, 8, 4096, **fused) == 1                 # 8 KiB per rank
+    assert dep(cd.ALLREDUCE, 8, 256 * 1024, **fused) == 1           # 512 KiB
+    assert dep(cd.ALLREDUCE, 8, 256 * 1024 + 8, **fused) == 0
+    assert dep(cd.ALLREDUCE, 8, 4096, encoding=cd.COLL_LL8, path=cd.COLL_PATH_STREAMED) == 0
+    assert dep(cd.ALLREDUCE, 8, 4096, encoding=cd.COLL_ENC_AUTO) == 1   # policy: fused
+    # all-gather: 64 KiB in, 512 KiB out per rank; twice that is past the bound
+    assert dep(cd.ALLGATHER, 8, 8 * 32 * 1024, **fused) == 1
+    assert dep(cd.ALLGATHER, 8, 8 * 64 * 1024, **fused) == 0

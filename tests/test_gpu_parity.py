@@ -356,3 +356,62 @@ def test_composed_reduce_scatter_and_all_to_all(cd, name, n, count, shape, monke
         coll.run(ins, outs)
         check(coll, outs, expected(cd, triple, xs, count), n)
         assert coll.epoch() == e + 1
+
+
+@pytest.mark.parametrize("enc", [0, 2])
+def test_dependent_launches_chain(cd, enc):
+    """Fused runs are dependent launches: each must wait for the kernel
+    before it and see all of its writes.  Chain A -> B -> A, each run's
+    inputs being the previous run's outputs, then a plain torch kernel
+    (an XOR of low mantissa bits) between two runs; eagerly and replayed
+    from a CUDA graph, bit-exact against the oracle applied step by step."""
+    import torch
+
+    n, count = 8, 4096
+    a = make(cd, cd.ALLREDUCE, n, count, encoding=enc, path=cd.COLL_PATH_FUSED)
+    b = make(cd, cd.ALLREDUCE, n, count, encoding=enc, path=cd.COLL_PATH_FUSED)
+    assert a.plan()["dependent_launch"] == 1 and b.plan()["dependent_launch"] == 1
+    masks = [0x0011 * (r + 1) & 0x007F for r in range(n)]
+    mask_d = [torch.tensor(m, dtype=torch.int16, device="cuda") for m in masks]
+    xs, ins, o1 = buffers(a, n, seed=31, dist="uniform1")
+    o2 = [empty_dev(count) for _ in range(n)]
+    o3 = [empty_dev(count) for _ in range(n)]
+    x4 = [empty_dev(count) for _ in range(n)]
+    o5 = [empty_dev(count) for _ in range(n)]
+
+    def chain(s):
+        a.run(ins, o1, stream=s)
+        b.run(o1, o2, stream=s)
+        a.run(o2, o3, stream=s)
+        with torch.cuda.stream(s):
+            for r in range(n):
+                torch.bitwise_xor(o3[r], mask_d[r], out=x4[r])
+        b.run(x4, o5, stream=s)
+
+    def expect(xs):
+        y1 = oracle.allreduce(xs)
+        y2 = oracle.allreduce(y1)
+        y3 = oracle.allreduce(y2)
+        y4 = [y3[r] ^ np.uint16(masks[r]) for r in range(n)]
+        return y3, oracle.allreduce(y4)
+
+    s = torch.cuda.Stream()
+    torch.cuda.synchronize()
+    chain(s)
+    s.synchronize()
+    y3, y5 = expect(xs)
+    check(a, o3, y3, n)
+    check(b, o5, y5, n)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        chain(s)
+    for rep in range(3):
+        xs = [synth.uniform_bf16(40 + rep, count, -1.0, 1.0, r) for r in range(n)]
+        for r in range(n):
+            ins[r].copy_(to_dev(xs[r]))
+        torch.cuda.synchronize()
+        g.replay()
+        torch.cuda.synchronize()
+        y3, y5 = expect(xs)
+        check(a, o3, y3, n)
+        check(b, o5, y5, n)
