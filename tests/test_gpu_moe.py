@@ -54,6 +54,11 @@ def counts_of(cd, coll, n, experts):
     (3, 50, 120, 4, 9, True),
     (8, 33, 960, 8, 512, False),
     (1, 17, 64, 2, 2, False),
+    # more than 32 choices per token (a copy warp's second register of rows)
+    (4, 70, 256, 40, 64, False),
+    (8, 40, 480, 64, 64, False),
+    # 32 local experts per rank: a token's 20 choices often all on one rank
+    (2, 90, 120, 20, 64, True),
 ])
 def test_moe_dispatch_small_cases_match_the_oracle(cd, n, tokens, hidden, k, experts, staged,
                                                    path):
