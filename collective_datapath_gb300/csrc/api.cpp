@@ -223,16 +223,19 @@ cudaError_t launch_phase(const Plan& p, const RunParams& P, int phase,
       all_copy = all_copy && it.kind == IK_COPY && !(it.flags & IF_PUBLISH);
     }
     if (all_fold && phase == 1)
-      return launch_fold(P, std::min<int>((int)items.size(), device_sms() * 2), st);
+      return launch_fold(P, std::min<int>((int)items.size(), device_sms() * 2), st,
+                         p.dependent_launch);
     if (all_copy)
-      return launch_copy(P, phase, std::min<int>((int)items.size(), device_sms() * 4), st);
+      return launch_copy(P, phase, std::min<int>((int)items.size(), device_sms() * 4), st,
+                         p.dependent_launch);
   }
-  return launch_consume(P, phase, p.consume_grid, st);
+  return launch_consume(P, phase, p.consume_grid, st, p.dependent_launch);
 }
 
 cudaError_t launch_stager(const Plan& p, const RunParams& P, int items, cudaStream_t st) {
-  if (p.enc == ENC_LL128) return launch_stage_pipe(P, std::min(items, device_sms() * 4), st);
-  return launch_stage(P, std::min(items, device_sms() * 8), st);
+  if (p.enc == ENC_LL128)
+    return launch_stage_pipe(P, std::min(items, device_sms() * 4), st, p.dependent_launch);
+  return launch_stage(P, std::min(items, device_sms() * 8), st, p.dependent_launch);
 }
 
 // Consume phase(s) of a run whose inputs are staged; the last launch

@@ -691,13 +691,19 @@ int derive(const DeriveInput& in, Plan& p) {
   p.AG.base = off;
   off += (uint64_t)p.slots * p.AG.slot_bytes;
   p.ws_bytes = off;
-  // One-launch runs up to 512 KiB per rank overlap their launch with the
-  // previous kernel's tail (8 ranks, warm, per op: 3.94 -> 3.59 us at 8 KiB,
-  // 10.78 -> 10.43 us at 512 KiB; 12.88 -> 13.75 us at 1 MiB, so not above).
+  // Dependent launches overlap each kernel's launch with the tail of the one
+  // before it.  8 ranks, warm, per op: one launch 3.94 -> 3.59 us at 8 KiB,
+  // 10.78 -> 10.43 us at 512 KiB, but 12.88 -> 13.75 us at 1 MiB; stream-
+  // ordered oneshot 5.37 -> 4.54 us at 8 KiB, 11.94 -> 11.31 us at 128 KiB,
+  // but 16.94 -> 18.54 us at 512 KiB and 75.8 -> 81.6 us for the twoshot at
+  // 4 MiB.  So: one-launch runs up to 512 KiB per rank (input or output),
+  // stream-ordered ones up to 128 KiB, the composed launch never.
   uint64_t largest = 0;
   for (int r = 0; r < n; ++r)
     largest = std::max(largest, std::max(p.in_elems[r], p.out_elems[r]));
-  p.dependent_launch = p.path == COLL_PATH_FUSED && largest * 2 <= 512 * 1024;
+  const uint64_t bytes = largest * 2;
+  p.dependent_launch = (p.path == COLL_PATH_FUSED && bytes <= 512 * 1024) ||
+                       (p.path == COLL_PATH_STREAMED && bytes <= 128 * 1024);
   return COLL_OK;
 }
 

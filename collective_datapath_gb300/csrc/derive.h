@@ -57,8 +57,9 @@ struct Plan {
   uint64_t timeout_ns;
   int slots = 2;      // staging slots per region
   int ctas_per_rank;  // fused path
-  // fused path: launched with programmatic stream serialization, so the
-  // run's CTAs are placed while the previous kernel in the stream finishes
+  // the run's kernels (fused, or stream-ordered) are launched with
+  // programmatic stream serialization, so each one's CTAs are placed while
+  // the kernel before it in the stream finishes
   bool dependent_launch = false;
   int consume_grid;   // streamed consume grid
   uint64_t in_elems[kMaxRanks], out_elems[kMaxRanks];

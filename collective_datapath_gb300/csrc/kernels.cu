@@ -661,26 +661,38 @@ int fused_capacity(int enc) {
 
 int block_threads() { return kThreads; }
 
-cudaError_t launch_stage(const RunParams& P, int grid, cudaStream_t s) {
-  if (grid <= 0) return cudaSuccess;
-  if (P.enc == ENC_LL8)
-    k_stage<ENC_LL8><<<grid, kThreads, 0, s>>>(P);
-  else if (P.enc == ENC_SENT)
-    k_stage<ENC_SENT><<<grid, kThreads, 0, s>>>(P);
-  else
-    k_stage<ENC_LL128><<<grid, kThreads, 0, s>>>(P);
-  return cudaGetLastError();
+// A launch of kThreads-thread CTAs; dependent: with programmatic stream
+// serialization (every kernel launched this way calls begin_run, which waits
+// for the previous kernel in the stream, before it touches any data).
+template <typename... KArgs, typename... Args>
+static cudaError_t launch_k(void (*kernel)(KArgs...), int grid, size_t smem, cudaStream_t s,
+                            bool dependent, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = dependent ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kernel, args...);
 }
 
-cudaError_t launch_consume(const RunParams& P, int phase, int grid, cudaStream_t s) {
+cudaError_t launch_stage(const RunParams& P, int grid, cudaStream_t s, bool dependent) {
+  if (grid <= 0) return cudaSuccess;
+  if (P.enc == ENC_LL8) return launch_k(k_stage<ENC_LL8>, grid, 0, s, dependent, P);
+  if (P.enc == ENC_SENT) return launch_k(k_stage<ENC_SENT>, grid, 0, s, dependent, P);
+  return launch_k(k_stage<ENC_LL128>, grid, 0, s, dependent, P);
+}
+
+cudaError_t launch_consume(const RunParams& P, int phase, int grid, cudaStream_t s,
+                           bool dependent) {
   if (grid <= 0) grid = 1;
-  if (P.enc == ENC_LL8)
-    k_consume<ENC_LL8><<<grid, kThreads, 0, s>>>(P, phase);
-  else if (P.enc == ENC_SENT)
-    k_consume<ENC_SENT><<<grid, kThreads, 0, s>>>(P, phase);
-  else
-    k_consume<ENC_LL128><<<grid, kThreads, 0, s>>>(P, phase);
-  return cudaGetLastError();
+  if (P.enc == ENC_LL8) return launch_k(k_consume<ENC_LL8>, grid, 0, s, dependent, P, phase);
+  if (P.enc == ENC_SENT) return launch_k(k_consume<ENC_SENT>, grid, 0, s, dependent, P, phase);
+  return launch_k(k_consume<ENC_LL128>, grid, 0, s, dependent, P, phase);
 }
 
 cudaError_t launch_fused(const RunParams& P, int grid, cudaStream_t s, bool dependent) {
@@ -701,31 +713,25 @@ cudaError_t launch_fused(const RunParams& P, int grid, cudaStream_t s, bool depe
   return cudaLaunchKernelEx(&cfg, k_fused<ENC_LL128>, P);
 }
 
-cudaError_t launch_fold(const RunParams& P, int grid, cudaStream_t s) {
+cudaError_t launch_fold(const RunParams& P, int grid, cudaStream_t s, bool dependent) {
   static size_t memo128[kMaxDevices], memo8[kMaxDevices];
   const size_t bytes = fold_smem_bytes(P.nranks);
   if (cudaError_t e = P.enc == ENC_LL8 ? raise_smem_limit(k_fold_ll8, bytes, memo8)
                                        : raise_smem_limit(k_fold_ll128, bytes, memo128))
     return e;
-  if (P.enc == ENC_LL8)
-    k_fold_ll8<<<grid, kThreads, bytes, s>>>(P);
-  else
-    k_fold_ll128<<<grid, kThreads, bytes, s>>>(P);
-  return cudaGetLastError();
+  if (P.enc == ENC_LL8) return launch_k(k_fold_ll8, grid, bytes, s, dependent, P);
+  return launch_k(k_fold_ll128, grid, bytes, s, dependent, P);
 }
 
-cudaError_t launch_copy(const RunParams& P, int phase, int grid, cudaStream_t s) {
+cudaError_t launch_copy(const RunParams& P, int phase, int grid, cudaStream_t s, bool dependent) {
   if (P.enc == ENC_LL8)
-    k_copy_ll8<<<grid, kThreads, copy_smem_bytes(), s>>>(P, phase);
-  else
-    k_copy_ll128<<<grid, kThreads, copy_smem_bytes(), s>>>(P, phase);
-  return cudaGetLastError();
+    return launch_k(k_copy_ll8, grid, copy_smem_bytes(), s, dependent, P, phase);
+  return launch_k(k_copy_ll128, grid, copy_smem_bytes(), s, dependent, P, phase);
 }
 
-cudaError_t launch_stage_pipe(const RunParams& P, int grid, cudaStream_t s) {
+cudaError_t launch_stage_pipe(const RunParams& P, int grid, cudaStream_t s, bool dependent) {
   if (grid <= 0) return cudaSuccess;
-  k_stage_ll128<<<grid, kThreads, copy_smem_bytes(), s>>>(P);
-  return cudaGetLastError();
+  return launch_k(k_stage_ll128, grid, copy_smem_bytes(), s, dependent, P);
 }
 
 cudaError_t launch_withhold(const RunParams& P, cudaStream_t s) {

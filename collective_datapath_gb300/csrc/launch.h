@@ -31,18 +31,21 @@ int block_threads();
 // Co-resident CTAs of the fused kernel on this device (0 if unknown).
 int fused_capacity(int enc);
 
-cudaError_t launch_stage(const RunParams& P, int grid, cudaStream_t s);
-cudaError_t launch_consume(const RunParams& P, int phase, int grid, cudaStream_t s);
+// dependent (here and below): programmatic stream serialization, as for
+// launch_fused.
+cudaError_t launch_stage(const RunParams& P, int grid, cudaStream_t s, bool dependent);
+cudaError_t launch_consume(const RunParams& P, int phase, int grid, cudaStream_t s,
+                           bool dependent);
 // dependent: programmatic stream serialization (the kernel's CTAs may be
 // placed before the previous kernel in the stream completes; begin_run waits
 // for it before touching any data).
 cudaError_t launch_fused(const RunParams& P, int grid, cudaStream_t s, bool dependent);
 // LL128 phase-1 folds through the shared-memory pipeline (all items IK_REDUCE).
-cudaError_t launch_fold(const RunParams& P, int grid, cudaStream_t s);
+cudaError_t launch_fold(const RunParams& P, int grid, cudaStream_t s, bool dependent);
 // LL128 copy phases (all items IK_COPY, plain outputs) and LL128 staging
 // through cp.async shared-memory rings.
-cudaError_t launch_copy(const RunParams& P, int phase, int grid, cudaStream_t s);
-cudaError_t launch_stage_pipe(const RunParams& P, int grid, cudaStream_t s);
+cudaError_t launch_copy(const RunParams& P, int phase, int grid, cudaStream_t s, bool dependent);
+cudaError_t launch_stage_pipe(const RunParams& P, int grid, cudaStream_t s, bool dependent);
 cudaError_t launch_withhold(const RunParams& P, cudaStream_t s);
 // Composed twoshot all-reduce: co-resident CTAs of the persistent kernel, and
 // the launch (P.cp filled in).

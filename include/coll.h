@@ -160,7 +160,8 @@ enum { COLL_RESET_FUSED = 0, COLL_RESET_KERNEL = 1, COLL_RESET_NONE = 2,
  * workspace or any input (griddepcontrol.wait).  Each of the library's
  * kernels allows the next dependent launch to be placed once it has read
  * the epoch; a caller's kernel launched that way must wait the same way
- * before it reads the outputs.  STREAMED =
+ * before it reads the outputs.  STREAMED (dependent launches, the same way,
+ * up to 128 KiB per rank) =
  * separate stage and consume kernels ordered by the stream; COMPOSED
  * (LL128 only: the twoshot all-reduce, reduce-scatter, all-to-all and
  * all-gather; AUTO never takes it for the all-gather, whose stream-ordered
@@ -367,9 +368,9 @@ coll_status_t coll_debug_items(const coll_spec_t *spec, int which, int64_t *buf,
 /* Summary of the derived plan: all-reduce algorithm (COLL_ONESHOT /
  * COLL_TWOSHOT, 0 for other collectives), launch path used when inputs are
  * given to coll_run (COLL_PATH_*), CTAs per rank of the fused path, the
- * encoding, and whether the fused launch is a dependent launch (1: launched
- * with programmatic stream serialization; see COLL_PATH_FUSED).  Any output
- * pointer may be NULL. */
+ * encoding, and whether the run's kernels are dependent launches (1:
+ * launched with programmatic stream serialization; see COLL_PATH_FUSED and
+ * COLL_PATH_STREAMED).  Any output pointer may be NULL. */
 coll_status_t coll_debug_plan(const coll_spec_t *spec, int *algorithm, int *path,
                               int *ctas_per_rank, int *encoding, int *dependent_launch);
 

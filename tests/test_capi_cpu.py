@@ -447,9 +447,10 @@ def test_fused_phases_fill_whole_rounds(cd, T):
 
 
 def test_dependent_launch_rule(cd):
-    """One-launch (fused) runs up to 512 KiB per rank, input or output, are
-    dependent launches; larger ones, and every other path, are not.  Plan
-    only (host)."""
+    """A run's kernels are dependent launches when it is one-launch (fused)
+    up to 512 KiB per rank, input or output, or stream-ordered up to
+    128 KiB; larger runs and the composed launch are not.  Plan only
+    (host)."""
     def dep(triple, n, count, **kw):
         s = cd.coll_spec_create(*triple, n, count, **kw)
         try:
@@ -461,7 +462,12 @@ def test_dependent_launch_rule(cd):
     assert dep(cd.ALLREDUCE, 8, 4096, **fused) == 1                 # 8 KiB per rank
     assert dep(cd.ALLREDUCE, 8, 256 * 1024, **fused) == 1           # 512 KiB
     assert dep(cd.ALLREDUCE, 8, 256 * 1024 + 8, **fused) == 0
-    assert dep(cd.ALLREDUCE, 8, 4096, encoding=cd.COLL_LL8, path=cd.COLL_PATH_STREAMED) == 0
+    streamed = dict(encoding=cd.COLL_LL128, path=cd.COLL_PATH_STREAMED)
+    assert dep(cd.ALLREDUCE, 8, 4096, **streamed) == 1
+    assert dep(cd.ALLREDUCE, 8, 64 * 1024, **streamed) == 1          # 128 KiB
+    assert dep(cd.ALLREDUCE, 8, 64 * 1024 + 8, **streamed) == 0
+    assert dep(cd.ALLREDUCE, 8, 8 * 60 * 1024, encoding=cd.COLL_LL128,
+               algorithm=cd.COLL_TWOSHOT, path=cd.COLL_PATH_COMPOSED) == 0
     assert dep(cd.ALLREDUCE, 8, 4096, encoding=cd.COLL_ENC_AUTO) == 1   # policy: fused
     # all-gather: 64 KiB in, 512 KiB out per rank; twice that is past the bound
     assert dep(cd.ALLGATHER, 8, 8 * 32 * 1024, **fused) == 1

@@ -358,18 +358,19 @@ def test_composed_reduce_scatter_and_all_to_all(cd, name, n, count, shape, monke
         assert coll.epoch() == e + 1
 
 
-@pytest.mark.parametrize("enc", [0, 2])
-def test_dependent_launches_chain(cd, enc):
-    """Fused runs are dependent launches: each must wait for the kernel
-    before it and see all of its writes.  Chain A -> B -> A, each run's
+@pytest.mark.parametrize("enc,path", [(0, 1), (2, 1), (0, 2), (1, 2)])
+def test_dependent_launches_chain(cd, enc, path):
+    """Small runs are dependent launches (one launch, or stream-ordered
+    kernels): each kernel must wait for the kernel before it and see all of
+    its writes.  Chain A -> B -> A, each run's
     inputs being the previous run's outputs, then a plain torch kernel
     (an XOR of low mantissa bits) between two runs; eagerly and replayed
     from a CUDA graph, bit-exact against the oracle applied step by step."""
     import torch
 
     n, count = 8, 4096
-    a = make(cd, cd.ALLREDUCE, n, count, encoding=enc, path=cd.COLL_PATH_FUSED)
-    b = make(cd, cd.ALLREDUCE, n, count, encoding=enc, path=cd.COLL_PATH_FUSED)
+    a = make(cd, cd.ALLREDUCE, n, count, encoding=enc, path=path)
+    b = make(cd, cd.ALLREDUCE, n, count, encoding=enc, path=path)
     assert a.plan()["dependent_launch"] == 1 and b.plan()["dependent_launch"] == 1
     masks = [0x0011 * (r + 1) & 0x007F for r in range(n)]
     mask_d = [torch.tensor(m, dtype=torch.int16, device="cuda") for m in masks]
