@@ -690,6 +690,48 @@ def sentinel_row(cd, count, stream, steps=5) -> dict:
             "rearm_bytes": (n + 1) * s, "status": st}
 
 
+def hbm_reference_row(stream, reps=10) -> dict:
+    """Reference DRAM rates of plain torch kernels (not the library), for
+    reading the write-heavy rows: a 2 GiB fill (writes only), a 2 GiB copy
+    (half reads, half writes, like the measured copy peak) and eight copies
+    fanning 256 MiB out into 2 GiB (the all-gather's traffic shape).  Every
+    buffer is larger than L2; CUDA events on the timing stream."""
+    import torch
+
+    nb = 2 << 30
+    a = torch.empty(nb, dtype=torch.uint8, device="cuda")
+    b = torch.empty(nb, dtype=torch.uint8, device="cuda")
+    src = torch.empty(nb // 8, dtype=torch.uint8, device="cuda")
+
+    def timed(fn):
+        with torch.cuda.stream(stream):
+            fn()
+            stream.synchronize()
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for _ in range(reps):
+                fn()
+            e1.record(stream)
+            stream.synchronize()
+        return e0.elapsed_time(e1) / reps
+
+    def fan():
+        for k in range(8):
+            a[k * (nb // 8):(k + 1) * (nb // 8)].copy_(src)
+
+    fill_ms = timed(lambda: a.fill_(1))
+    copy_ms = timed(lambda: b.copy_(a))
+    fan_ms = timed(fan)
+    del a, b, src
+    torch.cuda.empty_cache()
+    return {"fill_2GiB": {"ms": round(fill_ms, 4), "written_GB/s": round(nb / fill_ms / 1e6, 1)},
+            "copy_2GiB": {"ms": round(copy_ms, 4), "read+written_GB/s": round(2 * nb / copy_ms / 1e6, 1)},
+            "fan_out_256MiB_x8": {"ms": round(fan_ms, 4), "written_GB/s": round(nb / fan_ms / 1e6, 1)},
+            "note": "torch kernels, not the library: the write side's ceiling for reading "
+                    "write-heavy rows (all-gather, MoE dispatch)"}
+
+
 def moe_row(cd, stream, steps=5, path=None, tokens=4096) -> dict:
     """MoE dispatch: 8 ranks x `tokens` tokens x 7168 bf16, top-8 of 256
     experts (routing drawn on the device from a seeded generator)."""
@@ -783,7 +825,7 @@ def main() -> int:
     ap.add_argument("--row", default=None,
                     help="run one extra row alone and print it (profiling runs): "
                          "moe, moe_streamed, rs, rs_composed, ag, a2a, a2a_composed, "
-                         "sentinel, f32, staging16, sizes, rsv, agv, a2av")
+                         "sentinel, f32, staging16, sizes, rsv, agv, a2av, hbm_reference")
     ap.add_argument("--staging-mib", type=int, default=16,
                     help="staging MiB per rank of the bounded-staging row run alone")
     ap.add_argument("--moe-tokens", type=int, default=4096,
@@ -846,6 +888,7 @@ def main() -> int:
             "rsv": lambda: v_row(cd, "REDUCE_SCATTER_V", args.mib << 20, stream),
             "agv": lambda: v_row(cd, "ALLGATHER_V", args.mib << 20, stream),
             "a2av": lambda: v_row(cd, "ALLTOALL_V", args.mib << 20, stream),
+            "hbm_reference": lambda: hbm_reference_row(stream),
         }
         if args.row not in rows:
             raise SystemExit(f"unknown row {args.row}")
@@ -1006,6 +1049,7 @@ def main() -> int:
             "allreduce_256MiB_composed_staging_16MiB": bounded_staging_row(cd, count, stream),
             "bandwidth_regime_32_128MiB": sizes_row(cd, stream),
             "pipeline_depth_ablation_256MiB": atom_ablation(cd, stream),
+            "hbm_reference_torch": hbm_reference_row(stream),
         }
         line["latency_us_per_op"] = latency_sweep(cd, stream)
         if world == 1:
