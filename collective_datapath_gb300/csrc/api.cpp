@@ -161,7 +161,8 @@ ComposedParams composed_shape(const coll_spec* s) {
   int chunk = ar ? 256 : 128, lag = ar ? 28 : 40, discard = 1, variant = 0, lag2 = -1;
   uint64_t most = 0;
   for (const Seg& sg : p.pseg[0]) most = std::max<uint64_t>(most, sg.lines);
-  if (const char* env = std::getenv("COLL_COMPOSED_SHAPE")) {
+  const char* env = std::getenv("COLL_COMPOSED_SHAPE");
+  if (env != nullptr) {
     std::sscanf(env, "%d,%d,%d,%d,%d", &chunk, &lag, &discard, &variant, &lag2);
   } else if (ar) {
     // The queue fills and drains over 2 * lag steps; the chunk is the largest
@@ -181,19 +182,29 @@ ComposedParams composed_shape(const coll_spec* s) {
   q.lag2 = lag2 < 1 ? q.lag : lag2;
   // Bounded staging (Purlin §4.1): chunk c uses chunk slot c mod W of the
   // staging images.  A stage waits for the folds (copies) that read the
-  // slot's previous chunk and a fold for the gathers of its published slot,
-  // so both lags stay below W: every task then waits only for tasks earlier
-  // in the queue.  The chunk shrinks (to no less than kComposedMinChunk)
-  // until the images hold two slots.
+  // slot's previous chunk, W - lag queue steps back, and a fold for the
+  // gathers of its published slot's previous chunk, W - lag2 steps back.
+  // Both lags are at most W / 2: every task then waits only for earlier
+  // tasks, and no wait is on a task just a few steps back (with lags near W
+  // the queue advances one dependent task at a time; 8 x 256 MiB with W = 32
+  // and lags of 28 took 5.0 ms).  The chunk shrinks (to no less than
+  // kComposedMinChunk) until the images hold two slots.
   q.ring = 0;
   if (p.ring_lines > 0) {
     while (q.chunk_lines > kComposedMinChunk &&
            p.ring_lines / ((uint64_t)p.n * q.chunk_lines) < 2)
       q.chunk_lines /= 2;
+    // By default the chunk also halves, down to 64 lines, until the images
+    // hold 64 chunk slots: longer waits back in the queue pay more than the
+    // per-chunk cost (8 x 256 MiB, 4 MiB of staging per rank: 2.92 ms at 256
+    // lines, 2.06 at 128, 1.95 at 64; 8 MiB: 1.81, 1.53 and 1.95 ms)
+    while (env == nullptr && q.chunk_lines > 64 && q.chunk_lines / 2 >= kComposedMinChunk &&
+           p.ring_lines / ((uint64_t)p.n * q.chunk_lines) < 64)
+      q.chunk_lines /= 2;
     q.nchunks = (uint32_t)std::max<uint64_t>(1, (max_lines + q.chunk_lines - 1) / q.chunk_lines);
     q.ring = (uint32_t)(p.ring_lines / ((uint64_t)p.n * q.chunk_lines));
-    q.lag = std::min(q.lag, (int)q.ring - 1);
-    q.lag2 = std::min(q.lag2, (int)q.ring - 1);
+    q.lag = std::min(q.lag, std::max(1, (int)q.ring / 2));
+    q.lag2 = std::min(q.lag2, std::max(1, (int)q.ring / 2));
   }
   q.discard = discard;
   q.variant = variant >= 0 && variant <= 2 ? variant : 0;

@@ -132,7 +132,7 @@ def test_bandwidth_reduce_scatter_and_all_gather(cd, inputs, mib):
     torch.cuda.empty_cache()
 
 
-@pytest.mark.parametrize("mib,staging_mib", [(32, 0), (256, 0), (256, 8)])
+@pytest.mark.parametrize("mib,staging_mib", [(32, 0), (256, 0), (256, 8), (256, 4)])
 def test_bandwidth_allreduce_composed_twoshot(cd, inputs, mib, staging_mib):
     """The one-launch twoshot at full size: sampled against the oracle, and
     byte-identical to the stream-ordered twoshot on every element; also with
