@@ -300,17 +300,20 @@ def timed(step, k: int, w: int, stream, world: int) -> float:
 
 def latency_sweep(cd, stream, only_T=None, only_variant=None, encoding=None) -> dict:
     """8 ranks x [T x 4096] bf16, LL8 (config of the decode-time sweep), or
-    another readiness encoding."""
+    another readiness encoding; ahead of it 1, 2 and 4 KiB per rank, the
+    low end of the all-reduce latency metric (1 KB - 1 MB).  A given T
+    (--sweep-T) runs that size alone."""
     import torch
 
     enc = cd.COLL_LL8 if encoding is None else encoding
 
     out = {}
     flush = torch.empty(int(2 * L2_BYTES), dtype=torch.uint8, device="cuda")
-    for T in (1, 2, 4, 8, 16, 32, 64, 128):
-        if only_T is not None and T != only_T:
+    sizes = [(f"{kib}KiB", kib * 512, 3 + kib) for kib in (1, 2, 4)]
+    sizes += [(f"T={T}", T * 4096, 7 + T) for T in (1, 2, 4, 8, 16, 32, 64, 128)]
+    for key, count, seed in sizes:
+        if only_T is not None and key != f"T={only_T}":
             continue
-        count = T * 4096
         row = {}
         for algo, path, name in ((cd.COLL_ONESHOT, cd.COLL_PATH_FUSED, "oneshot_fused"),
                                  (cd.COLL_ONESHOT, cd.COLL_PATH_STREAMED, "oneshot_streamed"),
@@ -323,7 +326,7 @@ def latency_sweep(cd, stream, only_T=None, only_variant=None, encoding=None) -> 
             coll = cd.Collective(cd.ALLREDUCE, N_RANKS, count,
                                  encoding=cd.COLL_ENC_AUTO if name == "policy" else enc,
                                  algorithm=algo, path=path)
-            ins = make_inputs(count, 7 + T)
+            ins = make_inputs(count, seed)
             outs = [torch.empty(count, dtype=torch.int16, device="cuda")
                     for _ in range(N_RANKS)]
             with torch.cuda.stream(stream):
@@ -370,7 +373,7 @@ def latency_sweep(cd, stream, only_T=None, only_variant=None, encoding=None) -> 
                                        "path": pl["path"]}
             coll.close()
             del coll, ins, outs, g
-        out[f"T={T}"] = {"bytes_per_rank": count * 2, **row}
+        out[key] = {"bytes_per_rank": count * 2, **row}
     del flush
     torch.cuda.empty_cache()
     return out
