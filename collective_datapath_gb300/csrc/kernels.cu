@@ -448,6 +448,68 @@ __global__ void __launch_bounds__(kThreads, 4) k_copy_ll8(RunParams P, int phase
   finish_run(P, e);
 }
 
+// Validated copy of sentinel packs (deferred re-arm: a copy item re-arms
+// nothing).  The ring of k_copy_ll8: each warp row is 32 groups of two packs
+// (512 bytes), a lane's group arrives through a cp.async stage; a group that
+// still holds the all-ones pattern is polled (bounded) and reloaded, and the
+// 8 elements are stored as they are.
+__global__ void __launch_bounds__(kThreads, 4) k_copy_sent(RunParams P, int phase) {
+  extern __shared__ __align__(128) char smem[];
+  const uint64_t e = begin_run(P);
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
+  const Item* items = phase == 1 ? P.items1 : P.items2;
+  const int* beg = phase == 1 ? P.beg1 : P.beg2;
+  const bool inter = phase == 1 ? P.interleave1 : P.interleave2;
+  const Region& R = phase == 1 ? P.P : P.AG;
+  const int n_items = beg[P.nranks];
+  const uint32_t wbase = (uint32_t)__cvta_generic_to_shared(smem) +
+                         (uint32_t)(warp * kCopyStages * kRowBytes + 16 * lane);
+  for (int v = blockIdx.x; v < n_items; v += gridDim.x) {
+    if (aborted(P.ws)) break;
+    const int i = inter ? beg[v % P.nranks] + v / P.nranks : v;
+    const Item it = items[i];
+    const uint64_t* src = reinterpret_cast<const uint64_t*>(
+                              P.ws + R.base + (e & R.slot_mask) * R.slot_bytes +
+                              (uint64_t)it.src * R.rank_bytes) +
+                          it.src_line;
+    const uint32_t ngroups = it.nlines / kSentGroupLines;
+    const uint32_t nrows = (ngroups + 31) / 32;
+    const int nj = (uint32_t)warp < nrows ? (int)((nrows - warp + nwarps - 1) / nwarps) : 0;
+    auto issue = [&](int j) {
+      if (j < nj) {
+        const uint32_t g = (warp + j * nwarps) * 32 + lane;
+        cp_async16(wbase + (j % kCopyStages) * kRowBytes, src + 2 * (size_t)g, g < ngroups);
+      }
+      cp_async_commit();
+    };
+#pragma unroll
+    for (int j = 0; j < kCopyStages; ++j) issue(j);
+    bool ok = true;
+    for (int j = 0; j < nj; ++j) {
+      cp_async_wait<kCopyStages - 1>();
+      uint4 s = lds_v4(wbase + (j % kCopyStages) * kRowBytes);
+      issue(j + kCopyStages);
+      const uint32_t g = (warp + j * nwarps) * 32 + lane;
+      if (g < ngroups) {
+        const uint64_t a = (uint64_t)s.x | ((uint64_t)s.y << 32);
+        const uint64_t b = (uint64_t)s.z | ((uint64_t)s.w << 32);
+        if (a == kSentPack || b == kSentPack) {
+          const uint64_t* q = src + 2 * (size_t)g;
+          ok = sent_wait_pair(P, q, it.src, (int64_t)(it.src_line + 2 * (uint64_t)g));
+          uint64_t a2, b2;
+          ld_relaxed_v2u64(q, a2, b2);
+          s = make_uint4((uint32_t)a2, (uint32_t)(a2 >> 32), (uint32_t)b2, (uint32_t)(b2 >> 32));
+        }
+        if (ok) st_v4(P.out[it.dst] + it.out_off + 8 * (uint64_t)g, s);
+      }
+      if (!__all_sync(0xFFFFFFFFu, ok)) break;
+    }
+    cp_async_wait<0>();
+    if (!ok) break;
+  }
+  finish_run(P, e);
+}
+
 // Late producer: publish rank p's withheld lines in the given order, after
 // every consumer CTA has started polling.  One warp publishes, in order.
 template <int ENC>
@@ -726,6 +788,8 @@ cudaError_t launch_fold(const RunParams& P, int grid, cudaStream_t s, bool depen
 cudaError_t launch_copy(const RunParams& P, int phase, int grid, cudaStream_t s, bool dependent) {
   if (P.enc == ENC_LL8)
     return launch_k(k_copy_ll8, grid, copy_smem_bytes(), s, dependent, P, phase);
+  if (P.enc == ENC_SENT)
+    return launch_k(k_copy_sent, grid, copy_smem_bytes(), s, dependent, P, phase);
   return launch_k(k_copy_ll128, grid, copy_smem_bytes(), s, dependent, P, phase);
 }
 

@@ -233,6 +233,31 @@ def test_unpublished_pack_times_out_with_status(cd):
     check(cd, coll, outs, oracle.allreduce(xs), n)
 
 
+def test_unpublished_pack_in_a_copy_phase_times_out_with_status(cd):
+    """A stream-ordered all-gather copies packs through the pipelined
+    sentinel copy: a pack that rank 1 never publishes ends the wait at the
+    bound with COLL_ERR_TIMEOUT naming rank 1, and the next epoch works."""
+    import torch
+
+    n, count = 4, 4 * 480
+    coll = cd.Collective(cd.ALLGATHER, n, count, encoding=SENT, path=cd.COLL_PATH_STREAMED,
+                         timeout_ns=2_000_000)
+    xs, ins, outs = buffers(coll, n, seed=29)
+    lines = torch.tensor([5], dtype=torch.int64, device="cuda")
+    kind = torch.tensor([0], dtype=torch.int32, device="cuda")
+    poison = torch.tensor([0], dtype=torch.int16, device="cuda")
+    for r in range(n):
+        if r == 1:
+            cd.coll_stage_withheld(coll.spec, r, ins[r], lines, kind, poison)
+        else:
+            coll.stage(r, ins[r])
+    coll.run(None, outs)
+    code, rank, line = coll.status()
+    assert code == cd.COLL_ERR_TIMEOUT and rank == 1 and line >= 0
+    coll.run(ins, outs)                                  # the next epoch works
+    check(cd, coll, outs, oracle.all_gather(xs, count), n)
+
+
 def real_lines(cd, coll, n_seg):
     base, _, lb = cd.coll_staging_layout(coll.spec, 0, 0, 0, 0)
     out = []
