@@ -219,8 +219,8 @@ ComposedParams composed_shape(const coll_spec* s) {
   return q;
 }
 
-// One stream-ordered consume phase: phases made only of folds (LL128, LL8)
-// or only of plain-output copies (every encoding) run through the
+// One stream-ordered consume phase: phases made only of folds or only of
+// plain-output copies run through the
 // shared-memory pipelines, when no item re-arms what it read (LL128 lines,
 // or the deferred re-arm); anything else through the generic consume kernel.
 cudaError_t launch_phase(const Plan& p, const RunParams& P, int phase,
@@ -235,7 +235,7 @@ cudaError_t launch_phase(const Plan& p, const RunParams& P, int phase,
       all_fold = all_fold && it.kind == IK_REDUCE;
       all_copy = all_copy && it.kind == IK_COPY && !(it.flags & IF_PUBLISH);
     }
-    if (all_fold && phase == 1 && p.enc != ENC_SENT)
+    if (all_fold && phase == 1)
       return launch_fold(P, std::min<int>((int)items.size(), device_sms() * 2), st,
                          p.dependent_launch);
     if (all_copy)

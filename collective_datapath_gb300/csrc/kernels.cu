@@ -448,6 +448,91 @@ __global__ void __launch_bounds__(kThreads, 4) k_copy_ll8(RunParams P, int phase
   finish_run(P, e);
 }
 
+// Fold of sentinel packs (deferred re-arm: the fold re-arms only the other
+// slot of what it publishes).  The ring of k_fold_ll8: each lane takes a
+// pair of packs (8 elements) of every rank's image per warp row of 64 packs;
+// a pair that still holds the all-ones pattern is polled (bounded) and
+// reloaded; sent_fold8 folds them in rank order.
+__global__ void __launch_bounds__(kThreads, 2) k_fold_sent(RunParams P) {
+  extern __shared__ __align__(128) char smem[];
+  const uint64_t e = begin_run(P);
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
+  const int n = P.nranks;
+  const uint32_t wbase = (uint32_t)__cvta_generic_to_shared(smem) +
+                         (uint32_t)(warp * kFoldStages * n * kRowBytes + 16 * lane);
+  const int n_items = P.beg1[P.nranks];
+  const char* img = P.ws + P.P.base + (e & P.P.slot_mask) * P.P.slot_bytes;
+  for (int v = blockIdx.x; v < n_items; v += gridDim.x) {
+    if (aborted(P.ws)) break;
+    const int i = P.interleave1 ? P.beg1[v % P.nranks] + v / P.nranks : v;
+    const Item it = P.items1[i];
+    const bool publish = (it.flags & IF_PUBLISH) != 0;
+    const uint32_t ngroups = it.nlines / kSentGroupLines;
+    const uint32_t nrows = (ngroups + 31) / 32;
+    const int nj = (uint32_t)warp < nrows ? (int)((nrows - warp + nwarps - 1) / nwarps) : 0;
+    auto issue = [&](int j) {
+      if (j < nj) {
+        const uint32_t g = (warp + j * nwarps) * 32 + lane;
+        const uint64_t off = (it.src_line + 2 * (uint64_t)g) * kSentLineBytes;
+        const uint32_t slot = wbase + (uint32_t)((j % kFoldStages) * n * kRowBytes);
+        for (int p = 0; p < n; ++p)
+          cp_async16(slot + p * kRowBytes, img + (uint64_t)p * P.P.rank_bytes + off, g < ngroups);
+      }
+      cp_async_commit();
+    };
+#pragma unroll
+    for (int j = 0; j < kFoldStages; ++j) issue(j);
+    bool ok = true;
+    for (int j = 0; j < nj; ++j) {
+      cp_async_wait<kFoldStages - 1>();
+      const uint32_t slot = wbase + (uint32_t)((j % kFoldStages) * n * kRowBytes);
+      uint64_t lo[kMaxRanks], hi[kMaxRanks];
+#pragma unroll
+      for (int p = 0; p < kMaxRanks; ++p)
+        if (p < n) {
+          const uint4 w = lds_v4(slot + p * kRowBytes);
+          lo[p] = (uint64_t)w.x | ((uint64_t)w.y << 32);
+          hi[p] = (uint64_t)w.z | ((uint64_t)w.w << 32);
+        }
+      issue(j + kFoldStages);
+      const uint32_t g = (warp + j * nwarps) * 32 + lane;
+      const uint64_t line = it.src_line + 2 * (uint64_t)g;
+      if (g < ngroups) {
+#pragma unroll
+        for (int p = 0; p < kMaxRanks; ++p)
+          if (p < n && ok && (lo[p] == kSentPack || hi[p] == kSentPack)) {
+            const uint64_t* q =
+                reinterpret_cast<const uint64_t*>(img + (uint64_t)p * P.P.rank_bytes) + line;
+            ok = sent_wait_pair(P, q, p, (int64_t)line);
+            ld_relaxed_v2u64(q, lo[p], hi[p]);
+          }
+        if (ok) {
+          const uint4 res = sent_fold8(lo, hi, n, P.dtype);
+          if (publish) {
+            uint64_t* dst = reinterpret_cast<uint64_t*>(P.ws + P.AG.base +
+                                                        (e & P.AG.slot_mask) * P.AG.slot_bytes +
+                                                        (uint64_t)it.dst * P.AG.rank_bytes) +
+                            it.out_off + 2 * (uint64_t)g;
+            st_relaxed_v2u64(dst, (uint64_t)res.x | ((uint64_t)res.y << 32),
+                             (uint64_t)res.z | ((uint64_t)res.w << 32));
+            uint64_t* other = reinterpret_cast<uint64_t*>(
+                                  P.ws + P.AG.base + ((e + 1) & P.AG.slot_mask) * P.AG.slot_bytes +
+                                  (uint64_t)it.dst * P.AG.rank_bytes) +
+                              it.out_off + 2 * (uint64_t)g;
+            sent_rearm(other);
+          } else {
+            st_v4(P.out[it.dst] + it.out_off + 8 * (uint64_t)g, res);
+          }
+        }
+      }
+      if (!__all_sync(0xFFFFFFFFu, ok)) break;
+    }
+    cp_async_wait<0>();
+    if (!ok) break;
+  }
+  finish_run(P, e);
+}
+
 // Validated copy of sentinel packs (deferred re-arm: a copy item re-arms
 // nothing).  The ring of k_copy_ll8: each warp row is 32 groups of two packs
 // (512 bytes), a lane's group arrives through a cp.async stage; a group that
@@ -776,12 +861,14 @@ cudaError_t launch_fused(const RunParams& P, int grid, cudaStream_t s, bool depe
 }
 
 cudaError_t launch_fold(const RunParams& P, int grid, cudaStream_t s, bool dependent) {
-  static size_t memo128[kMaxDevices], memo8[kMaxDevices];
+  static size_t memo128[kMaxDevices], memo8[kMaxDevices], memo_sent[kMaxDevices];
   const size_t bytes = fold_smem_bytes(P.nranks);
-  if (cudaError_t e = P.enc == ENC_LL8 ? raise_smem_limit(k_fold_ll8, bytes, memo8)
-                                       : raise_smem_limit(k_fold_ll128, bytes, memo128))
+  if (cudaError_t e = P.enc == ENC_LL8    ? raise_smem_limit(k_fold_ll8, bytes, memo8)
+                      : P.enc == ENC_SENT ? raise_smem_limit(k_fold_sent, bytes, memo_sent)
+                                          : raise_smem_limit(k_fold_ll128, bytes, memo128))
     return e;
   if (P.enc == ENC_LL8) return launch_k(k_fold_ll8, grid, bytes, s, dependent, P);
+  if (P.enc == ENC_SENT) return launch_k(k_fold_sent, grid, bytes, s, dependent, P);
   return launch_k(k_fold_ll128, grid, bytes, s, dependent, P);
 }
 
