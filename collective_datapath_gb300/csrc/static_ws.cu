@@ -16,6 +16,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <cstddef>
 #include <mutex>
 
 #include "../../include/coll.h"
@@ -142,6 +143,18 @@ extern "C" coll_status_t coll_allreduce_static(int nranks, size_t count,
   P.P.slot_mask = 1;
   P.stage_rank = -1;
   P.advance_epoch = 1;
+
+  // A device-side timeout latches the status words and raises `abort` in
+  // the shared header, and an abort left standing would make every later
+  // call skip its fold.  So every call starts by clearing those words, in
+  // stream order ahead of its own launch; the status of an earlier call that
+  // timed out is dropped with them.
+  constexpr size_t kErrBegin = offsetof(WsHeader, status_code);
+  constexpr size_t kErrEnd = offsetof(WsHeader, abort) + sizeof(uint32_t);
+  static_assert(kErrEnd - kErrBegin == 20, "status code, rank, line and abort are contiguous");
+  if (cudaMemsetAsync(ds->ptr + kErrBegin, 0, kErrEnd - kErrBegin,
+                      reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return COLL_ERR_CUDA;
 
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(nranks * B);

@@ -384,6 +384,20 @@ coll_status_t coll_set_profile_events(coll_spec_t *spec, void *const *events, in
 /* Number of kernel launches the last coll_run issued. */
 coll_status_t coll_last_launches(const coll_spec_t *spec, int *launches);
 
+/* Launch floor, for measurement.  flash-comm (Appendix A, Table 8) calibrates
+ * an empty-kernel floor inside CUDA graphs, and its cost model (§3.2,
+ * Eq. (1)) carries a fixed per-operation term.  This enqueues one empty
+ * kernel on `stream` in exactly the launch configuration coll_run(spec, ins,
+ * outs) uses on the one-launch (fused) path: the same grid and block size,
+ * the cooperative attribute, and programmatic stream serialization when the
+ * spec's runs are dependent launches (the kernel then makes the same
+ * dependent-launch handshake as a run's prologue).  It reads and writes no
+ * memory and leaves the spec's device state (epoch, staging) untouched, so
+ * it may be timed between or instead of runs, eagerly or in a graph.
+ * Returns COLL_ERR_UNSUPPORTED for specs whose runs do not take the
+ * one-launch path, COLL_ERR_CUDA if the launch fails. */
+coll_status_t coll_launch_floor(coll_spec_t *spec, coll_stream_t stream);
+
 /* All-reduce without any allocation.  The pages have no counterpart: this is
  * an entry point for callers that cannot allocate device memory when they
  * need the collective -- code running under a stream capture that must not
@@ -405,8 +419,13 @@ coll_status_t coll_last_launches(const coll_spec_t *spec, int *launches);
  *   - every call on a device shares the one scratch array, which keeps the
  *     previous call's contents; calls that overlap on the GPU (other streams,
  *     other host threads) race and give undefined outputs;
- *   - a device-side wait that exceeds its bound (200 ms) leaves the outputs
- *     undefined; this entry point reports only host-side errors.
+ *   - a device-side wait that exceeds its bound (200 ms) leaves that call's
+ *     outputs undefined.  Such a timeout is not reported: this entry point
+ *     returns only host-side errors, and every call first clears the scratch's
+ *     status and abort words in stream order (a cudaMemsetAsync ahead of its
+ *     launch), so a timeout in one call never affects a later call, and its
+ *     status is dropped.  Callers that need device-side error reports use a
+ *     bound spec and coll_query_status.
  * It calls no cudaMalloc, cudaFree or other allocating routine. */
 coll_status_t coll_allreduce_static(int nranks, size_t count, const void *const *dev_ins,
                                     void *const *dev_outs, coll_stream_t stream);
