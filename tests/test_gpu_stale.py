@@ -41,7 +41,7 @@ def image_lines_of_real_lines(cd, coll, n_seg):
     return np.concatenate(out)
 
 
-@pytest.mark.parametrize("enc,algo,epochs", [(0, 1, 64), (1, 1, 64), (0, 2, 8), (1, 2, 8)])
+@pytest.mark.parametrize("enc,algo,epochs", [(0, 1, 64), (1, 1, 64), (0, 2, 64), (1, 2, 64)])
 def test_stale_lines_rejected_across_64_epochs(cd, enc, algo, epochs):
     import torch
 
