@@ -268,7 +268,7 @@ def real_lines(cd, coll, n_seg):
     return np.concatenate(out)
 
 
-@pytest.mark.parametrize("algo,epochs", [(1, 64), (2, 8)])
+@pytest.mark.parametrize("algo,epochs", [(1, 64), (2, 64)])
 def test_late_packs_rejected_until_published(cd, algo, epochs):
     """8 ranks x [16 x 7168] normal(0,1): each epoch a seeded 10 % of every
     rank's packs still hold the pattern when the consumers start and are
@@ -297,41 +297,3 @@ def test_late_packs_rejected_until_published(cd, algo, epochs):
         check(cd, coll, outs, oracle.allreduce(xs), n)
         assert coll.epoch() == e + 1
     assert cd.coll_get_rejections(coll.spec) > 0
-
-
-@pytest.mark.parametrize("mib", [32, 256])
-def test_bandwidth_allreduce_sentinel_sampled(cd, mib):
-    """8 ranks x 32 / 256 MiB uniform[-4,4], twoshot, streamed: every copy
-    identical, sampled positions equal to the oracle's fold."""
-    import torch
-
-    n, count = 8, mib * 1024 * 1024 // 2
-    ins = []
-    for r in range(n):
-        x = synth.uniform_bf16(29, count, -4.0, 4.0, mib, r)
-        ins.append(torch.from_numpy(x.view(np.int16)).cuda())
-        del x
-    coll = cd.Collective(cd.ALLREDUCE, n, count, encoding=SENT, algorithm=cd.COLL_TWOSHOT,
-                         path=cd.COLL_PATH_STREAMED)
-    outs = [torch.empty(count, dtype=torch.int16, device="cuda") for _ in range(n)]
-    for _ in range(2):
-        coll.run(ins, outs)
-    code, rank, line = coll.status()
-    assert code == cd.COLL_OK, (code, rank, line)
-    for r in range(1, n):
-        assert torch.equal(outs[r], outs[0])
-    g = np.random.Generator(np.random.Philox(mib))
-    m = oracle.shard_elems(count, n)
-    pos = set(g.integers(0, count, 20000).tolist())
-    for k in range(n + 1):
-        for d in (-9, -8, -1, 0, 1, 7, 8):
-            if 0 <= k * m + d < count:
-                pos.add(k * m + d)
-    pos = np.array(sorted(pos), dtype=np.int64)
-    idx = torch.from_numpy(pos).cuda()
-    cols = [ins[r][idx].cpu().numpy().view(np.uint16) for r in range(n)]
-    want = oracle.allreduce(cols)[0]
-    got = outs[0][idx].cpu().numpy().view(np.uint16)
-    assert np.array_equal(got, want)
-    del coll, outs, ins
-    torch.cuda.empty_cache()
