@@ -63,6 +63,21 @@ def kernel_bytes_allreduce_twoshot(n: int, s: float, eps: float) -> list[float]:
             n * s * eps + n * s]          # all-gather copy
 
 
+def kernel_floor_bytes_allreduce_twoshot(n: int, s: float, eps: float) -> list[float]:
+    """DRAM bytes each stream-ordered launch cannot avoid: the stage reads the
+    inputs and writes the lines (the next launch reads them from HBM); the
+    fold reads every rank's lines of its partition and publishes; the gather
+    reads each published line once from HBM (its N readers share L2) and
+    writes the outputs."""
+    return [n * s + n * s * eps, n * s * eps + s * eps, s * eps + n * s]
+
+
+def unique_bytes_allreduce(n: int, s: float) -> float:
+    """DRAM floor of a one-launch all-reduce: every input read once, every
+    output written once (staged and published lines never leave L2)."""
+    return 2 * n * s
+
+
 def bytes_allreduce_oneshot(n: int, s: float, eps: float) -> float:
     return 2 * n * s + n * s * eps + n * n * s * eps
 
@@ -85,6 +100,38 @@ def load_peaks() -> dict:
             d = json.load(f)
         return {"hbm_gbs": float(d.get("hbm_gbs", 6800.0)), "source": "measured"}
     return {"hbm_gbs": 6800.0, "source": "fallback"}
+
+
+def l2_copy_peak(stream) -> dict:
+    """Copy throughput of a buffer that stays in L2 (read + write bytes per
+    second): torch's b.copy_(a) repeated back to back on 16, 24 and 32 MiB
+    buffers (CUDA events on `stream`), the best of them.  The denominator of
+    the issue-level figure, whose bytes are mostly served by L2."""
+    import torch
+
+    best, where = 0.0, None
+    with torch.cuda.stream(stream):
+        for mib in (16, 24, 32):
+            a = torch.ones(mib << 19, dtype=torch.int16, device="cuda")
+            b = torch.empty_like(a)
+            for _ in range(20):
+                b.copy_(a)
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            reps = 200
+            e0.record(stream)
+            for _ in range(reps):
+                b.copy_(a)
+            e1.record(stream)
+            stream.synchronize()
+            gbs = 2 * (mib << 20) * reps / (e0.elapsed_time(e1) * 1e-3) / 1e9
+            if gbs > best:
+                best, where = gbs, mib
+            del a, b
+    return {"gbs": round(best, 1),
+            "how": f"torch b.copy_(a) on a {where} MiB buffer (best of 16/24/32 MiB), 200 "
+                   f"back-to-back copies after 20 warm-up copies, read + write bytes / "
+                   f"CUDA-event time, measured in this run"}
 
 
 class Clocks:
@@ -219,6 +266,66 @@ def cpu_oracle_allreduce(per_rank_mib: int, seed: int = 4, runs: int = 1) -> dic
                       f"counted with the same algorithmic bytes as the GPU line"}
 
 
+def _median_runs(fn, max_runs: int = 101, budget_s: float = 2.0, min_runs: int = 5) -> dict:
+    """Median wall time of up to `max_runs` calls of fn (at least `min_runs`,
+    stopping early once `budget_s` seconds have been spent)."""
+    times = []
+    t_start = time.perf_counter()
+    while len(times) < max_runs:
+        t0 = time.perf_counter()
+        fn()
+        times.append(time.perf_counter() - t0)
+        if len(times) >= min_runs and time.perf_counter() - t_start > budget_s:
+            break
+    return {"median_s": statistics.median(times), "runs": len(times)}
+
+
+def cpu_oracle_configs() -> dict:
+    """The plain C oracle (single thread, called through ctypes, timed with
+    time.perf_counter around each call) beside the small configurations:
+    c1 (2 ranks x 512 bf16, one all-reduce), the decode-time sweep (8 ranks x
+    [T x 4096] and 1 / 2 / 4 KiB per rank; all 8 output copies, as the GPU
+    op writes them) and c3 (one epoch of 8 ranks x [16 x 7168]: the oracle's
+    result for an epoch is the all-reduce of the published inputs).  Median
+    of up to 101 runs per size, bounded at 2 s of runs per size."""
+    import oracle
+    import synth
+
+    out = {}
+    xs = [synth.uniform_bf16(0, 512, -1.0, 1.0, 1, r) for r in range(2)]
+    m = _median_runs(lambda: oracle.allreduce(xs))
+    out["c1_allreduce_2x512"] = {"us_per_op": round(m["median_s"] * 1e6, 2), "runs": m["runs"]}
+    sweep = {}
+    sizes = [(f"{kib}KiB", kib * 512) for kib in (1, 2, 4)]
+    sizes += [(f"T={T}", T * 4096) for T in (1, 2, 4, 8, 16, 32, 64, 128)]
+    for key, count in sizes:
+        xs = [synth.normal_bf16(7, count, 0, r) for r in range(N_RANKS)]
+        m = _median_runs(lambda: oracle.allreduce(xs))
+        sweep[key] = {"bytes_per_rank": count * 2, "us_per_op": round(m["median_s"] * 1e6, 2),
+                      "runs": m["runs"]}
+    out["c2_allreduce_8x_Tx4096"] = sweep
+    xs = [synth.normal_bf16(3, 16 * 7168, 1, r) for r in range(N_RANKS)]
+    m = _median_runs(lambda: oracle.allreduce(xs))
+    out["c3_epoch_allreduce_8x16x7168"] = {"us_per_op": round(m["median_s"] * 1e6, 2),
+                                           "runs": m["runs"]}
+    return out
+
+
+def cpu_oracle_moe(ins_host, topk_host, experts: int) -> dict:
+    """c5: the oracle's MoE dispatch of the bench's own inputs and routing,
+    median of 3 runs (the first also touches the output pages)."""
+    import oracle
+
+    times = []
+    for _ in range(3):
+        t0 = time.perf_counter()
+        outs, _, _ = oracle.moe_dispatch(ins_host, topk_host, experts)
+        times.append(time.perf_counter() - t0)
+        del outs
+    return {"s_per_op": round(statistics.median(times), 3),
+            "runs_s": [round(t, 3) for t in times]}
+
+
 def workload_config(mib: int, path: str, world: int) -> dict:
     """The bench workload, named the same way by both arms."""
     return {"workload": f"all-reduce, {N_RANKS} emulated ranks, {mib} MiB bf16 per rank, "
@@ -298,6 +405,26 @@ def timed(step, k: int, w: int, stream, world: int) -> float:
     return e0.elapsed_time(e1)
 
 
+def graph_us_per_op(g, stream) -> float:
+    """Purlin's method for a captured graph of 128 ops: one warm-up replay,
+    then 8 timed replays per measurement (CUDA events on `stream`), per op;
+    the median of 5 such measurements, in microseconds."""
+    import torch
+
+    g.replay()
+    reps = []
+    for _ in range(5):
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(8):
+            g.replay()
+        e1.record(stream)
+        stream.synchronize()
+        reps.append(e0.elapsed_time(e1) * 1e3 / 1024)
+    return statistics.median(reps)
+
+
 def latency_sweep(cd, stream, only_T=None, only_variant=None, encoding=None) -> dict:
     """8 ranks x [T x 4096] bf16, LL8 (config of the decode-time sweep), or
     another readiness encoding; ahead of it 1, 2 and 4 KiB per rank, the
@@ -338,20 +465,18 @@ def latency_sweep(cd, stream, only_T=None, only_variant=None, encoding=None) -> 
                 with torch.cuda.graph(g, stream=stream):
                     for _ in range(128):
                         coll.run(ins, outs, stream)
-                g.replay()
-                # Purlin's method: 8 timed replays of the 128-op graph, per op;
-                # the median of 5 such measurements
-                reps = []
-                for _ in range(5):
-                    e0 = torch.cuda.Event(enable_timing=True)
-                    e1 = torch.cuda.Event(enable_timing=True)
-                    e0.record(stream)
-                    for _ in range(8):
-                        g.replay()
-                    e1.record(stream)
-                    stream.synchronize()
-                    reps.append(e0.elapsed_time(e1) * 1e3 / 1024)
-                warm = statistics.median(reps)
+                warm = graph_us_per_op(g, stream)
+                # the launch floor: an empty kernel in this run's one-launch
+                # configuration, timed the same way (flash-comm Appendix A)
+                floor = None
+                pl = coll.plan()
+                if pl["path"] == cd.COLL_PATH_FUSED:
+                    gf = torch.cuda.CUDAGraph()
+                    with torch.cuda.graph(gf, stream=stream):
+                        for _ in range(128):
+                            cd.coll_launch_floor(coll.spec, stream)
+                    floor = graph_us_per_op(gf, stream)
+                    del gf
                 # cold: L2 flushed (2x L2 written) before each op
                 evs = []
                 for _ in range(32):
@@ -367,8 +492,12 @@ def latency_sweep(cd, stream, only_T=None, only_variant=None, encoding=None) -> 
             st = coll.status(stream)
             row[name] = {"warm_us": round(warm, 3), "cold_us": round(cold, 3),
                          "status": st[0]}
+            if floor is not None:
+                row[name]["floor_us"] = round(floor, 3)
+                row[name]["excess_us"] = round(warm - floor, 3)
+                row[name]["launch"] = {"ctas": pl["ctas_per_rank"] * N_RANKS,
+                                       "dependent": pl["dependent_launch"]}
             if name == "policy":
-                pl = coll.plan()
                 row[name]["choice"] = {"encoding": pl["encoding"], "algorithm": pl["algorithm"],
                                        "path": pl["path"]}
             coll.close()
@@ -735,7 +864,7 @@ def hbm_reference_row(stream, reps=10) -> dict:
                     "write-heavy rows (all-gather, MoE dispatch)"}
 
 
-def moe_row(cd, stream, steps=5, path=None, tokens=4096) -> dict:
+def moe_row(cd, stream, steps=5, path=None, tokens=4096, cpu=False) -> dict:
     """MoE dispatch: 8 ranks x `tokens` tokens x 7168 bf16, top-8 of 256
     experts (routing drawn on the device from a seeded generator)."""
     import torch
@@ -792,7 +921,17 @@ def moe_row(cd, stream, steps=5, path=None, tokens=4096) -> dict:
     issue = rows * row_b + rows * line_b + rows * line_b + rows * row_b  # a row per choice
     ms = e0.elapsed_time(e1) / steps
     coll.close()
-    del coll, ins, outs, topk
+    del coll, outs
+    cpu_leg = None
+    if cpu:
+        import numpy as np
+
+        ins_h = [x.cpu().numpy().view(np.uint16).reshape(tokens, hidden) for x in ins]
+        topk_h = [t.cpu().numpy() for t in topk]
+        cpu_leg = cpu_oracle_moe(ins_h, topk_h, experts)
+        cpu_leg["GB/s"] = round(unique / (cpu_leg["s_per_op"] * 1e9), 4)
+        del ins_h, topk_h
+    del ins, topk
     torch.cuda.empty_cache()
     split = ({"routing_ms": round(times[0] / steps, 4),
               "stage_and_copy_ms": round(times[1] / steps, 4)} if composed else
@@ -803,7 +942,8 @@ def moe_row(cd, stream, steps=5, path=None, tokens=4096) -> dict:
             "routed_rows": rows, **split,
             "note": "bytes: each token row read once, staged as LL128 once per destination "
                     "rank it is routed to, each staged row read once and unpacked into "
-                    "every routed row", "status": st}
+                    "every routed row", "status": st,
+            **({"cpu_oracle": cpu_leg} if cpu_leg else {})}
 
 
 def main() -> int:
@@ -919,6 +1059,7 @@ def main() -> int:
         coll.run(ins, outs, stream)
         launches[0] += cd.coll_last_launches(coll.spec)
 
+    l2peak = l2_copy_peak(stream)
     clocks = Clocks(local)
     with torch.cuda.stream(stream):
         for i in range(W):
@@ -948,7 +1089,9 @@ def main() -> int:
     kernels = [{"name": names[k], "ms": round(dur[k], 4), "bytes": kb[k],
                 "GB/s": round(kb[k] / dur[k] / 1e6, 1)} for k in range(nk)]
     dom = max(range(nk), key=lambda k: dur[k])
-    achieved = kb[dom] / dur[dom] / 1e6
+    issue_gbs = kb[dom] / dur[dom] / 1e6
+    floor_bytes = ([unique_bytes_allreduce(N_RANKS, s_bytes)] if composed
+                   else kernel_floor_bytes_allreduce_twoshot(N_RANKS, s_bytes, EPS_LL128))
     traffic = None
     prof = os.path.join(ROOT, "profiles", "traffic.md")
     if os.path.exists(prof):
@@ -967,19 +1110,27 @@ def main() -> int:
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "bf16", "data": "synthetic",
         "config": workload_config(args.mib, args.path, world),
-        "roofline": {"bound": "hbm", "kernel": names[dom], "achieved": round(achieved, 1),
-                     "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                     "frac": round(achieved / peaks["hbm_gbs"], 4), "traffic": traffic,
-                     "peak_source": peaks["source"],
-                     # DRAM side: the ncu traffic per launch over this run's launch time
-                     **({"dram_achieved": round(traffic / dur[dom] / 1e6, 1),
-                         "dram_frac": round(traffic / dur[dom] / 1e6 / peaks["hbm_gbs"], 4)}
-                        if traffic else {})},
-        **({"roofline_note": "achieved counts every emulated rank's reads and writes "
-                             "(issue-level, as for the three-launch path); the staged and "
-                             "published lines stay in L2 and are dropped once read, so the "
-                             "DRAM traffic per op (traffic) is well below them and frac "
-                             "exceeds 1"} if composed else {}),
+        "roofline": {
+            "bound": "hbm", "kernel": names[dom],
+            # DRAM side: the kernel's ncu DRAM bytes per launch over this run's
+            # launch time (CUDA events around every launch of the timed steps)
+            "achieved": round(traffic / dur[dom] / 1e6, 1) if traffic else None,
+            "peak": peaks["hbm_gbs"], "unit": "GB/s",
+            "frac": round(traffic / dur[dom] / 1e6 / peaks["hbm_gbs"], 4) if traffic else None,
+            "traffic": traffic, "peak_source": peaks["source"],
+            "kernel_ms": round(dur[dom], 4),
+            # speed of light: the DRAM bytes the launch cannot avoid
+            "floor_bytes": floor_bytes[dom],
+            "sol_frac": round(floor_bytes[dom] / dur[dom] / 1e6 / peaks["hbm_gbs"], 4),
+            "issue_level": {"bytes": kb[dom], "achieved": round(issue_gbs, 1), "unit": "GB/s",
+                            "l2_peak": l2peak["gbs"],
+                            "frac_of_l2_peak": round(issue_gbs / l2peak["gbs"], 4),
+                            "l2_peak_how": l2peak["how"]},
+            "how": "achieved = traffic (ncu dram__bytes_read.sum + dram__bytes_write.sum per "
+                   "launch, profiles/traffic.md) / kernel_ms; frac = achieved / peak; "
+                   "sol_frac = floor_bytes / kernel_ms / peak; issue_level = every emulated "
+                   "rank's reads and writes (mostly L2 hits in one launch) against an L2 "
+                   "copy peak measured in this run"},
         "kernels": kernels,
         "gpu_launches": launches[0],
         "clocks": clk,
@@ -1016,6 +1167,27 @@ def main() -> int:
         if code != cd.COLL_OK:
             raise RuntimeError(f"device status {code} in the end-to-end runs")
         e2e_ms = min(copy_ms, direct_ms)
+        if world == 1:
+            # c4 on the host: the oracle's reduce-scatter of these very inputs
+            # (one fold per element in rank order, the all-reduce's arithmetic
+            # without its 8 output copies), median of 3
+            import numpy as np
+
+            xs_h = [h.numpy().view(np.uint16) for h in host_in]
+            import oracle
+
+            ts = []
+            for _ in range(3):
+                t0 = time.perf_counter()
+                oracle.reduce_scatter(xs_h)
+                ts.append(time.perf_counter() - t0)
+            rs_s = statistics.median(ts)
+            cpu_c4 = {"s_per_op": round(rs_s, 3), "runs_s": [round(t, 3) for t in ts],
+                      "GB/s": round(bytes_reduce_scatter(N_RANKS, s_bytes, EPS_LL128)
+                                    / rs_s / 1e9, 4),
+                      "what": f"reduce-scatter of the bench's own {N_RANKS} x {args.mib} MiB "
+                              f"inputs (GB/s with the reduce-scatter's algorithmic bytes)"}
+            del xs_h
         line["e2e"] = {"value": round(algo_bytes / (e2e_ms * 1e-3) / 1e9, 1), "unit": "GB/s",
                        "h2d_bytes_per_step": int(N_RANKS * s_bytes),
                        "d2h_bytes_per_step": int(N_RANKS * s_bytes),
@@ -1041,7 +1213,7 @@ def main() -> int:
             "all_to_all_256MiB": bandwidth_row(cd, cd.ALLTOALL, count, "a2a", stream),
             "all_to_all_256MiB_composed": bandwidth_row(cd, cd.ALLTOALL, count, "a2a", stream,
                                                         path=cd.COLL_PATH_COMPOSED),
-            "moe_dispatch_8x4096x7168_top8of256": moe_row(cd, stream),
+            "moe_dispatch_8x4096x7168_top8of256": moe_row(cd, stream, cpu=world == 1),
             "moe_dispatch_8x4096x7168_top8of256_streamed": moe_row(cd, stream,
                                                                    path=cd.COLL_PATH_STREAMED),
             "reduce_scatter_v_zipf_256MiB": v_row(cd, "REDUCE_SCATTER_V", 256 << 20, stream),
@@ -1057,6 +1229,15 @@ def main() -> int:
         line["latency_us_per_op"] = latency_sweep(cd, stream)
         if world == 1:
             line["cpu_baseline"] = cpu_oracle_allreduce(64, runs=3)
+            line["cpu_baselines"] = {
+                "host": host_cpu(), "threads": 1,
+                "how": "the plain C99 oracle (oracle/oracle.c) called through ctypes, one "
+                       "thread, wall time by time.perf_counter around each call",
+                **cpu_oracle_configs(),
+                "c4_reduce_scatter_256MiB": cpu_c4,
+                "c4_allreduce_64MiB_sample": line["cpu_baseline"],
+                "c5_moe_dispatch_8x4096x7168_top8of256":
+                    line["rows"]["moe_dispatch_8x4096x7168_top8of256"].get("cpu_oracle")}
     if rank == 0:
         print(json.dumps(line))
     if world > 1:

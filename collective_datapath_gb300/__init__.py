@@ -43,7 +43,8 @@ EXPORTS = [
     "coll_run_host", "coll_get_counts", "coll_query_status", "coll_get_epoch",
     "coll_staging_layout", "coll_stage_withheld", "coll_run_late",
     "coll_get_rejections", "coll_debug_items", "coll_debug_plan",
-    "coll_set_profile_events", "coll_last_launches", "coll_allreduce_static",
+    "coll_set_profile_events", "coll_last_launches", "coll_launch_floor",
+    "coll_allreduce_static",
     "coll_atom_copy", "coll_destroy", "coll_status_string",
 ]
 
@@ -97,6 +98,7 @@ _sig("coll_debug_plan", _st, _vp, _P(ctypes.c_int), _P(ctypes.c_int),
      _P(ctypes.c_int), _P(ctypes.c_int), _P(ctypes.c_int))
 _sig("coll_set_profile_events", _st, _vp, _P(_vp), ctypes.c_int)
 _sig("coll_last_launches", _st, _vp, _P(ctypes.c_int))
+_sig("coll_launch_floor", _st, _vp, _vp)
 _sig("coll_allreduce_static", _st, ctypes.c_int, _sz, _P(_vp), _P(_vp), _vp)
 _sig("coll_atom_copy", _st, _vp, _vp, _sz, ctypes.c_int, ctypes.c_int, ctypes.c_int,
      ctypes.c_int, _vp, _vp)
@@ -303,6 +305,11 @@ def coll_last_launches(spec: int) -> int:
     n = ctypes.c_int()
     _check(_lib.coll_last_launches(spec, ctypes.byref(n)), "coll_last_launches")
     return n.value
+
+
+def coll_launch_floor(spec: int, stream=None) -> None:
+    """One empty kernel in the spec's one-launch configuration (measurement)."""
+    _check(_lib.coll_launch_floor(spec, _stream_handle(stream)), "coll_launch_floor")
 
 
 def coll_allreduce_static(ins: Sequence, outs: Sequence, count: int, stream=None) -> None:

@@ -688,6 +688,16 @@ coll_status_t coll_set_profile_events(coll_spec_t* s, void* const* events, int n
   return COLL_OK;
 }
 
+coll_status_t coll_launch_floor(coll_spec_t* s, coll_stream_t stream) {
+  if (s == nullptr) return COLL_ERR_INVALID;
+  const Plan& p = s->plan;
+  const bool empty = p.items1.empty() && p.items2.empty();
+  if (p.kind == CK_MOE || p.path != COLL_PATH_FUSED || empty ||
+      (p.enc != ENC_LL128 && p.reset_mode == COLL_RESET_KERNEL))
+    return COLL_ERR_UNSUPPORTED;
+  return cuda_status(launch_floor(p.n * p.ctas_per_rank, as_stream(stream), p.dependent_launch));
+}
+
 coll_status_t coll_last_launches(const coll_spec_t* s, int* launches) {
   if (s == nullptr || launches == nullptr) return COLL_ERR_INVALID;
   *launches = s->launches;

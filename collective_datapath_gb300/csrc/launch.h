@@ -40,6 +40,8 @@ cudaError_t launch_consume(const RunParams& P, int phase, int grid, cudaStream_t
 // placed before the previous kernel in the stream completes; begin_run waits
 // for it before touching any data).
 cudaError_t launch_fused(const RunParams& P, int grid, cudaStream_t s, bool dependent);
+// An empty kernel in launch_fused's configuration (the fixed launch cost).
+cudaError_t launch_floor(int grid, cudaStream_t s, bool dependent);
 // LL128 phase-1 folds through the shared-memory pipeline (all items IK_REDUCE).
 cudaError_t launch_fold(const RunParams& P, int grid, cudaStream_t s, bool dependent);
 // LL128 copy phases (all items IK_COPY, plain outputs) and LL128 staging
