@@ -18,7 +18,7 @@ BUILD_DIR = os.path.join(ROOT, "_build")
 LIB = os.path.join(HERE, "libcoll.so")
 
 SOURCES = ["kernels.cu", "api.cpp", "derive.cpp", "static_ws.cu", "moe.cu", "composed.cu",
-           "atom.cu"]
+           "column.cu", "atom.cu"]
 HEADERS = ["plan.h", "derive.h", "launch.h", "dev_common.cuh", "ll8.cuh", "ll128.cuh",
            "pipe.cuh", "sent.cuh", "policy_table.h", "tma.cuh"]
 

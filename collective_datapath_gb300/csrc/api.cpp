@@ -143,35 +143,52 @@ cudaError_t launched(coll_spec* s, cudaError_t e, cudaStream_t st) {
   return cudaSuccess;
 }
 
-// Shape of the composed twoshot launch: chunks of 256 lines of every
-// partition (fewer for short runs, see below), a lag of 28 queue steps from
-// a chunk's stage to its fold and
-// from its fold to its gather, consumed lines dropped from L2, launch
-// variant 0.  COLL_COMPOSED_SHAPE = "chunk_lines,lag,discard,variant,lag2"
-// overrides it
-// (benchmark sweeps); chunks are a
-// power of two of at least kComposedMinChunk lines, the size the completion
-// flags were laid out for.
+// Shape of the composed launch.  COLL_COMPOSED_SHAPE =
+// "chunk_lines,lag,discard,variant,lag2,schedule" overrides the defaults
+// (benchmark sweeps and tests); chunks are a power of two of at least
+// kComposedMinChunk lines (rows per chunk are counted with shifts, and the
+// queue's completion flags are laid out for that size).
+//
+// schedule 0 (default), columns: a column is one chunk of one partition,
+// run start to end by one CTA, launch variant 2 (4 warps, 6 CTAs per SM).
+// Unbounded staging: the chunk is the largest of 128, 64 and 32 lines that
+// still gives every co-resident CTA four columns, so the last round of
+// columns is a small part of the run (measured at 8 x 32 / 128 / 256 MiB:
+// 64, 128 and 128 lines were best).  Bounded staging: CTA g owns chunk slot
+// g of every rank image, so the chunk is the largest of 128 .. 16 lines
+// whose slots cover every co-resident CTA.
+//
+// schedule 1, the queue of tasks (stage, fold, gather per chunk, with lags
+// of `lag` and `lag2` steps): defaults measured at 8 x 256 MiB, all-reduce
+// 256-line chunks and lag 28, reduce-scatter and all-to-all 128-line chunks
+// and lag 40; the all-reduce's chunk is the largest of 256, 128 and 64 lines
+// that still gives eight lags' worth of chunks (the queue fills and drains
+// over 2 * lag steps).
 ComposedParams composed_shape(const coll_spec* s) {
   const Plan& p = s->plan;
   ComposedParams q{};
-  // defaults measured at 8 x 256 MiB: all-reduce 256-line chunks, lag 28;
-  // reduce-scatter and all-to-all 128-line chunks, lag 40
   const bool ar = p.kind == CK_ALLREDUCE;
-  int chunk = ar ? 256 : 128, lag = ar ? 28 : 40, discard = 1, variant = 0, lag2 = -1;
+  int chunk = ar ? 256 : 128, lag = ar ? 28 : 40, discard = 1, variant = 0, lag2 = -1,
+      schedule = 0;
   uint64_t most = 0;
   for (const Seg& sg : p.pseg[0]) most = std::max<uint64_t>(most, sg.lines);
   const char* env = std::getenv("COLL_COMPOSED_SHAPE");
-  if (env != nullptr) {
-    std::sscanf(env, "%d,%d,%d,%d,%d", &chunk, &lag, &discard, &variant, &lag2);
-  } else if (ar) {
-    // The queue fills and drains over 2 * lag steps; the chunk is the largest
-    // of 256, 128 and 64 lines that still gives eight lags' worth of chunks
-    // (measured at 8 x 8 / 32 / 128 MiB: 64, 128 and 256 lines were best).
+  if (env != nullptr)
+    std::sscanf(env, "%d,%d,%d,%d,%d,%d", &chunk, &lag, &discard, &variant, &lag2, &schedule);
+  q.schedule = schedule == 1 ? 1 : 0;
+  if (q.schedule == 0 && env == nullptr) variant = 2;
+  q.variant = variant >= 0 && variant <= 2 ? variant : 0;
+  if (q.schedule == 0 && env == nullptr) {
+    const uint64_t cap = (uint64_t)std::max(1, column_capacity(q.variant));
+    chunk = 128;
+    if (p.ring_lines > 0) {
+      while (chunk > (int)kComposedMinChunk && p.ring_lines / (uint64_t)chunk < cap) chunk /= 2;
+    } else {
+      while (chunk > 32 && (most + chunk - 1) / chunk * (uint64_t)p.n < 4 * cap) chunk /= 2;
+    }
+  } else if (q.schedule == 1 && env == nullptr && ar) {
     while (chunk > 64 && (most + chunk - 1) / chunk < 8ull * (uint64_t)lag) chunk /= 2;
   }
-  // a power of two of at least kComposedMinChunk lines (rows per chunk are
-  // counted with shifts)
   int c2 = (int)kComposedMinChunk;
   while (c2 * 2 <= chunk && c2 < (1 << 20)) c2 *= 2;
   chunk = c2;
@@ -180,17 +197,25 @@ ComposedParams composed_shape(const coll_spec* s) {
   q.nchunks = (uint32_t)std::max<uint64_t>(1, (max_lines + chunk - 1) / chunk);
   q.lag = std::max(1, lag);
   q.lag2 = lag2 < 1 ? q.lag : lag2;
-  // Bounded staging (Purlin §4.1): chunk c uses chunk slot c mod W of the
-  // staging images.  A stage waits for the folds (copies) that read the
-  // slot's previous chunk, W - lag queue steps back, and a fold for the
-  // gathers of its published slot's previous chunk, W - lag2 steps back.
-  // Both lags are at most W / 2: every task then waits only for earlier
-  // tasks, and no wait is on a task just a few steps back (with lags near W
-  // the queue advances one dependent task at a time; 8 x 256 MiB with W = 32
-  // and lags of 28 took 5.0 ms).  The chunk shrinks (to no less than
-  // kComposedMinChunk) until the images hold two slots.
   q.ring = 0;
-  if (p.ring_lines > 0) {
+  if (p.ring_lines > 0 && q.schedule == 0) {
+    // Bounded staging (Purlin §4.1), columns: ring = chunk slots of each
+    // rank image; at least one per partition (the launch takes a multiple
+    // of N CTAs, one per slot at most).
+    while (q.chunk_lines > kComposedMinChunk && p.ring_lines / q.chunk_lines < (uint64_t)p.n)
+      q.chunk_lines /= 2;
+    q.nchunks = (uint32_t)std::max<uint64_t>(1, (max_lines + q.chunk_lines - 1) / q.chunk_lines);
+    q.ring = (uint32_t)(p.ring_lines / q.chunk_lines);
+  } else if (p.ring_lines > 0) {
+    // Bounded staging, queue: chunk c uses chunk slot c mod W of the
+    // staging images.  A stage waits for the folds (copies) that read the
+    // slot's previous chunk, W - lag queue steps back, and a fold for the
+    // gathers of its published slot's previous chunk, W - lag2 steps back.
+    // Both lags are at most W / 2: every task then waits only for earlier
+    // tasks, and no wait is on a task just a few steps back (with lags near
+    // W the queue advances one dependent task at a time; 8 x 256 MiB with
+    // W = 32 and lags of 28 took 5.0 ms).  The chunk shrinks (to no less
+    // than kComposedMinChunk) until the images hold two slots.
     while (q.chunk_lines > kComposedMinChunk &&
            p.ring_lines / ((uint64_t)p.n * q.chunk_lines) < 2)
       q.chunk_lines /= 2;
@@ -207,7 +232,6 @@ ComposedParams composed_shape(const coll_spec* s) {
     q.lag2 = std::min(q.lag2, std::max(1, (int)q.ring / 2));
   }
   q.discard = discard;
-  q.variant = variant >= 0 && variant <= 2 ? variant : 0;
   q.mode = p.kind == CK_REDUCE_SCATTER ? 1
            : p.kind == CK_ALLTOALL      ? 2
            : p.kind == CK_ALLGATHER     ? 3
@@ -469,6 +493,20 @@ coll_status_t coll_run(coll_spec_t* s, const void* const* dev_ins, void* const* 
         P.seg_elems[k] = p.pseg[k][0].elems;
         P.seg_in0[k] = p.shard * (uint64_t)k;
       }
+    }
+    if (P.cp.schedule == 0) {
+      // columns: every co-resident CTA, or with bounded staging a multiple
+      // of N CTAs that each own a chunk slot
+      const int cap = column_capacity(P.cp.variant);
+      int grid = cap;
+      if (P.cp.ring > 0) grid = std::min<int>(cap, (int)P.cp.ring);
+      grid -= grid % p.n;
+      if (grid < p.n) return COLL_ERR_CUDA;
+      // bounded staging: lines of column q carry epoch + q, so the run moves
+      // the epoch past all of them, by an odd step (Purlin §4.2)
+      P.advance_epoch =
+          P.cp.ring > 0 ? (int)(((uint64_t)P.cp.nchunks * (uint64_t)p.n) | 1u) : 1;
+      return cuda_status(launched(s, launch_column(P, grid, st), st));
     }
     const int cap = composed_capacity(P.cp.variant, P.cp.ring > 0);
     if (cap < 3) return COLL_ERR_CUDA;

@@ -223,19 +223,17 @@ __device__ __forceinline__ void stage_task(const Piece* pc, uint32_t wbase, int 
   __syncwarp();
 }
 
-// Fold chunk c of partition r over the N staged images; publish it as lines
-// of owner r (all-reduce) or write it into rank r's output (reduce-scatter).
+// Fold the `nl` lines of partition r that start at line t0 of the segment
+// (staged at line src_line of every rank image) over the N images, in rank
+// order; publish the result as lines at `ag` (all-reduce) or write it into
+// rank r's output (reduce-scatter).
 template <int kCWarps, int kCRing>
-__device__ __forceinline__ bool fold_task(const RunParams& P, uint32_t wbase, int lane, int warp,
-                                          int c, int r, uint64_t e, uint64_t seq, bool to_out,
-                                          uint32_t W) {
+__device__ __forceinline__ bool fold_rows(const RunParams& P, uint32_t wbase, int lane, int warp,
+                                          int r, uint32_t t0, int nl, uint64_t src_line,
+                                          char* ag, uint64_t e, uint64_t seq, bool to_out) {
   constexpr int kCFoldStages = kCRing / kMaxRanks;  // rows of all N images per warp
   const int n = P.nranks;
-  const uint32_t t0 = (uint32_t)c * P.cp.chunk_lines;
-  const int nl = chunk_lines_of(P, r, t0);
   const int li = lane >> 3;
-  const uint64_t src_line =
-      W ? ((uint64_t)(c % W) * n + r) * P.cp.chunk_lines : P.seg_line0[r] + t0;
   // rank p's rows of this piece start at src0 + p * rank_bytes
   const char* src0 = image_bytes(P, P.P, e, 0) + src_line * kLL128LineBytes;
   const uint64_t rb = P.P.rank_bytes;
@@ -255,8 +253,6 @@ __device__ __forceinline__ bool fold_task(const RunParams& P, uint32_t wbase, in
   };
 #pragma unroll
   for (int j = 0; j < kCFoldStages; ++j) issue(j);
-  char* ag = image_bytes(P, P.AG, e, r) +
-             (W ? (uint64_t)(c % W) * P.cp.chunk_lines : (uint64_t)t0) * kLL128LineBytes;
   bool ok = true;
   for (int j = 0; j < nj; ++j) {
     cp_async_wait<kCFoldStages - 1>();
@@ -307,6 +303,21 @@ __device__ __forceinline__ bool fold_task(const RunParams& P, uint32_t wbase, in
   cp_async_wait<0>();
   __syncwarp();
   return ok;
+}
+
+// Fold chunk c of partition r over the N staged images; publish it as lines
+// of owner r (all-reduce) or write it into rank r's output (reduce-scatter).
+template <int kCWarps, int kCRing>
+__device__ __forceinline__ bool fold_task(const RunParams& P, uint32_t wbase, int lane, int warp,
+                                          int c, int r, uint64_t e, uint64_t seq, bool to_out,
+                                          uint32_t W) {
+  const uint32_t t0 = (uint32_t)c * P.cp.chunk_lines;
+  const uint64_t src_line =
+      W ? ((uint64_t)(c % W) * P.nranks + r) * P.cp.chunk_lines : P.seg_line0[r] + t0;
+  char* ag = image_bytes(P, P.AG, e, r) +
+             (W ? (uint64_t)(c % W) * P.cp.chunk_lines : (uint64_t)t0) * kLL128LineBytes;
+  return fold_rows<kCWarps, kCRing>(P, wbase, lane, warp, r, t0, chunk_lines_of(P, r, t0),
+                                    src_line, ag, e, seq, to_out);
 }
 
 template <int kCWarps, int kCRing>

@@ -53,6 +53,9 @@ cudaError_t launch_withhold(const RunParams& P, cudaStream_t s);
 // the launch (P.cp filled in).
 int composed_capacity(int variant, bool cycle);
 cudaError_t launch_composed(const RunParams& P, int grid, cudaStream_t s);
+// The same collectives scheduled by columns (P.cp.schedule == 0).
+int column_capacity(int variant);
+cudaError_t launch_column(const RunParams& P, int grid, cudaStream_t s);
 // MoE dispatch: routing + gather-stage of one source (P.stage_rank) or all,
 // then the destination scan + validated copy (ends the run).
 cudaError_t launch_moe_stage_all(const RunParams& P, cudaStream_t s);

@@ -128,6 +128,8 @@ struct ComposedParams {
   int discard;           // drop consumed lines from L2 (no write-back):
                          // 1 = staged and published lines, 2 = staged only
   int variant;           // launch shape (ring depth and CTAs per SM)
+  int schedule;          // 0: columns (one CTA runs a column's stage, fold and
+                         // gather phases); 1: a queue of tasks with lags
   int mode;              // 0 all-reduce: stage, fold + publish, gather;
                          // 1 reduce-scatter: stage, fold into the outputs;
                          // 2 all-to-all: stage, copy into the outputs;
