@@ -5,8 +5,10 @@ Default workload (one step = one all-reduce through the whole datapath:
 stage as LL128 lines, validate + fold the partitions at their owners,
 publish, validate + unpack at every rank):
     8 emulated ranks, 256 MiB of bf16 per rank (uniform[-4, 4], seeded),
-    LL128 sequence-number lines, twoshot, one composed launch
-    (``--path streamed``: the three stream-ordered launches).
+    LL128 sequence-number lines, twoshot, one composed launch in which
+    each CTA runs the stage, fold + publish and gather of one chunk of a
+    partition at a time (``--path streamed``: the three stream-ordered
+    launches).
 The inputs (2 GiB) and staging (4.8 GiB) exceed the 126 MiB L2, so no L2
 flush is needed between steps.
 
@@ -102,36 +104,52 @@ def load_peaks() -> dict:
     return {"hbm_gbs": 6800.0, "source": "fallback"}
 
 
-def l2_copy_peak(stream) -> dict:
-    """Copy throughput of a buffer that stays in L2 (read + write bytes per
-    second): torch's b.copy_(a) repeated back to back on 16, 24 and 32 MiB
-    buffers (CUDA events on `stream`), the best of them.  The denominator of
-    the issue-level figure, whose bytes are mostly served by L2."""
+def l2_copy_peak(cd, stream) -> dict:
+    """Copy throughput of buffers that stay in L2 (read + write bytes per
+    second), the denominator of the issue-level figure, whose bytes are
+    mostly served by L2.  Two measurements, the larger kept: torch's
+    b.copy_(a) (a device-to-device cudaMemcpyAsync: it runs on a copy engine,
+    not on the SMs) and the library's own SM copy kernel (coll_atom_copy, the
+    cp.async engine, several launch shapes); 16 MiB copied each time, so
+    source and destination (32 MiB) fit in L2, back-to-back after warm-up,
+    CUDA events on `stream`."""
     import torch
 
-    best, where = 0.0, None
+    nbytes = 16 << 20
+    a = torch.ones(nbytes // 2, dtype=torch.int16, device="cuda")
+    b = torch.empty_like(a)
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    shapes = {"torch copy_ (copy engine)": None,
+              f"coll_atom_copy lsu, {4 * sms} CTAs x 4 stages x 4 KiB": (4 * sms, 4, 4096),
+              f"coll_atom_copy lsu, {6 * sms} CTAs x 2 stages x 4 KiB": (6 * sms, 2, 4096),
+              f"coll_atom_copy lsu, {2 * sms} CTAs x 8 stages x 8 KiB": (2 * sms, 8, 8192)}
+    res = {}
     with torch.cuda.stream(stream):
-        for mib in (16, 24, 32):
-            a = torch.ones(mib << 19, dtype=torch.int16, device="cuda")
-            b = torch.empty_like(a)
+        for name, shape in shapes.items():
+            if shape is None:
+                op = lambda: b.copy_(a)  # noqa: E731
+            else:
+                c, st, sb = shape
+                op = lambda c=c, st=st, sb=sb: cd.coll_atom_copy(  # noqa: E731
+                    b, a, nbytes, engine=cd.COLL_ATOM_LSU, ctas=c, stages=st, stage_bytes=sb,
+                    stream=stream)
             for _ in range(20):
-                b.copy_(a)
+                op()
             e0 = torch.cuda.Event(enable_timing=True)
             e1 = torch.cuda.Event(enable_timing=True)
             reps = 200
             e0.record(stream)
             for _ in range(reps):
-                b.copy_(a)
+                op()
             e1.record(stream)
             stream.synchronize()
-            gbs = 2 * (mib << 20) * reps / (e0.elapsed_time(e1) * 1e-3) / 1e9
-            if gbs > best:
-                best, where = gbs, mib
-            del a, b
-    return {"gbs": round(best, 1),
-            "how": f"torch b.copy_(a) on a {where} MiB buffer (best of 16/24/32 MiB), 200 "
-                   f"back-to-back copies after 20 warm-up copies, read + write bytes / "
-                   f"CUDA-event time, measured in this run"}
+            res[name] = round(2 * nbytes * reps / (e0.elapsed_time(e1) * 1e-3) / 1e9, 1)
+    del a, b
+    best = max(res, key=res.get)
+    return {"gbs": res[best], "how": f"{best}: 16 MiB copied (32 MiB resident in L2), 200 "
+                                     f"back-to-back copies after 20 warm-up copies, read + "
+                                     f"write bytes / CUDA-event time, measured in this run",
+            "candidates": res}
 
 
 class Clocks:
@@ -1021,6 +1039,8 @@ def main() -> int:
             "rs_composed": lambda: bandwidth_row(cd, cd.REDUCE_SCATTER, count, "rs", stream,
                                                  path=cd.COLL_PATH_COMPOSED),
             "ag": lambda: bandwidth_row(cd, cd.ALLGATHER, count, "ag", stream),
+            "ag_composed": lambda: bandwidth_row(cd, cd.ALLGATHER, count, "ag", stream,
+                                                 path=cd.COLL_PATH_COMPOSED),
             "a2a": lambda: bandwidth_row(cd, cd.ALLTOALL, count, "a2a", stream),
             "a2a_composed": lambda: bandwidth_row(cd, cd.ALLTOALL, count, "a2a", stream,
                                                   path=cd.COLL_PATH_COMPOSED),
@@ -1059,7 +1079,7 @@ def main() -> int:
         coll.run(ins, outs, stream)
         launches[0] += cd.coll_last_launches(coll.spec)
 
-    l2peak = l2_copy_peak(stream)
+    l2peak = l2_copy_peak(cd, stream)
     clocks = Clocks(local)
     with torch.cuda.stream(stream):
         for i in range(W):
@@ -1079,7 +1099,7 @@ def main() -> int:
 
     # per-kernel durations over the timed steps
     if composed:
-        names = ["composed twoshot (queue of stage / fold + publish / gather tasks)"]
+        names = ["composed twoshot (columns: stage, fold + publish, gather of one chunk of a partition per CTA)"]
         kb = [bytes_allreduce_twoshot(N_RANKS, s_bytes, EPS_LL128)]
     else:
         names = ["stage (LL128 encode)", "reduce-scatter fold + publish", "all-gather unpack"]
@@ -1125,7 +1145,8 @@ def main() -> int:
             "issue_level": {"bytes": kb[dom], "achieved": round(issue_gbs, 1), "unit": "GB/s",
                             "l2_peak": l2peak["gbs"],
                             "frac_of_l2_peak": round(issue_gbs / l2peak["gbs"], 4),
-                            "l2_peak_how": l2peak["how"]},
+                            "l2_peak_how": l2peak["how"],
+                            "l2_peak_candidates": l2peak["candidates"]},
             "how": "achieved = traffic (ncu dram__bytes_read.sum + dram__bytes_write.sum per "
                    "launch, profiles/traffic.md) / kernel_ms; frac = achieved / peak; "
                    "sol_frac = floor_bytes / kernel_ms / peak; issue_level = every emulated "
@@ -1210,6 +1231,8 @@ def main() -> int:
             "reduce_scatter_256MiB_composed": bandwidth_row(cd, cd.REDUCE_SCATTER, count, "rs",
                                                             stream, path=cd.COLL_PATH_COMPOSED),
             "all_gather_256MiB": bandwidth_row(cd, cd.ALLGATHER, count, "ag", stream),
+            "all_gather_256MiB_composed": bandwidth_row(cd, cd.ALLGATHER, count, "ag", stream,
+                                                        path=cd.COLL_PATH_COMPOSED),
             "all_to_all_256MiB": bandwidth_row(cd, cd.ALLTOALL, count, "a2a", stream),
             "all_to_all_256MiB_composed": bandwidth_row(cd, cd.ALLTOALL, count, "a2a", stream,
                                                         path=cd.COLL_PATH_COMPOSED),

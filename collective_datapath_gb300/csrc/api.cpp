@@ -151,12 +151,15 @@ cudaError_t launched(coll_spec* s, cudaError_t e, cudaStream_t st) {
 //
 // schedule 0 (default), columns: a column is one chunk of one partition,
 // run start to end by one CTA, launch variant 2 (4 warps, 6 CTAs per SM).
-// Unbounded staging: the chunk is the largest of 128, 64 and 32 lines that
-// still gives every co-resident CTA four columns, so the last round of
-// columns is a small part of the run (measured at 8 x 32 / 128 / 256 MiB:
-// 64, 128 and 128 lines were best).  Bounded staging: CTA g owns chunk slot
-// g of every rank image, so the chunk is the largest of 128 .. 16 lines
-// whose slots cover every co-resident CTA.
+// Unbounded staging: the chunk is 64 lines (128 for the all-gather, whose
+// column stages one piece and copies it N times), halved down to 32 while
+// the co-resident CTAs would get fewer than four columns each, so the last
+// round of columns stays a small part of the run.  Measured, 8 ranks, all-
+// reduce: 256 MiB 0.89 ms at 64 lines (0.93 at 128, 0.95 at 32); 128 MiB
+// 0.46 ms at 64; 32 MiB 0.136-0.139 ms at 32-64; 8 MiB 0.050 ms at 32;
+// all-gather 256 MiB 0.396 ms at 128 lines, 0.442 at 64.  Bounded staging:
+// CTA g owns chunk slot g of every rank image, so the chunk is the largest
+// of 64 .. 16 lines whose slots cover every co-resident CTA.
 //
 // schedule 1, the queue of tasks (stage, fold, gather per chunk, with lags
 // of `lag` and `lag2` steps): defaults measured at 8 x 256 MiB, all-reduce
@@ -180,7 +183,7 @@ ComposedParams composed_shape(const coll_spec* s) {
   q.variant = variant >= 0 && variant <= 2 ? variant : 0;
   if (q.schedule == 0 && env == nullptr) {
     const uint64_t cap = (uint64_t)std::max(1, column_capacity(q.variant));
-    chunk = 128;
+    chunk = p.kind == CK_ALLGATHER ? 128 : 64;
     if (p.ring_lines > 0) {
       while (chunk > (int)kComposedMinChunk && p.ring_lines / (uint64_t)chunk < cap) chunk /= 2;
     } else {

@@ -335,10 +335,12 @@ int derive(const DeriveInput& in, Plan& p) {
   // of the 8-rank sweeps on GB300.  Oneshot up to 512 KiB per rank (it reads
   // N^2 S of lines but has one phase), twoshot above; one fused cooperative
   // kernel up to 256 KiB per rank for LL8 and sentinel packs; the composed
-  // launch for the LL128 twoshot and reduce-scatter from 32 MiB per rank
-  // (where the calibrated table switches the all-reduce to it) and for the
-  // all-to-all from 16 MiB (8 x 16 MiB: 98 against 107 us streamed);
-  // stream-ordered kernels otherwise.  Two ranks always use oneshot (both move S per rank).
+  // launch for the LL128 twoshot and reduce-scatter (8 x 1 MiB reduce-
+  // scatter: 18 against 40 us stream-ordered), for the LL128 all-gather
+  // (equal up to 16 MiB, then faster: 8 x 256 MiB 0.40 against 0.55 ms) and
+  // for the all-to-all from 4 MiB (8 x 4 MiB: 32 against 34 us); stream-
+  // ordered kernels otherwise.  Two ranks always use oneshot (both move S
+  // per rank).
   p.algorithm = 0;
   if (p.kind == CK_ALLREDUCE) {
     p.algorithm = algo;
@@ -358,10 +360,9 @@ int derive(const DeriveInput& in, Plan& p) {
     if (in_bytes_per_rank <= 256 * 1024 && p.enc != ENC_LL128)
       p.path = COLL_PATH_FUSED;
     else if (p.enc == ENC_LL128 &&
-             ((in_bytes_per_rank >= (32u << 20) &&
-               ((p.kind == CK_ALLREDUCE && p.algorithm == COLL_TWOSHOT) ||
-                p.kind == CK_REDUCE_SCATTER)) ||
-              (in_bytes_per_rank >= (16u << 20) && p.kind == CK_ALLTOALL)))
+             ((p.kind == CK_ALLREDUCE && p.algorithm == COLL_TWOSHOT) ||
+              p.kind == CK_REDUCE_SCATTER || p.kind == CK_ALLGATHER ||
+              (in_bytes_per_rank >= (4u << 20) && p.kind == CK_ALLTOALL)))
       p.path = COLL_PATH_COMPOSED;
     else
       p.path = COLL_PATH_STREAMED;

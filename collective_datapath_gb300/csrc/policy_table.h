@@ -15,31 +15,27 @@ struct PolicyEntry {
 };
 
 constexpr PolicyEntry kPolicy2[] = {
-    {65536ull, 0, 1, 1, 64},  // LL8/oneshot/fused/narrow
-    {131072ull, 2, 1, 1, 64},  // SENT/oneshot/fused/narrow
-    {770048ull, 2, 1, 1, 0},  // SENT/oneshot/fused
-    {2998272ull, 2, 1, 1, 1024},  // SENT/oneshot/fused/wide
-    {7421952ull, 2, 2, 1, 1024},  // SENT/twoshot/fused/wide
-    {17432576ull, 1, 1, 2, 0},  // LL128/oneshot/streamed
-    {UINT64_MAX, 1, 2, 2, 0},  // LL128/twoshot/streamed
+    {49152ull, 0, 1, 1, 64},  // LL8/oneshot/fused/narrow
+    {131072ull, 0, 1, 1, 0},  // LL8/oneshot/fused
+    {262144ull, 2, 1, 1, 0},  // SENT/oneshot/fused
+    {2654208ull, 2, 1, 1, 1024},  // SENT/oneshot/fused/wide
+    {4456448ull, 2, 2, 1, 1024},  // SENT/twoshot/fused/wide
+    {UINT64_MAX, 1, 2, 3, 0},  // LL128/twoshot/composed
 };
 constexpr PolicyEntry kPolicy4[] = {
     {32768ull, 0, 1, 1, 64},  // LL8/oneshot/fused/narrow
-    {311296ull, 2, 1, 1, 0},  // SENT/oneshot/fused
-    {983040ull, 2, 1, 1, 1024},  // SENT/oneshot/fused/wide
-    {1900544ull, 2, 2, 1, 0},  // SENT/twoshot/fused
-    {7421952ull, 2, 2, 1, 1024},  // SENT/twoshot/fused/wide
-    {9109504ull, 1, 1, 2, 0},  // LL128/oneshot/streamed
-    {UINT64_MAX, 1, 2, 2, 0},  // LL128/twoshot/streamed
+    {376832ull, 2, 1, 1, 0},  // SENT/oneshot/fused
+    {1753088ull, 2, 1, 1, 1024},  // SENT/oneshot/fused/wide
+    {4194304ull, 2, 2, 1, 1024},  // SENT/twoshot/fused/wide
+    {UINT64_MAX, 1, 2, 3, 0},  // LL128/twoshot/composed
 };
 constexpr PolicyEntry kPolicy8[] = {
     {8192ull, 0, 1, 1, 64},  // LL8/oneshot/fused/narrow
-    {32768ull, 2, 1, 1, 64},  // SENT/oneshot/fused/narrow
-    {180224ull, 2, 1, 1, 0},  // SENT/oneshot/fused
-    {819200ull, 2, 1, 1, 1024},  // SENT/oneshot/fused/wide
-    {1835008ull, 2, 2, 1, 0},  // SENT/twoshot/fused
-    {7421952ull, 2, 2, 1, 1024},  // SENT/twoshot/fused/wide
-    {51150848ull, 1, 2, 2, 0},  // LL128/twoshot/streamed
+    {32768ull, 0, 1, 1, 0},  // LL8/oneshot/fused
+    {65536ull, 2, 1, 1, 0},  // SENT/oneshot/fused
+    {737280ull, 2, 1, 1, 1024},  // SENT/oneshot/fused/wide
+    {1851392ull, 2, 2, 1, 0},  // SENT/twoshot/fused
+    {2752512ull, 2, 2, 1, 1024},  // SENT/twoshot/fused/wide
     {UINT64_MAX, 1, 2, 3, 0},  // LL128/twoshot/composed
 };
 
