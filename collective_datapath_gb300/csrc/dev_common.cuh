@@ -210,26 +210,47 @@ __device__ __forceinline__ void count_rejection(char* ws) {
 // threads hold the value (the barrier's predicate consumes it).  The last CTA
 // of the grid advances the epoch once every CTA has arrived, so the next run
 // uses the other staging slot; no CTA waits at the end of its own work.
-__device__ __forceinline__ uint64_t begin_run(const RunParams& P) {
-  WsHeader* h = header(P.ws);
+// begin_run in two halves, for a kernel that issues loads of its own while
+// the epoch is in flight: run_wait_epoch waits for the previous kernel in
+// the stream and issues the epoch load; run_arrive (the first use of the
+// epoch) lets a dependent launch place its CTAs and counts this CTA in.
+__device__ __forceinline__ uint64_t run_wait_epoch(const RunParams& P) {
   // Under programmatic stream serialization the CTAs may start before the
   // previous kernel in the stream has completed: wait for it (and for its
   // writes) before reading anything; without that launch attribute the wait
-  // returns at once.  Then let a dependent launch place its CTAs.
+  // returns at once.
   asm volatile("griddepcontrol.wait;" ::: "memory");
-  const uint64_t e = ld_relaxed_u64(&h->epoch);
+  return ld_relaxed_u64(&header(P.ws)->epoch);
+}
+
+__device__ __forceinline__ void run_arrive(const RunParams& P, uint64_t e) {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   if (P.advance_epoch) {
     const int z = __syncthreads_or((int)(e >> 63));  // 0: the epoch never gets there
     if (threadIdx.x == 0)
-      asm volatile("red.relaxed.gpu.global.add.u32 [%0], %1;" ::"l"(&h->arrived),
+      asm volatile("red.relaxed.gpu.global.add.u32 [%0], %1;" ::"l"(&header(P.ws)->arrived),
                    "r"(1u + (uint32_t)z)
                    : "memory");
   }
+}
+
+__device__ __forceinline__ uint64_t begin_run(const RunParams& P) {
+  const uint64_t e = run_wait_epoch(P);
+  run_arrive(P, e);
   return e;
 }
 
-__device__ __forceinline__ void finish_run(const RunParams& P, uint64_t epoch) {
+// The arrival count as the grid's last CTA sees it early (before its last
+// phase of work), so that finish_run usually need not read it again; other
+// CTAs, and launches that do not end a run, get 0.
+__device__ __forceinline__ uint32_t early_arrivals(const RunParams& P) {
+  if (!P.advance_epoch || threadIdx.x != 0 || blockIdx.x != gridDim.x - 1) return 0;
+  return ld_relaxed_u32(&header(P.ws)->arrived);
+}
+
+// `seen`: an arrival count this CTA read earlier (early_arrivals), or 0.
+__device__ __forceinline__ void finish_run(const RunParams& P, uint64_t epoch,
+                                           uint32_t seen = 0) {
   if (!P.advance_epoch || threadIdx.x != 0) return;
   const uint32_t total = gridDim.x * gridDim.y * gridDim.z;
   if (blockIdx.x != gridDim.x - 1) return;
@@ -238,7 +259,7 @@ __device__ __forceinline__ void finish_run(const RunParams& P, uint64_t epoch) {
   // finishes; the 10 s bound only guards against a broken launch.  This wait
   // ignores `abort`: the epoch must not move before every CTA has read it.
   const uint64_t t0 = globaltimer_ns();
-  while (ld_relaxed_u32(&h->arrived) < total) {
+  while (seen < total && ld_relaxed_u32(&h->arrived) < total) {
     if (globaltimer_ns() - t0 > 10000000000ull) {
       latch_error(P.ws, kStatusTimeout, 0xFFFFFFFFu, -2);
       break;

@@ -696,31 +696,63 @@ __device__ void late_producer(const RunParams& P, uint64_t e, int p, int workers
   }
 }
 
+// A run in one launch is a chain of dependent global-memory round trips, so
+// the prologue overlaps the ones that do not depend on each other: this
+// CTA's first stage and consume items are read before the wait for the
+// previous kernel (the plan's items are written when the workspace is bound
+// and never change), and the first input load of the stage is issued while
+// the epoch is in flight.  The grid's last CTA reads the arrival count
+// before its consume phase, so the end of the run need not wait on it.
 template <int ENC>
 __global__ void __launch_bounds__(kThreads, 2) k_fused(RunParams P) {
-  const uint64_t e = begin_run(P);
   const int B = P.ctas_per_rank;
   const int workers = P.nranks * B;
-  if ((int)blockIdx.x >= workers) {
+  const bool worker = (int)blockIdx.x < workers;
+  const int d = worker ? (int)blockIdx.x / B : 0, b = worker ? (int)blockIdx.x % B : 0;
+  const int s0 = P.sbeg[d] + b, i0 = P.beg1[d] + b;
+  const bool has_s = worker && P.sitems != nullptr && s0 < P.sbeg[d + 1];
+  const bool has_i = worker && i0 < P.beg1[d + 1];
+  StageItem si{};
+  Item it1{};
+  if (has_s) si = P.sitems[s0];
+  if (has_i) it1 = P.items1[i0];
+  const uint64_t e = run_wait_epoch(P);
+  uint2 first8 = make_uint2(0, 0);
+  uint4 firsts = make_uint4(0, 0, 0, 0);
+  if (has_s) {
+    if (ENC == ENC_LL8) first8 = ll8_stage_first(P, si);
+    if (ENC == ENC_SENT) firsts = sent_stage_first(P, si);
+  }
+  run_arrive(P, e);
+  if (!worker) {
     late_producer<ENC>(P, e, ((int)blockIdx.x - workers) % P.nranks, workers);
     finish_run(P, e);
     return;
   }
-  const int d = blockIdx.x / B, b = blockIdx.x % B;
-  if (P.sitems != nullptr)
-    for (int i = P.sbeg[d] + b; i < P.sbeg[d + 1]; i += B)
-      stage_item<ENC, true>(P, P.sitems[i], e);
+  if (has_s) {
+    if (ENC == ENC_LL8)
+      ll8_stage_tile(P, si, e, true, first8);
+    else if (ENC == ENC_SENT)
+      sent_stage_tile(P, si, e, true, firsts);
+    else
+      stage_item<ENC, true>(P, si, e);
+    for (int i = s0 + B; i < P.sbeg[d + 1]; i += B) stage_item<ENC, true>(P, P.sitems[i], e);
+  }
   if (threadIdx.x == 0) atomicAdd(&header(P.ws)->started[e & 1], 1u);
-  for (int i = P.beg1[d] + b; i < P.beg1[d + 1]; i += B) {
-    if (aborted(P.ws)) break;
-    consume_item<ENC, true>(P, P.P, P.items1[i], e);
+  const uint32_t seen = early_arrivals(P);
+  if (has_i && !aborted(P.ws)) {
+    consume_item<ENC, true>(P, P.P, it1, e);
+    for (int i = i0 + B; i < P.beg1[d + 1]; i += B) {
+      if (aborted(P.ws)) break;
+      consume_item<ENC, true>(P, P.P, P.items1[i], e);
+    }
   }
   if (P.items2 != nullptr)
     for (int i = P.beg2[d] + b; i < P.beg2[d + 1]; i += B) {
       if (aborted(P.ws)) break;
       consume_item<ENC, true>(P, P.AG, P.items2[i], e);
     }
-  finish_run(P, e);
+  finish_run(P, e, seen);
 }
 
 // Overwrite the listed lines of rank `stage_rank`'s image with stale

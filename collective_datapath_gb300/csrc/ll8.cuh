@@ -110,8 +110,18 @@ constexpr int kGroupsInFlight = 4;
 // covers 512 contiguous bytes (16 fully written sectors).
 constexpr int kPairsInFlight = 8;
 
+// The first input pair this thread stages from a tile (pair threadIdx.x):
+// a one-launch run loads it while the epoch is still in flight and hands it
+// to ll8_stage_tile as `first` (with have_first).
+__device__ __forceinline__ uint2 ll8_stage_first(const RunParams& P, const StageItem& it) {
+  return threadIdx.x < it.nlines / 2
+             ? ld_stream_v2(P.in[it.rank] + it.in_elem + 4 * (size_t)threadIdx.x)
+             : make_uint2(0, 0);
+}
+
 __device__ __forceinline__ void ll8_stage_tile(const RunParams& P, const StageItem& it,
-                                               uint64_t epoch) {
+                                               uint64_t epoch, bool have_first = false,
+                                               uint2 first = make_uint2(0, 0)) {
   const uint16_t* in = P.in[it.rank] + it.in_elem;
   uint64_t* img = image_lines(P, P.P, epoch, it.rank) + it.dst_line;
   // Deferred re-arm: the same lines of the other slot were consumed by the
@@ -125,8 +135,9 @@ __device__ __forceinline__ void ll8_stage_tile(const RunParams& P, const StageIt
 #pragma unroll
     for (int j = 0; j < kPairsInFlight; ++j) {
       const uint32_t q = q0 + j * blockDim.x;
-      if (q < npairs) v[j] = ld_stream_v2(in + 4 * (size_t)q);
+      if (q < npairs) v[j] = (j == 0 && have_first) ? first : ld_stream_v2(in + 4 * (size_t)q);
     }
+    have_first = false;  // it held the first batch's pair only
 #pragma unroll
     for (int j = 0; j < kPairsInFlight; ++j) {
       const uint32_t q = q0 + j * blockDim.x;

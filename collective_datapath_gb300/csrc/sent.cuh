@@ -69,11 +69,21 @@ static __device__ __noinline__ bool sent_wait_pair(const RunParams& P, const uin
   }
 }
 
+// The first input group this thread stages from a tile (group threadIdx.x):
+// a one-launch run loads it while the epoch is still in flight and hands it
+// to sent_stage_tile as `first` (with have_first).
+__device__ __forceinline__ uint4 sent_stage_first(const RunParams& P, const StageItem& it) {
+  return threadIdx.x < it.nlines / kSentGroupLines
+             ? ld_stream_v4(P.in[it.rank] + it.in_elem + 8 * (size_t)threadIdx.x)
+             : make_uint4(0, 0, 0, 0);
+}
+
 // Encode one staging tile (nlines is even: segments hold multiples of 8
 // elements).  Deferred re-arm writes the pattern over the same packs of the
 // other slot, which the completed previous run consumed.
 __device__ __forceinline__ void sent_stage_tile(const RunParams& P, const StageItem& it,
-                                                uint64_t epoch) {
+                                                uint64_t epoch, bool have_first = false,
+                                                uint4 first = make_uint4(0, 0, 0, 0)) {
   const uint16_t* in = P.in[it.rank] + it.in_elem;
   uint64_t* img = image_lines(P, P.P, epoch, it.rank) + it.dst_line;
   const bool deferred = P.reset_mode == kResetDeferred;
@@ -84,8 +94,9 @@ __device__ __forceinline__ void sent_stage_tile(const RunParams& P, const StageI
 #pragma unroll
     for (int j = 0; j < kGroupsInFlight; ++j) {
       const uint32_t g = g0 + j * blockDim.x;
-      if (g < ngroups) v[j] = ld_stream_v4(in + 8 * (size_t)g);
+      if (g < ngroups) v[j] = (j == 0 && have_first) ? first : ld_stream_v4(in + 8 * (size_t)g);
     }
+    have_first = false;  // it held the first batch's group only
 #pragma unroll
     for (int j = 0; j < kGroupsInFlight; ++j) {
       const uint32_t g = g0 + j * blockDim.x;
@@ -156,13 +167,33 @@ __device__ __forceinline__ void sent_consume_item(const RunParams& P, const Regi
 #pragma unroll
       for (int p = 0; p < kMaxRanks; ++p)
         if (p < n) ld_relaxed_v2u64(image_lines(P, R, epoch, p) + line, lo[p], hi[p]);
+      uint32_t missing = 0;
 #pragma unroll
       for (int p = 0; p < kMaxRanks; ++p)
-        if (p < n && (lo[p] == kSentPack || hi[p] == kSentPack)) {
-          const uint64_t* src = image_lines(P, R, epoch, p) + line;
-          ok = ok && sent_wait_pair(P, src, p, (int64_t)line);
-          ld_relaxed_v2u64(src, lo[p], hi[p]);
+        if (p < n && (lo[p] == kSentPack || hi[p] == kSentPack)) missing |= 1u << p;
+      if (missing != 0u) {
+        // Re-poll the missing ranks' pairs together (bounded) and keep what
+        // the poll read: a pack that is no longer the pattern holds its
+        // final data, as its 8 bytes are one single-copy-atomic element.
+        count_rejection(P.ws);
+        Waiter w;
+        while (missing != 0u) {
+          if (w.expired(P.ws, P.timeout_ns)) {
+            latch_error(P.ws, kStatusTimeout, __ffs(missing) - 1, (int64_t)line);
+            ok = false;
+            break;
+          }
+          __nanosleep(32);
+#pragma unroll
+          for (int p = 0; p < kMaxRanks; ++p)
+            if ((missing >> p) & 1u)
+              ld_relaxed_v2u64(image_lines(P, R, epoch, p) + line, lo[p], hi[p]);
+#pragma unroll
+          for (int p = 0; p < kMaxRanks; ++p)
+            if (((missing >> p) & 1u) && lo[p] != kSentPack && hi[p] != kSentPack)
+              missing &= ~(1u << p);
         }
+      }
       if (!ok) break;
       const uint4 res = sent_fold8(lo, hi, n, P.dtype);
       if (sole) {
