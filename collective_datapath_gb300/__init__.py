@@ -45,7 +45,7 @@ EXPORTS = [
     "coll_get_rejections", "coll_debug_items", "coll_debug_plan",
     "coll_set_profile_events", "coll_last_launches", "coll_launch_floor",
     "coll_allreduce_static",
-    "coll_atom_copy", "coll_destroy", "coll_status_string",
+    "coll_atom_copy", "coll_copy_passes", "coll_destroy", "coll_status_string",
 ]
 
 
@@ -102,6 +102,7 @@ _sig("coll_launch_floor", _st, _vp, _vp)
 _sig("coll_allreduce_static", _st, ctypes.c_int, _sz, _P(_vp), _P(_vp), _vp)
 _sig("coll_atom_copy", _st, _vp, _vp, _sz, ctypes.c_int, ctypes.c_int, ctypes.c_int,
      ctypes.c_int, _vp, _vp)
+_sig("coll_copy_passes", _st, _vp, _vp, _sz, ctypes.c_int, ctypes.c_int, _vp)
 _sig("coll_destroy", _st, _vp)
 _sig("coll_status_string", ctypes.c_char_p, ctypes.c_int)
 
@@ -325,6 +326,13 @@ def coll_atom_copy(dst, src, nbytes: int, engine: int = COLL_ATOM_BULK, ctas: in
     `ctas` CTAs of `stages` pipeline stages of `stage_bytes` each."""
     _check(_lib.coll_atom_copy(_ptr(dst), _ptr(src), nbytes, engine, ctas, stages, stage_bytes,
                                _ptr(status), _stream_handle(stream)), "coll_atom_copy")
+
+
+def coll_copy_passes(dst, src, nbytes: int, passes: int, ctas: int = 0, stream=None) -> None:
+    """`passes` copies of `nbytes` from `src` to `dst` in one launch (a copy
+    ceiling probe: buffers that fit L2 give the SM <-> L2 copy rate)."""
+    _check(_lib.coll_copy_passes(_ptr(dst), _ptr(src), nbytes, passes, ctas,
+                                 _stream_handle(stream)), "coll_copy_passes")
 
 
 def coll_destroy(spec: int) -> None:

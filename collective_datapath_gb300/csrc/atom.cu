@@ -191,9 +191,44 @@ cudaError_t launch_atom_copy(void* dst, const void* src, uint64_t bytes, int eng
   }
 }
 
+// Copy ceiling probe: `passes` full copies of src -> dst in one launch with
+// grid-stride 16-byte accesses (loads cached in L2 only), so that buffers
+// that fit L2 measure the SM <-> L2 copy throughput with no launch gaps
+// between passes.
+__global__ void __launch_bounds__(256) k_copy_passes(uint4* dst, const uint4* src, uint64_t n16,
+                                                     int passes) {
+  const uint64_t stride = (uint64_t)gridDim.x * blockDim.x;
+  for (int p = 0; p < passes; ++p)
+    for (uint64_t i = blockIdx.x * (uint64_t)blockDim.x + threadIdx.x; i < n16; i += stride) {
+      uint4 v;
+      asm volatile("ld.global.cg.v4.u32 {%0, %1, %2, %3}, [%4];"
+                   : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                   : "l"(src + i));
+      asm volatile("st.global.v4.u32 [%0], {%1, %2, %3, %4};" ::"l"(dst + i), "r"(v.x),
+                   "r"(v.y), "r"(v.z), "r"(v.w)
+                   : "memory");
+    }
+}
+
 }  // namespace coll
 
 using namespace coll;
+
+extern "C" coll_status_t coll_copy_passes(void* dev_dst, const void* dev_src, size_t bytes,
+                                          int passes, int ctas, coll_stream_t stream) {
+  if (passes < 1 || passes > 65535 || ctas < 0 || ctas > 65535) return COLL_ERR_INVALID;
+  if (bytes % 16 != 0) return COLL_ERR_ALIGN;
+  if (bytes == 0) return COLL_OK;
+  if (dev_dst == nullptr || dev_src == nullptr) return COLL_ERR_INVALID;
+  const uintptr_t d = reinterpret_cast<uintptr_t>(dev_dst);
+  const uintptr_t s = reinterpret_cast<uintptr_t>(dev_src);
+  if ((d | s) & 15u) return COLL_ERR_ALIGN;
+  if (d < s + bytes && s < d + bytes) return COLL_ERR_INVALID;  // overlapping ranges
+  if (ctas == 0) ctas = 8 * device_sms();
+  k_copy_passes<<<ctas, 256, 0, static_cast<cudaStream_t>(stream)>>>(
+      static_cast<uint4*>(dev_dst), static_cast<const uint4*>(dev_src), bytes / 16, passes);
+  return cudaGetLastError() == cudaSuccess ? COLL_OK : COLL_ERR_CUDA;
+}
 
 extern "C" coll_status_t coll_atom_copy(void* dev_dst, const void* dev_src, size_t bytes,
                                         int engine, int ctas, int stages, int stage_bytes,

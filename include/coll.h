@@ -457,6 +457,19 @@ coll_status_t coll_atom_copy(void *dev_dst, const void *dev_src, size_t bytes, i
                              int ctas, int stages, int stage_bytes, int32_t *dev_status,
                              coll_stream_t stream);
 
+/* Copy ceiling probe, for measurement: `passes` full copies of
+ * dev_src[0 .. bytes) into dev_dst in ONE launch, with `ctas` CTAs of 256
+ * threads (0 = eight per SM) moving 16-byte granules grid-stride; loads are
+ * cached in L2 only.  With both buffers small enough to stay in L2 it gives
+ * the SM <-> L2 copy throughput this GPU reaches (read + write bytes =
+ * 2 * bytes * passes over the launch's time) without the launch gaps a loop
+ * of short copies would measure.  Both pointers are device addresses of this
+ * GPU, 16-byte aligned, not overlapping; bytes a multiple of 16 (0 = no
+ * launch).  Out-of-range arguments or overlapping ranges return
+ * COLL_ERR_INVALID, misalignment COLL_ERR_ALIGN; asynchronous on `stream`. */
+coll_status_t coll_copy_passes(void *dev_dst, const void *dev_src, size_t bytes, int passes,
+                               int ctas, coll_stream_t stream);
+
 /* Release the spec's host state (never the caller's device memory). */
 coll_status_t coll_destroy(coll_spec_t *spec);
 

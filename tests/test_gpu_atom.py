@@ -120,3 +120,40 @@ def test_atom_copy_256mib_full_size(cd, engine, ctas):
         del dst
     del src
     torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("nbytes,passes,ctas", [(16, 1, 1), (4096 + 48, 3, 0), (1 << 20, 2, 7)])
+def test_copy_passes_probe_copies_every_byte(cd, nbytes, passes, ctas):
+    """The copy ceiling probe (several copies in one launch) leaves the
+    destination equal to the source, byte for byte (the oracle's copy), and
+    the bytes past it untouched."""
+    import torch
+
+    host = synth.random_bits32(11, (nbytes + 3) // 4, nbytes, passes)
+    src = torch.from_numpy(host.view(np.int32)).cuda()
+    dst = torch.full(((nbytes + GUARD) // 4,), 0x5A5A5A5A, dtype=torch.int32, device="cuda")
+    cd.coll_copy_passes(dst, src, nbytes, passes, ctas=ctas)
+    torch.cuda.synchronize()
+    got = dst.cpu().numpy().view(np.uint8)
+    want = oracle.one_sided_copy(host.view(np.uint8)[:nbytes])
+    assert np.array_equal(got[:nbytes], want)
+    assert np.all(got[nbytes:].view(np.uint32) == 0x5A5A5A5A)
+
+
+def test_copy_passes_probe_rejects_bad_arguments(cd):
+    import ctypes
+
+    import torch
+
+    lib = ctypes.CDLL(cd.library_path())
+    fn = lib.coll_copy_passes
+    fn.restype = ctypes.c_int
+    fn.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int, ctypes.c_int,
+                   ctypes.c_void_p]
+    a = torch.zeros(64, dtype=torch.int32, device="cuda")
+    b = torch.zeros(64, dtype=torch.int32, device="cuda")
+    assert fn(b.data_ptr(), a.data_ptr(), 256, 0, 0, None) == cd.COLL_ERR_INVALID    # passes
+    assert fn(b.data_ptr(), a.data_ptr(), 24, 1, 0, None) == cd.COLL_ERR_ALIGN       # size
+    assert fn(b.data_ptr() + 4, a.data_ptr(), 64, 1, 0, None) == cd.COLL_ERR_ALIGN   # pointer
+    assert fn(a.data_ptr() + 16, a.data_ptr(), 64, 1, 0, None) == cd.COLL_ERR_INVALID  # overlap
+    assert fn(b.data_ptr(), a.data_ptr(), 0, 1, 0, None) == cd.COLL_OK              # nothing
