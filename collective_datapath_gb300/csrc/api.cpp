@@ -104,8 +104,10 @@ void fill_base(coll_spec* s) {
     M.rows_dest = reinterpret_cast<uint32_t*>(s->ws + p.off_rows_dest);
     M.counts_out = reinterpret_cast<int32_t*>(s->ws + p.off_counts_out);
     M.flag_stage = reinterpret_cast<uint64_t*>(s->ws + p.off_moe_flags);
-    M.lag = 6;
-    if (const char* env = std::getenv("COLL_MOE_LAG")) M.lag = std::max(1, std::atoi(env));
+    // composed dispatch: by columns (lag 0), or the queue of stage and copy
+    // tasks with this lag in blocks (COLL_MOE_LAG, measurement runs)
+    M.lag = 0;
+    if (const char* env = std::getenv("COLL_MOE_LAG")) M.lag = std::max(0, std::atoi(env));
     P.sitems = nullptr;
     P.items1 = nullptr;
   }

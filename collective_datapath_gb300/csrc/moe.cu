@@ -27,8 +27,12 @@
 //  k_moe_copy     one warp per staged row: validate its LL128 lines through a
 //                 cp.async ring and unpack them into each of the token's
 //                 output rows on that destination (one per choice there)
-//  k_moe_composed the stage and copy steps as tasks of one launch (after the
-//                 routing kernels), staged rows read back mostly from L2
+//  k_moe_column   the stage and copy steps in one launch (after the routing
+//                 kernels) by columns: one CTA stages a source's token
+//                 sub-block and copies those rows into their destinations,
+//                 so staged rows are read back from L2 and dropped there
+//  k_moe_composed the same launch as a queue of stage and copy tasks with a
+//                 lag (selected with COLL_MOE_LAG, measurement runs)
 #include <cuda_runtime.h>
 
 #include "launch.h"
@@ -564,6 +568,145 @@ __global__ void __launch_bounds__(kMcWarps * 32, 3) k_moe_composed(RunParams P) 
   finish_run(P, e);
 }
 
+// ---- dispatch by columns -----------------------------------------------------------
+// A column is (source p, one sub-block of kMoeSubTokens tokens), and one CTA
+// runs all of it: thread 0 loads the sub-block's token rows into shared
+// memory with TMA; the warps stage one LL128 row per (token, destination
+// holding one of its experts) -- source p's stage -- and, after a CTA
+// barrier, copy each staged row, validated, into every output row of its
+// token on that destination -- destination d's copy of what p sent it --
+// dropping the staged lines from L2 once read.  The next column's rows load
+// while the current one is copied.  CTAs take columns from one counter and
+// never wait for each other, and a staged row is read back a few
+// microseconds after it was written, by the same SM, before L2 writes it
+// back.
+__global__ void __launch_bounds__(kMcWarps * 32, 3) k_moe_column(RunParams P) {
+  extern __shared__ __align__(128) char smem[];
+  __shared__ __align__(8) uint64_t mbar[kMoeSubTokens];
+  __shared__ int s_col[2], s_ok;
+  const uint64_t e = begin_run(P);
+  const MoeParams& M = P.moe;
+  WsHeader* h = header(P.ws);
+  const int n = P.nranks;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const uint32_t row_bytes = (uint32_t)M.hidden * 2;
+  const uint32_t buf_stride = (row_bytes + 127) / 128 * 128;
+  const uint32_t sbuf = (uint32_t)__cvta_generic_to_shared(smem);
+  const uint32_t sbar = (uint32_t)__cvta_generic_to_shared(mbar);
+  const uint32_t wbase =
+      sbuf + kMoeSubTokens * buf_stride + (uint32_t)(warp * kMcRing * kRowBytes);
+  const int slot = (int)(e & 1);
+  const int ncols = M.nblocks * kMoeSubs * n;
+  const int nrows_w = (int)(M.row_lines / kLL128RowLines);
+  char* img0 = P.ws + P.P.base + (e & P.P.slot_mask) * P.P.slot_bytes;
+  // column q: source q % n, tokens [t0, t0 + nt) of sub-block q / n
+  auto col_src = [&](int q, int& p, int& t0, int& nt) {
+    p = q % n;
+    t0 = (q / n) * kMoeSubTokens;
+    nt = max(0, min(kMoeSubTokens, M.tokens - t0));
+  };
+  uint32_t uses[kMoeSubTokens] = {};  // thread 0: loads waited for, per buffer
+  int issued = -1;                    // thread 0: the column whose loads are in flight
+  auto load = [&](int q) {            // thread 0
+    int p, t0, nt;
+    col_src(q, p, t0, nt);
+    const uint64_t in_pol = l2_evict_first_policy();  // token rows are read once
+    for (int k = 0; k < nt; ++k) {
+      fence_proxy_async_smem();
+      mbar_expect_tx(sbar + 8 * k, row_bytes);
+      tma_load_1d_hint(sbuf + k * buf_stride, P.in[p] + (size_t)(t0 + k) * M.hidden, row_bytes,
+                       sbar + 8 * k, in_pol);
+    }
+    issued = q;
+  };
+  auto wait_loads = [&](int q) -> bool {  // thread 0, bounded
+    int p, t0, nt;
+    col_src(q, p, t0, nt);
+    bool ok = true;
+    for (int k = 0; k < nt; ++k) {
+      if (!mbar_wait_bounded(sbar + 8 * k, uses[k] & 1, P.timeout_ns)) {
+        latch_error(P.ws, kStatusTimeout, p, (int64_t)(t0 + k));
+        ok = false;
+      }
+      uses[k] += 1;
+    }
+    issued = -1;
+    return ok;
+  };
+  if (threadIdx.x == 0) {
+    for (int k = 0; k < kMoeSubTokens; ++k) mbar_init(sbar + 8 * k, 1);
+    fence_mbarrier_init();
+    s_col[0] = (int)atomicAdd(&h->task_next[slot], 1u);
+    s_ok = 1;
+    if (s_col[0] < ncols) load(s_col[0]);
+  }
+  __syncthreads();
+  for (int it = 0;; ++it) {
+    const int q = s_col[it & 1];
+    if (q >= ncols) break;
+    int p, t0, nt;
+    col_src(q, p, t0, nt);
+    if (threadIdx.x == 0 && !wait_loads(q)) s_ok = 0;
+    __syncthreads();
+    if (!s_ok) break;
+    // stage: the sub-block's rows, one per (token, destination with a choice
+    // of it); lane j of every warp looks up pair j, warp w writes the parts
+    // w, w + kMcWarps, ... of the list
+    static_assert(kMoeSubTokens * kMaxRanks <= 32, "a lane per (token, destination)");
+    char* img = img0 + (uint64_t)p * P.P.rank_bytes;
+    int64_t srow = -1;
+    if (lane < nt * n) srow = moe_staged_row(M, n, p, t0 + lane / n, lane % n);
+    const uint32_t real = __ballot_sync(0xFFFFFFFFu, srow >= 0);
+    {
+      uint32_t m = real;
+      for (int i = 0; m; ++i, m &= m - 1) {
+        const int j = __ffs(m) - 1;
+        const int64_t sr = __shfl_sync(0xFFFFFFFFu, srow, j);
+        for (int part = 0; part < kMcSplit; ++part)
+          if ((i * kMcSplit + part) % kMcWarps == warp)
+            moe_write_row(img + (uint64_t)sr * M.row_lines * kLL128LineBytes,
+                          sbuf + (j / n) * buf_stride, row_bytes, part * nrows_w / kMcSplit,
+                          (part + 1) * nrows_w / kMcSplit, lane, e);
+      }
+    }
+    // the staged rows are written (the barrier orders them before the
+    // copies' loads at CTA scope) and the row buffers are free again
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      const int qn = aborted(P.ws) ? ncols : (int)atomicAdd(&h->task_next[slot], 1u);
+      s_col[(it + 1) & 1] = qn;
+      if (qn < ncols) load(qn);
+    }
+    // copy: every staged row into its token's output rows on its destination
+    {
+      uint32_t m = real;
+      for (int i = 0; m; ++i, m &= m - 1) {
+        const int j = __ffs(m) - 1;
+        const int64_t sr = __shfl_sync(0xFFFFFFFFu, srow, j);
+        const int t = t0 + j / n, d = j % n;
+        bool any = false;
+        for (int part = 0; part < kMcSplit; ++part)
+          any = any || (i * kMcSplit + part) % kMcWarps == warp;
+        if (!any) continue;
+        const MoeFan f = moe_dest_rows(M, n, p, t, d, lane);
+        const char* src = img + (uint64_t)sr * M.row_lines * kLL128LineBytes;
+        for (int part = 0; part < kMcSplit; ++part)
+          if ((i * kMcSplit + part) % kMcWarps == warp &&
+              !moe_copy_row<kMcRing>(P, src, sr * M.row_lines, p, P.out[d],
+                                     part * nrows_w / kMcSplit, (part + 1) * nrows_w / kMcSplit,
+                                     f, wbase, lane, e, true))
+            s_ok = 0;
+      }
+    }
+    __syncthreads();  // s_col and s_ok are final
+    if (!s_ok) break;
+  }
+  // a column whose rows were requested but that this CTA leaves unprocessed
+  // (after an error): wait (bounded) for its loads before the CTA exits
+  if (threadIdx.x == 0 && issued >= 0) wait_loads(issued);
+  finish_run(P, e);
+}
+
 // ---- launchers ------------------------------------------------------------------
 
 cudaError_t launch_moe_stage_all(const RunParams& P, cudaStream_t s) {
@@ -603,10 +746,12 @@ cudaError_t launch_moe_routing(const RunParams& P, cudaStream_t s) {
 
 cudaError_t launch_moe_composed(const RunParams& P, cudaStream_t s) {
   const size_t bytes = moe_composed_smem_bytes(P.moe.hidden);
-  static size_t memo[kMaxDevices];
-  if (cudaError_t e = raise_smem_limit(k_moe_composed, bytes, memo)) return e;
+  const bool columns = P.moe.lag <= 0;
+  auto* kernel = columns ? k_moe_column : k_moe_composed;
+  static size_t memo[2][kMaxDevices];
+  if (cudaError_t e = raise_smem_limit(kernel, bytes, memo[columns ? 1 : 0])) return e;
   int per_sm = 0;
-  if (cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_moe_composed,
+  if (cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel,
                                                                     kMcWarps * 32, bytes))
     return e;
   if (per_sm < 1) return cudaErrorInvalidConfiguration;
@@ -620,7 +765,7 @@ cudaError_t launch_moe_composed(const RunParams& P, cudaStream_t s) {
   attr[0].val.cooperative = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, k_moe_composed, P);
+  return cudaLaunchKernelEx(&cfg, kernel, P);
 }
 
 cudaError_t launch_moe_consume(const RunParams& P, cudaStream_t s) {

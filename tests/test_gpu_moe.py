@@ -46,7 +46,7 @@ def counts_of(cd, coll, n, experts):
     return c[:n * el * n].reshape(n, el, n), c[n * el * n:]
 
 
-@pytest.mark.parametrize("path", [2, 3])
+@pytest.mark.parametrize("path", [2, 3, "3q"])
 @pytest.mark.parametrize("n,tokens,hidden,k,experts,staged", [
     (4, 300, 64, 3, 16, False),
     (2, 128, 136, 2, 4, True),
@@ -61,12 +61,16 @@ def counts_of(cd, coll, n, experts):
     (2, 90, 120, 20, 64, True),
 ])
 def test_moe_dispatch_small_cases_match_the_oracle(cd, n, tokens, hidden, k, experts, staged,
-                                                   path):
+                                                   path, monkeypatch):
     """Both launch forms: routing, stage and copy launches (2), and routing
-    plus one launch of stage and copy tasks (3); staged runs take the first
-    form's copy."""
+    plus one launch (3) of columns (a source's token sub-block staged and
+    copied by one CTA) or, "3q", of the queue of stage and copy tasks with a
+    lag of 6 blocks; staged runs take the first form's copy."""
     import torch
 
+    if path == "3q":
+        monkeypatch.setenv("COLL_MOE_LAG", "6")
+        path = 3
     coll = make_moe(cd, n, tokens, hidden, k, experts, path=path)
     xs = [synth.normal_bf16(5, tokens * hidden, n, r).reshape(tokens, hidden) for r in range(n)]
     tk = [synth.topk_experts(5, tokens, k, experts, n, r) for r in range(n)]

@@ -233,12 +233,14 @@ def test_graph_replay_advances_epoch_on_device(cd, enc):
 
 @pytest.mark.parametrize("n,count", [(8, 8 * 1000), (8, 8 * 60 * 1024 + 64), (3, 3000),
                                      (2, 2 * 4096), (8, 8 * 60 * 300)])
-@pytest.mark.parametrize("shape", [None, "16,1,1", "64,3,0", "32,40,1", "256,8,1", "64,4,1,1", "16,2,0,1", "32,4,1,2", "128,6,2,2"])
+@pytest.mark.parametrize("shape", [None, "16,1,1", "64,3,0", "32,40,1", "256,8,1", "64,4,1,1", "16,2,0,1", "32,4,1,2", "128,6,2,2",
+                                   "64,3,0,0,-1,1", "32,40,1,0,-1,1", "64,4,1,1,-1,1", "128,6,2,2,-1,1"])
 def test_composed_twoshot_matches_the_oracle(cd, n, count, shape, monkeypatch):
-    """The one-launch twoshot (a queue of stage / fold / gather tasks per
-    chunk): bit-exact against the oracle over several epochs, for several
-    chunk sizes and queue lags, with and without dropping consumed lines
-    from L2."""
+    """The one-launch twoshot: bit-exact against the oracle over several
+    epochs, scheduled by columns (the default) for several chunk sizes and
+    launch shapes, and (sixth field 1) as the queue of stage / fold / gather
+    tasks per chunk with several lags; with and without dropping consumed
+    lines from L2."""
     if shape is not None:
         monkeypatch.setenv("COLL_COMPOSED_SHAPE", shape)
     coll = make(cd, cd.ALLREDUCE, n, count, encoding=cd.COLL_LL128,
@@ -255,7 +257,8 @@ def test_composed_twoshot_matches_the_oracle(cd, n, count, shape, monkeypatch):
 
 @pytest.mark.parametrize("n,count", [(8, 8 * 60 * 1024 + 64), (3, 3000), (8, 24), (2, 2 * 4096),
                                      (8, 8 * 60 * 300)])
-@pytest.mark.parametrize("shape", [None, "16,1,1", "64,3,0", "32,5,1,2", "128,40,1,1"])
+@pytest.mark.parametrize("shape", [None, "16,1,1", "64,3,0", "32,5,1,2", "128,40,1,1", "16,1,1,0,-1,1",
+                                   "128,40,1,1,-1,1"])
 def test_composed_all_gather(cd, n, count, shape, monkeypatch):
     """The one-launch all-gather: each source stages its packed segment, each
     destination copies every source's chunk (the N-th copy drops the staged
@@ -279,15 +282,18 @@ def test_composed_all_gather(cd, n, count, shape, monkeypatch):
                                           ("REDUCE_SCATTER", 8, 8 * 60 * 1024 + 64),
                                           ("ALLTOALL", 8, 8 * 60 * 512), ("ALLTOALL", 4, 4 * 1000)])
 @pytest.mark.parametrize("min_chunk_slots,shape", [(2, "16,1,1"), (3, "16,2,1"), (5, "64,40,1"),
-                                                   (4, "32,3,0"), (9, None), (40, "16,8,1,2")])
+                                                   (4, "32,3,0"), (9, None), (40, "16,8,1,2"),
+                                                   (3, "16,2,1,0,-1,1"), (9, "64,40,1,0,-1,1")])
 def test_composed_cycling_staging(cd, name, n, count, min_chunk_slots, shape, monkeypatch):
     """Purlin §4.1 bounded staging: each rank's staging image holds only a few
-    chunk slots (min_chunk_slots of the 16-line chunk) and chunks cycle through
-    them -- a stage waits for the readers of its slot's previous chunk, a fold
-    for the gathers of its published slot's previous chunk.  Staged lines of
-    chunk c carry epoch + c (§4.2).  Bit-exact over several epochs, every run
-    advances the epoch by an odd step, and stale lines from the previous
-    cycles and runs are never taken."""
+    chunk slots (min_chunk_slots of the 16-line chunk).  By columns, each CTA
+    owns a slot and reuses it column after column; in the queue schedule
+    (sixth field 1) chunks cycle through the slots, a stage waiting for the
+    readers of its slot's previous chunk and a fold for the gathers of its
+    published slot's previous chunk.  Lines carry epoch + the column or chunk
+    index (§4.2).  Bit-exact over several epochs, every run advances the epoch
+    by an odd step, and stale lines from the previous cycles and runs are
+    never taken."""
     if shape is not None:
         monkeypatch.setenv("COLL_COMPOSED_SHAPE", shape)
     triple = getattr(cd, name)
@@ -339,7 +345,7 @@ def test_four_rotating_slots(cd, enc, reset, path):
                                           ("REDUCE_SCATTER", 3, 3000), ("REDUCE_SCATTER", 8, 24),
                                           ("ALLTOALL", 8, 8 * 60 * 512), ("ALLTOALL", 4, 4 * 1000),
                                           ("ALLTOALL", 2, 2 * 8)])
-@pytest.mark.parametrize("shape", [None, "16,1,1", "64,3,0", "32,5,1,2"])
+@pytest.mark.parametrize("shape", [None, "16,1,1", "64,3,0", "32,5,1,2", "32,5,1,2,-1,1"])
 def test_composed_reduce_scatter_and_all_to_all(cd, name, n, count, shape, monkeypatch):
     """The one-launch form of reduce-scatter (stage, fold into the outputs)
     and all-to-all (stage, copy), bit-exact over several epochs."""
