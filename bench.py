@@ -588,11 +588,12 @@ def sizes_row(cd, stream, sizes_mib=(32, 128)) -> dict:
     return out
 
 
-def v_row(cd, name, total_bytes, stream, steps=5) -> dict:
+def v_row(cd, name, total_bytes, stream, steps=5, path=None) -> dict:
     """Variable-length collective on a Zipf split (exponent 0.125) of a total
-    of `total_bytes` over 8 ranks, LL128 lines, streamed path.  all-to-all V
-    rotates each source's split right by (source + 1).  `algbw` is the
-    total T over the time, as the variable-length experiment reports it."""
+    of `total_bytes` over 8 ranks, LL128 lines, the composed launch by
+    columns (or `path`).  all-to-all V rotates each source's split right by
+    (source + 1).  `algbw` is the total T over the time, as the
+    variable-length experiment reports it."""
     import torch
 
     import synth
@@ -605,7 +606,7 @@ def v_row(cd, name, total_bytes, stream, steps=5) -> dict:
     else:
         v, count = base, sum(base)
     coll = cd.Collective(getattr(cd, name), n, count, encoding=cd.COLL_LL128,
-                         path=cd.COLL_PATH_STREAMED, vcounts=v)
+                         path=cd.COLL_PATH_COMPOSED if path is None else path, vcounts=v)
     ins = make_inputs(max(max(coll.elems(r)[0] for r in range(n)), 8), 12)
     ins = [x[:coll.elems(r)[0]] for r, x in enumerate(ins)]
     outs = [torch.empty(max(coll.elems(r)[1], 8), dtype=torch.int16, device="cuda")
@@ -988,7 +989,8 @@ def main() -> int:
     ap.add_argument("--row", default=None,
                     help="run one extra row alone and print it (profiling runs): "
                          "moe, moe_streamed, rs, rs_composed, ag, a2a, a2a_composed, "
-                         "sentinel, f32, staging16, sizes, rsv, agv, a2av, hbm_reference")
+                         "sentinel, f32, staging16, sizes, rsv, agv, a2av (and their _streamed "
+                         "forms), hbm_reference")
     ap.add_argument("--staging-mib", type=int, default=16,
                     help="staging MiB per rank of the bounded-staging row run alone")
     ap.add_argument("--moe-tokens", type=int, default=4096,
@@ -1053,6 +1055,12 @@ def main() -> int:
             "rsv": lambda: v_row(cd, "REDUCE_SCATTER_V", args.mib << 20, stream),
             "agv": lambda: v_row(cd, "ALLGATHER_V", args.mib << 20, stream),
             "a2av": lambda: v_row(cd, "ALLTOALL_V", args.mib << 20, stream),
+            "rsv_streamed": lambda: v_row(cd, "REDUCE_SCATTER_V", args.mib << 20, stream,
+                                          path=cd.COLL_PATH_STREAMED),
+            "agv_streamed": lambda: v_row(cd, "ALLGATHER_V", args.mib << 20, stream,
+                                          path=cd.COLL_PATH_STREAMED),
+            "a2av_streamed": lambda: v_row(cd, "ALLTOALL_V", args.mib << 20, stream,
+                                           path=cd.COLL_PATH_STREAMED),
             "hbm_reference": lambda: hbm_reference_row(stream),
         }
         if args.row not in rows:

@@ -175,8 +175,12 @@ ComposedParams composed_shape(const coll_spec* s) {
   const bool ar = p.kind == CK_ALLREDUCE;
   int chunk = ar ? 256 : 128, lag = ar ? 28 : 40, discard = 1, variant = 0, lag2 = -1,
       schedule = 0;
+  // the longest partition of any rank image (the all-gathers' sources
+  // differ in length with V sizes)
   uint64_t most = 0;
-  for (const Seg& sg : p.pseg[0]) most = std::max<uint64_t>(most, sg.lines);
+  for (int r = 0; r < p.n; ++r)
+    for (const Seg& sg : p.pseg[r]) most = std::max<uint64_t>(most, sg.lines);
+  const bool gather = p.kind == CK_ALLGATHER || p.kind == CK_ALLGATHER_V;
   const char* env = std::getenv("COLL_COMPOSED_SHAPE");
   if (env != nullptr)
     std::sscanf(env, "%d,%d,%d,%d,%d,%d", &chunk, &lag, &discard, &variant, &lag2, &schedule);
@@ -185,7 +189,7 @@ ComposedParams composed_shape(const coll_spec* s) {
   q.variant = variant >= 0 && variant <= 2 ? variant : 0;
   if (q.schedule == 0 && env == nullptr) {
     const uint64_t cap = (uint64_t)std::max(1, column_capacity(q.variant));
-    chunk = p.kind == CK_ALLGATHER ? 128 : 64;
+    chunk = gather ? 128 : 64;
     if (p.ring_lines > 0) {
       while (chunk > (int)kComposedMinChunk && p.ring_lines / (uint64_t)chunk < cap) chunk /= 2;
     } else {
@@ -237,14 +241,15 @@ ComposedParams composed_shape(const coll_spec* s) {
     q.lag2 = std::min(q.lag2, std::max(1, (int)q.ring / 2));
   }
   q.discard = discard;
-  q.mode = p.kind == CK_REDUCE_SCATTER ? 1
-           : p.kind == CK_ALLTOALL      ? 2
-           : p.kind == CK_ALLGATHER     ? 3
-                                        : 0;
+  q.mode = p.kind == CK_REDUCE_SCATTER || p.kind == CK_REDUCE_SCATTER_V ? 1
+           : p.kind == CK_ALLTOALL || p.kind == CK_ALLTOALL_V            ? 2
+           : gather                                                      ? 3
+                                                                         : 0;
   char* f = s->ws + p.off_cflags;
   q.flag_stage = reinterpret_cast<uint64_t*>(f);
   q.flag_fold = q.flag_stage + p.composed_max_chunks * p.n;
   q.gather_cnt = q.flag_fold + p.composed_max_chunks * p.n;
+  q.exch = p.exch.empty() ? nullptr : reinterpret_cast<const ExchPiece*>(s->ws + p.off_exch);
   return q;
 }
 
@@ -416,6 +421,11 @@ coll_status_t coll_bind(coll_spec_t* s, void* dev_workspace, size_t bytes,
                                         p.items2.size() * sizeof(Item),
                                         cudaMemcpyHostToDevice, st))
       return cuda_status(e);
+  if (!p.exch.empty())
+    if (cudaError_t e = cudaMemcpyAsync(s->ws + p.off_exch, p.exch.data(),
+                                        p.exch.size() * sizeof(ExchPiece),
+                                        cudaMemcpyHostToDevice, st))
+      return cuda_status(e);
   if (cudaError_t e = cudaStreamSynchronize(st)) return cuda_status(e);
   fill_base(s);
   s->bound = true;
@@ -491,12 +501,24 @@ coll_status_t coll_run(coll_spec_t* s, const void* const* dev_ins, void* const* 
   if (dev_ins != nullptr && p.path == COLL_PATH_COMPOSED && !empty) {
     P.cp = composed_shape(s);
     if (P.cp.mode == 3) {
-      // all-gather: each source stages its own packed segment; the kernel
-      // takes source k's segment and its offset in the gathered output
+      // all-gather (V): each source stages its own packed segment; the
+      // kernel takes source k's segment and its offset in the gathered
+      // output, the sum of the earlier sources' lengths
+      uint64_t at = 0;
       for (int k = 0; k < p.n; ++k) {
         P.seg_line0[k] = p.pseg[k][0].line0;
         P.seg_elems[k] = p.pseg[k][0].elems;
-        P.seg_in0[k] = p.shard * (uint64_t)k;
+        P.seg_in0[k] = at;
+        at += p.pseg[k][0].elems;
+      }
+    } else if (P.cp.mode == 2) {
+      // all-to-all (V): the pieces come from the exchange table; column x
+      // spans the longest source's partition x
+      if (P.cp.schedule != 0 && p.kind == CK_ALLTOALL_V) return COLL_ERR_UNSUPPORTED;
+      for (int x = 0; x < p.n; ++x) {
+        uint64_t most = 0;
+        for (int q = 0; q < p.n; ++q) most = std::max<uint64_t>(most, p.pseg[q][x].elems);
+        P.seg_elems[x] = most;
       }
     }
     if (P.cp.schedule == 0) {
@@ -688,8 +710,19 @@ coll_status_t coll_run_late(coll_spec_t* s, const void* const* dev_ins, void* co
 
 coll_status_t coll_debug_items(const coll_spec_t* s, int which, int64_t* buf, size_t cap,
                                size_t* n) {
-  if (s == nullptr || n == nullptr || which < 0 || which > 2) return COLL_ERR_INVALID;
+  if (s == nullptr || n == nullptr || which < 0 || which > 3) return COLL_ERR_INVALID;
   const Plan& p = s->plan;
+  if (which == 3) {
+    *n = p.exch.size();
+    for (size_t i = 0; i < p.exch.size() && i < cap && buf; ++i) {
+      const ExchPiece& x = p.exch[i];
+      int64_t* o = buf + 10 * i;
+      o[0] = (int64_t)(i / p.n); o[1] = (int64_t)(i % p.n);
+      o[2] = (int64_t)x.line0; o[3] = (int64_t)x.elems; o[4] = (int64_t)x.in0;
+      o[5] = (int64_t)x.out0; o[6] = o[7] = o[8] = o[9] = 0;
+    }
+    return COLL_OK;
+  }
   if (which == 0) {
     *n = p.sitems.size();
     for (size_t i = 0; i < p.sitems.size() && i < cap && buf; ++i) {

@@ -300,6 +300,21 @@ __device__ __forceinline__ int seg_lines(const RunParams& P, int k) {
   return (int)((P.seg_elems[k] + kLL128Elems - 1) / kLL128Elems);
 }
 
+// An all-to-all piece of chunk t0: `elems` units at `plain` (the input of
+// the stage, or the output of the copy), whose lines start at `line` of
+// `image`.  A source partition shorter than the column has fewer lines (or
+// none) in the chunk.
+__device__ __forceinline__ void exch_piece(ColPiece& pc, const uint16_t* plain, char* image,
+                                           uint64_t line, uint64_t elems, uint32_t t0,
+                                           uint32_t CL) {
+  const int64_t lines = (int64_t)((elems + kLL128Elems - 1) / kLL128Elems) - (int64_t)t0;
+  const int64_t bytes = 2 * ((int64_t)elems - (int64_t)t0 * kLL128Elems);
+  pc.plain = const_cast<char*>(reinterpret_cast<const char*>(plain + (uint64_t)t0 * kLL128Elems));
+  pc.lines = image + line * kLL128LineBytes;
+  pc.nl = (int)max((int64_t)0, min((int64_t)CL, lines));
+  pc.left = (int)max((int64_t)0, min((int64_t)CL * (2 * kLL128Elems), bytes));
+}
+
 template <int kW, int kRing, int kMinBlocks, bool kF32>
 __global__ void __launch_bounds__(kW * 32, kMinBlocks) k_column_ll128(RunParams P) {
   extern __shared__ __align__(128) char smem[];
@@ -342,16 +357,29 @@ __global__ void __launch_bounds__(kW * 32, kMinBlocks) k_column_ll128(RunParams 
     const int64_t lx = 2 * ((int64_t)P.seg_elems[x] - (int64_t)t0 * kLL128Elems);
     const int left = (int)(lx < (int64_t)CL * (2 * kLL128Elems) ? lx
                                                                 : (int64_t)CL * (2 * kLL128Elems));
-    // stage: rank p's piece of column x (all-gather: source x's one piece)
+    if (nl == 0) {
+      // partition x is shorter than the longest one (V sizes): nothing to
+      // move in this chunk.  The barrier publishes the next column.
+      __syncthreads();
+      continue;
+    }
+    // stage: rank p's piece of column x (all-gather: source x's one piece;
+    // all-to-all: source p's partition x, whose length is its own)
     const int nstage = Q.mode == 3 ? 1 : n;
     if ((int)threadIdx.x < nstage) {
       const int p = Q.mode == 3 ? x : (int)threadIdx.x;
       ColPiece& pc = s_piece[0][threadIdx.x];
-      pc.plain = const_cast<char*>(reinterpret_cast<const char*>(
-          P.in[p] + (Q.mode == 3 ? 0 : P.seg_in0[x]) + (uint64_t)t0 * kLL128Elems));
-      pc.lines = image_bytes(P, P.P, e, p) + pline * kLL128LineBytes;
-      pc.nl = nl;
-      pc.left = left;
+      if (Q.mode == 2) {
+        const ExchPiece v = Q.exch[p * n + x];
+        exch_piece(pc, P.in[p] + v.in0, image_bytes(P, P.P, e, p), bounded ? pline : v.line0 + t0,
+                   v.elems, t0, CL);
+      } else {
+        pc.plain = const_cast<char*>(reinterpret_cast<const char*>(
+            P.in[p] + (Q.mode == 3 ? 0 : P.seg_in0[x]) + (uint64_t)t0 * kLL128Elems));
+        pc.lines = image_bytes(P, P.P, e, p) + pline * kLL128LineBytes;
+        pc.nl = nl;
+        pc.left = left;
+      }
     }
     __syncthreads();
     col_stage<kW, kRing>(s_piece[0], nstage, rsh, wbase, lane, warp, seq, pol);
@@ -379,14 +407,17 @@ __global__ void __launch_bounds__(kW * 32, kMinBlocks) k_column_ll128(RunParams 
           pc.lines = ag;
           pc.plain = reinterpret_cast<char*>(P.out[d] + P.seg_in0[x] + (uint64_t)t0 * kLL128Elems);
         } else if (Q.mode == 2) {
-          pc.lines = image_bytes(P, P.P, e, d) + pline * kLL128LineBytes;
-          pc.plain = reinterpret_cast<char*>(P.out[x] + P.seg_in0[d] + (uint64_t)t0 * kLL128Elems);
+          const ExchPiece v = Q.exch[d * n + x];
+          exch_piece(pc, P.out[x] + v.out0, image_bytes(P, P.P, e, d),
+                     bounded ? pline : v.line0 + t0, v.elems, t0, CL);
         } else {
           pc.lines = image_bytes(P, P.P, e, x) + pline * kLL128LineBytes;
           pc.plain = reinterpret_cast<char*>(P.out[d] + P.seg_in0[x] + (uint64_t)t0 * kLL128Elems);
         }
-        pc.nl = nl;
-        pc.left = left;
+        if (Q.mode != 2) {
+          pc.nl = nl;
+          pc.left = left;
+        }
       }
       __syncthreads();
       if (!col_gather<kW, kRing>(P, s_piece[1], n, rsh, wbase, lane, warp, seq, pol)) s_ok = 0;
@@ -396,10 +427,12 @@ __global__ void __launch_bounds__(kW * 32, kMinBlocks) k_column_ll128(RunParams 
         // every reader of these lines is done (the barrier above): drop them
         // before they are written back.  All-to-all: the N sources' staged
         // pieces; otherwise the one piece every destination read.
+        // Each piece's own line count: past it lie other columns' lines.
         const int npieces = Q.mode == 2 ? n : 1;
         for (int k = 0; k < npieces; ++k) {
           const char* src = s_piece[1][k].lines;
-          for (int j = threadIdx.x; j < nl; j += blockDim.x)
+          const int pnl = s_piece[1][k].nl;
+          for (int j = threadIdx.x; j < pnl; j += blockDim.x)
             discard_l2_line(src + (size_t)j * kLL128LineBytes);
         }
       }

@@ -353,7 +353,8 @@ int derive(const DeriveInput& in, Plan& p) {
   // other path is refused (its kernels address the whole message).
   const bool composable = p.enc == ENC_LL128 &&
                           ((p.kind == CK_ALLREDUCE && p.algorithm == COLL_TWOSHOT) ||
-                           p.kind == CK_REDUCE_SCATTER || p.kind == CK_ALLTOALL);
+                           p.kind == CK_REDUCE_SCATTER || p.kind == CK_REDUCE_SCATTER_V ||
+                           p.kind == CK_ALLTOALL || p.kind == CK_ALLTOALL_V);
   const bool capped = in.staging_bytes > 0;
   if (capped && p.path == COLL_PATH_AUTO && composable) p.path = COLL_PATH_COMPOSED;
   if (p.path == COLL_PATH_AUTO) {
@@ -362,19 +363,23 @@ int derive(const DeriveInput& in, Plan& p) {
     else if (p.enc == ENC_LL128 &&
              ((p.kind == CK_ALLREDUCE && p.algorithm == COLL_TWOSHOT) ||
               p.kind == CK_REDUCE_SCATTER || p.kind == CK_ALLGATHER ||
-              (in_bytes_per_rank >= (4u << 20) && p.kind == CK_ALLTOALL)))
+              p.kind == CK_REDUCE_SCATTER_V || p.kind == CK_ALLGATHER_V ||
+              (in_bytes_per_rank >= (4u << 20) &&
+               (p.kind == CK_ALLTOALL || p.kind == CK_ALLTOALL_V))))
       p.path = COLL_PATH_COMPOSED;
     else
       p.path = COLL_PATH_STREAMED;
   }
 
   // The composed launch: the LL128 twoshot all-reduce, reduce-scatter,
-  // all-to-all and all-gather (stage plus one or two consuming kinds of task
-  // per chunk).
+  // all-to-all and all-gather, and their V forms (stage plus one or two
+  // consuming kinds of task per chunk).
   if (p.path == COLL_PATH_COMPOSED &&
       !(p.enc == ENC_LL128 &&
         ((p.kind == CK_ALLREDUCE && p.algorithm == COLL_TWOSHOT) ||
-         p.kind == CK_REDUCE_SCATTER || p.kind == CK_ALLTOALL || p.kind == CK_ALLGATHER)))
+         p.kind == CK_REDUCE_SCATTER || p.kind == CK_ALLTOALL || p.kind == CK_ALLGATHER ||
+         p.kind == CK_REDUCE_SCATTER_V || p.kind == CK_ALLGATHER_V ||
+         p.kind == CK_ALLTOALL_V)))
     return COLL_ERR_UNSUPPORTED;
 
   // Rank images of region P.
@@ -662,10 +667,27 @@ int derive(const DeriveInput& in, Plan& p) {
   off = round_up(off + (uint64_t)std::max<uint32_t>(p.ncounters, 1) * 4, 256);
   if (p.path == COLL_PATH_COMPOSED) {
     uint64_t most = 0;
-    for (const Seg& sg : p.pseg[0]) most = std::max<uint64_t>(most, sg.lines);
+    for (int r = 0; r < n; ++r)
+      for (const Seg& sg : p.pseg[r]) most = std::max<uint64_t>(most, sg.lines);
     p.composed_max_chunks = std::max<uint64_t>(1, (most + kComposedMinChunk - 1) / kComposedMinChunk);
     p.off_cflags = off;
     off += p.composed_max_chunks * ((uint64_t)n * 16 + 8);
+    if (p.kind == CK_ALLTOALL || p.kind == CK_ALLTOALL_V) {
+      // source q's partition d goes to destination d after the partitions
+      // d of sources 0 .. q-1
+      p.exch.assign((size_t)n * n, ExchPiece{});
+      for (int d = 0; d < n; ++d) {
+        uint64_t at = 0;
+        for (int q = 0; q < n; ++q) {
+          const Seg& sg = p.pseg[q][d];
+          p.exch[(size_t)q * n + d] = ExchPiece{sg.line0, sg.elems, sg.in_elem, at};
+          at += sg.elems;
+        }
+      }
+      off = round_up(off, 256);
+      p.off_exch = off;
+      off += p.exch.size() * sizeof(ExchPiece);
+    }
   }
   off = round_up(off, 4096);
   const uint64_t lb = (uint64_t)line_bytes(p.enc);

@@ -81,6 +81,9 @@ struct Plan {
   // composed twoshot: completion flags for chunks of at least
   // kComposedMinChunk lines (stage, fold: [chunks][N] u64; gather: [chunks] u64)
   uint64_t off_cflags = 0, composed_max_chunks = 0;
+  // composed all-to-all (V): the [N][N] exchange pieces
+  std::vector<ExchPiece> exch;
+  uint64_t off_exch = 0;
   // composed launch with bounded staging: lines of each rank's staging
   // image per slot (chunks cycle through it); 0 = one place per chunk
   uint64_t ring_lines = 0;

@@ -120,6 +120,16 @@ struct MoeParams {
 // Composed twoshot all-reduce (one persistent launch, Purlin Algorithm 1):
 // the chunking of every partition, the task queue's lag and the per-task
 // completion flags (epoch values, in the workspace).
+// One piece of an all-to-all (V) exchange, source p's partition x: its
+// place in p's rank image and input, its length, and its offset in
+// destination x's output.  The composed all-to-all reads table[p * N + x].
+struct ExchPiece {
+  uint64_t line0;  // first line in rank p's image
+  uint64_t elems;  // 16-bit units (V[p][x], or the uniform partition)
+  uint64_t in0;    // offset in rank p's input
+  uint64_t out0;   // offset in rank x's output: the earlier sources' lengths
+};
+
 struct ComposedParams {
   uint32_t chunk_lines;  // lines of one partition per chunk (multiple of 4)
   uint32_t nchunks;
@@ -140,6 +150,7 @@ struct ComposedParams {
   uint64_t* flag_stage;  // [nchunks][N]: epoch once rank p staged chunk c
   uint64_t* flag_fold;   // [nchunks][N]: epoch once owner r published chunk c
   uint64_t* gather_cnt;  // [nchunks]: (epoch << 8) | gathers of chunk c done
+  const ExchPiece* exch; // all-to-all (V), columns: [N][N] pieces
 };
 
 // Everything a kernel launch needs; passed by value (captured by graphs).

@@ -354,13 +354,17 @@ coll_status_t coll_get_rejections(coll_spec_t *spec, coll_stream_t stream,
 
 /* Inspection of the derived schedule (host only, no CUDA call).  which = 0:
  * staging items, 1: first consume phase, 2: second consume phase (twoshot
- * all-gather).  Each item is written as 10 int64 values:
+ * all-gather), 3: the exchange pieces of a composed all-to-all (V).  Each
+ * item is written as 10 int64 values:
  *   consume: kind (0 fold, 1 copy), flags (1 publish, 2 sole-reader re-arm,
  *            4 counted re-arm), dst rank, src rank, readers, lines, elements,
  *            first source line, output offset (element, or line when
  *            publishing), counter index;
  *   staging: rank, 0, 0, 0, 0, lines, elements, first image line, first
- *            input element, 0.
+ *            input element, 0;
+ *   exchange: source rank p, destination rank x, first line of partition x
+ *            in p's image, elements, first input element in p, first output
+ *            element in x, 0, 0, 0, 0 (an empty list for other plans).
  * *n receives the number of items; at most cap items are written. */
 coll_status_t coll_debug_items(const coll_spec_t *spec, int which, int64_t *buf,
                                size_t cap, size_t *n);

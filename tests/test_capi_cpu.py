@@ -263,6 +263,51 @@ def test_derived_v_schedule_computes_the_oracle_result(cd, name, n, v, enc, path
         cd.coll_destroy(spec)
 
 
+@pytest.mark.parametrize("name,n,v", [
+    ("ALLTOALL_V", 8, [synth.rotate_right(zipf_elems(8 * 960 * 2, 8), p + 1) for p in range(8)]),
+    ("ALLTOALL_V", 3, [[8, 0, 240], [0, 0, 16], [128, 64, 8]]),
+    ("ALLTOALL", 4, 4 * 1000),
+])
+def test_composed_exchange_table_moves_every_partition(cd, name, n, v):
+    """The composed all-to-all (V) reads one piece per (source p, destination
+    x) from a table: partition x of p's input goes to destination x after the
+    partitions x of sources 0 .. p-1, from lines that lie inside p's staged
+    image without overlapping.  Copying by the table alone must give the
+    oracle's exchange."""
+    triple = getattr(cd, name)
+    vec = name == "ALLTOALL_V"
+    spec = cd.coll_spec_create(*triple, n, 0 if vec else v, encoding=cd.COLL_LL128,
+                               path=cd.COLL_PATH_COMPOSED, vcounts=v if vec else None)
+    try:
+        ins = [synth.random_bits16(21, cd.coll_buffer_elems(spec, r)[0], n, r) for r in range(n)]
+        outs = [np.full(cd.coll_buffer_elems(spec, r)[1], 0xFFFF, dtype=np.uint16)
+                for r in range(n)]
+        table = cd.coll_debug_items(spec, 3)
+        assert len(table) == n * n
+        stage = cd.coll_debug_items(spec, 0)
+        image_lines = {r: 0 for r in range(n)}
+        for it in stage:
+            image_lines[int(it[0])] = max(image_lines[int(it[0])], int(it[7] + it[5]))
+        used = {r: [] for r in range(n)}
+        for p, x, line0, elems, in0, out0, *_ in table.tolist():
+            outs[x][out0:out0 + elems] = ins[p][in0:in0 + elems]
+            lines = -(-elems // 60)
+            used[p].append((line0, line0 + lines))
+        for r in range(n):
+            spans = sorted(used[r])
+            assert all(a[1] <= b[0] for a, b in zip(spans, spans[1:])), spans
+            assert spans[-1][1] <= max(image_lines[r], 1)
+        want = oracle.all_to_all_v(ins, v) if vec else oracle.all_to_all(ins)
+        for r in range(n):
+            assert np.array_equal(outs[r], want[r]), f"rank {r}"
+    finally:
+        cd.coll_destroy(spec)
+    other = cd.coll_spec_create(*cd.REDUCE_SCATTER, 4, 4 * 64, encoding=cd.COLL_LL128,
+                                path=cd.COLL_PATH_COMPOSED)
+    assert len(cd.coll_debug_items(other, 3)) == 0
+    cd.coll_destroy(other)
+
+
 def test_v_argument_validation(cd):
     def status_of(*a, **kw):
         with pytest.raises(cd.CollError) as e:
