@@ -338,7 +338,10 @@ int derive(const DeriveInput& in, Plan& p) {
   // launch for the LL128 twoshot and reduce-scatter (8 x 1 MiB reduce-
   // scatter: 18 against 40 us stream-ordered), for the LL128 all-gather
   // (equal up to 16 MiB, then faster: 8 x 256 MiB 0.40 against 0.55 ms) and
-  // for the all-to-all from 4 MiB (8 x 4 MiB: 32 against 34 us); stream-
+  // for the all-to-all from 4 MiB (8 x 4 MiB: 32 against 34 us); the V forms
+  // follow the same rules (Zipf split of 256 MiB: reduce-scatter V 0.58
+  // against 1.11 ms, all-gather V 0.40 against 0.55, all-to-all V 0.87
+  // against 1.44); stream-
   // ordered kernels otherwise.  Two ranks always use oneshot (both move S
   // per rank).
   p.algorithm = 0;
