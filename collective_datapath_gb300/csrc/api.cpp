@@ -146,10 +146,10 @@ cudaError_t launched(coll_spec* s, cudaError_t e, cudaStream_t st) {
 }
 
 // Shape of the composed launch.  COLL_COMPOSED_SHAPE =
-// "chunk_lines,lag,discard,variant,lag2,schedule" overrides the defaults
-// (benchmark sweeps and tests); chunks are a power of two of at least
-// kComposedMinChunk lines (rows per chunk are counted with shifts, and the
-// queue's completion flags are laid out for that size).
+// "chunk_lines,lag,discard,variant,lag2,schedule,tail,tail_hw,stagger"
+// overrides the defaults (benchmark sweeps and tests); chunks are a power
+// of two of at least kComposedMinChunk lines (the queue counts rows with
+// shifts, and its completion flags are laid out for that size).
 //
 // schedule 0 (default), columns: a column is one chunk of one partition,
 // run start to end by one CTA, launch variant 2 (4 warps, 6 CTAs per SM).
@@ -159,9 +159,21 @@ cudaError_t launched(coll_spec* s, cudaError_t e, cudaStream_t st) {
 // round of columns stays a small part of the run.  Measured, 8 ranks, all-
 // reduce: 256 MiB 0.89 ms at 64 lines (0.93 at 128, 0.95 at 32); 128 MiB
 // 0.46 ms at 64; 32 MiB 0.136-0.139 ms at 32-64; 8 MiB 0.050 ms at 32;
-// all-gather 256 MiB 0.396 ms at 128 lines, 0.442 at 64.  Bounded staging:
-// CTA g owns chunk slot g of every rank image, so the chunk is the largest
-// of 64 .. 16 lines whose slots cover every co-resident CTA.
+// all-gather 256 MiB 0.396 ms at 128 lines, 0.442 at 64.
+// Each CTA's first column is one of a staggered group of `stagger` (8)
+// lengths, 1/8 .. 8/8 of a chunk: with equal first columns every CTA staged
+// at once (inputs read from HBM while the previous run's outputs were
+// written back: the first stage took 16 us against 8.5 later) and the
+// phases took three columns to drift apart.  The last columns, over
+// `tail_hw` (1) half-rounds of the CTAs' work, are `tail` (16) lines long,
+// so that the CTAs run out of work together.  8 ranks, all-reduce, 32 /
+// 128 / 256 MiB: 0.1405 / 0.460 / 0.889 ms without, 0.1315 / 0.450 / 0.876
+// with both (0.1322 / 0.451 / 0.877 with the stagger alone); all-to-all 32
+// / 256 MiB 0.126 / 0.821 ms without, 0.120 / 0.816 with; reduce-scatter
+// 0.087 / 0.568 and 0.086 / 0.562.  Not the all-gather.
+// Bounded staging: CTA g owns chunk slot g of every rank image, so the
+// chunk is the largest of 64 .. 16 lines whose slots cover every co-
+// resident CTA, and every column is a chunk.
 //
 // schedule 1, the queue of tasks (stage, fold, gather per chunk, with lags
 // of `lag` and `lag2` steps): defaults measured at 8 x 256 MiB, all-reduce
@@ -174,7 +186,7 @@ ComposedParams composed_shape(const coll_spec* s) {
   ComposedParams q{};
   const bool ar = p.kind == CK_ALLREDUCE;
   int chunk = ar ? 256 : 128, lag = ar ? 28 : 40, discard = 1, variant = 0, lag2 = -1,
-      schedule = 0;
+      schedule = 0, tail = 0, tail_hw = 2, stagger = 0;
   // the longest partition of any rank image (the all-gathers' sources
   // differ in length with V sizes)
   uint64_t most = 0;
@@ -183,9 +195,17 @@ ComposedParams composed_shape(const coll_spec* s) {
   const bool gather = p.kind == CK_ALLGATHER || p.kind == CK_ALLGATHER_V;
   const char* env = std::getenv("COLL_COMPOSED_SHAPE");
   if (env != nullptr)
-    std::sscanf(env, "%d,%d,%d,%d,%d,%d", &chunk, &lag, &discard, &variant, &lag2, &schedule);
+    std::sscanf(env, "%d,%d,%d,%d,%d,%d,%d,%d,%d", &chunk, &lag, &discard, &variant, &lag2,
+                &schedule, &tail, &tail_hw, &stagger);
   q.schedule = schedule == 1 ? 1 : 0;
-  if (q.schedule == 0 && env == nullptr) variant = 2;
+  if (q.schedule == 0 && env == nullptr) {
+    variant = 2;
+    // the all-gather's columns stage one piece each, and neither form paid
+    // there (8 x 256 MiB: 0.392 ms plain, 0.398 with both)
+    stagger = gather ? 0 : 8;
+    tail = gather ? 0 : 16;
+    tail_hw = 1;
+  }
   q.variant = variant >= 0 && variant <= 2 ? variant : 0;
   if (q.schedule == 0 && env == nullptr) {
     const uint64_t cap = (uint64_t)std::max(1, column_capacity(q.variant));
@@ -239,6 +259,41 @@ ComposedParams composed_shape(const coll_spec* s) {
     q.ring = (uint32_t)(p.ring_lines / ((uint64_t)p.n * q.chunk_lines));
     q.lag = std::min(q.lag, std::max(1, (int)q.ring / 2));
     q.lag2 = std::min(q.lag2, std::max(1, (int)q.ring / 2));
+  }
+  q.first_cols = 0;
+  q.first_lines = 0;
+  q.stagger = 1;
+  q.head_chunks = q.nchunks;
+  q.tail_lines = q.chunk_lines;
+  if (q.schedule == 0 && q.ring == 0 && ((stagger > 0) || (tail > 0 && tail_hw > 0))) {
+    const uint64_t cap = (uint64_t)std::max(1, column_capacity(q.variant));
+    const uint64_t CL = q.chunk_lines, cr = CL / kLL128RowLines;
+    if (stagger > 0) {
+      // one staggered column per CTA of the launch (coll_run's grid): groups
+      // of G columns of 1/G .. G/G of a chunk, at least a row each
+      const uint64_t G = (uint64_t)std::min(stagger, 64);
+      q.stagger = (uint32_t)G;
+      q.first_cols = (uint32_t)(cap - cap % (uint64_t)p.n);
+      uint64_t rows = 0;
+      for (uint64_t j = 0; j < q.first_cols / (uint64_t)p.n; ++j)
+        rows += std::max<uint64_t>(1, ((j % G + 1) * cr) / G);
+      q.first_lines = (uint32_t)(rows * kLL128RowLines);
+    }
+    const uint64_t rest = most > q.first_lines ? most - q.first_lines : 0;
+    q.head_chunks = (uint32_t)((rest + CL - 1) / CL);
+    if (tail > 0 && tail_hw > 0) {
+      // columns of `tail` lines for the last `tail_hw` half-rounds of the
+      // co-resident CTAs' work
+      uint32_t ts = kComposedMinChunk;
+      while (ts * 2 <= (uint32_t)tail && ts * 2 < q.chunk_lines) ts *= 2;
+      if (ts < q.chunk_lines) {
+        const uint64_t tl = (uint64_t)tail_hw * cap * CL / (2 * (uint64_t)p.n);
+        q.head_chunks = (uint32_t)((rest > tl ? rest - tl : 0) / CL);
+        q.tail_lines = ts;
+      }
+    }
+    const uint64_t after = rest - std::min<uint64_t>(rest, (uint64_t)q.head_chunks * CL);
+    q.nchunks = q.head_chunks + (uint32_t)((after + q.tail_lines - 1) / q.tail_lines);
   }
   q.discard = discard;
   q.mode = p.kind == CK_REDUCE_SCATTER || p.kind == CK_REDUCE_SCATTER_V ? 1

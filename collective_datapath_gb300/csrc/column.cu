@@ -60,16 +60,16 @@ __device__ __forceinline__ void discard_l2_line(const void* p) {
 // Stage: input rows (480 payload bytes) -> LL128 rows (512 bytes).  Here a
 // piece's `plain` is the input and `lines` the staged lines.
 template <int kW, int kRing>
-__device__ __forceinline__ void col_stage(const ColPiece* pc, int np, int rsh, uint32_t wbase,
+__device__ __forceinline__ void col_stage(const ColPiece* pc, int np, int R, uint32_t wbase,
                                           int lane, int warp, uint64_t seq, uint64_t pol) {
-  const int T = np << rsh, rmask = (1 << rsh) - 1;
+  const int T = np * R;
   const int lo = (T * warp) / kW, nj = (T * (warp + 1)) / kW - lo;
   if (nj <= 0) return;
   const int li = lane >> 3, kk = lane & 7;
   const int G = 15 * li + 2 * kk;  // first payload granule of this lane's line chunk
   // lanes 30 and 31 load no input (their load bound is never met)
   const int lb = lane < 30 ? 16 * lane : 1 << 30;
-  int lk = lo >> rsh, lr = lo & rmask;
+  int lk = lo / R, lr = lo - lk * R;
   const char* lsrc = pc[lk].plain + (size_t)lr * (2 * kRowElems);
   int lleft = pc[lk].left - lr * (2 * kRowElems);
   auto issue = [&](int j) {
@@ -79,7 +79,7 @@ __device__ __forceinline__ void col_stage(const ColPiece* pc, int np, int rsh, u
                       lsrc + (valid ? 16 * lane : 0), valid, pol);
       lsrc += 2 * kRowElems;
       lleft -= 2 * kRowElems;
-      if (++lr > rmask) {
+      if (++lr == R) {
         lr = 0;
         if (++lk < np) {
           lsrc = pc[lk].plain;
@@ -89,7 +89,7 @@ __device__ __forceinline__ void col_stage(const ColPiece* pc, int np, int rsh, u
     }
     cp_async_commit();
   };
-  int sk = lo >> rsh, sr = lo & rmask;
+  int sk = lk, sr = lr;
   char* sdst = pc[sk].lines + (size_t)sr * kRowBytes;
   int snl = pc[sk].nl - kLL128RowLines * sr;
 #pragma unroll 1
@@ -108,7 +108,7 @@ __device__ __forceinline__ void col_stage(const ColPiece* pc, int np, int rsh, u
                              min((int)kLL128RowLines, snl), seq);
     sdst += kRowBytes;
     snl -= kLL128RowLines;
-    if (++sr > rmask) {
+    if (++sr == R) {
       sr = 0;
       if (++sk < np) {
         sdst = pc[sk].lines;
@@ -125,9 +125,9 @@ __device__ __forceinline__ void col_stage(const ColPiece* pc, int np, int rsh, u
 // the rank.
 template <int kW, int kRing>
 __device__ __forceinline__ bool col_gather(const RunParams& P, const ColPiece* pc, int np,
-                                           int rsh, uint32_t wbase, int lane, int warp,
+                                           int R, uint32_t wbase, int lane, int warp,
                                            uint64_t seq, uint64_t pol) {
-  const int T = np << rsh, rmask = (1 << rsh) - 1;
+  const int T = np * R;
   const int lo = (T * warp) / kW, nj = (T * (warp + 1)) / kW - lo;
   if (nj <= 0) return true;
   const int li = lane >> 3;
@@ -138,7 +138,7 @@ __device__ __forceinline__ bool col_gather(const RunParams& P, const ColPiece* p
   const int lb = lane < 30 ? 16 * lane : 1 << 30;
   const uint32_t g0off = 128 * ((2 * q) / 15) + 8 * ((2 * q) % 15);
   const uint32_t g1off = 128 * ((2 * q + 1) / 15) + 8 * ((2 * q + 1) % 15);
-  int lk = lo >> rsh, lr = lo & rmask;
+  int lk = lo / R, lr = lo - lk * R;
   const char* lsrc = pc[lk].lines + (size_t)lr * kRowBytes;
   int lnl = pc[lk].nl - kLL128RowLines * lr;
   auto issue = [&](int j) {
@@ -146,7 +146,7 @@ __device__ __forceinline__ bool col_gather(const RunParams& P, const ColPiece* p
       cp_async16(wbase + (j % kRing) * kRowBytes + 16 * lane, lsrc + 16 * lane, li < lnl);
       lsrc += kRowBytes;
       lnl -= kLL128RowLines;
-      if (++lr > rmask) {
+      if (++lr == R) {
         lr = 0;
         if (++lk < np) {
           lsrc = pc[lk].lines;
@@ -156,7 +156,7 @@ __device__ __forceinline__ bool col_gather(const RunParams& P, const ColPiece* p
     }
     cp_async_commit();
   };
-  int sk = lo >> rsh, sr = lo & rmask;
+  int sk = lk, sr = lr;
   const char* ssrc = pc[sk].lines + (size_t)sr * kRowBytes;
   char* sdst = pc[sk].plain + (size_t)sr * (2 * kRowElems);
   int snl = pc[sk].nl - kLL128RowLines * sr;
@@ -190,7 +190,7 @@ __device__ __forceinline__ bool col_gather(const RunParams& P, const ColPiece* p
     sdst += 2 * kRowElems;
     snl -= kLL128RowLines;
     sleft -= 2 * kRowElems;
-    if (++sr > rmask) {
+    if (++sr == R) {
       sr = 0;
       if (++sk < np) {
         ssrc = pc[sk].lines;
@@ -315,6 +315,49 @@ __device__ __forceinline__ void exch_piece(ColPiece& pc, const uint16_t* plain, 
   pc.left = (int)max((int64_t)0, min((int64_t)CL * (2 * kLL128Elems), bytes));
 }
 
+// Rows of the g-th column of a staggered group (g = 0 .. G-1): 1/G, 2/G,
+// .. of a chunk, at least one row.
+__device__ __forceinline__ int stagger_rows(int g, int G, int chunk_rows) {
+  return max(1, ((g + 1) * chunk_rows) / G);
+}
+
+// Column q of an unbounded run: its partition x, first line t0 and lines.
+// The first `first_cols` columns (one per CTA at the start) come in groups
+// of `stagger` columns of 1/G, 2/G, .. of a chunk, so that the CTAs end
+// their first column at different times and their later phases do not all
+// hit memory together; then chunks of chunk_lines, and after head_chunks of
+// them, chunks of tail_lines.
+struct ColumnAt {
+  int x;
+  uint32_t t0, len;
+};
+__device__ __forceinline__ ColumnAt column_at(const ComposedParams& Q, int q, int n) {
+  ColumnAt a;
+  if (q < (int)Q.first_cols) {
+    const int j = q / n, G = (int)Q.stagger, cr = (int)Q.chunk_lines / kLL128RowLines;
+    const int grp = j / G, g = j - grp * G;
+    int rows = 0;
+    for (int i = 0; i < G; ++i) rows += stagger_rows(i, G, cr);
+    rows *= grp;
+    for (int i = 0; i < g; ++i) rows += stagger_rows(i, G, cr);
+    a.x = q - j * n;
+    a.t0 = (uint32_t)rows * kLL128RowLines;
+    a.len = (uint32_t)stagger_rows(g, G, cr) * kLL128RowLines;
+    return a;
+  }
+  q -= (int)Q.first_cols;
+  const int c = q / n;
+  a.x = q - c * n;
+  if (c < (int)Q.head_chunks) {
+    a.t0 = Q.first_lines + (uint32_t)c * Q.chunk_lines;
+    a.len = Q.chunk_lines;
+  } else {
+    a.t0 = Q.first_lines + Q.head_chunks * Q.chunk_lines + (uint32_t)(c - (int)Q.head_chunks) * Q.tail_lines;
+    a.len = Q.tail_lines;
+  }
+  return a;
+}
+
 template <int kW, int kRing, int kMinBlocks, bool kF32>
 __global__ void __launch_bounds__(kW * 32, kMinBlocks) k_column_ll128(RunParams P) {
   extern __shared__ __align__(128) char smem[];
@@ -327,16 +370,17 @@ __global__ void __launch_bounds__(kW * 32, kMinBlocks) k_column_ll128(RunParams 
   const int n = P.nranks;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int slot = (int)(e & 1);
-  const int ncols = (int)Q.nchunks * n;
+  const int ncols = (int)Q.first_cols + (int)Q.nchunks * n;
   const bool bounded = Q.ring != 0;
   const uint32_t CL = Q.chunk_lines;
-  const int rsh = __ffs((int)CL / kLL128RowLines) - 1;  // rows per chunk = 2^rsh
   const uint32_t wbase =
       (uint32_t)__cvta_generic_to_shared(smem) + (uint32_t)(warp * kRing * kRowBytes);
   const bool folds = Q.mode == 0 || Q.mode == 1, gathers = Q.mode != 1;
   const uint64_t pol = l2_evict_first_policy();  // inputs and outputs are touched once
   if (threadIdx.x == 0) {
-    s_col[0] = bounded ? (int)blockIdx.x : (int)atomicAdd(&h->task_next[slot], 1u);
+    // every CTA's first column is its own index; later ones come from the
+    // run's counter, past the grid (bounded staging: every grid-th column)
+    s_col[0] = (int)blockIdx.x;
     s_ok = 1;
   }
   __syncthreads();
@@ -346,17 +390,26 @@ __global__ void __launch_bounds__(kW * 32, kMinBlocks) k_column_ll128(RunParams 
     if (threadIdx.x == 0)
       s_col[(it + 1) & 1] = aborted(P.ws) ? ncols
                             : bounded     ? q + (int)gridDim.x
-                                          : (int)atomicAdd(&h->task_next[slot], 1u);
-    const int c = q / n, x = q - c * n;
-    const uint32_t t0 = (uint32_t)c * CL;
+                                          : (int)gridDim.x + (int)atomicAdd(&h->task_next[slot], 1u);
+    ColumnAt at;
+    if (bounded) {
+      at.x = q % n;
+      at.t0 = (uint32_t)(q / n) * CL;
+      at.len = CL;
+    } else {
+      at = column_at(Q, q, n);
+    }
+    const int x = at.x;
+    const uint32_t t0 = at.t0, cl = at.len;
+    const int R = (int)cl / kLL128RowLines;  // rows per piece
     const uint64_t seq = bounded ? e + (uint64_t)q : e;
     // the column's line in every rank image, and in owner x's published image
     const uint64_t pline = bounded ? (uint64_t)blockIdx.x * CL : P.seg_line0[x] + t0;
     const uint64_t agline = bounded ? (uint64_t)(blockIdx.x / n) * CL : (uint64_t)t0;
-    const int nl = max(0, min((int)CL, seg_lines(P, x) - (int)t0));
+    const int nl = max(0, min((int)cl, seg_lines(P, x) - (int)t0));
     const int64_t lx = 2 * ((int64_t)P.seg_elems[x] - (int64_t)t0 * kLL128Elems);
-    const int left = (int)(lx < (int64_t)CL * (2 * kLL128Elems) ? lx
-                                                                : (int64_t)CL * (2 * kLL128Elems));
+    const int left = (int)(lx < (int64_t)cl * (2 * kLL128Elems) ? lx
+                                                                : (int64_t)cl * (2 * kLL128Elems));
     if (nl == 0) {
       // partition x is shorter than the longest one (V sizes): nothing to
       // move in this chunk.  The barrier publishes the next column.
@@ -372,7 +425,7 @@ __global__ void __launch_bounds__(kW * 32, kMinBlocks) k_column_ll128(RunParams 
       if (Q.mode == 2) {
         const ExchPiece v = Q.exch[p * n + x];
         exch_piece(pc, P.in[p] + v.in0, image_bytes(P, P.P, e, p), bounded ? pline : v.line0 + t0,
-                   v.elems, t0, CL);
+                   v.elems, t0, cl);
       } else {
         pc.plain = const_cast<char*>(reinterpret_cast<const char*>(
             P.in[p] + (Q.mode == 3 ? 0 : P.seg_in0[x]) + (uint64_t)t0 * kLL128Elems));
@@ -382,7 +435,7 @@ __global__ void __launch_bounds__(kW * 32, kMinBlocks) k_column_ll128(RunParams 
       }
     }
     __syncthreads();
-    col_stage<kW, kRing>(s_piece[0], nstage, rsh, wbase, lane, warp, seq, pol);
+    col_stage<kW, kRing>(s_piece[0], nstage, R, wbase, lane, warp, seq, pol);
     __syncthreads();
     char* ag = image_bytes(P, P.AG, e, x) + agline * kLL128LineBytes;
     if (folds) {
@@ -409,7 +462,7 @@ __global__ void __launch_bounds__(kW * 32, kMinBlocks) k_column_ll128(RunParams 
         } else if (Q.mode == 2) {
           const ExchPiece v = Q.exch[d * n + x];
           exch_piece(pc, P.out[x] + v.out0, image_bytes(P, P.P, e, d),
-                     bounded ? pline : v.line0 + t0, v.elems, t0, CL);
+                     bounded ? pline : v.line0 + t0, v.elems, t0, cl);
         } else {
           pc.lines = image_bytes(P, P.P, e, x) + pline * kLL128LineBytes;
           pc.plain = reinterpret_cast<char*>(P.out[d] + P.seg_in0[x] + (uint64_t)t0 * kLL128Elems);
@@ -420,7 +473,7 @@ __global__ void __launch_bounds__(kW * 32, kMinBlocks) k_column_ll128(RunParams 
         }
       }
       __syncthreads();
-      if (!col_gather<kW, kRing>(P, s_piece[1], n, rsh, wbase, lane, warp, seq, pol)) s_ok = 0;
+      if (!col_gather<kW, kRing>(P, s_piece[1], n, R, wbase, lane, warp, seq, pol)) s_ok = 0;
       __syncthreads();
       if (!s_ok) break;
       if (Q.discard) {

@@ -133,6 +133,16 @@ struct ExchPiece {
 struct ComposedParams {
   uint32_t chunk_lines;  // lines of one partition per chunk (multiple of 4)
   uint32_t nchunks;
+  // columns (unbounded staging): first_cols staggered columns (groups of
+  // `stagger` columns of 1/G .. G/G of a chunk) cover each partition's first
+  // first_lines lines; then head_chunks chunks of chunk_lines and the rest in
+  // chunks of tail_lines.  nchunks counts the chunks after the staggered
+  // columns.
+  uint32_t first_cols;
+  uint32_t first_lines;
+  uint32_t stagger;
+  uint32_t head_chunks;
+  uint32_t tail_lines;
   int lag;               // queue steps between a chunk's stage and its fold
   int lag2;              // queue steps between a chunk's fold and its gather
   int discard;           // drop consumed lines from L2 (no write-back):

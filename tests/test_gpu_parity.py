@@ -255,6 +255,41 @@ def test_composed_twoshot_matches_the_oracle(cd, n, count, shape, monkeypatch):
         assert coll.epoch() == e + 1
 
 
+@pytest.mark.parametrize("name,n,count", [("ALLREDUCE", 8, 8 * 60 * 5000 + 64),
+                                          ("ALLREDUCE", 3, 3 * 60 * 4000 + 8),
+                                          ("REDUCE_SCATTER", 8, 8 * 60 * 5000 + 64),
+                                          ("ALLGATHER", 8, 8 * 60 * 5000 + 64),
+                                          ("ALLTOALL", 8, 8 * 60 * 5000)])
+@pytest.mark.parametrize("shape", ["64,1,1,2,-1,0,16,1", "64,1,1,2,-1,0,32,3", "32,1,1,0,-1,0,16,1",
+                                   "128,1,1,2,-1,0,16,2", "64,1,1,1,-1,0,16,40",
+                                   "64,1,1,2,-1,0,0,2,8", "64,1,1,2,-1,0,16,1,8",
+                                   "32,1,1,0,-1,0,16,1,4", "64,1,1,2,-1,0,0,2,3",
+                                   "128,1,1,2,-1,0,32,2,5", "16,1,1,2,-1,0,0,2,64"])
+def test_composed_short_tail_columns(cd, name, n, count, shape, monkeypatch):
+    """Columns of several lengths: each CTA's first column is one of a
+    staggered group (ninth field G: 1/G, 2/G, .. of a chunk, at least a row),
+    then chunks of the chunk size, and the last columns the CTAs take the
+    tail size (seventh field), over the last few half-rounds of the
+    co-resident CTAs' work (eighth field; 40 puts every later chunk in the
+    tail).  Bit-exact over several epochs across every boundary and the
+    ragged end."""
+    monkeypatch.setenv("COLL_COMPOSED_SHAPE", shape)
+    triple = getattr(cd, name)
+    opts = dict(encoding=cd.COLL_LL128, path=cd.COLL_PATH_COMPOSED)
+    if name == "ALLREDUCE":
+        opts["algorithm"] = cd.COLL_TWOSHOT
+    coll = make(cd, triple, n, count, **opts)
+    _, ins, outs = buffers(coll, n, seed=45)
+    for e in range(1, 4):
+        xs = [synth.random_bits16(700 + e, coll.elems(r)[0], n, r) if name in ("ALLGATHER", "ALLTOALL")
+              else synth.normal_bf16(700 + e, coll.elems(r)[0], n, r) for r in range(n)]
+        for r in range(n):
+            ins[r][:xs[r].size].copy_(to_dev(xs[r]))
+        coll.run(ins, outs)
+        check(coll, outs, expected(cd, triple, xs, count), n)
+        assert coll.epoch() == e + 1
+
+
 @pytest.mark.parametrize("n,count", [(8, 8 * 60 * 1024 + 64), (3, 3000), (8, 24), (2, 2 * 4096),
                                      (8, 8 * 60 * 300)])
 @pytest.mark.parametrize("shape", [None, "16,1,1", "64,3,0", "32,5,1,2", "128,40,1,1", "16,1,1,0,-1,1",
