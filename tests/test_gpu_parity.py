@@ -351,6 +351,31 @@ def test_composed_cycling_staging(cd, name, n, count, min_chunk_slots, shape, mo
         last = now
 
 
+@pytest.mark.parametrize("name", ["ALLREDUCE", "REDUCE_SCATTER", "ALLGATHER", "ALLTOALL"])
+@pytest.mark.parametrize("n,count", [(1, 8), (1, 4096), (2, 16), (2, 2 * 120 + 16), (8, 64)])
+def test_composed_degenerate_sizes(cd, name, n, count):
+    """The composed launch at its edges: one rank (the fold of one value is
+    that value; every copy is the identity), partitions shorter than one
+    LL128 line, and a ragged last line; then an empty run, which only moves
+    the epoch."""
+    triple = getattr(cd, name)
+    opts = dict(encoding=cd.COLL_LL128, path=cd.COLL_PATH_COMPOSED)
+    if name == "ALLREDUCE":
+        opts["algorithm"] = cd.COLL_TWOSHOT
+    coll = make(cd, triple, n, count, **opts)
+    for e in range(1, 3):
+        xs, ins, outs = buffers(coll, n, seed=50 + e, dist="bits" if name in
+                                ("ALLGATHER", "ALLTOALL") else "normal", tag=count)
+        coll.run(ins, outs)
+        check(coll, outs, expected(cd, triple, xs, count), n)
+        assert coll.epoch() == e + 1
+    empty = make(cd, triple, n, 0, **opts)
+    outs0 = [empty_dev(0) for _ in range(n)]
+    empty.run([empty_dev(0) for _ in range(n)], outs0)
+    code, _, _ = empty.status()
+    assert code == cd.COLL_OK and empty.epoch() == 2
+
+
 @pytest.mark.parametrize("enc,reset", [(0, 0), (0, 1), (0, 3), (1, 2), (2, 0), (2, 1), (2, 3)])
 @pytest.mark.parametrize("path", [1, 2, 3])
 def test_four_rotating_slots(cd, enc, reset, path):
