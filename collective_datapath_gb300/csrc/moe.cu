@@ -410,14 +410,19 @@ constexpr int kMcWarps = 8, kMcRing = 8;
 // barrier, where its busiest warp sets the pace).
 constexpr int kMcSplit = 2;
 
-// Two row buffers and the warps' copy rings.
+// Token-row buffers of the composed and column kernels: one per token of a
+// sub-block (the stage kernel's double buffer when sub-blocks are smaller),
+// then each warp's copy ring.  Both kernels place the rings after
+// kMcRowBufs buffers, so a different sub-block size resizes them together.
+constexpr int kMcRowBufs = kMoeSubTokens > 2 ? kMoeSubTokens : 2;
 size_t moe_composed_smem_bytes(int hidden) {
-  return moe_stage_smem_bytes(hidden) + (size_t)kMcWarps * kMcRing * kRowBytes;
+  return (size_t)kMcRowBufs * (((size_t)hidden * 2 + 127) / 128 * 128) +
+         (size_t)kMcWarps * kMcRing * kRowBytes;
 }
 
 __global__ void __launch_bounds__(kMcWarps * 32, 3) k_moe_composed(RunParams P) {
   extern __shared__ __align__(128) char smem[];
-  __shared__ __align__(8) uint64_t mbar[2];
+  __shared__ __align__(8) uint64_t mbar[kMcRowBufs];  // one per token row buffer
   __shared__ int s_task[2], s_ok;
   __shared__ int s_tok[kMoeBlockTokens];        // copy task: its staged rows' tokens
   const uint64_t e = begin_run(P);
@@ -429,17 +434,16 @@ __global__ void __launch_bounds__(kMcWarps * 32, 3) k_moe_composed(RunParams P) 
   const uint32_t buf_stride = (row_bytes + 127) / 128 * 128;
   const uint32_t sbuf = (uint32_t)__cvta_generic_to_shared(smem);
   const uint32_t sbar = (uint32_t)__cvta_generic_to_shared(mbar);
-  const uint32_t wbase = sbuf + 2 * buf_stride + (uint32_t)(warp * kMcRing * kRowBytes);
+  const uint32_t wbase = sbuf + kMcRowBufs * buf_stride + (uint32_t)(warp * kMcRing * kRowBytes);
   const int slot = (int)(e & 1);
   const int per_step = n * kMoeSubs + n * n;
   const int ntasks = (M.nblocks + M.lag) * per_step;
   const int nsub_total = M.nblocks * kMoeSubs;
   const size_t img_stride = P.P.rank_bytes;
   char* img0 = P.ws + P.P.base + (e & P.P.slot_mask) * P.P.slot_bytes;
-  uint32_t uses[2] = {0, 0};                     // thread 0: loads into each buffer so far
+  uint32_t uses[kMcRowBufs] = {};                // thread 0: loads into each buffer so far
   if (threadIdx.x == 0) {
-    mbar_init(sbar, 1);
-    mbar_init(sbar + 8, 1);
+    for (int k = 0; k < kMcRowBufs; ++k) mbar_init(sbar + 8 * k, 1);
     fence_mbarrier_init();
     s_task[0] = (int)atomicAdd(&h->task_next[slot], 1u);
     s_ok = 1;
@@ -582,7 +586,7 @@ __global__ void __launch_bounds__(kMcWarps * 32, 3) k_moe_composed(RunParams P) 
 // back.
 __global__ void __launch_bounds__(kMcWarps * 32, 3) k_moe_column(RunParams P) {
   extern __shared__ __align__(128) char smem[];
-  __shared__ __align__(8) uint64_t mbar[kMoeSubTokens];
+  __shared__ __align__(8) uint64_t mbar[kMcRowBufs];
   __shared__ int s_col[2], s_ok;
   const uint64_t e = begin_run(P);
   const MoeParams& M = P.moe;
@@ -594,7 +598,7 @@ __global__ void __launch_bounds__(kMcWarps * 32, 3) k_moe_column(RunParams P) {
   const uint32_t sbuf = (uint32_t)__cvta_generic_to_shared(smem);
   const uint32_t sbar = (uint32_t)__cvta_generic_to_shared(mbar);
   const uint32_t wbase =
-      sbuf + kMoeSubTokens * buf_stride + (uint32_t)(warp * kMcRing * kRowBytes);
+      sbuf + kMcRowBufs * buf_stride + (uint32_t)(warp * kMcRing * kRowBytes);
   const int slot = (int)(e & 1);
   const int ncols = M.nblocks * kMoeSubs * n;
   const int nrows_w = (int)(M.row_lines / kLL128RowLines);
@@ -605,7 +609,7 @@ __global__ void __launch_bounds__(kMcWarps * 32, 3) k_moe_column(RunParams P) {
     t0 = (q / n) * kMoeSubTokens;
     nt = max(0, min(kMoeSubTokens, M.tokens - t0));
   };
-  uint32_t uses[kMoeSubTokens] = {};  // thread 0: loads waited for, per buffer
+  uint32_t uses[kMcRowBufs] = {};  // thread 0: loads waited for, per buffer
   int issued = -1;                    // thread 0: the column whose loads are in flight
   auto load = [&](int q) {            // thread 0
     int p, t0, nt;
@@ -634,7 +638,7 @@ __global__ void __launch_bounds__(kMcWarps * 32, 3) k_moe_column(RunParams P) {
     return ok;
   };
   if (threadIdx.x == 0) {
-    for (int k = 0; k < kMoeSubTokens; ++k) mbar_init(sbar + 8 * k, 1);
+    for (int k = 0; k < kMcRowBufs; ++k) mbar_init(sbar + 8 * k, 1);
     fence_mbarrier_init();
     s_col[0] = (int)atomicAdd(&h->task_next[slot], 1u);
     s_ok = 1;
