@@ -490,7 +490,7 @@ def latency_sweep(cd, stream, only_T=None, only_variant=None, encoding=None) -> 
                 # configuration, timed the same way (flash-comm Appendix A)
                 floor = None
                 pl = coll.plan()
-                if pl["path"] == cd.COLL_PATH_FUSED:
+                if pl["path"] in (cd.COLL_PATH_FUSED, cd.COLL_PATH_COMPOSED):
                     gf = torch.cuda.CUDAGraph()
                     with torch.cuda.graph(gf, stream=stream):
                         for _ in range(128):
@@ -515,8 +515,10 @@ def latency_sweep(cd, stream, only_T=None, only_variant=None, encoding=None) -> 
             if floor is not None:
                 row[name]["floor_us"] = round(floor, 3)
                 row[name]["excess_us"] = round(warm - floor, 3)
-                row[name]["launch"] = {"ctas": pl["ctas_per_rank"] * N_RANKS,
-                                       "dependent": pl["dependent_launch"]}
+                row[name]["launch"] = ({"ctas": pl["ctas_per_rank"] * N_RANKS}
+                                       if pl["path"] == cd.COLL_PATH_FUSED else
+                                       {"columns": "composed"})
+                row[name]["launch"]["dependent"] = pl["dependent_launch"]
             if name == "policy":
                 row[name]["choice"] = {"encoding": pl["encoding"], "algorithm": pl["algorithm"],
                                        "path": pl["path"]}

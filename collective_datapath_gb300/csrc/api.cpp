@@ -181,6 +181,20 @@ cudaError_t launched(coll_spec* s, cudaError_t e, cudaStream_t st) {
 // and lag 40; the all-reduce's chunk is the largest of 256, 128 and 64 lines
 // that still gives eight lags' worth of chunks (the queue fills and drains
 // over 2 * lag steps).
+// CTAs of a launch by columns: the co-resident CTAs, no more than there are
+// columns (a short run launches only what it uses), or with bounded staging
+// a multiple of N CTAs that each own a chunk slot.  0 if none fit.
+int column_grid(const Plan& p, const ComposedParams& q) {
+  const int cap = column_capacity(q.variant);
+  if (q.ring > 0) {
+    int grid = std::min<int>(cap, (int)q.ring);
+    grid -= grid % p.n;
+    return grid < p.n ? 0 : grid;
+  }
+  const uint64_t cols = (uint64_t)q.first_cols + (uint64_t)q.nchunks * p.n;
+  return (int)std::min<uint64_t>((uint64_t)std::max(cap, 0), cols);
+}
+
 ComposedParams composed_shape(const coll_spec* s) {
   const Plan& p = s->plan;
   ComposedParams q{};
@@ -214,6 +228,14 @@ ComposedParams composed_shape(const coll_spec* s) {
       while (chunk > (int)kComposedMinChunk && p.ring_lines / (uint64_t)chunk < cap) chunk /= 2;
     } else {
       while (chunk > 32 && (most + chunk - 1) / chunk * (uint64_t)p.n < 4 * cap) chunk /= 2;
+      if ((most + chunk - 1) / chunk * (uint64_t)p.n < cap) {
+        // a short run: fewer columns than co-resident CTAs even at 32 lines.
+        // 16-line columns, each CTA takes at most one, and no staggered
+        // start or short tail (they shape the start and end of long runs)
+        chunk = (int)kComposedMinChunk;
+        stagger = 0;
+        tail = 0;
+      }
     }
   } else if (q.schedule == 1 && env == nullptr && ar) {
     while (chunk > 64 && (most + chunk - 1) / chunk < 8ull * (uint64_t)lag) chunk /= 2;
@@ -577,18 +599,13 @@ coll_status_t coll_run(coll_spec_t* s, const void* const* dev_ins, void* const* 
       }
     }
     if (P.cp.schedule == 0) {
-      // columns: every co-resident CTA, or with bounded staging a multiple
-      // of N CTAs that each own a chunk slot
-      const int cap = column_capacity(P.cp.variant);
-      int grid = cap;
-      if (P.cp.ring > 0) grid = std::min<int>(cap, (int)P.cp.ring);
-      grid -= grid % p.n;
-      if (grid < p.n) return COLL_ERR_CUDA;
+      const int grid = column_grid(p, P.cp);
+      if (grid < 1) return COLL_ERR_CUDA;
       // bounded staging: lines of column q carry epoch + q, so the run moves
       // the epoch past all of them, by an odd step (Purlin §4.2)
       P.advance_epoch =
           P.cp.ring > 0 ? (int)(((uint64_t)P.cp.nchunks * (uint64_t)p.n) | 1u) : 1;
-      return cuda_status(launched(s, launch_column(P, grid, st), st));
+      return cuda_status(launched(s, launch_column(P, grid, st, p.dependent_launch), st));
     }
     const int cap = composed_capacity(P.cp.variant, P.cp.ring > 0);
     if (cap < 3) return COLL_ERR_CUDA;
@@ -823,6 +840,16 @@ coll_status_t coll_launch_floor(coll_spec_t* s, coll_stream_t stream) {
   if (s == nullptr) return COLL_ERR_INVALID;
   const Plan& p = s->plan;
   const bool empty = p.items1.empty() && p.items2.empty();
+  if (p.kind != CK_MOE && p.path == COLL_PATH_COMPOSED && !empty) {
+    // the launch by columns: its grid, block and attributes
+    if (!s->bound) return COLL_ERR_STATE;
+    const ComposedParams q = composed_shape(s);
+    if (q.schedule != 0) return COLL_ERR_UNSUPPORTED;
+    const int grid = column_grid(p, q);
+    if (grid < 1) return COLL_ERR_CUDA;
+    return cuda_status(launch_floor(grid, as_stream(stream), p.dependent_launch, true,
+                                    column_threads(q.variant)));
+  }
   if (p.kind == CK_MOE || p.path != COLL_PATH_FUSED || empty ||
       (p.enc != ENC_LL128 && p.reset_mode == COLL_RESET_KERNEL))
     return COLL_ERR_UNSUPPORTED;

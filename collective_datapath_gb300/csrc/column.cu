@@ -518,13 +518,18 @@ int capacity_of() {
 
 }  // namespace
 
+int column_threads(int variant) {
+  const int v = variant >= 0 && variant <= 2 ? variant : 0;
+  return kColVariants[v].warps * 32;
+}
+
 int column_capacity(int variant) {
   if (variant == 1) return capacity_of<8, 24, 2>();
   if (variant == 2) return capacity_of<4, 16, 6>();
   return capacity_of<8, 16, 3>();
 }
 
-cudaError_t launch_column(const RunParams& P, int grid, cudaStream_t s) {
+cudaError_t launch_column(const RunParams& P, int grid, cudaStream_t s, bool dependent) {
   const int v = P.cp.variant >= 0 && P.cp.variant <= 2 ? P.cp.variant : 0;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
@@ -533,11 +538,13 @@ cudaError_t launch_column(const RunParams& P, int grid, cudaStream_t s) {
   cfg.stream = s;
   // co-resident CTAs: the grid's last CTA counts every CTA in before it
   // advances the epoch
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeCooperative;
   attr[0].val.cooperative = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = dependent ? 2 : 1;
   const bool f32 = P.dtype == kDtF32;
   if (v == 1)
     return f32 ? cudaLaunchKernelEx(&cfg, k_column_ll128<8, 24, 2, true>, P)

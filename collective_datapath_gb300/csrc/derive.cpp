@@ -723,13 +723,16 @@ int derive(const DeriveInput& in, Plan& p) {
   // ordered oneshot 5.37 -> 4.54 us at 8 KiB, 11.94 -> 11.31 us at 128 KiB,
   // but 16.94 -> 18.54 us at 512 KiB and 75.8 -> 81.6 us for the twoshot at
   // 4 MiB.  So: one-launch runs up to 512 KiB per rank (input or output),
-  // stream-ordered ones up to 128 KiB, the composed launch never.
+  // stream-ordered ones up to 128 KiB.  The composed launch by columns: up
+  // to 512 KiB too (8 ranks, all-reduce, 16 KiB / 128 KiB / 512 KiB: 7.35
+  // -> 6.80, 7.89 -> 7.25, 8.00 -> 7.43 us), not at 1 MiB (9.74 -> 11.51).
   uint64_t largest = 0;
   for (int r = 0; r < n; ++r)
     largest = std::max(largest, std::max(p.in_elems[r], p.out_elems[r]));
   const uint64_t bytes = largest * 2;
-  p.dependent_launch = (p.path == COLL_PATH_FUSED && bytes <= 512 * 1024) ||
-                       (p.path == COLL_PATH_STREAMED && bytes <= 128 * 1024);
+  p.dependent_launch =
+      ((p.path == COLL_PATH_FUSED || p.path == COLL_PATH_COMPOSED) && bytes <= 512 * 1024) ||
+      (p.path == COLL_PATH_STREAMED && bytes <= 128 * 1024);
   return COLL_OK;
 }
 

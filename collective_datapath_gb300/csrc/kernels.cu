@@ -901,10 +901,11 @@ __global__ void __launch_bounds__(kThreads) k_floor() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
-cudaError_t launch_floor(int grid, cudaStream_t s, bool dependent) {
+cudaError_t launch_floor(int grid, cudaStream_t s, bool dependent, bool cooperative,
+                         int threads) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
-  cfg.blockDim = dim3(kThreads);
+  cfg.blockDim = dim3(threads > 0 ? threads : kThreads);
   cfg.dynamicSmemBytes = 0;
   cfg.stream = s;
   cudaLaunchAttribute attr[2];
@@ -912,8 +913,8 @@ cudaError_t launch_floor(int grid, cudaStream_t s, bool dependent) {
   attr[0].val.cooperative = 1;
   attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[1].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = dependent ? 2 : 1;
+  cfg.attrs = cooperative ? attr : attr + 1;
+  cfg.numAttrs = (cooperative ? 1 : 0) + (dependent ? 1 : 0);
   return cudaLaunchKernelEx(&cfg, k_floor);
 }
 

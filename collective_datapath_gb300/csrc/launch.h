@@ -40,8 +40,10 @@ cudaError_t launch_consume(const RunParams& P, int phase, int grid, cudaStream_t
 // placed before the previous kernel in the stream completes; begin_run waits
 // for it before touching any data).
 cudaError_t launch_fused(const RunParams& P, int grid, cudaStream_t s, bool dependent);
-// An empty kernel in launch_fused's configuration (the fixed launch cost).
-cudaError_t launch_floor(int grid, cudaStream_t s, bool dependent);
+// An empty kernel in launch_fused's configuration (the fixed launch cost),
+// or with `threads` per CTA (0 = launch_fused's block).
+cudaError_t launch_floor(int grid, cudaStream_t s, bool dependent, bool cooperative = true,
+                         int threads = 0);
 // LL128 phase-1 folds through the shared-memory pipeline (all items IK_REDUCE).
 cudaError_t launch_fold(const RunParams& P, int grid, cudaStream_t s, bool dependent);
 // LL128 copy phases (all items IK_COPY, plain outputs) and LL128 staging
@@ -55,7 +57,8 @@ int composed_capacity(int variant, bool cycle);
 cudaError_t launch_composed(const RunParams& P, int grid, cudaStream_t s);
 // The same collectives scheduled by columns (P.cp.schedule == 0).
 int column_capacity(int variant);
-cudaError_t launch_column(const RunParams& P, int grid, cudaStream_t s);
+int column_threads(int variant);
+cudaError_t launch_column(const RunParams& P, int grid, cudaStream_t s, bool dependent);
 // MoE dispatch: routing + gather-stage of one source (P.stage_rank) or all,
 // then the destination scan + validated copy (ends the run).
 cudaError_t launch_moe_stage_all(const RunParams& P, cudaStream_t s);

@@ -15,27 +15,30 @@ struct PolicyEntry {
 };
 
 constexpr PolicyEntry kPolicy2[] = {
-    {49152ull, 0, 1, 1, 64},  // LL8/oneshot/fused/narrow
-    {131072ull, 0, 1, 1, 0},  // LL8/oneshot/fused
-    {262144ull, 2, 1, 1, 0},  // SENT/oneshot/fused
-    {2654208ull, 2, 1, 1, 1024},  // SENT/oneshot/fused/wide
-    {4456448ull, 2, 2, 1, 1024},  // SENT/twoshot/fused/wide
+    {16384ull, 2, 1, 1, 64},  // SENT/oneshot/fused/narrow
+    {32768ull, 0, 1, 1, 64},  // LL8/oneshot/fused/narrow
+    {131072ull, 2, 1, 1, 64},  // SENT/oneshot/fused/narrow
+    {344064ull, 2, 1, 1, 0},  // SENT/oneshot/fused
+    {7421952ull, 2, 1, 1, 1024},  // SENT/oneshot/fused/wide
+    {8421376ull, 2, 1, 2, 0},  // SENT/oneshot/streamed
     {UINT64_MAX, 1, 2, 3, 0},  // LL128/twoshot/composed
 };
 constexpr PolicyEntry kPolicy4[] = {
     {32768ull, 0, 1, 1, 64},  // LL8/oneshot/fused/narrow
-    {376832ull, 2, 1, 1, 0},  // SENT/oneshot/fused
-    {1753088ull, 2, 1, 1, 1024},  // SENT/oneshot/fused/wide
-    {4194304ull, 2, 2, 1, 1024},  // SENT/twoshot/fused/wide
+    {65536ull, 2, 1, 1, 64},  // SENT/oneshot/fused/narrow
+    {245760ull, 2, 1, 1, 0},  // SENT/oneshot/fused
+    {524288ull, 2, 1, 1, 1024},  // SENT/oneshot/fused/wide
+    {1982464ull, 1, 2, 3, 0},  // LL128/twoshot/composed
+    {4456448ull, 2, 2, 1, 1024},  // SENT/twoshot/fused/wide
     {UINT64_MAX, 1, 2, 3, 0},  // LL128/twoshot/composed
 };
 constexpr PolicyEntry kPolicy8[] = {
-    {8192ull, 0, 1, 1, 64},  // LL8/oneshot/fused/narrow
+    {16384ull, 0, 1, 1, 64},  // LL8/oneshot/fused/narrow
     {32768ull, 0, 1, 1, 0},  // LL8/oneshot/fused
     {65536ull, 2, 1, 1, 0},  // SENT/oneshot/fused
-    {737280ull, 2, 1, 1, 1024},  // SENT/oneshot/fused/wide
-    {1851392ull, 2, 2, 1, 0},  // SENT/twoshot/fused
-    {2752512ull, 2, 2, 1, 1024},  // SENT/twoshot/fused/wide
+    {311296ull, 2, 1, 1, 1024},  // SENT/oneshot/fused/wide
+    {1769472ull, 1, 2, 3, 0},  // LL128/twoshot/composed
+    {2097152ull, 2, 2, 1, 1024},  // SENT/twoshot/fused/wide
     {UINT64_MAX, 1, 2, 3, 0},  // LL128/twoshot/composed
 };
 

@@ -65,14 +65,14 @@ class Candidate:
 def candidates_for(nbytes: int) -> list[Candidate]:
     """The protocols worth measuring at one size (bytes per rank): one
     cooperative launch only up to 4 MiB (in two launch shapes, three up to
-    256 KiB), the composed launch from 1 MiB."""
+    256 KiB), the composed launch from 256 KiB."""
     out = []
     for enc in (LL8, SENT, LL128):
         for algo in (ONESHOT, TWOSHOT):
             for path in (FUSED, STREAMED, COMPOSED):
                 if path == FUSED and nbytes > (4 << 20):
                     continue
-                if path == COMPOSED and (enc != LL128 or algo != TWOSHOT or nbytes < (1 << 20)):
+                if path == COMPOSED and (enc != LL128 or algo != TWOSHOT or nbytes < (256 << 10)):
                     continue
                 if enc == LL128 and path == FUSED:
                     continue

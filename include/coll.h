@@ -392,14 +392,16 @@ coll_status_t coll_last_launches(const coll_spec_t *spec, int *launches);
  * an empty-kernel floor inside CUDA graphs, and its cost model (§3.2,
  * Eq. (1)) carries a fixed per-operation term.  This enqueues one empty
  * kernel on `stream` in exactly the launch configuration coll_run(spec, ins,
- * outs) uses on the one-launch (fused) path: the same grid and block size,
- * the cooperative attribute, and programmatic stream serialization when the
- * spec's runs are dependent launches (the kernel then makes the same
- * dependent-launch handshake as a run's prologue).  It reads and writes no
- * memory and leaves the spec's device state (epoch, staging) untouched, so
- * it may be timed between or instead of runs, eagerly or in a graph.
- * Returns COLL_ERR_UNSUPPORTED for specs whose runs do not take the
- * one-launch path, COLL_ERR_CUDA if the launch fails. */
+ * outs) uses on the one-launch paths, the fused kernel or the composed
+ * launch by columns: the same grid and block size, the cooperative
+ * attribute, and programmatic stream serialization when the spec's runs are
+ * dependent launches (the kernel then makes the same dependent-launch
+ * handshake as a run's prologue).  It reads and writes no memory and leaves
+ * the spec's device state (epoch, staging) untouched, so it may be timed
+ * between or instead of runs, eagerly or in a graph.  Returns
+ * COLL_ERR_UNSUPPORTED for specs whose runs take neither path (or the
+ * composed queue schedule), COLL_ERR_STATE for a composed spec not yet
+ * bound, COLL_ERR_CUDA if the launch fails. */
 coll_status_t coll_launch_floor(coll_spec_t *spec, coll_stream_t stream);
 
 /* All-reduce without any allocation.  The pages have no counterpart: this is

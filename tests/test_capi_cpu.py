@@ -492,10 +492,9 @@ def test_fused_phases_fill_whole_rounds(cd, T):
 
 
 def test_dependent_launch_rule(cd):
-    """A run's kernels are dependent launches when it is one-launch (fused)
-    up to 512 KiB per rank, input or output, or stream-ordered up to
-    128 KiB; larger runs and the composed launch are not.  Plan only
-    (host)."""
+    """A run's kernels are dependent launches when it is one-launch (fused
+    or composed) up to 512 KiB per rank, input or output, or stream-ordered
+    up to 128 KiB; larger runs are not.  Plan only (host)."""
     def dep(triple, n, count, **kw):
         s = cd.coll_spec_create(*triple, n, count, **kw)
         try:
@@ -511,8 +510,11 @@ def test_dependent_launch_rule(cd):
     assert dep(cd.ALLREDUCE, 8, 4096, **streamed) == 1
     assert dep(cd.ALLREDUCE, 8, 64 * 1024, **streamed) == 1          # 128 KiB
     assert dep(cd.ALLREDUCE, 8, 64 * 1024 + 8, **streamed) == 0
-    assert dep(cd.ALLREDUCE, 8, 8 * 60 * 1024, encoding=cd.COLL_LL128,
-               algorithm=cd.COLL_TWOSHOT, path=cd.COLL_PATH_COMPOSED) == 0
+    composed = dict(encoding=cd.COLL_LL128, algorithm=cd.COLL_TWOSHOT,
+                    path=cd.COLL_PATH_COMPOSED)
+    assert dep(cd.ALLREDUCE, 8, 4096, **composed) == 1
+    assert dep(cd.ALLREDUCE, 8, 256 * 1024, **composed) == 1          # 512 KiB
+    assert dep(cd.ALLREDUCE, 8, 256 * 1024 + 8, **composed) == 0
     assert dep(cd.ALLREDUCE, 8, 4096, encoding=cd.COLL_ENC_AUTO) == 1   # policy: fused
     # all-gather: 64 KiB in, 512 KiB out per rank; twice that is past the bound
     assert dep(cd.ALLGATHER, 8, 8 * 32 * 1024, **fused) == 1

@@ -424,7 +424,7 @@ def test_composed_reduce_scatter_and_all_to_all(cd, name, n, count, shape, monke
         assert coll.epoch() == e + 1
 
 
-@pytest.mark.parametrize("enc,path", [(0, 1), (2, 1), (0, 2), (1, 2)])
+@pytest.mark.parametrize("enc,path", [(0, 1), (2, 1), (0, 2), (1, 2), (1, 3)])
 def test_dependent_launches_chain(cd, enc, path):
     """Small runs are dependent launches (one launch, or stream-ordered
     kernels): each kernel must wait for the kernel before it and see all of
@@ -435,8 +435,11 @@ def test_dependent_launches_chain(cd, enc, path):
     import torch
 
     n, count = 8, 4096
-    a = make(cd, cd.ALLREDUCE, n, count, encoding=enc, path=path)
-    b = make(cd, cd.ALLREDUCE, n, count, encoding=enc, path=path)
+    kw = dict(encoding=enc, path=path)
+    if path == 3:
+        kw["algorithm"] = cd.COLL_TWOSHOT  # the composed launch's all-reduce
+    a = make(cd, cd.ALLREDUCE, n, count, **kw)
+    b = make(cd, cd.ALLREDUCE, n, count, **kw)
     assert a.plan()["dependent_launch"] == 1 and b.plan()["dependent_launch"] == 1
     masks = [0x0011 * (r + 1) & 0x007F for r in range(n)]
     mask_d = [torch.tensor(m, dtype=torch.int16, device="cuda") for m in masks]
@@ -482,3 +485,33 @@ def test_dependent_launches_chain(cd, enc, path):
         y3, y5 = expect(xs)
         check(a, o3, y3, n)
         check(b, o5, y5, n)
+
+
+def test_launch_floor_leaves_the_run_state_alone(cd):
+    """coll_launch_floor enqueues an empty kernel in a one-launch spec's
+    configuration (fused, or composed by columns): the epoch and the next
+    run's result are unchanged; specs with no one-launch path refuse it."""
+    import torch
+
+    n, count = 8, 4096
+    for kw in (dict(encoding=cd.COLL_LL8, path=cd.COLL_PATH_FUSED),
+               dict(encoding=cd.COLL_LL128, algorithm=cd.COLL_TWOSHOT,
+                    path=cd.COLL_PATH_COMPOSED),
+               dict(encoding=cd.COLL_LL128, algorithm=cd.COLL_TWOSHOT,
+                    path=cd.COLL_PATH_COMPOSED, staging_bytes=4 * n * 16 * 128)):
+        coll = make(cd, cd.ALLREDUCE, n, count, **kw)
+        xs, ins, outs = buffers(coll, n, seed=60)
+        before = coll.epoch()
+        s = torch.cuda.current_stream()
+        for _ in range(3):
+            cd.coll_launch_floor(coll.spec, s)
+        torch.cuda.synchronize()
+        assert coll.epoch() == before
+        coll.run(ins, outs)
+        check(coll, outs, oracle.allreduce(xs), n)
+        coll.close()
+    coll = make(cd, cd.ALLREDUCE, n, count, encoding=cd.COLL_LL128, path=cd.COLL_PATH_STREAMED)
+    with pytest.raises(cd.CollError) as e:
+        cd.coll_launch_floor(coll.spec, torch.cuda.current_stream())
+    assert e.value.status == cd.COLL_ERR_UNSUPPORTED
+    coll.close()
