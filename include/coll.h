@@ -152,28 +152,31 @@ enum { COLL_RESET_FUSED = 0, COLL_RESET_KERNEL = 1, COLL_RESET_NONE = 2,
        COLL_RESET_DEFERRED = 3 };
 
 /* Launch path: FUSED = stage and consume inside one cooperative kernel
- * (all CTAs co-resident; a CTA serves one emulated rank).  Up to 512 KiB per
- * rank (input or output, whichever is larger) that kernel is a dependent
- * launch: it carries programmatic stream serialization, so its CTAs can be
- * placed while the previous kernel in the stream finishes, and they wait
- * for that kernel to complete, with its writes visible, before reading the
- * workspace or any input (griddepcontrol.wait).  Each of the library's
- * kernels allows the next dependent launch to be placed once it has read
- * the epoch; a caller's kernel launched that way must wait the same way
- * before it reads the outputs.  STREAMED (dependent launches, the same way,
- * up to 128 KiB per rank) =
- * separate stage and consume kernels ordered by the stream; COMPOSED
- * (LL128 only: the twoshot all-reduce, reduce-scatter, all-to-all and
- * all-gather; AUTO never takes it for the all-gather, whose stream-ordered
- * copy measured faster at every size) = one
- * persistent cooperative kernel that runs stage, fold (+ publish) and
- * gather or copy tasks chunk by chunk from one queue, each chunk's lines
- * staying in L2 between its producer and its reader (Purlin §3.2,
- * Algorithm 1, Figure 5).  AUTO picks FUSED for LL8 and sentinel packs up
- * to 256 KiB per rank, COMPOSED for LL128 from 32 MiB per rank (all-to-all:
- * from 16 MiB) and, for
- * all-reduce, ONESHOT up to 512 KiB per rank (boundaries on measured GB300
- * points); with COLL_ENC_AUTO the all-reduce takes the calibrated table. */
+ * (all CTAs co-resident; a CTA serves one emulated rank).  STREAMED =
+ * separate stage and consume kernels ordered by the stream.  COMPOSED (LL128
+ * only: the twoshot all-reduce, reduce-scatter, all-gather, all-to-all and
+ * their V forms) = one cooperative launch by columns: a column is one chunk
+ * of one partition, and one CTA runs its stage, fold (+ publish) and gather
+ * or copy phases back to back, so the chunk's lines stay in L2 between
+ * their producer and their reader and no CTA waits for another (Purlin
+ * §3.2, Algorithm 1, Figure 5, with the chunk counter inside a CTA).  A
+ * short run (fewer columns than co-resident CTAs) launches one CTA per
+ * 16-line column; a longer one staggers each CTA's first column and ends
+ * on 16-line columns.
+ * Dependent launches: FUSED and COMPOSED runs up to 512 KiB per rank (input
+ * or output, whichever is larger), STREAMED runs up to 128 KiB, carry
+ * programmatic stream serialization, so their CTAs can be placed while the
+ * previous kernel in the stream finishes; they wait for that kernel to
+ * complete, with its writes visible, before reading the workspace or any
+ * input (griddepcontrol.wait).  Each of the library's kernels allows the
+ * next dependent launch to be placed once it has read the epoch; a caller's
+ * kernel launched that way must wait the same way before it reads the
+ * outputs.
+ * AUTO picks FUSED for LL8 and sentinel packs up to 256 KiB per rank,
+ * COMPOSED for LL128 (the all-to-all and all-to-all V from 4 MiB per rank),
+ * STREAMED otherwise, and, for the all-reduce, ONESHOT up to 512 KiB per rank
+ * (boundaries on measured GB300 points); with COLL_ENC_AUTO the all-reduce
+ * takes the calibrated table. */
 enum { COLL_PATH_AUTO = 0, COLL_PATH_FUSED = 1, COLL_PATH_STREAMED = 2,
        COLL_PATH_COMPOSED = 3 };
 
@@ -211,10 +214,12 @@ typedef struct {
                             slot, in bytes; 0 (default) = the whole message.
                             Purlin §4.1: when the staging a collective needs
                             exceeds the capacity, chunks cycle through a
-                            fixed number of chunk slots.  A capacity below
+                            fixed number of chunk slots (in the launch by
+                            columns, each CTA owns one).  A capacity below
                             the message requires the composed launch (the
-                            LL128 twoshot all-reduce, reduce-scatter or
-                            all-to-all; path AUTO selects it) and must hold
+                            LL128 twoshot all-reduce, reduce-scatter,
+                            all-to-all and their V forms; path AUTO selects
+                            it) and must hold
                             at least 4096 * nranks bytes (two chunk slots of
                             the smallest chunk), else COLL_ERR_UNSUPPORTED /
                             COLL_ERR_INVALID.  Such a spec runs only through
@@ -284,11 +289,11 @@ coll_status_t coll_stage(coll_spec_t *spec, int rank, const void *dev_in,
                          coll_stream_t stream);
 
 /* Run the collective for the current epoch, then advance the epoch (by 1;
- * with bounded staging by the run's chunk count rounded up to odd).
+ * with bounded staging by the run's column count rounded up to odd).
  * dev_ins == NULL: every rank was staged by coll_stage; the consume kernels
  * validate and consume.  dev_ins != NULL (nranks input pointers): staging is
  * done here too -- inside the same cooperative kernel on the FUSED path, as
- * the stage tasks of the one persistent launch on the COMPOSED path.
+ * the stage phase of each column of the one launch on the COMPOSED path.
  * dev_outs: nranks output pointers (16-byte aligned).  Consumers reduce in
  * rank order 0..N-1 whatever order lines become ready in (flash-comm §3.3). */
 coll_status_t coll_run(coll_spec_t *spec, const void *const *dev_ins,
