@@ -117,9 +117,6 @@ struct MoeParams {
   int32_t* counts_out;  // [N dest][el][N src] counts, then rows per destination
 };
 
-// Composed twoshot all-reduce (one persistent launch, Purlin Algorithm 1):
-// the chunking of every partition, the task queue's lag and the per-task
-// completion flags (epoch values, in the workspace).
 // One piece of an all-to-all (V) exchange, source p's partition x: its
 // place in p's rank image and input, its length, and its offset in
 // destination x's output.  The composed all-to-all reads table[p * N + x].
@@ -130,6 +127,9 @@ struct ExchPiece {
   uint64_t out0;   // offset in rank x's output: the earlier sources' lengths
 };
 
+// The composed launch (Purlin Algorithm 1), by columns or as a queue of
+// tasks: the chunking of every partition, the column lengths, the queue's
+// lags and per-task completion flags (epoch values, in the workspace).
 struct ComposedParams {
   uint32_t chunk_lines;  // lines of one partition per chunk (multiple of 4)
   uint32_t nchunks;
