@@ -321,7 +321,6 @@ ComposedParams composed_shape(const coll_spec* s) {
   q.mode = p.kind == CK_REDUCE_SCATTER || p.kind == CK_REDUCE_SCATTER_V ? 1
            : p.kind == CK_ALLTOALL || p.kind == CK_ALLTOALL_V            ? 2
            : gather                                                      ? 3
-           : p.algorithm == COLL_ONESHOT                                 ? 4
                                                                          : 0;
   char* f = s->ws + p.off_cflags;
   q.flag_stage = reinterpret_cast<uint64_t*>(f);
@@ -599,8 +598,6 @@ coll_status_t coll_run(coll_spec_t* s, const void* const* dev_ins, void* const* 
         P.seg_elems[x] = most;
       }
     }
-    // the oneshot all-reduce runs by columns only
-    if (P.cp.mode == 4 && P.cp.schedule != 0) return COLL_ERR_UNSUPPORTED;
     if (P.cp.schedule == 0) {
       const int grid = column_grid(p, P.cp);
       if (grid < 1) return COLL_ERR_CUDA;

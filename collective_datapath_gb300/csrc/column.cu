@@ -375,7 +375,7 @@ __global__ void __launch_bounds__(kW * 32, kMinBlocks) k_column_ll128(RunParams 
   const uint32_t CL = Q.chunk_lines;
   const uint32_t wbase =
       (uint32_t)__cvta_generic_to_shared(smem) + (uint32_t)(warp * kRing * kRowBytes);
-  const bool folds = Q.mode == 0 || Q.mode == 1, gathers = Q.mode == 0 || Q.mode == 2 || Q.mode == 3;
+  const bool folds = Q.mode == 0 || Q.mode == 1, gathers = Q.mode != 1;
   const uint64_t pol = l2_evict_first_policy();  // inputs and outputs are touched once
   if (threadIdx.x == 0) {
     // every CTA's first column is its own index; later ones come from the
@@ -446,19 +446,6 @@ __global__ void __launch_bounds__(kW * 32, kMinBlocks) k_column_ll128(RunParams 
       if (!col_fold<kW, kRing, kF32>(P, wbase, lane, warp, nl, pline, ag,
                                      Q.mode == 1 ? out : nullptr, left, e, seq, dsc))
         s_ok = 0;
-      __syncthreads();
-      if (!s_ok) break;
-    } else if (Q.mode == 4) {
-      // oneshot: every destination d reads the column's rows of all N
-      // images itself, checks them and folds them into its own output; the
-      // last reader drops the staged lines
-      const bool dsc = Q.discard != 0;
-      for (int d = 0; d < n; ++d) {
-        uint16_t* out = P.out[d] + P.seg_in0[x] + (uint64_t)t0 * kLL128Elems;
-        if (!col_fold<kW, kRing, kF32>(P, wbase, lane, warp, nl, pline, nullptr, out, left, e,
-                                       seq, dsc && d == n - 1))
-          s_ok = 0;
-      }
       __syncthreads();
       if (!s_ok) break;
     }

@@ -347,9 +347,8 @@ int derive(const DeriveInput& in, Plan& p) {
   p.algorithm = 0;
   if (p.kind == CK_ALLREDUCE) {
     p.algorithm = algo;
-    // the composed launch's all-reduce is the twoshot unless the oneshot is
-    // asked for: by columns the oneshot's N folds per column run in turn
-    // (8 ranks, 32 KiB to 1 MiB: 10.3-13.9 us against 7.3-10.7)
+    // the composed launch runs the twoshot all-reduce (a oneshot by
+    // columns was measured slower: its N folds per column run in turn)
     if (p.algorithm == COLL_ALGO_AUTO)
       p.algorithm = path == COLL_PATH_COMPOSED ? COLL_TWOSHOT
                     : (n <= 2 || in_bytes_per_rank <= 512 * 1024) ? COLL_ONESHOT
@@ -379,12 +378,12 @@ int derive(const DeriveInput& in, Plan& p) {
       p.path = COLL_PATH_STREAMED;
   }
 
-  // The composed launch: the LL128 all-reduce (twoshot, or oneshot by
-  // columns), reduce-scatter, all-to-all and all-gather, and their V forms
-  // (stage plus one or two consuming kinds of task per chunk).
+  // The composed launch: the LL128 twoshot all-reduce, reduce-scatter,
+  // all-to-all and all-gather, and their V forms (stage plus one or two
+  // consuming kinds of task per chunk).
   if (p.path == COLL_PATH_COMPOSED &&
       !(p.enc == ENC_LL128 &&
-        (p.kind == CK_ALLREDUCE ||
+        ((p.kind == CK_ALLREDUCE && p.algorithm == COLL_TWOSHOT) ||
          p.kind == CK_REDUCE_SCATTER || p.kind == CK_ALLTOALL || p.kind == CK_ALLGATHER ||
          p.kind == CK_REDUCE_SCATTER_V || p.kind == CK_ALLGATHER_V ||
          p.kind == CK_ALLTOALL_V)))

@@ -153,9 +153,7 @@ struct ComposedParams {
   int mode;              // 0 all-reduce: stage, fold + publish, gather;
                          // 1 reduce-scatter: stage, fold into the outputs;
                          // 2 all-to-all: stage, copy into the outputs;
-                         // 3 all-gather: stage, copy every source's chunk;
-                         // 4 oneshot all-reduce: stage, every destination
-                         //   folds into its own output
+                         // 3 all-gather: stage, copy every source's chunk
   uint32_t ring;         // chunk slots the staging images cycle through (0: none,
                          // every chunk has its own place); staged and published
                          // lines of chunk c then carry epoch + c

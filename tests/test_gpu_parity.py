@@ -255,43 +255,6 @@ def test_composed_twoshot_matches_the_oracle(cd, n, count, shape, monkeypatch):
         assert coll.epoch() == e + 1
 
 
-@pytest.mark.parametrize("n,count", [(8, 8 * 1000), (8, 8 * 60 * 1024 + 64), (3, 3000), (2, 2 * 4096),
-                                     (8, 8 * 60 * 5000 + 64), (1, 4096)])
-@pytest.mark.parametrize("shape", [None, "16,1,1,0,-1,0,0,2,0", "64,1,1,2,-1,0,16,1,8",
-                                   "32,1,1,1,-1,0,0,2,0"])
-def test_composed_oneshot_matches_the_oracle(cd, n, count, shape, monkeypatch):
-    """The oneshot all-reduce by columns: a CTA stages every rank's piece of a
-    column, and after a CTA barrier each destination in turn reads the rows
-    of all N images, checks their numbers and folds them into its own output
-    (the last reader drops the staged lines).  Bit-exact over several
-    epochs, for short runs (one CTA per 16-line column), longer ones with a
-    staggered start and short tail, and several launch shapes."""
-    if shape is not None:
-        monkeypatch.setenv("COLL_COMPOSED_SHAPE", shape)
-    coll = make(cd, cd.ALLREDUCE, n, count, encoding=cd.COLL_LL128, algorithm=cd.COLL_ONESHOT,
-                path=cd.COLL_PATH_COMPOSED)
-    assert coll.plan()["algorithm"] == cd.COLL_ONESHOT
-    _, ins, outs = buffers(coll, n, seed=47)
-    for e in range(1, 4):
-        xs = [synth.normal_bf16(900 + e, count, n, r) for r in range(n)]
-        for r in range(n):
-            ins[r].copy_(to_dev(xs[r]))
-        coll.run(ins, outs)
-        check(coll, outs, oracle.allreduce(xs), n)
-        assert coll.epoch() == e + 1
-
-
-def test_composed_oneshot_refuses_the_queue_schedule(cd, monkeypatch):
-    monkeypatch.setenv("COLL_COMPOSED_SHAPE", "64,3,0,0,-1,1")
-    coll = make(cd, cd.ALLREDUCE, 8, 8 * 1000, encoding=cd.COLL_LL128, algorithm=cd.COLL_ONESHOT,
-                path=cd.COLL_PATH_COMPOSED)
-    _, ins, outs = buffers(coll, 8, seed=48)
-    with pytest.raises(cd.CollError) as e:
-        coll.run(ins, outs)
-    assert e.value.status == cd.COLL_ERR_UNSUPPORTED
-    coll.close()
-
-
 @pytest.mark.parametrize("name,n,count", [("ALLREDUCE", 8, 8 * 60 * 5000 + 64),
                                           ("ALLREDUCE", 3, 3 * 60 * 4000 + 8),
                                           ("REDUCE_SCATTER", 8, 8 * 60 * 5000 + 64),
