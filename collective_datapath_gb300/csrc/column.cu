@@ -19,7 +19,14 @@
 // line's number is still checked.  A staged or published line is read back
 // a few microseconds after it was written, by the same SM, and dropped from
 // L2 once read, so staging stays out of HBM, and CTAs never wait for each
-// other.  CTAs take columns from one counter, in chunk-major order.
+// other.  Every CTA takes its first column by its own index and later ones
+// from one counter, in chunk-major order.  Columns are of three lengths
+// (column_at): each CTA's first column is one of a staggered group (1/G ..
+// G/G of a chunk), so the CTAs do not all stage at once; then full chunks;
+// and the last half round of the CTAs' work in short columns, so they run
+// out of work together.  A short run uses 16-line columns only, one per CTA.
+// The all-to-all (V) reads its pieces from an exchange table, so each
+// source's piece of a column has its own length.
 //
 // Bounded staging (Purlin §4.1, P.cp.ring > 0 chunk slots per rank image):
 // CTA g owns slot g of every rank image and slot g / N of one owner's
@@ -28,7 +35,8 @@
 // advances the epoch by the column count rounded up to odd (§4.2).
 //
 // Inside a phase each warp takes a contiguous range of the phase's rows
-// (rows of piece k are numbered k * R + r) and walks it with two cursors:
+// (rows of piece k are numbered k * R + r, R rows of 4 lines per piece) and
+// walks it with two cursors:
 // the load cursor runs a ring of kRing rows ahead of the store cursor, and
 // a cursor reloads its piece's fields only when it crosses into the next
 // piece.
