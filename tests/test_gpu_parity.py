@@ -515,3 +515,43 @@ def test_launch_floor_leaves_the_run_state_alone(cd):
         cd.coll_launch_floor(coll.spec, torch.cuda.current_stream())
     assert e.value.status == cd.COLL_ERR_UNSUPPORTED
     coll.close()
+
+
+@pytest.mark.parametrize("name", ["REDUCE_SCATTER", "ALLGATHER", "ALLTOALL", "REDUCE_SCATTER_V",
+                                  "ALLGATHER_V", "ALLTOALL_V"])
+def test_composed_collectives_on_four_slots(cd, name):
+    """Every collective of the composed launch with four rotating staging
+    slots (flash-comm §4.2): run e stages into slot e mod 4; nine epochs
+    with new inputs each time stay bit-exact against the oracle."""
+    n = 8
+    triple = getattr(cd, name)
+    kw = dict(encoding=cd.COLL_LL128, path=cd.COLL_PATH_COMPOSED, slots=4)
+    if name.endswith("_V"):
+        base = [b // 2 for b in synth.zipf_split(1 << 21, n)]
+        v = [synth.rotate_right(base, p + 1) for p in range(n)] if name == "ALLTOALL_V" else base
+        count = 0 if name == "ALLTOALL_V" else int(sum(base))
+        kw["vcounts"] = v
+    else:
+        v, count = None, 8 * 60 * 700
+    coll = make(cd, triple, n, count, **kw)
+    _, ins, outs = buffers(coll, n, seed=61)
+    for e in range(1, 10):
+        sizes = [coll.elems(r)[0] for r in range(n)]
+        bits = name not in ("REDUCE_SCATTER", "REDUCE_SCATTER_V")
+        xs = [synth.random_bits16(1000 + e, sizes[r], n, r) if bits
+              else synth.normal_bf16(1000 + e, sizes[r], n, r) for r in range(n)]
+        for r in range(n):
+            if sizes[r]:
+                ins[r][:sizes[r]].copy_(to_dev(xs[r]))
+        coll.run(ins, outs)
+        if name == "REDUCE_SCATTER_V":
+            want = oracle.reduce_scatter_v(xs, v)
+        elif name == "ALLGATHER_V":
+            want = oracle.all_gather_v(xs, v)
+        elif name == "ALLTOALL_V":
+            want = oracle.all_to_all_v(xs, v)
+        else:
+            want = expected(cd, triple, xs, count)
+        check(coll, outs, want, n)
+        assert coll.epoch() == e + 1
+    coll.close()
