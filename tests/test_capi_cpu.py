@@ -308,6 +308,35 @@ def test_composed_exchange_table_moves_every_partition(cd, name, n, v):
     cd.coll_destroy(other)
 
 
+def test_composed_path_admits_every_ll128_collective(cd):
+    """The composed launch takes the LL128 twoshot all-reduce, the reduce-
+    scatter, all-gather, all-to-all and their V forms; other encodings, and
+    an all-reduce asked for as a oneshot, are refused.  An all-reduce left on
+    algorithm AUTO takes the twoshot there.  Plan only (host)."""
+    n = 8
+    zipf = zipf_elems(8 * 4096 * 2, n)
+    cases = [("ALLREDUCE", 8 * 1200, None), ("REDUCE_SCATTER", 8 * 1200, None),
+             ("ALLGATHER", 8 * 1200, None), ("ALLTOALL", 8 * 1200, None),
+             ("REDUCE_SCATTER_V", sum(zipf), zipf), ("ALLGATHER_V", sum(zipf), zipf),
+             ("ALLTOALL_V", 0, [synth.rotate_right(zipf, p + 1) for p in range(n)])]
+    for name, count, v in cases:
+        kw = dict(path=cd.COLL_PATH_COMPOSED, vcounts=v)
+        s = cd.coll_spec_create(*getattr(cd, name), n, count, encoding=cd.COLL_LL128, **kw)
+        plan = cd.coll_debug_plan(s)
+        assert plan["path"] == cd.COLL_PATH_COMPOSED, name
+        if name == "ALLREDUCE":
+            assert plan["algorithm"] == cd.COLL_TWOSHOT
+        cd.coll_destroy(s)
+        for enc in (cd.COLL_LL8, cd.COLL_SENT):
+            with pytest.raises(cd.CollError) as e:
+                cd.coll_spec_create(*getattr(cd, name), n, count, encoding=enc, **kw)
+            assert e.value.status == cd.COLL_ERR_UNSUPPORTED, (name, enc)
+    with pytest.raises(cd.CollError) as e:
+        cd.coll_spec_create(*cd.ALLREDUCE, n, 8 * 1200, encoding=cd.COLL_LL128,
+                            algorithm=cd.COLL_ONESHOT, path=cd.COLL_PATH_COMPOSED)
+    assert e.value.status == cd.COLL_ERR_UNSUPPORTED
+
+
 def test_v_argument_validation(cd):
     def status_of(*a, **kw):
         with pytest.raises(cd.CollError) as e:
