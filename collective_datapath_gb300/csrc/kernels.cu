@@ -740,7 +740,11 @@ __global__ void __launch_bounds__(kThreads, 2) k_fused(RunParams P) {
   }
   if (threadIdx.x == 0) atomicAdd(&header(P.ws)->started[e & 1], 1u);
   const uint32_t seen = early_arrivals(P);
-  if (has_i && !aborted(P.ws)) {
+  // The first item is consumed without reading the abort word first: that
+  // read, made by every thread of every CTA at once, sat on the critical
+  // path of a small run, and a wait inside the item still gives up once an
+  // error is latched.  Later items check it as before.
+  if (has_i) {
     consume_item<ENC, true>(P, P.P, it1, e);
     for (int i = i0 + B; i < P.beg1[d + 1]; i += B) {
       if (aborted(P.ws)) break;
