@@ -712,17 +712,24 @@ __global__ void __launch_bounds__(kThreads, 2) k_fused(RunParams P) {
   const int s0 = P.sbeg[d] + b, i0 = P.beg1[d] + b;
   const bool has_s = worker && P.sitems != nullptr && s0 < P.sbeg[d + 1];
   const bool has_i = worker && i0 < P.beg1[d + 1];
+  __shared__ uint64_t s_epoch;
   StageItem si{};
   Item it1{};
   if (has_s) si = P.sitems[s0];
   if (has_i) it1 = P.items1[i0];
-  const uint64_t e = run_wait_epoch(P);
+  // The epoch is read once per CTA (thread 0) and handed over in shared
+  // memory: a read by every warp of every CTA at once is a hot spot on one
+  // L2 line.  The first input load is in flight meanwhile.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  if (threadIdx.x == 0) s_epoch = ld_relaxed_u64(&header(P.ws)->epoch);
   uint2 first8 = make_uint2(0, 0);
   uint4 firsts = make_uint4(0, 0, 0, 0);
   if (has_s) {
     if (ENC == ENC_LL8) first8 = ll8_stage_first(P, si);
     if (ENC == ENC_SENT) firsts = sent_stage_first(P, si);
   }
+  __syncthreads();
+  const uint64_t e = s_epoch;
   run_arrive(P, e);
   if (!worker) {
     late_producer<ENC>(P, e, ((int)blockIdx.x - workers) % P.nranks, workers);
