@@ -204,25 +204,16 @@ __device__ __forceinline__ void count_rejection(char* ws) {
               (unsigned long long)__popc(mask));
 }
 
-// Epoch protocol of a launch.  Every thread reads the device epoch itself
-// (one L2 request per warp, issued next to the launch's first data loads); in
-// the launch that ends a run each CTA then adds one to `arrived` once all its
-// threads hold the value (the barrier's predicate consumes it).  The last CTA
-// of the grid advances the epoch once every CTA has arrived, so the next run
-// uses the other staging slot; no CTA waits at the end of its own work.
-// begin_run in two halves, for a kernel that issues loads of its own while
-// the epoch is in flight: run_wait_epoch waits for the previous kernel in
-// the stream and issues the epoch load; run_arrive (the first use of the
-// epoch) lets a dependent launch place its CTAs and counts this CTA in.
-__device__ __forceinline__ uint64_t run_wait_epoch(const RunParams& P) {
-  // Under programmatic stream serialization the CTAs may start before the
-  // previous kernel in the stream has completed: wait for it (and for its
-  // writes) before reading anything; without that launch attribute the wait
-  // returns at once.
-  asm volatile("griddepcontrol.wait;" ::: "memory");
-  return ld_relaxed_u64(&header(P.ws)->epoch);
-}
-
+// Epoch protocol of a launch.  Thread 0 of each CTA reads the device epoch
+// and hands it to the CTA in shared memory: a read by every warp of every CTA
+// at the same moment queues on one L2 line, on the critical path of a short
+// run.  In the launch that ends a run each CTA then adds one to `arrived`
+// once all its threads hold the value (the barrier's predicate consumes it).
+// The last CTA of the grid advances the epoch once every CTA has arrived, so
+// the next run uses the other staging slot; no CTA waits at the end of its
+// own work.  run_arrive (the first use of the epoch) lets a dependent launch
+// place its CTAs and counts this CTA in; a kernel that issues loads of its
+// own while the epoch is in flight calls it after its own read.
 __device__ __forceinline__ void run_arrive(const RunParams& P, uint64_t e) {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   if (P.advance_epoch) {
@@ -235,7 +226,15 @@ __device__ __forceinline__ void run_arrive(const RunParams& P, uint64_t e) {
 }
 
 __device__ __forceinline__ uint64_t begin_run(const RunParams& P) {
-  const uint64_t e = run_wait_epoch(P);
+  __shared__ uint64_t s_run_epoch;
+  // Under programmatic stream serialization the CTAs may start before the
+  // previous kernel in the stream has completed: wait for it (and for its
+  // writes) before reading anything; without that launch attribute the wait
+  // returns at once.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  if (threadIdx.x == 0) s_run_epoch = ld_relaxed_u64(&header(P.ws)->epoch);
+  __syncthreads();
+  const uint64_t e = s_run_epoch;
   run_arrive(P, e);
   return e;
 }
