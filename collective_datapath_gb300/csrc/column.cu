@@ -372,7 +372,7 @@ __global__ void __launch_bounds__(kW * 32, kMinBlocks) k_column_ll128(RunParams 
   __shared__ ColPiece s_piece[2][kMaxRanks];  // [0] stage pieces, [1] gather pieces
   __shared__ int s_col[2];
   __shared__ int s_ok;
-  const uint64_t e = begin_run(P);
+  const uint64_t e = begin_run_per_thread(P);
   const ComposedParams& Q = P.cp;
   WsHeader* h = header(P.ws);
   const int n = P.nranks;

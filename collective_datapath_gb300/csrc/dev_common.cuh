@@ -239,6 +239,18 @@ __device__ __forceinline__ uint64_t begin_run(const RunParams& P) {
   return e;
 }
 
+// begin_run with every thread reading the epoch itself (one L2 request per
+// warp).  The column-scheduled composed kernel keeps this form: its DRAM
+// counters were measured with it.  The shared-memory form above took an
+// 8 x 1 MiB composed all-reduce from 9.69 to 9.30 us on the same GPU, but
+// that kernel has not been profiled with it.
+__device__ __forceinline__ uint64_t begin_run_per_thread(const RunParams& P) {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  const uint64_t e = ld_relaxed_u64(&header(P.ws)->epoch);
+  run_arrive(P, e);
+  return e;
+}
+
 // The arrival count as the grid's last CTA sees it early (before its last
 // phase of work), so that finish_run usually need not read it again; other
 // CTAs, and launches that do not end a run, get 0.
