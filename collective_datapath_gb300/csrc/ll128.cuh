@@ -249,7 +249,8 @@ __device__ __forceinline__ uint4 ll128_fold(const uint4* s, int n, int dtype) {
                     pack_bf16x2(a[4], a[5]), pack_bf16x2(a[6], a[7]));
 }
 
-// The same bf16 fold in fewer instructions (no change in any result bit):
+// Two steps of the bf16 fold in fewer instructions (no change in any result
+// bit):
 //  * add.rn.f32.bf16 takes the bf16 operand as it is (its widening to
 //    binary32 is exact) and rounds the sum once, so it equals widening first
 //    and __fadd_rn -- an exhaustive run on GB300 over every bf16 operand
@@ -270,43 +271,11 @@ __device__ __forceinline__ uint32_t cvt_rn_bf16x2(float lo, float hi) {
   asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
   return r;
 }
-__device__ __forceinline__ uint4 ll128_fold_fast(const uint4* s, int n, int dtype) {
-  if (dtype == kDtF32) return ll128_fold_f32(s, n);
-  float a[8];
-  a[0] = bf16_lo_to_f32(s[0].x); a[1] = bf16_hi_to_f32(s[0].x);
-  a[2] = bf16_lo_to_f32(s[0].y); a[3] = bf16_hi_to_f32(s[0].y);
-  a[4] = bf16_lo_to_f32(s[0].z); a[5] = bf16_hi_to_f32(s[0].z);
-  a[6] = bf16_lo_to_f32(s[0].w); a[7] = bf16_hi_to_f32(s[0].w);
-#pragma unroll
-  for (int p = 1; p < kMaxRanks; ++p) {
-    if (p < n) {
-      add_bf16x2_f32(s[p].x, a[0], a[1]);
-      add_bf16x2_f32(s[p].y, a[2], a[3]);
-      add_bf16x2_f32(s[p].z, a[4], a[5]);
-      add_bf16x2_f32(s[p].w, a[6], a[7]);
-    }
-  }
-  uint32_t r[4];
-  bool nan = false;
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    r[i] = cvt_rn_bf16x2(a[2 * i], a[2 * i + 1]);
-    nan = nan || a[2 * i] != a[2 * i] || a[2 * i + 1] != a[2 * i + 1];
-  }
-  if (nan) {
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      if (a[2 * i] != a[2 * i]) r[i] = (r[i] & 0xFFFF0000u) | 0x7FC0u;
-      if (a[2 * i + 1] != a[2 * i + 1]) r[i] = (r[i] & 0x0000FFFFu) | 0x7FC00000u;
-    }
-  }
-  return make_uint4(r[0], r[1], r[2], r[3]);
-}
 
-// The same fold, taken one rank at a time: first() with rank 0's chunk, then
-// add() with each later rank's chunk in rank order, then result().  Only
-// the running sums are live, not every rank's chunk, which keeps register
-// pressure low in the kernels that read ranks one by one.
+// The fold of ll128_fold, taken one rank at a time: first() with rank 0's
+// chunk, then add() with each later rank's chunk in rank order, then
+// result().  Only the running sums are live, not every rank's chunk, which
+// keeps register pressure low in the kernels that read ranks one by one.
 template <bool kF32>
 struct ChunkFold {
   float a[8];
