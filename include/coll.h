@@ -353,7 +353,10 @@ coll_status_t coll_run_late(coll_spec_t *spec, const void *const *dev_ins,
                             const int64_t *n_late, coll_stream_t stream);
 
 /* Number of stale lines the consumers of the last runs observed and rejected
- * (a diagnostic counter, reset by coll_bind). */
+ * (a diagnostic counter, reset by coll_bind).  Synchronizes `stream`, then
+ * reads the counter from the workspace into *rejections (host memory).
+ * COLL_ERR_INVALID for a NULL argument, COLL_ERR_STATE before coll_bind,
+ * COLL_ERR_CUDA if the synchronization or the copy fails. */
 coll_status_t coll_get_rejections(coll_spec_t *spec, coll_stream_t stream,
                                   uint64_t *rejections);
 
@@ -390,7 +393,8 @@ coll_status_t coll_debug_plan(const coll_spec_t *spec, int *algorithm, int *path
  * array is copied, so the caller may reuse its own storage. */
 coll_status_t coll_set_profile_events(coll_spec_t *spec, void *const *events, int n);
 
-/* Number of kernel launches the last coll_run issued. */
+/* Number of kernel launches the last coll_run issued (host state, no CUDA
+ * call; 0 before the first run).  COLL_ERR_INVALID for a NULL argument. */
 coll_status_t coll_last_launches(const coll_spec_t *spec, int *launches);
 
 /* Launch floor, for measurement.  flash-comm (Appendix A, Table 8) calibrates
@@ -484,6 +488,8 @@ coll_status_t coll_copy_passes(void *dev_dst, const void *dev_src, size_t bytes,
 /* Release the spec's host state (never the caller's device memory). */
 coll_status_t coll_destroy(coll_spec_t *spec);
 
+/* A short English description of a status code (a static string, never
+ * NULL; "unknown status" for a value outside coll_status_t). */
 const char *coll_status_string(coll_status_t status);
 
 #ifdef __cplusplus
